@@ -1,0 +1,242 @@
+/*
+ * specverify.h -- C ABI of the batched draft-verification sampler for
+ * speculative decoding (sm_103a, one GPU).
+ *
+ * What it computes (web pages cited by title and section):
+ *
+ *  - "Speculative Decoding: Draft, Verify, and Correct" (DVC)
+ *      'Name the two distributions at one prefix': accept a draft y ~ q with
+ *      probability min(1, p(y)/q(y)); on rejection draw from the normalised
+ *      residual [p - q]+.  'Verify several proposed tokens in one target pass':
+ *      walk the drafts in order, stop at the first rejection, and add a bonus
+ *      token from p when every draft is accepted.  'Speculation needs cache
+ *      rollback': cache lengths must agree with the emitted tokens.
+ *      'Preserve the distribution you actually intend': p and q are the
+ *      post-temperature, post-mask sampling laws.
+ *  - "Speculative Decoding: How a Small Model Speeds Up a Big One Without
+ *    Changing Its Output" (SMB) 'The Guarantee Behind Rejection Sampling':
+ *      the greedy rule (keep the draft iff it is the target argmax, else emit
+ *      the argmax); 'Beyond Two Models: The EAGLE Line': draft trees verified
+ *      in one pass, the best branch kept.
+ *  - "Speculative decoding: why correcting a rejection is not resampling
+ *    from the target" (CRS) sections 1-2, 5: the same rule, masks before
+ *    correction, one to K+1 tokens per cycle.
+ *  - "Margins, Not Windows: Training-Free Per-Step Lossy Speculative
+ *    Decoding" (MNW) section 3: promote a mismatched draft when
+ *    p_target(draft) / p_target(top1) exceeds kappa.
+ *
+ * Conventions for every entry point:
+ *  - All array pointers are DEVICE pointers owned by the caller; the library
+ *    never allocates, never frees and never synchronises the stream.
+ *  - Arrays are dense, row-major, with the shapes given in brackets.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and runs asynchronously; read results after synchronising.
+ *  - Argument errors return a spec_status before anything is enqueued and
+ *    write no output.  Data errors in a row (NaN logit, token id out of
+ *    range, ...) set that row's row_status; the row's accepted_len becomes
+ *    -1, num_emitted 0 and its token outputs -1; other rows are unaffected.
+ *  - Workspace: `ws` is caller-owned device memory of at least the size the
+ *    matching *_workspace_size() returns, 256-byte aligned, ZERO-FILLED
+ *    before its first use (cudaMemset or spec_workspace_init).  Every
+ *    completed call leaves it zero-filled again, so it can be reused by the
+ *    next call on the same stream.  Calls that may overlap in time (other
+ *    streams) need separate workspaces.
+ *  - Logits are bf16 (SPEC_BF16) or fp32 (SPEC_F32).  Rows whose byte
+ *    length is a multiple of 16 with a 16-byte aligned base take the bulk-
+ *    copy (TMA) path; any other V still works, more slowly.
+ *  - The calls are stateless apart from a per-process cache of device
+ *    occupancy queries (thread safe).
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes of every entry point. */
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_ERR_NULL = 1,      /* a required pointer is NULL */
+  SPEC_ERR_SHAPE = 2,     /* B, K, N or V outside the supported range */
+  SPEC_ERR_DTYPE = 3,     /* unknown dtype or mode */
+  SPEC_ERR_ALIGN = 4,     /* a pointer is not aligned to its element size */
+  SPEC_ERR_ARG = 5,       /* another bad scalar argument (e.g. kappa is NaN) */
+  SPEC_ERR_CUDA = 6,      /* a CUDA runtime call failed (no device, launch error) */
+  SPEC_ERR_WORKSPACE = 7  /* workspace NULL, misaligned or too small */
+} spec_status;
+
+/* Per-row data status written to row_status[b].  When several problems meet
+ * in one row the smallest code is reported. */
+enum {
+  SPEC_ROW_OK = 0,
+  SPEC_ROW_NONFINITE = 1,       /* a logit the row reads is NaN or +inf */
+  SPEC_ROW_BAD_TOKEN = 2,       /* a draft / node token outside [0, V) */
+  SPEC_ROW_BAD_UNIFORM = 3,     /* a uniform outside [0, 1) */
+  SPEC_ROW_BAD_PARENT = 4,      /* tree: parent[0] != -1 or not 0 <= parent[i] < i */
+  SPEC_ROW_EMPTY = 5,           /* a logit row that is -inf everywhere */
+  SPEC_ROW_TIMEOUT = 6,         /* a bounded on-device wait gave up (see below) */
+  SPEC_ROW_BAD_TEMPERATURE = 7  /* temperature used and not finite and > 0 */
+};
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+typedef enum { SPEC_STOCHASTIC = 0, SPEC_GREEDY = 1 } spec_mode;
+
+/* Limits checked by the entry points. */
+#define SPEC_MAX_K 1023          /* drafts per chain */
+#define SPEC_MAX_TREE_NODES 1024 /* nodes per tree, root included */
+#define SPEC_MAX_V 262144        /* vocabulary size */
+
+/* ------------------------------------------------------------------ chain */
+
+typedef struct {
+  int32_t B;                 /* rows (>= 0) */
+  int32_t K;                 /* drafts per row, 0 <= K <= SPEC_MAX_K */
+  int32_t V;                 /* vocabulary size, 1 <= V <= SPEC_MAX_V */
+  int32_t dtype;             /* spec_dtype of both logit arrays */
+  int32_t mode;              /* spec_mode */
+  float margin_kappa;        /* GREEDY only: margin threshold; <= 0 = strict match */
+  const void *target_logits; /* [B, K+1, V]: row j is the target's logits for the
+                                token at draft position j (row K: bonus) */
+  const void *draft_logits;  /* [B, K, V]: the logits the drafter sampled y_j from;
+                                masked entries are -inf.  STOCHASTIC only (may be
+                                NULL in GREEDY) */
+  const int32_t *draft_tokens; /* [B, K] */
+  const float *temperature;  /* [B] per-row T > 0 applied to both laws; NULL = 1.
+                                GREEDY uses it only inside the margin ratio */
+  const float *u_accept;     /* [B, K] uniforms in [0,1) of the acceptance tests
+                                (STOCHASTIC only) */
+  const float *u_sample;     /* [B, K+1] uniforms in [0,1): u_sample[b,j] draws the
+                                correction when position j is the first rejection,
+                                u_sample[b,K] draws the bonus (STOCHASTIC only) */
+} spec_chain_args;
+
+typedef struct {
+  int32_t *accepted_len; /* [B] number of accepted drafts a, 0..K (-1: bad row) */
+  int32_t *out_tokens;   /* [B, K+1] y_0..y_{a-1}, then the correction or bonus
+                            token, then -1 */
+  int32_t *num_emitted;  /* [B] a + 1 (0: bad row) */
+  int32_t *row_status;   /* [B] SPEC_ROW_* */
+  /* Optional diagnostics (NULL to skip), STOCHASTIC only, one value per
+   * position j < K computed independently of the walk (unspecified for rows
+   * with a nonzero row_status): */
+  float *p_at_draft;     /* [B, K] p_j(y_j) */
+  float *q_at_draft;     /* [B, K] q_j(y_j) */
+  float *resid_mass;     /* [B, K] sum_v [p_j - q_j]+ where position j's own test
+                            rejects, else 0 */
+} spec_chain_out;
+
+/* Bytes of workspace spec_verify_chain needs for these sizes (any mode and
+ * dtype).  0 on invalid sizes. */
+size_t spec_verify_chain_workspace_size(int32_t B, int32_t K, int32_t V);
+
+/*
+ * spec_verify_chain -- one verification step of B independent chains.
+ *
+ * STOCHASTIC (DVC; CRS section 2): p_j = softmax(target_j / T_b),
+ * q_j = softmax(draft_j / T_b).  Position j accepts iff
+ * p_j(y_j)/q_j(y_j) >= 1 or u_accept[b,j] < p_j(y_j)/q_j(y_j).  The walk
+ * stops at the first rejecting j and emits the inverse CDF of [p_j - q_j]+
+ * at u_sample[b,j] (the smallest v whose cumulative residual mass, in
+ * vocabulary order, exceeds u * total); if the residual is numerically zero
+ * it draws from p_j instead.  If all K drafts pass, the bonus is the inverse
+ * CDF of p_K at u_sample[b,K].
+ *
+ * GREEDY (SMB; MNW section 3): position j accepts iff y_j is the lowest-
+ * index argmax of target_j, or margin_kappa > 0 and
+ * p(y_j)/p(top1) > margin_kappa at temperature T_b (evaluated in fp64 as
+ * l(y_j) - l(top1) > T_b * ln(kappa)).  The first failure emits the argmax;
+ * if all pass, the bonus is argmax target_K.  draft_logits is not read.
+ *
+ * Precision: fp32 arithmetic (fp32 accumulation, hardware exp2/log2); the
+ * greedy, tree and margin decisions are exact.
+ */
+spec_status spec_verify_chain(const spec_chain_args *args, const spec_chain_out *out,
+                              void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------- tree */
+
+typedef struct {
+  int32_t B;                 /* rows (>= 0) */
+  int32_t N;                 /* nodes per tree incl. the root, 1..SPEC_MAX_TREE_NODES */
+  int32_t V;                 /* vocabulary size */
+  int32_t dtype;             /* spec_dtype */
+  float margin_kappa;        /* <= 0: strict argmax match */
+  const void *target_logits; /* [B, N, V]: row i = target logits after node i
+                                (node 0 = root = last committed token) */
+  const int32_t *parent;     /* [B, N]: parent[b,0] = -1, 0 <= parent[b,i] < i */
+  const int32_t *node_tokens;/* [B, N]: token of node i (entry 0 ignored) */
+  const float *temperature;  /* [B] for the margin ratio; NULL = 1 */
+} spec_tree_args;
+
+typedef struct {
+  int32_t *accepted_len; /* [B] depth d of the kept node (edges from the root) */
+  int32_t *path_nodes;   /* [B, N] node ids on the kept root path, root
+                            excluded, then -1 (use to compact tree KV entries) */
+  int32_t *out_tokens;   /* [B, N] tokens of those nodes, then argmax of the kept
+                            node's target row, then -1 */
+  int32_t *num_emitted;  /* [B] d + 1 */
+  int32_t *row_status;   /* [B] SPEC_ROW_* */
+} spec_tree_out;
+
+size_t spec_verify_tree_workspace_size(int32_t B, int32_t N, int32_t V);
+
+/*
+ * spec_verify_tree -- greedy (+ margin) verification of one parent-indexed
+ * draft tree per row (SMB 'Beyond Two Models'; MNW section 3).  Node i >= 1
+ * is accepted iff its parent is accepted and node_tokens[i] is the argmax of
+ * target[parent[i]] or the margin rule promotes it.  The kept node is the
+ * deepest accepted one (ties: lowest node index).
+ */
+spec_status spec_verify_tree(const spec_tree_args *args, const spec_tree_out *out,
+                             void *ws, size_t ws_bytes, void *stream);
+
+/* --------------------------------------------------------------- rollback */
+
+/*
+ * spec_rollback_lengths -- committed KV-cache lengths that agree with the
+ * emitted tokens (DVC 'Speculation needs cache rollback'; CRS section 5).
+ *
+ * kv_len_in [B]: cache entries before the verify pass.  The pass fed the
+ * last emitted token and the drafts, so the entries of that token and of the
+ * accepted drafts are valid; the new correction/bonus token has none yet.
+ * Emission is cut after the first eos_id (kept; eos_id < 0: none) and so the
+ * sequence (kv_len_in + 1 tokens before the step) does not exceed max_len[b]
+ * (max_len NULL: no limit).  With n tokens kept and a = accepted_len[b]:
+ *   committed_kv_len[b] = kv_len_in[b] + 1 + min(n, a),  num_emitted_out[b] = n.
+ * Rows with accepted_len < 0 keep kv_len_in and emit 0.
+ * out_tokens [B, max_emit] and num_emitted_in [B] are the verify outputs.
+ */
+spec_status spec_rollback_lengths(int32_t B, int32_t max_emit, const int32_t *kv_len_in,
+                                  const int32_t *accepted_len, const int32_t *num_emitted_in,
+                                  const int32_t *out_tokens, int32_t eos_id,
+                                  const int32_t *max_len, int32_t *committed_kv_len,
+                                  int32_t *num_emitted_out, void *stream);
+
+/* ------------------------------------------------------------------ misc */
+
+/* Zero-fill a workspace on `stream` (a cudaMemsetAsync). */
+spec_status spec_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/* Human-readable name of a spec_status. */
+const char *spec_status_string(spec_status s);
+
+/*
+ * Bounded on-device waits.  Every wait of the kernels on an asynchronous
+ * copy gives up after this many nanoseconds (default 1e9 = 1 s), marks the
+ * rows it served SPEC_ROW_TIMEOUT and lets the kernel finish.  Process-wide
+ * setting, read at each launch.  spec_debug_force_wait_timeout(1) makes every
+ * kernel additionally wait on a barrier that nothing completes, so the give-up
+ * path can be tested on a healthy GPU; 0 turns it off.
+ */
+void spec_set_wait_timeout_ns(uint64_t ns);
+uint64_t spec_get_wait_timeout_ns(void);
+void spec_debug_force_wait_timeout(int on);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPECVERIFY_H */

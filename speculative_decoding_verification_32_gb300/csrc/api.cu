@@ -1,0 +1,366 @@
+// api.cu -- the C ABI of include/specverify.h: argument validation (before
+// any CUDA call), launch-shape selection from the device's occupancy, and the
+// launches.  No allocation, no synchronisation.
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+
+#include "internal.h"
+#include "specverify.h"
+
+using namespace sv;
+
+namespace {
+
+std::atomic<uint64_t> g_wait_ns{1000000000ull};
+std::atomic<int> g_force_timeout{0};
+
+struct DevInfo {
+  int sms = 0;
+  int smem_optin = 0;
+};
+
+std::mutex g_mu;
+std::map<int, DevInfo> g_dev;
+std::map<std::tuple<int, int, int, int, size_t>, int> g_clusters;
+std::map<std::tuple<int, int, size_t>, int> g_blocks;
+
+constexpr size_t kStochCtrlBytes = 2048;
+constexpr size_t kGreedyCtrlBytes = 1024;
+constexpr int kMinGreedySlice = 2048;
+
+// SPECVERIFY_VERBOSE=1 prints each distinct launch shape once (stderr).
+void report(const char *what, long long a, long long b, long long c, long long d, long long e,
+            long long f, long long g) {
+  static const bool on = [] {
+    const char *v = std::getenv("SPECVERIFY_VERBOSE");
+    return v && *v && *v != '0';
+  }();
+  if (!on) return;
+  static std::mutex mu;
+  static std::map<std::tuple<std::string, long long, long long, long long, long long, long long,
+                             long long, long long>, int> seen;
+  std::lock_guard<std::mutex> lk(mu);
+  auto key = std::make_tuple(std::string(what), a, b, c, d, e, f, g);
+  if (seen.count(key)) return;
+  seen[key] = 1;
+  std::fprintf(stderr, "[specverify] %s: %lld %lld %lld %lld %lld %lld %lld\n", what, a, b, c, d,
+               e, f, g);
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+bool aligned(const void *p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+cudaError_t device_info(int *dev, DevInfo *info) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_dev.find(*dev);
+  if (it != g_dev.end()) {
+    *info = it->second;
+    return cudaSuccess;
+  }
+  DevInfo d;
+  e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, *dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, *dev);
+  if (e != cudaSuccess) return e;
+  g_dev[*dev] = d;
+  *info = d;
+  return cudaSuccess;
+}
+
+cudaError_t max_clusters(int dev, bool bf16, int nv, int C, size_t smem, int *out) {
+  auto key = std::make_tuple(dev, (int)bf16, nv, C, smem);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_clusters.find(key);
+    if (it != g_clusters.end()) {
+      *out = it->second;
+      return cudaSuccess;
+    }
+  }
+  cudaError_t e = chain_stochastic_max_clusters(bf16, nv, C, smem, out);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_clusters[key] = *out;
+  return cudaSuccess;
+}
+
+cudaError_t greedy_blocks(int dev, bool bf16, size_t smem, int *out) {
+  auto key = std::make_tuple(dev, (int)bf16, smem);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_blocks.find(key);
+    if (it != g_blocks.end()) {
+      *out = it->second;
+      return cudaSuccess;
+    }
+  }
+  cudaError_t e = greedy_max_blocks_per_sm(bf16, smem, out);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_blocks[key] = *out;
+  return cudaSuccess;
+}
+
+size_t counters_bytes(int32_t B) { return align_up(static_cast<size_t>(B) * 4, 256); }
+
+size_t greedy_partials_max(int32_t B, int32_t npos, int32_t V) {
+  return static_cast<size_t>(B) * npos * ceil_div(V, kMinGreedySlice) * sizeof(GreedyPart);
+}
+
+bool valid_sizes(int32_t B, int32_t V) { return B >= 0 && V >= 1 && V <= SPEC_MAX_V; }
+
+// Greedy launch shared by the chain (GREEDY mode) and tree entry points.
+spec_status run_greedy(GreedyParams &p, bool bf16, int esz, void *ws, cudaStream_t stream) {
+  int dev;
+  DevInfo di;
+  if (device_info(&dev, &di) != cudaSuccess) return SPEC_ERR_CUDA;
+  const int epv = 16 / esz;
+  const long long positions = static_cast<long long>(p.B) * p.npos;
+  // slices small enough to give every SM work, large enough to amortise
+  const int want = static_cast<int>(std::max<long long>(1, (2LL * di.sms + positions - 1) / positions));
+  int slice = static_cast<int>(align_up(static_cast<size_t>(ceil_div(p.V, want)), 64));
+  slice = std::max(slice, kMinGreedySlice);
+  slice = std::min(slice, kGreedySlice);
+  slice = static_cast<int>(align_up(static_cast<size_t>(slice), static_cast<size_t>(epv)));
+  p.slice = slice;
+  p.nslices = ceil_div(p.V, slice);
+  p.use_tma = aligned(p.target, 16) && (static_cast<long long>(p.V) * esz) % 16 == 0;
+  p.buf_bytes = static_cast<int>(align_up(static_cast<size_t>(slice) * esz, 128));
+  const size_t scratch = p.tree ? align_up(static_cast<size_t>(p.npos) * 20, 128) : 0;
+  const size_t fixed = kGreedyCtrlBytes + scratch;
+  int stages = static_cast<int>((static_cast<size_t>(di.smem_optin) - fixed) / p.buf_bytes);
+  stages = std::max(1, std::min(stages, 4));
+  p.stages = stages;
+  const size_t smem = static_cast<size_t>(stages) * p.buf_bytes + fixed;
+  p.wait_limit_ns = g_wait_ns.load();
+  p.force_timeout = g_force_timeout.load();
+  p.row_counter = static_cast<uint32_t *>(ws);
+  p.part = reinterpret_cast<GreedyPart *>(static_cast<char *>(ws) + counters_bytes(p.B));
+  int per_sm = 0;
+  if (greedy_blocks(dev, bf16, smem, &per_sm) != cudaSuccess || per_sm < 1) return SPEC_ERR_CUDA;
+  const long long items = positions * p.nslices;
+  const int grid = static_cast<int>(std::min<long long>(items, static_cast<long long>(di.sms) * per_sm));
+  report("greedy slice nslices stages smem per_sm grid tma", slice, p.nslices, stages,
+         (long long)smem, per_sm, grid, p.use_tma);
+  if (launch_greedy(p, bf16, grid, smem, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t spec_verify_chain_workspace_size(int32_t B, int32_t K, int32_t V) {
+  if (!valid_sizes(B, V) || K < 0 || K > SPEC_MAX_K) return 0;
+  const size_t rec = static_cast<size_t>(B) * (K + 1) * sizeof(ChainRec);
+  const size_t part = greedy_partials_max(B, K + 1, V);
+  return counters_bytes(B) + std::max(rec, part);
+}
+
+size_t spec_verify_tree_workspace_size(int32_t B, int32_t N, int32_t V) {
+  if (!valid_sizes(B, V) || N < 1 || N > SPEC_MAX_TREE_NODES) return 0;
+  return counters_bytes(B) + greedy_partials_max(B, N, V);
+}
+
+spec_status spec_verify_chain(const spec_chain_args *a, const spec_chain_out *o, void *ws,
+                              size_t ws_bytes, void *stream) {
+  if (!a || !o) return SPEC_ERR_NULL;
+  if (!valid_sizes(a->B, a->V) || a->K < 0 || a->K > SPEC_MAX_K) return SPEC_ERR_SHAPE;
+  if (a->dtype != SPEC_F32 && a->dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  if (a->mode != SPEC_STOCHASTIC && a->mode != SPEC_GREEDY) return SPEC_ERR_DTYPE;
+  if (std::isnan(a->margin_kappa)) return SPEC_ERR_ARG;
+  const bool stoch = a->mode == SPEC_STOCHASTIC;
+  const int K = a->K;
+  if (!a->target_logits || !o->accepted_len || !o->out_tokens || !o->num_emitted ||
+      !o->row_status)
+    return SPEC_ERR_NULL;
+  if (K > 0 && !a->draft_tokens) return SPEC_ERR_NULL;
+  if (stoch && (!a->u_sample || (K > 0 && (!a->draft_logits || !a->u_accept))))
+    return SPEC_ERR_NULL;
+  const int esz = a->dtype == SPEC_BF16 ? 2 : 4;
+  if (!aligned(a->target_logits, esz) || (stoch && a->draft_logits && !aligned(a->draft_logits, esz)))
+    return SPEC_ERR_ALIGN;
+  const void *i32s[] = {a->draft_tokens, a->temperature, a->u_accept, a->u_sample,
+                        o->accepted_len, o->out_tokens, o->num_emitted, o->row_status,
+                        o->p_at_draft, o->q_at_draft, o->resid_mass};
+  for (const void *p : i32s)
+    if (p && !aligned(p, 4)) return SPEC_ERR_ALIGN;
+  const size_t need = spec_verify_chain_workspace_size(a->B, K, a->V);
+  if (!ws || !aligned(ws, 256) || ws_bytes < need) return SPEC_ERR_WORKSPACE;
+  if (a->B == 0) return SPEC_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool bf16 = a->dtype == SPEC_BF16;
+
+  if (!stoch) {
+    GreedyParams p = {};
+    p.target = a->target_logits;
+    p.tokens = a->draft_tokens;
+    p.parent = nullptr;
+    p.temperature = a->temperature;
+    p.use_margin = a->margin_kappa > 0.f;
+    p.ln_kappa = p.use_margin ? std::log(static_cast<double>(a->margin_kappa)) : 0.0;
+    p.tree = 0;
+    p.accepted_len = o->accepted_len;
+    p.out_tokens = o->out_tokens;
+    p.num_emitted = o->num_emitted;
+    p.row_status = o->row_status;
+    p.path_nodes = nullptr;
+    p.B = a->B;
+    p.npos = K + 1;
+    p.V = a->V;
+    return run_greedy(p, bf16, esz, ws, s);
+  }
+
+  int dev;
+  DevInfo di;
+  if (device_info(&dev, &di) != cudaSuccess) return SPEC_ERR_CUDA;
+  const int epv = 16 / esz;
+  const long long W = static_cast<long long>(a->B) * (K + 1);
+  const int cap = kThreads * kMaxElemsPerThread;  // elements per CTA kept in registers
+  int C = 1;
+  while (C < 16 && ceil_div(a->V, C) > cap) C *= 2;
+  if (ceil_div(a->V, C) > cap) return SPEC_ERR_SHAPE;
+  auto buf_of = [&](int c) {
+    const size_t L = align_up(static_cast<size_t>(ceil_div(a->V, c)), static_cast<size_t>(epv));
+    return align_up(L * esz, 128);
+  };
+  // keep at least two pipeline stages
+  while (C < 16 && 2 * 2 * buf_of(C) + kStochCtrlBytes > static_cast<size_t>(di.smem_optin)) C *= 2;
+  // small problems: split the vocabulary further so every SM has work
+  while (C < 8 && W * C < 2LL * di.sms && ceil_div(a->V, 2 * C) >= 2048) C *= 2;
+  const int L = static_cast<int>(align_up(static_cast<size_t>(ceil_div(a->V, C)), static_cast<size_t>(epv)));
+  int nv = ceil_div(ceil_div(L, epv), kThreads);
+  nv = nv <= 1 ? 1 : nv <= 2 ? 2 : nv <= 4 ? 4 : 8;
+  if (bf16 && nv > 4) return SPEC_ERR_SHAPE;
+
+  ChainStochParams p = {};
+  p.target = a->target_logits;
+  p.draft = a->draft_logits;
+  p.tokens = a->draft_tokens;
+  p.temperature = a->temperature;
+  p.u_accept = a->u_accept;
+  p.u_sample = a->u_sample;
+  p.accepted_len = o->accepted_len;
+  p.out_tokens = o->out_tokens;
+  p.num_emitted = o->num_emitted;
+  p.row_status = o->row_status;
+  p.p_at_draft = o->p_at_draft;
+  p.q_at_draft = o->q_at_draft;
+  p.resid_mass = o->resid_mass;
+  p.row_counter = static_cast<uint32_t *>(ws);
+  p.rec = reinterpret_cast<ChainRec *>(static_cast<char *>(ws) + counters_bytes(a->B));
+  p.B = a->B;
+  p.K = K;
+  p.V = a->V;
+  p.L = L;
+  p.use_tma = aligned(a->target_logits, 16) && (K == 0 || aligned(a->draft_logits, 16)) &&
+              (static_cast<long long>(a->V) * esz) % 16 == 0;
+  p.buf_bytes = static_cast<int>(buf_of(C));
+  int stages = static_cast<int>((static_cast<size_t>(di.smem_optin) - kStochCtrlBytes) / (2 * static_cast<size_t>(p.buf_bytes)));
+  stages = std::max(1, std::min(stages, 4));
+  p.stages = stages;
+  p.wait_limit_ns = g_wait_ns.load();
+  p.force_timeout = g_force_timeout.load();
+  const size_t smem = static_cast<size_t>(stages) * 2 * p.buf_bytes + kStochCtrlBytes;
+  int maxc = 0;
+  if (max_clusters(dev, bf16, nv, C, smem, &maxc) != cudaSuccess || maxc < 1) return SPEC_ERR_CUDA;
+  const int grid_clusters = static_cast<int>(std::min<long long>(W, maxc));
+  report("stochastic C L nv stages smem max_clusters tma", C, L, nv, stages, (long long)smem, maxc,
+         p.use_tma);
+  if (launch_chain_stochastic(p, bf16, nv, C, grid_clusters, smem, s) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+spec_status spec_verify_tree(const spec_tree_args *a, const spec_tree_out *o, void *ws,
+                             size_t ws_bytes, void *stream) {
+  if (!a || !o) return SPEC_ERR_NULL;
+  if (!valid_sizes(a->B, a->V) || a->N < 1 || a->N > SPEC_MAX_TREE_NODES) return SPEC_ERR_SHAPE;
+  if (a->dtype != SPEC_F32 && a->dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  if (std::isnan(a->margin_kappa)) return SPEC_ERR_ARG;
+  if (!a->target_logits || !a->parent || !a->node_tokens || !o->accepted_len || !o->path_nodes ||
+      !o->out_tokens || !o->num_emitted || !o->row_status)
+    return SPEC_ERR_NULL;
+  const int esz = a->dtype == SPEC_BF16 ? 2 : 4;
+  if (!aligned(a->target_logits, esz)) return SPEC_ERR_ALIGN;
+  const void *i32s[] = {a->parent, a->node_tokens, a->temperature, o->accepted_len,
+                        o->path_nodes, o->out_tokens, o->num_emitted, o->row_status};
+  for (const void *p : i32s)
+    if (p && !aligned(p, 4)) return SPEC_ERR_ALIGN;
+  const size_t need = spec_verify_tree_workspace_size(a->B, a->N, a->V);
+  if (!ws || !aligned(ws, 256) || ws_bytes < need) return SPEC_ERR_WORKSPACE;
+  if (a->B == 0) return SPEC_OK;
+  GreedyParams p = {};
+  p.target = a->target_logits;
+  p.tokens = a->node_tokens;
+  p.parent = a->parent;
+  p.temperature = a->temperature;
+  p.use_margin = a->margin_kappa > 0.f;
+  p.ln_kappa = p.use_margin ? std::log(static_cast<double>(a->margin_kappa)) : 0.0;
+  p.tree = 1;
+  p.accepted_len = o->accepted_len;
+  p.out_tokens = o->out_tokens;
+  p.num_emitted = o->num_emitted;
+  p.row_status = o->row_status;
+  p.path_nodes = o->path_nodes;
+  p.B = a->B;
+  p.npos = a->N;
+  p.V = a->V;
+  return run_greedy(p, a->dtype == SPEC_BF16, esz, ws, static_cast<cudaStream_t>(stream));
+}
+
+spec_status spec_rollback_lengths(int32_t B, int32_t max_emit, const int32_t *kv_len_in,
+                                  const int32_t *accepted_len, const int32_t *num_emitted_in,
+                                  const int32_t *out_tokens, int32_t eos_id,
+                                  const int32_t *max_len, int32_t *committed_kv_len,
+                                  int32_t *num_emitted_out, void *stream) {
+  if (B < 0 || max_emit < 1) return SPEC_ERR_SHAPE;
+  if (!kv_len_in || !accepted_len || !num_emitted_in || !out_tokens || !committed_kv_len ||
+      !num_emitted_out)
+    return SPEC_ERR_NULL;
+  const void *ptrs[] = {kv_len_in, accepted_len, num_emitted_in, out_tokens, max_len,
+                        committed_kv_len, num_emitted_out};
+  for (const void *p : ptrs)
+    if (p && !aligned(p, 4)) return SPEC_ERR_ALIGN;
+  if (B == 0) return SPEC_OK;
+  RollbackParams p = {B, max_emit, kv_len_in, accepted_len, num_emitted_in, out_tokens, eos_id,
+                      max_len, committed_kv_len, num_emitted_out};
+  return launch_rollback(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SPEC_OK
+                                                                               : SPEC_ERR_CUDA;
+}
+
+spec_status spec_workspace_init(void *ws, size_t ws_bytes, void *stream) {
+  if (!ws) return SPEC_ERR_NULL;
+  return cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SPEC_OK
+             : SPEC_ERR_CUDA;
+}
+
+const char *spec_status_string(spec_status s) {
+  switch (s) {
+    case SPEC_OK: return "SPEC_OK";
+    case SPEC_ERR_NULL: return "SPEC_ERR_NULL: a required pointer is NULL";
+    case SPEC_ERR_SHAPE: return "SPEC_ERR_SHAPE: a size is outside the supported range";
+    case SPEC_ERR_DTYPE: return "SPEC_ERR_DTYPE: unknown dtype or mode";
+    case SPEC_ERR_ALIGN: return "SPEC_ERR_ALIGN: a pointer is misaligned";
+    case SPEC_ERR_ARG: return "SPEC_ERR_ARG: bad scalar argument";
+    case SPEC_ERR_CUDA: return "SPEC_ERR_CUDA: a CUDA runtime call failed";
+    case SPEC_ERR_WORKSPACE: return "SPEC_ERR_WORKSPACE: workspace missing, misaligned or too small";
+  }
+  return "unknown spec_status";
+}
+
+void spec_set_wait_timeout_ns(uint64_t ns) { g_wait_ns.store(ns); }
+uint64_t spec_get_wait_timeout_ns(void) { return g_wait_ns.load(); }
+void spec_debug_force_wait_timeout(int on) { g_force_timeout.store(on ? 1 : 0); }
+
+}  // extern "C"

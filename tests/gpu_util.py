@@ -1,0 +1,57 @@
+"""Helpers of the GPU parity tests: numpy <-> CUDA marshalling and the band rule."""
+import numpy as np
+import torch
+
+BAND = 1e-5  # decision margin below which fp32 and fp64 may legitimately disagree
+PROB_ATOL = 1e-5
+
+
+def cuda(a):
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(a).cuda()
+
+
+def host(d):
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in d.items()}
+
+
+def run_chain(sv, inp, mode="stochastic", kappa=0.0, diagnostics=True, draft=True):
+    g = sv.spec_verify_chain(cuda(inp["target"]), cuda(inp["draft"]) if draft else None,
+                             cuda(inp["draft_tokens"]), cuda(inp.get("temperature")),
+                             cuda(inp.get("u_accept")), cuda(inp.get("u_sample")), mode=mode,
+                             margin_kappa=kappa, diagnostics=diagnostics)
+    return host(g)
+
+
+def compare_stochastic(g, o, band=BAND):
+    """Per-sample parity under the band rule.  Returns the number of rows whose
+    outputs differ while the oracle's smallest decision margin is below band;
+    fails on any difference outside the band."""
+    assert np.array_equal(g["row_status"], o["row_status"]), (g["row_status"], o["row_status"])
+    ok = o["row_status"] == 0
+    same = (g["accepted_len"] == o["accepted_len"]) & np.all(g["out_tokens"] == o["out_tokens"], axis=1)
+    mism = ~same & ok
+    outside = mism & (o["row_margin"] >= band)
+    if outside.any():
+        b = int(np.nonzero(outside)[0][0])
+        raise AssertionError(
+            f"{int(outside.sum())} rows differ outside the band; row {b}: gpu len "
+            f"{g['accepted_len'][b]} toks {g['out_tokens'][b]} vs oracle len "
+            f"{o['accepted_len'][b]} toks {o['out_tokens'][b]} margin {o['row_margin'][b]}")
+    bad = ~ok
+    assert np.all(g["accepted_len"][bad] == -1) and np.all(g["num_emitted"][bad] == 0)
+    assert np.all(g["out_tokens"][bad] == -1)
+    assert np.array_equal(g["num_emitted"][ok], g["accepted_len"][ok] + 1)
+    if "p_at_draft" in g and g["p_at_draft"].size:
+        np.testing.assert_allclose(g["p_at_draft"][ok], o["p_at_draft"][ok], atol=PROB_ATOL, rtol=0)
+        np.testing.assert_allclose(g["q_at_draft"][ok], o["q_at_draft"][ok], atol=PROB_ATOL, rtol=0)
+        # residual mass where both sides took the same decision at that position
+        decided = (o["accept_margin"] >= band) & ok[:, None]
+        np.testing.assert_allclose(g["resid_mass"][decided], o["resid_mass"][decided],
+                                   atol=PROB_ATOL, rtol=0)
+    return int(mism.sum())

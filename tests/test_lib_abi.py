@@ -1,0 +1,155 @@
+"""The C-ABI library loads, exports every declared entry point, and rejects bad
+arguments on the host before touching CUDA (runs without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "specverify.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from speculative_decoding_verification_32_gb300 import build as lib_build
+    from speculative_decoding_verification_32_gb300 import _binding
+
+    lib_build.build()
+    return _binding.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert "spec_verify_chain" in names and "spec_verify_tree" in names
+    assert "spec_rollback_lengths" in names
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in specverify.h but not exported"
+
+
+def test_status_strings(L):
+    for code in range(8):
+        s = L.spec_status_string(code).decode()
+        assert s.startswith("SPEC_")
+
+
+def test_workspace_sizes(L):
+    assert L.spec_verify_chain_workspace_size(64, 5, 128256) > 64 * 6 * 16
+    assert L.spec_verify_chain_workspace_size(0, 5, 100) >= 0
+    assert L.spec_verify_chain_workspace_size(-1, 5, 100) == 0
+    assert L.spec_verify_chain_workspace_size(4, -1, 100) == 0
+    assert L.spec_verify_chain_workspace_size(4, 5, 0) == 0
+    assert L.spec_verify_chain_workspace_size(4, 5, 262145) == 0
+    assert L.spec_verify_tree_workspace_size(32, 60, 151936) > 32 * 60 * 16
+    assert L.spec_verify_tree_workspace_size(32, 0, 100) == 0
+    assert L.spec_verify_tree_workspace_size(32, 1025, 100) == 0
+
+
+def _fake(addr):
+    return ctypes.c_void_p(addr)
+
+
+def _chain_args(B=2, K=3, V=1000, dtype=1, mode=0, kappa=0.0, base=0x10000000):
+    from speculative_decoding_verification_32_gb300._binding import SpecChainArgs, SpecChainOut
+    a = SpecChainArgs(B, K, V, dtype, mode, kappa, _fake(base), _fake(base + 0x100000),
+                      _fake(base + 0x200000), None, _fake(base + 0x300000), _fake(base + 0x400000))
+    o = SpecChainOut(_fake(base + 0x500000), _fake(base + 0x600000), _fake(base + 0x700000),
+                     _fake(base + 0x800000), None, None, None)
+    return a, o
+
+
+def test_chain_argument_errors_return_before_cuda(L):
+    ws = _fake(0x20000000)
+    big = 1 << 30
+    a, o = _chain_args()
+    assert L.spec_verify_chain(None, ctypes.byref(o), ws, big, None) == 1
+    a, o = _chain_args(B=-1)
+    assert L.spec_verify_chain(ctypes.byref(a), ctypes.byref(o), ws, big, None) == 2
+    a, o = _chain_args(K=2000)
+    assert L.spec_verify_chain(ctypes.byref(a), ctypes.byref(o), ws, big, None) == 2
+    a, o = _chain_args(V=0)
+    assert L.spec_verify_chain(ctypes.byref(a), ctypes.byref(o), ws, big, None) == 2
+    a, o = _chain_args(dtype=7)
+    assert L.spec_verify_chain(ctypes.byref(a), ctypes.byref(o), ws, big, None) == 3
+    a, o = _chain_args(mode=3)
+    assert L.spec_verify_chain(ctypes.byref(a), ctypes.byref(o), ws, big, None) == 3
+    a, o = _chain_args(kappa=float("nan"))
+    assert L.spec_verify_chain(ctypes.byref(a), ctypes.byref(o), ws, big, None) == 5
+    a, o = _chain_args()
+    a.u_sample = None
+    assert L.spec_verify_chain(ctypes.byref(a), ctypes.byref(o), ws, big, None) == 1
+    a, o = _chain_args()
+    o.row_status = None
+    assert L.spec_verify_chain(ctypes.byref(a), ctypes.byref(o), ws, big, None) == 1
+    a, o = _chain_args()
+    a.target_logits = _fake(0x10000001)  # bf16 needs 2-byte alignment
+    assert L.spec_verify_chain(ctypes.byref(a), ctypes.byref(o), ws, big, None) == 4
+    a, o = _chain_args()
+    a.draft_tokens = _fake(0x10000002)
+    assert L.spec_verify_chain(ctypes.byref(a), ctypes.byref(o), ws, big, None) == 4
+    a, o = _chain_args()
+    assert L.spec_verify_chain(ctypes.byref(a), ctypes.byref(o), None, big, None) == 7
+    assert L.spec_verify_chain(ctypes.byref(a), ctypes.byref(o), _fake(0x20000010), big, None) == 7
+    assert L.spec_verify_chain(ctypes.byref(a), ctypes.byref(o), ws, 16, None) == 7
+    # greedy mode does not need draft logits or uniforms, but needs tokens
+    a, o = _chain_args(mode=1)
+    a.draft_tokens = None
+    assert L.spec_verify_chain(ctypes.byref(a), ctypes.byref(o), ws, big, None) == 1
+    # B == 0 is a valid no-op that never touches the device
+    a, o = _chain_args(B=0)
+    assert L.spec_verify_chain(ctypes.byref(a), ctypes.byref(o), ws, big, None) == 0
+
+
+def test_tree_and_rollback_argument_errors(L):
+    from speculative_decoding_verification_32_gb300._binding import SpecTreeArgs, SpecTreeOut
+    ws = _fake(0x20000000)
+    big = 1 << 30
+    b = 0x10000000
+
+    def tree(N=8, V=100, dtype=1):
+        a = SpecTreeArgs(2, N, V, dtype, 0.3, _fake(b), _fake(b + 0x1000), _fake(b + 0x2000), None)
+        o = SpecTreeOut(_fake(b + 0x3000), _fake(b + 0x4000), _fake(b + 0x5000),
+                        _fake(b + 0x6000), _fake(b + 0x7000))
+        return a, o
+    a, o = tree(N=0)
+    assert L.spec_verify_tree(ctypes.byref(a), ctypes.byref(o), ws, big, None) == 2
+    a, o = tree(N=1025)
+    assert L.spec_verify_tree(ctypes.byref(a), ctypes.byref(o), ws, big, None) == 2
+    a, o = tree(dtype=2)
+    assert L.spec_verify_tree(ctypes.byref(a), ctypes.byref(o), ws, big, None) == 3
+    a, o = tree()
+    a.parent = None
+    assert L.spec_verify_tree(ctypes.byref(a), ctypes.byref(o), ws, big, None) == 1
+    a, o = tree()
+    assert L.spec_verify_tree(ctypes.byref(a), ctypes.byref(o), ws, 8, None) == 7
+    p = _fake(b)
+    assert L.spec_rollback_lengths(-1, 4, p, p, p, p, -1, None, p, p, None) == 2
+    assert L.spec_rollback_lengths(2, 0, p, p, p, p, -1, None, p, p, None) == 2
+    assert L.spec_rollback_lengths(2, 4, None, p, p, p, -1, None, p, p, None) == 1
+    assert L.spec_rollback_lengths(2, 4, _fake(b + 2), p, p, p, -1, None, p, p, None) == 4
+    assert L.spec_rollback_lengths(0, 4, p, p, p, p, -1, None, p, p, None) == 0
+
+
+def test_wait_timeout_setting(L):
+    old = L.spec_get_wait_timeout_ns()
+    L.spec_set_wait_timeout_ns(12345)
+    assert L.spec_get_wait_timeout_ns() == 12345
+    L.spec_set_wait_timeout_ns(old)
+
+
+def test_product_path_never_imports_the_oracle():
+    """The package and its C sources name nothing under oracle/."""
+    pkg = os.path.join(ROOT, "speculative_decoding_verification_32_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "spec_oracle" not in text and "so_verify" not in text, f
