@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sets", type=int, default=0,
+                    help="rotating input sets (0: enough to exceed 3x L2)")
     return ap.parse_args()
 
 
@@ -207,7 +209,7 @@ def run_ours(args):
     B, K = inp["draft_tokens"].shape
     V = inp["target"].shape[-1]
     step_bytes = inp["target"].nbytes + inp["draft"].nbytes
-    sets = max(2, -(-3 * L2_BYTES // step_bytes) + 1)  # rotating copies, > 3x L2 in total
+    sets = args.sets or max(2, -(-3 * L2_BYTES // step_bytes) + 1)  # rotating copies, > 3x L2
     small = {k: to_cuda(inp[k], dev) for k in ("draft_tokens", "temperature", "u_accept", "u_sample")}
     tgt0 = to_cuda(inp["target"], dev)
     drf0 = to_cuda(inp["draft"], dev)

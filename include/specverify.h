@@ -32,15 +32,18 @@
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *    stream) and runs asynchronously; read results after synchronising.
  *  - Argument errors return a spec_status before anything is enqueued and
- *    write no output.  Data errors in a row (NaN logit, token id out of
- *    range, ...) set that row's row_status; the row's accepted_len becomes
- *    -1, num_emitted 0 and its token outputs -1; other rows are unaffected.
+ *    write no output.  B == 0 is a valid no-op (pointers may then be NULL).
+ *    Data errors in a row (NaN logit, token id out of range, ...) set that
+ *    row's row_status; the row's accepted_len becomes -1, num_emitted 0 and
+ *    its token outputs -1; other rows are unaffected.
  *  - Workspace: `ws` is caller-owned device memory of at least the size the
- *    matching *_workspace_size() returns, 256-byte aligned, ZERO-FILLED
- *    before its first use (cudaMemset or spec_workspace_init).  Every
- *    completed call leaves it zero-filled again, so it can be reused by the
- *    next call on the same stream.  Calls that may overlap in time (other
- *    streams) need separate workspaces.
+ *    matching *_workspace_size() returns, 256-byte aligned.  Its contents
+ *    need no initialisation: each call overwrites what it reads.  Calls on
+ *    one stream may share a workspace; calls that may overlap in time
+ *    (different streams) need separate workspaces.
+ *  - Each verify call enqueues two kernels: the streaming kernel and a small
+ *    per-row walk kernel that starts early and waits for it on the device
+ *    (programmatic dependent launch).
  *  - Logits are bf16 (SPEC_BF16) or fp32 (SPEC_F32).  Rows whose byte
  *    length is a multiple of 16 with a 16-byte aligned base take the bulk-
  *    copy (TMA) path; any other V still works, more slowly.
@@ -120,13 +123,14 @@ typedef struct {
                             token, then -1 */
   int32_t *num_emitted;  /* [B] a + 1 (0: bad row) */
   int32_t *row_status;   /* [B] SPEC_ROW_* */
-  /* Optional diagnostics (NULL to skip), STOCHASTIC only, one value per
-   * position j < K computed independently of the walk (unspecified for rows
-   * with a nonzero row_status): */
+  /* Optional diagnostics (NULL to skip), STOCHASTIC only, unspecified for
+   * rows with a nonzero row_status.  p and q are given for every j < K,
+   * independently of the walk: */
   float *p_at_draft;     /* [B, K] p_j(y_j) */
   float *q_at_draft;     /* [B, K] q_j(y_j) */
-  float *resid_mass;     /* [B, K] sum_v [p_j - q_j]+ where position j's own test
-                            rejects, else 0 */
+  float *resid_mass;     /* [B, K] sum_v [p_j - q_j]+ at the position where the
+                            walk stops on a rejection (the residual that is
+                            sampled), 0 at every other position */
 } spec_chain_out;
 
 /* Bytes of workspace spec_verify_chain needs for these sizes (any mode and
@@ -218,7 +222,8 @@ spec_status spec_rollback_lengths(int32_t B, int32_t max_emit, const int32_t *kv
 
 /* ------------------------------------------------------------------ misc */
 
-/* Zero-fill a workspace on `stream` (a cudaMemsetAsync). */
+/* Zero-fill a workspace on `stream` (a cudaMemsetAsync).  Optional: the
+ * verify calls do not need a zeroed workspace. */
 spec_status spec_workspace_init(void *ws, size_t ws_bytes, void *stream);
 
 /* Human-readable name of a spec_status. */

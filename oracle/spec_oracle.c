@@ -186,7 +186,8 @@ static int margin_promotes(double l_d, double l_top, double T, float kappa) {
  * correction or bonus, then -1), num_emitted [B] = accepted_len + 1,
  * row_status [B].  Optional (NULL to skip), STOCHASTIC only, every j < K
  * independent of the walk: p_at_draft, q_at_draft, ratio [B,K]; resid_mass
- * [B,K] = sum_v [p_j - q_j]_+ where position j's own test rejects, else 0.
+ * [B,K] = sum_v [p_j - q_j]_+ at the position where the walk stops on a
+ * rejection (the residual that is sampled), 0 at every other position.
  * Band bookkeeping (optional): accept_margin [B,K] = |u - min(1, ratio)|;
  * row_margin [B] = smallest decision margin met by the walk (accept margins
  * of positions 0..stop and the sampling gap at the stop; +inf for greedy).
@@ -288,13 +289,14 @@ void so_verify_chain(int B, int K, int V, int dtype, int mode,
         if (p_at_draft) p_at_draft[o] = p[y];
         if (q_at_draft) q_at_draft[o] = q[y];
         if (ratio_out) ratio_out[o] = ratio;
-        if (resid_mass) resid_mass[o] = accept ? 0.0 : Z;
+        if (resid_mass) resid_mass[o] = 0.0;
         if (accept_margin) accept_margin[o] = m_acc;
         if (stop >= 0) continue; /* walk already stopped: diagnostics only */
         if (m_acc < margin) margin = m_acc;
         if (!accept) {
           double gap;
           stop = j;
+          if (resid_mass) resid_mass[o] = Z;
           token = Z > 0.0 ? inverse_cdf(r, V, (double)u_sample[trow0 + j], &gap)
                           : inverse_cdf(p, V, (double)u_sample[trow0 + j], &gap);
           if (gap < margin) margin = gap;

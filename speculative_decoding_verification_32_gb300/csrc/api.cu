@@ -27,11 +27,10 @@ struct DevInfo {
 
 std::mutex g_mu;
 std::map<int, DevInfo> g_dev;
-std::map<std::tuple<int, int, int, int, size_t>, int> g_clusters;
 std::map<std::tuple<int, int, size_t>, int> g_blocks;
 
-constexpr size_t kStochCtrlBytes = 2048;
 constexpr size_t kGreedyCtrlBytes = 1024;
+constexpr size_t kSoftCtrlBytes = 2048;
 constexpr int kMinGreedySlice = 2048;
 
 // SPECVERIFY_VERBOSE=1 prints each distinct launch shape once (stderr).
@@ -76,20 +75,20 @@ cudaError_t device_info(int *dev, DevInfo *info) {
   return cudaSuccess;
 }
 
-cudaError_t max_clusters(int dev, bool bf16, int nv, int C, size_t smem, int *out) {
-  auto key = std::make_tuple(dev, (int)bf16, nv, C, smem);
+cudaError_t soft_blocks(int dev, bool bf16, int nv, size_t smem, int *out) {
+  auto key = std::make_tuple(dev, 2 + (int)bf16 + 2 * nv, smem);
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    auto it = g_clusters.find(key);
-    if (it != g_clusters.end()) {
+    auto it = g_blocks.find(key);
+    if (it != g_blocks.end()) {
       *out = it->second;
       return cudaSuccess;
     }
   }
-  cudaError_t e = chain_stochastic_max_clusters(bf16, nv, C, smem, out);
+  cudaError_t e = soft_partials_blocks_per_sm(bf16, nv, smem, out);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lk(g_mu);
-  g_clusters[key] = *out;
+  g_blocks[key] = *out;
   return cudaSuccess;
 }
 
@@ -109,8 +108,6 @@ cudaError_t greedy_blocks(int dev, bool bf16, size_t smem, int *out) {
   g_blocks[key] = *out;
   return cudaSuccess;
 }
-
-size_t counters_bytes(int32_t B) { return align_up(static_cast<size_t>(B) * 4, 256); }
 
 size_t greedy_partials_max(int32_t B, int32_t npos, int32_t V) {
   return static_cast<size_t>(B) * npos * ceil_div(V, kMinGreedySlice) * sizeof(GreedyPart);
@@ -135,16 +132,14 @@ spec_status run_greedy(GreedyParams &p, bool bf16, int esz, void *ws, cudaStream
   p.nslices = ceil_div(p.V, slice);
   p.use_tma = aligned(p.target, 16) && (static_cast<long long>(p.V) * esz) % 16 == 0;
   p.buf_bytes = static_cast<int>(align_up(static_cast<size_t>(slice) * esz, 128));
-  const size_t scratch = p.tree ? align_up(static_cast<size_t>(p.npos) * 20, 128) : 0;
-  const size_t fixed = kGreedyCtrlBytes + scratch;
+  const size_t fixed = kGreedyCtrlBytes;
   int stages = static_cast<int>((static_cast<size_t>(di.smem_optin) - fixed) / p.buf_bytes);
   stages = std::max(1, std::min(stages, 4));
   p.stages = stages;
   const size_t smem = static_cast<size_t>(stages) * p.buf_bytes + fixed;
   p.wait_limit_ns = g_wait_ns.load();
   p.force_timeout = g_force_timeout.load();
-  p.row_counter = static_cast<uint32_t *>(ws);
-  p.part = reinterpret_cast<GreedyPart *>(static_cast<char *>(ws) + counters_bytes(p.B));
+  p.part = static_cast<GreedyPart *>(ws);
   int per_sm = 0;
   if (greedy_blocks(dev, bf16, smem, &per_sm) != cudaSuccess || per_sm < 1) return SPEC_ERR_CUDA;
   const long long items = positions * p.nslices;
@@ -161,14 +156,17 @@ extern "C" {
 
 size_t spec_verify_chain_workspace_size(int32_t B, int32_t K, int32_t V) {
   if (!valid_sizes(B, V) || K < 0 || K > SPEC_MAX_K) return 0;
-  const size_t rec = static_cast<size_t>(B) * (K + 1) * sizeof(ChainRec);
+  // stochastic: one partial per (logit row, slice), the smallest slice being
+  // the fp32 one; greedy: one partial per (position, slice)
+  const size_t rows = static_cast<size_t>(B) * (K + 1) + static_cast<size_t>(B) * K;
+  const size_t soft = rows * ceil_div(V, kSoftMinSlice) * sizeof(SoftPart) + align_up(rows * 4, 256);
   const size_t part = greedy_partials_max(B, K + 1, V);
-  return counters_bytes(B) + std::max(rec, part);
+  return align_up(std::max(std::max(soft, part), static_cast<size_t>(256)), 256);
 }
 
 size_t spec_verify_tree_workspace_size(int32_t B, int32_t N, int32_t V) {
   if (!valid_sizes(B, V) || N < 1 || N > SPEC_MAX_TREE_NODES) return 0;
-  return counters_bytes(B) + greedy_partials_max(B, N, V);
+  return align_up(std::max(greedy_partials_max(B, N, V), static_cast<size_t>(256)), 256);
 }
 
 spec_status spec_verify_chain(const spec_chain_args *a, const spec_chain_out *o, void *ws,
@@ -178,6 +176,7 @@ spec_status spec_verify_chain(const spec_chain_args *a, const spec_chain_out *o,
   if (a->dtype != SPEC_F32 && a->dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
   if (a->mode != SPEC_STOCHASTIC && a->mode != SPEC_GREEDY) return SPEC_ERR_DTYPE;
   if (std::isnan(a->margin_kappa)) return SPEC_ERR_ARG;
+  if (a->B == 0) return SPEC_OK;  // nothing to do; empty arrays may be NULL
   const bool stoch = a->mode == SPEC_STOCHASTIC;
   const int K = a->K;
   if (!a->target_logits || !o->accepted_len || !o->out_tokens || !o->num_emitted ||
@@ -224,24 +223,6 @@ spec_status spec_verify_chain(const spec_chain_args *a, const spec_chain_out *o,
   DevInfo di;
   if (device_info(&dev, &di) != cudaSuccess) return SPEC_ERR_CUDA;
   const int epv = 16 / esz;
-  const long long W = static_cast<long long>(a->B) * (K + 1);
-  const int cap = kThreads * kMaxElemsPerThread;  // elements per CTA kept in registers
-  int C = 1;
-  while (C < 16 && ceil_div(a->V, C) > cap) C *= 2;
-  if (ceil_div(a->V, C) > cap) return SPEC_ERR_SHAPE;
-  auto buf_of = [&](int c) {
-    const size_t L = align_up(static_cast<size_t>(ceil_div(a->V, c)), static_cast<size_t>(epv));
-    return align_up(L * esz, 128);
-  };
-  // keep at least two pipeline stages
-  while (C < 16 && 2 * 2 * buf_of(C) + kStochCtrlBytes > static_cast<size_t>(di.smem_optin)) C *= 2;
-  // small problems: split the vocabulary further so every SM has work
-  while (C < 8 && W * C < 2LL * di.sms && ceil_div(a->V, 2 * C) >= 2048) C *= 2;
-  const int L = static_cast<int>(align_up(static_cast<size_t>(ceil_div(a->V, C)), static_cast<size_t>(epv)));
-  int nv = ceil_div(ceil_div(L, epv), kThreads);
-  nv = nv <= 1 ? 1 : nv <= 2 ? 2 : nv <= 4 ? 4 : 8;
-  if (bf16 && nv > 4) return SPEC_ERR_SHAPE;
-
   ChainStochParams p = {};
   p.target = a->target_logits;
   p.draft = a->draft_logits;
@@ -256,28 +237,57 @@ spec_status spec_verify_chain(const spec_chain_args *a, const spec_chain_out *o,
   p.p_at_draft = o->p_at_draft;
   p.q_at_draft = o->q_at_draft;
   p.resid_mass = o->resid_mass;
-  p.row_counter = static_cast<uint32_t *>(ws);
-  p.rec = reinterpret_cast<ChainRec *>(static_cast<char *>(ws) + counters_bytes(a->B));
+  p.part = static_cast<SoftPart *>(ws);
   p.B = a->B;
   p.K = K;
   p.V = a->V;
-  p.L = L;
   p.use_tma = aligned(a->target_logits, 16) && (K == 0 || aligned(a->draft_logits, 16)) &&
               (static_cast<long long>(a->V) * esz) % 16 == 0;
-  p.buf_bytes = static_cast<int>(buf_of(C));
-  int stages = static_cast<int>((static_cast<size_t>(di.smem_optin) - kStochCtrlBytes) / (2 * static_cast<size_t>(p.buf_bytes)));
-  stages = std::max(1, std::min(stages, 4));
-  p.stages = stages;
   p.wait_limit_ns = g_wait_ns.load();
   p.force_timeout = g_force_timeout.load();
-  const size_t smem = static_cast<size_t>(stages) * 2 * p.buf_bytes + kStochCtrlBytes;
-  int maxc = 0;
-  if (max_clusters(dev, bf16, nv, C, smem, &maxc) != cudaSuccess || maxc < 1) return SPEC_ERR_CUDA;
-  const int grid_clusters = static_cast<int>(std::min<long long>(W, maxc));
-  report("stochastic C L nv stages smem max_clusters tma", C, L, nv, stages, (long long)smem, maxc,
-         p.use_tma);
-  if (launch_chain_stochastic(p, bf16, nv, C, grid_clusters, smem, s) != cudaSuccess)
-    return SPEC_ERR_CUDA;
+  // stream kernel: fixed-size items (16 or 32 KB), a bulk-copy ring per CTA;
+  // SPECVERIFY_SOFT_VECS (4 or 8) and SPECVERIFY_SOFT_STAGES (2..4) override
+  // the defaults for tuning
+  int nv = kSoftVecs;
+  if (const char *ov = std::getenv("SPECVERIFY_SOFT_VECS")) nv = std::atoi(ov) == 8 ? 8 : 4;
+  p.slice = kSoftThreads * nv * epv;
+  p.nslices = ceil_div(a->V, p.slice);
+  p.buf_bytes = 2 * p.slice * esz;  // target tile + draft tile
+  p.stages = kSoftStages;
+  if (const char *ov = std::getenv("SPECVERIFY_SOFT_STAGES")) {
+    const int st = std::atoi(ov);
+    if (st >= 2 && st <= 4) p.stages = st;
+  }
+  const size_t smem = static_cast<size_t>(p.stages) * p.buf_bytes + kSoftCtrlBytes;
+  {
+    const size_t rows = static_cast<size_t>(a->B) * (K + 1) + static_cast<size_t>(a->B) * K;
+    p.ylog = reinterpret_cast<float *>(static_cast<char *>(ws) +
+                                       align_up(rows * p.nslices * sizeof(SoftPart), 256));
+  }
+  int per_sm = 0;
+  if (soft_blocks(dev, bf16, nv, smem, &per_sm) != cudaSuccess || per_sm < 1) return SPEC_ERR_CUDA;
+  const long long tiles = (static_cast<long long>(a->B) * (K + 1) + static_cast<long long>(a->B) * K) * p.nslices;
+  const int grid = static_cast<int>(std::min<long long>(tiles, static_cast<long long>(di.sms) * per_sm));
+  // resolve kernel: a cluster of C CTAs per row, at most 16 rounds of 32
+  // vectors per warp
+  constexpr int kRW = kResolveThreads / 32;
+  auto rounds = [&](int c) {
+    const int L = static_cast<int>(align_up(static_cast<size_t>(ceil_div(a->V, c)), static_cast<size_t>(epv)));
+    return ceil_div(ceil_div(ceil_div(L, epv), kRW), 32);
+  };
+  int C = 1;
+  while (C < 16 && rounds(C) > kResolveMaxRounds) C *= 2;
+  if (rounds(C) > kResolveMaxRounds) return SPEC_ERR_SHAPE;
+  while (C < 8 && ceil_div(a->V, 2 * C) >= 2048) C *= 2;  // spread each row's work
+  if (const char *ov = std::getenv("SPECVERIFY_CLUSTER")) {  // tuning override
+    const int c = std::atoi(ov);
+    if (c >= C && c <= 16 && (c & (c - 1)) == 0) C = c;
+  }
+  p.L = static_cast<int>(align_up(static_cast<size_t>(ceil_div(a->V, C)), static_cast<size_t>(epv)));
+  p.vpw = 32 * rounds(C);
+  report("stochastic slice nslices stages grid per_sm cluster L", p.slice, p.nslices, p.stages,
+         grid, per_sm, C, p.L);
+  if (launch_chain_stochastic(p, bf16, nv, grid, smem, C, s) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
 }
 
@@ -287,6 +297,7 @@ spec_status spec_verify_tree(const spec_tree_args *a, const spec_tree_out *o, vo
   if (!valid_sizes(a->B, a->V) || a->N < 1 || a->N > SPEC_MAX_TREE_NODES) return SPEC_ERR_SHAPE;
   if (a->dtype != SPEC_F32 && a->dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
   if (std::isnan(a->margin_kappa)) return SPEC_ERR_ARG;
+  if (a->B == 0) return SPEC_OK;
   if (!a->target_logits || !a->parent || !a->node_tokens || !o->accepted_len || !o->path_nodes ||
       !o->out_tokens || !o->num_emitted || !o->row_status)
     return SPEC_ERR_NULL;
@@ -324,6 +335,7 @@ spec_status spec_rollback_lengths(int32_t B, int32_t max_emit, const int32_t *kv
                                   const int32_t *max_len, int32_t *committed_kv_len,
                                   int32_t *num_emitted_out, void *stream) {
   if (B < 0 || max_emit < 1) return SPEC_ERR_SHAPE;
+  if (B == 0) return SPEC_OK;
   if (!kv_len_in || !accepted_len || !num_emitted_in || !out_tokens || !committed_kv_len ||
       !num_emitted_out)
     return SPEC_ERR_NULL;

@@ -1,28 +1,35 @@
-// chain_stochastic.cu -- the stochastic chain verifier (one kernel per step).
+// chain_stochastic.cu -- the stochastic chain verifier.
 //
-// Computes, for every row b and draft position j, the tests of
-// "Speculative Decoding: Draft, Verify, and Correct" ('Name the two
-// distributions at one prefix', 'Verify several proposed tokens in one target
-// pass'): p = softmax(target/T), q = softmax(draft/T), accept y_j iff
-// p(y_j)/q(y_j) >= 1 or u < p(y_j)/q(y_j); at a rejection draw from
-// [p - q]+ by inverse CDF; at j = K draw the bonus from p.  The walk to the
-// first rejection is fused in as a "last position of the row finishes" step.
+// Computes the test of "Speculative Decoding: Draft, Verify, and Correct"
+// ('Name the two distributions at one prefix', 'Verify several proposed tokens
+// in one target pass'): p = softmax(target/T), q = softmax(draft/T); position
+// j accepts y_j iff p(y_j)/q(y_j) >= 1 or u < p(y_j)/q(y_j); the walk stops at
+// the first rejection and draws the correction from the residual [p - q]+ by
+// inverse CDF; if every draft passes, the bonus token is drawn from p_K.
 //
-// Layout of the work: a persistent grid of thread-block clusters of C CTAs.
-// Each cluster owns a round-robin share of the B*(K+1) positions; CTA r of the
-// cluster owns vocabulary slice [r*L, (r+1)*L) of each position.  Per position:
-//   1. bulk copies (TMA, non-multicast) of the CTA's target and draft slices
-//      land in a `stages`-deep shared-memory ring, prefetched ahead;
-//   2. pass 1 moves the slice to registers and finds the NaN-propagating max;
-//      max exchanged across the cluster through distributed shared memory;
-//   3. pass 2 turns every logit into exp2((x - max) * log2(e) / T) in place
-//      (one exp per logit, kept in registers) and sums; sums exchanged;
-//   4. the acceptance ratio is formed in log2 space from the draft token's
-//      logits; a rejecting position sums its residual [p - q]+ from the
-//      registers (no more exps, no more HBM traffic), exchanges the per-CTA
-//      masses, and the CTA whose range holds u * Z finds the token with a
-//      hierarchical scan (round -> warp -> lane -> element, vocabulary order).
-// Every logit is read from HBM exactly once.
+// Two kernels per call:
+//
+//  softmax_partials_kernel -- the HBM stream.  A persistent grid (several CTAs
+//    per SM, no clusters) walks (logit row, vocabulary slice) items through a
+//    bulk-copy (TMA) ring in shared memory.  Each item yields the slice's max
+//    logit m and sum of exp2((x - m) log2(e) / T) (an online softmax: each
+//    thread exponentiates against its own max, warps and the CTA fold the
+//    pairs) and, if the slice holds the draft token, its logit.  Every logit
+//    is read from HBM exactly once here, with one exp per logit.  Rows are
+//    streamed from the last draft position down to position 0, and positions
+//    0 and 1 are loaded without the evict-first hint, so the rows where walks
+//    most often stop are still in L2 for the second kernel.
+//
+//  chain_resolve_kernel -- one thread-block cluster per batch row, launched as
+//    a programmatic dependent of the first kernel.  Every CTA folds the row's
+//    partials into the global max and sum of each position, forms the
+//    acceptance ratios in log2 space and finds the first rejection.  The
+//    cluster then re-reads only the stopping position (the residual needs the
+//    global normalisers, so it cannot be formed during the stream): each CTA
+//    sums the residual mass of its vocabulary slice, one cluster barrier
+//    exchanges the masses through distributed shared memory, and the CTA,
+//    warp, round, lane and element whose cumulative interval holds u * mass
+//    are chosen in vocabulary order.
 #include <cuda_bf16.h>
 
 #include <atomic>
@@ -33,36 +40,19 @@
 namespace sv {
 namespace {
 
-constexpr int NT = kThreads;
-constexpr int NW = NT / 32;
-constexpr int kMaxNV = 8;
-constexpr int kMaxStages = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kInf = __builtin_huge_valf();
-
-struct alignas(16) Ctrl {
-  uint64_t full[kMaxStages];  // stage "data landed" barriers
-  uint64_t never;             // a barrier nothing completes (forced-timeout test)
-  uint64_t pad0;
-  float4 mailbox[2];          // this CTA's slot of the cluster exchange (double buffered)
-  float4 part[NW];            // block-reduction partials
-  float wtot[kMaxNV][NW];     // inverse-CDF search: per-round warp totals
-  float sel_t;                // search: remainder handed to the chosen warp
-  int sel[3];                 // search: chosen round, warp, element
-};
-static_assert(sizeof(Ctrl) <= 2048, "control block must fit its reservation");
+constexpr int kMaxStages = 4;
 
 template <bool BF16>
 struct Fmt {
   static constexpr int EPV = BF16 ? 8 : 4;  // elements per 16-byte vector
   static constexpr int ESZ = BF16 ? 2 : 4;
   static constexpr uint32_t NEG_INF_WORD = BF16 ? 0xFF80FF80u : 0xFF800000u;
-  // element e of a 16-byte vector held as 4 words
   static __device__ __forceinline__ float elem(const uint32_t *w, int e) {
     if constexpr (BF16) return (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]);
     else return __uint_as_float(w[e]);
   }
-  // set elements [valid, EPV) to -inf
   static __device__ __forceinline__ void mask_tail(uint32_t *w, int valid) {
 #pragma unroll
     for (int e = 0; e < EPV; ++e) {
@@ -76,23 +66,22 @@ struct Fmt {
       }
     }
   }
-  static __device__ __forceinline__ float load_logit(const void *base, size_t idx) {
-    if constexpr (BF16)
-      return __uint_as_float(static_cast<uint32_t>(__ldg(static_cast<const unsigned short *>(base) + idx)) << 16);
-    else return __ldg(static_cast<const float *>(base) + idx);
-  }
-  // One vector of the slice: from the shared-memory stage (bulk-copy path) or
-  // straight from global memory (unaligned rows).  Elements >= len are -inf.
-  static __device__ __forceinline__ void load_vec(uint32_t *w, bool tma, const unsigned char *sbuf,
-                                                  const char *gsrc, int v, int len) {
+  // Vector v of a slice of `len` elements starting at gsrc: from a shared-
+  // memory copy (sbuf != nullptr), else from global memory (16-byte loads when
+  // `aligned`, element loads otherwise).  Elements >= len read as -inf.
+  static __device__ __forceinline__ void load_vec(uint32_t *w, const unsigned char *sbuf,
+                                                  const char *gsrc, bool aligned, int v, int len) {
     const int valid = len - v * EPV;
     if (valid <= 0) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) w[i] = NEG_INF_WORD;
       return;
     }
-    if (tma) {
-      uint4 r = ld_shared_u4(sbuf + (size_t)v * 16);
+    if (sbuf) {
+      const uint4 r = ld_shared_u4(sbuf + (size_t)v * 16);
+      w[0] = r.x; w[1] = r.y; w[2] = r.z; w[3] = r.w;
+    } else if (aligned) {
+      const uint4 r = __ldg(reinterpret_cast<const uint4 *>(gsrc) + v);
       w[0] = r.x; w[1] = r.y; w[2] = r.z; w[3] = r.w;
     } else {
 #pragma unroll
@@ -100,8 +89,8 @@ struct Fmt {
         if constexpr (BF16) {
           const int e0 = v * 8 + 2 * i;
           const unsigned short *g = reinterpret_cast<const unsigned short *>(gsrc);
-          uint32_t lo = e0 < len ? __ldg(g + e0) : 0xFF80u;
-          uint32_t hi = e0 + 1 < len ? __ldg(g + e0 + 1) : 0xFF80u;
+          const uint32_t lo = e0 < len ? __ldg(g + e0) : 0xFF80u;
+          const uint32_t hi = e0 + 1 < len ? __ldg(g + e0 + 1) : 0xFF80u;
           w[i] = lo | (hi << 16);
         } else {
           const int e = v * 4 + i;
@@ -113,604 +102,915 @@ struct Fmt {
   }
 };
 
-// Block reduction of two floats; result valid in thread 0.  `op` combines.
-template <class Op>
-__device__ __forceinline__ float2 block_reduce2(float a, float b, float ident, Op op, Ctrl &ctl,
-                                                int lane, int warp) {
+// Fold (max, sum relative to that max) pairs across the lanes of a warp in a
+// fixed butterfly order; every lane gets the result.  -inf maxima carry no mass.
+__device__ __forceinline__ void fold_max_sum(float m, float s, float s2, float *Mout, float *Sout) {
+  float M = m;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    a = op(a, __shfl_xor_sync(FULL_MASK, a, o));
-    b = op(b, __shfl_xor_sync(FULL_MASK, b, o));
-  }
-  if (lane == 0) ctl.part[warp] = make_float4(a, b, 0.f, 0.f);
-  __syncthreads();
-  float2 r = make_float2(ident, ident);
-  if (warp == 0) {
-    if (lane < NW) {
-      float4 v = ctl.part[lane];
-      r = make_float2(v.x, v.y);
-    }
+  for (int o = 16; o > 0; o >>= 1) M = fmax_nan(M, __shfl_xor_sync(FULL_MASK, M, o));
+  float v = (m == -kInf || s == 0.f) ? 0.f : s * ex2(__fmul_rn(m - M, s2));
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      r.x = op(r.x, __shfl_xor_sync(FULL_MASK, r.x, o));
-      r.y = op(r.y, __shfl_xor_sync(FULL_MASK, r.y, o));
-    }
-  }
-  return r;
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL_MASK, v, o);
+  *Mout = M;
+  *Sout = v;
 }
 
-// Publish this CTA's value in mailbox[slot], then every warp fetches the C
-// values of the cluster: lane c (< C) holds CTA c's value on return.
-__device__ __forceinline__ float4 cluster_exchange(float4 mine, Ctrl &ctl, int slot, uint32_t C,
-                                                   int tid, int lane) {
-  if (tid == 0) ctl.mailbox[slot] = mine;
-  cluster_sync();
-  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (lane < (int)C) v = ld_dsmem_f4(dsmem_addr(&ctl.mailbox[slot], (uint32_t)lane));
-  return v;
-}
-
-// Choose the CTA whose cumulative interval (CTA order = vocabulary order)
-// holds u * total of the per-CTA masses held by lanes 0..C-1.  Returns the CTA
-// (or -1 without mass) and the remainder inside it (+inf: clamp to the last
-// positive entry of that CTA).
-__device__ __forceinline__ int cluster_pick(float mass_lane, uint32_t C, float u, float *t_local,
-                                            float *total) {
-  float Z = 0.f;
-  for (uint32_t c = 0; c < C; ++c) Z += __shfl_sync(FULL_MASK, mass_lane, c);
-  const float t = u * Z;
-  float acc = 0.f, tl = 0.f;
+// The first of n entries (lane c holds entry c's mass, in order) whose
+// cumulative interval holds t; past the total it clamps to the last positive
+// entry.  Returns the entry and the remainder inside it (+inf when clamped),
+// or -1 without mass.
+__device__ __forceinline__ int pick_entry(float mass_lane, int n, float t, float *t_in) {
+  float acc = 0.f, tl = kInf;
   int cs = -1, clast = -1;
-  for (uint32_t c = 0; c < C; ++c) {
+  for (int c = 0; c < n; ++c) {
     const float m = __shfl_sync(FULL_MASK, mass_lane, c);
     const float prev = acc;
     acc += m;
-    if (m > 0.f) clast = (int)c;
-    if (cs < 0 && m > 0.f && acc > t) {
-      cs = (int)c;
-      tl = t - prev;
+    if (m > 0.f) {
+      clast = c;
+      if (cs < 0 && acc > t) {
+        cs = c;
+        tl = t - prev;
+      }
     }
   }
   if (cs < 0) {
     cs = clast;
     tl = kInf;
   }
-  *t_local = tl;
-  *total = Z;
+  *t_in = tl;
   return cs;
 }
 
-// Inverse CDF inside one CTA: the slice-local index of the element whose
-// cumulative interval (vocabulary order) holds t, masses mass(i) for register
-// slot i = k*EPV + e (element (tid + k*NT)*EPV + e of the slice).  t = +inf
-// or a t past the total picks the last element with positive mass.  Every
-// level (round, warp, lane, element) uses intervals built from the same sums
-// it compares against, so the choice always lands on positive mass.
-template <int NV, int EPV, class F>
-__device__ __forceinline__ int cta_inverse_cdf(float t, F mass, Ctrl &ctl, int tid, int lane,
-                                               int warp) {
-  float rs[NV], incl[NV];
-#pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    float r = 0.f;
-#pragma unroll
-    for (int e = 0; e < EPV; ++e) r += mass(k * EPV + e);
-    rs[k] = r;
-    incl[k] = warp_inclusive_scan(r, lane);
-    if (lane == 31) ctl.wtot[k][warp] = incl[k];
+__device__ __forceinline__ float sum_lanes(float v, int n) {
+  float s = 0.f;
+  for (int c = 0; c < n; ++c) s += __shfl_sync(FULL_MASK, v, c);
+  return s;
+}
+
+// ============================================================ kernel 1
+
+// Per-tile facts every consumer needs, computed by the producer warp and
+// kept next to the tile's stage.  A tile is the same vocabulary range of a
+// position's target row and (for j < K) its draft row, streamed together so
+// that both laws see the same arithmetic.
+struct alignas(16) TileInfo {
+  long long tsrc;  // byte offset of the target tile
+  long long dsrc;  // byte offset of the draft tile (pair tiles only)
+  int trow;        // partial row of the target row
+  int drow;        // partial row of the draft row, -1 for the bonus position
+  int run0;        // tile index (within the row) where this run of tiles starts
+  int t;           // tile index within the row
+  int len;         // elements in the tile
+  int yl;          // tile index of the draft token, -1 if not here
+  float s2;        // log2(e) / T
+  int keep;        // 1: load without the evict-first hint
+  int first;       // 1: first tile of a run
+  int last;        // 1: last tile of a run
+};
+
+struct alignas(16) SoftCtrl {
+  uint64_t full[kMaxStages];   // stage s holds its tile (producer -> consumers)
+  uint64_t empty[kMaxStages];  // every consumer warp has copied stage s (consumers -> producer)
+  uint64_t never;              // a barrier nothing completes (forced-timeout test)
+  int broken;                  // a wait gave up: stop the pipeline
+  int pad0;
+  TileInfo info[kMaxStages];   // facts of the tile in stage s
+  float4 wpart[2 * kMaxStages][kSoftThreads / 32];  // per-warp (max p, sum p, max q, sum q), by run
+  uint32_t tflags[2 * kMaxStages];                  // timeout seen, by run
+  int arrived[2 * kMaxStages];                      // warps done, by run
+};
+static_assert(sizeof(SoftCtrl) <= 2048, "control block must fit its reservation");
+
+// Positions in stream order: the bonus positions (j = K), then j = K-1 down
+// to 0, each over b = 0..B-1.
+__device__ __forceinline__ void stream_pos(int i, int B, int K, int *b, int *j) {
+  *j = K - i / B;
+  *b = i - (K - *j) * B;
+}
+
+// A phase is a range of positions [p0, p1) of the stream; its tiles cost 1
+// (bonus position: target only) or 2 (target and draft).  Returns the first
+// tile (phase-relative) of CTA g's even share of the phase's cost.
+__device__ __forceinline__ int phase_split(int p0, int p1, int B, int K, int nt, int g, int G) {
+  const int nb = max(0, min(p1, B) - p0) * nt;     // bonus tiles (they come first)
+  const int np = (p1 - p0) * nt - nb;              // pair tiles
+  const long long cost = (long long)nb + 2LL * np;
+  const long long c = cost * g / G;
+  return c <= nb ? (int)c : nb + (int)((c - nb + 1) / 2);
+}
+
+template <bool BF16>
+__device__ __forceinline__ TileInfo make_tile(const ChainStochParams &P, int gt, int lo, int hi) {
+  TileInfo it;
+  const int B = P.B, K = P.K, nt = P.nslices;
+  const int i = gt / nt;
+  it.t = gt - i * nt;
+  int b, j;
+  stream_pos(i, B, K, &b, &j);
+  const int s0 = it.t * P.slice;
+  it.len = min(P.V - s0, P.slice);
+  it.trow = b * (K + 1) + j;
+  it.tsrc = ((long long)it.trow * P.V + s0) * Fmt<BF16>::ESZ;
+  if (j < K) {
+    it.drow = B * (K + 1) + b * K + j;
+    it.dsrc = ((long long)(b * K + j) * P.V + s0) * Fmt<BF16>::ESZ;
+  } else {
+    it.drow = -1;
+    it.dsrc = 0;
   }
-  __syncthreads();
-  if (tid == 0) {
-    float acc = 0.f, t2 = 0.f;
-    int ks = -1, ws = -1;
-    for (int k = 0; k < NV && ks < 0; ++k)
-      for (int w = 0; w < NW; ++w) {
-        const float m = ctl.wtot[k][w];
-        const float prev = acc;
-        acc += m;
-        if (m > 0.f && acc > t) {
-          ks = k;
-          ws = w;
-          t2 = t - prev;
-          break;
-        }
-      }
-    if (ks < 0) {
-      for (int k = NV - 1; k >= 0 && ks < 0; --k)
-        for (int w = NW - 1; w >= 0; --w)
-          if (ctl.wtot[k][w] > 0.f) {
-            ks = k;
-            ws = w;
-            t2 = kInf;
-            break;
-          }
-    }
-    ctl.sel[0] = ks;
-    ctl.sel[1] = ws;
-    ctl.sel[2] = -1;
-    ctl.sel_t = t2;
+  it.keep = j <= 1;
+  // a run is the part of a row inside [lo, hi): it starts at the later of lo
+  // and the row's first tile
+  it.first = (gt == lo) || it.t == 0;
+  it.last = (gt == hi - 1) || it.t == nt - 1;
+  it.run0 = max(lo - (gt - it.t), 0);
+  float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
+  if (!(T > 0.f && T < kInf)) T = 1.0f;  // the resolve kernel flags the row
+  it.s2 = __fdiv_rn(kLog2e, T);
+  it.yl = -1;
+  if (j < K) {
+    const int y = __ldg(P.tokens + (size_t)b * K + j);
+    if (y >= s0 && y < s0 + it.len) it.yl = y - s0;
   }
-  __syncthreads();
-  const int ks = ctl.sel[0], ws = ctl.sel[1];
-  const float t2 = ctl.sel_t;
-  if (ks >= 0 && warp == ws) {
-    float my_incl = 0.f, my_r = 0.f;
-#pragma unroll
-    for (int k = 0; k < NV; ++k)
-      if (k == ks) {
-        my_incl = incl[k];
-        my_r = rs[k];
-      }
-    float excl = __shfl_up_sync(FULL_MASK, my_incl, 1);
-    if (lane == 0) excl = 0.f;
-    const unsigned hit = __ballot_sync(FULL_MASK, my_r > 0.f && my_incl > t2);
-    int ls;
-    bool clamp = false;
-    if (hit) {
-      ls = __ffs(hit) - 1;
-    } else {
-      const unsigned pos = __ballot_sync(FULL_MASK, my_r > 0.f);
-      ls = 31 - __clz(pos);
-      clamp = true;
-    }
-    if (lane == ls) {
-      const float t3 = clamp ? kInf : t2 - excl;
-      float c = 0.f;
-      int es = -1, elast = -1;
+  return it;
+}
+
+// The n-th tile of the CTA, rebuilt by a consumer after a wait gave up.
+template <bool BF16>
+__device__ __noinline__ TileInfo rebuild_tile(const ChainStochParams &P, int n, int na, int lo_a,
+                                              int hi_a, int lo_b, int hi_b) {
+  return n < na ? make_tile<BF16>(P, lo_a + n, lo_a, hi_a)
+                : make_tile<BF16>(P, lo_b + (n - na), lo_b, hi_b);
+}
+
+template <bool BF16, int NV>
+__device__ __forceinline__ void load_tile(uint32_t (&w)[NV * 4], bool tma, uint32_t sbase,
+                                          const char *gsrc, int tid, int nvec, int len) {
+  using F = Fmt<BF16>;
+  if (tma) {  // whole 16-byte vectors: tiles are multiples of 8 bf16 / 4 fp32 here
+    const uint32_t a = sbase + tid * 16;
+    if (nvec == NV * kSoftThreads) {
 #pragma unroll
       for (int k = 0; k < NV; ++k)
-        if (k == ks) {
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[4 * k]), "=r"(w[4 * k + 1]), "=r"(w[4 * k + 2]), "=r"(w[4 * k + 3])
+                     : "r"(a + k * kSoftThreads * 16));
+    } else {
+#pragma unroll
+      for (int k = 0; k < NV; ++k) {
+        if (tid + k * kSoftThreads < nvec) {
+          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(w[4 * k]), "=r"(w[4 * k + 1]), "=r"(w[4 * k + 2]), "=r"(w[4 * k + 3])
+                       : "r"(a + k * kSoftThreads * 16));
+        } else {
+          w[4 * k] = w[4 * k + 1] = w[4 * k + 2] = w[4 * k + 3] = F::NEG_INF_WORD;
+        }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < NV; ++k) F::load_vec(w + 4 * k, nullptr, gsrc, false, tid + k * kSoftThreads, len);
+  }
+}
+
+template <bool BF16, int NV>
+__device__ __forceinline__ float tile_max(const uint32_t (&w)[NV * 4]) {
+  using F = Fmt<BF16>;
+  if constexpr (BF16) {
+    uint32_t pm0 = F::NEG_INF_WORD, pm1 = F::NEG_INF_WORD;
+#pragma unroll
+    for (int i = 0; i < NV * 4; i += 2) {
+      pm0 = bf16x2_max_nan(pm0, w[i]);
+      pm1 = bf16x2_max_nan(pm1, w[i + 1]);
+    }
+    pm0 = bf16x2_max_nan(pm0, pm1);
+    return fmax_nan(bf16_lo(pm0), bf16_hi(pm0));
+  } else {
+    float m0 = -kInf, m1 = -kInf;
+#pragma unroll
+    for (int i = 0; i < NV * 4; i += 2) {
+      m0 = fmax_nan(m0, __uint_as_float(w[i]));
+      m1 = fmax_nan(m1, __uint_as_float(w[i + 1]));
+    }
+    return fmax_nan(m0, m1);
+  }
+}
+
+// Fold one tile into a running (max, sum of exp2((x - max) s2)).
+template <bool BF16, int NV>
+__device__ __forceinline__ void tile_accumulate(const uint32_t (&w)[NV * 4], float s2, int tid,
+                                                int nvec, float &m_run, float &s_run) {
+  using F = Fmt<BF16>;
+  const float m = tile_max<BF16, NV>(w);
+  const float m_new = fmax_nan(m_run, m);
+  if (m_run != -kInf && m_new != m_run) s_run *= ex2(__fmul_rn(m_run - m_new, s2));
+  m_run = m_new;
+  const float off = (m_run == -kInf) ? 0.f : -__fmul_rn(m_run, s2);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};  // independent chains for the adds
+  if (nvec == NV * kSoftThreads) {  // full tile: no bounds
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+#pragma unroll
+      for (int e = 0; e < F::EPV; ++e) acc[e & 3] += ex2(__fmaf_rn(F::elem(w + 4 * k, e), s2, off));
+  } else {
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      if (tid + k * kSoftThreads < nvec) {
+#pragma unroll
+        for (int e = 0; e < F::EPV; ++e) acc[e & 3] += ex2(__fmaf_rn(F::elem(w + 4 * k, e), s2, off));
+      }
+    }
+  }
+  s_run += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
+// Warp-specialised stream.  Each CTA owns one contiguous share (even in cost)
+// of the tiles of phase A (positions >= 2) and one of phase B (positions 0
+// and 1, streamed last so they stay in L2 for the resolve kernel).  Warp NW
+// (the producer) walks them in order, writes each tile's facts next to its
+// stage and issues the bulk copies; warps 0..NW-1 (the consumers) take the
+// tile into registers, release the stage, and fold it into a running (max,
+// sum) per thread and per law: a run of tiles of one position costs one
+// rescale per tile and a single CTA-wide fold at its end.  Producer and
+// consumers meet only on the full/empty barriers of each stage.
+template <bool BF16, int NV, int S>
+__global__ void __launch_bounds__(kSoftThreads + 32, 3) softmax_partials_kernel(const __grid_constant__ ChainStochParams P) {
+  using F = Fmt<BF16>;
+  constexpr int NT = kSoftThreads, NW = NT / 32;
+  constexpr int EPV = F::EPV, ESZ = F::ESZ;
+  // let the resolve kernel be scheduled; it waits for this grid on the device
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  SoftCtrl &ctl = *reinterpret_cast<SoftCtrl *>(smem + (size_t)S * P.buf_bytes);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nt = P.nslices, B = P.B, K = P.K;
+  const int npos = B * (K + 1);
+  const int pa = K >= 2 ? B * (K - 1) : 0;  // positions with j >= 2 come first
+  const int G = (int)gridDim.x, g = (int)blockIdx.x;
+  const int lo_a = phase_split(0, pa, B, K, nt, g, G);
+  const int hi_a = phase_split(0, pa, B, K, nt, g + 1, G);
+  const int lo_b = pa * nt + phase_split(pa, npos, B, K, nt, g, G);
+  const int hi_b = pa * nt + phase_split(pa, npos, B, K, nt, g + 1, G);
+  const int na = hi_a - lo_a;
+  const int my_tiles = na + (hi_b - lo_b);
+  auto tile_of = [&](int n, int *lo, int *hi) {  // n-th tile of this CTA
+    if (n < na) {
+      *lo = lo_a;
+      *hi = hi_a;
+      return lo_a + n;
+    }
+    *lo = lo_b;
+    *hi = hi_b;
+    return lo_b + (n - na);
+  };
+  const bool tma = P.use_tma != 0;
+  const int half = P.buf_bytes / 2;  // target half, then draft half of a stage
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&ctl.full[s], 1);
+      mbar_init(&ctl.empty[s], NW);
+    }
+    mbar_init(&ctl.never, 1);
+    ctl.broken = 0;
+    for (int i = 0; i < 2 * kMaxStages; ++i) {
+      ctl.arrived[i] = 0;
+      ctl.tflags[i] = 0;
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == NW) {  // ---------------------------------------------- producer
+    if (lane != 0) return;
+    const uint64_t pol_first = l2_policy_evict_first();
+    const uint64_t pol_normal = l2_policy_evict_normal();
+    int issued = 0;
+    for (int n = 0; n < my_tiles; ++n) {
+      const int s = n % S;
+      if (n >= S &&
+          !mbar_wait_bounded(&ctl.empty[s], static_cast<uint32_t>(n / S - 1) & 1u, P.wait_limit_ns))
+        ctl.broken = 1;
+      if (*reinterpret_cast<volatile int *>(&ctl.broken)) break;
+      int lo, hi;
+      const int gt = tile_of(n, &lo, &hi);
+      const TileInfo it = make_tile<BF16>(P, gt, lo, hi);
+      ctl.info[s] = it;
+      if (tma) {
+        const uint32_t bytes = static_cast<uint32_t>(it.len) * ESZ;
+        const uint64_t pol = it.keep ? pol_normal : pol_first;
+        mbar_arrive_expect_tx(&ctl.full[s], it.drow >= 0 ? 2 * bytes : bytes);  // release: info[s] too
+        bulk_g2s(smem + (size_t)s * P.buf_bytes, static_cast<const char *>(P.target) + it.tsrc,
+                 bytes, &ctl.full[s], pol);
+        if (it.drow >= 0)
+          bulk_g2s(smem + (size_t)s * P.buf_bytes + half,
+                   static_cast<const char *>(P.draft) + it.dsrc, bytes, &ctl.full[s], pol);
+      } else {
+        mbar_arrive(&ctl.full[s]);
+      }
+      ++issued;
+    }
+    // copies still landing after a give-up: wait (bounded) for the last phase
+    // of every stage before leaving
+    for (int s = 0; s < S && s < issued; ++s) {
+      const int last = s + ((issued - 1 - s) / S) * S;
+      mbar_wait_bounded(&ctl.full[s], static_cast<uint32_t>(last / S) & 1u, P.wait_limit_ns);
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- consumers
+  float mp = -kInf, sp = 0.f, mq = -kInf, sq = 0.f;  // running (max, sum) of p and q
+  uint32_t run_to = 0;  // a timeout met in the current run (warp-uniform)
+  int runs = 0;         // runs finished so far
+  int s = 0;
+  uint32_t parity = 0;
+  const uint32_t smem0 = smem_u32(smem);
+  for (int n = 0; n < my_tiles; ++n, s = (s + 1 == S) ? 0 : s + 1, parity ^= (s == 0)) {
+    bool timed_out = false;
+    if (!*reinterpret_cast<volatile int *>(&ctl.broken)) {
+      timed_out = P.force_timeout ? !mbar_wait_bounded(&ctl.never, 0u, P.wait_limit_ns)
+                                  : !mbar_wait_bounded(&ctl.full[s], parity, P.wait_limit_ns);
+    } else {
+      timed_out = true;  // the pipeline stopped: this tile's data never came
+    }
+    // The facts next to the stage are only valid once its barrier completed;
+    // after a give-up the consumer rebuilds them (the stage data is then
+    // garbage but every index stays in bounds, and the row is flagged).
+    TileInfo it;
+    if (timed_out) {
+      it = rebuild_tile<BF16>(P, n, na, lo_a, hi_a, lo_b, hi_b);
+    } else {
+      it = ctl.info[s];
+    }
+    const bool pair = it.drow >= 0;
+    const unsigned char *sb = smem + (size_t)s * P.buf_bytes;
+    const int nvec = (it.len + EPV - 1) / EPV;
+
+    const uint32_t sbase = smem0 + s * P.buf_bytes;
+    uint32_t wp[NV * 4];
+    load_tile<BF16, NV>(wp, tma, sbase, static_cast<const char *>(P.target) + it.tsrc, tid, nvec, it.len);
+    if (it.yl >= 0 && tid == 0) {  // the draft token's logits, if this tile holds them
+      float a, c;
+      if (tma) {
+        const unsigned char *pv = sb + (size_t)it.yl * ESZ;
+        if constexpr (BF16) {
+          a = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short *>(pv)) << 16);
+          c = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short *>(pv + half)) << 16);
+        } else {
+          a = *reinterpret_cast<const float *>(pv);
+          c = *reinterpret_cast<const float *>(pv + half);
+        }
+      } else {
+        const char *tg = static_cast<const char *>(P.target) + it.tsrc;
+        const char *dg = static_cast<const char *>(P.draft) + it.dsrc;
+        if constexpr (BF16) {
+          a = __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short *>(tg) + it.yl)) << 16);
+          c = __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short *>(dg) + it.yl)) << 16);
+        } else {
+          a = __ldg(reinterpret_cast<const float *>(tg) + it.yl);
+          c = __ldg(reinterpret_cast<const float *>(dg) + it.yl);
+        }
+      }
+      P.ylog[it.trow] = a;
+      P.ylog[it.drow] = c;
+    }
+    const float s2 = it.s2;
+    if (it.first) {
+      mp = mq = -kInf;
+      sp = sq = 0.f;
+    }
+    tile_accumulate<BF16, NV>(wp, s2, tid, nvec, mp, sp);
+    if (pair) {
+      load_tile<BF16, NV>(wp, tma, sbase + half, static_cast<const char *>(P.draft) + it.dsrc, tid, nvec,
+                          it.len);
+    }
+    // this warp is done with the stage
+    const bool warp_to = __any_sync(FULL_MASK, timed_out);
+    __syncwarp();
+    if (lane == 0) {
+      if (warp_to) ctl.broken = 1;
+      mbar_arrive(&ctl.empty[s]);
+    }
+    if (warp_to) run_to = F_TIMEOUT;
+    if (pair) tile_accumulate<BF16, NV>(wp, s2, tid, nvec, mq, sq);
+
+    if (it.last) {  // the run ends: fold the CTA's partials
+      const int slot = runs % (2 * S);
+      ++runs;
+      float Mpw, Spw, Mqw, Sqw;
+      fold_max_sum(mp, sp, s2, &Mpw, &Spw);
+      fold_max_sum(mq, sq, s2, &Mqw, &Sqw);
+      int last = 0;
+      if (lane == 0) {
+        ctl.wpart[slot][warp] = make_float4(Mpw, Spw, Mqw, Sqw);
+        if (run_to) atomicOr(&ctl.tflags[slot], run_to);
+        __threadfence_block();
+        last = atomicAdd(&ctl.arrived[slot], 1) == NW - 1;
+      }
+      run_to = 0;
+      if (__shfl_sync(FULL_MASK, last, 0)) {
+        __threadfence_block();
+        const float4 v = lane < NW ? ctl.wpart[slot][lane] : make_float4(-kInf, 0.f, -kInf, 0.f);
+        float M1, S1, M2, S2;
+        fold_max_sum(v.x, v.y, s2, &M1, &S1);
+        fold_max_sum(v.z, v.w, s2, &M2, &S2);
+        const uint32_t tf = ctl.tflags[slot];
+        SoftPart *rp = P.part + (size_t)it.trow * nt;
+        SoftPart *rq = pair ? P.part + (size_t)it.drow * nt : nullptr;
+        for (int t = it.run0 + 1 + lane; t <= it.t; t += 32) {
+          rp[t] = SoftPart{-kInf, 0.f, 0.f, 0u};
+          if (pair) rq[t] = SoftPart{-kInf, 0.f, 0.f, 0u};
+        }
+        if (lane == 0) {
+          rp[it.run0] = SoftPart{M1, S1, 0.f, tf};
+          if (pair) rq[it.run0] = SoftPart{M2, S2, 0.f, tf};
+          ctl.arrived[slot] = 0;
+          ctl.tflags[slot] = 0;
+        }
+      }
+    }
+  }
+}
+
+// ============================================================ kernel 2
+
+struct alignas(16) ResolveCtrl {
+  float4 mailbox[2];         // this CTA's mass for the cluster exchange
+  float wsum[kResolveThreads / 32];
+  float Mp, Sp, Mq, Sq;      // normalisers of the stopping position
+  float u;                   // its u_sample
+  int stop;                  // first rejecting position (K: none)
+  uint32_t flags;            // row status bits
+  int pad;
+};
+
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Fold the tile partials of every logit row of row b (target rows 0..K, then
+// draft rows 0..K-1) in one round trip: lanes form groups of GS (a power of
+// two >= the tile count, at most 32), one group per logit row; lane l of a
+// group folds tiles l, l+GS, ... in order, then the group folds in a fixed
+// butterfly order.  rstat[r] = (max, sum, draft-token logit, flags).
+__device__ void fold_rows(const ChainStochParams &P, int b, float s2, int warp, int lane,
+                          float4 *rstat) {
+  constexpr int NW = kResolveThreads / 32;
+  const int K = P.K, npos = K + 1, nt = P.nslices;
+  int GS = 1;
+  while (GS < nt && GS < 32) GS <<= 1;
+  const int per_warp = 32 / GS;
+  const int sub = lane % GS;
+  for (int r0 = warp * per_warp; r0 < npos + K; r0 += NW * per_warp) {
+    const int r = r0 + lane / GS;
+    float m = -kInf, sacc = 0.f, yv = 0.f;
+    uint32_t f = 0;
+    if (r < npos + K) {
+      const bool draft = r > K;
+      const int j = draft ? r - npos : r;
+      const int prow = draft ? P.B * npos + b * K + j : b * npos + j;
+      if (sub == 0 && j < K) yv = P.ylog[prow];
+      for (int t = sub; t < nt; t += GS) {
+        const SoftPart q = P.part[(size_t)prow * nt + t];
+        f |= q.flags;
+        const float mn = fmax_nan(m, q.m);
+        sacc = (m == -kInf ? 0.f : sacc * ex2(__fmul_rn(m - mn, s2))) +
+               (q.m == -kInf ? 0.f : q.s * ex2(__fmul_rn(q.m - mn, s2)));
+        m = mn;
+      }
+    }
+    // butterfly inside the group
+    float M = m;
+    for (int o = GS >> 1; o > 0; o >>= 1) M = fmax_nan(M, __shfl_xor_sync(FULL_MASK, M, o));
+    float v = (m == -kInf || sacc == 0.f) ? 0.f : sacc * ex2(__fmul_rn(m - M, s2));
+    for (int o = GS >> 1; o > 0; o >>= 1) {
+      v += __shfl_xor_sync(FULL_MASK, v, o);
+      f |= __shfl_xor_sync(FULL_MASK, f, o);
+    }
+    if (sub == 0 && r < npos + K) rstat[r] = make_float4(M, v, yv, __uint_as_float(f));
+  }
+}
+
+// One row's decisions from the folded statistics: validates the row's inputs,
+// forms each ratio in log2 space, finds the first rejection.  One warp; in
+// CTA 0 it also writes the diagnostics.
+// The scalars lane j of warp 0 needs for position j (first chunk of 32),
+// loaded before the dependency wait: they are inputs, never written by the
+// stream kernel.
+struct RowScalars {
+  float us, ua;
+  int y;
+};
+
+__device__ __forceinline__ RowScalars load_scalars(const ChainStochParams &P, int b, int j) {
+  RowScalars r = {0.f, 0.f, -1};
+  const int K = P.K;
+  if (j <= K) r.us = __ldg(P.u_sample + (size_t)b * (K + 1) + j);
+  if (j < K) {
+    r.y = __ldg(P.tokens + (size_t)b * K + j);
+    r.ua = __ldg(P.u_accept + (size_t)b * K + j);
+  }
+  return r;
+}
+
+__device__ void decide_row(const ChainStochParams &P, int b, float s2, uint32_t tflags, int lane,
+                           bool diag, const float4 *rstat, RowScalars first, ResolveCtrl &ctl) {
+  const int K = P.K, npos = K + 1, V = P.V;
+  uint32_t flags = tflags;
+  int stop = K;
+  for (int j0 = 0; j0 < npos; j0 += 32) {
+    const int j = j0 + lane;
+    bool rejects = false;
+    float4 tp = make_float4(-kInf, 0.f, 0.f, 0.f), dq = make_float4(-kInf, 0.f, 0.f, 0.f);
+    float us = 0.f;
+    if (j < npos) {
+      const RowScalars sc = j0 == 0 ? first : load_scalars(P, b, j);
+      us = sc.us;
+      if (!(us >= 0.f && us < 1.f)) flags |= F_BAD_UNIFORM;
+      tp = rstat[j];
+      flags |= __float_as_uint(tp.w);
+      if (tp.x != tp.x || tp.x == kInf) flags |= F_NONFINITE;
+      else if (tp.x == -kInf) flags |= F_EMPTY;
+      if (j < K) {
+        const int y = sc.y;
+        const float ua = sc.ua;
+        if (!(ua >= 0.f && ua < 1.f)) flags |= F_BAD_UNIFORM;
+        if (y < 0 || y >= V) flags |= F_BAD_TOKEN;
+        dq = rstat[npos + j];
+        flags |= __float_as_uint(dq.w);
+        if (dq.x != dq.x || dq.x == kInf) flags |= F_NONFINITE;
+        else if (dq.x == -kInf) flags |= F_EMPTY;
+        // ratio p(y)/q(y) in log2 space: identical logits give exactly 0
+        const float l2p = __fadd_rn(__fmaf_rn(tp.z, s2, -__fmul_rn(tp.x, s2)), -lg2(tp.y));
+        const float l2q = __fadd_rn(__fmaf_rn(dq.z, s2, -__fmul_rn(dq.x, s2)), -lg2(dq.y));
+        const float l2r = __fadd_rn(l2p, -l2q);
+        rejects = !((l2r >= 0.f) || (ua < ex2(l2r)));
+        if (diag) {
+          const size_t d = (size_t)b * K + j;
+          if (P.p_at_draft) P.p_at_draft[d] = ex2(l2p);
+          if (P.q_at_draft) P.q_at_draft[d] = ex2(l2q);
+        }
+      }
+    }
+    const unsigned rej = __ballot_sync(FULL_MASK, rejects);
+    const bool found_here = stop == K && rej;
+    const int src = found_here ? __ffs(rej) - 1 : K - j0;  // stop lane, or the bonus lane
+    if ((found_here || (stop == K && j0 + 32 >= npos)) && lane == src) {
+      ctl.Mp = tp.x;
+      ctl.Sp = tp.y;
+      ctl.Mq = found_here ? dq.x : -kInf;
+      ctl.Sq = found_here ? dq.y : 0.f;
+      ctl.u = us;
+    }
+    if (found_here) stop = j0 + src;
+  }
+  flags = __reduce_or_sync(FULL_MASK, flags);
+  if (diag && P.resid_mass)
+    for (int j = lane; j < K; j += 32)
+      if (j != stop) P.resid_mass[(size_t)b * K + j] = 0.f;
+  if (lane == 0) {
+    ctl.stop = stop;
+    ctl.flags = flags;
+  }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kResolveThreads, 4) chain_resolve_kernel(const __grid_constant__ ChainStochParams P) {
+  using F = Fmt<BF16>;
+  constexpr int NT = kResolveThreads, NW = NT / 32, EPV = F::EPV, ESZ = F::ESZ;
+  __shared__ ResolveCtrl ctl;
+  extern __shared__ __align__(16) unsigned char rsm[];
+  float4 *rstat = reinterpret_cast<float4 *>(rsm);                         // [2K+1]
+  float *rsum = reinterpret_cast<float *>(rsm + (size_t)(2 * P.K + 1) * 16);  // [rounds][NT]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int crank = (int)cluster_ctarank(), C = (int)cluster_nctarank();
+  const int b = (int)cluster_id_x();
+  const int K = P.K, npos = K + 1, V = P.V;
+  const float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
+  const uint32_t tflags = (T > 0.f && T < kInf) ? 0u : F_BAD_TEMPERATURE;
+  const float s2 = tflags ? 1.f : __fdiv_rn(kLog2e, T);
+
+  // The logits are inputs the stream kernel never writes, so the rows where
+  // walks most often stop (position 0) can be pulled into L2 before waiting.
+  if (tid == 0 && P.use_tma) {
+    const int s0p = crank * P.L;
+    const int lenp = max(0, min(V, s0p + P.L) - s0p);
+    if (lenp > 0) {
+      bulk_prefetch_l2(static_cast<const char *>(P.target) + ((size_t)(b * npos) * V + s0p) * ESZ,
+                       static_cast<uint32_t>(lenp) * ESZ);
+      if (K > 0)
+        bulk_prefetch_l2(static_cast<const char *>(P.draft) + ((size_t)(b * K) * V + s0p) * ESZ,
+                         static_cast<uint32_t>(lenp) * ESZ);
+    }
+  }
+  const RowScalars first = load_scalars(P, b, lane);
+  // the stream kernel's partials are visible after this line; nothing above
+  // reads them
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  fold_rows(P, b, s2, warp, lane, rstat);
+  __syncthreads();
+  if (warp == 0) decide_row(P, b, s2, tflags, lane, crank == 0, rstat, first, ctl);
+  __syncthreads();
+  const uint32_t flags = ctl.flags;
+  const int stop = ctl.stop;
+  if (flags) {  // identical in every CTA of the cluster: all leave together
+    if (crank == 0 && warp == 0) {
+      for (int j = lane; j < npos; j += 32) P.out_tokens[(size_t)b * npos + j] = -1;
+      if (lane == 0) {
+        P.accepted_len[b] = -1;
+        P.num_emitted[b] = 0;
+        P.row_status[b] = lowest_code(flags);
+      }
+    }
+    return;
+  }
+
+  const float nMp = -__fmul_rn(ctl.Mp, s2), nMq = -__fmul_rn(ctl.Mq, s2);
+  const float iSp = __frcp_rn(ctl.Sp), iSq = ctl.Sq > 0.f ? __frcp_rn(ctl.Sq) : 0.f;
+  const float u = ctl.u;
+  const int s0 = crank * P.L;
+  const int len = max(0, min(V, s0 + P.L) - s0);
+  const int nr = P.vpw / 32;  // rounds of 32 vectors per warp
+  const int vbase = warp * P.vpw;
+  const bool aligned = P.use_tma != 0;
+  const char *tg = static_cast<const char *>(P.target) + ((size_t)(b * npos + stop) * V + s0) * ESZ;
+  const char *dg = stop < K
+                       ? static_cast<const char *>(P.draft) + ((size_t)(b * K + stop) * V + s0) * ESZ
+                       : nullptr;
+
+  int task = stop < K ? 1 : 2;  // 1: residual [p - q]+, 2: the target law p
+  float Z = 0.f;
+  int xs = 0;
+  int owner_cta = -1;
+  float t_c = 0.f;
+  // mass of element e of a vector pair under the current task
+  auto mass = [&](const uint32_t *wp, const uint32_t *wq, int e) {
+    const float pe = ex2(__fmaf_rn(F::elem(wp, e), s2, nMp));
+    if (task == 2) return pe;
+    const float qe = ex2(__fmaf_rn(F::elem(wq, e), s2, nMq));
+    return fmaxf(__fmaf_rn(pe, iSp, -__fmul_rn(qe, iSq)), 0.f);
+  };
+  while (true) {
+    // ---- pass: per-round masses (kept for the search), then the CTA total
+    float tsum = 0.f;
+    if (aligned && task == 1) {
+#pragma unroll 1
+      for (int k0 = 0; k0 < nr; k0 += 4) {
+        uint4 vp[4], vq[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int v = vbase + 32 * (k0 + k) + lane;
+          const bool in = (k0 + k < nr) && v * EPV < len;
+          vp[k] = in ? __ldg(reinterpret_cast<const uint4 *>(tg) + v) : make_uint4(F::NEG_INF_WORD, F::NEG_INF_WORD, F::NEG_INF_WORD, F::NEG_INF_WORD);
+          vq[k] = in ? __ldg(reinterpret_cast<const uint4 *>(dg) + v) : make_uint4(F::NEG_INF_WORD, F::NEG_INF_WORD, F::NEG_INF_WORD, F::NEG_INF_WORD);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t *wp = reinterpret_cast<const uint32_t *>(&vp[k]);
+          const uint32_t *wq = reinterpret_cast<const uint32_t *>(&vq[k]);
+          float r = 0.f;
 #pragma unroll
           for (int e = 0; e < EPV; ++e) {
-            const float m = mass(k * EPV + e);
+            const float pe = ex2(__fmaf_rn(F::elem(wp, e), s2, nMp));
+            const float qe = ex2(__fmaf_rn(F::elem(wq, e), s2, nMq));
+            r += fmaxf(__fmaf_rn(pe, iSp, -__fmul_rn(qe, iSq)), 0.f);
+          }
+          if (k0 + k < nr) rsum[(k0 + k) * NT + tid] = r;
+          tsum += r;
+        }
+      }
+    } else if (aligned) {
+#pragma unroll 1
+      for (int k0 = 0; k0 < nr; k0 += 4) {
+        uint4 vp[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int v = vbase + 32 * (k0 + k) + lane;
+          const bool in = (k0 + k < nr) && v * EPV < len;
+          vp[k] = in ? __ldg(reinterpret_cast<const uint4 *>(tg) + v) : make_uint4(F::NEG_INF_WORD, F::NEG_INF_WORD, F::NEG_INF_WORD, F::NEG_INF_WORD);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t *wp = reinterpret_cast<const uint32_t *>(&vp[k]);
+          float r = 0.f;
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) r += ex2(__fmaf_rn(F::elem(wp, e), s2, nMp));
+          if (k0 + k < nr) rsum[(k0 + k) * NT + tid] = r;
+          tsum += r;
+        }
+      }
+    } else {  // rows that are not 16-byte aligned: element loads with masking
+#pragma unroll 1
+      for (int k0 = 0; k0 < nr; k0 += 4) {
+        uint32_t wp[4][4], wq[4][4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int v = vbase + 32 * (k0 + k) + lane;
+          const int vlen = (k0 + k < nr) ? len : 0;  // rounds past nr read nothing
+          F::load_vec(wp[k], nullptr, tg, false, v, vlen);
+          if (task == 1) F::load_vec(wq[k], nullptr, dg, false, v, vlen);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float r = 0.f;
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) r += mass(wp[k], wq[k], e);
+          if (k0 + k < nr) rsum[(k0 + k) * NT + tid] = r;
+          tsum += r;
+        }
+      }
+    }
+    const float wsum = warp_sum(tsum);
+    if (lane == 0) ctl.wsum[warp] = wsum;
+    __syncthreads();
+    if (tid == 0) {
+      float c = 0.f;
+      for (int w2 = 0; w2 < NW; ++w2) c += ctl.wsum[w2];
+      ctl.mailbox[xs] = make_float4(c, 0.f, 0.f, 0.f);
+    }
+    cluster_sync();
+    const float cm = lane < C ? ld_dsmem_f4(dsmem_addr(&ctl.mailbox[xs], (uint32_t)lane)).x : 0.f;
+    xs ^= 1;
+    const float tot = sum_lanes(cm, C);
+    if (task == 1 && !(tot > 0.f)) {  // the residual vanished in fp32: draw from p
+      task = 2;
+      continue;
+    }
+    if (task == 1) Z = tot;
+    owner_cta = pick_entry(cm, C, u * tot, &t_c);
+    break;
+  }
+  cluster_arrive();  // done with the peers' mailboxes
+
+  if (crank == owner_cta) {
+    float t_w;
+    const float wm = lane < NW ? ctl.wsum[lane] : 0.f;
+    const int owner_warp = pick_entry(wm, NW, t_c, &t_w);
+    if (warp == owner_warp) {
+      // round of 32 vectors, then lane, then element, in vocabulary order
+      int ks = -1, klast = -1;
+      float t1 = 0.f, acc = 0.f;
+      for (int k = 0; k < nr; ++k) {
+        const float Wk = warp_sum(rsum[k * NT + tid]);
+        const float prev = acc;
+        acc += Wk;
+        if (Wk > 0.f) {
+          klast = k;
+          if (ks < 0 && acc > t_w) {
+            ks = k;
+            t1 = t_w - prev;
+          }
+        }
+      }
+      if (ks < 0) {
+        ks = klast;
+        t1 = kInf;
+      }
+      int token = -1;
+      if (ks >= 0) {
+        const float my = rsum[ks * NT + tid];
+        const int v = vbase + 32 * ks + lane;
+        uint32_t wp[4], wq[4];
+        F::load_vec(wp, nullptr, tg, aligned, v, len);
+        if (task == 1) F::load_vec(wq, nullptr, dg, aligned, v, len);
+        const float incl = warp_inclusive_scan(my, lane);
+        float excl = __shfl_up_sync(FULL_MASK, incl, 1);
+        if (lane == 0) excl = 0.f;
+        const unsigned hit = __ballot_sync(FULL_MASK, my > 0.f && incl > t1);
+        int ls;
+        bool clamp = false;
+        if (hit) {
+          ls = __ffs(hit) - 1;
+        } else {
+          ls = 31 - __clz(__ballot_sync(FULL_MASK, my > 0.f));
+          clamp = true;
+        }
+        int pos = -1;
+        if (lane == ls) {
+          const float t3 = clamp ? kInf : t1 - excl;
+          float c = 0.f;
+          int es = -1, elast = -1;
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) {
+            const float m = mass(wp, wq, e);
             c += m;
             if (m > 0.f) {
               elast = e;
               if (es < 0 && c > t3) es = e;
             }
           }
+          if (es < 0) es = elast;
+          pos = s0 + v * EPV + es;
         }
-      if (es < 0) es = elast;
-      ctl.sel[2] = (tid + ks * NT) * EPV + es;
-    }
-  }
-  __syncthreads();
-  return ctl.sel[2];
-}
-
-// Row walk of "Verify several proposed tokens in one target pass": first
-// rejecting position, then the emitted tokens.  One warp.
-__device__ void walk_chain_row(const ChainStochParams &P, int b, int lane) {
-  const int K = P.K, npos = K + 1;
-  const ChainRec *R = P.rec + (size_t)b * npos;
-  uint32_t flags = 0;
-  int stop = K;
-  for (int j0 = 0; j0 < npos; j0 += 32) {
-    const int j = j0 + lane;
-    int acc = 1;
-    if (j < npos) {
-      const int4 r = __ldcg(reinterpret_cast<const int4 *>(R + j));
-      flags |= static_cast<uint32_t>(r.z);
-      if (j < K) acc = r.y;
-    }
-    const unsigned rej = __ballot_sync(FULL_MASK, !acc);
-    if (stop == K && rej) stop = j0 + __ffs(rej) - 1;
-  }
-  flags = __reduce_or_sync(FULL_MASK, flags);
-  const int tok = __ldcg(&R[stop].token);
-  for (int j = lane; j < npos; j += 32) {
-    int o = -1;
-    if (!flags) o = j < stop ? __ldg(P.tokens + (size_t)b * K + j) : (j == stop ? tok : -1);
-    P.out_tokens[(size_t)b * npos + j] = o;
-  }
-  if (lane == 0) {
-    P.accepted_len[b] = flags ? -1 : stop;
-    P.num_emitted[b] = flags ? 0 : stop + 1;
-    P.row_status[b] = lowest_code(flags);
-    P.row_counter[b] = 0u;  // leave the workspace zero-filled for the next call
-  }
-}
-
-template <bool BF16, int NV>
-__global__ void __launch_bounds__(NT, 1) chain_stochastic_kernel(const __grid_constant__ ChainStochParams P) {
-  using F = Fmt<BF16>;
-  constexpr int EPV = F::EPV;
-  constexpr int E = NV * EPV;
-  constexpr int ESZ = F::ESZ;
-  static_assert(E <= kMaxElemsPerThread, "register budget");
-
-  extern __shared__ __align__(128) unsigned char smem[];
-  const int S = P.stages;
-  Ctrl &ctl = *reinterpret_cast<Ctrl *>(smem + (size_t)S * 2 * P.buf_bytes);
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t crank = cluster_ctarank(), C = cluster_nctarank();
-  const int cid = (int)cluster_id_x(), NC = (int)num_clusters_x();
-  const int B = P.B, K = P.K, V = P.V, npos = K + 1;
-  const int W = B * npos;
-  const int my_items = cid < W ? (W - 1 - cid) / NC + 1 : 0;
-  const int s0 = (int)crank * P.L;
-  const int len = max(0, min(V, s0 + P.L) - s0);
-  const bool tma = P.use_tma != 0;
-
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(&ctl.full[s], 1);
-    mbar_init(&ctl.never, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  cluster_sync();  // every CTA of the cluster is running: DSMEM may be used from here on
-
-  auto decode = [&](int n, int &b, int &j) {  // drafts first (heavier), bonus rows last
-    const int it = cid + n * NC;
-    if (it < B * K) {
-      b = it / K;
-      j = it - b * K;
-    } else {
-      b = it - B * K;
-      j = K;
-    }
-  };
-  const uint64_t pol = l2_policy_evict_first();
-  auto issue = [&](int n) {  // thread 0: bulk copies of item n into stage n % S
-    int b, j;
-    decode(n, b, j);
-    const int s = n % S;
-    unsigned char *tb = smem + (size_t)s * 2 * P.buf_bytes;
-    const uint32_t bytes = static_cast<uint32_t>(len) * ESZ;
-    mbar_arrive_expect_tx(&ctl.full[s], bytes * (j < K ? 2u : 1u));
-    if (bytes) {
-      bulk_g2s(tb, static_cast<const char *>(P.target) + ((size_t)(b * npos + j) * V + s0) * ESZ,
-               bytes, &ctl.full[s], pol);
-      if (j < K)
-        bulk_g2s(tb + P.buf_bytes,
-                 static_cast<const char *>(P.draft) + ((size_t)(b * K + j) * V + s0) * ESZ, bytes,
-                 &ctl.full[s], pol);
-    }
-  };
-
-  int issued = 0;     // thread 0: items whose copies were issued
-  int n_break = -1;   // first item whose wait gave up (CTA-uniform)
-  if (tma && tid == 0)
-    for (; issued < min(S, my_items); ++issued) issue(issued);
-
-  int xslot = 0;
-  for (int n = 0; n < my_items; ++n) {
-    int b, j;
-    decode(n, b, j);
-    const int s = n % S;
-    const uint32_t parity = static_cast<uint32_t>(n / S) & 1u;
-
-    // ---- item scalars (identical in every CTA of the cluster)
-    uint32_t iflags = 0;
-    const float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
-    if (!(T > 0.f && T < kInf)) iflags |= F_BAD_TEMPERATURE;
-    const float s2 = (iflags & F_BAD_TEMPERATURE) ? 1.f : __fdiv_rn(kLog2e, T);
-    const float u_s = __ldg(P.u_sample + (size_t)b * npos + j);
-    if (!(u_s >= 0.f && u_s < 1.f)) iflags |= F_BAD_UNIFORM;
-    int y = 0;
-    float u_a = 0.f, a_y = 0.f, b_y = 0.f;
-    if (j < K) {
-      y = __ldg(P.tokens + (size_t)b * K + j);
-      u_a = __ldg(P.u_accept + (size_t)b * K + j);
-      if (!(u_a >= 0.f && u_a < 1.f)) iflags |= F_BAD_UNIFORM;
-      if (y < 0 || y >= V) {
-        iflags |= F_BAD_TOKEN;
-        y = 0;
+        token = __shfl_sync(FULL_MASK, pos, ls);
       }
-      a_y = F::load_logit(P.target, (size_t)(b * npos + j) * V + y);
-      b_y = F::load_logit(P.draft, (size_t)(b * K + j) * V + y);
-    }
-
-    // ---- wait for the slices (bounded)
-    bool timed_out = false;
-    if (tma && n_break < 0)
-      timed_out = P.force_timeout ? !mbar_wait_bounded(&ctl.never, 0u, P.wait_limit_ns)
-                                  : !mbar_wait_bounded(&ctl.full[s], parity, P.wait_limit_ns);
-
-    // ---- pass 1: slice -> registers, NaN-propagating max
-    const unsigned char *tb = smem + (size_t)s * 2 * P.buf_bytes;
-    const char *tg = static_cast<const char *>(P.target) + ((size_t)(b * npos + j) * V + s0) * ESZ;
-    const char *dg = static_cast<const char *>(P.draft) + ((size_t)(b * K + j) * V + s0) * ESZ;
-    uint32_t wp[NV * 4], wq[NV * 4];
-    float mp = -kInf, mq = -kInf;
-    {
-      uint32_t pmp = F::NEG_INF_WORD, pmq = F::NEG_INF_WORD;
-#pragma unroll
-      for (int k = 0; k < NV; ++k) {
-        F::load_vec(wp + 4 * k, tma, tb, tg, tid + k * NT, len);
-        if constexpr (BF16) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) pmp = bf16x2_max_nan(pmp, wp[4 * k + i]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) mp = fmax_nan(mp, __uint_as_float(wp[4 * k + i]));
-        }
+      // ---- the row's outputs
+      for (int j = lane; j < npos; j += 32) {
+        const int o = j < stop ? __ldg(P.tokens + (size_t)b * K + j) : (j == stop ? token : -1);
+        P.out_tokens[(size_t)b * npos + j] = o;
       }
-      if (j < K) {
-#pragma unroll
-        for (int k = 0; k < NV; ++k) {
-          F::load_vec(wq + 4 * k, tma, tb + P.buf_bytes, dg, tid + k * NT, len);
-          if constexpr (BF16) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) pmq = bf16x2_max_nan(pmq, wq[4 * k + i]);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) mq = fmax_nan(mq, __uint_as_float(wq[4 * k + i]));
-          }
-        }
-      }
-      if constexpr (BF16) {
-        mp = fmax_nan(bf16_lo(pmp), bf16_hi(pmp));
-        mq = fmax_nan(bf16_lo(pmq), bf16_hi(pmq));
-      }
-    }
-    // everyone has read stage s; a wait that gave up anywhere breaks the pipeline
-    if (__syncthreads_or(timed_out) && n_break < 0) n_break = n;
-    if (n_break >= 0) iflags |= F_TIMEOUT;
-    if (tma && tid == 0 && n_break < 0 && issued < my_items) issue(issued++);
-
-    // ---- exchange 1: max of p and q logits, row flags
-    float4 xv;
-    {
-      const float2 r = block_reduce2(mp, mq, -kInf, fmax_nan, ctl, lane, warp);
-      xv = cluster_exchange(make_float4(r.x, r.y, __uint_as_float(iflags), 0.f), ctl, xslot, C,
-                            tid, lane);
-      xslot ^= 1;
-    }
-    float Mp = -kInf, Mq = -kInf;
-    uint32_t flags = 0;
-    for (uint32_t c = 0; c < C; ++c) {
-      Mp = fmax_nan(Mp, __shfl_sync(FULL_MASK, xv.x, c));
-      Mq = fmax_nan(Mq, __shfl_sync(FULL_MASK, xv.y, c));
-      flags |= __float_as_uint(__shfl_sync(FULL_MASK, xv.z, c));
-    }
-    if (Mp != Mp || Mp == kInf) flags |= F_NONFINITE;
-    else if (Mp == -kInf) flags |= F_EMPTY;
-    if (j < K) {
-      if (Mq != Mq || Mq == kInf) flags |= F_NONFINITE;
-      else if (Mq == -kInf) flags |= F_EMPTY;
-    }
-
-    int owner = 0, token = -1, accept = (j < K) ? 0 : 1;
-    float p_y = 0.f, q_y = 0.f, Z = 0.f;
-    if (!flags) {
-      // ---- pass 2: exp2 in registers, sums
-      const float nMp = -__fmul_rn(Mp, s2), nMq = -__fmul_rn(Mq, s2);
-      float ep[E], eq[E];
-      float sp = 0.f, sq = 0.f;
-#pragma unroll
-      for (int k = 0; k < NV; ++k) {
-        float r = 0.f;
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          ep[k * EPV + e] = ex2(__fmaf_rn(F::elem(wp + 4 * k, e), s2, nMp));
-          r += ep[k * EPV + e];
-        }
-        sp += r;
-      }
-      if (j < K) {
-#pragma unroll
-        for (int k = 0; k < NV; ++k) {
-          float r = 0.f;
-#pragma unroll
-          for (int e = 0; e < EPV; ++e) {
-            eq[k * EPV + e] = ex2(__fmaf_rn(F::elem(wq + 4 * k, e), s2, nMq));
-            r += eq[k * EPV + e];
-          }
-          sq += r;
-        }
-      }
-      // ---- exchange 2: partition sums
-      const float2 r2 = block_reduce2(sp, sq, 0.f, [](float a, float c) { return a + c; }, ctl,
-                                      lane, warp);
-      const float4 sv = cluster_exchange(make_float4(r2.x, r2.y, 0.f, 0.f), ctl, xslot, C, tid,
-                                         lane);
-      xslot ^= 1;
-      float Sp = 0.f, Sq = 0.f;
-      for (uint32_t c = 0; c < C; ++c) {
-        Sp += __shfl_sync(FULL_MASK, sv.x, c);
-        Sq += __shfl_sync(FULL_MASK, sv.y, c);
-      }
-
-      int search = 0;  // 0: none, 1: residual [p - q]+, 2: target law p
-      float mass_lane = sv.x;
-      if (j < K) {
-        // ratio p(y)/q(y) in log2 space: identical logits give exactly 0
-        const float l2p = __fadd_rn(__fmaf_rn(a_y, s2, nMp), -lg2(Sp));
-        const float l2q = __fadd_rn(__fmaf_rn(b_y, s2, nMq), -lg2(Sq));
-        const float l2r = __fadd_rn(l2p, -l2q);
-        accept = (l2r >= 0.f) || (u_a < ex2(l2r));
-        p_y = ex2(l2p);
-        q_y = ex2(l2q);
-        if (!accept) {
-          const float iSp = __frcp_rn(Sp), iSq = __frcp_rn(Sq);
-          float rsum = 0.f;
-#pragma unroll
-          for (int k = 0; k < NV; ++k) {
-            float r = 0.f;
-#pragma unroll
-            for (int e = 0; e < EPV; ++e)
-              r += fmaxf(__fmaf_rn(ep[k * EPV + e], iSp, -__fmul_rn(eq[k * EPV + e], iSq)), 0.f);
-            rsum += r;
-          }
-          // ---- exchange 3: residual mass per CTA
-          const float2 r3 = block_reduce2(rsum, 0.f, 0.f, [](float a, float c) { return a + c; },
-                                          ctl, lane, warp);
-          const float4 rv = cluster_exchange(make_float4(r3.x, 0.f, 0.f, 0.f), ctl, xslot, C, tid,
-                                             lane);
-          xslot ^= 1;
-          float tl_unused, Zr;
-          cluster_pick(rv.x, C, 0.f, &tl_unused, &Zr);
-          Z = Zr;
-          if (Z > 0.f) {
-            search = 1;
-            mass_lane = rv.x;
-          } else {
-            search = 2;  // residual vanished in fp32: draw from p
-          }
-          if (search == 1) {
-            float tl, tot;
-            owner = cluster_pick(mass_lane, C, u_s, &tl, &tot);
-            if ((int)crank == owner) {
-              const int li = cta_inverse_cdf<NV, EPV>(
-                  tl,
-                  [&](int i) {
-                    return fmaxf(__fmaf_rn(ep[i], iSp, -__fmul_rn(eq[i], iSq)), 0.f);
-                  },
-                  ctl, tid, lane, warp);
-              token = s0 + li;
-            }
-          }
-        }
-      } else {
-        search = 2;  // bonus
-      }
-      if (search == 2) {
-        float tl, tot;
-        owner = cluster_pick(sv.x, C, u_s, &tl, &tot);
-        if ((int)crank == owner) {
-          const int li = cta_inverse_cdf<NV, EPV>(tl, [&](int i) { return ep[i]; }, ctl, tid, lane,
-                                                  warp);
-          token = s0 + li;
-        }
-      }
-    }
-
-    // ---- record, diagnostics, and the row walk by the last position to finish
-    if (owner < 0) owner = 0;  // never leave a position without a writer
-    if ((int)crank == owner && warp == 0) {
-      unsigned old = 0;
       if (lane == 0) {
-        const size_t o = (size_t)b * npos + j;
-        __stcg(reinterpret_cast<int4 *>(P.rec + o),
-               make_int4(token, accept, static_cast<int>(flags), 0));
-        if (j < K) {
-          const size_t d = (size_t)b * K + j;
-          if (P.p_at_draft) P.p_at_draft[d] = p_y;
-          if (P.q_at_draft) P.q_at_draft[d] = q_y;
-          if (P.resid_mass) P.resid_mass[d] = accept ? 0.f : Z;
-        }
-        __threadfence();
-        old = atomicAdd(P.row_counter + b, 1u);
-      }
-      old = __shfl_sync(FULL_MASK, old, 0);
-      if (old == static_cast<unsigned>(K)) {
-        __threadfence();
-        walk_chain_row(P, b, lane);
+        P.accepted_len[b] = stop;
+        P.num_emitted[b] = stop + 1;
+        P.row_status[b] = 0;
+        if (stop < K && P.resid_mass) P.resid_mass[(size_t)b * K + stop] = Z;
       }
     }
   }
-
-  // copies issued after a wait gave up may still be landing: let them finish
-  if (tma && n_break >= 0 && tid == 0)
-    for (int m = n_break; m < issued; ++m)
-      mbar_wait_bounded(&ctl.full[m % S], static_cast<uint32_t>(m / S) & 1u, P.wait_limit_ns);
-  __syncthreads();
-  cluster_sync();  // no CTA leaves while a peer may still read its mailbox
+  cluster_wait();  // no CTA leaves while a peer may still read its mailbox
 }
 
-// Function attributes are set once per device (and again only when a larger
-// shared-memory size is needed), so steady-state launches make no driver
-// calls besides the launch itself and can be captured into a CUDA graph.
-template <bool BF16, int NV>
+size_t resolve_smem(const ChainStochParams &p) {
+  return static_cast<size_t>(2 * p.K + 1) * 16 + static_cast<size_t>(p.vpw / 32) * kResolveThreads * 4;
+}
+
+// Function attributes are set once per device (again only when more shared
+// memory is needed), so steady-state launches make no other driver calls and
+// can be captured into a CUDA graph.
+template <bool BF16, int NV, int S>
 cudaError_t prepare(size_t smem, int cluster) {
   static std::atomic<size_t> done_smem[kMaxDevices];
   static std::atomic<int> done_nonportable[kMaxDevices];
+  static std::atomic<int> done_resolve[kMaxDevices];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  auto k = chain_stochastic_kernel<BF16, NV>;
   if (done_smem[dev].load() < smem) {
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(softmax_partials_kernel<BF16, NV, S>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     done_smem[dev].store(smem);
   }
+  if (!done_resolve[dev].load()) {
+    e = cudaFuncSetAttribute(chain_resolve_kernel<BF16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+    if (e != cudaSuccess) return e;
+    done_resolve[dev].store(1);
+  }
   if (cluster > 8 && !done_nonportable[dev].load()) {
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(chain_resolve_kernel<BF16>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     done_nonportable[dev].store(1);
   }
   return cudaSuccess;
 }
 
-template <bool BF16, int NV>
-cudaError_t launch_t(const ChainStochParams &p, int cluster, int grid_clusters, size_t smem,
+template <bool BF16, int NV, int S>
+cudaError_t launch_t(const ChainStochParams &p, int grid, size_t smem, int cluster,
                      cudaStream_t s) {
-  cudaError_t e = prepare<BF16, NV>(smem, cluster);
+  cudaError_t e = prepare<BF16, NV, S>(smem, cluster);
+  if (e != cudaSuccess) return e;
+  softmax_partials_kernel<BF16, NV, S><<<grid, kSoftThreads + 32, smem, s>>>(p);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(cluster * grid_clusters));
-  cfg.blockDim = dim3(NT);
-  cfg.dynamicSmemBytes = smem;
+  cfg.gridDim = dim3(static_cast<unsigned>(p.B * cluster));
+  cfg.blockDim = dim3(kResolveThreads);
+  cfg.dynamicSmemBytes = resolve_smem(p);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, chain_stochastic_kernel<BF16, NV>, p);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, chain_resolve_kernel<BF16>, p);
 }
 
-template <bool BF16, int NV>
-cudaError_t max_clusters_t(int cluster, size_t smem, int *out) {
-  cudaError_t e = prepare<BF16, NV>(smem, cluster);
+template <bool BF16, int NV, int S>
+cudaError_t blocks_t(size_t smem, int *blocks) {
+  cudaError_t e = prepare<BF16, NV, S>(smem, 1);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(cluster * 64));
-  cfg.blockDim = dim3(NT);
-  cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(out, chain_stochastic_kernel<BF16, NV>, &cfg);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, softmax_partials_kernel<BF16, NV, S>,
+                                                       kSoftThreads + 32, smem);
 }
 
 }  // namespace
 
-cudaError_t launch_chain_stochastic(const ChainStochParams &p, bool bf16, int nv, int cluster,
-                                    int grid_clusters, size_t smem, cudaStream_t s) {
-  if (bf16) {
-    switch (nv) {
-      case 1: return launch_t<true, 1>(p, cluster, grid_clusters, smem, s);
-      case 2: return launch_t<true, 2>(p, cluster, grid_clusters, smem, s);
-      case 4: return launch_t<true, 4>(p, cluster, grid_clusters, smem, s);
-      default: return cudaErrorInvalidValue;
-    }
-  }
-  switch (nv) {
-    case 1: return launch_t<false, 1>(p, cluster, grid_clusters, smem, s);
-    case 2: return launch_t<false, 2>(p, cluster, grid_clusters, smem, s);
-    case 4: return launch_t<false, 4>(p, cluster, grid_clusters, smem, s);
-    case 8: return launch_t<false, 8>(p, cluster, grid_clusters, smem, s);
-    default: return cudaErrorInvalidValue;
-  }
+cudaError_t launch_chain_stochastic(const ChainStochParams &p, bool bf16, int nv, int grid,
+                                    size_t smem, int cluster, cudaStream_t s) {
+  (void)nv;
+  if (p.stages == 3)
+    return bf16 ? launch_t<true, 4, 3>(p, grid, smem, cluster, s) : launch_t<false, 4, 3>(p, grid, smem, cluster, s);
+  return bf16 ? launch_t<true, 4, 2>(p, grid, smem, cluster, s) : launch_t<false, 4, 2>(p, grid, smem, cluster, s);
 }
 
-cudaError_t chain_stochastic_max_clusters(bool bf16, int nv, int cluster, size_t smem,
-                                          int *clusters) {
-  if (bf16) {
-    switch (nv) {
-      case 1: return max_clusters_t<true, 1>(cluster, smem, clusters);
-      case 2: return max_clusters_t<true, 2>(cluster, smem, clusters);
-      case 4: return max_clusters_t<true, 4>(cluster, smem, clusters);
-      default: return cudaErrorInvalidValue;
-    }
-  }
-  switch (nv) {
-    case 1: return max_clusters_t<false, 1>(cluster, smem, clusters);
-    case 2: return max_clusters_t<false, 2>(cluster, smem, clusters);
-    case 4: return max_clusters_t<false, 4>(cluster, smem, clusters);
-    case 8: return max_clusters_t<false, 8>(cluster, smem, clusters);
-    default: return cudaErrorInvalidValue;
-  }
+cudaError_t soft_partials_blocks_per_sm(bool bf16, int nv, size_t smem, int *blocks) {
+  (void)nv;
+  if (smem > 80 * 1024)
+    return bf16 ? blocks_t<true, 4, 3>(smem, blocks) : blocks_t<false, 4, 3>(smem, blocks);
+  return bf16 ? blocks_t<true, 4, 2>(smem, blocks) : blocks_t<false, 4, 2>(smem, blocks);
 }
 
 }  // namespace sv

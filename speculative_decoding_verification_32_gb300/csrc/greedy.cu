@@ -35,10 +35,6 @@ struct alignas(16) GCtrl {
   float part_v[NW];
   int part_i[NW];
   uint32_t part_f[NW];
-  int walk_best;
-  int walk_depth;
-  uint32_t walk_flags;
-  int pad1;
 };
 static_assert(sizeof(GCtrl) <= 1024, "control block must fit its reservation");
 
@@ -91,7 +87,7 @@ __device__ __forceinline__ void combine_partials(const GreedyPart *pp, int nslic
   int bi = -1;
   uint32_t f = 0;
   for (int s = 0; s < nslices; ++s) {
-    const int4 r = __ldcg(reinterpret_cast<const int4 *>(pp + s));
+    const int4 r = *reinterpret_cast<const int4 *>(pp + s);
     const float v = __int_as_float(r.x);
     f |= static_cast<uint32_t>(r.z);
     if (v > best) {  // slices in vocabulary order: ties keep the earlier slice
@@ -105,6 +101,7 @@ __device__ __forceinline__ void combine_partials(const GreedyPart *pp, int nslic
   *top = bi;
   *flags = f;
 }
+
 
 // Margin rule in fp64: l(draft) - l(top1) > T * ln(kappa).
 __device__ __forceinline__ bool margin_promotes(float l_d, float l_top, float T, double ln_kappa) {
@@ -161,7 +158,6 @@ __device__ void walk_greedy_chain(const GreedyParams &P, int b, int lane) {
     P.accepted_len[b] = flags ? -1 : stop;
     P.num_emitted[b] = flags ? 0 : stop + 1;
     P.row_status[b] = lowest_code(flags);
-    P.row_counter[b] = 0u;
   }
 }
 
@@ -169,7 +165,7 @@ __device__ void walk_greedy_chain(const GreedyParams &P, int b, int lane) {
 // is the parent's argmax (or promoted by the margin rule); keep the deepest
 // accepted node, lowest index on ties.  `scr` is shared scratch for N nodes.
 template <bool BF16>
-__device__ void walk_tree(const GreedyParams &P, int b, int lane, unsigned char *scr, GCtrl &ctl) {
+__device__ void walk_tree(const GreedyParams &P, int b, int lane, unsigned char *scr, int *shared_best) {
   using F = GFmt<BF16>;
   const int N = P.npos, V = P.V;
   int *top_s = reinterpret_cast<int *>(scr);
@@ -231,13 +227,13 @@ __device__ void walk_tree(const GreedyParams &P, int b, int lane, unsigned char 
       }
       const int d = dep_s[best];
       for (int n = best, k = d - 1; k >= 0; n = par_s[n], --k) path_s[k] = n;
-      ctl.walk_best = best;
-      ctl.walk_depth = d;
+      shared_best[0] = best;
+      shared_best[1] = d;
     }
     __syncwarp();
   }
-  const int best = flags ? 0 : ctl.walk_best;
-  const int d = flags ? -1 : ctl.walk_depth;
+  const int best = flags ? 0 : shared_best[0];
+  const int d = flags ? -1 : shared_best[1];
   for (int i = lane; i < N; i += 32) {
     int pn = -1, ot = -1;
     if (!flags) {
@@ -255,7 +251,6 @@ __device__ void walk_tree(const GreedyParams &P, int b, int lane, unsigned char 
     P.accepted_len[b] = flags ? -1 : d;
     P.num_emitted[b] = flags ? 0 : d + 1;
     P.row_status[b] = lowest_code(flags);
-    P.row_counter[b] = 0u;
   }
   __syncwarp();
 }
@@ -268,15 +263,17 @@ __global__ void __launch_bounds__(NT, 1) greedy_kernel(const __grid_constant__ G
   extern __shared__ __align__(128) unsigned char smem[];
   const int S = P.stages;
   GCtrl &ctl = *reinterpret_cast<GCtrl *>(smem + (size_t)S * P.buf_bytes);
-  unsigned char *scratch = smem + (size_t)S * P.buf_bytes + 1024;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int B = P.B, npos = P.npos, V = P.V, nsl = P.nslices;
+  const int npos = P.npos, V = P.V, nsl = P.nslices;
+  const int B = P.B;
   const int W = B * npos * nsl;
   const int G = (int)gridDim.x, g = (int)blockIdx.x;
   const int my_items = g < W ? (W - 1 - g) / G + 1 : 0;
   const bool tma = P.use_tma != 0;
-  const unsigned arrivals = static_cast<unsigned>(npos * nsl);
+
+  // let the walk kernel be scheduled now; it waits for this grid anyway
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&ctl.full[s], 1);
@@ -370,27 +367,33 @@ __global__ void __launch_bounds__(NT, 1) greedy_kernel(const __grid_constant__ G
         }
       }
       f = __reduce_or_sync(FULL_MASK, f);
-      unsigned old = 0;
-      const int b = pos / npos;
       if (lane == 0) {
         const int slice = (g + n * G) - pos * nsl;
-        __stcg(reinterpret_cast<int4 *>(P.part + (size_t)pos * nsl + slice),
-               make_int4(__float_as_int(best), bidx >= 0 ? s0 + bidx : -1, static_cast<int>(f), 0));
-        __threadfence();
-        old = atomicAdd(P.row_counter + b, 1u);
-      }
-      old = __shfl_sync(FULL_MASK, old, 0);
-      if (old == arrivals - 1u) {
-        __threadfence();
-        if (P.tree) walk_tree<BF16>(P, b, lane, scratch, ctl);
-        else walk_greedy_chain<BF16>(P, b, lane);
+        P.part[(size_t)pos * nsl + slice] =
+            GreedyPart{best, bidx >= 0 ? s0 + bidx : -1, f, 0};
       }
     }
-    __syncthreads();  // warp 0's use of the partial slots and the walk scratch is done
   }
   if (tma && n_break >= 0 && tid == 0)
     for (int m = n_break; m < issued; ++m)
       mbar_wait_bounded(&ctl.full[m % S], static_cast<uint32_t>(m / S) & 1u, P.wait_limit_ns);
+}
+
+// One warp per row: combine the row's partials and walk the chain or the
+// tree.  Waits for the partial kernel (programmatic dependent launch).
+template <bool BF16>
+__global__ void greedy_walk_kernel(const __grid_constant__ GreedyParams P) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  extern __shared__ __align__(16) unsigned char wsm[];
+  const int lane = threadIdx.x & 31;
+  const int b = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  if (b >= P.B) return;
+  if (P.tree) {
+    int *best = reinterpret_cast<int *>(wsm);
+    walk_tree<BF16>(P, b, lane, wsm + 16, best);
+  } else {
+    walk_greedy_chain<BF16>(P, b, lane);
+  }
 }
 
 // Set the shared-memory attribute once per device (again only if more is needed).
@@ -415,7 +418,23 @@ cudaError_t launch_greedy(const GreedyParams &p, bool bf16, int grid, size_t sme
   if (e != cudaSuccess) return e;
   if (bf16) greedy_kernel<true><<<grid, NT, smem, s>>>(p);
   else greedy_kernel<false><<<grid, NT, smem, s>>>(p);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // walk: trees need N*20 bytes of scratch per row, so one warp per block;
+  // chains take four rows per block
+  const int rows_per_block = p.tree ? 1 : 4;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((p.B + rows_per_block - 1) / rows_per_block));
+  cfg.blockDim = dim3(static_cast<unsigned>(32 * rows_per_block));
+  cfg.dynamicSmemBytes = p.tree ? 16 + static_cast<size_t>(p.npos) * 20 : 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return bf16 ? cudaLaunchKernelEx(&cfg, greedy_walk_kernel<true>, p)
+              : cudaLaunchKernelEx(&cfg, greedy_walk_kernel<false>, p);
 }
 
 cudaError_t greedy_max_blocks_per_sm(bool bf16, size_t smem, int *blocks) {

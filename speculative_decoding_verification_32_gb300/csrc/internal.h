@@ -7,13 +7,15 @@
 
 namespace sv {
 
-// One 16-byte record per (row, position) written by the stochastic chain
-// kernel and read by the row walk.
-struct alignas(16) ChainRec {
-  int32_t token;   // correction / bonus token drawn at this position
-  int32_t accept;  // 1: the position's test accepts its draft
-  uint32_t flags;  // row-status bits met at this position
+// One 16-byte partial per (logit row, tile) written by the softmax-partial
+// kernel: a run of consecutive tiles of one row streamed by one CTA leaves its
+// max logit m and sum of exp2((x - m) s2) at the run's first tile and empty
+// partials (m = -inf, s = 0) at its other tiles.
+struct alignas(16) SoftPart {
+  float m;
+  float s;
   float pad;
+  uint32_t flags;
 };
 
 // One 16-byte partial per (row, position, vocabulary slice) written by the
@@ -39,13 +41,16 @@ struct ChainStochParams {
   float *p_at_draft;
   float *q_at_draft;
   float *resid_mass;
-  uint32_t *row_counter;  // [B] workspace, zero between calls
-  ChainRec *rec;          // [B*(K+1)] workspace
+  SoftPart *part;  // [(B*(K+1) + B*K) * nslices] workspace
+  float *ylog;     // [B*(K+1) + B*K] workspace: the draft token's logit per logit row
   int B, K, V;
-  int L;          // vocabulary slice per CTA (elements, multiple of the vector width)
-  int use_tma;    // rows are 16-byte aligned: bulk copies; else direct loads
-  int stages;     // bulk-copy pipeline depth
-  int buf_bytes;  // bytes of one tensor slice buffer in shared memory
+  int slice;       // elements per tile of the partial kernel
+  int nslices;     // tiles per logit row
+  int use_tma;     // rows are 16-byte aligned: bulk copies; else direct loads
+  int stages;      // bulk-copy pipeline depth of the partial kernel
+  int buf_bytes;   // bytes of one stage buffer
+  int L;           // resolve kernel: vocabulary slice per cluster CTA
+  int vpw;         // resolve kernel: 16-byte vectors per warp (multiple of 32)
   uint64_t wait_limit_ns;
   int force_timeout;
 };
@@ -63,7 +68,6 @@ struct GreedyParams {
   int32_t *num_emitted;
   int32_t *row_status;
   int32_t *path_nodes;     // tree only
-  uint32_t *row_counter;   // [B] workspace
   GreedyPart *part;        // [B*npos*nslices] workspace
   int B, npos, V;
   int slice;               // elements per slice
@@ -87,21 +91,32 @@ struct RollbackParams {
   int32_t *num_emitted_out;
 };
 
-// Threads per CTA of the streaming kernels.
+// Threads per CTA: greedy partial kernel, softmax partial kernel (consumer
+// warps; one producer warp comes on top), resolve kernel.
 constexpr int kThreads = 512;
-// Largest elements per thread per tensor the stochastic kernel keeps in registers.
-constexpr int kMaxElemsPerThread = 32;
+constexpr int kSoftThreads = 256;
+constexpr int kResolveThreads = 256;
+// 16-byte vectors per consumer thread per tensor in a softmax-partial tile:
+// a tile is kSoftThreads * kSoftVecs vectors of the target row and as many of
+// the draft row (kSoftVecs = 4: 8192 bf16 or 4096 fp32 logits per tensor).
+constexpr int kSoftVecs = 4;
+// Depth of the softmax-partial kernel's bulk-copy ring.
+constexpr int kSoftStages = 2;
+// Smallest tile (elements) any build of the partial kernel uses: sizes the
+// workspace.
+constexpr int kSoftMinSlice = kSoftThreads * 4 * 4;
+// Largest rounds of 32 vectors per warp in the resolve kernel.
+constexpr int kResolveMaxRounds = 16;
 // Elements per greedy work item.
 constexpr int kGreedySlice = 16384;
 // Devices whose per-kernel attributes are cached.
 constexpr int kMaxDevices = 64;
 
-// Host launchers (defined next to their kernels).  `nv` = 16-byte vectors per
-// thread per tensor; returns the CUDA error of the launch.
-cudaError_t launch_chain_stochastic(const ChainStochParams &p, bool bf16, int nv, int cluster,
-                                    int grid_clusters, size_t smem, cudaStream_t s);
-cudaError_t chain_stochastic_max_clusters(bool bf16, int nv, int cluster, size_t smem,
-                                          int *clusters);
+// Host launchers (defined next to their kernels); each returns the CUDA error
+// of its launches.
+cudaError_t launch_chain_stochastic(const ChainStochParams &p, bool bf16, int nv, int grid,
+                                    size_t smem, int cluster, cudaStream_t s);
+cudaError_t soft_partials_blocks_per_sm(bool bf16, int nv, size_t smem, int *blocks);
 cudaError_t launch_greedy(const GreedyParams &p, bool bf16, int grid, size_t smem,
                           cudaStream_t s);
 cudaError_t greedy_max_blocks_per_sm(bool bf16, size_t smem, int *blocks);

@@ -50,8 +50,8 @@ def compare_stochastic(g, o, band=BAND):
     if "p_at_draft" in g and g["p_at_draft"].size:
         np.testing.assert_allclose(g["p_at_draft"][ok], o["p_at_draft"][ok], atol=PROB_ATOL, rtol=0)
         np.testing.assert_allclose(g["q_at_draft"][ok], o["q_at_draft"][ok], atol=PROB_ATOL, rtol=0)
-        # residual mass where both sides took the same decision at that position
-        decided = (o["accept_margin"] >= band) & ok[:, None]
-        np.testing.assert_allclose(g["resid_mass"][decided], o["resid_mass"][decided],
+        # residual mass (reported at the stopping position) of rows that agree
+        rows = same & ok
+        np.testing.assert_allclose(g["resid_mass"][rows], o["resid_mass"][rows],
                                    atol=PROB_ATOL, rtol=0)
     return int(mism.sum())
