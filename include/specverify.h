@@ -69,7 +69,8 @@ typedef enum {
   SPEC_ERR_ALIGN = 4,     /* a pointer is not aligned to its element size */
   SPEC_ERR_ARG = 5,       /* another bad scalar argument (e.g. kappa is NaN) */
   SPEC_ERR_CUDA = 6,      /* a CUDA runtime call failed (no device, launch error) */
-  SPEC_ERR_WORKSPACE = 7  /* workspace NULL, misaligned or too small */
+  SPEC_ERR_WORKSPACE = 7, /* workspace NULL, misaligned or too small */
+  SPEC_ERR_STATIC_LIMIT = 8 /* problem too large for spec_verify_chain_static */
 } spec_status;
 
 /* Per-row data status written to row_status[b].  When several problems meet
@@ -160,6 +161,41 @@ size_t spec_verify_chain_workspace_size(int32_t B, int32_t K, int32_t V);
  */
 spec_status spec_verify_chain(const spec_chain_args *args, const spec_chain_out *out,
                               void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * spec_verify_chain_static -- spec_verify_chain with a scratch buffer built
+ * into the library instead of one the caller passes.  The pages have no
+ * counterpart: this is a convenience of this library, not part of the method.
+ *
+ * It is meant for callers that cannot allocate device memory where they
+ * verify: a plain C host loop that has no device allocator of its own, a
+ * serving engine whose memory pool has already claimed the device's free
+ * memory for its KV cache, or a decode loop that must not pay the
+ * device-wide synchronisation a cudaFree implies.  The call itself never
+ * allocates or frees anything.
+ *
+ * Limit: the built-in buffer holds SPEC_STATIC_WS_BYTES (4 MiB) per device.
+ * A problem whose spec_verify_chain_workspace_size(B, K, V) is larger is
+ * rejected with SPEC_ERR_STATIC_LIMIT before anything is launched.  4 MiB
+ * covers, for example, B = 256 chains of K = 8 drafts over V = 128256.
+ *
+ * Set-up: the first call on a device (with that device current) looks up
+ * the buffer's device address once; that lookup may load the library's
+ * kernels onto the device.  Make that first call before any stream capture
+ * begins.
+ *
+ * Concurrency: all calls on one device share the one buffer.  Calls queued
+ * on one stream run one after another and are safe; calls whose kernels may
+ * overlap on the GPU (other streams, other host threads) race on the buffer
+ * and produce wrong results.  The kernels write every scratch word before
+ * they read it, so the buffer never needs clearing.
+ *
+ * Arguments, outputs and status codes are otherwise those of
+ * spec_verify_chain.
+ */
+#define SPEC_STATIC_WS_BYTES ((size_t)4 << 20)
+spec_status spec_verify_chain_static(const spec_chain_args *args, const spec_chain_out *out,
+                                     void *stream);
 
 /* ------------------------------------------------------------------- tree */
 

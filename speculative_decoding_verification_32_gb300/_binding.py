@@ -81,6 +81,8 @@ def _bind(L):
     L.spec_verify_tree_workspace_size.restype = sz
     L.spec_verify_chain.argtypes = [_c.POINTER(SpecChainArgs), _c.POINTER(SpecChainOut), _P, sz, _P]
     L.spec_verify_chain.restype = _c.c_int
+    L.spec_verify_chain_static.argtypes = [_c.POINTER(SpecChainArgs), _c.POINTER(SpecChainOut), _P]
+    L.spec_verify_chain_static.restype = _c.c_int
     L.spec_verify_tree.argtypes = [_c.POINTER(SpecTreeArgs), _c.POINTER(SpecTreeOut), _P, sz, _P]
     L.spec_verify_tree.restype = _c.c_int
     L.spec_rollback_lengths.argtypes = [i32, i32, _P, _P, _P, _P, i32, _P, _P, _P, _P]

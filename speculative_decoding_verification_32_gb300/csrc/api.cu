@@ -15,6 +15,10 @@
 
 using namespace sv;
 
+// Scratch of spec_verify_chain_static: part of the library image, one copy
+// per device, so that entry point never allocates.
+static __device__ __align__(256) unsigned char g_static_ws[SPEC_STATIC_WS_BYTES];
+
 namespace {
 
 std::atomic<uint64_t> g_wait_ns{1000000000ull};
@@ -28,6 +32,7 @@ struct DevInfo {
 std::mutex g_mu;
 std::map<int, DevInfo> g_dev;
 std::map<std::tuple<int, int, size_t>, int> g_blocks;
+void *g_static_ws_ptr[kMaxDevices] = {};  // device address of g_static_ws, per device
 
 constexpr size_t kGreedyCtrlBytes = 1024;
 constexpr size_t kSoftCtrlBytes = 2048;
@@ -291,6 +296,29 @@ spec_status spec_verify_chain(const spec_chain_args *a, const spec_chain_out *o,
   return SPEC_OK;
 }
 
+spec_status spec_verify_chain_static(const spec_chain_args *a, const spec_chain_out *o,
+                                     void *stream) {
+  if (!a || !o) return SPEC_ERR_NULL;
+  const size_t need = spec_verify_chain_workspace_size(a->B, a->K, a->V);
+  if (need == 0) return SPEC_ERR_SHAPE;
+  if (need > SPEC_STATIC_WS_BYTES) return SPEC_ERR_STATIC_LIMIT;
+  int dev;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_CUDA;
+  void *ws = nullptr;
+  {
+    // first call on this device: look up the buffer's address (the device is
+    // current here, as the lookup requires)
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_static_ws_ptr[dev]) {
+      void *ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_static_ws) != cudaSuccess || !ptr) return SPEC_ERR_CUDA;
+      g_static_ws_ptr[dev] = ptr;
+    }
+    ws = g_static_ws_ptr[dev];
+  }
+  return spec_verify_chain(a, o, ws, SPEC_STATIC_WS_BYTES, stream);
+}
+
 spec_status spec_verify_tree(const spec_tree_args *a, const spec_tree_out *o, void *ws,
                              size_t ws_bytes, void *stream) {
   if (!a || !o) return SPEC_ERR_NULL;
@@ -367,6 +395,9 @@ const char *spec_status_string(spec_status s) {
     case SPEC_ERR_ARG: return "SPEC_ERR_ARG: bad scalar argument";
     case SPEC_ERR_CUDA: return "SPEC_ERR_CUDA: a CUDA runtime call failed";
     case SPEC_ERR_WORKSPACE: return "SPEC_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case SPEC_ERR_STATIC_LIMIT:
+      return "SPEC_ERR_STATIC_LIMIT: the problem needs more scratch than the built-in "
+             "SPEC_STATIC_WS_BYTES buffer of spec_verify_chain_static holds";
   }
   return "unknown spec_status";
 }
