@@ -32,6 +32,10 @@ WORKLOAD = "c3"
 METRIC = "verify steps/s and achieved HBM GB/s (B=64,K=5,V=128256 bf16) vs 8 TB/s"
 UNIT = "verify steps/s"
 L2_BYTES = 129 * 1024 * 1024
+# ncu dram__bytes_read.sum + dram__bytes_write.sum of one softmax_partials_kernel
+# launch on this workload (profiles/softmax_partials_c3.md); None until the
+# current kernel has been captured
+TRAFFIC = None
 
 
 def parse():
@@ -61,6 +65,27 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def rank_seed(rank):
+    """Each rank verifies its own independent batch (weak scaling by rows)."""
+    return S.CONFIGS[WORKLOAD]["seed"] + 7919 * rank
+
+
+def max_over_ranks(ms, device):
+    """The slowest rank's time: the job's time.  No other data crosses ranks."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world, steps, ms):
+    """Whole-job throughput: the steps of all ranks over the slowest rank's time."""
+    return world * steps / (ms / 1e3)
 
 
 def peaks():
@@ -204,7 +229,7 @@ def run_ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    seed = S.CONFIGS[WORKLOAD]["seed"] + 7919 * rank  # each rank its own batch
+    seed = rank_seed(rank)
     inp = S.make(WORKLOAD, seed=seed)
     B, K = inp["draft_tokens"].shape
     V = inp["target"].shape[-1]
@@ -271,12 +296,9 @@ def run_ours(args):
         torch.distributed.barrier()
     clocks = sampler.stop()
     ms = ev0.elapsed_time(ev1)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
     ms_per_step = ms / steps
-    value = ws * steps / (ms / 1e3)
+    value = job_value(ws, steps, ms)
     gbs = step_bytes / (ms_per_step / 1e3) / 1e9
     peak, peak_kind = peaks()
 
@@ -328,8 +350,10 @@ def run_ours(args):
         "achieved_hbm_gbs": gbs,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                      "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
-                     "kernel": "chain_stochastic_kernel<bf16, 4>",
-                     "algorithmic_bytes_per_launch": step_bytes, "traffic": None},
+                     "kernel": "softmax_partials_kernel<bf16,4,2> (dominant) + "
+                               "chain_resolve_kernel<bf16> (PDL); achieved = algorithmic "
+                               "bytes / whole-step time, a lower bound for the stream kernel",
+                     "algorithmic_bytes_per_launch": step_bytes, "traffic": TRAFFIC},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": steps,
