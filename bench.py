@@ -36,6 +36,9 @@ L2_BYTES = 129 * 1024 * 1024
 # launch on this workload (profiles/softmax_partials_c3.md); None until the
 # current kernel has been captured
 TRAFFIC = None
+# kernels one stochastic spec_verify_chain call enqueues: the stream kernel
+# and the resolve kernel
+KERNELS_PER_STEP = 2
 
 
 def parse():
@@ -356,7 +359,7 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": step_bytes, "traffic": TRAFFIC},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": steps,
+        "gpu_launches": KERNELS_PER_STEP * steps,
         "clocks": clocks,
         "parity_spot_check": spot,
     }

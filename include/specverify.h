@@ -38,17 +38,24 @@
  *    its token outputs -1; other rows are unaffected.
  *  - Workspace: `ws` is caller-owned device memory of at least the size the
  *    matching *_workspace_size() returns, 256-byte aligned.  Its contents
- *    need no initialisation: each call overwrites what it reads.  Calls on
- *    one stream may share a workspace; calls that may overlap in time
- *    (different streams) need separate workspaces.
+ *    need no initialisation.  The stochastic chain call keeps a small header
+ *    in the last 16 bytes of the `ws_bytes` it is given, plus one word per
+ *    row just below it.  Between calls these hold a work counter and a
+ *    generation count per row.  On the first call with a given workspace
+ *    the stream kernel assigns every tile statically; from the second call
+ *    on it hands out the last tiles dynamically, which balances the stream
+ *    (results are identical either way).  Keep passing the same `ws_bytes`
+ *    for the same buffer to keep that benefit.  Calls on one stream may
+ *    share a workspace; calls that may overlap in time (different streams)
+ *    need separate workspaces.
  *  - Each verify call enqueues two kernels: the streaming kernel and a small
  *    per-row walk kernel that starts early and waits for it on the device
  *    (programmatic dependent launch).
  *  - Logits are bf16 (SPEC_BF16) or fp32 (SPEC_F32).  Rows whose byte
  *    length is a multiple of 16 with a 16-byte aligned base take the bulk-
  *    copy (TMA) path; any other V still works, more slowly.
- *  - The calls are stateless apart from a per-process cache of device
- *    occupancy queries (thread safe).
+ *  - Apart from the workspace header above, the calls keep no state other
+ *    than a per-process cache of device occupancy queries (thread safe).
  */
 #ifndef SPECVERIFY_H
 #define SPECVERIFY_H
@@ -187,8 +194,7 @@ spec_status spec_verify_chain(const spec_chain_args *args, const spec_chain_out 
  * Concurrency: all calls on one device share the one buffer.  Calls queued
  * on one stream run one after another and are safe; calls whose kernels may
  * overlap on the GPU (other streams, other host threads) race on the buffer
- * and produce wrong results.  The kernels write every scratch word before
- * they read it, so the buffer never needs clearing.
+ * and produce wrong results.  The buffer never needs clearing.
  *
  * Arguments, outputs and status codes are otherwise those of
  * spec_verify_chain.

@@ -1,7 +1,7 @@
 """ctypes binding of libspecverify.so: argument marshalling only.
 
 Takes torch CUDA tensors, passes their device pointers, the current CUDA
-stream and a cached zero-filled workspace to the C ABI declared in
+stream and a cached workspace to the C ABI declared in
 include/specverify.h, and returns the output tensors.  Every step of the
 computation runs in the library's kernels; there is no other code path.
 """
@@ -129,8 +129,9 @@ def _req(t, name, device, dtype=None):
     return t
 
 
-# Workspaces: one zero-filled buffer per (device, stream), grown on demand.
-# Each completed call leaves its workspace zero-filled again.
+# Workspaces: one buffer per (device, stream), grown on demand.  The library
+# needs no particular contents; it keeps a small header at the buffer's end
+# between calls, so the same buffer is always passed with its full size.
 _ws = {}
 _ws_lock = threading.Lock()
 

@@ -166,12 +166,15 @@ size_t spec_verify_chain_workspace_size(int32_t B, int32_t K, int32_t V) {
   const size_t rows = static_cast<size_t>(B) * (K + 1) + static_cast<size_t>(B) * K;
   const size_t soft = rows * ceil_div(V, kSoftMinSlice) * sizeof(SoftPart) + align_up(rows * 4, 256);
   const size_t part = greedy_partials_max(B, K + 1, V);
-  return align_up(std::max(std::max(soft, part), static_cast<size_t>(256)), 256);
+  return align_up(std::max(std::max(soft, part), static_cast<size_t>(256)), 256) + ws_tail_bytes(B);
 }
 
 size_t spec_verify_tree_workspace_size(int32_t B, int32_t N, int32_t V) {
   if (!valid_sizes(B, V) || N < 1 || N > SPEC_MAX_TREE_NODES) return 0;
-  return align_up(std::max(greedy_partials_max(B, N, V), static_cast<size_t>(256)), 256);
+  // the tail is reserved (unused here) so a workspace shared with chain calls
+  // keeps their header
+  return align_up(std::max(greedy_partials_max(B, N, V), static_cast<size_t>(256)), 256) +
+         ws_tail_bytes(B);
 }
 
 spec_status spec_verify_chain(const spec_chain_args *a, const spec_chain_out *o, void *ws,
@@ -250,6 +253,23 @@ spec_status spec_verify_chain(const spec_chain_args *a, const spec_chain_out *o,
               (static_cast<long long>(a->V) * esz) % 16 == 0;
   p.wait_limit_ns = g_wait_ns.load();
   p.force_timeout = g_force_timeout.load();
+  {
+    // workspace tail: header {claim, -, magic} in the last 16 bytes, one
+    // generation word per row below it
+    char *end = static_cast<char *>(ws) + (ws_bytes & ~static_cast<size_t>(15));
+    p.claim = reinterpret_cast<uint32_t *>(end - 16);
+    p.magic = reinterpret_cast<unsigned long long *>(end - 8);
+    p.gen = reinterpret_cast<uint32_t *>(end - 16);
+    // SPECVERIFY_DYNAMIC=0 keeps every tile statically assigned;
+    // SPECVERIFY_DYN_CHUNK sets the tiles per claim (tuning)
+    const char *dv = std::getenv("SPECVERIFY_DYNAMIC");
+    p.dyn = !(dv && *dv == '0');
+    p.dyn_chunk = 2;
+    if (const char *dc = std::getenv("SPECVERIFY_DYN_CHUNK")) {
+      const int c = std::atoi(dc);
+      if (c >= 1 && c <= 64) p.dyn_chunk = c;
+    }
+  }
   // stream kernel: fixed-size items (16 or 32 KB), a bulk-copy ring per CTA;
   // SPECVERIFY_SOFT_VECS (4 or 8) and SPECVERIFY_SOFT_STAGES (2..4) override
   // the defaults for tuning

@@ -167,6 +167,7 @@ struct alignas(16) TileInfo {
   int keep;        // 1: load without the evict-first hint
   int first;       // 1: first tile of a run
   int last;        // 1: last tile of a run
+  uint32_t tag;    // generation + 1 of the row: stamped on its partial records
 };
 
 struct alignas(16) SoftCtrl {
@@ -233,6 +234,7 @@ __device__ __forceinline__ TileInfo make_tile(const ChainStochParams &P, int gt,
     const int y = __ldg(P.tokens + (size_t)b * K + j);
     if (y >= s0 && y < s0 + it.len) it.yl = y - s0;
   }
+  it.tag = P.gen[-1 - b] + 1u;
   return it;
 }
 
@@ -353,9 +355,14 @@ __global__ void __launch_bounds__(kSoftThreads + 32, 3) softmax_partials_kernel(
   const int hi_a = phase_split(0, pa, B, K, nt, g + 1, G);
   const int lo_b = pa * nt + phase_split(pa, npos, B, K, nt, g, G);
   const int hi_b = pa * nt + phase_split(pa, npos, B, K, nt, g + 1, G);
+  // With an armed workspace only phase A is split statically; the tiles of
+  // phase B are claimed in chunks as CTAs run out of work, so CTAs that
+  // stream faster take more of the tail.
+  const bool dyn = P.dyn != 0 && *reinterpret_cast<volatile const unsigned long long *>(P.magic) == kWsMagic;
+  const int dyn_from = pa * nt;
   const int na = hi_a - lo_a;
-  const int my_tiles = na + (hi_b - lo_b);
-  auto tile_of = [&](int n, int *lo, int *hi) {  // n-th tile of this CTA
+  const int my_tiles = dyn ? na : na + (hi_b - lo_b);  // statically assigned tiles
+  auto tile_of = [&](int n, int *lo, int *hi) {  // n-th static tile of this CTA
     if (n < na) {
       *lo = lo_a;
       *hi = hi_a;
@@ -387,15 +394,18 @@ __global__ void __launch_bounds__(kSoftThreads + 32, 3) softmax_partials_kernel(
     if (lane != 0) return;
     const uint64_t pol_first = l2_policy_evict_first();
     const uint64_t pol_normal = l2_policy_evict_normal();
-    int issued = 0;
-    for (int n = 0; n < my_tiles; ++n) {
-      const int s = n % S;
-      if (n >= S &&
-          !mbar_wait_bounded(&ctl.empty[s], static_cast<uint32_t>(n / S - 1) & 1u, P.wait_limit_ns))
+    int issued = 0;  // stages posted, the end marker included
+    // wait until stage issued % S is free; false once the pipeline is broken
+    auto next_stage = [&]() {
+      const int s = issued % S;
+      if (issued >= S &&
+          !mbar_wait_bounded(&ctl.empty[s], static_cast<uint32_t>(issued / S - 1) & 1u, P.wait_limit_ns))
         ctl.broken = 1;
-      if (*reinterpret_cast<volatile int *>(&ctl.broken)) break;
-      int lo, hi;
-      const int gt = tile_of(n, &lo, &hi);
+      return !*reinterpret_cast<volatile int *>(&ctl.broken);
+    };
+    auto post = [&](int gt, int lo, int hi) {
+      if (!next_stage()) return false;
+      const int s = issued % S;
       const TileInfo it = make_tile<BF16>(P, gt, lo, hi);
       ctl.info[s] = it;
       if (tma) {
@@ -410,6 +420,35 @@ __global__ void __launch_bounds__(kSoftThreads + 32, 3) softmax_partials_kernel(
       } else {
         mbar_arrive(&ctl.full[s]);
       }
+      ++issued;
+      return true;
+    };
+    bool ok = true;
+    for (int n = 0; n < my_tiles && ok; ++n) {
+      int lo, hi;
+      const int gt = tile_of(n, &lo, &hi);
+      ok = post(gt, lo, hi);
+    }
+    if (dyn && ok) {
+      const int total = npos * nt;
+      const int nchunks = (total - dyn_from + P.dyn_chunk - 1) / P.dyn_chunk;
+      // A chunk is claimed only when the previous one is down to its last
+      // tile, so no CTA holds more of the tail than its ring can take; the
+      // claim's round trip overlaps the wait for that tile's stage.
+      uint32_t claim = atomicAdd(P.claim, 1u);
+      while (ok && claim < static_cast<uint32_t>(nchunks)) {
+        const int lo = dyn_from + static_cast<int>(claim) * P.dyn_chunk;
+        const int hi = min(lo + P.dyn_chunk, total);
+        for (int gt = lo; gt < hi && ok; ++gt) {
+          if (gt == hi - 1) claim = atomicAdd(P.claim, 1u);
+          ok = post(gt, lo, hi);
+        }
+      }
+    }
+    if (ok && next_stage()) {  // end marker: a stage with no data
+      const int s = issued % S;
+      ctl.info[s].len = -1;
+      mbar_arrive(&ctl.full[s]);
       ++issued;
     }
     // copies still landing after a give-up: wait (bounded) for the last phase
@@ -428,7 +467,8 @@ __global__ void __launch_bounds__(kSoftThreads + 32, 3) softmax_partials_kernel(
   int s = 0;
   uint32_t parity = 0;
   const uint32_t smem0 = smem_u32(smem);
-  for (int n = 0; n < my_tiles; ++n, s = (s + 1 == S) ? 0 : s + 1, parity ^= (s == 0)) {
+  // Stages arrive in the producer's order until its end marker (len < 0).
+  for (int n = 0;; ++n, s = (s + 1 == S) ? 0 : s + 1, parity ^= (s == 0)) {
     bool timed_out = false;
     if (!*reinterpret_cast<volatile int *>(&ctl.broken)) {
       timed_out = P.force_timeout ? !mbar_wait_bounded(&ctl.never, 0u, P.wait_limit_ns)
@@ -436,14 +476,19 @@ __global__ void __launch_bounds__(kSoftThreads + 32, 3) softmax_partials_kernel(
     } else {
       timed_out = true;  // the pipeline stopped: this tile's data never came
     }
-    // The facts next to the stage are only valid once its barrier completed;
-    // after a give-up the consumer rebuilds them (the stage data is then
-    // garbage but every index stays in bounds, and the row is flagged).
+    timed_out = __any_sync(FULL_MASK, timed_out);
+    // The facts next to the stage are only valid once its barrier completed.
+    // After a give-up a statically assigned tile is rebuilt (the stage data is
+    // then garbage but every index stays in bounds, and the row is flagged); a
+    // claimed tile cannot be named, so the warp stops and that tile's records
+    // keep an old stamp, which the resolve kernel reports as a timeout.
     TileInfo it;
     if (timed_out) {
+      if (n >= my_tiles) break;
       it = rebuild_tile<BF16>(P, n, na, lo_a, hi_a, lo_b, hi_b);
     } else {
       it = ctl.info[s];
+      if (it.len < 0) break;  // end marker
     }
     const bool pair = it.drow >= 0;
     const unsigned char *sb = smem + (size_t)s * P.buf_bytes;
@@ -520,13 +565,14 @@ __global__ void __launch_bounds__(kSoftThreads + 32, 3) softmax_partials_kernel(
         const uint32_t tf = ctl.tflags[slot];
         SoftPart *rp = P.part + (size_t)it.trow * nt;
         SoftPart *rq = pair ? P.part + (size_t)it.drow * nt : nullptr;
+        const float stamp = __uint_as_float(it.tag);
         for (int t = it.run0 + 1 + lane; t <= it.t; t += 32) {
-          rp[t] = SoftPart{-kInf, 0.f, 0.f, 0u};
-          if (pair) rq[t] = SoftPart{-kInf, 0.f, 0.f, 0u};
+          rp[t] = SoftPart{-kInf, 0.f, stamp, 0u};
+          if (pair) rq[t] = SoftPart{-kInf, 0.f, stamp, 0u};
         }
         if (lane == 0) {
-          rp[it.run0] = SoftPart{M1, S1, 0.f, tf};
-          if (pair) rq[it.run0] = SoftPart{M2, S2, 0.f, tf};
+          rp[it.run0] = SoftPart{M1, S1, stamp, tf};
+          if (pair) rq[it.run0] = SoftPart{M2, S2, stamp, tf};
           ctl.arrived[slot] = 0;
           ctl.tflags[slot] = 0;
         }
@@ -559,8 +605,8 @@ __device__ __forceinline__ void cluster_wait() {
 // two >= the tile count, at most 32), one group per logit row; lane l of a
 // group folds tiles l, l+GS, ... in order, then the group folds in a fixed
 // butterfly order.  rstat[r] = (max, sum, draft-token logit, flags).
-__device__ void fold_rows(const ChainStochParams &P, int b, float s2, int warp, int lane,
-                          float4 *rstat) {
+__device__ void fold_rows(const ChainStochParams &P, int b, float s2, uint32_t tag, int warp,
+                          int lane, float4 *rstat) {
   constexpr int NW = kResolveThreads / 32;
   const int K = P.K, npos = K + 1, nt = P.nslices;
   int GS = 1;
@@ -579,6 +625,7 @@ __device__ void fold_rows(const ChainStochParams &P, int b, float s2, int warp, 
       for (int t = sub; t < nt; t += GS) {
         const SoftPart q = P.part[(size_t)prow * nt + t];
         f |= q.flags;
+        if (__float_as_uint(q.stamp) != tag) f |= F_TIMEOUT;  // not written by this call
         const float mn = fmax_nan(m, q.m);
         sacc = (m == -kInf ? 0.f : sacc * ex2(__fmul_rn(m - mn, s2))) +
                (q.m == -kInf ? 0.f : q.s * ex2(__fmul_rn(q.m - mn, s2)));
@@ -710,15 +757,26 @@ __global__ void __launch_bounds__(kResolveThreads, 4) chain_resolve_kernel(const
     }
   }
   const RowScalars first = load_scalars(P, b, lane);
+  // The row's generation: only this row's cluster changes it, at the end of
+  // this kernel; the split barrier below keeps that change after every CTA
+  // of the cluster has read it.
+  const uint32_t gen = *reinterpret_cast<volatile const uint32_t *>(P.gen - 1 - b);
+  cluster_arrive();
   // the stream kernel's partials are visible after this line; nothing above
   // reads them
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  fold_rows(P, b, s2, warp, lane, rstat);
+  if (blockIdx.x == 0 && tid == 0) {  // the stream kernel is done with the claim counter
+    *P.claim = 0u;
+    *P.magic = kWsMagic;
+  }
+  fold_rows(P, b, s2, gen + 1u, warp, lane, rstat);
   __syncthreads();
   if (warp == 0) decide_row(P, b, s2, tflags, lane, crank == 0, rstat, first, ctl);
   __syncthreads();
   const uint32_t flags = ctl.flags;
   const int stop = ctl.stop;
+  cluster_wait();  // every CTA of the cluster has read the generation
+  if (crank == 0 && tid == 0) P.gen[-1 - b] = gen + 1u;
   if (flags) {  // identical in every CTA of the cluster: all leave together
     if (crank == 0 && warp == 0) {
       for (int j = lane; j < npos; j += 32) P.out_tokens[(size_t)b * npos + j] = -1;

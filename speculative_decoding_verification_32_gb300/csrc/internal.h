@@ -10,11 +10,12 @@ namespace sv {
 // One 16-byte partial per (logit row, tile) written by the softmax-partial
 // kernel: a run of consecutive tiles of one row streamed by one CTA leaves its
 // max logit m and sum of exp2((x - m) s2) at the run's first tile and empty
-// partials (m = -inf, s = 0) at its other tiles.
+// partials (m = -inf, s = 0) at its other tiles.  `stamp` holds the bits of
+// the row's generation + 1 at the time of writing.
 struct alignas(16) SoftPart {
   float m;
   float s;
-  float pad;
+  float stamp;
   uint32_t flags;
 };
 
@@ -53,7 +54,26 @@ struct ChainStochParams {
   int vpw;         // resolve kernel: 16-byte vectors per warp (multiple of 32)
   uint64_t wait_limit_ns;
   int force_timeout;
+  // Dynamic tail of the partial kernel.  The workspace ends with a header
+  // {claim counter, -, magic} and, below it, one generation word per row.
+  // When the header holds kWsMagic the tiles of the last phase are claimed in
+  // chunks of dyn_chunk through the counter (the resolve kernel re-arms the
+  // header afterwards); otherwise every tile is assigned statically.  Each
+  // partial record carries its row's generation + 1, which the resolve
+  // kernel checks, so a record this call did not write is never used.
+  uint32_t *claim;
+  unsigned long long *magic;
+  uint32_t *gen;       // gen[-1 - b]: generation word of row b
+  int dyn;             // 0: static assignment only
+  int dyn_chunk;       // tiles per claim
 };
+
+constexpr unsigned long long kWsMagic = 0x5EC7E21F1CA7E5EDull;  // armed workspace header
+// Workspace tail: header (16 bytes) plus one 4-byte generation word per row,
+// with room for the header's 16-byte alignment below an arbitrary end.
+inline size_t ws_tail_bytes(long long B) {
+  return (32 + 4 * static_cast<size_t>(B) + 255) / 256 * 256;
+}
 
 struct GreedyParams {
   const void *target;

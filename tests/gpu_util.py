@@ -55,3 +55,38 @@ def compare_stochastic(g, o, band=BAND):
         np.testing.assert_allclose(g["resid_mass"][rows], o["resid_mass"][rows],
                                    atol=PROB_ATOL, rtol=0)
     return int(mism.sum())
+
+
+def chain_via_abi(L, inp, ws, nbytes=None, diagnostics=True):
+    """spec_verify_chain (stochastic) through the C ABI with the caller's
+    workspace tensor `ws` (uint8, CUDA); returns host arrays."""
+    import ctypes
+    from speculative_decoding_verification_32_gb300._binding import (SPEC_BF16, SPEC_F32,
+                                                                      SPEC_STOCHASTIC,
+                                                                      SpecChainArgs, SpecChainOut)
+    B, K1, V = inp["target"].shape
+    K = K1 - 1
+    dev = ws.device
+    t = {k: cuda(inp.get(k)) for k in ("target", "draft", "draft_tokens", "temperature",
+                                       "u_accept", "u_sample")}
+    out = {k: torch.empty(B, dtype=torch.int32, device=dev)
+           for k in ("accepted_len", "num_emitted", "row_status")}
+    out["out_tokens"] = torch.empty(B, K1, dtype=torch.int32, device=dev)
+    if diagnostics:
+        for k in ("p_at_draft", "q_at_draft", "resid_mass"):
+            out[k] = torch.empty(B, K, dtype=torch.float32, device=dev)
+
+    def ptr(x):
+        return None if x is None else ctypes.c_void_p(x.data_ptr())
+    dt = SPEC_BF16 if inp["target"].dtype == np.uint16 else SPEC_F32
+    a = SpecChainArgs(B, K, V, dt, SPEC_STOCHASTIC, 0.0, ptr(t["target"]), ptr(t["draft"]),
+                      ptr(t["draft_tokens"]), ptr(t["temperature"]), ptr(t["u_accept"]),
+                      ptr(t["u_sample"]))
+    o = SpecChainOut(ptr(out["accepted_len"]), ptr(out["out_tokens"]), ptr(out["num_emitted"]),
+                     ptr(out["row_status"]), ptr(out.get("p_at_draft")),
+                     ptr(out.get("q_at_draft")), ptr(out.get("resid_mass")))
+    stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    rc = L.spec_verify_chain(ctypes.byref(a), ctypes.byref(o), ptr(ws),
+                             ws.numel() if nbytes is None else nbytes, stream)
+    assert rc == 0, L.spec_status_string(rc)
+    return host(out)

@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 from oracle import oracle as O
-from tests.gpu_util import compare_stochastic, cuda, host, run_chain
+from tests.gpu_util import chain_via_abi, compare_stochastic, cuda, host, run_chain
 from tests.util import grid_chain_inputs, log_probs, within_sigma
 from workloads import synthetic as S
 
@@ -239,3 +239,32 @@ def test_bounded_wait_gives_up_and_recovers(sv):
         sv.set_wait_timeout_ns(old)
     g = run_chain(sv, inp)
     compare_stochastic(g, oracle_chain(inp))
+
+
+WS_MAGIC = 0x5EC7E21F1CA7E5ED
+
+
+@pytest.mark.parametrize("name", ["c2", "c3"])
+def test_workspace_first_use_and_reuse(sv, name):
+    """Any workspace works.  On its first call (zero-filled or arbitrary
+    contents) every tile is assigned statically and the call leaves the header
+    at the workspace's end armed; later calls claim the last phase's tiles
+    dynamically.  Every call matches the oracle, and a workspace whose size
+    is not a multiple of 16 keeps its header 16-byte aligned."""
+    import torch
+    from speculative_decoding_verification_32_gb300 import _binding as Bn
+    L = Bn.lib()
+    inp = S.make(name)
+    o = oracle_chain(inp)
+    B, K1, V = inp["target"].shape
+    need = L.spec_verify_chain_workspace_size(B, K1 - 1, V)
+    for fill, extra in ((0, 0), (0xA5, 40), (0xFF, 7)):
+        ws = torch.full((need + extra,), fill, dtype=torch.uint8, device="cuda")
+        end = (need + extra) // 16 * 16
+        for call in range(3):
+            g = chain_via_abi(L, inp, ws)
+            compare_stochastic(g, o)
+            magic = int(ws[end - 8:end].cpu().numpy().view(np.uint64)[0])
+            assert magic == WS_MAGIC, (fill, call, hex(magic))
+            claim = int(ws[end - 16:end - 12].cpu().numpy().view(np.uint32)[0])
+            assert claim == 0  # the resolve kernel left the counter reset
