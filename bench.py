@@ -33,9 +33,9 @@ METRIC = "verify steps/s and achieved HBM GB/s (B=64,K=5,V=128256 bf16) vs 8 TB/
 UNIT = "verify steps/s"
 L2_BYTES = 129 * 1024 * 1024
 # ncu dram__bytes_read.sum + dram__bytes_write.sum of one softmax_partials_kernel
-# launch on this workload (profiles/softmax_partials_c3.md); None until the
-# current kernel has been captured
-TRAFFIC = None
+# launch on this workload (profiles/softmax_partials_chain_c3.md): 180,649,472
+# read + 3,506,944 written; reset to None whenever that kernel changes
+TRAFFIC = 180649472 + 3506944
 # kernels one stochastic spec_verify_chain call enqueues: the stream kernel
 # and the resolve kernel
 KERNELS_PER_STEP = 2

@@ -53,6 +53,11 @@ struct Fmt {
     if constexpr (BF16) return (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]);
     else return __uint_as_float(w[e]);
   }
+  // elements 2i and 2i+1 of a 16-byte vector
+  static __device__ __forceinline__ float2 pair(const uint32_t *w, int i) {
+    if constexpr (BF16) return make_float2(bf16_lo(w[i]), bf16_hi(w[i]));
+    else return make_float2(__uint_as_float(w[2 * i]), __uint_as_float(w[2 * i + 1]));
+  }
   static __device__ __forceinline__ void mask_tail(uint32_t *w, int valid) {
 #pragma unroll
     for (int e = 0; e < EPV; ++e) {
@@ -792,6 +797,8 @@ __global__ void __launch_bounds__(kResolveThreads, 4) chain_resolve_kernel(const
   const float nMp = -__fmul_rn(ctl.Mp, s2), nMq = -__fmul_rn(ctl.Mq, s2);
   const float iSp = __frcp_rn(ctl.Sp), iSq = ctl.Sq > 0.f ? __frcp_rn(ctl.Sq) : 0.f;
   const float u = ctl.u;
+  const float2 s2v = make_float2(s2, s2), nMpv = make_float2(nMp, nMp), nMqv = make_float2(nMq, nMq);
+  const float2 iSpv = make_float2(iSp, iSp), niSqv = make_float2(-iSq, -iSq);
   const int s0 = crank * P.L;
   const int len = max(0, min(V, s0 + P.L) - s0);
   const int nr = P.vpw / 32;  // rounds of 32 vectors per warp
@@ -832,13 +839,18 @@ __global__ void __launch_bounds__(kResolveThreads, 4) chain_resolve_kernel(const
         for (int k = 0; k < 4; ++k) {
           const uint32_t *wp = reinterpret_cast<const uint32_t *>(&vp[k]);
           const uint32_t *wq = reinterpret_cast<const uint32_t *>(&vq[k]);
-          float r = 0.f;
+          // element pairs through packed fp32: the same per-element values
+          // as mass(); only the order of the vector's sum differs
+          float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) {
-            const float pe = ex2(__fmaf_rn(F::elem(wp, e), s2, nMp));
-            const float qe = ex2(__fmaf_rn(F::elem(wq, e), s2, nMq));
-            r += fmaxf(__fmaf_rn(pe, iSp, -__fmul_rn(qe, iSq)), 0.f);
+          for (int i = 0; i < EPV / 2; ++i) {
+            const float2 ap = ffma2(F::pair(wp, i), s2v, nMpv);
+            const float2 aq = ffma2(F::pair(wq, i), s2v, nMqv);
+            const float2 t = fmul2(make_float2(ex2(aq.x), ex2(aq.y)), niSqv);
+            const float2 d = ffma2(make_float2(ex2(ap.x), ex2(ap.y)), iSpv, t);
+            acc = fadd2(acc, make_float2(fmaxf(d.x, 0.f), fmaxf(d.y, 0.f)));
           }
+          const float r = acc.x + acc.y;
           if (k0 + k < nr) rsum[(k0 + k) * NT + tid] = r;
           tsum += r;
         }
@@ -856,9 +868,13 @@ __global__ void __launch_bounds__(kResolveThreads, 4) chain_resolve_kernel(const
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint32_t *wp = reinterpret_cast<const uint32_t *>(&vp[k]);
-          float r = 0.f;
+          float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) r += ex2(__fmaf_rn(F::elem(wp, e), s2, nMp));
+          for (int i = 0; i < EPV / 2; ++i) {
+            const float2 ap = ffma2(F::pair(wp, i), s2v, nMpv);
+            acc = fadd2(acc, make_float2(ex2(ap.x), ex2(ap.y)));
+          }
+          const float r = acc.x + acc.y;
           if (k0 + k < nr) rsum[(k0 + k) * NT + tid] = r;
           tsum += r;
         }
