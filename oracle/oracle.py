@@ -43,6 +43,11 @@ def _bind(L):
     L.so_expected_tokens.restype = f64
     L.so_speedup.argtypes = [f64, i32, f64, f64]
     L.so_speedup.restype = f64
+    ll = ctypes.c_longlong
+    L.so_kv_compact_tree.argtypes = [i32, i32, i32, ll, ll, P, ll, ll, ll, P, P, P, P]
+    L.so_kv_compact_tree.restype = None
+    L.so_adaptive_policy.argtypes = [i32, f64, f64, P, P, P, f64, i32, P, P, P, P, P, P]
+    L.so_adaptive_policy.restype = None
     L.so_max_threads.argtypes = []
     L.so_max_threads.restype = i32
     return L
@@ -151,3 +156,40 @@ def speedup(alpha, gamma, c, g=1.0, L=None):
 
 def max_threads(L=None):
     return (L or lib()).so_max_threads()
+
+
+def kv_compact_tree(kv, kv_len_in, accepted_len, path_nodes, L=None):
+    """Compact the accepted tree path of each row in a copy of `kv`.
+
+    kv: uint8 array [planes, B, S_max, E] (C order); path_nodes: [B, N] int32.
+    Returns (new_kv, row_status)."""
+    kv = np.array(kv, dtype=np.uint8, order="C", copy=True)
+    P_, B, S_max, E = kv.shape
+    path = np.ascontiguousarray(path_nodes, dtype=np.int32)
+    N = path.shape[1]
+    kvl = np.ascontiguousarray(kv_len_in, dtype=np.int32)
+    acc = np.ascontiguousarray(accepted_len, dtype=np.int32)
+    st = np.zeros(B, dtype=np.int32)
+    (L or lib()).so_kv_compact_tree(B, N, P_, S_max, E, _ptr(kv), B * S_max * E, S_max * E, E,
+                                    _ptr(kvl), _ptr(acc), _ptr(path), _ptr(st))
+    return kv, st
+
+
+SHALLOW, DEEP = (3, 4, 4), (7, 1, 8)
+
+
+def adaptive_policy(accepted_len, depth, draft_top1, ema, zero_run, alpha=0.3, divisor=1.0,
+                    lo=SHALLOW, hi=DEEP, start=SHALLOW, ema0=0.0, breaker=5, L=None):
+    """One policy step.  Returns (shape [B,3] int32, new ema, new zero_run)."""
+    acc = np.ascontiguousarray(accepted_len, dtype=np.int32)
+    B = acc.shape[0]
+    dep = np.ascontiguousarray(depth, dtype=np.int32)
+    p1 = np.ascontiguousarray(draft_top1, dtype=np.float32)
+    e = np.array(ema, dtype=np.float64, copy=True)
+    z = np.array(zero_run, dtype=np.int32, copy=True)
+    shape = np.zeros((B, 3), dtype=np.int32)
+    lo_, hi_, st_ = (np.ascontiguousarray(x, dtype=np.int32) for x in (lo, hi, start))
+    (L or lib()).so_adaptive_policy(B, float(alpha), float(divisor), _ptr(lo_), _ptr(hi_),
+                                    _ptr(st_), float(ema0), int(breaker), _ptr(acc), _ptr(dep),
+                                    _ptr(p1), _ptr(e), _ptr(z), _ptr(shape))
+    return shape, e, z

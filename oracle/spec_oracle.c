@@ -461,6 +461,105 @@ void so_rollback_lengths(int B, int max_emit, const int32_t *kv_len_in,
   }
 }
 
+/* ------------------------------------------------------ KV compaction */
+
+/*
+ * so_kv_compact_tree: keep the KV entries of the accepted root path of a
+ * verified draft tree ([DVC] "Speculation needs cache rollback": keep the
+ * cache for the accepted prefix; [SMB] "Where Speculative Decoding
+ * Disappoints": rejected drafts' keys and values must be rewound).
+ *
+ * Cache layout (bytes): entry (plane p, row b, token slot s) starts at
+ * p*plane_stride + b*row_stride + s*tok_stride and is E bytes long.  The
+ * verify pass wrote tree node i of row b at slot kv_len_in[b] + i (node 0 is
+ * the root, the last committed token).  With a = accepted_len[b] and root
+ * path nodes path[b][0..a-1], the entry of path[b][k] moves to slot
+ * kv_len_in[b] + 1 + k.  Defined out of place: all sources are read before
+ * any destination is written.  A row whose path is not strictly increasing
+ * within [1, N), or whose slots leave [0, S_max), is left untouched and gets
+ * status 4; a < 0 (a failed verify) is a no-op with status 0.
+ */
+void so_kv_compact_tree(int B, int N, int planes, long long S_max, long long E,
+                        unsigned char *kv, long long plane_stride, long long row_stride,
+                        long long tok_stride, const int32_t *kv_len_in,
+                        const int32_t *accepted_len, const int32_t *path_nodes,
+                        int32_t *row_status) {
+  unsigned char *tmp = (unsigned char *)malloc((size_t)(E > 0 ? E : 1) * (size_t)(N > 0 ? N : 1));
+  for (int b = 0; b < B; ++b) {
+    const int a = accepted_len[b];
+    const long long base = kv_len_in[b];
+    int ok = 1;
+    if (a > 0) {
+      if (a > N - 1 || base < 0 || base + N > S_max) ok = 0;
+      int prev = 0;
+      for (int k = 0; ok && k < a; ++k) {
+        const int n = path_nodes[(size_t)b * N + k];
+        if (n <= prev || n >= N) ok = 0;
+        prev = n;
+      }
+    }
+    row_status[b] = ok ? 0 : 4;
+    if (!ok || a <= 0) continue;
+    for (int p = 0; p < planes; ++p) {
+      unsigned char *row = kv + (size_t)p * plane_stride + (size_t)b * row_stride;
+      for (int k = 0; k < a; ++k)
+        memcpy(tmp + (size_t)k * E, row + (size_t)(base + path_nodes[(size_t)b * N + k]) * tok_stride, (size_t)E);
+      for (int k = 0; k < a; ++k)
+        memcpy(row + (size_t)(base + 1 + k) * tok_stride, tmp + (size_t)k * E, (size_t)E);
+    }
+  }
+  free(tmp);
+}
+
+/* ------------------------------------------------- AdaptiveSpec tree policy */
+
+/*
+ * so_adaptive_policy: one step of the per-sequence draft-tree shape policy of
+ * [MNW] "Method", dynamic draft tree-shaping.  For each row:
+ *   a       = accepted_len / depth (0 when depth <= 0; clamped to [0, 1]):
+ *             the fraction of the verified draft depth that was accepted
+ *   ema     = alpha * a + (1 - alpha) * ema            (rolling acceptance)
+ *   zero    = accepted_len == 0 ? zero + 1 : 0
+ *   if zero >= breaker: shape = start, ema = ema0, zero = 0  (circuit breaker)
+ *   else: dcs = clamp(p1 * ema / divisor, 0, 1)    (draft confidence score;
+ *         p1 = the draft's top-1 probability, clamped to [0, 1], NaN -> 0)
+ *         shape[i] = floor(lo[i] + dcs * (hi[i] - lo[i]) + 0.5)
+ *   with shape = (nsteps, top-k, ndt), lo = the shallow-wide end and hi = the
+ *   deep-narrow end ((3, 4, 4) and (7, 1, 8) on the page): depth and draft
+ *   tokens grow with dcs, branching with 1 - dcs.
+ * fp64, each operation rounded separately in the order written.
+ */
+void so_adaptive_policy(int B, double alpha, double divisor, const int32_t *lo,
+                        const int32_t *hi, const int32_t *start, double ema0, int breaker,
+                        const int32_t *accepted_len, const int32_t *depth,
+                        const float *draft_top1, double *ema, int32_t *zero_run,
+                        int32_t *shape) {
+  for (int b = 0; b < B; ++b) {
+    double a = 0.0;
+    if (depth[b] > 0) a = (double)accepted_len[b] / (double)depth[b];
+    if (!(a >= 0.0)) a = 0.0;
+    if (a > 1.0) a = 1.0;
+    const double e = alpha * a + (1.0 - alpha) * ema[b];
+    int32_t z = accepted_len[b] == 0 ? zero_run[b] + 1 : 0;
+    if (z >= breaker) {
+      ema[b] = ema0;
+      zero_run[b] = 0;
+      for (int i = 0; i < 3; ++i) shape[(size_t)b * 3 + i] = start[i];
+      continue;
+    }
+    ema[b] = e;
+    zero_run[b] = z;
+    double p1 = (double)draft_top1[b];
+    if (!(p1 >= 0.0)) p1 = 0.0;
+    if (p1 > 1.0) p1 = 1.0;
+    double dcs = p1 * e / divisor;
+    if (!(dcs >= 0.0)) dcs = 0.0;
+    if (dcs > 1.0) dcs = 1.0;
+    for (int i = 0; i < 3; ++i)
+      shape[(size_t)b * 3 + i] = (int32_t)floor((double)lo[i] + dcs * (double)(hi[i] - lo[i]) + 0.5);
+  }
+}
+
 /* ----------------------------------------------------------- cost model */
 
 /* Expected tokens per verification cycle under a constant acceptance rate
