@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="chain", choices=["chain", "kv_compact", "policy"],
+                    help="chain: the headline verify step (default); kv_compact / policy: "
+                         "the post-verification entry points")
     ap.add_argument("--sets", type=int, default=0,
                     help="rotating input sets (0: enough to exceed 3x L2)")
     return ap.parse_args()
@@ -370,8 +373,115 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+def _time_graph(torch, stream, step, n_sets, steps, warmup):
+    """CUDA-event time per step of a graph of n_sets steps replayed."""
+    with torch.cuda.stream(stream):
+        for i in range(n_sets):
+            step(i)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(n_sets):
+            step(i)
+    reps_w, reps = max(1, warmup // n_sets), max(1, steps // n_sets)
+    with torch.cuda.stream(stream):
+        for _ in range(reps_w):
+            graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (reps * n_sets), reps * n_sets, reps_w * n_sets
+
+
+def run_next(args):
+    """Measurements of the post-verification entry points (one GPU)."""
+    import torch
+    import speculative_decoding_verification_32_gb300 as sv
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    peak, peak_kind = peaks()
+    sampler = ClockSampler(0)
+    steps, warmup = min(args.steps, 2000), max(args.warmup, 3)
+    if args.workload == "kv_compact":
+        # paths from verifying the tree workload; a Llama-8B-like cache:
+        # 32 layers x {K, V} planes, 8 KV heads x 128 bf16 per entry
+        inp = S.make("c4")
+        g = sv.spec_verify_tree(to_cuda(inp["target"], dev), to_cuda(inp["parent"], dev),
+                                to_cuda(inp["node_tokens"], dev), margin_kappa=0.3)
+        torch.cuda.synchronize()
+        B, N = inp["parent"].shape
+        planes, S_max, heads, hd = 64, 128, 8, 128
+        E = heads * hd * 2
+        kvl = torch.zeros(B, dtype=torch.int32, device=dev)
+        one = planes * B * S_max * E
+        n_sets = max(2, -(-3 * L2_BYTES // one) + 1)
+        caches = [torch.randint(0, 2 ** 15, (planes, B, S_max, heads, hd), dtype=torch.int16,
+                                device=dev).view(torch.bfloat16) for _ in range(n_sets)]
+        acc = g["accepted_len"].cpu().numpy()
+        moved = int(np.clip(acc, 0, None).sum()) * planes * E * 2  # read + write
+
+        def step(i):
+            sv.spec_kv_compact_tree(caches[i], kvl, g["accepted_len"], g["path_nodes"],
+                                    stream=stream)
+        sampler.start()
+        time.sleep(0.3)
+        ms, n, w = _time_graph(torch, stream, step, n_sets, steps, warmup)
+        clocks = sampler.stop()
+        gbs = moved / (ms / 1e3) / 1e9
+        line = {"metric": "KV path compaction: bytes moved per second", "workload": "kv_compact",
+                "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": n, "warmup": w,
+                "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
+                "data": "synthetic",
+                "config": {"workload": f"tree paths of B={B} N={N} verified trees "
+                                       f"(mean accepted depth {acc.clip(0).mean():.2f}), "
+                                       f"{planes} planes x {E}-byte entries",
+                           "l2": f"{n_sets} rotating caches of {one / 1e6:.0f} MB > L2"},
+                "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                             "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
+                             "kernel": "kv_compact_tree_kernel",
+                             "algorithmic_bytes_per_launch": moved, "traffic": None},
+                "gpu_launches": n, "clocks": clocks}
+    else:
+        B = 4096
+        rng = np.random.default_rng(3)
+        acc = torch.from_numpy(rng.integers(0, 8, B).astype(np.int32)).to(dev)
+        dep = torch.full((B,), 7, dtype=torch.int32, device=dev)
+        p1 = torch.from_numpy(rng.random(B).astype(np.float32)).to(dev)
+        ema = torch.zeros(B, dtype=torch.float64, device=dev)
+        zero = torch.zeros(B, dtype=torch.int32, device=dev)
+
+        def step(i):
+            sv.spec_adaptive_tree_policy(acc, dep, p1, ema, zero, stream=stream)
+        sampler.start()
+        time.sleep(0.3)
+        ms, n, w = _time_graph(torch, stream, step, 8, steps, warmup)
+        clocks = sampler.stop()
+        line = {"metric": "AdaptiveSpec policy steps per second", "workload": "policy",
+                "value": 1e3 / ms, "unit": "policy steps/s", "n_gpus": 1, "steps": n,
+                "warmup": w, "ms_per_step": ms, "higher_is_better": True, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": f"{B} sequences per step"},
+                "roofline": {"bound": "latency", "achieved": None, "peak": None,
+                             "kernel": "adaptive_policy_kernel",
+                             "note": "one thread per sequence; launch and latency bound"},
+                "gpu_launches": n, "clocks": clocks}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
+    if args.workload != "chain":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "workload": args.workload,
+                              "unavailable": "the reference arm covers the headline chain workload only"}))
+            return
+        run_next(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

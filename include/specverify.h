@@ -264,6 +264,90 @@ spec_status spec_rollback_lengths(int32_t B, int32_t max_emit, const int32_t *kv
 
 /* ------------------------------------------------------------------ misc */
 
+/* ------------------------------------------------------- after verification */
+
+/*
+ * spec_kv_compact_tree -- keep the KV-cache entries of each row's accepted
+ * tree path ("Speculative Decoding: Draft, Verify, and Correct", 'Speculation
+ * needs cache rollback': keep the cache for the accepted prefix and discard
+ * the rest; "Speculative Decoding: How a Small Model Speeds Up a Big One",
+ * 'Where Speculative Decoding Disappoints': rejected drafts' keys and values
+ * must be rewound).
+ *
+ * The verify pass wrote tree node i of row b at token slot kv_len_in[b] + i
+ * (node 0 is the root, the last committed token).  With a = accepted_len[b]
+ * and path_nodes[b][0..a-1] as returned by spec_verify_tree, the entry of
+ * path node k moves to slot kv_len_in[b] + 1 + k, in place, in every plane;
+ * spec_rollback_lengths then gives the committed length.  A chain needs no
+ * move (its accepted drafts already sit in order).
+ *
+ * Cache layout, all in bytes: the entry of (plane p, row b, slot s) starts at
+ * kv + p*plane_stride + b*row_stride + s*tok_stride and is entry_bytes long
+ * (for example planes = layers x {K, V}, entry = heads x head_dim x element
+ * size).  kv must be 16-byte aligned and entry_bytes and the three strides
+ * multiples of 16 (else SPEC_ERR_ALIGN).  The moved entries must not overlap
+ * other rows' or planes' entries.
+ *
+ * row_status[b] (optional, device, [B]): 0, or SPEC_ROW_BAD_PARENT when the
+ * path is not strictly increasing within [1, N) or the slots leave
+ * [0, S_max); such a row is left untouched.  a <= 0 is a no-op.
+ * B, planes <= 65535.  Asynchronous on `stream`; no workspace.
+ */
+typedef struct {
+  int32_t B;              /* rows */
+  int32_t N;              /* tree nodes per row, root included: 1..SPEC_MAX_TREE_NODES */
+  int32_t planes;         /* independent planes (layer x K/V, ...) */
+  int32_t pad;
+  int64_t S_max;          /* token slots per row */
+  int64_t entry_bytes;    /* bytes of one token's entry in one plane */
+  int64_t plane_stride;   /* bytes between planes */
+  int64_t row_stride;     /* bytes between rows */
+  int64_t tok_stride;     /* bytes between token slots */
+  void *kv;               /* device, read and written in place */
+  const int32_t *kv_len_in;     /* [B] cache length before the verify pass */
+  const int32_t *accepted_len;  /* [B] from spec_verify_tree */
+  const int32_t *path_nodes;    /* [B, N] from spec_verify_tree */
+} spec_kv_compact_args;
+
+spec_status spec_kv_compact_tree(const spec_kv_compact_args *args, int32_t *row_status,
+                                 void *stream);
+
+/*
+ * spec_adaptive_tree_policy -- one step of the per-sequence draft-tree shape
+ * policy of "Margins, Not Windows: Training-Free Per-Step Lossy Speculative
+ * Decoding" ('Method', dynamic draft tree-shaping), for B sequences at once.
+ * For each row, with the step's accepted_len, the verified draft depth and
+ * the draft's top-1 probability p1 for the next step:
+ *   f    = accepted_len / depth, clamped to [0, 1] (0 if depth <= 0)
+ *   ema  = alpha * f + (1 - alpha) * ema          (alpha = 0.3 on the page)
+ *   zero = accepted_len == 0 ? zero + 1 : 0
+ *   zero >= breaker (5 on the page): shape = start, ema = ema0, zero = 0
+ *   else dcs = min(1, clamp(p1, 0, 1) * ema / divisor) and
+ *        shape[i] = floor(shallow[i] + dcs * (deep[i] - shallow[i]) + 0.5)
+ * with shape = (nsteps, top-k, number of draft tokens).  The page's range is
+ * shallow (3, 4, 4) <-> deep (7, 1, 8).  The page does not print the score's
+ * formula; this product form, saturating through the divisor, is the
+ * plainest reading of its description.  All arithmetic in fp64, each
+ * operation rounded on its own, so results are reproducible bit for bit.
+ * ema [B] (fp64) and zero_run [B] are per-sequence state, read and written;
+ * shape [B, 3] is written.  SPEC_ERR_ARG: alpha outside [0, 1], divisor not
+ * finite and > 0, ema0 not finite, or breaker < 1.
+ */
+typedef struct {
+  double alpha;       /* weight of the newest step in the moving average */
+  double divisor;     /* saturation point of the confidence score */
+  double ema0;        /* moving average after a reset */
+  int32_t shallow[3]; /* (nsteps, top-k, ndt) at score 0 */
+  int32_t deep[3];    /* (nsteps, top-k, ndt) at score 1 */
+  int32_t start[3];   /* shape restored by the circuit breaker */
+  int32_t breaker;    /* consecutive zero-accept steps that trigger it */
+} spec_adaptive_params;
+
+spec_status spec_adaptive_tree_policy(const spec_adaptive_params *params, int32_t B,
+                                      const int32_t *accepted_len, const int32_t *depth,
+                                      const float *draft_top1, double *ema, int32_t *zero_run,
+                                      int32_t *shape, void *stream);
+
 /* Zero-fill a workspace on `stream` (a cudaMemsetAsync).  Optional: the
  * verify calls do not need a zeroed workspace. */
 spec_status spec_workspace_init(void *ws, size_t ws_bytes, void *stream);

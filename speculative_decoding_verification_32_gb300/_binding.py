@@ -46,6 +46,19 @@ class SpecTreeOut(_c.Structure):
                 ("num_emitted", _P), ("row_status", _P)]
 
 
+class SpecKvCompactArgs(_c.Structure):
+    _fields_ = [("B", _c.c_int32), ("N", _c.c_int32), ("planes", _c.c_int32), ("pad", _c.c_int32),
+                ("S_max", _c.c_int64), ("entry_bytes", _c.c_int64), ("plane_stride", _c.c_int64),
+                ("row_stride", _c.c_int64), ("tok_stride", _c.c_int64), ("kv", _P),
+                ("kv_len_in", _P), ("accepted_len", _P), ("path_nodes", _P)]
+
+
+class SpecAdaptiveParams(_c.Structure):
+    _fields_ = [("alpha", _c.c_double), ("divisor", _c.c_double), ("ema0", _c.c_double),
+                ("shallow", _c.c_int32 * 3), ("deep", _c.c_int32 * 3), ("start", _c.c_int32 * 3),
+                ("breaker", _c.c_int32)]
+
+
 class SpecError(RuntimeError):
     """A spec_* entry point returned a non-zero spec_status."""
 
@@ -85,6 +98,11 @@ def _bind(L):
     L.spec_verify_chain_static.restype = _c.c_int
     L.spec_verify_tree.argtypes = [_c.POINTER(SpecTreeArgs), _c.POINTER(SpecTreeOut), _P, sz, _P]
     L.spec_verify_tree.restype = _c.c_int
+    L.spec_kv_compact_tree.argtypes = [_c.POINTER(SpecKvCompactArgs), _P, _P]
+    L.spec_kv_compact_tree.restype = _c.c_int
+    L.spec_adaptive_tree_policy.argtypes = [_c.POINTER(SpecAdaptiveParams), i32, _P, _P, _P, _P,
+                                            _P, _P, _P]
+    L.spec_adaptive_tree_policy.restype = _c.c_int
     L.spec_rollback_lengths.argtypes = [i32, i32, _P, _P, _P, _P, i32, _P, _P, _P, _P]
     L.spec_rollback_lengths.restype = _c.c_int
     L.spec_workspace_init.argtypes = [_P, sz, _P]
@@ -250,6 +268,52 @@ def spec_rollback_lengths(kv_len_in, accepted_len, num_emitted, out_tokens, eos_
                                        _ptr(num_emitted), _ptr(out_tokens), int(eos_id),
                                        _ptr(max_len), _ptr(committed), _ptr(n_out), sp))
     return committed, n_out
+
+
+def spec_kv_compact_tree(kv, kv_len_in, accepted_len, path_nodes, stream=None):
+    """Compact each row's accepted tree path in place (see spec_kv_compact_tree
+    in include/specverify.h).
+
+    kv: a CUDA tensor [planes, B, S_max, ...] whose trailing dimensions form
+    one token's entry (contiguous, any dtype); path_nodes [B, N] int32.
+    Returns row_status [B] int32.
+    """
+    dev = kv.device
+    if not kv.is_contiguous() or kv.dim() < 3:
+        raise ValueError("kv must be a contiguous [planes, B, S_max, ...] tensor")
+    for t, n in ((kv_len_in, "kv_len_in"), (accepted_len, "accepted_len"),
+                 (path_nodes, "path_nodes")):
+        _req(t, n, dev, torch.int32)
+    planes, B, S_max = kv.shape[:3]
+    E = kv[0, 0, 0].numel() * kv.element_size() if kv.numel() else 0
+    status = torch.empty(B, dtype=torch.int32, device=dev)
+    a = SpecKvCompactArgs(B, path_nodes.shape[1], planes, 0, S_max, E, B * S_max * E, S_max * E, E,
+                          _ptr(kv), _ptr(kv_len_in), _ptr(accepted_len), _ptr(path_nodes))
+    _, sp = _stream(dev, stream)
+    _check(lib().spec_kv_compact_tree(_c.byref(a), _ptr(status), sp))
+    return status
+
+
+def spec_adaptive_tree_policy(accepted_len, depth, draft_top1, ema, zero_run, alpha=0.3,
+                              divisor=1.0, shallow=(3, 4, 4), deep=(7, 1, 8), start=(3, 4, 4),
+                              ema0=0.0, breaker=5, stream=None):
+    """One policy step for B sequences (see spec_adaptive_tree_policy in
+    include/specverify.h).  ema (float64) and zero_run (int32) are updated in
+    place; returns shape [B, 3] int32 = (nsteps, top-k, ndt)."""
+    dev = accepted_len.device
+    for t, n, dt in ((accepted_len, "accepted_len", torch.int32), (depth, "depth", torch.int32),
+                     (draft_top1, "draft_top1", torch.float32), (ema, "ema", torch.float64),
+                     (zero_run, "zero_run", torch.int32)):
+        _req(t, n, dev, dt)
+    B = accepted_len.shape[0]
+    shape = torch.empty(B, 3, dtype=torch.int32, device=dev)
+    q = SpecAdaptiveParams(float(alpha), float(divisor), float(ema0), (_c.c_int32 * 3)(*shallow),
+                           (_c.c_int32 * 3)(*deep), (_c.c_int32 * 3)(*start), int(breaker))
+    _, sp = _stream(dev, stream)
+    _check(lib().spec_adaptive_tree_policy(_c.byref(q), B, _ptr(accepted_len), _ptr(depth),
+                                           _ptr(draft_top1), _ptr(ema), _ptr(zero_run),
+                                           _ptr(shape), sp))
+    return shape
 
 
 def set_wait_timeout_ns(ns):

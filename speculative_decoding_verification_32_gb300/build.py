@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspecverify.so")
-SOURCES = ["api.cu", "chain_stochastic.cu", "greedy.cu", "rollback.cu"]
+SOURCES = ["api.cu", "chain_stochastic.cu", "greedy.cu", "rollback.cu", "kv_policy.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -153,3 +153,39 @@ def test_product_path_never_imports_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "spec_oracle" not in text and "so_verify" not in text, f
+
+
+def test_kv_compact_and_policy_argument_errors(L):
+    from speculative_decoding_verification_32_gb300._binding import (SpecAdaptiveParams,
+                                                                      SpecKvCompactArgs)
+    b = 0x10000000
+    p = _fake(b)
+
+    def kv(B=2, N=8, planes=2, E=256, kvp=b, ts=256):
+        return SpecKvCompactArgs(B, N, planes, 0, 64, E, 2 * 64 * E, 64 * E, ts, _fake(kvp),
+                                 p, p, p)
+    assert L.spec_kv_compact_tree(None, None, None) == 1
+    assert L.spec_kv_compact_tree(ctypes.byref(kv(N=0)), None, None) == 2
+    assert L.spec_kv_compact_tree(ctypes.byref(kv(B=-1)), None, None) == 2
+    assert L.spec_kv_compact_tree(ctypes.byref(kv(kvp=b + 8)), None, None) == 4
+    assert L.spec_kv_compact_tree(ctypes.byref(kv(E=24)), None, None) == 4
+    assert L.spec_kv_compact_tree(ctypes.byref(kv(ts=100)), None, None) == 4
+    a = kv()
+    a.path_nodes = None
+    assert L.spec_kv_compact_tree(ctypes.byref(a), None, None) == 1
+    assert L.spec_kv_compact_tree(ctypes.byref(kv(B=0)), None, None) == 0
+
+    def par(alpha=0.3, d=1.0, e0=0.0, brk=5):
+        t3 = ctypes.c_int32 * 3
+        return SpecAdaptiveParams(alpha, d, e0, t3(3, 4, 4), t3(7, 1, 8), t3(3, 4, 4), brk)
+    args = (p, p, p, p, p, p, None)
+    assert L.spec_adaptive_tree_policy(None, 4, *args) == 1
+    assert L.spec_adaptive_tree_policy(ctypes.byref(par()), -1, *args) == 2
+    assert L.spec_adaptive_tree_policy(ctypes.byref(par(alpha=1.5)), 4, *args) == 5
+    assert L.spec_adaptive_tree_policy(ctypes.byref(par(d=0.0)), 4, *args) == 5
+    assert L.spec_adaptive_tree_policy(ctypes.byref(par(d=float("inf"))), 4, *args) == 5
+    assert L.spec_adaptive_tree_policy(ctypes.byref(par(brk=0)), 4, *args) == 5
+    assert L.spec_adaptive_tree_policy(ctypes.byref(par()), 4, None, p, p, p, p, p, None) == 1
+    assert L.spec_adaptive_tree_policy(ctypes.byref(par()), 4, p, p, p, _fake(b + 4), p, p,
+                                       None) == 4  # ema needs 8-byte alignment
+    assert L.spec_adaptive_tree_policy(ctypes.byref(par()), 0, *args) == 0
