@@ -48,6 +48,8 @@ def _bind(L):
     L.so_kv_compact_tree.restype = None
     L.so_adaptive_policy.argtypes = [i32, f64, f64, P, P, P, f64, i32, P, P, P, P, P, P]
     L.so_adaptive_policy.restype = None
+    L.so_drift_residuals.argtypes = [i32, i32, i32, i32, P, P, P, i32, P, P, P, i32]
+    L.so_drift_residuals.restype = None
     L.so_max_threads.argtypes = []
     L.so_max_threads.restype = i32
     return L
@@ -193,3 +195,21 @@ def adaptive_policy(accepted_len, depth, draft_top1, ema, zero_run, alpha=0.3, d
                                     _ptr(st_), float(ema0), int(breaker), _ptr(acc), _ptr(dep),
                                     _ptr(p1), _ptr(e), _ptr(z), _ptr(shape))
     return shape, e, z
+
+
+def drift_residuals(target, draft, temperature=None, m=32, nthreads=0, L=None):
+    """Top-m target support and log p - log q on it at every drafted position.
+
+    target [B,K+1,V], draft [B,K,V] (float32, or bf16 as uint16 bits).
+    Returns (support [B,K,m] int32, residual [B,K,m] float32, row_status [B])."""
+    t, dt = _logits(target)
+    d, _ = _logits(draft)
+    B, K1, V = t.shape
+    K = K1 - 1
+    temp = None if temperature is None else np.ascontiguousarray(temperature, dtype=np.float32)
+    sup = np.zeros((B, K, m), dtype=np.int32)
+    res = np.zeros((B, K, m), dtype=np.float32)
+    st = np.zeros(B, dtype=np.int32)
+    (L or lib()).so_drift_residuals(B, K, V, dt, _ptr(t), _ptr(d), _ptr(temp), int(m), _ptr(sup),
+                                    _ptr(res), _ptr(st), int(nthreads))
+    return sup, res, st

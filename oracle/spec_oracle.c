@@ -461,6 +461,102 @@ void so_rollback_lengths(int B, int max_emit, const int32_t *kv_len_in,
   }
 }
 
+/* -------------------------------------------------- DRIFT residuals */
+
+/*
+ * so_drift_residuals: the free supervision signal of [DRIFT] "DRIFT:
+ * Gradient-Free Draft Recalibration From Verification Feedback" (the residual
+ * paragraph): at every drafted position j < K of row b, restrict the target
+ * and draft distributions to a shared support of m tokens and take the
+ * target log-probability minus the draft log-probability there.
+ * Reading: the support is the m tokens of highest target probability (ties
+ * to the lower index), listed in that order; the log-probabilities are those
+ * of the full temperature-scaled distributions, natural log.  A draft
+ * probability of 0 (a masked logit) gives +inf.  Rows failing the input
+ * checks (status 1, 5 or 7, as in verification) get support -1 and NaN.
+ * support [B*K*m] int32, residual [B*K*m] float, row_status [B].
+ */
+void so_drift_residuals(int B, int K, int V, int dtype, const void *target, const void *draft,
+                        const float *temperature, int m, int32_t *support, float *residual,
+                        int32_t *row_status, int nthreads) {
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (int b = 0; b < B; ++b) {
+    const double T = temperature ? (double)temperature[b] : 1.0;
+    unsigned flags = 0;
+    if (!(T > 0.0) || isinf(T)) flags |= 1u << O_ROW_BAD_TEMPERATURE;
+    for (int j = 0; j < K; ++j) {
+      flags |= row_flags(target, dtype, ((size_t)b * (K + 1) + j) * (size_t)V, V);
+      flags |= row_flags(draft, dtype, ((size_t)b * K + j) * (size_t)V, V);
+    }
+    row_status[b] = lowest_code(flags);
+    unsigned char *taken = (unsigned char *)calloc((size_t)V, 1);
+    double *lp = (double *)malloc(sizeof(double) * (size_t)V);
+    double *lq = (double *)malloc(sizeof(double) * (size_t)V);
+    for (int j = 0; j < K; ++j) {
+      int32_t *sup = support + ((size_t)b * K + j) * (size_t)m;
+      float *res = residual + ((size_t)b * K + j) * (size_t)m;
+      if (flags) {
+        for (int i = 0; i < m; ++i) {
+          sup[i] = -1;
+          res[i] = NAN;
+        }
+        continue;
+      }
+      const size_t to = ((size_t)b * (K + 1) + j) * (size_t)V;
+      const size_t dof = ((size_t)b * K + j) * (size_t)V;
+      /* log-softmax of l / T, each: x = l / T, m = max x, log S = log sum exp(x - m) */
+      for (int pass = 0; pass < 2; ++pass) {
+        const void *base = pass == 0 ? target : draft;
+        const size_t off = pass == 0 ? to : dof;
+        double *out = pass == 0 ? lp : lq;
+        double mx = -INFINITY;
+        for (int v = 0; v < V; ++v) {
+          const double x = logit_at(base, dtype, off + (size_t)v) / T;
+          if (x > mx) mx = x;
+        }
+        double S = 0.0;
+        for (int v = 0; v < V; ++v) {
+          const double x = logit_at(base, dtype, off + (size_t)v) / T;
+          if (x != -INFINITY) S += exp(x - mx);
+        }
+        const double lS = log(S);
+        for (int v = 0; v < V; ++v) {
+          const double x = logit_at(base, dtype, off + (size_t)v) / T;
+          out[v] = x == -INFINITY ? -INFINITY : (x - mx) - lS;
+        }
+      }
+      /* the m largest target logits, one scan per rank, lower index first */
+      memset(taken, 0, (size_t)V);
+      for (int i = 0; i < m; ++i) {
+        int best = -1;
+        double bv = 0.0;
+        for (int v = 0; v < V; ++v) {
+          if (taken[v]) continue;
+          const double x = logit_at(target, dtype, to + (size_t)v);
+          if (best < 0 || x > bv) {
+            best = v;
+            bv = x;
+          }
+        }
+        if (best < 0) { /* m > V */
+          sup[i] = -1;
+          res[i] = NAN;
+          continue;
+        }
+        taken[best] = 1;
+        sup[i] = best;
+        res[i] = (float)(lp[best] - lq[best]);
+      }
+    }
+    free(taken);
+    free(lp);
+    free(lq);
+  }
+}
+
 /* ------------------------------------------------------ KV compaction */
 
 /*

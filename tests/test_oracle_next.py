@@ -117,3 +117,60 @@ def test_kv_compaction_rejects_bad_paths_and_skips_failed_rows():
     out, st = O.kv_compact_tree(kv, [14, 0, 0, 0], [1, -1, 0, 0], np.tile([[1, 2, 3, 0]], (4, 1)))
     assert st.tolist() == [4, 0, 0, 0]  # slots past S_max; a < 0 is a no-op
     assert np.array_equal(out, kv)
+
+
+# ------------------------------------------------------- DRIFT residuals
+def _log_softmax(x):
+    from scipy.special import logsumexp
+    return x - logsumexp(x)
+
+
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_drift_residual_closed_form(T):
+    """Draft logits a * target: log q is log_softmax(a l / T), computed here by
+    scipy's logsumexp; the support is the top-m of the target by a stable
+    lexsort (ties to the lower index)."""
+    rng = np.random.default_rng(3)
+    B, K, V, m = 2, 3, 500, 32
+    tgt = (rng.normal(0, 3, (B, K + 1, V))).astype(np.float32)
+    tgt[0, 0, 10:20] = tgt[0, 0, 7]  # a run of ties inside the support
+    tgt[0, 0, 7] = tgt[0, 0].max() + 1.0
+    tgt[0, 0, 10:20] = tgt[0, 0, 7] - 0.5
+    drf = (0.6 * tgt[:, :K]).astype(np.float32)
+    sup, res, st = O.drift_residuals(tgt, drf, np.full(B, T, np.float32), m=m)
+    assert np.all(st == 0)
+    for b in range(B):
+        for j in range(K):
+            l = tgt[b, j].astype(np.float64)
+            order = np.lexsort((np.arange(V), -l))[:m]
+            assert np.array_equal(sup[b, j], order)
+            lp = _log_softmax(l / T)
+            lq = _log_softmax(drf[b, j].astype(np.float64) / T)
+            np.testing.assert_allclose(res[b, j], (lp - lq)[order], rtol=0, atol=1e-5)
+    assert sup[0, 0, 0] == 7 and list(sup[0, 0, 1:11]) == list(range(10, 20))
+
+
+def test_drift_residual_identical_laws_and_masks():
+    """draft = target + c: q = p, so the residual is 0; a masked draft logit
+    inside the support gives +inf."""
+    rng = np.random.default_rng(4)
+    tgt = rng.normal(0, 2, (1, 3, 300)).astype(np.float32)
+    drf = (tgt[:, :2] + 3.0).astype(np.float32)
+    sup, res, _ = O.drift_residuals(tgt, drf, m=16)
+    assert np.all(np.abs(res) < 1e-12 + 1e-6)
+    drf[0, 1, sup[0, 1, 3]] = -np.inf
+    sup2, res2, st = O.drift_residuals(tgt, drf, m=16)
+    assert st[0] == 0 and np.array_equal(sup2, sup)
+    assert res2[0, 1, 3] == np.inf and np.isfinite(np.delete(res2[0, 1], 3)).all()
+
+
+def test_drift_residual_bad_rows():
+    tgt = np.zeros((2, 2, 40), np.float32)
+    drf = np.zeros((2, 1, 40), np.float32)
+    tgt[1, 0, 5] = np.nan
+    sup, res, st = O.drift_residuals(tgt, drf, np.array([1.0, 1.0], np.float32), m=4)
+    assert st.tolist() == [0, 1]
+    assert np.all(sup[1] == -1) and np.all(np.isnan(res[1]))
+    assert sup[0, 0].tolist() == [0, 1, 2, 3]  # all equal: lowest indices
+    _, _, st = O.drift_residuals(tgt, drf, np.array([0.0, 1.0], np.float32), m=4)
+    assert st[0] == 7
