@@ -50,7 +50,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="chain", choices=["chain", "kv_compact", "policy"],
+    ap.add_argument("--workload", default="chain",
+                    choices=["chain", "kv_compact", "policy", "drift"],
                     help="chain: the headline verify step (default); kv_compact / policy: "
                          "the post-verification entry points")
     ap.add_argument("--sets", type=int, default=0,
@@ -447,6 +448,37 @@ def run_next(args):
                              "kernel": "kv_compact_tree_kernel",
                              "algorithmic_bytes_per_launch": moved, "traffic": None},
                 "gpu_launches": n, "clocks": clocks}
+    elif args.workload == "drift":
+        # top-32 DRIFT residuals on the headline chain workload
+        inp = S.make(WORKLOAD)
+        B, K = inp["draft_tokens"].shape
+        V = inp["target"].shape[-1]
+        m = 32
+        step_bytes = inp["target"].nbytes + inp["draft"].nbytes
+        n_sets = max(2, -(-3 * L2_BYTES // step_bytes) + 1)
+        tgt0, drf0 = to_cuda(inp["target"], dev), to_cuda(inp["draft"], dev)
+        sets = [(tgt0, drf0)] + [(tgt0.clone(), drf0.clone()) for _ in range(n_sets - 1)]
+        temp = to_cuda(inp["temperature"], dev)
+        alg = 2 * B * K * V * 2  # target rows at drafted positions + draft rows, bf16
+
+        def step(i):
+            sv.spec_drift_residuals(sets[i][0], sets[i][1], temp, m=m, stream=stream)
+        sampler.start()
+        time.sleep(0.3)
+        ms, n, w = _time_graph(torch, stream, step, n_sets, steps, warmup)
+        clocks = sampler.stop()
+        gbs = alg / (ms / 1e3) / 1e9
+        line = {"metric": "DRIFT residual extraction steps/s (top-32 support per drafted position)",
+                "workload": "drift", "value": 1e3 / ms, "unit": "steps/s", "n_gpus": 1,
+                "steps": n, "warmup": w, "ms_per_step": ms, "higher_is_better": True,
+                "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": f"chain B={B} K={K} V={V} bf16, m={m}",
+                           "l2": f"{n_sets} rotating input sets > L2"},
+                "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                             "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
+                             "kernel": "softmax_partials_kernel + drift_select_kernel",
+                             "algorithmic_bytes_per_launch": alg, "traffic": None},
+                "gpu_launches": 2 * n, "clocks": clocks}
     else:
         B = 4096
         rng = np.random.default_rng(3)

@@ -264,6 +264,32 @@ spec_status spec_rollback_lengths(int32_t B, int32_t max_emit, const int32_t *kv
 
 /* ------------------------------------------------------------------ misc */
 
+/*
+ * spec_drift_residuals -- the free supervision signal of "Speculative
+ * Decoding Under Distribution Shift: DRIFT Recalibration" (the residual
+ * paragraph of its method): at every drafted position j < K of row b, the m
+ * tokens of highest target probability (ties to the lower token id), in
+ * that order, and the target minus the draft log-probability on them, in
+ * nats, from the full temperature-scaled distributions (p and q as in
+ * spec_verify_chain).  The page's "shared top m tokens" is read as the
+ * target's top m.  A masked (-inf) draft logit gives +inf.
+ *
+ * Reads target_logits, draft_logits, temperature, B, K, V and dtype of
+ * `args` (the rest is ignored; draft_tokens may be NULL).  K <= 64,
+ * 1 <= m <= 64 and m <= V (else SPEC_ERR_SHAPE / SPEC_ERR_ARG), B <= 65535.
+ * support [B, K, m] int32, residual [B, K, m] float32, row_status [B]
+ * (device, caller-owned): a row with a non-finite logit, no finite logit or
+ * a bad temperature at any drafted position gets its code and support -1,
+ * residual NaN.  The workspace is spec_verify_chain's (same size function).
+ * Two kernels: the stream kernel of the chain verifier, then one CTA per
+ * drafted position that selects the support by radix selection on the
+ * target logits.  Residuals carry fp32 rounding: agreement with an exact
+ * computation is within about 1e-4 nats for logits of magnitude up to ~50/T.
+ */
+spec_status spec_drift_residuals(const spec_chain_args *args, int32_t m, int32_t *support,
+                                 float *residual, int32_t *row_status, void *ws, size_t ws_bytes,
+                                 void *stream);
+
 /* ------------------------------------------------------- after verification */
 
 /*

@@ -514,18 +514,18 @@ void so_drift_residuals(int B, int K, int V, int dtype, const void *target, cons
         double *out = pass == 0 ? lp : lq;
         double mx = -INFINITY;
         for (int v = 0; v < V; ++v) {
-          const double x = logit_at(base, dtype, off + (size_t)v) / T;
-          if (x > mx) mx = x;
+          const double xs = logit_at(base, dtype, off + (size_t)v) / T;
+          if (xs > mx) mx = xs;
         }
         double S = 0.0;
         for (int v = 0; v < V; ++v) {
-          const double x = logit_at(base, dtype, off + (size_t)v) / T;
-          if (x != -INFINITY) S += exp(x - mx);
+          const double xs = logit_at(base, dtype, off + (size_t)v) / T;
+          if (xs != -INFINITY) S += exp(xs - mx);
         }
         const double lS = log(S);
         for (int v = 0; v < V; ++v) {
-          const double x = logit_at(base, dtype, off + (size_t)v) / T;
-          out[v] = x == -INFINITY ? -INFINITY : (x - mx) - lS;
+          const double xs = logit_at(base, dtype, off + (size_t)v) / T;
+          out[v] = xs == -INFINITY ? -INFINITY : (xs - mx) - lS;
         }
       }
       /* the m largest target logits, one scan per rank, lower index first */

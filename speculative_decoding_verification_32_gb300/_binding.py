@@ -98,6 +98,8 @@ def _bind(L):
     L.spec_verify_chain_static.restype = _c.c_int
     L.spec_verify_tree.argtypes = [_c.POINTER(SpecTreeArgs), _c.POINTER(SpecTreeOut), _P, sz, _P]
     L.spec_verify_tree.restype = _c.c_int
+    L.spec_drift_residuals.argtypes = [_c.POINTER(SpecChainArgs), i32, _P, _P, _P, _P, sz, _P]
+    L.spec_drift_residuals.restype = _c.c_int
     L.spec_kv_compact_tree.argtypes = [_c.POINTER(SpecKvCompactArgs), _P, _P]
     L.spec_kv_compact_tree.restype = _c.c_int
     L.spec_adaptive_tree_policy.argtypes = [_c.POINTER(SpecAdaptiveParams), i32, _P, _P, _P, _P,
@@ -268,6 +270,31 @@ def spec_rollback_lengths(kv_len_in, accepted_len, num_emitted, out_tokens, eos_
                                        _ptr(num_emitted), _ptr(out_tokens), int(eos_id),
                                        _ptr(max_len), _ptr(committed), _ptr(n_out), sp))
     return committed, n_out
+
+
+def spec_drift_residuals(target_logits, draft_logits, temperature=None, m=32, stream=None):
+    """Top-m target support and log p - log q on it at every drafted position
+    (see spec_drift_residuals in include/specverify.h).  Returns (support
+    [B,K,m] int32, residual [B,K,m] float32, row_status [B] int32)."""
+    dev = target_logits.device
+    _req(target_logits, "target_logits", dev)
+    _req(draft_logits, "draft_logits", dev, target_logits.dtype)
+    _req(temperature, "temperature", dev, torch.float32)
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    sup = torch.empty(B, K, m, dtype=torch.int32, device=dev)
+    res = torch.empty(B, K, m, dtype=torch.float32, device=dev)
+    st = torch.empty(B, dtype=torch.int32, device=dev)
+    args = SpecChainArgs(B, K, V, _dtype_code(target_logits), SPEC_STOCHASTIC, 0.0,
+                         _ptr(target_logits), _ptr(draft_logits), None, _ptr(temperature),
+                         None, None)
+    L = lib()
+    nbytes = L.spec_verify_chain_workspace_size(B, K, V)
+    s, sp = _stream(dev, stream)
+    ws = workspace(dev, nbytes, s.cuda_stream)
+    _check(L.spec_drift_residuals(_c.byref(args), int(m), _ptr(sup), _ptr(res), _ptr(st),
+                                  _ptr(ws), ws.numel(), sp))
+    return sup, res, st
 
 
 def spec_kv_compact_tree(kv, kv_len_in, accepted_len, path_nodes, stream=None):

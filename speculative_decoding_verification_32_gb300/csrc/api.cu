@@ -155,6 +155,95 @@ spec_status run_greedy(GreedyParams &p, bool bf16, int esz, void *ws, cudaStream
   return SPEC_OK;
 }
 
+// Parameters and launch shapes of the stochastic stream kernel and of the
+// resolve kernel's cluster split, from the arguments and the workspace;
+// output pointers are left for the caller.
+spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes, ChainStochParams &p,
+                             int &grid, size_t &smem, int &nv, int &C) {
+  const int K = a->K;
+  const int esz = a->dtype == SPEC_BF16 ? 2 : 4;
+  const bool bf16 = a->dtype == SPEC_BF16;
+  int dev;
+  DevInfo di;
+  if (device_info(&dev, &di) != cudaSuccess) return SPEC_ERR_CUDA;
+  const int epv = 16 / esz;
+  p = ChainStochParams{};
+  p.target = a->target_logits;
+  p.draft = a->draft_logits;
+  p.tokens = a->draft_tokens;
+  p.temperature = a->temperature;
+  p.u_accept = a->u_accept;
+  p.u_sample = a->u_sample;
+  p.part = static_cast<SoftPart *>(ws);
+  p.B = a->B;
+  p.K = K;
+  p.V = a->V;
+  p.use_tma = aligned(a->target_logits, 16) && (K == 0 || aligned(a->draft_logits, 16)) &&
+              (static_cast<long long>(a->V) * esz) % 16 == 0;
+  p.wait_limit_ns = g_wait_ns.load();
+  p.force_timeout = g_force_timeout.load();
+  {
+    // workspace tail: header {claim, -, magic} in the last 16 bytes, one
+    // generation word per row below it
+    char *end = static_cast<char *>(ws) + (ws_bytes & ~static_cast<size_t>(15));
+    p.claim = reinterpret_cast<uint32_t *>(end - 16);
+    p.magic = reinterpret_cast<unsigned long long *>(end - 8);
+    p.gen = reinterpret_cast<uint32_t *>(end - 16);
+    // SPECVERIFY_DYNAMIC=0 keeps every tile statically assigned;
+    // SPECVERIFY_DYN_CHUNK sets the tiles per claim (tuning)
+    const char *dv = std::getenv("SPECVERIFY_DYNAMIC");
+    p.dyn = !(dv && *dv == '0');
+    p.dyn_chunk = 2;
+    if (const char *dc = std::getenv("SPECVERIFY_DYN_CHUNK")) {
+      const int c = std::atoi(dc);
+      if (c >= 1 && c <= 64) p.dyn_chunk = c;
+    }
+  }
+  // stream kernel: fixed-size items (16 or 32 KB), a bulk-copy ring per CTA;
+  // SPECVERIFY_SOFT_VECS (4 or 8) and SPECVERIFY_SOFT_STAGES (2..4) override
+  // the defaults for tuning
+  nv = kSoftVecs;
+  if (const char *ov = std::getenv("SPECVERIFY_SOFT_VECS")) nv = std::atoi(ov) == 8 ? 8 : 4;
+  p.slice = kSoftThreads * nv * epv;
+  p.nslices = ceil_div(a->V, p.slice);
+  p.buf_bytes = 2 * p.slice * esz;  // target tile + draft tile
+  p.stages = kSoftStages;
+  if (const char *ov = std::getenv("SPECVERIFY_SOFT_STAGES")) {
+    const int st = std::atoi(ov);
+    if (st >= 2 && st <= 4) p.stages = st;
+  }
+  smem = static_cast<size_t>(p.stages) * p.buf_bytes + kSoftCtrlBytes;
+  {
+    const size_t rows = static_cast<size_t>(a->B) * (K + 1) + static_cast<size_t>(a->B) * K;
+    p.ylog = reinterpret_cast<float *>(static_cast<char *>(ws) +
+                                       align_up(rows * p.nslices * sizeof(SoftPart), 256));
+  }
+  int per_sm = 0;
+  if (soft_blocks(dev, bf16, nv, smem, &per_sm) != cudaSuccess || per_sm < 1) return SPEC_ERR_CUDA;
+  const long long tiles = (static_cast<long long>(a->B) * (K + 1) + static_cast<long long>(a->B) * K) * p.nslices;
+  grid = static_cast<int>(std::min<long long>(tiles, static_cast<long long>(di.sms) * per_sm));
+  // resolve kernel: a cluster of C CTAs per row, at most 16 rounds of 32
+  // vectors per warp
+  constexpr int kRW = kResolveThreads / 32;
+  auto rounds = [&](int c) {
+    const int L = static_cast<int>(align_up(static_cast<size_t>(ceil_div(a->V, c)), static_cast<size_t>(epv)));
+    return ceil_div(ceil_div(ceil_div(L, epv), kRW), 32);
+  };
+  C = 1;
+  while (C < 16 && rounds(C) > kResolveMaxRounds) C *= 2;
+  if (rounds(C) > kResolveMaxRounds) return SPEC_ERR_SHAPE;
+  while (C < 8 && ceil_div(a->V, 2 * C) >= 2048) C *= 2;  // spread each row's work
+  if (const char *ov = std::getenv("SPECVERIFY_CLUSTER")) {  // tuning override
+    const int c = std::atoi(ov);
+    if (c >= C && c <= 16 && (c & (c - 1)) == 0) C = c;
+  }
+  p.L = static_cast<int>(align_up(static_cast<size_t>(ceil_div(a->V, C)), static_cast<size_t>(epv)));
+  p.vpw = 32 * rounds(C);
+  report("stochastic slice nslices stages grid per_sm cluster L", p.slice, p.nslices, p.stages,
+         grid, per_sm, C, p.L);
+  return SPEC_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -227,17 +316,13 @@ spec_status spec_verify_chain(const spec_chain_args *a, const spec_chain_out *o,
     return run_greedy(p, bf16, esz, ws, s);
   }
 
-  int dev;
-  DevInfo di;
-  if (device_info(&dev, &di) != cudaSuccess) return SPEC_ERR_CUDA;
-  const int epv = 16 / esz;
-  ChainStochParams p = {};
-  p.target = a->target_logits;
-  p.draft = a->draft_logits;
-  p.tokens = a->draft_tokens;
-  p.temperature = a->temperature;
-  p.u_accept = a->u_accept;
-  p.u_sample = a->u_sample;
+  ChainStochParams p;
+  int grid = 0, nv = 0, C = 0;
+  size_t smem = 0;
+  {
+    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, smem, nv, C);
+    if (st != SPEC_OK) return st;
+  }
   p.accepted_len = o->accepted_len;
   p.out_tokens = o->out_tokens;
   p.num_emitted = o->num_emitted;
@@ -245,75 +330,45 @@ spec_status spec_verify_chain(const spec_chain_args *a, const spec_chain_out *o,
   p.p_at_draft = o->p_at_draft;
   p.q_at_draft = o->q_at_draft;
   p.resid_mass = o->resid_mass;
-  p.part = static_cast<SoftPart *>(ws);
-  p.B = a->B;
-  p.K = K;
-  p.V = a->V;
-  p.use_tma = aligned(a->target_logits, 16) && (K == 0 || aligned(a->draft_logits, 16)) &&
-              (static_cast<long long>(a->V) * esz) % 16 == 0;
-  p.wait_limit_ns = g_wait_ns.load();
-  p.force_timeout = g_force_timeout.load();
-  {
-    // workspace tail: header {claim, -, magic} in the last 16 bytes, one
-    // generation word per row below it
-    char *end = static_cast<char *>(ws) + (ws_bytes & ~static_cast<size_t>(15));
-    p.claim = reinterpret_cast<uint32_t *>(end - 16);
-    p.magic = reinterpret_cast<unsigned long long *>(end - 8);
-    p.gen = reinterpret_cast<uint32_t *>(end - 16);
-    // SPECVERIFY_DYNAMIC=0 keeps every tile statically assigned;
-    // SPECVERIFY_DYN_CHUNK sets the tiles per claim (tuning)
-    const char *dv = std::getenv("SPECVERIFY_DYNAMIC");
-    p.dyn = !(dv && *dv == '0');
-    p.dyn_chunk = 2;
-    if (const char *dc = std::getenv("SPECVERIFY_DYN_CHUNK")) {
-      const int c = std::atoi(dc);
-      if (c >= 1 && c <= 64) p.dyn_chunk = c;
-    }
-  }
-  // stream kernel: fixed-size items (16 or 32 KB), a bulk-copy ring per CTA;
-  // SPECVERIFY_SOFT_VECS (4 or 8) and SPECVERIFY_SOFT_STAGES (2..4) override
-  // the defaults for tuning
-  int nv = kSoftVecs;
-  if (const char *ov = std::getenv("SPECVERIFY_SOFT_VECS")) nv = std::atoi(ov) == 8 ? 8 : 4;
-  p.slice = kSoftThreads * nv * epv;
-  p.nslices = ceil_div(a->V, p.slice);
-  p.buf_bytes = 2 * p.slice * esz;  // target tile + draft tile
-  p.stages = kSoftStages;
-  if (const char *ov = std::getenv("SPECVERIFY_SOFT_STAGES")) {
-    const int st = std::atoi(ov);
-    if (st >= 2 && st <= 4) p.stages = st;
-  }
-  const size_t smem = static_cast<size_t>(p.stages) * p.buf_bytes + kSoftCtrlBytes;
-  {
-    const size_t rows = static_cast<size_t>(a->B) * (K + 1) + static_cast<size_t>(a->B) * K;
-    p.ylog = reinterpret_cast<float *>(static_cast<char *>(ws) +
-                                       align_up(rows * p.nslices * sizeof(SoftPart), 256));
-  }
-  int per_sm = 0;
-  if (soft_blocks(dev, bf16, nv, smem, &per_sm) != cudaSuccess || per_sm < 1) return SPEC_ERR_CUDA;
-  const long long tiles = (static_cast<long long>(a->B) * (K + 1) + static_cast<long long>(a->B) * K) * p.nslices;
-  const int grid = static_cast<int>(std::min<long long>(tiles, static_cast<long long>(di.sms) * per_sm));
-  // resolve kernel: a cluster of C CTAs per row, at most 16 rounds of 32
-  // vectors per warp
-  constexpr int kRW = kResolveThreads / 32;
-  auto rounds = [&](int c) {
-    const int L = static_cast<int>(align_up(static_cast<size_t>(ceil_div(a->V, c)), static_cast<size_t>(epv)));
-    return ceil_div(ceil_div(ceil_div(L, epv), kRW), 32);
-  };
-  int C = 1;
-  while (C < 16 && rounds(C) > kResolveMaxRounds) C *= 2;
-  if (rounds(C) > kResolveMaxRounds) return SPEC_ERR_SHAPE;
-  while (C < 8 && ceil_div(a->V, 2 * C) >= 2048) C *= 2;  // spread each row's work
-  if (const char *ov = std::getenv("SPECVERIFY_CLUSTER")) {  // tuning override
-    const int c = std::atoi(ov);
-    if (c >= C && c <= 16 && (c & (c - 1)) == 0) C = c;
-  }
-  p.L = static_cast<int>(align_up(static_cast<size_t>(ceil_div(a->V, C)), static_cast<size_t>(epv)));
-  p.vpw = 32 * rounds(C);
-  report("stochastic slice nslices stages grid per_sm cluster L", p.slice, p.nslices, p.stages,
-         grid, per_sm, C, p.L);
   if (launch_chain_stochastic(p, bf16, nv, grid, smem, C, s) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
+}
+
+spec_status spec_drift_residuals(const spec_chain_args *a, int32_t m, int32_t *support,
+                                 float *residual, int32_t *row_status, void *ws, size_t ws_bytes,
+                                 void *stream) {
+  if (!a) return SPEC_ERR_NULL;
+  if (!valid_sizes(a->B, a->V) || a->K < 0 || a->K > kDriftMaxK || a->B > 65535)
+    return SPEC_ERR_SHAPE;
+  if (a->dtype != SPEC_F32 && a->dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  if (m < 1 || m > kDriftMaxSupport || m > a->V) return SPEC_ERR_ARG;
+  if (a->B == 0 || a->K == 0) return SPEC_OK;
+  if (!a->target_logits || !a->draft_logits || !support || !residual || !row_status)
+    return SPEC_ERR_NULL;
+  const int esz = a->dtype == SPEC_BF16 ? 2 : 4;
+  if (!aligned(a->target_logits, esz) || !aligned(a->draft_logits, esz)) return SPEC_ERR_ALIGN;
+  const void *i32s[] = {a->temperature, a->draft_tokens, support, residual, row_status};
+  for (const void *q : i32s)
+    if (q && !aligned(q, 4)) return SPEC_ERR_ALIGN;
+  const size_t need = spec_verify_chain_workspace_size(a->B, a->K, a->V);
+  if (!ws || !aligned(ws, 256) || ws_bytes < need) return SPEC_ERR_WORKSPACE;
+  ChainStochParams p;
+  int grid = 0, nv = 0, C = 0;
+  size_t smem = 0;
+  {
+    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, smem, nv, C);
+    if (st != SPEC_OK) return st;
+  }
+  p.dyn = 0;  // the selection kernel does not re-arm the workspace header
+  p.row_status = row_status;
+  p.drift_m = m;
+  p.drift_support = support;
+  p.drift_residual = residual;
+  report("drift grid m", grid, m, 0, 0, 0, 0, 0);
+  return launch_drift(p, a->dtype == SPEC_BF16, grid, smem, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? SPEC_OK
+             : SPEC_ERR_CUDA;
 }
 
 spec_status spec_verify_chain_static(const spec_chain_args *a, const spec_chain_out *o,

@@ -36,11 +36,13 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "specverify.h"
 
 namespace sv {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kInf = __builtin_huge_valf();
 constexpr int kMaxStages = 4;
 
@@ -235,7 +237,7 @@ __device__ __forceinline__ TileInfo make_tile(const ChainStochParams &P, int gt,
   if (!(T > 0.f && T < kInf)) T = 1.0f;  // the resolve kernel flags the row
   it.s2 = __fdiv_rn(kLog2e, T);
   it.yl = -1;
-  if (j < K) {
+  if (j < K && P.tokens) {
     const int y = __ldg(P.tokens + (size_t)b * K + j);
     if (y >= s0 && y < s0 + it.len) it.yl = y - s0;
   }
@@ -1000,6 +1002,437 @@ __global__ void __launch_bounds__(kResolveThreads, 4) chain_resolve_kernel(const
   cluster_wait();  // no CTA leaves while a peer may still read its mailbox
 }
 
+// ============================================================ DRIFT selection
+//
+// "Speculative Decoding Under Distribution Shift: DRIFT Recalibration" (the
+// residual paragraph of its method): at every drafted position, restrict
+// target and draft to the m tokens of highest target probability and report
+// log p - log q there.  One CTA per (position j < K, row b).  The m-th
+// largest target logit is found by radix selection on order-preserving
+// integer keys, 8 bits a pass from the top; equal keys at the boundary are
+// taken in vocabulary order, so the support matches the oracle's exactly.
+
+constexpr int kDriftThreads = 512;
+constexpr int kDriftWarps = kDriftThreads / 32;
+constexpr int kDriftMaxM = kDriftMaxSupport;
+constexpr int kDriftMaxRows = kDriftMaxK;
+
+constexpr int kDriftCand = 2048;  // candidate list of the sampled-threshold path
+constexpr int kDriftSample = 64;  // sampling stride of that threshold
+
+struct alignas(16) DriftCtrl {
+  int hist[kDriftWarps][256];  // whole-row radix fallback
+  struct {
+    uint32_t key[kDriftCand];
+    int idx[kDriftCand];
+  } cand;                      // candidates at or above the sampled threshold
+  int chist[256];              // radix digits over samples and candidates
+  int n_cand;
+  int sel_idx[kDriftMaxM];
+  uint32_t sel_key[kDriftMaxM];
+  int scan[kDriftWarps];
+  int n_gt, n_eq, digit, above;
+  float Mp, Sp, Mq, Sq;
+  uint32_t flags;
+};
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t order_key(uint32_t bits) {
+  if constexpr (BF16) return (bits & 0x8000u) ? (~bits & 0xFFFFu) : (bits | 0x8000u);
+  else return (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+}
+
+// Raw bits of element e of a 16-byte vector.
+template <bool BF16>
+__device__ __forceinline__ uint32_t elem_bits(const uint32_t *w, int e) {
+  if constexpr (BF16) return (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
+  else return w[e];
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kDriftThreads) drift_select_kernel(const __grid_constant__ ChainStochParams P) {
+  using F = Fmt<BF16>;
+  constexpr int EPV = F::EPV, ESZ = F::ESZ;
+  constexpr int KEYBITS = BF16 ? 16 : 32;
+  __shared__ DriftCtrl ctl;
+  __shared__ float4 rstat[2 * kDriftMaxRows + 1];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int j = blockIdx.x, b = blockIdx.y;
+  const int K = P.K, npos = K + 1, V = P.V, m = P.drift_m;
+  const float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
+  const uint32_t tflags = (T > 0.f && T < kInf) ? 0u : F_BAD_TEMPERATURE;
+  const float s2 = tflags ? 1.f : __fdiv_rn(kLog2e, T);
+  const uint32_t gen = *reinterpret_cast<volatile const uint32_t *>(P.gen - 1 - b);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // every position's statistics (the row's status covers all of them)
+  if (warp < kResolveThreads / 32) fold_rows(P, b, s2, gen + 1u, warp, lane, rstat);
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t f = tflags;
+    for (int r = 0; r < npos + K; ++r) {
+      if (r == K) continue;  // the bonus position is not a drafted one
+      const float4 v = rstat[r];
+      f |= __float_as_uint(v.w);
+      if (v.x != v.x || v.x == kInf) f |= F_NONFINITE;
+      else if (v.x == -kInf) f |= F_EMPTY;
+    }
+    ctl.flags = f;
+    ctl.Mp = rstat[j].x;
+    ctl.Sp = rstat[j].y;
+    ctl.Mq = rstat[npos + j].x;
+    ctl.Sq = rstat[npos + j].y;
+    if (j == 0 && P.row_status) P.row_status[b] = lowest_code(f);
+  }
+  __syncthreads();
+  int32_t *sup = P.drift_support + ((size_t)b * K + j) * m;
+  float *res = P.drift_residual + ((size_t)b * K + j) * m;
+  if (ctl.flags) {
+    for (int i = tid; i < m; i += kDriftThreads) {
+      sup[i] = -1;
+      res[i] = __int_as_float(0x7fc00000);
+    }
+    return;
+  }
+  const char *tg = static_cast<const char *>(P.target) + ((size_t)(b * npos + j) * V) * ESZ;
+  const bool aligned = P.use_tma != 0;
+  const int nvec = (V + EPV - 1) / EPV;
+
+  auto bits_at = [&](int i) -> uint32_t {
+    if constexpr (BF16) return __ldg(reinterpret_cast<const unsigned short *>(tg) + i);
+    else return __ldg(reinterpret_cast<const unsigned int *>(tg) + i);
+  };
+  const float nMp = -__fmul_rn(ctl.Mp, s2), nMq = -__fmul_rn(ctl.Mq, s2);
+  const float l2Sp = lg2(ctl.Sp), l2Sq = lg2(ctl.Sq);
+  const char *dg = static_cast<const char *>(P.draft) + ((size_t)(b * K + j) * V) * ESZ;
+  // support entry `rank` is token ii: log2 p and log2 q as in the walk, the
+  // difference in nats
+  auto emit = [&](int rank, int ii) {
+    float lt, ld;
+    if constexpr (BF16) {
+      lt = bf16_lo(__ldg(reinterpret_cast<const unsigned short *>(tg) + ii));
+      ld = bf16_lo(__ldg(reinterpret_cast<const unsigned short *>(dg) + ii));
+    } else {
+      lt = __ldg(reinterpret_cast<const float *>(tg) + ii);
+      ld = __ldg(reinterpret_cast<const float *>(dg) + ii);
+    }
+    const float l2p = __fadd_rn(__fmaf_rn(lt, s2, nMp), -l2Sp);
+    const float l2q = ld == -kInf ? -kInf : __fadd_rn(__fmaf_rn(ld, s2, nMq), -l2Sq);
+    sup[rank] = ii;
+    res[rank] = __fmul_rn(__fadd_rn(l2p, -l2q), kLn2);
+  };
+
+  // One radix digit of a block-wide key set: keys matching `prefix` on
+  // `pmask` are counted by their digit at `shift`; returns the digit holding
+  // the rem-th largest, the count above it and the count in it.
+  auto digit_pass = [&](auto for_each_key, int shift, uint32_t prefix, uint32_t pmask, int rem,
+                        int &above_out, int &in_out) {
+    for (int i = tid; i < 256; i += kDriftThreads) ctl.chist[i] = 0;
+    __syncthreads();
+    for_each_key([&](uint32_t k) {
+      if ((k & pmask) == prefix) atomicAdd(&ctl.chist[(k >> shift) & 255u], 1);
+    });
+    __syncthreads();
+    if (warp == 0) {
+      int cnt[8], own = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        cnt[i] = ctl.chist[255 - 8 * lane - i];
+        own += cnt[i];
+      }
+      int incl = own;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(FULL_MASK, incl, o);
+        if (lane >= o) incl += n;
+      }
+      int above = incl - own;
+      if (above < rem && rem <= incl) {
+        int dgt = 255 - 8 * lane;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (above + cnt[i] >= rem) {
+            dgt = 255 - 8 * lane - i;
+            break;
+          }
+          above += cnt[i];
+        }
+        ctl.digit = dgt;
+        ctl.above = above;
+      }
+    }
+    __syncthreads();
+    const int dgt = ctl.digit;
+    above_out = ctl.above;
+    in_out = ctl.chist[dgt];
+    __syncthreads();
+    return dgt;
+  };
+  // The r-th largest key of a set with at least r keys: its value, the
+  // number of keys above it and the number equal to it.
+  auto kth_largest = [&](auto for_each_key, int r, int &n_above, int &n_equal) {
+    uint32_t prefix = 0, pmask = 0;
+    int rem = r, in = 0;
+    for (int shift = KEYBITS - 8; shift >= 0; shift -= 8) {
+      int above = 0;
+      const int dgt = digit_pass(for_each_key, shift, prefix, pmask, rem, above, in);
+      rem -= above;
+      prefix |= static_cast<uint32_t>(dgt) << shift;
+      pmask |= 255u << shift;
+    }
+    n_above = r - rem;
+    n_equal = in;
+    return prefix;
+  };
+
+  // ---- threshold: the r-th largest key of a strided sample (every
+  // kDriftSample-th token); about r * kDriftSample keys of the row lie at or
+  // above it
+  constexpr int kNS = (SPEC_MAX_V + kDriftSample * kDriftThreads - 1) / (kDriftSample * kDriftThreads);
+  uint32_t smp[kNS];
+#pragma unroll
+  for (int q = 0; q < kNS; ++q) {
+    const int i = (tid + q * kDriftThreads) * kDriftSample;
+    smp[q] = i < V ? order_key<BF16>(bits_at(i)) : 0u;  // 0: no sample
+  }
+  const int n_samples = (V + kDriftSample - 1) / kDriftSample;
+  auto samples = [&](auto f) {
+#pragma unroll
+    for (int q = 0; q < kNS; ++q)
+      if ((tid + q * kDriftThreads) * kDriftSample < V) f(smp[q]);
+  };
+  auto sample_rank = [&](int r) -> uint32_t {
+    if (r > n_samples) return 0u;  // too few samples: every key qualifies
+    int na, ne;
+    return kth_largest(samples, r, na, ne);
+  };
+  // ---- one pass: every key >= tau into the candidate list
+  auto collect = [&](uint32_t tau) {
+    if (tid == 0) ctl.n_cand = 0;
+    __syncthreads();
+    constexpr int U = 4;  // vectors in flight per thread
+    for (int v0 = tid; v0 < nvec; v0 += U * kDriftThreads) {
+      uint32_t w[U][4];
+#pragma unroll
+      for (int u = 0; u < U; ++u) F::load_vec(w[u], nullptr, tg, aligned, v0 + u * kDriftThreads, V);
+      const unsigned act = __activemask();
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          const int idx = (v0 + u * kDriftThreads) * EPV + e;
+          const uint32_t k = order_key<BF16>(elem_bits<BF16>(w[u], e));
+          const bool c = k >= tau && idx < V;
+          const unsigned bal = __ballot_sync(act, c);
+          if (bal) {
+            const int leader = __ffs(bal) - 1;
+            int base = 0;
+            if (lane == leader) base = atomicAdd(&ctl.n_cand, __popc(bal));
+            base = __shfl_sync(act, base, leader);
+            if (c) {
+              const int slot = base + __popc(bal & ((1u << lane) - 1u));
+              if (slot < kDriftCand) {
+                ctl.cand.key[slot] = k;
+                ctl.cand.idx[slot] = idx;
+              }
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();
+    return ctl.n_cand;
+  };
+  int r = 8;
+  for (int attempt = 0; attempt < 3; ++attempt) {
+    const int nc = collect(sample_rank(r));
+    if (nc >= m && nc <= kDriftCand) {
+      // the m-th largest candidate key; every candidate above it is taken,
+      // and of those equal to it the lowest token ids
+      auto cands = [&](auto f) {
+        for (int i = tid; i < nc; i += kDriftThreads) f(ctl.cand.key[i]);
+      };
+      int n_above, n_equal;
+      const uint32_t tkey = kth_largest(cands, m, n_above, n_equal);
+      const int need_eq = m - n_above;
+      if (tid == 0) {
+        ctl.n_gt = 0;
+        ctl.n_eq = 0;
+      }
+      __syncthreads();
+      for (int i = tid; i < nc; i += kDriftThreads) {
+        const uint32_t k = ctl.cand.key[i];
+        const int ii = ctl.cand.idx[i];
+        if (k > tkey) {
+          const int slot = atomicAdd(&ctl.n_gt, 1);
+          ctl.sel_idx[slot] = ii;
+          ctl.sel_key[slot] = k;
+        } else if (k == tkey) {
+          bool take = true;
+          if (n_equal > need_eq) {  // ties straddle the boundary: lowest ids
+            int before = 0;
+            for (int q = 0; q < nc; ++q)
+              before += ctl.cand.key[q] == tkey && ctl.cand.idx[q] < ii;
+            take = before < need_eq;
+          }
+          if (take) {
+            const int slot = n_above + atomicAdd(&ctl.n_eq, 1);
+            ctl.sel_idx[slot] = ii;
+            ctl.sel_key[slot] = k;
+          }
+        }
+      }
+      __syncthreads();
+      for (int i = tid; i < m; i += kDriftThreads) {
+        const uint32_t ki = ctl.sel_key[i];
+        const int ii = ctl.sel_idx[i];
+        int rank = 0;
+        for (int q = 0; q < m; ++q) {
+          const uint32_t kq = ctl.sel_key[q];
+          rank += (kq > ki) || (kq == ki && ctl.sel_idx[q] < ii);
+        }
+        emit(rank, ii);
+      }
+      return;
+    }
+    if (nc < m) r *= 4;                  // threshold too high: lower it
+    else if (r > 1) r = max(1, r / 4);   // too many candidates: raise it
+    else break;                          // even the largest sample admits too many
+    __syncthreads();
+  }
+  __syncthreads();
+  // ---- fallback (the sample missed: too few or too many candidates):
+  // radix selection of the m-th largest key over the whole row
+  uint32_t prefix = 0, pmask = 0;
+  int rem = m;  // rank still to find within the keys matching prefix
+  int last_count = 0;
+  for (int shift = KEYBITS - 8; shift >= 0; shift -= 8) {
+    for (int i = tid; i < kDriftWarps * 256; i += kDriftThreads) (&ctl.hist[0][0])[i] = 0;
+    __syncthreads();
+    for (int v = tid; v < nvec; v += kDriftThreads) {
+      uint32_t w[4];
+      F::load_vec(w, nullptr, tg, aligned, v, V);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const uint32_t k = order_key<BF16>(elem_bits<BF16>(w, e));
+        if ((k & pmask) == prefix && v * EPV + e < V) {
+          const uint32_t d = (k >> shift) & 255u;
+          const unsigned same = __match_any_sync(__activemask(), d);
+          if (lane == __ffs(same) - 1) atomicAdd(&ctl.hist[warp][d], __popc(same));
+        }
+      }
+    }
+    __syncthreads();
+    if (tid < 256) {
+      int c = 0;
+      for (int w2 = 0; w2 < kDriftWarps; ++w2) c += ctl.hist[w2][tid];
+      ctl.hist[0][tid] = c;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns bins 255-8l .. 248-8l (descending); suffix counts from the top
+      int cnt[8], own = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        cnt[i] = ctl.hist[0][255 - 8 * lane - i];
+        own += cnt[i];
+      }
+      int incl = own;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(FULL_MASK, incl, o);
+        if (lane >= o) incl += n;
+      }
+      int above = incl - own;  // keys in higher bins than this lane's
+      if (above < rem && rem <= incl) {
+        int dgt = 255 - 8 * lane;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (above + cnt[i] >= rem) {
+            dgt = 255 - 8 * lane - i;
+            break;
+          }
+          above += cnt[i];
+        }
+        ctl.digit = dgt;
+        ctl.above = above;
+      }
+    }
+    __syncthreads();
+    const int dgt = ctl.digit;
+    rem -= ctl.above;
+    last_count = ctl.hist[0][dgt];
+    prefix |= static_cast<uint32_t>(dgt) << shift;
+    pmask |= 255u << shift;
+    __syncthreads();  // hist and digit are reused by the next pass
+  }
+  const uint32_t tkey = prefix;  // key of the m-th largest
+  const int n_gt = m - rem;      // keys above it, all selected
+  // ---- collect: every key above tkey; rem keys equal to it, lowest index first
+  if (tid == 0) {
+    ctl.n_gt = 0;
+    ctl.n_eq = 0;
+  }
+  __syncthreads();
+  const bool take_all_eq = last_count == rem;
+  for (int v = tid; v < nvec; v += kDriftThreads) {
+    uint32_t w[4];
+    F::load_vec(w, nullptr, tg, aligned, v, V);
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) {
+      const int idx = v * EPV + e;
+      if (idx >= V) continue;
+      const uint32_t k = order_key<BF16>(elem_bits<BF16>(w, e));
+      if (k > tkey) {
+        const int slot = atomicAdd(&ctl.n_gt, 1);
+        ctl.sel_idx[slot] = idx;
+        ctl.sel_key[slot] = k;
+      } else if (k == tkey && take_all_eq) {
+        const int slot = n_gt + atomicAdd(&ctl.n_eq, 1);
+        ctl.sel_idx[slot] = idx;
+        ctl.sel_key[slot] = k;
+      }
+    }
+  }
+  if (!take_all_eq) {
+    // ties straddle the boundary: each thread counts the equal keys of its
+    // contiguous index range, an exclusive scan orders them, and the first
+    // rem in vocabulary order are taken
+    const int span = (V + kDriftThreads - 1) / kDriftThreads;
+    const int i0 = min(V, tid * span), i1 = min(V, i0 + span);
+    int mine = 0;
+    for (int i = i0; i < i1; ++i) mine += order_key<BF16>(bits_at(i)) == tkey;
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(FULL_MASK, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) ctl.scan[warp] = incl;
+    __syncthreads();
+    int base = incl - mine;
+    for (int w2 = 0; w2 < warp; ++w2) base += ctl.scan[w2];
+    for (int i = i0; i < i1 && base < rem; ++i) {
+      if (order_key<BF16>(bits_at(i)) == tkey) {
+        ctl.sel_idx[n_gt + base] = i;
+        ctl.sel_key[n_gt + base] = tkey;
+        ++base;
+      }
+    }
+  }
+  __syncthreads();
+  // ---- rank (key descending, index ascending) among the m selected
+  for (int i = tid; i < m; i += kDriftThreads) {
+    const uint32_t ki = ctl.sel_key[i];
+    const int ii = ctl.sel_idx[i];
+    int rank = 0;
+    for (int q = 0; q < m; ++q) {
+      const uint32_t kq = ctl.sel_key[q];
+      rank += (kq > ki) || (kq == ki && ctl.sel_idx[q] < ii);
+    }
+    emit(rank, ii);
+  }
+}
+
 size_t resolve_smem(const ChainStochParams &p) {
   return static_cast<size_t>(2 * p.K + 1) * 16 + static_cast<size_t>(p.vpw / 32) * kResolveThreads * 4;
 }
@@ -1062,6 +1495,25 @@ cudaError_t launch_t(const ChainStochParams &p, int grid, size_t smem, int clust
   return cudaLaunchKernelEx(&cfg, chain_resolve_kernel<BF16>, p);
 }
 
+template <bool BF16, int S>
+cudaError_t launch_drift_t(const ChainStochParams &p, int grid, size_t smem, cudaStream_t s) {
+  cudaError_t e = prepare<BF16, 4, S>(smem, 1);
+  if (e != cudaSuccess) return e;
+  softmax_partials_kernel<BF16, 4, S><<<grid, kSoftThreads + 32, smem, s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.K), static_cast<unsigned>(p.B));
+  cfg.blockDim = dim3(kDriftThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, drift_select_kernel<BF16>, p);
+}
+
 template <bool BF16, int NV, int S>
 cudaError_t blocks_t(size_t smem, int *blocks) {
   cudaError_t e = prepare<BF16, NV, S>(smem, 1);
@@ -1078,6 +1530,13 @@ cudaError_t launch_chain_stochastic(const ChainStochParams &p, bool bf16, int nv
   if (p.stages == 3)
     return bf16 ? launch_t<true, 4, 3>(p, grid, smem, cluster, s) : launch_t<false, 4, 3>(p, grid, smem, cluster, s);
   return bf16 ? launch_t<true, 4, 2>(p, grid, smem, cluster, s) : launch_t<false, 4, 2>(p, grid, smem, cluster, s);
+}
+
+cudaError_t launch_drift(const ChainStochParams &p, bool bf16, int grid, size_t smem,
+                         cudaStream_t s) {
+  if (p.stages == 3)
+    return bf16 ? launch_drift_t<true, 3>(p, grid, smem, s) : launch_drift_t<false, 3>(p, grid, smem, s);
+  return bf16 ? launch_drift_t<true, 2>(p, grid, smem, s) : launch_drift_t<false, 2>(p, grid, smem, s);
 }
 
 cudaError_t soft_partials_blocks_per_sm(bool bf16, int nv, size_t smem, int *blocks) {

@@ -66,6 +66,10 @@ struct ChainStochParams {
   uint32_t *gen;       // gen[-1 - b]: generation word of row b
   int dyn;             // 0: static assignment only
   int dyn_chunk;       // tiles per claim
+  // DRIFT residual extraction (spec_drift_residuals): support size and outputs
+  int drift_m;
+  int32_t *drift_support;   // [B, K, m]
+  float *drift_residual;    // [B, K, m]
 };
 
 constexpr unsigned long long kWsMagic = 0x5EC7E21F1CA7E5EDull;  // armed workspace header
@@ -131,11 +135,16 @@ constexpr int kResolveMaxRounds = 16;
 constexpr int kGreedySlice = 16384;
 // Devices whose per-kernel attributes are cached.
 constexpr int kMaxDevices = 64;
+constexpr int kDriftMaxK = 64;        // drafted positions per row for spec_drift_residuals
+constexpr int kDriftMaxSupport = 64;  // largest support size m
 
 // Host launchers (defined next to their kernels); each returns the CUDA error
 // of its launches.
 cudaError_t launch_chain_stochastic(const ChainStochParams &p, bool bf16, int nv, int grid,
                                     size_t smem, int cluster, cudaStream_t s);
+// Stream kernel then the DRIFT selection kernel (one CTA per drafted position).
+cudaError_t launch_drift(const ChainStochParams &p, bool bf16, int grid, size_t smem,
+                         cudaStream_t s);
 cudaError_t soft_partials_blocks_per_sm(bool bf16, int nv, size_t smem, int *blocks);
 cudaError_t launch_greedy(const GreedyParams &p, bool bf16, int grid, size_t smem,
                           cudaStream_t s);

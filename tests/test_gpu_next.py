@@ -101,3 +101,63 @@ def test_kv_compaction_random_paths_and_bad_rows(sv, E):
     assert st_o[1:5].tolist() == [4, 4, 4, 4] and st_o[0] == 0
     assert np.array_equal(out["st"], st_o)
     assert np.array_equal(out["kv"], want)
+
+
+# ------------------------------------------------------- DRIFT residuals
+DRIFT_ATOL = 2e-4  # nats: fp32 rounding of l*s2 - M*s2 - log2 S at |l*s2| <~ 100
+
+
+def compare_drift(g, o):
+    gs, gr, gst = g
+    os_, or_, ost = o
+    assert np.array_equal(gst, ost)
+    assert np.array_equal(gs, os_)
+    fin = np.isfinite(or_)
+    assert np.array_equal(np.isfinite(gr), fin)
+    assert np.array_equal(np.isnan(gr), np.isnan(or_))
+    assert np.array_equal(gr[np.isinf(or_)], or_[np.isinf(or_)])
+    np.testing.assert_allclose(gr[fin], or_[fin], atol=DRIFT_ATOL, rtol=0)
+
+
+def run_drift(sv, inp, m):
+    g = sv.spec_drift_residuals(cuda(inp["target"]), cuda(inp["draft"]),
+                                cuda(inp.get("temperature")), m=m)
+    return tuple(x.cpu().numpy() for x in g)
+
+
+@pytest.mark.parametrize("name,m", [("c2", 32), ("c3", 32), ("c5", 8), ("c1", 16)])
+def test_drift_workloads(sv, name, m):
+    inp = S.make(name, B=16) if name == "c5" else S.make(name)
+    o = O.drift_residuals(inp["target"], inp["draft"], inp.get("temperature"), m=m)
+    compare_drift(run_drift(sv, inp, m), o)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("V", [37, 1001, 40000])
+def test_drift_ties_unaligned_and_edges(sv, dtype, V):
+    rng = np.random.default_rng(V)
+    B, K, m = 6, 3, 24
+    t = rng.normal(0, 3, (B, K + 1, V)).astype(np.float32)
+    d = (t[:, :K] + rng.normal(0, 2, (B, K, V))).astype(np.float32)
+    # row 0: forty equal logits straddle the support boundary
+    t[0, 1, :] = np.minimum(t[0, 1, :], 5.0)
+    t[0, 1, rng.choice(V, min(V, 40), replace=False)] = 5.0
+    # row 1: all logits equal
+    t[1, 2, :] = 1.25
+    # row 2: masked draft logits inside the support
+    d[2, 0, np.argsort(-t[2, 0])[:5]] = -np.inf
+    # row 3: identical laws
+    d[3] = t[3, :K]
+    # row 4: a NaN; row 5: bad temperature
+    t[4, 0, 3] = np.nan
+    temp = np.full(B, 0.8, np.float32)
+    temp[5] = 0.0
+    if dtype == "bf16":
+        t, d = S.f32_to_bf16_bits(t), S.f32_to_bf16_bits(d)
+    inp = dict(target=t, draft=d, temperature=temp)
+    o = O.drift_residuals(t, d, temp, m=min(m, V))
+    g = run_drift(sv, inp, min(m, V))
+    compare_drift(g, o)
+    assert g[2][4] == 1 and g[2][5] == 7
+    assert np.all(g[1][3] == 0.0)  # identical laws: exactly zero
+    assert np.isinf(g[1][2, 0]).sum() == 5

@@ -189,3 +189,24 @@ def test_kv_compact_and_policy_argument_errors(L):
     assert L.spec_adaptive_tree_policy(ctypes.byref(par()), 4, p, p, p, _fake(b + 4), p, p,
                                        None) == 4  # ema needs 8-byte alignment
     assert L.spec_adaptive_tree_policy(ctypes.byref(par()), 0, *args) == 0
+
+
+def test_drift_argument_errors(L):
+    from speculative_decoding_verification_32_gb300._binding import SpecChainArgs
+    b = 0x10000000
+    p = _fake(b)
+    ws = _fake(0x20000000)
+    big = 1 << 30
+
+    def args(B=2, K=3, V=1000):
+        return SpecChainArgs(B, K, V, 1, 0, 0.0, p, _fake(b + 0x100000), None, None, None, None)
+    o = (p, p, p, ws, big, None)
+    assert L.spec_drift_residuals(None, 8, *o) == 1
+    assert L.spec_drift_residuals(ctypes.byref(args(K=65)), 8, *o) == 2
+    assert L.spec_drift_residuals(ctypes.byref(args()), 0, *o) == 5
+    assert L.spec_drift_residuals(ctypes.byref(args()), 65, *o) == 5
+    assert L.spec_drift_residuals(ctypes.byref(args(V=20)), 32, *o) == 5
+    assert L.spec_drift_residuals(ctypes.byref(args(B=0)), 8, *o) == 0
+    assert L.spec_drift_residuals(ctypes.byref(args(K=0)), 8, *o) == 0
+    assert L.spec_drift_residuals(ctypes.byref(args()), 8, None, p, p, ws, big, None) == 1
+    assert L.spec_drift_residuals(ctypes.byref(args()), 8, p, p, p, ws, 16, None) == 7
