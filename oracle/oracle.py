@@ -35,6 +35,9 @@ def _bind(L):
     L.so_verify_chain.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, f32,
                                   P, P, P, P, P, P, P, P, P, P, i32]
     L.so_verify_chain.restype = None
+    L.so_verify_chain_trunc.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, f32, P, P,
+                                        P, P, P, P, P, P, P, P, P, P, i32]
+    L.so_verify_chain_trunc.restype = None
     L.so_verify_tree.argtypes = [i32, i32, i32, i32, P, P, P, P, f32, P, P, P, P, P, i32]
     L.so_verify_tree.restype = None
     L.so_rollback_lengths.argtypes = [i32, i32, P, P, P, P, ctypes.c_int32, P, P, P]
@@ -72,8 +75,10 @@ def _logits(a):
 
 
 def verify_chain(target, draft, draft_tokens, temperature=None, u_accept=None,
-                 u_sample=None, mode=STOCHASTIC, kappa=0.0, nthreads=0, L=None):
-    """Run the oracle chain verifier.  Returns a dict of numpy outputs."""
+                 u_sample=None, mode=STOCHASTIC, kappa=0.0, nthreads=0, L=None,
+                 top_k=None, top_p=None):
+    """Run the oracle chain verifier.  Returns a dict of numpy outputs.
+    top_k [B] int32 / top_p [B] float32 (optional) truncate p and q."""
     L = L or lib()
     target, dt = _logits(target)
     B, K1, V = target.shape
@@ -100,8 +105,10 @@ def verify_chain(target, draft, draft_tokens, temperature=None, u_accept=None,
         accept_margin=np.zeros((B, K)),
         row_margin=np.zeros(B),
     )
-    L.so_verify_chain(B, K, V, dt, mode, _ptr(target), _ptr(draft), _ptr(toks), _ptr(temp),
-                      _ptr(ua), _ptr(us), float(kappa),
+    tk = None if top_k is None else np.ascontiguousarray(top_k, dtype=np.int32).reshape(B)
+    tp = None if top_p is None else np.ascontiguousarray(top_p, dtype=np.float32).reshape(B)
+    L.so_verify_chain_trunc(B, K, V, dt, mode, _ptr(target), _ptr(draft), _ptr(toks), _ptr(temp),
+                      _ptr(ua), _ptr(us), float(kappa), _ptr(tk), _ptr(tp),
                       _ptr(out["accepted_len"]), _ptr(out["out_tokens"]),
                       _ptr(out["num_emitted"]), _ptr(out["row_status"]),
                       _ptr(out["p_at_draft"]), _ptr(out["q_at_draft"]), _ptr(out["ratio"]),

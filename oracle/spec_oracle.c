@@ -131,6 +131,77 @@ static int inverse_cdf(const double *w, int V, double u, double *gap) {
   return -1;
 }
 
+/* Top-k / top-p truncation of a distribution already computed by
+ * softmax_row ([DVC] "Preserve the distribution you actually intend": when
+ * top-p filtering (or top-k) defines the sampling law, acceptance and
+ * correction both use the truncated p, and q must be the truncated law that
+ * produced the draft).  Order: temperature (already in p), then top-k, then
+ * top-p.
+ *   top-k (1 <= k < V): keep the tokens whose logit is >= the k-th largest
+ *     logit (ties at the boundary are kept).
+ *   top-p (0 < top_p < 1): over the kept tokens, renormalised, take whole
+ *     groups of equal logits in descending order until the cumulative mass
+ *     reaches top_p; keep the tokens of those groups.
+ * p is zeroed outside the kept set and renormalised.  *gap (if not NULL) is
+ * lowered to the distance of top_p to the cumulative masses on either side
+ * of the chosen boundary -- the margin of the one floating-point decision. */
+typedef struct {
+  double l;
+  double w;
+} lw_pair;
+
+static int by_logit_desc(const void *a, const void *b) {
+  const double x = ((const lw_pair *)a)->l, y = ((const lw_pair *)b)->l;
+  return (x < y) - (x > y);
+}
+
+static void truncate_dist(const void *base, int dtype, size_t off, int V, int top_k,
+                          double top_p, double *p, lw_pair *tmp, double *gap) {
+  const int use_k = top_k >= 1 && top_k < V;
+  const int use_p = top_p > 0.0 && top_p < 1.0;
+  if (!use_k && !use_p) return;
+  for (int v = 0; v < V; ++v) {
+    tmp[v].l = logit_at(base, dtype, off + (size_t)v);
+    tmp[v].w = p[v];
+  }
+  qsort(tmp, (size_t)V, sizeof(lw_pair), by_logit_desc);
+  double theta = tmp[V - 1].l; /* keep everything */
+  int n = V;                   /* kept tokens, a prefix of the sorted list */
+  if (use_k) {
+    theta = tmp[top_k - 1].l;
+    n = top_k;
+    while (n < V && tmp[n].l == theta) ++n;
+  }
+  if (use_p) {
+    double mass = 0.0;
+    for (int i = 0; i < n; ++i) mass += tmp[i].w;
+    double cum = 0.0;
+    int i = 0;
+    while (i < n) {
+      int e = i; /* the group of logits equal to tmp[i].l */
+      double g = 0.0;
+      while (e < n && tmp[e].l == tmp[i].l) g += tmp[e++].w;
+      const double before = cum;
+      cum += g / mass;
+      if (cum >= top_p || e == n) {
+        theta = tmp[i].l;
+        if (gap) {
+          const double m = fmin(cum - top_p, top_p - before);
+          if (m < *gap) *gap = m > 0.0 ? m : 0.0;
+        }
+        break;
+      }
+      i = e;
+    }
+  }
+  double S = 0.0;
+  for (int v = 0; v < V; ++v) {
+    if (logit_at(base, dtype, off + (size_t)v) >= theta) S += p[v];
+    else p[v] = 0.0;
+  }
+  for (int v = 0; v < V; ++v) p[v] /= S;
+}
+
 /* Lowest index of the largest logit (ties -> lowest index).  Greedy rule of
  * [SMB] "The Guarantee Behind Rejection Sampling": keep the draft iff it is
  * the target's argmax.  Temperature does not move an argmax. */
@@ -192,6 +263,22 @@ static int margin_promotes(double l_d, double l_top, double T, float kappa) {
  * row_margin [B] = smallest decision margin met by the walk (accept margins
  * of positions 0..stop and the sampling gap at the stop; +inf for greedy).
  */
+/* so_verify_chain_trunc: so_verify_chain with per-row top-k (top_k[b] <= 0
+ * or >= V: off) and top-p (top_p[b] >= 1: off) applied to every p and q of
+ * the stochastic walk (see truncate_dist); NULL arrays turn each off.  The
+ * top-p boundary margins of the positions the walk reads join row_margin.
+ * Greedy mode is unaffected (truncation keeps the argmax). */
+void so_verify_chain_trunc(int B, int K, int V, int dtype, int mode,
+                           const void *target, const void *draft,
+                           const int32_t *draft_tokens, const float *temperature,
+                           const float *u_accept, const float *u_sample, float kappa,
+                           const int32_t *top_k, const float *top_p,
+                           int32_t *accepted_len, int32_t *out_tokens,
+                           int32_t *num_emitted, int32_t *row_status,
+                           double *p_at_draft, double *q_at_draft, double *ratio_out,
+                           double *resid_mass, double *accept_margin,
+                           double *row_margin, int nthreads);
+
 void so_verify_chain(int B, int K, int V, int dtype, int mode,
                      const void *target, const void *draft,
                      const int32_t *draft_tokens, const float *temperature,
@@ -201,6 +288,22 @@ void so_verify_chain(int B, int K, int V, int dtype, int mode,
                      double *p_at_draft, double *q_at_draft, double *ratio_out,
                      double *resid_mass, double *accept_margin,
                      double *row_margin, int nthreads) {
+  so_verify_chain_trunc(B, K, V, dtype, mode, target, draft, draft_tokens, temperature,
+                        u_accept, u_sample, kappa, NULL, NULL, accepted_len, out_tokens,
+                        num_emitted, row_status, p_at_draft, q_at_draft, ratio_out,
+                        resid_mass, accept_margin, row_margin, nthreads);
+}
+
+void so_verify_chain_trunc(int B, int K, int V, int dtype, int mode,
+                           const void *target, const void *draft,
+                           const int32_t *draft_tokens, const float *temperature,
+                           const float *u_accept, const float *u_sample, float kappa,
+                           const int32_t *top_k, const float *top_p,
+                           int32_t *accepted_len, int32_t *out_tokens,
+                           int32_t *num_emitted, int32_t *row_status,
+                           double *p_at_draft, double *q_at_draft, double *ratio_out,
+                           double *resid_mass, double *accept_margin,
+                           double *row_margin, int nthreads) {
 #ifdef _OPENMP
   if (nthreads > 0) omp_set_num_threads(nthreads);
 #pragma omp parallel
@@ -209,10 +312,13 @@ void so_verify_chain(int B, int K, int V, int dtype, int mode,
     double *p = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
     double *q = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
     double *r = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+    lw_pair *tmp = (lw_pair *)malloc(sizeof(lw_pair) * (size_t)(V > 0 ? V : 1));
 #ifdef _OPENMP
 #pragma omp for schedule(dynamic, 1)
 #endif
     for (int b = 0; b < B; ++b) {
+      const int tk = top_k ? top_k[b] : 0;
+      const double tp = top_p ? (double)top_p[b] : 1.0;
       const size_t trow0 = (size_t)b * (size_t)(K + 1);
       const size_t drow0 = (size_t)b * (size_t)K;
       double T = temperature ? (double)temperature[b] : 1.0;
@@ -273,8 +379,11 @@ void so_verify_chain(int B, int K, int V, int dtype, int mode,
       int stop = -1, token = -1;
       double margin = INFINITY;
       for (int j = 0; j < K; ++j) {
+        double tgap = INFINITY; /* top-p boundary margins of this position */
         softmax_row(target, dtype, (trow0 + j) * (size_t)V, V, T, p);
         softmax_row(draft, dtype, (drow0 + j) * (size_t)V, V, T, q);
+        truncate_dist(target, dtype, (trow0 + j) * (size_t)V, V, tk, tp, p, tmp, &tgap);
+        truncate_dist(draft, dtype, (drow0 + j) * (size_t)V, V, tk, tp, q, tmp, &tgap);
         int32_t y = draft_tokens[drow0 + j];
         double ratio = p[y] / q[y];
         float u = u_accept[drow0 + j];
@@ -293,6 +402,7 @@ void so_verify_chain(int B, int K, int V, int dtype, int mode,
         if (accept_margin) accept_margin[o] = m_acc;
         if (stop >= 0) continue; /* walk already stopped: diagnostics only */
         if (m_acc < margin) margin = m_acc;
+        if (tgap < margin) margin = tgap;
         if (!accept) {
           double gap;
           stop = j;
@@ -306,6 +416,9 @@ void so_verify_chain(int B, int K, int V, int dtype, int mode,
         double gap;
         stop = K;
         softmax_row(target, dtype, (trow0 + K) * (size_t)V, V, T, p);
+        double tgap = INFINITY;
+        truncate_dist(target, dtype, (trow0 + K) * (size_t)V, V, tk, tp, p, tmp, &tgap);
+        if (tgap < margin) margin = tgap;
         token = inverse_cdf(p, V, (double)u_sample[trow0 + K], &gap);
         if (gap < margin) margin = gap;
       }
@@ -318,6 +431,7 @@ void so_verify_chain(int B, int K, int V, int dtype, int mode,
     free(p);
     free(q);
     free(r);
+    free(tmp);
   }
 }
 
