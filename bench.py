@@ -51,7 +51,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="chain",
-                    choices=["chain", "kv_compact", "policy", "drift"],
+                    choices=["chain", "kv_compact", "policy", "drift", "truncated"],
                     help="chain: the headline verify step (default); kv_compact / policy: "
                          "the post-verification entry points")
     ap.add_argument("--sets", type=int, default=0,
@@ -448,6 +448,45 @@ def run_next(args):
                              "kernel": "kv_compact_tree_kernel",
                              "algorithmic_bytes_per_launch": moved, "traffic": None},
                 "gpu_launches": n, "clocks": clocks}
+    elif args.workload == "truncated":
+        # the headline chain step with top-k = 50 and top-p = 0.9 on every row
+        inp = S.make(WORKLOAD)
+        B, K = inp["draft_tokens"].shape
+        step_bytes = inp["target"].nbytes + inp["draft"].nbytes
+        n_sets = max(2, -(-3 * L2_BYTES // step_bytes) + 1)
+        tgt0, drf0 = to_cuda(inp["target"], dev), to_cuda(inp["draft"], dev)
+        sets = [(tgt0, drf0)] + [(tgt0.clone(), drf0.clone()) for _ in range(n_sets - 1)]
+        small = {k: to_cuda(inp[k], dev) for k in ("draft_tokens", "temperature", "u_accept",
+                                                    "u_sample")}
+        tk = torch.full((B,), 50, dtype=torch.int32, device=dev)
+        tp = torch.full((B,), 0.9, dtype=torch.float32, device=dev)
+        outs = [dict(accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
+                     out_tokens=torch.empty(B, K + 1, dtype=torch.int32, device=dev),
+                     num_emitted=torch.empty(B, dtype=torch.int32, device=dev),
+                     row_status=torch.empty(B, dtype=torch.int32, device=dev))
+                for _ in range(n_sets)]
+
+        def step(i):
+            sv.spec_verify_chain(sets[i][0], sets[i][1], small["draft_tokens"],
+                                 small["temperature"], small["u_accept"], small["u_sample"],
+                                 out=outs[i], stream=stream, top_k=tk, top_p=tp)
+        sampler.start()
+        time.sleep(0.3)
+        ms, n, w = _time_graph(torch, stream, step, n_sets, steps, warmup)
+        clocks = sampler.stop()
+        gbs = step_bytes / (ms / 1e3) / 1e9
+        line = {"metric": "truncated verify steps/s (top-k 50, top-p 0.9)", "workload": "truncated",
+                "value": 1e3 / ms, "unit": "verify steps/s", "n_gpus": 1, "steps": n,
+                "warmup": w, "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
+                "data": "synthetic",
+                "config": {"workload": f"chain B={B} K={K} V={inp['target'].shape[-1]} bf16, "
+                                       "top_k=50, top_p=0.9 on every row",
+                           "l2": f"{n_sets} rotating input sets > L2"},
+                "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                             "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
+                             "kernel": "softmax_partials + trunc + chain_resolve",
+                             "algorithmic_bytes_per_launch": step_bytes, "traffic": None},
+                "gpu_launches": 3 * n, "clocks": clocks}
     elif args.workload == "drift":
         # top-32 DRIFT residuals on the headline chain workload
         inp = S.make(WORKLOAD)

@@ -265,6 +265,37 @@ spec_status spec_rollback_lengths(int32_t B, int32_t max_emit, const int32_t *kv
 /* ------------------------------------------------------------------ misc */
 
 /*
+ * spec_verify_chain_truncated -- spec_verify_chain (STOCHASTIC mode only,
+ * else SPEC_ERR_DTYPE) with top-k / top-p truncated target and draft laws
+ * ("Speculative Decoding: Draft, Verify, and Correct", 'Preserve the
+ * distribution you actually intend': if top-p (or top-k) filtering defines
+ * the target sampling law, acceptance and correction both use the truncated
+ * p, and q must be the truncated law that actually produced the draft).
+ *
+ * Per row b, applied to every p_j and q_j after the temperature: top-k
+ * (1 <= top_k[b] < V, else off) keeps the tokens whose logit is >= the k-th
+ * largest (ties at the boundary kept); then top-p (0 < top_p[b] < 1, else
+ * off) keeps, of those, whole groups of equal logits in descending order
+ * until their renormalised mass reaches top_p[b].  Everything else of
+ * spec_verify_chain holds with p and q replaced by the renormalised
+ * truncated laws: a draft outside the kept set of p is rejected, the
+ * residual and the bonus are drawn from them.  Either array may be NULL;
+ * both NULL is spec_verify_chain.  The top-p boundary is a floating-point
+ * decision taken in fp32 (the band rule covers rows whose cumulative mass
+ * lands within ~1e-5 of top_p).  Same workspace as spec_verify_chain.
+ * Three kernels: the stream, one threshold search per truncated logit row,
+ * the per-row resolve.
+ */
+typedef struct {
+  const int32_t *top_k;  /* [B] device, or NULL */
+  const float *top_p;    /* [B] device, or NULL */
+} spec_truncation;
+
+spec_status spec_verify_chain_truncated(const spec_chain_args *args, const spec_truncation *trunc,
+                                        const spec_chain_out *out, void *ws, size_t ws_bytes,
+                                        void *stream);
+
+/*
  * spec_drift_residuals -- the free supervision signal of "Speculative
  * Decoding Under Distribution Shift: DRIFT Recalibration" (the residual
  * paragraph of its method): at every drafted position j < K of row b, the m

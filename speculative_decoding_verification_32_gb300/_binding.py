@@ -46,6 +46,10 @@ class SpecTreeOut(_c.Structure):
                 ("num_emitted", _P), ("row_status", _P)]
 
 
+class SpecTruncation(_c.Structure):
+    _fields_ = [("top_k", _P), ("top_p", _P)]
+
+
 class SpecKvCompactArgs(_c.Structure):
     _fields_ = [("B", _c.c_int32), ("N", _c.c_int32), ("planes", _c.c_int32), ("pad", _c.c_int32),
                 ("S_max", _c.c_int64), ("entry_bytes", _c.c_int64), ("plane_stride", _c.c_int64),
@@ -98,6 +102,9 @@ def _bind(L):
     L.spec_verify_chain_static.restype = _c.c_int
     L.spec_verify_tree.argtypes = [_c.POINTER(SpecTreeArgs), _c.POINTER(SpecTreeOut), _P, sz, _P]
     L.spec_verify_tree.restype = _c.c_int
+    L.spec_verify_chain_truncated.argtypes = [_c.POINTER(SpecChainArgs), _c.POINTER(SpecTruncation),
+                                              _c.POINTER(SpecChainOut), _P, sz, _P]
+    L.spec_verify_chain_truncated.restype = _c.c_int
     L.spec_drift_residuals.argtypes = [_c.POINTER(SpecChainArgs), i32, _P, _P, _P, _P, sz, _P]
     L.spec_drift_residuals.restype = _c.c_int
     L.spec_kv_compact_tree.argtypes = [_c.POINTER(SpecKvCompactArgs), _P, _P]
@@ -173,7 +180,7 @@ def _stream(device, stream):
 
 def spec_verify_chain(target_logits, draft_logits, draft_tokens, temperature=None,
                       u_accept=None, u_sample=None, mode="stochastic", margin_kappa=0.0,
-                      diagnostics=False, out=None, stream=None):
+                      diagnostics=False, out=None, stream=None, top_k=None, top_p=None):
     """Verify B draft chains (see spec_verify_chain in include/specverify.h).
 
     target_logits [B,K+1,V] and draft_logits [B,K,V] (bf16 or fp32, CUDA),
@@ -181,6 +188,8 @@ def spec_verify_chain(target_logits, draft_logits, draft_tokens, temperature=Non
     u_sample [B,K+1] fp32 (stochastic mode).  mode: "stochastic" | "greedy".
     Returns a dict of CUDA tensors: accepted_len, out_tokens, num_emitted,
     row_status (+ p_at_draft, q_at_draft, resid_mass with diagnostics=True).
+    top_k [B] int32 / top_p [B] float32 (stochastic mode, optional) truncate
+    p and q (spec_verify_chain_truncated).
     """
     dev = target_logits.device
     greedy = mode == "greedy"
@@ -215,7 +224,16 @@ def spec_verify_chain(target_logits, draft_logits, draft_tokens, temperature=Non
     nbytes = L.spec_verify_chain_workspace_size(B, K, V)
     s, sp = _stream(dev, stream)
     ws = workspace(dev, nbytes, s.cuda_stream)
-    _check(L.spec_verify_chain(_c.byref(args), _c.byref(o), _ptr(ws), ws.numel(), sp))
+    if top_k is None and top_p is None:
+        _check(L.spec_verify_chain(_c.byref(args), _c.byref(o), _ptr(ws), ws.numel(), sp))
+    else:
+        if greedy:
+            raise ValueError("top_k / top_p apply to mode='stochastic' only")
+        _req(top_k, "top_k", dev, torch.int32)
+        _req(top_p, "top_p", dev, torch.float32)
+        t = SpecTruncation(_ptr(top_k), _ptr(top_p))
+        _check(L.spec_verify_chain_truncated(_c.byref(args), _c.byref(t), _c.byref(o), _ptr(ws),
+                                             ws.numel(), sp))
     return out
 
 

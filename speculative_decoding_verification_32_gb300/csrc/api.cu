@@ -217,6 +217,8 @@ spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes
     const size_t rows = static_cast<size_t>(a->B) * (K + 1) + static_cast<size_t>(a->B) * K;
     p.ylog = reinterpret_cast<float *>(static_cast<char *>(ws) +
                                        align_up(rows * p.nslices * sizeof(SoftPart), 256));
+    p.trunc = nullptr;  // set by the truncated entry point
+    p.trunc_area = reinterpret_cast<TruncRec *>(reinterpret_cast<char *>(p.ylog) + align_up(rows * 4, 256));
   }
   int per_sm = 0;
   if (soft_blocks(dev, bf16, nv, smem, &per_sm) != cudaSuccess || per_sm < 1) return SPEC_ERR_CUDA;
@@ -253,7 +255,8 @@ size_t spec_verify_chain_workspace_size(int32_t B, int32_t K, int32_t V) {
   // stochastic: one partial per (logit row, slice), the smallest slice being
   // the fp32 one; greedy: one partial per (position, slice)
   const size_t rows = static_cast<size_t>(B) * (K + 1) + static_cast<size_t>(B) * K;
-  const size_t soft = rows * ceil_div(V, kSoftMinSlice) * sizeof(SoftPart) + align_up(rows * 4, 256);
+  const size_t soft = rows * ceil_div(V, kSoftMinSlice) * sizeof(SoftPart) + align_up(rows * 4, 256) +
+                      rows * sizeof(TruncRec);
   const size_t part = greedy_partials_max(B, K + 1, V);
   return align_up(std::max(std::max(soft, part), static_cast<size_t>(256)), 256) + ws_tail_bytes(B);
 }
@@ -332,6 +335,61 @@ spec_status spec_verify_chain(const spec_chain_args *a, const spec_chain_out *o,
   p.resid_mass = o->resid_mass;
   if (launch_chain_stochastic(p, bf16, nv, grid, smem, C, s) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
+}
+
+spec_status spec_verify_chain_truncated(const spec_chain_args *a, const spec_truncation *t,
+                                        const spec_chain_out *o, void *ws, size_t ws_bytes,
+                                        void *stream) {
+  if (!a || !t) return SPEC_ERR_NULL;
+  if (a->mode != SPEC_STOCHASTIC) return SPEC_ERR_DTYPE;
+  if (!t->top_k && !t->top_p) return spec_verify_chain(a, o, ws, ws_bytes, stream);
+  if (a->B > 0) {
+    const void *q[] = {t->top_k, t->top_p};
+    for (const void *x : q)
+      if (x && !aligned(x, 4)) return SPEC_ERR_ALIGN;
+  }
+  if (!o) return SPEC_ERR_NULL;
+  if (!valid_sizes(a->B, a->V) || a->K < 0 || a->K > SPEC_MAX_K) return SPEC_ERR_SHAPE;
+  if (a->dtype != SPEC_F32 && a->dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  if (a->B == 0) return SPEC_OK;
+  const int K = a->K;
+  if (!a->target_logits || !o->accepted_len || !o->out_tokens || !o->num_emitted ||
+      !o->row_status || !a->u_sample)
+    return SPEC_ERR_NULL;
+  if (K > 0 && (!a->draft_tokens || !a->draft_logits || !a->u_accept)) return SPEC_ERR_NULL;
+  const int esz = a->dtype == SPEC_BF16 ? 2 : 4;
+  if (!aligned(a->target_logits, esz) || (a->draft_logits && !aligned(a->draft_logits, esz)))
+    return SPEC_ERR_ALIGN;
+  const void *i32s[] = {a->draft_tokens, a->temperature, a->u_accept, a->u_sample,
+                        o->accepted_len, o->out_tokens, o->num_emitted, o->row_status,
+                        o->p_at_draft, o->q_at_draft, o->resid_mass};
+  for (const void *x : i32s)
+    if (x && !aligned(x, 4)) return SPEC_ERR_ALIGN;
+  const size_t need = spec_verify_chain_workspace_size(a->B, K, a->V);
+  if (!ws || !aligned(ws, 256) || ws_bytes < need) return SPEC_ERR_WORKSPACE;
+  if (static_cast<long long>(a->B) * (2 * K + 1) > 0x7fffffffLL) return SPEC_ERR_SHAPE;
+  ChainStochParams p;
+  int grid = 0, nv = 0, C = 0;
+  size_t smem = 0;
+  {
+    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, smem, nv, C);
+    if (st != SPEC_OK) return st;
+  }
+  p.accepted_len = o->accepted_len;
+  p.out_tokens = o->out_tokens;
+  p.num_emitted = o->num_emitted;
+  p.row_status = o->row_status;
+  p.p_at_draft = o->p_at_draft;
+  p.q_at_draft = o->q_at_draft;
+  p.resid_mass = o->resid_mass;
+  p.top_k = t->top_k;
+  p.top_p = t->top_p;
+  p.trunc = p.trunc_area;
+  report("truncated grid cluster", grid, C, 0, 0, 0, 0, 0);
+  return launch_chain_truncated(p, a->dtype == SPEC_BF16, grid, smem, C,
+                                static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SPEC_OK
+             : SPEC_ERR_CUDA;
 }
 
 spec_status spec_drift_residuals(const spec_chain_args *a, int32_t m, int32_t *support,

@@ -197,6 +197,40 @@ __device__ __forceinline__ void stream_pos(int i, int B, int K, int *b, int *j) 
   *b = i - (K - *j) * B;
 }
 
+// Order-preserving integer key of a logit's raw bits (larger logit, larger
+// key; -inf smallest).
+template <bool BF16>
+__device__ __forceinline__ uint32_t order_key(uint32_t bits) {
+  if constexpr (BF16) return (bits & 0x8000u) ? (~bits & 0xFFFFu) : (bits | 0x8000u);
+  else return (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+}
+
+// Raw bits of element e of a 16-byte vector.
+template <bool BF16>
+__device__ __forceinline__ uint32_t elem_bits(const uint32_t *w, int e) {
+  if constexpr (BF16) return (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
+  else return w[e];
+}
+
+// The row's top-k / top-p parameters; false when neither truncates.
+__device__ __forceinline__ bool trunc_active(const ChainStochParams &P, int b, int V, int *k,
+                                             float *tp) {
+  *k = P.top_k ? P.top_k[b] : 0;
+  *tp = P.top_p ? P.top_p[b] : 1.0f;
+  const bool use_k = *k >= 1 && *k < V;
+  const bool use_p = *tp > 0.f && *tp < 1.f;
+  if (!use_k) *k = 0;
+  if (!use_p) *tp = 1.0f;
+  return use_k || use_p;
+}
+
+// Element offset of partial row `row` (targets b*(K+1)+j, then drafts
+// B*(K+1) + b*K + j) in its logits tensor.
+__device__ __forceinline__ long long row_offset(const ChainStochParams &P, int row) {
+  const int npos = P.K + 1;
+  return row < P.B * npos ? (long long)row * P.V : (long long)(row - P.B * npos) * P.V;
+}
+
 // A phase is a range of positions [p0, p1) of the stream; its tiles cost 1
 // (bonus position: target only) or 2 (target and draft).  Returns the first
 // tile (phase-relative) of CTA g's even share of the phase's cost.
@@ -597,8 +631,20 @@ struct alignas(16) ResolveCtrl {
   float u;                   // its u_sample
   int stop;                  // first rejecting position (K: none)
   uint32_t flags;            // row status bits
-  int pad;
+  int trunc;                 // the row is truncated (top-k / top-p)
+  uint32_t thp, thq;         // key thresholds of the stopping position's p and q
+  int pad2[2];
 };
+
+// Order-preserving key of a logit value held in fp32 (exact for bf16 logits).
+__device__ __forceinline__ uint32_t key_of(float l, bool bf16) {
+  const uint32_t u = __float_as_uint(l);
+  if (bf16) {
+    const uint32_t h = u >> 16;
+    return (h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u);
+  }
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
 
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
@@ -674,21 +720,32 @@ __device__ __forceinline__ RowScalars load_scalars(const ChainStochParams &P, in
 }
 
 __device__ void decide_row(const ChainStochParams &P, int b, float s2, uint32_t tflags, int lane,
-                           bool diag, const float4 *rstat, RowScalars first, ResolveCtrl &ctl) {
+                           bool diag, const float4 *rstat, RowScalars first, ResolveCtrl &ctl,
+                           bool bf16) {
   const int K = P.K, npos = K + 1, V = P.V;
   uint32_t flags = tflags;
+  int tk_;
+  float tp_;
+  const bool trunc = P.trunc && trunc_active(P, b, V, &tk_, &tp_);
   int stop = K;
   for (int j0 = 0; j0 < npos; j0 += 32) {
     const int j = j0 + lane;
     bool rejects = false;
     float4 tp = make_float4(-kInf, 0.f, 0.f, 0.f), dq = make_float4(-kInf, 0.f, 0.f, 0.f);
     float us = 0.f;
+    uint32_t thp = 0, thq = 0;  // truncation thresholds (0: keep all)
     if (j < npos) {
       const RowScalars sc = j0 == 0 ? first : load_scalars(P, b, j);
       us = sc.us;
       if (!(us >= 0.f && us < 1.f)) flags |= F_BAD_UNIFORM;
       tp = rstat[j];
       flags |= __float_as_uint(tp.w);
+      if (trunc) {  // the kept mass replaces the full sum
+        const TruncRec rt = P.trunc[(size_t)b * npos + j];
+        flags |= rt.flags ? F_TIMEOUT : 0u;
+        thp = rt.theta;
+        tp.y = rt.kept;
+      }
       if (tp.x != tp.x || tp.x == kInf) flags |= F_NONFINITE;
       else if (tp.x == -kInf) flags |= F_EMPTY;
       if (j < K) {
@@ -698,11 +755,20 @@ __device__ void decide_row(const ChainStochParams &P, int b, float s2, uint32_t 
         if (y < 0 || y >= V) flags |= F_BAD_TOKEN;
         dq = rstat[npos + j];
         flags |= __float_as_uint(dq.w);
+        if (trunc) {
+          const TruncRec rd = P.trunc[(size_t)P.B * npos + (size_t)b * K + j];
+          flags |= rd.flags ? F_TIMEOUT : 0u;
+          thq = rd.theta;
+          dq.y = rd.kept;
+        }
         if (dq.x != dq.x || dq.x == kInf) flags |= F_NONFINITE;
         else if (dq.x == -kInf) flags |= F_EMPTY;
         // ratio p(y)/q(y) in log2 space: identical logits give exactly 0
-        const float l2p = __fadd_rn(__fmaf_rn(tp.z, s2, -__fmul_rn(tp.x, s2)), -lg2(tp.y));
-        const float l2q = __fadd_rn(__fmaf_rn(dq.z, s2, -__fmul_rn(dq.x, s2)), -lg2(dq.y));
+        // (a token outside a truncated law has probability 0)
+        const float l2p = key_of(tp.z, bf16) < thp ? -kInf
+                        : __fadd_rn(__fmaf_rn(tp.z, s2, -__fmul_rn(tp.x, s2)), -lg2(tp.y));
+        const float l2q = key_of(dq.z, bf16) < thq ? -kInf
+                        : __fadd_rn(__fmaf_rn(dq.z, s2, -__fmul_rn(dq.x, s2)), -lg2(dq.y));
         const float l2r = __fadd_rn(l2p, -l2q);
         rejects = !((l2r >= 0.f) || (ua < ex2(l2r)));
         if (diag) {
@@ -721,6 +787,8 @@ __device__ void decide_row(const ChainStochParams &P, int b, float s2, uint32_t 
       ctl.Mq = found_here ? dq.x : -kInf;
       ctl.Sq = found_here ? dq.y : 0.f;
       ctl.u = us;
+      ctl.thp = thp;
+      ctl.thq = found_here ? thq : 0u;
     }
     if (found_here) stop = j0 + src;
   }
@@ -731,6 +799,7 @@ __device__ void decide_row(const ChainStochParams &P, int b, float s2, uint32_t 
   if (lane == 0) {
     ctl.stop = stop;
     ctl.flags = flags;
+    ctl.trunc = trunc;
   }
 }
 
@@ -778,7 +847,7 @@ __global__ void __launch_bounds__(kResolveThreads, 4) chain_resolve_kernel(const
   }
   fold_rows(P, b, s2, gen + 1u, warp, lane, rstat);
   __syncthreads();
-  if (warp == 0) decide_row(P, b, s2, tflags, lane, crank == 0, rstat, first, ctl);
+  if (warp == 0) decide_row(P, b, s2, tflags, lane, crank == 0, rstat, first, ctl, BF16);
   __syncthreads();
   const uint32_t flags = ctl.flags;
   const int stop = ctl.stop;
@@ -816,17 +885,35 @@ __global__ void __launch_bounds__(kResolveThreads, 4) chain_resolve_kernel(const
   int xs = 0;
   int owner_cta = -1;
   float t_c = 0.f;
-  // mass of element e of a vector pair under the current task
+  // mass of element e of a vector pair under the current task (with
+  // truncation, tokens below a law's threshold have probability 0)
+  const bool trunc = ctl.trunc != 0;
+  const uint32_t thp = ctl.thp, thq = ctl.thq;
   auto mass = [&](const uint32_t *wp, const uint32_t *wq, int e) {
-    const float pe = ex2(__fmaf_rn(F::elem(wp, e), s2, nMp));
+    const bool kp = !trunc || order_key<BF16>(elem_bits<BF16>(wp, e)) >= thp;
+    const float pe = kp ? ex2(__fmaf_rn(F::elem(wp, e), s2, nMp)) : 0.f;
     if (task == 2) return pe;
-    const float qe = ex2(__fmaf_rn(F::elem(wq, e), s2, nMq));
+    const bool kq = !trunc || order_key<BF16>(elem_bits<BF16>(wq, e)) >= thq;
+    const float qe = kq ? ex2(__fmaf_rn(F::elem(wq, e), s2, nMq)) : 0.f;
     return fmaxf(__fmaf_rn(pe, iSp, -__fmul_rn(qe, iSq)), 0.f);
   };
   while (true) {
     // ---- pass: per-round masses (kept for the search), then the CTA total
     float tsum = 0.f;
-    if (aligned && task == 1) {
+    if (trunc) {  // truncated laws: element by element, with the thresholds
+#pragma unroll 1
+      for (int k = 0; k < nr; ++k) {
+        const int v = vbase + 32 * k + lane;
+        uint32_t wp[4], wq[4];
+        F::load_vec(wp, nullptr, tg, aligned, v, len);
+        if (task == 1) F::load_vec(wq, nullptr, dg, aligned, v, len);
+        float r = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) r += mass(wp, wq, e);
+        rsum[k * NT + tid] = r;
+        tsum += r;
+      }
+    } else if (aligned && task == 1) {
 #pragma unroll 1
       for (int k0 = 0; k0 < nr; k0 += 4) {
         uint4 vp[4], vq[4];
@@ -1036,18 +1123,7 @@ struct alignas(16) DriftCtrl {
   uint32_t flags;
 };
 
-template <bool BF16>
-__device__ __forceinline__ uint32_t order_key(uint32_t bits) {
-  if constexpr (BF16) return (bits & 0x8000u) ? (~bits & 0xFFFFu) : (bits | 0x8000u);
-  else return (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
-}
 
-// Raw bits of element e of a 16-byte vector.
-template <bool BF16>
-__device__ __forceinline__ uint32_t elem_bits(const uint32_t *w, int e) {
-  if constexpr (BF16) return (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
-  else return w[e];
-}
 
 template <bool BF16>
 __global__ void __launch_bounds__(kDriftThreads) drift_select_kernel(const __grid_constant__ ChainStochParams P) {
@@ -1433,6 +1509,257 @@ __global__ void __launch_bounds__(kDriftThreads) drift_select_kernel(const __gri
   }
 }
 
+// ============================================================ truncation
+//
+// "Speculative Decoding: Draft, Verify, and Correct", 'Preserve the
+// distribution you actually intend': when top-k / top-p define the sampling
+// law, acceptance and correction use the truncated p, and q is the truncated
+// law that produced the draft.  Per logit row this kernel finds the key
+// threshold theta of the kept set -- top-k: the largest theta with at least
+// k keys >= theta (boundary ties kept); then top-p: the largest theta whose
+// keys >= theta carry at least top_p of the top-k mass -- and the kept mass.
+// Both searches are bisections on the integer key over a candidate list
+// (every key at or above a sampled threshold); rows the candidates cannot
+// settle are searched over the whole row.  Sums run in a fixed order, so
+// the result is deterministic.
+
+
+// Largest key x (0 .. 2^bits - 1) with pred(x) true, pred being monotone
+// (true for small x).
+template <typename Pred>
+__device__ __forceinline__ uint32_t largest_key(int bits, Pred pred) {
+  uint32_t x = 0;
+  for (int bit = bits - 1; bit >= 0; --bit) {
+    const uint32_t c = x | (1u << bit);
+    if (pred(c)) x = c;
+  }
+  return x;
+}
+
+struct alignas(16) TruncCtrl {
+  uint32_t key[kDriftCand];
+  float e[kDriftCand];
+  float fred[kDriftWarps];
+  int ired[kDriftWarps];
+  int chist[256];
+  int n_cand, digit, above;
+  float M, S;
+  uint32_t flags;
+};
+
+template <bool BF16>
+__global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_constant__ ChainStochParams P) {
+  using F = Fmt<BF16>;
+  constexpr int EPV = F::EPV, ESZ = F::ESZ;
+  constexpr int KEYBITS = BF16 ? 16 : 32;
+  __shared__ TruncCtrl ctl;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K = P.K, V = P.V, npos = K + 1;
+  const int row = blockIdx.x;  // partial-row numbering: targets, then drafts
+  const bool is_target = row < P.B * npos;
+  const int b = is_target ? row / npos : (row - P.B * npos) / max(K, 1);
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // Every CTA waits for the stream kernel before it leaves, even when its
+  // row is not truncated: the resolve kernel waits only for this grid, so
+  // this grid must not complete before the stream kernel has.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  int tk;
+  float tp;
+  if (!trunc_active(P, b, V, &tk, &tp)) return;
+  const float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
+  const float s2 = (T > 0.f && T < kInf) ? __fdiv_rn(kLog2e, T) : 1.f;
+  const uint32_t gen = *reinterpret_cast<volatile const uint32_t *>(P.gen - 1 - b);
+  // ---- this row's max and sum (warp 0 folds its partial records)
+  const int nt = P.nslices;
+  if (warp == 0) {
+    float m = -kInf, sacc = 0.f;
+    uint32_t f = 0;
+    for (int t = lane; t < nt; t += 32) {
+      const SoftPart q = P.part[(size_t)row * nt + t];
+      f |= q.flags;
+      if (__float_as_uint(q.stamp) != gen + 1u) f |= F_TIMEOUT;
+      const float mn = fmax_nan(m, q.m);
+      sacc = (m == -kInf ? 0.f : sacc * ex2(__fmul_rn(m - mn, s2))) +
+             (q.m == -kInf ? 0.f : q.s * ex2(__fmul_rn(q.m - mn, s2)));
+      m = mn;
+    }
+    float Mw, Sw;
+    fold_max_sum(m, sacc, s2, &Mw, &Sw);
+    f = __reduce_or_sync(FULL_MASK, f);
+    if (lane == 0) {
+      if (Mw != Mw || Mw == kInf || Mw == -kInf) f |= F_NONFINITE;
+      ctl.M = Mw;
+      ctl.S = Sw;
+      ctl.flags = f;
+    }
+  }
+  __syncthreads();
+  TruncRec *rec = P.trunc + row;
+  if (ctl.flags) {  // the resolve kernel flags this row from its own fold
+    if (tid == 0) *rec = TruncRec{0u, 0.f, 1u, 0u};
+    return;
+  }
+  const float nM = -__fmul_rn(ctl.M, s2);
+  const char *src = static_cast<const char *>(is_target ? P.target : P.draft) + (size_t)row_offset(P, row) * ESZ;
+  const bool aligned = P.use_tma != 0;
+  const int nvec = (V + EPV - 1) / EPV;
+  auto bits_at = [&](int i) -> uint32_t {
+    if constexpr (BF16) return __ldg(reinterpret_cast<const unsigned short *>(src) + i);
+    else return __ldg(reinterpret_cast<const unsigned int *>(src) + i);
+  };
+  auto mass_of = [&](uint32_t bits) {  // exp2((l - M) s2) of one element
+    const float l = BF16 ? __uint_as_float(bits << 16) : __uint_as_float(bits);
+    return l == -kInf ? 0.f : ex2(__fmaf_rn(l, s2, nM));
+  };
+  // block sums in a fixed order
+  auto block_sum_i = [&](int v) {
+    v = __reduce_add_sync(FULL_MASK, v);
+    if (lane == 0) ctl.ired[warp] = v;
+    __syncthreads();
+    int t = 0;
+    for (int w2 = 0; w2 < kDriftWarps; ++w2) t += ctl.ired[w2];
+    __syncthreads();
+    return t;
+  };
+  auto block_sum_f = [&](float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL_MASK, v, o);
+    if (lane == 0) ctl.fred[warp] = v;
+    __syncthreads();
+    float t = 0.f;
+    for (int w2 = 0; w2 < kDriftWarps; ++w2) t += ctl.fred[w2];
+    __syncthreads();
+    return t;
+  };
+  // ---- sampled threshold tau (as in the DRIFT selection): the r-th largest
+  // key of every kDriftSample-th element
+  const int n_samples = (V + kDriftSample - 1) / kDriftSample;
+  auto sample_tau = [&](int r) -> uint32_t {
+    if (r > n_samples) return 0u;
+    return largest_key(KEYBITS, [&](uint32_t x) {
+      int c = 0;
+      for (int i = tid * kDriftSample; i < V; i += kDriftThreads * kDriftSample)
+        c += order_key<BF16>(bits_at(i)) >= x;
+      return block_sum_i(c) >= r;
+    });
+  };
+  // ---- candidates: every key >= tau, with its mass
+  auto collect = [&](uint32_t tau) {
+    if (tid == 0) ctl.n_cand = 0;
+    __syncthreads();
+    constexpr int U = 4;
+    for (int v0 = tid; v0 < nvec; v0 += U * kDriftThreads) {
+      uint32_t w[U][4];
+#pragma unroll
+      for (int u = 0; u < U; ++u) F::load_vec(w[u], nullptr, src, aligned, v0 + u * kDriftThreads, V);
+      const unsigned act = __activemask();
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          const int idx = (v0 + u * kDriftThreads) * EPV + e;
+          const uint32_t bits = elem_bits<BF16>(w[u], e);
+          const uint32_t k = order_key<BF16>(bits);
+          const bool c = k >= tau && idx < V;
+          const unsigned bal = __ballot_sync(act, c);
+          if (bal) {
+            const int leader = __ffs(bal) - 1;
+            int base = 0;
+            if (lane == leader) base = atomicAdd(&ctl.n_cand, __popc(bal));
+            base = __shfl_sync(act, base, leader);
+            if (c) {
+              const int slot = base + __popc(bal & ((1u << lane) - 1u));
+              if (slot < kDriftCand) {
+                ctl.key[slot] = k;
+                ctl.e[slot] = mass_of(bits);
+              }
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();
+    return ctl.n_cand;
+  };
+  auto cand_count = [&](uint32_t x, int nc) {
+    int c = 0;
+    for (int i = tid; i < nc; i += kDriftThreads) c += ctl.key[i] >= x;
+    return block_sum_i(c);
+  };
+  auto cand_mass = [&](uint32_t x, int nc) {
+    float sm = 0.f;
+    for (int i = tid; i < nc; i += kDriftThreads) sm += ctl.key[i] >= x ? ctl.e[i] : 0.f;
+    return block_sum_f(sm);
+  };
+  uint32_t theta = 0;
+  float kept = 0.f;
+  bool done = false;
+  int r = tk > 0 ? max(16, (2 * tk) / kDriftSample + 2) : 16;
+  for (int attempt = 0; attempt < 3 && !done; ++attempt) {
+    const uint32_t tau = sample_tau(r);
+    const int nc = collect(tau);
+    if (nc > kDriftCand) {  // too many: raise the threshold
+      if (r <= 1) break;
+      r = max(1, r / 4);
+      continue;
+    }
+    uint32_t thk = tau;
+    float Sk = ctl.S;
+    if (tk > 0) {
+      if (nc < tk) {  // the top k are not all candidates: lower the threshold
+        r *= 4;
+        continue;
+      }
+      thk = largest_key(KEYBITS, [&](uint32_t x) { return cand_count(x, nc) >= tk; });
+      Sk = cand_mass(thk, nc);
+    }
+    if (tp < 1.f) {
+      const float target = __fmul_rn(tp, Sk);
+      if (!(cand_mass(tau, nc) >= target)) {  // the nucleus reaches below tau
+        r *= 4;
+        continue;
+      }
+      theta = largest_key(KEYBITS, [&](uint32_t x) { return cand_mass(x, nc) >= target; });
+      kept = cand_mass(theta, nc);
+    } else {
+      theta = thk;
+      kept = Sk;
+    }
+    done = true;
+  }
+  if (!done) {
+    // the whole row: the same searches, every evaluation one pass over it
+    auto row_count = [&](uint32_t x) {
+      int c = 0;
+      for (int i = tid; i < V; i += kDriftThreads) c += order_key<BF16>(bits_at(i)) >= x;
+      return block_sum_i(c);
+    };
+    auto row_mass = [&](uint32_t x) {
+      float sm = 0.f;
+      for (int i = tid; i < V; i += kDriftThreads) {
+        const uint32_t bits = bits_at(i);
+        if (order_key<BF16>(bits) >= x) sm += mass_of(bits);
+      }
+      return block_sum_f(sm);
+    };
+    uint32_t thk = 0;
+    float Sk = ctl.S;
+    if (tk > 0) {
+      thk = largest_key(KEYBITS, [&](uint32_t x) { return row_count(x) >= tk; });
+      Sk = row_mass(thk);
+    }
+    if (tp < 1.f) {
+      const float target = __fmul_rn(tp, Sk);
+      theta = largest_key(KEYBITS, [&](uint32_t x) { return row_mass(x) >= target; });
+      kept = row_mass(theta);
+    } else {
+      theta = thk;
+      kept = Sk;
+    }
+  }
+  if (tid == 0) *rec = TruncRec{theta, kept, 0u, 0u};
+}
+
 size_t resolve_smem(const ChainStochParams &p) {
   return static_cast<size_t>(2 * p.K + 1) * 16 + static_cast<size_t>(p.vpw / 32) * kResolveThreads * 4;
 }
@@ -1470,6 +1797,9 @@ cudaError_t prepare(size_t smem, int cluster) {
   return cudaSuccess;
 }
 
+template <bool BF16>
+cudaError_t launch_resolve(const ChainStochParams &p, int cluster, cudaStream_t s);
+
 template <bool BF16, int NV, int S>
 cudaError_t launch_t(const ChainStochParams &p, int grid, size_t smem, int cluster,
                      cudaStream_t s) {
@@ -1478,6 +1808,35 @@ cudaError_t launch_t(const ChainStochParams &p, int grid, size_t smem, int clust
   softmax_partials_kernel<BF16, NV, S><<<grid, kSoftThreads + 32, smem, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  return launch_resolve<BF16>(p, cluster, s);
+}
+
+template <bool BF16, int NV, int S>
+cudaError_t launch_truncated_t(const ChainStochParams &p, int grid, size_t smem, int cluster,
+                               cudaStream_t s) {
+  cudaError_t e = prepare<BF16, NV, S>(smem, cluster);
+  if (e != cudaSuccess) return e;
+  softmax_partials_kernel<BF16, NV, S><<<grid, kSoftThreads + 32, smem, s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.B * (p.K + 1) + p.B * p.K));
+  cfg.blockDim = dim3(kDriftThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, trunc_kernel<BF16>, p);
+  if (e != cudaSuccess) return e;
+  return launch_resolve<BF16>(p, cluster, s);
+}
+
+// The resolve kernel: a cluster of `cluster` CTAs per row, a programmatic
+// dependent of the kernel launched just before it.
+template <bool BF16>
+cudaError_t launch_resolve(const ChainStochParams &p, int cluster, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.B * cluster));
   cfg.blockDim = dim3(kResolveThreads);
@@ -1530,6 +1889,15 @@ cudaError_t launch_chain_stochastic(const ChainStochParams &p, bool bf16, int nv
   if (p.stages == 3)
     return bf16 ? launch_t<true, 4, 3>(p, grid, smem, cluster, s) : launch_t<false, 4, 3>(p, grid, smem, cluster, s);
   return bf16 ? launch_t<true, 4, 2>(p, grid, smem, cluster, s) : launch_t<false, 4, 2>(p, grid, smem, cluster, s);
+}
+
+cudaError_t launch_chain_truncated(const ChainStochParams &p, bool bf16, int grid, size_t smem,
+                                   int cluster, cudaStream_t s) {
+  if (p.stages == 3)
+    return bf16 ? launch_truncated_t<true, 4, 3>(p, grid, smem, cluster, s)
+                : launch_truncated_t<false, 4, 3>(p, grid, smem, cluster, s);
+  return bf16 ? launch_truncated_t<true, 4, 2>(p, grid, smem, cluster, s)
+              : launch_truncated_t<false, 4, 2>(p, grid, smem, cluster, s);
 }
 
 cudaError_t launch_drift(const ChainStochParams &p, bool bf16, int grid, size_t smem,

@@ -19,6 +19,16 @@ struct alignas(16) SoftPart {
   uint32_t flags;
 };
 
+// Truncation of one logit row (top-k / top-p): the kept tokens are those
+// whose order-preserving key is >= theta; kept holds sum exp2((l - m) s2)
+// over them, m being the row's max logit.
+struct alignas(16) TruncRec {
+  uint32_t theta;
+  float kept;
+  uint32_t flags;  // nonzero: no threshold was found (the row is flagged)
+  uint32_t pad;
+};
+
 // One 16-byte partial per (row, position, vocabulary slice) written by the
 // greedy kernel: the slice's largest logit and its lowest index.
 struct alignas(16) GreedyPart {
@@ -66,6 +76,12 @@ struct ChainStochParams {
   uint32_t *gen;       // gen[-1 - b]: generation word of row b
   int dyn;             // 0: static assignment only
   int dyn_chunk;       // tiles per claim
+  // top-k / top-p truncation (spec_verify_chain_truncated): per-row
+  // parameters (NULL: off) and one record per logit row
+  const int32_t *top_k;
+  const float *top_p;
+  TruncRec *trunc;        // NULL: no truncation
+  TruncRec *trunc_area;   // where the workspace keeps the records
   // DRIFT residual extraction (spec_drift_residuals): support size and outputs
   int drift_m;
   int32_t *drift_support;   // [B, K, m]
@@ -142,6 +158,9 @@ constexpr int kDriftMaxSupport = 64;  // largest support size m
 // of its launches.
 cudaError_t launch_chain_stochastic(const ChainStochParams &p, bool bf16, int nv, int grid,
                                     size_t smem, int cluster, cudaStream_t s);
+// Stream kernel, truncation thresholds, then the resolve kernel.
+cudaError_t launch_chain_truncated(const ChainStochParams &p, bool bf16, int grid, size_t smem,
+                                   int cluster, cudaStream_t s);
 // Stream kernel then the DRIFT selection kernel (one CTA per drafted position).
 cudaError_t launch_drift(const ChainStochParams &p, bool bf16, int grid, size_t smem,
                          cudaStream_t s);

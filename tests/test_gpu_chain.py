@@ -268,3 +268,57 @@ def test_workspace_first_use_and_reuse(sv, name):
             assert magic == WS_MAGIC, (fill, call, hex(magic))
             claim = int(ws[end - 16:end - 12].cpu().numpy().view(np.uint32)[0])
             assert claim == 0  # the resolve kernel left the counter reset
+
+
+# ------------------------------------------------------ top-k / top-p truncation
+def _trunc_params(rng, B, V):
+    k = rng.choice([0, 1, 2, 20, 50, 1000, V], B).astype(np.int32)
+    p = rng.choice([1.0, 0.5, 0.8, 0.9, 0.99], B).astype(np.float32)
+    return k, p
+
+
+def run_trunc(sv, inp, k, p):
+    g = sv.spec_verify_chain(cuda(inp["target"]), cuda(inp["draft"]), cuda(inp["draft_tokens"]),
+                             cuda(inp.get("temperature")), cuda(inp.get("u_accept")),
+                             cuda(inp.get("u_sample")), diagnostics=True, top_k=cuda(k),
+                             top_p=cuda(p))
+    return host(g)
+
+
+@pytest.mark.parametrize("name", ["c2", "c3", "c5"])
+def test_truncated_workloads(sv, name):
+    inp = S.make(name, B=48) if name == "c5" else S.make(name)
+    B, _, V = inp["target"].shape
+    k, p = _trunc_params(np.random.default_rng(len(name) + B), B, V)
+    # draft tokens drawn from the untruncated q may fall outside q's kept set:
+    # both sides then take q'(y) = 0 (accept iff p'(y) > 0)
+    g = run_trunc(sv, inp, k, p)
+    o = O.verify_chain(inp["target"], inp["draft"], inp["draft_tokens"], inp.get("temperature"),
+                       inp["u_accept"], inp["u_sample"], top_k=k, top_p=p)
+    n_band = compare_stochastic(g, o)
+    assert n_band <= max(1, B // 50)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_truncated_flat_rows_ties_and_fp32(sv, dtype):
+    """Flat rows (the nucleus spans most of the vocabulary: the whole-row
+    search), rows of ties at the top-k boundary, and small vocabularies."""
+    rng = np.random.default_rng(21)
+    B, K, V = 12, 3, 3000
+    t = rng.normal(0, 0.05, (B, K + 1, V)).astype(np.float32)   # nearly flat
+    t[:4] = rng.normal(0, 3, (4, K + 1, V)).astype(np.float32)  # peaked rows
+    t[4:6, :, :40] = 2.0                                        # 40-way ties at the top
+    d = (t[:, :K] + rng.normal(0, 0.5, (B, K, V))).astype(np.float32)
+    if dtype == "bf16":
+        t, d = S.f32_to_bf16_bits(t), S.f32_to_bf16_bits(d)
+    toks = rng.integers(0, V, (B, K)).astype(np.int32)
+    inp = dict(target=t, draft=d, draft_tokens=toks,
+               temperature=np.full(B, 0.9, np.float32),
+               u_accept=rng.random((B, K), dtype=np.float32),
+               u_sample=rng.random((B, K + 1), dtype=np.float32))
+    k = np.array([0, 5, 50, 0, 20, 41, 0, 10, 0, 2999, 1, 0], np.int32)
+    p = np.array([0.9, 1, 0.7, 0.3, 1, 0.95, 0.9, 0.5, 0.99, 0.8, 1, 0.6], np.float32)
+    g = run_trunc(sv, inp, k, p)
+    o = O.verify_chain(t, d, toks, inp["temperature"], inp["u_accept"], inp["u_sample"],
+                       top_k=k, top_p=p)
+    assert compare_stochastic(g, o) <= 1
