@@ -1089,6 +1089,67 @@ __global__ void __launch_bounds__(kResolveThreads, 4) chain_resolve_kernel(const
   cluster_wait();  // no CTA leaves while a peer may still read its mailbox
 }
 
+// ============================================================ block selection
+//
+// Block-wide radix selection, 8 bits a pass from the top, of the r-th
+// largest key of a set that `each(f)` enumerates (every thread hands its own
+// keys to f).  Needs at least r keys.  Returns the key; n_above and n_equal
+// count the keys above it and equal to it.  Every thread of the block calls
+// it; chist (256 ints), s_digit and s_above are shared scratch.
+template <int KEYBITS, int NT, typename Each>
+__device__ uint32_t block_kth_largest(Each each, int r, int *chist, int *s_digit, int *s_above,
+                                      int &n_above, int &n_equal) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t prefix = 0, pmask = 0;
+  int rem = r, in = 0;
+  for (int shift = KEYBITS - 8; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += NT) chist[i] = 0;
+    __syncthreads();
+    each([&](uint32_t k) {
+      if ((k & pmask) == prefix) atomicAdd(&chist[(k >> shift) & 255u], 1);
+    });
+    __syncthreads();
+    if (warp == 0) {  // lane l owns bins 255-8l .. 248-8l
+      int cnt[8], own = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        cnt[i] = chist[255 - 8 * lane - i];
+        own += cnt[i];
+      }
+      int incl = own;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(FULL_MASK, incl, o);
+        if (lane >= o) incl += n;
+      }
+      int above = incl - own;
+      if (above < rem && rem <= incl) {
+        int dgt = 255 - 8 * lane;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (above + cnt[i] >= rem) {
+            dgt = 255 - 8 * lane - i;
+            break;
+          }
+          above += cnt[i];
+        }
+        *s_digit = dgt;
+        *s_above = above;
+      }
+    }
+    __syncthreads();
+    const int dgt = *s_digit;
+    rem -= *s_above;
+    in = chist[dgt];
+    prefix |= static_cast<uint32_t>(dgt) << shift;
+    pmask |= 255u << shift;
+    __syncthreads();
+  }
+  n_above = r - rem;
+  n_equal = in;
+  return prefix;
+}
+
 // ============================================================ DRIFT selection
 //
 // "Speculative Decoding Under Distribution Shift: DRIFT Recalibration" (the
@@ -1197,67 +1258,9 @@ __global__ void __launch_bounds__(kDriftThreads) drift_select_kernel(const __gri
     res[rank] = __fmul_rn(__fadd_rn(l2p, -l2q), kLn2);
   };
 
-  // One radix digit of a block-wide key set: keys matching `prefix` on
-  // `pmask` are counted by their digit at `shift`; returns the digit holding
-  // the rem-th largest, the count above it and the count in it.
-  auto digit_pass = [&](auto for_each_key, int shift, uint32_t prefix, uint32_t pmask, int rem,
-                        int &above_out, int &in_out) {
-    for (int i = tid; i < 256; i += kDriftThreads) ctl.chist[i] = 0;
-    __syncthreads();
-    for_each_key([&](uint32_t k) {
-      if ((k & pmask) == prefix) atomicAdd(&ctl.chist[(k >> shift) & 255u], 1);
-    });
-    __syncthreads();
-    if (warp == 0) {
-      int cnt[8], own = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        cnt[i] = ctl.chist[255 - 8 * lane - i];
-        own += cnt[i];
-      }
-      int incl = own;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(FULL_MASK, incl, o);
-        if (lane >= o) incl += n;
-      }
-      int above = incl - own;
-      if (above < rem && rem <= incl) {
-        int dgt = 255 - 8 * lane;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (above + cnt[i] >= rem) {
-            dgt = 255 - 8 * lane - i;
-            break;
-          }
-          above += cnt[i];
-        }
-        ctl.digit = dgt;
-        ctl.above = above;
-      }
-    }
-    __syncthreads();
-    const int dgt = ctl.digit;
-    above_out = ctl.above;
-    in_out = ctl.chist[dgt];
-    __syncthreads();
-    return dgt;
-  };
-  // The r-th largest key of a set with at least r keys: its value, the
-  // number of keys above it and the number equal to it.
-  auto kth_largest = [&](auto for_each_key, int r, int &n_above, int &n_equal) {
-    uint32_t prefix = 0, pmask = 0;
-    int rem = r, in = 0;
-    for (int shift = KEYBITS - 8; shift >= 0; shift -= 8) {
-      int above = 0;
-      const int dgt = digit_pass(for_each_key, shift, prefix, pmask, rem, above, in);
-      rem -= above;
-      prefix |= static_cast<uint32_t>(dgt) << shift;
-      pmask |= 255u << shift;
-    }
-    n_above = r - rem;
-    n_equal = in;
-    return prefix;
+  auto kth_largest = [&](auto each, int r, int &n_above, int &n_equal) {
+    return block_kth_largest<KEYBITS, kDriftThreads>(each, r, ctl.chist, &ctl.digit, &ctl.above,
+                                                    n_above, n_equal);
   };
 
   // ---- threshold: the r-th largest key of a strided sample (every
@@ -1537,12 +1540,12 @@ __device__ __forceinline__ uint32_t largest_key(int bits, Pred pred) {
 }
 
 struct alignas(16) TruncCtrl {
-  uint32_t key[kDriftCand];
-  float e[kDriftCand];
+  unsigned long long ck[kDriftCand];  // (key << 32) | (~token id): sorts key desc, id asc
+  float e[kDriftCand];                // candidate masses, then their prefix sums
   float fred[kDriftWarps];
   int ired[kDriftWarps];
   int chist[256];
-  int n_cand, digit, above;
+  int n_cand, digit, above, pos;
   float M, S;
   uint32_t flags;
 };
@@ -1634,14 +1637,15 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
   // ---- sampled threshold tau (as in the DRIFT selection): the r-th largest
   // key of every kDriftSample-th element
   const int n_samples = (V + kDriftSample - 1) / kDriftSample;
+  auto samples = [&](auto f) {
+    for (int i = tid * kDriftSample; i < V; i += kDriftThreads * kDriftSample)
+      f(order_key<BF16>(bits_at(i)));
+  };
   auto sample_tau = [&](int r) -> uint32_t {
     if (r > n_samples) return 0u;
-    return largest_key(KEYBITS, [&](uint32_t x) {
-      int c = 0;
-      for (int i = tid * kDriftSample; i < V; i += kDriftThreads * kDriftSample)
-        c += order_key<BF16>(bits_at(i)) >= x;
-      return block_sum_i(c) >= r;
-    });
+    int na, ne;
+    return block_kth_largest<KEYBITS, kDriftThreads>(samples, r, ctl.chist, &ctl.digit, &ctl.above,
+                                                    na, ne);
   };
   // ---- candidates: every key >= tau, with its mass
   auto collect = [&](uint32_t tau) {
@@ -1670,7 +1674,7 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
             if (c) {
               const int slot = base + __popc(bal & ((1u << lane) - 1u));
               if (slot < kDriftCand) {
-                ctl.key[slot] = k;
+                ctl.ck[slot] = (static_cast<unsigned long long>(k) << 32) | (~static_cast<uint32_t>(idx));
                 ctl.e[slot] = mass_of(bits);
               }
             }
@@ -1681,15 +1685,58 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
     __syncthreads();
     return ctl.n_cand;
   };
-  auto cand_count = [&](uint32_t x, int nc) {
-    int c = 0;
-    for (int i = tid; i < nc; i += kDriftThreads) c += ctl.key[i] >= x;
-    return block_sum_i(c);
-  };
-  auto cand_mass = [&](uint32_t x, int nc) {
-    float sm = 0.f;
-    for (int i = tid; i < nc; i += kDriftThreads) sm += ctl.key[i] >= x ? ctl.e[i] : 0.f;
-    return block_sum_f(sm);
+  auto key_at = [&](int i) { return static_cast<uint32_t>(ctl.ck[i] >> 32); };
+  // ---- sort the candidates (key desc, id asc) and prefix-sum their masses
+  auto sort_and_scan = [&](int nc) {
+    int N = 64;
+    while (N < nc) N <<= 1;
+    for (int i = nc + tid; i < N; i += kDriftThreads) {
+      ctl.ck[i] = 0ull;
+      ctl.e[i] = 0.f;
+    }
+    __syncthreads();
+    for (int size = 2; size <= N; size <<= 1) {  // bitonic, descending
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int t = tid; t < N / 2; t += kDriftThreads) {
+          const int lo = 2 * t - (t & (stride - 1)), hi = lo + stride;
+          const bool up = (lo & size) == 0;
+          const unsigned long long a = ctl.ck[lo], c = ctl.ck[hi];
+          if ((a < c) == up) {
+            ctl.ck[lo] = c;
+            ctl.ck[hi] = a;
+            const float t0 = ctl.e[lo];
+            ctl.e[lo] = ctl.e[hi];
+            ctl.e[hi] = t0;
+          }
+        }
+        __syncthreads();
+      }
+    }
+    // inclusive prefix sums in sorted order: four consecutive per thread
+    constexpr int PER = kDriftCand / kDriftThreads;
+    float v[PER], run = 0.f;
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int i = tid * PER + q;
+      run += i < N ? ctl.e[i] : 0.f;
+      v[q] = run;
+    }
+    float incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float n = __shfl_up_sync(FULL_MASK, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) ctl.fred[warp] = incl;
+    __syncthreads();
+    float off = incl - run;
+    for (int w2 = 0; w2 < warp; ++w2) off += ctl.fred[w2];
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int i = tid * PER + q;
+      if (i < N) ctl.e[i] = off + v[q];
+    }
+    __syncthreads();
   };
   uint32_t theta = 0;
   float kept = 0.f;
@@ -1703,26 +1750,48 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
       r = max(1, r / 4);
       continue;
     }
-    uint32_t thk = tau;
+    if (nc < max(tk, 1)) {  // the top k are not all candidates: lower it
+      r *= 4;
+      continue;
+    }
+    sort_and_scan(nc);
+    // top-k: the k-th candidate's key, through the end of its group of ties
+    int gk = nc - 1;
     float Sk = ctl.S;
     if (tk > 0) {
-      if (nc < tk) {  // the top k are not all candidates: lower the threshold
-        r *= 4;
-        continue;
+      if (tid == 0) {
+        int g = tk - 1;
+        while (g + 1 < nc && key_at(g + 1) == key_at(tk - 1)) ++g;
+        ctl.pos = g;
       }
-      thk = largest_key(KEYBITS, [&](uint32_t x) { return cand_count(x, nc) >= tk; });
-      Sk = cand_mass(thk, nc);
+      __syncthreads();
+      gk = ctl.pos;
+      Sk = ctl.e[gk];
     }
     if (tp < 1.f) {
       const float target = __fmul_rn(tp, Sk);
-      if (!(cand_mass(tau, nc) >= target)) {  // the nucleus reaches below tau
+      if (tk == 0 && !(ctl.e[nc - 1] >= target)) {  // the nucleus reaches below tau
         r *= 4;
+        __syncthreads();
         continue;
       }
-      theta = largest_key(KEYBITS, [&](uint32_t x) { return cand_mass(x, nc) >= target; });
-      kept = cand_mass(theta, nc);
+      if (tid == 0) {  // first prefix reaching the target, then the end of its group
+        int lo = 0, hi = gk;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (ctl.e[mid] >= target) hi = mid;
+          else lo = mid + 1;
+        }
+        int g = lo;
+        while (g + 1 < nc && key_at(g + 1) == key_at(lo)) ++g;
+        ctl.pos = lo;
+        ctl.digit = g;
+      }
+      __syncthreads();
+      theta = key_at(ctl.pos);
+      kept = ctl.e[ctl.digit];
     } else {
-      theta = thk;
+      theta = key_at(gk);
       kept = Sk;
     }
     done = true;
