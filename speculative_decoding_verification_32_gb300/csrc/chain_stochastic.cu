@@ -33,6 +33,7 @@
 #include <cuda_bf16.h>
 
 #include <atomic>
+#include <cstddef>
 
 #include "common.cuh"
 #include "internal.h"
@@ -191,10 +192,18 @@ struct alignas(16) SoftCtrl {
 static_assert(sizeof(SoftCtrl) <= 2048, "control block must fit its reservation");
 
 // Positions in stream order: the bonus positions (j = K), then j = K-1 down
-// to 0, each over b = 0..B-1.
+// to 2, each over b = 0..B-1; then positions 1 and 0 row by row.
 __device__ __forceinline__ void stream_pos(int i, int B, int K, int *b, int *j) {
-  *j = K - i / B;
-  *b = i - (K - *j) * B;
+  const int pa = K >= 2 ? B * (K - 1) : 0;
+  if (i < pa) {  // positions K .. 2, each over every row
+    *j = K - i / B;
+    *b = i - (K - *j) * B;
+  } else {       // the rest row by row, so rows complete one after another
+    const int npb = K >= 2 ? 2 : K + 1;
+    const int i2 = i - pa;
+    *b = i2 / npb;
+    *j = npb - 1 - (i2 - *b * npb);
+  }
 }
 
 // Order-preserving integer key of a logit's raw bits (larger logit, larger
@@ -222,6 +231,24 @@ __device__ __forceinline__ bool trunc_active(const ChainStochParams &P, int b, i
   if (!use_k) *k = 0;
   if (!use_p) *tp = 1.0f;
   return use_k || use_p;
+}
+
+// Stamped partial records (see SoftPart).
+__device__ __forceinline__ void store_part(SoftPart *d, float m, float s, uint32_t flags, uint32_t tag) {
+  st_relaxed_u64(&d->a, static_cast<unsigned long long>(__float_as_uint(m)) |
+                            (static_cast<unsigned long long>(tag) << 32));
+  st_relaxed_u64(&d->b, static_cast<unsigned long long>(__float_as_uint(s)) |
+                            (static_cast<unsigned long long>((flags & 0xffu) | (tag << 8)) << 32));
+}
+// false while either word still holds an older record
+__device__ __forceinline__ bool load_part(const SoftPart *d, uint32_t tag, float *m, float *s,
+                                          uint32_t *flags) {
+  const unsigned long long a = ld_relaxed_u64(&d->a), b = ld_relaxed_u64(&d->b);
+  *m = __uint_as_float(static_cast<uint32_t>(a));
+  *s = __uint_as_float(static_cast<uint32_t>(b));
+  const uint32_t hb = static_cast<uint32_t>(b >> 32);
+  *flags = hb & 0xffu;
+  return static_cast<uint32_t>(a >> 32) == tag && (hb >> 8) == (tag & 0xffffffu);
 }
 
 // Element offset of partial row `row` (targets b*(K+1)+j, then drafts
@@ -560,8 +587,8 @@ __global__ void __launch_bounds__(kSoftThreads + 32, 3) softmax_partials_kernel(
           c = __ldg(reinterpret_cast<const float *>(dg) + it.yl);
         }
       }
-      P.ylog[it.trow] = a;
-      P.ylog[it.drow] = c;
+      st_relaxed_u64(P.ylog + it.trow, __float_as_uint(a) | (static_cast<unsigned long long>(it.tag) << 32));
+      st_relaxed_u64(P.ylog + it.drow, __float_as_uint(c) | (static_cast<unsigned long long>(it.tag) << 32));
     }
     const float s2 = it.s2;
     if (it.first) {
@@ -606,14 +633,13 @@ __global__ void __launch_bounds__(kSoftThreads + 32, 3) softmax_partials_kernel(
         const uint32_t tf = ctl.tflags[slot];
         SoftPart *rp = P.part + (size_t)it.trow * nt;
         SoftPart *rq = pair ? P.part + (size_t)it.drow * nt : nullptr;
-        const float stamp = __uint_as_float(it.tag);
         for (int t = it.run0 + 1 + lane; t <= it.t; t += 32) {
-          rp[t] = SoftPart{-kInf, 0.f, stamp, 0u};
-          if (pair) rq[t] = SoftPart{-kInf, 0.f, stamp, 0u};
+          store_part(rp + t, -kInf, 0.f, 0u, it.tag);
+          if (pair) store_part(rq + t, -kInf, 0.f, 0u, it.tag);
         }
         if (lane == 0) {
-          rp[it.run0] = SoftPart{M1, S1, stamp, tf};
-          if (pair) rq[it.run0] = SoftPart{M2, S2, stamp, tf};
+          store_part(rp + it.run0, M1, S1, tf, it.tag);
+          if (pair) store_part(rq + it.run0, M2, S2, tf, it.tag);
           ctl.arrived[slot] = 0;
           ctl.tflags[slot] = 0;
         }
@@ -635,6 +661,10 @@ struct alignas(16) ResolveCtrl {
   uint32_t thp, thq;         // key thresholds of the stopping position's p and q
   int pad2[2];
 };
+
+// Non-zero ranks copy Mp .. thq (three 16-byte blocks) from rank 0.
+static_assert(offsetof(ResolveCtrl, Mp) % 16 == 0 && offsetof(ResolveCtrl, thq) < offsetof(ResolveCtrl, Mp) + 48,
+              "the decision fields must be three aligned 16-byte blocks");
 
 // Order-preserving key of a logit value held in fp32 (exact for bf16 logits).
 __device__ __forceinline__ uint32_t key_of(float l, bool bf16) {
@@ -658,8 +688,9 @@ __device__ __forceinline__ void cluster_wait() {
 // two >= the tile count, at most 32), one group per logit row; lane l of a
 // group folds tiles l, l+GS, ... in order, then the group folds in a fixed
 // butterfly order.  rstat[r] = (max, sum, draft-token logit, flags).
-__device__ void fold_rows(const ChainStochParams &P, int b, float s2, uint32_t tag, int warp,
+__device__ bool fold_rows(const ChainStochParams &P, int b, float s2, uint32_t tag, int warp,
                           int lane, float4 *rstat) {
+  bool ready = true;  // every record this lane read carries the tag
   constexpr int NW = kResolveThreads / 32;
   const int K = P.K, npos = K + 1, nt = P.nslices;
   int GS = 1;
@@ -674,14 +705,23 @@ __device__ void fold_rows(const ChainStochParams &P, int b, float s2, uint32_t t
       const bool draft = r > K;
       const int j = draft ? r - npos : r;
       const int prow = draft ? P.B * npos + b * K + j : b * npos + j;
-      if (sub == 0 && j < K) yv = P.ylog[prow];
+      if (sub == 0 && j < K) {
+        // the draft token's logit: written only when the token is in range
+        const int y = P.tokens ? __ldg(P.tokens + (size_t)b * K + j) : -1;
+        if (y >= 0 && y < P.V) {
+          const unsigned long long w = ld_relaxed_u64(P.ylog + prow);
+          yv = __uint_as_float(static_cast<uint32_t>(w));
+          ready &= static_cast<uint32_t>(w >> 32) == tag;
+        }
+      }
       for (int t = sub; t < nt; t += GS) {
-        const SoftPart q = P.part[(size_t)prow * nt + t];
-        f |= q.flags;
-        if (__float_as_uint(q.stamp) != tag) f |= F_TIMEOUT;  // not written by this call
-        const float mn = fmax_nan(m, q.m);
+        float qm, qs;
+        uint32_t qf;
+        ready &= load_part(P.part + (size_t)prow * nt + t, tag, &qm, &qs, &qf);
+        f |= qf;
+        const float mn = fmax_nan(m, qm);
         sacc = (m == -kInf ? 0.f : sacc * ex2(__fmul_rn(m - mn, s2))) +
-               (q.m == -kInf ? 0.f : q.s * ex2(__fmul_rn(q.m - mn, s2)));
+               (qm == -kInf ? 0.f : qs * ex2(__fmul_rn(qm - mn, s2)));
         m = mn;
       }
     }
@@ -695,6 +735,7 @@ __device__ void fold_rows(const ChainStochParams &P, int b, float s2, uint32_t t
     }
     if (sub == 0 && r < npos + K) rstat[r] = make_float4(M, v, yv, __uint_as_float(f));
   }
+  return ready;
 }
 
 // One row's decisions from the folded statistics: validates the row's inputs,
@@ -832,28 +873,50 @@ __global__ void __launch_bounds__(kResolveThreads, 4) chain_resolve_kernel(const
                          static_cast<uint32_t>(lenp) * ESZ);
     }
   }
-  const RowScalars first = load_scalars(P, b, lane);
-  // The row's generation: only this row's cluster changes it, at the end of
-  // this kernel; the split barrier below keeps that change after every CTA
-  // of the cluster has read it.
-  const uint32_t gen = *reinterpret_cast<volatile const uint32_t *>(P.gen - 1 - b);
-  cluster_arrive();
-  // the stream kernel's partials are visible after this line; nothing above
-  // reads them
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (blockIdx.x == 0 && tid == 0) {  // the stream kernel is done with the claim counter
-    *P.claim = 0u;
-    *P.magic = kWsMagic;
+  // The stream kernel releases the claim counter only when it completes:
+  // block 0 re-arms the workspace header after waiting for that, on its way
+  // out.
+  auto rearm_header = [&]() {
+    if (blockIdx.x == 0 && tid == 0) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      *P.claim = 0u;
+      *P.magic = kWsMagic;
+    }
+  };
+  // Rank 0 of the cluster polls the row's partial records until every one
+  // carries this call's tag -- the stream kernel stamps them as it goes, so
+  // a row is resolved as soon as its own tiles are done, not when the whole
+  // stream is -- folds them and takes the walk's decisions.  The other CTAs
+  // read those decisions after one cluster barrier.
+  if (crank == 0) {
+    const RowScalars first = load_scalars(P, b, lane);
+    const uint32_t gen = *reinterpret_cast<volatile const uint32_t *>(P.gen - 1 - b);
+    // a truncated verify also needs the threshold kernel's records (that
+    // grid completes after the stream kernel)
+    if (P.trunc) asm volatile("griddepcontrol.wait;" ::: "memory");
+    bool gave_up = false;
+    const uint64_t t0 = global_timer_ns();
+    while (!__syncthreads_and(fold_rows(P, b, s2, gen + 1u, warp, lane, rstat))) {
+      if (__syncthreads_or(global_timer_ns() - t0 > P.wait_limit_ns)) {  // bounded
+        gave_up = true;
+        break;
+      }
+      __nanosleep(200);
+    }
+    if (warp == 0)
+      decide_row(P, b, s2, tflags | (gave_up ? F_TIMEOUT : 0u), lane, true, rstat, first, ctl, BF16);
+    __syncthreads();
+    if (tid == 0) P.gen[-1 - b] = gen + 1u;  // only this CTA read it
   }
-  fold_rows(P, b, s2, gen + 1u, warp, lane, rstat);
-  __syncthreads();
-  if (warp == 0) decide_row(P, b, s2, tflags, lane, crank == 0, rstat, first, ctl, BF16);
+  cluster_sync();  // rank 0's decisions are in its shared memory
+  if (crank != 0 && tid < 3) {  // Mp..Sq, u..trunc, thp..: three 16-byte blocks
+    char *mine = reinterpret_cast<char *>(&ctl.Mp) + 16 * tid;
+    *reinterpret_cast<float4 *>(mine) = ld_dsmem_f4(dsmem_addr(mine, 0));
+  }
   __syncthreads();
   const uint32_t flags = ctl.flags;
   const int stop = ctl.stop;
-  cluster_wait();  // every CTA of the cluster has read the generation
-  if (crank == 0 && tid == 0) P.gen[-1 - b] = gen + 1u;
-  if (flags) {  // identical in every CTA of the cluster: all leave together
+  if (flags) {  // rank 0's decision: every CTA of the cluster leaves here
     if (crank == 0 && warp == 0) {
       for (int j = lane; j < npos; j += 32) P.out_tokens[(size_t)b * npos + j] = -1;
       if (lane == 0) {
@@ -862,6 +925,7 @@ __global__ void __launch_bounds__(kResolveThreads, 4) chain_resolve_kernel(const
         P.row_status[b] = lowest_code(flags);
       }
     }
+    rearm_header();
     return;
   }
 
@@ -1087,6 +1151,7 @@ __global__ void __launch_bounds__(kResolveThreads, 4) chain_resolve_kernel(const
     }
   }
   cluster_wait();  // no CTA leaves while a peer may still read its mailbox
+  rearm_header();
 }
 
 // ============================================================ block selection
@@ -1202,10 +1267,11 @@ __global__ void __launch_bounds__(kDriftThreads) drift_select_kernel(const __gri
   const uint32_t gen = *reinterpret_cast<volatile const uint32_t *>(P.gen - 1 - b);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // every position's statistics (the row's status covers all of them)
-  if (warp < kResolveThreads / 32) fold_rows(P, b, s2, gen + 1u, warp, lane, rstat);
-  __syncthreads();
+  bool ready = true;
+  if (warp < kResolveThreads / 32) ready = fold_rows(P, b, s2, gen + 1u, warp, lane, rstat);
+  ready = __syncthreads_and(ready);  // the stream kernel is done: stale means lost
   if (tid == 0) {
-    uint32_t f = tflags;
+    uint32_t f = tflags | (ready ? 0u : F_TIMEOUT);
     for (int r = 0; r < npos + K; ++r) {
       if (r == K) continue;  // the bonus position is not a drafted one
       const float4 v = rstat[r];
@@ -1578,12 +1644,13 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
     float m = -kInf, sacc = 0.f;
     uint32_t f = 0;
     for (int t = lane; t < nt; t += 32) {
-      const SoftPart q = P.part[(size_t)row * nt + t];
-      f |= q.flags;
-      if (__float_as_uint(q.stamp) != gen + 1u) f |= F_TIMEOUT;
-      const float mn = fmax_nan(m, q.m);
+      float qm, qs;
+      uint32_t qf;
+      if (!load_part(P.part + (size_t)row * nt + t, gen + 1u, &qm, &qs, &qf)) f |= F_TIMEOUT;
+      f |= qf;
+      const float mn = fmax_nan(m, qm);
       sacc = (m == -kInf ? 0.f : sacc * ex2(__fmul_rn(m - mn, s2))) +
-             (q.m == -kInf ? 0.f : q.s * ex2(__fmul_rn(q.m - mn, s2)));
+             (qm == -kInf ? 0.f : qs * ex2(__fmul_rn(qm - mn, s2)));
       m = mn;
     }
     float Mw, Sw;

@@ -10,13 +10,12 @@ namespace sv {
 // One 16-byte partial per (logit row, tile) written by the softmax-partial
 // kernel: a run of consecutive tiles of one row streamed by one CTA leaves its
 // max logit m and sum of exp2((x - m) s2) at the run's first tile and empty
-// partials (m = -inf, s = 0) at its other tiles.  `stamp` holds the bits of
-// the row's generation + 1 at the time of writing.
+// partials (m = -inf, s = 0) at its other tiles.  Two 64-bit words, each
+// written by one relaxed store and each carrying the row's generation + 1
+// (the tag): a = m | tag << 32, b = s | (flags & 0xff | tag << 8) << 32.  A
+// reader that finds the tag in both words holds a record of this call.
 struct alignas(16) SoftPart {
-  float m;
-  float s;
-  float stamp;
-  uint32_t flags;
+  unsigned long long a, b;
 };
 
 // Truncation of one logit row (top-k / top-p): the kept tokens are those
@@ -53,7 +52,8 @@ struct ChainStochParams {
   float *q_at_draft;
   float *resid_mass;
   SoftPart *part;  // [(B*(K+1) + B*K) * nslices] workspace
-  float *ylog;     // [B*(K+1) + B*K] workspace: the draft token's logit per logit row
+  unsigned long long *ylog;  // [B*(K+1) + B*K] workspace: the draft token's logit per logit
+                            // row, as (logit bits | tag << 32)
   int B, K, V;
   int slice;       // elements per tile of the partial kernel
   int nslices;     // tiles per logit row
