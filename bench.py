@@ -33,9 +33,12 @@ METRIC = "verify steps/s and achieved HBM GB/s (B=64,K=5,V=128256 bf16) vs 8 TB/
 UNIT = "verify steps/s"
 L2_BYTES = 129 * 1024 * 1024
 # ncu dram__bytes_read.sum + dram__bytes_write.sum of one softmax_partials_kernel
-# launch on this workload (profiles/softmax_partials_chain_c3.md): 180,649,472
-# read + 3,506,944 written; reset to None whenever that kernel changes
-TRAFFIC = 180649472 + 3506944
+# launch on this workload (profiles/softmax_partials_chain_c3.md): 180,649,728
+# read + 3,448,576 written; reset to None whenever that kernel changes
+TRAFFIC = 180649728 + 3448576
+# the same for one greedy_kernel launch on the tree workload
+# (profiles/greedy_tree_c4.md): 583,470,336 read + 3,753,984 written
+TREE_TRAFFIC = 583470336 + 3753984
 # kernels one stochastic spec_verify_chain call enqueues: the stream kernel
 # and the resolve kernel
 KERNELS_PER_STEP = 2
@@ -51,7 +54,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="chain",
-                    choices=["chain", "kv_compact", "policy", "drift", "truncated"],
+                    choices=["chain", "kv_compact", "policy", "drift", "truncated", "tree"],
                     help="chain: the headline verify step (default); kv_compact / policy: "
                          "the post-verification entry points")
     ap.add_argument("--sets", type=int, default=0,
@@ -487,6 +490,39 @@ def run_next(args):
                              "kernel": "softmax_partials + trunc + chain_resolve",
                              "algorithmic_bytes_per_launch": step_bytes, "traffic": None},
                 "gpu_launches": 3 * n, "clocks": clocks}
+    elif args.workload == "tree":
+        # greedy tree verification with the margin rule on the tree workload
+        inp = S.make("c4")
+        B, N = inp["parent"].shape
+        step_bytes = inp["target"].nbytes
+        n_sets = max(2, -(-3 * L2_BYTES // step_bytes) + 1)
+        tgt0 = to_cuda(inp["target"], dev)
+        sets = [tgt0] + [tgt0.clone() for _ in range(n_sets - 1)]
+        par, toks = to_cuda(inp["parent"], dev), to_cuda(inp["node_tokens"], dev)
+        outs = [dict(accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
+                     path_nodes=torch.empty(B, N, dtype=torch.int32, device=dev),
+                     out_tokens=torch.empty(B, N, dtype=torch.int32, device=dev),
+                     num_emitted=torch.empty(B, dtype=torch.int32, device=dev),
+                     row_status=torch.empty(B, dtype=torch.int32, device=dev))
+                for _ in range(n_sets)]
+
+        def step(i):
+            sv.spec_verify_tree(sets[i], par, toks, margin_kappa=0.3, out=outs[i], stream=stream)
+        sampler.start()
+        time.sleep(0.3)
+        ms, n, w = _time_graph(torch, stream, step, n_sets, steps, warmup)
+        clocks = sampler.stop()
+        gbs = step_bytes / (ms / 1e3) / 1e9
+        line = {"metric": "tree verify steps/s (greedy + margin rule)", "workload": "tree",
+                "value": 1e3 / ms, "unit": "verify steps/s", "n_gpus": 1, "steps": n, "warmup": w,
+                "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": f"tree B={B} N={N} V={inp['target'].shape[-1]} bf16, kappa=0.3",
+                           "l2": f"{n_sets} rotating input sets > L2"},
+                "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                             "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
+                             "kernel": "greedy_kernel + greedy_walk_kernel",
+                             "algorithmic_bytes_per_launch": step_bytes, "traffic": TREE_TRAFFIC},
+                "gpu_launches": 2 * n, "clocks": clocks}
     elif args.workload == "drift":
         # top-32 DRIFT residuals on the headline chain workload
         inp = S.make(WORKLOAD)

@@ -413,9 +413,11 @@ spec_status spec_workspace_init(void *ws, size_t ws_bytes, void *stream);
 const char *spec_status_string(spec_status s);
 
 /*
- * Bounded on-device waits.  Every wait of the kernels on an asynchronous
- * copy gives up after this many nanoseconds (default 1e9 = 1 s), marks the
- * rows it served SPEC_ROW_TIMEOUT and lets the kernel finish.  Process-wide
+ * Bounded on-device waits.  Every wait of the stochastic kernels on an
+ * asynchronous copy or on another block's record gives up after this many
+ * nanoseconds (default 1e9 = 1 s), marks the rows it served SPEC_ROW_TIMEOUT
+ * and lets the kernel finish.  The greedy and tree kernels stream with plain
+ * loads and never wait.  Process-wide
  * setting, read at each launch.  spec_debug_force_wait_timeout(1) makes every
  * kernel additionally wait on a barrier that nothing completes, so the give-up
  * path can be tested on a healthy GPU; 0 turns it off.

@@ -32,9 +32,9 @@ struct DevInfo {
 std::mutex g_mu;
 std::map<int, DevInfo> g_dev;
 std::map<std::tuple<int, int, size_t>, int> g_blocks;
+std::map<std::tuple<int, int, int>, int> g_greedy_blocks;
 void *g_static_ws_ptr[kMaxDevices] = {};  // device address of g_static_ws, per device
 
-constexpr size_t kGreedyCtrlBytes = 1024;
 constexpr size_t kSoftCtrlBytes = 2048;
 constexpr int kMinGreedySlice = 2048;
 
@@ -97,20 +97,20 @@ cudaError_t soft_blocks(int dev, bool bf16, int nv, size_t smem, int *out) {
   return cudaSuccess;
 }
 
-cudaError_t greedy_blocks(int dev, bool bf16, size_t smem, int *out) {
-  auto key = std::make_tuple(dev, (int)bf16, smem);
+cudaError_t greedy_blocks(int dev, bool bf16, bool vec, int *out) {
+  auto key = std::make_tuple(dev, (int)bf16, (int)vec);
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    auto it = g_blocks.find(key);
-    if (it != g_blocks.end()) {
+    auto it = g_greedy_blocks.find(key);
+    if (it != g_greedy_blocks.end()) {
       *out = it->second;
       return cudaSuccess;
     }
   }
-  cudaError_t e = greedy_max_blocks_per_sm(bf16, smem, out);
+  cudaError_t e = greedy_max_blocks_per_sm(bf16, vec, out);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lk(g_mu);
-  g_blocks[key] = *out;
+  g_greedy_blocks[key] = *out;
   return cudaSuccess;
 }
 
@@ -121,37 +121,43 @@ size_t greedy_partials_max(int32_t B, int32_t npos, int32_t V) {
 bool valid_sizes(int32_t B, int32_t V) { return B >= 0 && V >= 1 && V <= SPEC_MAX_V; }
 
 // Greedy launch shared by the chain (GREEDY mode) and tree entry points.
+// The slice (elements per work item) is picked from 2048..16384 to minimise
+// the busiest warp's load: rounds of items per warp times (slice bytes + a
+// fixed per-item cost of about 2 KB of streaming).
 spec_status run_greedy(GreedyParams &p, bool bf16, int esz, void *ws, cudaStream_t stream) {
   int dev;
   DevInfo di;
   if (device_info(&dev, &di) != cudaSuccess) return SPEC_ERR_CUDA;
-  const int epv = 16 / esz;
+  p.vec = aligned(p.target, 16) && (static_cast<long long>(p.V) * esz) % 16 == 0;
+  int per_sm = 0;
+  if (greedy_blocks(dev, bf16, p.vec != 0, &per_sm) != cudaSuccess || per_sm < 1) return SPEC_ERR_CUDA;
+  const long long warps = static_cast<long long>(di.sms) * per_sm * (kGreedyThreads / 32);
   const long long positions = static_cast<long long>(p.B) * p.npos;
-  // slices small enough to give every SM work, large enough to amortise
-  const int want = static_cast<int>(std::max<long long>(1, (2LL * di.sms + positions - 1) / positions));
-  int slice = static_cast<int>(align_up(static_cast<size_t>(ceil_div(p.V, want)), 64));
-  slice = std::max(slice, kMinGreedySlice);
-  slice = std::min(slice, kGreedySlice);
-  slice = static_cast<int>(align_up(static_cast<size_t>(slice), static_cast<size_t>(epv)));
+  int slice = kGreedySlice;
+  double best_cost = 0.0;
+  for (int sl = kGreedySlice; sl >= kMinGreedySlice; sl /= 2) {
+    const long long items = positions * ceil_div(p.V, sl);
+    const double cost = static_cast<double>((items + warps - 1) / warps) *
+                        (static_cast<double>(std::min(sl, p.V)) * esz + 2048.0);
+    if (sl == kGreedySlice || cost < best_cost) {
+      best_cost = cost;
+      slice = sl;
+    }
+  }
+  // SPECVERIFY_GREEDY_SLICE (2048..16384 elements) overrides it for tuning
+  if (const char *ov = std::getenv("SPECVERIFY_GREEDY_SLICE")) {
+    const int sl = std::atoi(ov);
+    if (sl >= kMinGreedySlice && sl <= kGreedySlice) slice = static_cast<int>(align_up(static_cast<size_t>(sl), 8));
+  }
   p.slice = slice;
   p.nslices = ceil_div(p.V, slice);
-  p.use_tma = aligned(p.target, 16) && (static_cast<long long>(p.V) * esz) % 16 == 0;
-  p.buf_bytes = static_cast<int>(align_up(static_cast<size_t>(slice) * esz, 128));
-  const size_t fixed = kGreedyCtrlBytes;
-  int stages = static_cast<int>((static_cast<size_t>(di.smem_optin) - fixed) / p.buf_bytes);
-  stages = std::max(1, std::min(stages, 4));
-  p.stages = stages;
-  const size_t smem = static_cast<size_t>(stages) * p.buf_bytes + fixed;
-  p.wait_limit_ns = g_wait_ns.load();
-  p.force_timeout = g_force_timeout.load();
   p.part = static_cast<GreedyPart *>(ws);
-  int per_sm = 0;
-  if (greedy_blocks(dev, bf16, smem, &per_sm) != cudaSuccess || per_sm < 1) return SPEC_ERR_CUDA;
   const long long items = positions * p.nslices;
-  const int grid = static_cast<int>(std::min<long long>(items, static_cast<long long>(di.sms) * per_sm));
-  report("greedy slice nslices stages smem per_sm grid tma", slice, p.nslices, stages,
-         (long long)smem, per_sm, grid, p.use_tma);
-  if (launch_greedy(p, bf16, grid, smem, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (items > 0x7fffffffLL) return SPEC_ERR_SHAPE;
+  const long long need = (items + kGreedyThreads / 32 - 1) / (kGreedyThreads / 32);
+  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(need, static_cast<long long>(di.sms) * per_sm)));
+  report("greedy slice nslices per_sm grid vec", slice, p.nslices, per_sm, grid, p.vec, 0, 0);
+  if (launch_greedy(p, bf16, grid, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
 }
 

@@ -238,6 +238,16 @@ __device__ __forceinline__ uint4 ld_shared_u4(const void *p) {
   return v;
 }
 
+// Streaming 16-byte global load of read-once data: not kept in L1, and
+// marked in L2 with `policy` (l2_policy_evict_first for data read once).
+__device__ __forceinline__ uint4 ld_stream_u4(const void *p, uint64_t policy) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
+}
+
 // ------------------------------------------------------- warp primitives
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

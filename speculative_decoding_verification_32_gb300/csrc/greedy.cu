@@ -7,12 +7,15 @@
 // branch kept.  "Margins, Not Windows" section 3: a mismatched draft is
 // promoted when p_target(draft) / p_target(top1) exceeds kappa.
 //
-// Only the target logits are read.  A persistent grid streams (position,
-// vocabulary slice) work items through a bulk-copy (TMA) ring in shared
-// memory; each item leaves its slice's largest logit and lowest index of it
-// as a 16-byte partial.  The CTA that completes the last item of a row
-// combines the row's partials (slices in vocabulary order, so ties keep the
-// lowest index) and walks the chain or the tree in one warp.
+// Only the target logits are read.  A persistent grid of warps streams
+// (position, vocabulary slice) work items straight from HBM: each warp owns
+// an item, keeps eight 16-byte loads per lane in flight, folds each vector to
+// its largest element (packed bf16x2 max) and leaves the slice's largest
+// logit and lowest index of it as a 16-byte partial -- no shared memory and
+// no block barrier on the streaming path.  A second kernel, launched as a
+// programmatic dependent, combines each row's partials (slices in vocabulary
+// order, so ties keep the lowest index) with all its warps and walks the
+// chain or the tree in one warp.
 #include <cuda_bf16.h>
 
 #include <atomic>
@@ -23,20 +26,11 @@
 namespace sv {
 namespace {
 
-constexpr int NT = kThreads;
-constexpr int NW = NT / 32;
-constexpr int kMaxStages = 8;
+constexpr int kGWarps = kGreedyThreads / 32;
+constexpr int kGU = 8;  // 16-byte vectors in flight per lane
+constexpr int kWalkThreads = 256;
+constexpr int kWalkWarps = kWalkThreads / 32;
 constexpr float kInf = __builtin_huge_valf();
-
-struct alignas(16) GCtrl {
-  uint64_t full[kMaxStages];
-  uint64_t never;
-  uint64_t pad0;
-  float part_v[NW];
-  int part_i[NW];
-  uint32_t part_f[NW];
-};
-static_assert(sizeof(GCtrl) <= 1024, "control block must fit its reservation");
 
 template <bool BF16>
 struct GFmt {
@@ -51,65 +45,84 @@ struct GFmt {
       return __uint_as_float(static_cast<uint32_t>(__ldg(static_cast<const unsigned short *>(base) + idx)) << 16);
     else return __ldg(static_cast<const float *>(base) + idx);
   }
-  // elements [v*EPV, v*EPV+EPV) of the slice; entries past len are -inf
-  static __device__ __forceinline__ void load_vec(uint32_t *w, bool tma, const unsigned char *sbuf,
-                                                  const char *gsrc, int v, int len) {
-    if (tma) {
-      uint4 r = ld_shared_u4(sbuf + (size_t)v * 16);
+  // largest element of a vector; NaN if it holds one
+  static __device__ __forceinline__ float vec_max(const uint32_t *w) {
+    if constexpr (BF16) {
+      const uint32_t m = bf16x2_max_nan(bf16x2_max_nan(w[0], w[1]), bf16x2_max_nan(w[2], w[3]));
+      return fmax_nan(bf16_lo(m), bf16_hi(m));
+    } else {
+      return fmax_nan(fmax_nan(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                      fmax_nan(__uint_as_float(w[2]), __uint_as_float(w[3])));
+    }
+  }
+  // elements [v*EPV, v*EPV+EPV) of a slice starting at `src`; entries past
+  // len are -inf.  VEC: one 16-byte load (the slice is whole vectors and
+  // 16-byte aligned); otherwise element loads.
+  template <bool VEC>
+  static __device__ __forceinline__ void load_vec(uint32_t *w, const char *src, int v, int len,
+                                                  uint64_t pol) {
+    if constexpr (VEC) {
+      const uint4 r = ld_stream_u4(src + (size_t)v * 16, pol);
       w[0] = r.x; w[1] = r.y; w[2] = r.z; w[3] = r.w;
     } else {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         if constexpr (BF16) {
           const int e0 = v * 8 + 2 * i;
-          const unsigned short *g = reinterpret_cast<const unsigned short *>(gsrc);
-          uint32_t lo = e0 < len ? __ldg(g + e0) : 0xFF80u;
-          uint32_t hi = e0 + 1 < len ? __ldg(g + e0 + 1) : 0xFF80u;
+          const unsigned short *g = reinterpret_cast<const unsigned short *>(src);
+          const uint32_t lo = e0 < len ? __ldg(g + e0) : 0xFF80u;
+          const uint32_t hi = e0 + 1 < len ? __ldg(g + e0 + 1) : 0xFF80u;
           w[i] = lo | (hi << 16);
         } else {
           const int e = v * 4 + i;
-          w[i] = e < len ? __ldg(reinterpret_cast<const unsigned int *>(gsrc) + e) : 0xFF800000u;
+          w[i] = e < len ? __ldg(reinterpret_cast<const unsigned int *>(src) + e) : 0xFF800000u;
         }
       }
     }
   }
 };
 
-// (value, index) pair order: larger value first, then lower index.
-__device__ __forceinline__ bool pair_better(float v, int i, float bv, int bi) {
-  return v > bv || (v == bv && (unsigned)i < (unsigned)bi);
-}
-
-// Combined (max, lowest argmax, flags) of one position from its slice partials.
-__device__ __forceinline__ void combine_partials(const GreedyPart *pp, int nslices, float *mx,
-                                                 int *top, uint32_t *flags) {
+// Combined (max, lowest argmax, flags) of one position from its slice
+// partials, by one warp: each lane folds slices lane, lane+32, ... (in
+// vocabulary order, so a later slice replaces only on a strictly larger
+// value), then the warp takes the largest value and, among the lanes holding
+// it, the lowest index.  A NaN partial is skipped; its flag marks the row.
+__device__ __forceinline__ void combine_position(const GreedyPart *pp, int nslices, int lane,
+                                                 float *mx, int *top, uint32_t *flags) {
   float best = -kInf;
-  int bi = -1;
-  uint32_t f = 0;
-  for (int s = 0; s < nslices; ++s) {
+  uint32_t bi = 0xFFFFFFFFu, f = 0;
+  for (int s = lane; s < nslices; s += 32) {
     const int4 r = *reinterpret_cast<const int4 *>(pp + s);
     const float v = __int_as_float(r.x);
     f |= static_cast<uint32_t>(r.z);
-    if (v > best) {  // slices in vocabulary order: ties keep the earlier slice
+    if (v > best) {
       best = v;
-      bi = r.y;
+      bi = static_cast<uint32_t>(r.y);
     }
   }
-  if (best == kInf) f |= F_NONFINITE;
-  else if (best == -kInf) f |= F_EMPTY;
-  *mx = best;
-  *top = bi;
+  float M = best;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL_MASK, M, o));
+  bi = __reduce_min_sync(FULL_MASK, best == M ? bi : 0xFFFFFFFFu);
+  f = __reduce_or_sync(FULL_MASK, f);
+  if (M == kInf) f |= F_NONFINITE;
+  else if (M == -kInf) f |= F_EMPTY;
+  *mx = M;
+  *top = bi == 0xFFFFFFFFu ? -1 : static_cast<int>(bi);
   *flags = f;
 }
-
 
 // Margin rule in fp64: l(draft) - l(top1) > T * ln(kappa).
 __device__ __forceinline__ bool margin_promotes(float l_d, float l_top, float T, double ln_kappa) {
   return __dsub_rn((double)l_d, (double)l_top) > __dmul_rn((double)T, ln_kappa);
 }
 
+// Chain walk: draft j is kept iff it is position j's argmax (or promoted by
+// the margin rule); the first miss emits that position's argmax, a full pass
+// the bonus argmax.  mx_s / top_s / fl_s hold the combined positions.
 template <bool BF16>
-__device__ void walk_greedy_chain(const GreedyParams &P, int b, int lane) {
+__device__ void walk_greedy_chain(const GreedyParams &P, int b, int lane, const float *mx_s,
+                                  const int *top_s, const uint32_t *fl_s) {
   using F = GFmt<BF16>;
   const int npos = P.npos, K = npos - 1, V = P.V;
   uint32_t flags = 0;
@@ -123,9 +136,9 @@ __device__ void walk_greedy_chain(const GreedyParams &P, int b, int lane) {
     const int j = j0 + lane;
     int ok = 1, top = -1;
     if (j < npos) {
-      float mx;
-      uint32_t f;
-      combine_partials(P.part + ((size_t)b * npos + j) * P.nslices, P.nslices, &mx, &top, &f);
+      const float mx = mx_s[j];
+      const uint32_t f = fl_s[j];
+      top = top_s[j];
       flags |= f;
       if (j < K) {
         const int y = __ldg(P.tokens + (size_t)b * K + j);
@@ -163,14 +176,14 @@ __device__ void walk_greedy_chain(const GreedyParams &P, int b, int lane) {
 
 // Tree walk: node i >= 1 is accepted iff its parent is accepted and its token
 // is the parent's argmax (or promoted by the margin rule); keep the deepest
-// accepted node, lowest index on ties.  `scr` is shared scratch for N nodes.
+// accepted node, lowest index on ties.  mx_s / top_s / fl_s hold the combined
+// nodes; `scr` is shared scratch of 12 bytes per node.
 template <bool BF16>
-__device__ void walk_tree(const GreedyParams &P, int b, int lane, unsigned char *scr, int *shared_best) {
+__device__ void walk_tree(const GreedyParams &P, int b, int lane, const float *mx_s, const int *top_s,
+                          const uint32_t *fl_s, unsigned char *scr, int *shared_best) {
   using F = GFmt<BF16>;
   const int N = P.npos, V = P.V;
-  int *top_s = reinterpret_cast<int *>(scr);
-  float *mx_s = reinterpret_cast<float *>(top_s + N);
-  int *par_s = reinterpret_cast<int *>(mx_s + N);
+  int *par_s = reinterpret_cast<int *>(scr);
   int *path_s = par_s + N;
   short *dep_s = reinterpret_cast<short *>(path_s + N);
   unsigned char *ok_s = reinterpret_cast<unsigned char *>(dep_s + N);
@@ -185,13 +198,7 @@ __device__ void walk_tree(const GreedyParams &P, int b, int lane, unsigned char 
     if (!(T > 0.f && T < kInf)) flags |= F_BAD_TEMPERATURE;
   }
   for (int i = lane; i < N; i += 32) {
-    float mx;
-    int top;
-    uint32_t f;
-    combine_partials(P.part + ((size_t)b * N + i) * P.nslices, P.nslices, &mx, &top, &f);
-    flags |= f;
-    top_s[i] = top;
-    mx_s[i] = mx;
+    flags |= fl_s[i];
     const int pa = __ldg(par_g + i);
     if (i == 0 ? pa != -1 : (pa < 0 || pa >= i)) flags |= F_BAD_PARENT;
     par_s[i] = (i == 0 || pa < 0 || pa >= i) ? 0 : pa;
@@ -255,178 +262,134 @@ __device__ void walk_tree(const GreedyParams &P, int b, int lane, unsigned char 
   __syncwarp();
 }
 
-template <bool BF16>
-__global__ void __launch_bounds__(NT, 1) greedy_kernel(const __grid_constant__ GreedyParams P) {
+// Streaming pass: warp gw takes items gw, gw + GW, ... (item = position-major
+// (position, slice)); per lane, U vectors are loaded before any is used.  A
+// lane keeps the largest vector maximum it has seen (strictly larger
+// replaces, so the earliest of its vectors wins a tie) with that vector's
+// words; the warp then takes the largest value, the lowest vector index
+// holding it, and that vector's first element equal to it.
+template <bool BF16, bool VEC>
+__global__ void __launch_bounds__(kGreedyThreads) greedy_kernel(const __grid_constant__ GreedyParams P) {
   using F = GFmt<BF16>;
   constexpr int EPV = F::EPV;
   constexpr int ESZ = F::ESZ;
-  extern __shared__ __align__(128) unsigned char smem[];
-  const int S = P.stages;
-  GCtrl &ctl = *reinterpret_cast<GCtrl *>(smem + (size_t)S * P.buf_bytes);
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int npos = P.npos, V = P.V, nsl = P.nslices;
-  const int B = P.B;
-  const int W = B * npos * nsl;
-  const int G = (int)gridDim.x, g = (int)blockIdx.x;
-  const int my_items = g < W ? (W - 1 - g) / G + 1 : 0;
-  const bool tma = P.use_tma != 0;
-
   // let the walk kernel be scheduled now; it waits for this grid anyway
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(&ctl.full[s], 1);
-    mbar_init(&ctl.never, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  auto geom = [&](int n, int &pos, int &s0, int &len) {
-    const int it = g + n * G;
-    pos = it / nsl;
-    s0 = (it - pos * nsl) * P.slice;
-    len = min(V - s0, P.slice);
-  };
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * kGWarps + (threadIdx.x >> 5);
+  const int GW = gridDim.x * kGWarps;
+  const int V = P.V, nsl = P.nslices;
+  const int W = P.B * P.npos * nsl;
   const uint64_t pol = l2_policy_evict_first();
-  auto issue = [&](int n) {
-    int pos, s0, len;
-    geom(n, pos, s0, len);
-    const int s = n % S;
-    const uint32_t bytes = static_cast<uint32_t>(len) * ESZ;
-    mbar_arrive_expect_tx(&ctl.full[s], bytes);
-    bulk_g2s(smem + (size_t)s * P.buf_bytes,
-             static_cast<const char *>(P.target) + ((size_t)pos * V + s0) * ESZ, bytes, &ctl.full[s],
-             pol);
-  };
-  int issued = 0, n_break = -1;
-  if (tma && tid == 0)
-    for (; issued < min(S, my_items); ++issued) issue(issued);
-
-  for (int n = 0; n < my_items; ++n) {
-    int pos, s0, len;
-    geom(n, pos, s0, len);
-    const int s = n % S;
-    const uint32_t parity = static_cast<uint32_t>(n / S) & 1u;
-    bool timed_out = false;
-    if (tma && n_break < 0)
-      timed_out = P.force_timeout ? !mbar_wait_bounded(&ctl.never, 0u, P.wait_limit_ns)
-                                  : !mbar_wait_bounded(&ctl.full[s], parity, P.wait_limit_ns);
-    const unsigned char *sb = smem + (size_t)s * P.buf_bytes;
-    const char *gsrc = static_cast<const char *>(P.target) + ((size_t)pos * V + s0) * ESZ;
+  for (int it = gw; it < W; it += GW) {
+    const int pos = it / nsl;
+    const int s0 = (it - pos * nsl) * P.slice;
+    const int len = min(V - s0, P.slice);
     const int nvec = (len + EPV - 1) / EPV;
+    const char *src = static_cast<const char *>(P.target) + ((size_t)pos * V + s0) * ESZ;
     float best = -kInf, nan_acc = -kInf;
-    int bidx = -1;
-    for (int v = tid; v < nvec; v += NT) {
-      uint32_t w[4];
-      F::load_vec(w, tma, sb, gsrc, v, len);
-      const int valid = len - v * EPV;
+    int bv = -1;
+    uint32_t wb[4] = {0u, 0u, 0u, 0u};
+    for (int v0 = 0; v0 < nvec; v0 += 32 * kGU) {
+      uint32_t w[kGU][4];
+      if (v0 + 32 * kGU <= nvec) {  // every lane's vectors are in range
 #pragma unroll
-      for (int e = 0; e < EPV; ++e) {
-        const float x = (e < valid) ? F::elem(w, e) : -kInf;
-        nan_acc = fmax_nan(nan_acc, x);
-        if (x > best) {
-          best = x;
-          bidx = v * EPV + e;
+        for (int u = 0; u < kGU; ++u) F::template load_vec<VEC>(w[u], src, v0 + u * 32 + lane, len, pol);
+      } else {
+#pragma unroll
+        for (int u = 0; u < kGU; ++u) {
+          const int v = v0 + u * 32 + lane;
+          if (v < nvec) {
+            F::template load_vec<VEC>(w[u], src, v, len, pol);
+          } else {
+            w[u][0] = w[u][1] = w[u][2] = w[u][3] = BF16 ? 0xFF80FF80u : 0xFF800000u;
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kGU; ++u) {
+        const float vm = F::vec_max(w[u]);
+        nan_acc = fmax_nan(nan_acc, vm);
+        if (vm > best) {
+          best = vm;
+          bv = v0 + u * 32 + lane;
+          wb[0] = w[u][0]; wb[1] = w[u][1]; wb[2] = w[u][2]; wb[3] = w[u][3];
         }
       }
     }
-    if (__syncthreads_or(timed_out) && n_break < 0) n_break = n;
-    if (tma && tid == 0 && n_break < 0 && issued < my_items) issue(issued++);
-
-    uint32_t f = (nan_acc != nan_acc) ? F_NONFINITE : 0u;
-    if (n_break >= 0) f |= F_TIMEOUT;
-    // block reduction of (best, lowest index), flags
+    float M = best;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(FULL_MASK, best, o);
-      const int oi = __shfl_xor_sync(FULL_MASK, bidx, o);
-      if (pair_better(ov, oi, best, bidx)) {
-        best = ov;
-        bidx = oi;
-      }
-    }
-    f = __reduce_or_sync(FULL_MASK, f);
-    if (lane == 0) {
-      ctl.part_v[warp] = best;
-      ctl.part_i[warp] = bidx;
-      ctl.part_f[warp] = f;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      best = lane < NW ? ctl.part_v[lane] : -kInf;
-      bidx = lane < NW ? ctl.part_i[lane] : -1;
-      f = lane < NW ? ctl.part_f[lane] : 0u;
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL_MASK, M, o));
+    const uint32_t vmin =
+        __reduce_min_sync(FULL_MASK, best == M ? static_cast<uint32_t>(bv) : 0xFFFFFFFFu);
+    const bool nonfinite = __any_sync(FULL_MASK, nan_acc != nan_acc);
+    // the lane holding the winning vector finds its first element equal to M
+    const bool owner = vmin != 0xFFFFFFFFu && static_cast<uint32_t>(bv) == vmin && best == M;
+    const unsigned who = __ballot_sync(FULL_MASK, owner);
+    if (who == 0u) {  // every element is -inf
+      if (lane == 0)
+        P.part[it] = GreedyPart{nonfinite ? __int_as_float(0x7fc00000) : -kInf, -1,
+                                nonfinite ? F_NONFINITE : 0u, 0};
+    } else if (lane == __ffs(who) - 1) {
+      int e = EPV - 1;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(FULL_MASK, best, o);
-        const int oi = __shfl_xor_sync(FULL_MASK, bidx, o);
-        if (pair_better(ov, oi, best, bidx)) {
-          best = ov;
-          bidx = oi;
-        }
-      }
-      f = __reduce_or_sync(FULL_MASK, f);
-      if (lane == 0) {
-        const int slice = (g + n * G) - pos * nsl;
-        P.part[(size_t)pos * nsl + slice] =
-            GreedyPart{best, bidx >= 0 ? s0 + bidx : -1, f, 0};
-      }
+      for (int k = EPV - 1; k >= 0; --k)
+        if (F::elem(wb, k) == M) e = k;
+      P.part[it] = GreedyPart{nonfinite ? __int_as_float(0x7fc00000) : M,
+                              s0 + static_cast<int>(vmin) * EPV + e, nonfinite ? F_NONFINITE : 0u, 0};
     }
   }
-  if (tma && n_break >= 0 && tid == 0)
-    for (int m = n_break; m < issued; ++m)
-      mbar_wait_bounded(&ctl.full[m % S], static_cast<uint32_t>(m / S) & 1u, P.wait_limit_ns);
 }
 
-// One warp per row: combine the row's partials and walk the chain or the
-// tree.  Waits for the partial kernel (programmatic dependent launch).
+// One CTA per row: its warps combine the row's positions into shared memory,
+// then warp 0 walks the chain or the tree.  Waits for the streaming kernel
+// (programmatic dependent launch).
 template <bool BF16>
-__global__ void greedy_walk_kernel(const __grid_constant__ GreedyParams P) {
+__global__ void __launch_bounds__(kWalkThreads) greedy_walk_kernel(const __grid_constant__ GreedyParams P) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   extern __shared__ __align__(16) unsigned char wsm[];
-  const int lane = threadIdx.x & 31;
-  const int b = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-  if (b >= P.B) return;
-  if (P.tree) {
-    int *best = reinterpret_cast<int *>(wsm);
-    walk_tree<BF16>(P, b, lane, wsm + 16, best);
-  } else {
-    walk_greedy_chain<BF16>(P, b, lane);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int b = blockIdx.x;
+  const int npos = P.npos;
+  int *best = reinterpret_cast<int *>(wsm);
+  float *mx_s = reinterpret_cast<float *>(wsm + 16);
+  int *top_s = reinterpret_cast<int *>(mx_s + npos);
+  uint32_t *fl_s = reinterpret_cast<uint32_t *>(top_s + npos);
+  for (int j = warp; j < npos; j += kWalkWarps) {
+    float mx;
+    int top;
+    uint32_t f;
+    combine_position(P.part + ((size_t)b * npos + j) * P.nslices, P.nslices, lane, &mx, &top, &f);
+    if (lane == 0) {
+      mx_s[j] = mx;
+      top_s[j] = top;
+      fl_s[j] = f;
+    }
   }
+  __syncthreads();
+  if (warp != 0) return;
+  if (P.tree) walk_tree<BF16>(P, b, lane, mx_s, top_s, fl_s, reinterpret_cast<unsigned char *>(fl_s + npos), best);
+  else walk_greedy_chain<BF16>(P, b, lane, mx_s, top_s, fl_s);
 }
 
-// Set the shared-memory attribute once per device (again only if more is needed).
-template <bool BF16>
-cudaError_t prepare(size_t smem) {
-  static std::atomic<size_t> done_smem[kMaxDevices];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (done_smem[dev].load() >= smem) return cudaSuccess;
-  e = cudaFuncSetAttribute(greedy_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
-  if (e == cudaSuccess) done_smem[dev].store(smem);
-  return e;
+template <bool BF16, bool VEC>
+void launch_stream(const GreedyParams &p, int grid, cudaStream_t s) {
+  greedy_kernel<BF16, VEC><<<grid, kGreedyThreads, 0, s>>>(p);
 }
 
 }  // namespace
 
-cudaError_t launch_greedy(const GreedyParams &p, bool bf16, int grid, size_t smem, cudaStream_t s) {
-  cudaError_t e = bf16 ? prepare<true>(smem) : prepare<false>(smem);
+cudaError_t launch_greedy(const GreedyParams &p, bool bf16, int grid, cudaStream_t s) {
+  if (bf16) p.vec ? launch_stream<true, true>(p, grid, s) : launch_stream<true, false>(p, grid, s);
+  else p.vec ? launch_stream<false, true>(p, grid, s) : launch_stream<false, false>(p, grid, s);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (bf16) greedy_kernel<true><<<grid, NT, smem, s>>>(p);
-  else greedy_kernel<false><<<grid, NT, smem, s>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  // walk: trees need N*20 bytes of scratch per row, so one warp per block;
-  // chains take four rows per block
-  const int rows_per_block = p.tree ? 1 : 4;
+  // walk: 16 bytes + 12 per position for the combined positions, and 12 more
+  // per node for the tree walk's scratch
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((p.B + rows_per_block - 1) / rows_per_block));
-  cfg.blockDim = dim3(static_cast<unsigned>(32 * rows_per_block));
-  cfg.dynamicSmemBytes = p.tree ? 16 + static_cast<size_t>(p.npos) * 20 : 0;
+  cfg.gridDim = dim3(static_cast<unsigned>(p.B));
+  cfg.blockDim = dim3(kWalkThreads);
+  cfg.dynamicSmemBytes = 16 + static_cast<size_t>(p.npos) * (p.tree ? 24 : 12);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -437,11 +400,10 @@ cudaError_t launch_greedy(const GreedyParams &p, bool bf16, int grid, size_t sme
               : cudaLaunchKernelEx(&cfg, greedy_walk_kernel<false>, p);
 }
 
-cudaError_t greedy_max_blocks_per_sm(bool bf16, size_t smem, int *blocks) {
-  cudaError_t e = bf16 ? prepare<true>(smem) : prepare<false>(smem);
-  if (e != cudaSuccess) return e;
-  return bf16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, greedy_kernel<true>, NT, smem)
-              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, greedy_kernel<false>, NT, smem);
+cudaError_t greedy_max_blocks_per_sm(bool bf16, bool vec, int *blocks) {
+  const void *k = bf16 ? (vec ? (const void *)greedy_kernel<true, true> : (const void *)greedy_kernel<true, false>)
+                       : (vec ? (const void *)greedy_kernel<false, true> : (const void *)greedy_kernel<false, false>);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, k, kGreedyThreads, 0);
 }
 
 }  // namespace sv

@@ -110,13 +110,9 @@ struct GreedyParams {
   int32_t *path_nodes;     // tree only
   GreedyPart *part;        // [B*npos*nslices] workspace
   int B, npos, V;
-  int slice;               // elements per slice
+  int slice;               // elements per slice (a multiple of 16 bytes' worth)
   int nslices;
-  int use_tma;
-  int stages;
-  int buf_bytes;
-  uint64_t wait_limit_ns;
-  int force_timeout;
+  int vec;                 // rows are 16-byte aligned: whole-vector loads
 };
 
 struct RollbackParams {
@@ -148,7 +144,8 @@ constexpr int kSoftMinSlice = kSoftThreads * 4 * 4;
 // Largest rounds of 32 vectors per warp in the resolve kernel.
 constexpr int kResolveMaxRounds = 16;
 // Elements per greedy work item.
-constexpr int kGreedySlice = 16384;
+constexpr int kGreedySlice = 16384;  // largest slice (elements)
+constexpr int kGreedyThreads = 256;  // streaming greedy kernel block
 // Devices whose per-kernel attributes are cached.
 constexpr int kMaxDevices = 64;
 constexpr int kDriftMaxK = 64;        // drafted positions per row for spec_drift_residuals
@@ -165,9 +162,8 @@ cudaError_t launch_chain_truncated(const ChainStochParams &p, bool bf16, int gri
 cudaError_t launch_drift(const ChainStochParams &p, bool bf16, int grid, size_t smem,
                          cudaStream_t s);
 cudaError_t soft_partials_blocks_per_sm(bool bf16, int nv, size_t smem, int *blocks);
-cudaError_t launch_greedy(const GreedyParams &p, bool bf16, int grid, size_t smem,
-                          cudaStream_t s);
-cudaError_t greedy_max_blocks_per_sm(bool bf16, size_t smem, int *blocks);
+cudaError_t launch_greedy(const GreedyParams &p, bool bf16, int grid, cudaStream_t s);
+cudaError_t greedy_max_blocks_per_sm(bool bf16, bool vec, int *blocks);
 cudaError_t launch_rollback(const RollbackParams &p, cudaStream_t s);
 
 }  // namespace sv
