@@ -39,9 +39,9 @@ TRAFFIC = 180649728 + 3448576
 # the same for one greedy_kernel launch on the tree workload
 # (profiles/greedy_tree_c4.md): 583,470,336 read + 3,753,984 written
 TREE_TRAFFIC = 583470336 + 3753984
-# kernels one stochastic spec_verify_chain call enqueues: the stream kernel
-# and the resolve kernel
-KERNELS_PER_STEP = 2
+# kernels one stochastic spec_verify_chain call enqueues: the one-thread
+# generation step, the stream kernel and the resolve kernel
+KERNELS_PER_STEP = 3
 
 
 def parse():
@@ -489,7 +489,7 @@ def run_next(args):
                              "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
                              "kernel": "softmax_partials + trunc + chain_resolve",
                              "algorithmic_bytes_per_launch": step_bytes, "traffic": None},
-                "gpu_launches": 3 * n, "clocks": clocks}
+                "gpu_launches": 4 * n, "clocks": clocks}
     elif args.workload == "tree":
         # greedy tree verification with the margin rule on the tree workload
         inp = S.make("c4")
@@ -553,7 +553,7 @@ def run_next(args):
                              "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
                              "kernel": "softmax_partials_kernel + drift_select_kernel",
                              "algorithmic_bytes_per_launch": alg, "traffic": None},
-                "gpu_launches": 2 * n, "clocks": clocks}
+                "gpu_launches": 3 * n, "clocks": clocks}
     else:
         B = 4096
         rng = np.random.default_rng(3)

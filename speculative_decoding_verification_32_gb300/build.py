@@ -28,6 +28,7 @@ def _nvcc():
 def _deps():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
     files.append(os.path.join(INCLUDE, "specverify.h"))
+    files.append(os.path.abspath(__file__))
     return files
 
 
@@ -43,6 +44,8 @@ def build(force=False, verbose_ptxas=False):
              "-I", INCLUDE, "-I", CSRC]
     if verbose_ptxas:
         flags += ["-Xptxas", "-v"]
+    # extra nvcc flags for tuning builds (e.g. -DSV_FUSED_U=4)
+    flags += os.environ.get("SPECVERIFY_NVCC_FLAGS", "").split()
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")

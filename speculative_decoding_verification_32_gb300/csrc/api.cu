@@ -189,12 +189,11 @@ spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes
   p.wait_limit_ns = g_wait_ns.load();
   p.force_timeout = g_force_timeout.load();
   {
-    // workspace tail: header {claim, -, magic} in the last 16 bytes, one
-    // generation word per row below it
+    // workspace tail: header {claim, generation, magic} in the last 16 bytes
     char *end = static_cast<char *>(ws) + (ws_bytes & ~static_cast<size_t>(15));
     p.claim = reinterpret_cast<uint32_t *>(end - 16);
+    p.gen = reinterpret_cast<uint32_t *>(end - 12);
     p.magic = reinterpret_cast<unsigned long long *>(end - 8);
-    p.gen = reinterpret_cast<uint32_t *>(end - 16);
     // SPECVERIFY_DYNAMIC=0 keeps every tile statically assigned;
     // SPECVERIFY_DYN_CHUNK sets the tiles per claim (tuning)
     const char *dv = std::getenv("SPECVERIFY_DYNAMIC");

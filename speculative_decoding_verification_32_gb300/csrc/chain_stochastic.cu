@@ -175,7 +175,7 @@ struct alignas(16) TileInfo {
   int keep;        // 1: load without the evict-first hint
   int first;       // 1: first tile of a run
   int last;        // 1: last tile of a run
-  uint32_t tag;    // generation + 1 of the row: stamped on its partial records
+  uint32_t tag;    // the call's tag: stamped on the partial records
 };
 
 struct alignas(16) SoftCtrl {
@@ -302,7 +302,7 @@ __device__ __forceinline__ TileInfo make_tile(const ChainStochParams &P, int gt,
     const int y = __ldg(P.tokens + (size_t)b * K + j);
     if (y >= s0 && y < s0 + it.len) it.yl = y - s0;
   }
-  it.tag = P.gen[-1 - b] + 1u;
+  it.tag = *reinterpret_cast<volatile const uint32_t *>(P.gen);
   return it;
 }
 
@@ -890,13 +890,13 @@ __global__ void __launch_bounds__(kResolveThreads, 4) chain_resolve_kernel(const
   // read those decisions after one cluster barrier.
   if (crank == 0) {
     const RowScalars first = load_scalars(P, b, lane);
-    const uint32_t gen = *reinterpret_cast<volatile const uint32_t *>(P.gen - 1 - b);
+    const uint32_t tag = *reinterpret_cast<volatile const uint32_t *>(P.gen);
     // a truncated verify also needs the threshold kernel's records (that
     // grid completes after the stream kernel)
     if (P.trunc) asm volatile("griddepcontrol.wait;" ::: "memory");
     bool gave_up = false;
     const uint64_t t0 = global_timer_ns();
-    while (!__syncthreads_and(fold_rows(P, b, s2, gen + 1u, warp, lane, rstat))) {
+    while (!__syncthreads_and(fold_rows(P, b, s2, tag, warp, lane, rstat))) {
       if (__syncthreads_or(global_timer_ns() - t0 > P.wait_limit_ns)) {  // bounded
         gave_up = true;
         break;
@@ -906,7 +906,6 @@ __global__ void __launch_bounds__(kResolveThreads, 4) chain_resolve_kernel(const
     if (warp == 0)
       decide_row(P, b, s2, tflags | (gave_up ? F_TIMEOUT : 0u), lane, true, rstat, first, ctl, BF16);
     __syncthreads();
-    if (tid == 0) P.gen[-1 - b] = gen + 1u;  // only this CTA read it
   }
   cluster_sync();  // rank 0's decisions are in its shared memory
   if (crank != 0 && tid < 3) {  // Mp..Sq, u..trunc, thp..: three 16-byte blocks
@@ -1264,11 +1263,11 @@ __global__ void __launch_bounds__(kDriftThreads) drift_select_kernel(const __gri
   const float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
   const uint32_t tflags = (T > 0.f && T < kInf) ? 0u : F_BAD_TEMPERATURE;
   const float s2 = tflags ? 1.f : __fdiv_rn(kLog2e, T);
-  const uint32_t gen = *reinterpret_cast<volatile const uint32_t *>(P.gen - 1 - b);
+  const uint32_t tag = *reinterpret_cast<volatile const uint32_t *>(P.gen);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // every position's statistics (the row's status covers all of them)
   bool ready = true;
-  if (warp < kResolveThreads / 32) ready = fold_rows(P, b, s2, gen + 1u, warp, lane, rstat);
+  if (warp < kResolveThreads / 32) ready = fold_rows(P, b, s2, tag, warp, lane, rstat);
   ready = __syncthreads_and(ready);  // the stream kernel is done: stale means lost
   if (tid == 0) {
     uint32_t f = tflags | (ready ? 0u : F_TIMEOUT);
@@ -1637,7 +1636,7 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
   if (!trunc_active(P, b, V, &tk, &tp)) return;
   const float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
   const float s2 = (T > 0.f && T < kInf) ? __fdiv_rn(kLog2e, T) : 1.f;
-  const uint32_t gen = *reinterpret_cast<volatile const uint32_t *>(P.gen - 1 - b);
+  const uint32_t tag = *reinterpret_cast<volatile const uint32_t *>(P.gen);
   // ---- this row's max and sum (warp 0 folds its partial records)
   const int nt = P.nslices;
   if (warp == 0) {
@@ -1646,7 +1645,7 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
     for (int t = lane; t < nt; t += 32) {
       float qm, qs;
       uint32_t qf;
-      if (!load_part(P.part + (size_t)row * nt + t, gen + 1u, &qm, &qs, &qf)) f |= F_TIMEOUT;
+      if (!load_part(P.part + (size_t)row * nt + t, tag, &qm, &qs, &qf)) f |= F_TIMEOUT;
       f |= qf;
       const float mn = fmax_nan(m, qm);
       sacc = (m == -kInf ? 0.f : sacc * ex2(__fmul_rn(m - mn, s2))) +
@@ -1936,10 +1935,21 @@ cudaError_t prepare(size_t smem, int cluster) {
 template <bool BF16>
 cudaError_t launch_resolve(const ChainStochParams &p, int cluster, cudaStream_t s);
 
+// Advances the workspace's generation word: the call's tag (one thread, a
+// plain launch ahead of the stream kernel).
+__global__ void advance_generation_kernel(uint32_t *gen) { *gen += 1u; }
+
+cudaError_t launch_advance_generation(uint32_t *gen, cudaStream_t s) {
+  advance_generation_kernel<<<1, 1, 0, s>>>(gen);
+  return cudaGetLastError();
+}
+
 template <bool BF16, int NV, int S>
 cudaError_t launch_t(const ChainStochParams &p, int grid, size_t smem, int cluster,
                      cudaStream_t s) {
   cudaError_t e = prepare<BF16, NV, S>(smem, cluster);
+  if (e != cudaSuccess) return e;
+  e = launch_advance_generation(p.gen, s);
   if (e != cudaSuccess) return e;
   softmax_partials_kernel<BF16, NV, S><<<grid, kSoftThreads + 32, smem, s>>>(p);
   e = cudaGetLastError();
@@ -1951,6 +1961,8 @@ template <bool BF16, int NV, int S>
 cudaError_t launch_truncated_t(const ChainStochParams &p, int grid, size_t smem, int cluster,
                                cudaStream_t s) {
   cudaError_t e = prepare<BF16, NV, S>(smem, cluster);
+  if (e != cudaSuccess) return e;
+  e = launch_advance_generation(p.gen, s);
   if (e != cudaSuccess) return e;
   softmax_partials_kernel<BF16, NV, S><<<grid, kSoftThreads + 32, smem, s>>>(p);
   e = cudaGetLastError();
@@ -1993,6 +2005,8 @@ cudaError_t launch_resolve(const ChainStochParams &p, int cluster, cudaStream_t 
 template <bool BF16, int S>
 cudaError_t launch_drift_t(const ChainStochParams &p, int grid, size_t smem, cudaStream_t s) {
   cudaError_t e = prepare<BF16, 4, S>(smem, 1);
+  if (e != cudaSuccess) return e;
+  e = launch_advance_generation(p.gen, s);
   if (e != cudaSuccess) return e;
   softmax_partials_kernel<BF16, 4, S><<<grid, kSoftThreads + 32, smem, s>>>(p);
   e = cudaGetLastError();

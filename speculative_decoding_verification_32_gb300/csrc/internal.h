@@ -11,9 +11,10 @@ namespace sv {
 // kernel: a run of consecutive tiles of one row streamed by one CTA leaves its
 // max logit m and sum of exp2((x - m) s2) at the run's first tile and empty
 // partials (m = -inf, s = 0) at its other tiles.  Two 64-bit words, each
-// written by one relaxed store and each carrying the row's generation + 1
-// (the tag): a = m | tag << 32, b = s | (flags & 0xff | tag << 8) << 32.  A
-// reader that finds the tag in both words holds a record of this call.
+// written by one relaxed store and each carrying the call's tag (the
+// workspace's generation word, advanced before every call): a = m | tag << 32,
+// b = s | (flags & 0xff | tag << 8) << 32.  A reader that finds the tag in both
+// words holds a record of this call.
 struct alignas(16) SoftPart {
   unsigned long long a, b;
 };
@@ -65,15 +66,17 @@ struct ChainStochParams {
   uint64_t wait_limit_ns;
   int force_timeout;
   // Dynamic tail of the partial kernel.  The workspace ends with a header
-  // {claim counter, -, magic} and, below it, one generation word per row.
-  // When the header holds kWsMagic the tiles of the last phase are claimed in
-  // chunks of dyn_chunk through the counter (the resolve kernel re-arms the
-  // header afterwards); otherwise every tile is assigned statically.  Each
-  // partial record carries its row's generation + 1, which the resolve
-  // kernel checks, so a record this call did not write is never used.
+  // {claim counter, generation, magic}.  When the header holds kWsMagic the
+  // tiles of the last phase are claimed in chunks of dyn_chunk through the
+  // counter (the resolve kernel re-arms the header afterwards); otherwise
+  // every tile is assigned statically.  The generation word is advanced
+  // before every call and stamped on every record as its tag, which the
+  // readers check, so a record this call did not write is never used --
+  // whatever shapes earlier calls on the workspace had (their records sit at
+  // other offsets, but all carry older tags).
   uint32_t *claim;
   unsigned long long *magic;
-  uint32_t *gen;       // gen[-1 - b]: generation word of row b
+  uint32_t *gen;       // the workspace's generation word (the call's tag)
   int dyn;             // 0: static assignment only
   int dyn_chunk;       // tiles per claim
   // top-k / top-p truncation (spec_verify_chain_truncated): per-row
@@ -89,11 +92,9 @@ struct ChainStochParams {
 };
 
 constexpr unsigned long long kWsMagic = 0x5EC7E21F1CA7E5EDull;  // armed workspace header
-// Workspace tail: header (16 bytes) plus one 4-byte generation word per row,
-// with room for the header's 16-byte alignment below an arbitrary end.
-inline size_t ws_tail_bytes(long long B) {
-  return (32 + 4 * static_cast<size_t>(B) + 255) / 256 * 256;
-}
+// Workspace tail: the header (16 bytes), with room for its 16-byte alignment
+// below an arbitrary end.
+inline size_t ws_tail_bytes(long long) { return 256; }
 
 struct GreedyParams {
   const void *target;

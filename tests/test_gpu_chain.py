@@ -270,6 +270,29 @@ def test_workspace_first_use_and_reuse(sv, name):
             assert claim == 0  # the resolve kernel left the counter reset
 
 
+def test_workspace_shared_across_shapes(sv):
+    """One workspace serves calls of different shapes in turn: their records
+    sit at different offsets, and only the generation stamp keeps a call from
+    reading what an earlier call of another shape left there."""
+    import torch
+    from speculative_decoding_verification_32_gb300 import _binding as Bn
+    L = Bn.lib()
+    shapes = [("c2", {}), ("chain", dict(B=6, K=1, V=4099)), ("c2", dict(B=3)),
+              ("chain", dict(B=8, K=3, V=20000)), ("c2", {}), ("chain", dict(B=6, K=1, V=4099))]
+    cases = []
+    for name, kw in shapes:
+        if name == "chain":
+            inp = S.chain_inputs(dtype="bf16", sigma=2.0, seed=kw["V"] + kw["K"], temperature=(0.7, 1.3), **kw)
+        else:
+            inp = S.make(name, **kw)
+        cases.append(inp)
+    need = max(L.spec_verify_chain_workspace_size(i["target"].shape[0], i["target"].shape[1] - 1,
+                                                  i["target"].shape[2]) for i in cases)
+    ws = torch.full((need,), 0xA5, dtype=torch.uint8, device="cuda")
+    for inp in cases:
+        compare_stochastic(chain_via_abi(L, inp, ws), oracle_chain(inp))
+
+
 # ------------------------------------------------------ top-k / top-p truncation
 def _trunc_params(rng, B, V):
     k = rng.choice([0, 1, 2, 20, 50, 1000, V], B).astype(np.int32)
