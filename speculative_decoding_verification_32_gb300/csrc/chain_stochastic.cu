@@ -221,6 +221,34 @@ __device__ __forceinline__ uint32_t elem_bits(const uint32_t *w, int e) {
   else return w[e];
 }
 
+// The logit value whose order key is k (inverse of order_key).
+template <bool BF16>
+__device__ __forceinline__ float key_value(uint32_t k) {
+  if constexpr (BF16) {
+    const uint32_t bits = (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
+    return __uint_as_float(bits << 16);
+  } else {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+  }
+}
+
+// Whether some element of a 16-byte vector may have an order key >= the key
+// of value tf: its packed maximum is not below tf.  Conservative (a NaN
+// element or threshold answers yes); every element whose key reaches the
+// threshold has a value >= tf, so a "no" is exact.
+template <bool BF16>
+__device__ __forceinline__ bool vec_may_reach(const uint32_t *w, float tf) {
+  float m;
+  if constexpr (BF16) {
+    const uint32_t p = bf16x2_max_nan(bf16x2_max_nan(w[0], w[1]), bf16x2_max_nan(w[2], w[3]));
+    m = fmax_nan(bf16_lo(p), bf16_hi(p));
+  } else {
+    m = fmax_nan(fmax_nan(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                 fmax_nan(__uint_as_float(w[2]), __uint_as_float(w[3])));
+  }
+  return !(m < tf);
+}
+
 // The row's top-k / top-p parameters; false when neither truncates.
 __device__ __forceinline__ bool trunc_active(const ChainStochParams &P, int b, int V, int *k,
                                              float *tp) {
@@ -1352,32 +1380,28 @@ __global__ void __launch_bounds__(kDriftThreads) drift_select_kernel(const __gri
   // ---- one pass: every key >= tau into the candidate list
   auto collect = [&](uint32_t tau) {
     if (tid == 0) ctl.n_cand = 0;
+    const float tau_f = key_value<BF16>(tau);
     __syncthreads();
     constexpr int U = 4;  // vectors in flight per thread
     for (int v0 = tid; v0 < nvec; v0 += U * kDriftThreads) {
       uint32_t w[U][4];
 #pragma unroll
       for (int u = 0; u < U; ++u) F::load_vec(w[u], nullptr, tg, aligned, v0 + u * kDriftThreads, V);
-      const unsigned act = __activemask();
 #pragma unroll
       for (int u = 0; u < U; ++u) {
+        // fewer than one vector in ten holds a candidate: each lane looks at
+        // its own elements only when its vector's maximum reaches tau, and
+        // appends them one by one (the selection does not depend on order)
+        if (!vec_may_reach<BF16>(w[u], tau_f)) continue;
 #pragma unroll
         for (int e = 0; e < EPV; ++e) {
           const int idx = (v0 + u * kDriftThreads) * EPV + e;
           const uint32_t k = order_key<BF16>(elem_bits<BF16>(w[u], e));
-          const bool c = k >= tau && idx < V;
-          const unsigned bal = __ballot_sync(act, c);
-          if (bal) {
-            const int leader = __ffs(bal) - 1;
-            int base = 0;
-            if (lane == leader) base = atomicAdd(&ctl.n_cand, __popc(bal));
-            base = __shfl_sync(act, base, leader);
-            if (c) {
-              const int slot = base + __popc(bal & ((1u << lane) - 1u));
-              if (slot < kDriftCand) {
-                ctl.cand.key[slot] = k;
-                ctl.cand.idx[slot] = idx;
-              }
+          if (k >= tau && idx < V) {
+            const int slot = atomicAdd(&ctl.n_cand, 1);
+            if (slot < kDriftCand) {
+              ctl.cand.key[slot] = k;
+              ctl.cand.idx[slot] = idx;
             }
           }
         }
@@ -1702,10 +1726,18 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
   };
   // ---- sampled threshold tau (as in the DRIFT selection): the r-th largest
   // key of every kDriftSample-th element
+  constexpr int kNS = (SPEC_MAX_V + kDriftSample * kDriftThreads - 1) / (kDriftSample * kDriftThreads);
+  uint32_t smp[kNS];  // this thread's samples, loaded once
+#pragma unroll
+  for (int q = 0; q < kNS; ++q) {
+    const int i = (tid + q * kDriftThreads) * kDriftSample;
+    smp[q] = i < V ? order_key<BF16>(bits_at(i)) : 0u;
+  }
   const int n_samples = (V + kDriftSample - 1) / kDriftSample;
   auto samples = [&](auto f) {
-    for (int i = tid * kDriftSample; i < V; i += kDriftThreads * kDriftSample)
-      f(order_key<BF16>(bits_at(i)));
+#pragma unroll
+    for (int q = 0; q < kNS; ++q)
+      if ((tid + q * kDriftThreads) * kDriftSample < V) f(smp[q]);
   };
   auto sample_tau = [&](int r) -> uint32_t {
     if (r > n_samples) return 0u;
@@ -1716,33 +1748,28 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
   // ---- candidates: every key >= tau, with its mass
   auto collect = [&](uint32_t tau) {
     if (tid == 0) ctl.n_cand = 0;
+    const float tau_f = key_value<BF16>(tau);
     __syncthreads();
     constexpr int U = 4;
     for (int v0 = tid; v0 < nvec; v0 += U * kDriftThreads) {
       uint32_t w[U][4];
 #pragma unroll
       for (int u = 0; u < U; ++u) F::load_vec(w[u], nullptr, src, aligned, v0 + u * kDriftThreads, V);
-      const unsigned act = __activemask();
 #pragma unroll
       for (int u = 0; u < U; ++u) {
+        // a lane looks at its elements only when its vector's maximum
+        // reaches tau, and appends them one by one (they are sorted later)
+        if (!vec_may_reach<BF16>(w[u], tau_f)) continue;
 #pragma unroll
         for (int e = 0; e < EPV; ++e) {
           const int idx = (v0 + u * kDriftThreads) * EPV + e;
           const uint32_t bits = elem_bits<BF16>(w[u], e);
           const uint32_t k = order_key<BF16>(bits);
-          const bool c = k >= tau && idx < V;
-          const unsigned bal = __ballot_sync(act, c);
-          if (bal) {
-            const int leader = __ffs(bal) - 1;
-            int base = 0;
-            if (lane == leader) base = atomicAdd(&ctl.n_cand, __popc(bal));
-            base = __shfl_sync(act, base, leader);
-            if (c) {
-              const int slot = base + __popc(bal & ((1u << lane) - 1u));
-              if (slot < kDriftCand) {
-                ctl.ck[slot] = (static_cast<unsigned long long>(k) << 32) | (~static_cast<uint32_t>(idx));
-                ctl.e[slot] = mass_of(bits);
-              }
+          if (k >= tau && idx < V) {
+            const int slot = atomicAdd(&ctl.n_cand, 1);
+            if (slot < kDriftCand) {
+              ctl.ck[slot] = (static_cast<unsigned long long>(k) << 32) | (~static_cast<uint32_t>(idx));
+              ctl.e[slot] = mass_of(bits);
             }
           }
         }
@@ -1820,14 +1847,49 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
       r *= 4;
       continue;
     }
-    sort_and_scan(nc);
+    // With top-k only the candidates at or above the k-th largest key (ties
+    // included) can be kept, and the nucleus lies among them: select that key
+    // by radix, keep those candidates, sort only them.  Their order and prefix
+    // sums are those of the full sort's first entries.
+    int ns = nc;
+    if (tk > 0) {
+      auto cand_keys = [&](auto f) {
+        for (int i = tid; i < nc; i += kDriftThreads) f(key_at(i));
+      };
+      int na, ne;
+      const uint32_t thk = block_kth_largest<KEYBITS, kDriftThreads>(cand_keys, tk, ctl.chist, &ctl.digit,
+                                                                    &ctl.above, na, ne);
+      constexpr int PER = kDriftCand / kDriftThreads;
+      unsigned long long kk[PER];
+      float ee[PER];
+#pragma unroll
+      for (int q = 0; q < PER; ++q) {
+        const int i = tid + q * kDriftThreads;
+        kk[q] = i < nc ? ctl.ck[i] : 0ull;
+        ee[q] = i < nc ? ctl.e[i] : 0.f;
+      }
+      if (tid == 0) ctl.n_cand = 0;
+      __syncthreads();
+#pragma unroll
+      for (int q = 0; q < PER; ++q) {
+        const int i = tid + q * kDriftThreads;
+        if (i < nc && static_cast<uint32_t>(kk[q] >> 32) >= thk) {
+          const int slot = atomicAdd(&ctl.n_cand, 1);
+          ctl.ck[slot] = kk[q];
+          ctl.e[slot] = ee[q];
+        }
+      }
+      __syncthreads();
+      ns = ctl.n_cand;
+    }
+    sort_and_scan(ns);
     // top-k: the k-th candidate's key, through the end of its group of ties
-    int gk = nc - 1;
+    int gk = ns - 1;
     float Sk = ctl.S;
     if (tk > 0) {
       if (tid == 0) {
         int g = tk - 1;
-        while (g + 1 < nc && key_at(g + 1) == key_at(tk - 1)) ++g;
+        while (g + 1 < ns && key_at(g + 1) == key_at(tk - 1)) ++g;
         ctl.pos = g;
       }
       __syncthreads();
@@ -1836,7 +1898,7 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
     }
     if (tp < 1.f) {
       const float target = __fmul_rn(tp, Sk);
-      if (tk == 0 && !(ctl.e[nc - 1] >= target)) {  // the nucleus reaches below tau
+      if (tk == 0 && !(ctl.e[ns - 1] >= target)) {  // the nucleus reaches below tau
         r *= 4;
         __syncthreads();
         continue;
@@ -1849,7 +1911,7 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
           else lo = mid + 1;
         }
         int g = lo;
-        while (g + 1 < nc && key_at(g + 1) == key_at(lo)) ++g;
+        while (g + 1 < ns && key_at(g + 1) == key_at(lo)) ++g;
         ctl.pos = lo;
         ctl.digit = g;
       }
