@@ -32,10 +32,10 @@ WORKLOAD = "c3"
 METRIC = "verify steps/s and achieved HBM GB/s (B=64,K=5,V=128256 bf16) vs 8 TB/s"
 UNIT = "verify steps/s"
 L2_BYTES = 129 * 1024 * 1024
-# ncu dram__bytes_read.sum + dram__bytes_write.sum of one softmax_partials_kernel
-# launch on this workload (profiles/softmax_partials_chain_c3.md): 180,649,728
+# ncu dram__bytes_read.sum + dram__bytes_write.sum of one stream_partials_kernel
+# launch on this workload (profiles/stream_partials_chain_c3.md): 180,649,728
 # read + 3,448,576 written; reset to None whenever that kernel changes
-TRAFFIC = 180649728 + 3448576
+TRAFFIC = None
 # the same for one greedy_kernel launch on the tree workload
 # (profiles/greedy_tree_c4.md): 583,470,336 read + 3,753,984 written
 TREE_TRAFFIC = 583470336 + 3753984
@@ -360,7 +360,7 @@ def run_ours(args):
         "achieved_hbm_gbs": gbs,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                      "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
-                     "kernel": "softmax_partials_kernel<bf16,4,2> (dominant) + "
+                     "kernel": "stream_partials_kernel<bf16> (dominant) + "
                                "chain_resolve_kernel<bf16> (PDL); achieved = algorithmic "
                                "bytes / whole-step time, a lower bound for the stream kernel",
                      "algorithmic_bytes_per_launch": step_bytes, "traffic": TRAFFIC},
@@ -487,7 +487,7 @@ def run_next(args):
                            "l2": f"{n_sets} rotating input sets > L2"},
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                              "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
-                             "kernel": "softmax_partials + trunc + chain_resolve",
+                             "kernel": "stream_partials + trunc + chain_resolve",
                              "algorithmic_bytes_per_launch": step_bytes, "traffic": None},
                 "gpu_launches": 4 * n, "clocks": clocks}
     elif args.workload == "tree":
@@ -551,7 +551,7 @@ def run_next(args):
                            "l2": f"{n_sets} rotating input sets > L2"},
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                              "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
-                             "kernel": "softmax_partials_kernel + drift_select_kernel",
+                             "kernel": "stream_partials_kernel + drift_select_kernel",
                              "algorithmic_bytes_per_launch": alg, "traffic": None},
                 "gpu_launches": 3 * n, "clocks": clocks}
     else:

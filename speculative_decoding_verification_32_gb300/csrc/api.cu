@@ -35,8 +35,8 @@ std::map<std::tuple<int, int, size_t>, int> g_blocks;
 std::map<std::tuple<int, int, int>, int> g_greedy_blocks;
 void *g_static_ws_ptr[kMaxDevices] = {};  // device address of g_static_ws, per device
 
-constexpr size_t kSoftCtrlBytes = 2048;
 constexpr int kMinGreedySlice = 2048;
+constexpr size_t kRingCtrlBytes = 2048;  // the ring stream kernel's control block
 
 // SPECVERIFY_VERBOSE=1 prints each distinct launch shape once (stderr).
 void report(const char *what, long long a, long long b, long long c, long long d, long long e,
@@ -80,8 +80,8 @@ cudaError_t device_info(int *dev, DevInfo *info) {
   return cudaSuccess;
 }
 
-cudaError_t soft_blocks(int dev, bool bf16, int nv, size_t smem, int *out) {
-  auto key = std::make_tuple(dev, 2 + (int)bf16 + 2 * nv, smem);
+cudaError_t soft_blocks(int dev, bool bf16, bool vec, int *out) {
+  auto key = std::make_tuple(dev, 2 + (int)bf16, static_cast<size_t>(vec));
   {
     std::lock_guard<std::mutex> lk(g_mu);
     auto it = g_blocks.find(key);
@@ -90,7 +90,24 @@ cudaError_t soft_blocks(int dev, bool bf16, int nv, size_t smem, int *out) {
       return cudaSuccess;
     }
   }
-  cudaError_t e = soft_partials_blocks_per_sm(bf16, nv, smem, out);
+  cudaError_t e = stream_blocks_per_sm(bf16, vec, out);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_blocks[key] = *out;
+  return cudaSuccess;
+}
+
+cudaError_t ring_blocks(int dev, bool bf16, int stages, size_t smem, int *out) {
+  auto key = std::make_tuple(dev, 8 + (int)bf16 + 2 * stages, smem);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_blocks.find(key);
+    if (it != g_blocks.end()) {
+      *out = it->second;
+      return cudaSuccess;
+    }
+  }
+  cudaError_t e = ring_blocks_per_sm(bf16, stages, smem, out);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lk(g_mu);
   g_blocks[key] = *out;
@@ -165,7 +182,7 @@ spec_status run_greedy(GreedyParams &p, bool bf16, int esz, void *ws, cudaStream
 // resolve kernel's cluster split, from the arguments and the workspace;
 // output pointers are left for the caller.
 spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes, ChainStochParams &p,
-                             int &grid, size_t &smem, int &nv, int &C) {
+                             int &grid, int &C, bool ring, size_t *smem) {
   const int K = a->K;
   const int esz = a->dtype == SPEC_BF16 ? 2 : 4;
   const bool bf16 = a->dtype == SPEC_BF16;
@@ -188,36 +205,40 @@ spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes
               (static_cast<long long>(a->V) * esz) % 16 == 0;
   p.wait_limit_ns = g_wait_ns.load();
   p.force_timeout = g_force_timeout.load();
+  // workspace tail: a 16-byte header {claim counter, generation, -}
   {
-    // workspace tail: header {claim, generation, magic} in the last 16 bytes
     char *end = static_cast<char *>(ws) + (ws_bytes & ~static_cast<size_t>(15));
     p.claim = reinterpret_cast<uint32_t *>(end - 16);
     p.gen = reinterpret_cast<uint32_t *>(end - 12);
-    p.magic = reinterpret_cast<unsigned long long *>(end - 8);
-    // SPECVERIFY_DYNAMIC=0 keeps every tile statically assigned;
-    // SPECVERIFY_DYN_CHUNK sets the tiles per claim (tuning)
-    const char *dv = std::getenv("SPECVERIFY_DYNAMIC");
-    p.dyn = !(dv && *dv == '0');
+  }
+  // SPECVERIFY_DYNAMIC=0: no claimed tail in either stream kernel (tuning)
+  p.stream_dyn = 1;
+  if (const char *ov = std::getenv("SPECVERIFY_DYNAMIC")) p.stream_dyn = std::atoi(ov) != 0;
+  *smem = 0;
+  if (ring) {
+    // the bulk-copy ring: pair tiles of 8192 bf16 / 4096 fp32 logits per law;
+    // SPECVERIFY_SOFT_STAGES (2 or 3) and SPECVERIFY_DYN_CHUNK (tiles per
+    // claim) override the defaults for tuning
+    p.slice = kSoftThreads * kSoftVecs * epv;
+    p.stages = kSoftStages;
+    if (const char *ov = std::getenv("SPECVERIFY_SOFT_STAGES")) p.stages = std::atoi(ov) == 3 ? 3 : 2;
     p.dyn_chunk = 2;
     if (const char *dc = std::getenv("SPECVERIFY_DYN_CHUNK")) {
       const int c = std::atoi(dc);
       if (c >= 1 && c <= 64) p.dyn_chunk = c;
     }
+    p.buf_bytes = 2 * p.slice * esz;  // target tile + draft tile
+    *smem = static_cast<size_t>(p.stages) * p.buf_bytes + kRingCtrlBytes;
+  } else {
+    // the plain-load stream: one item per (logit row, 4096-logit slice);
+    // SPECVERIFY_STREAM_SLICE (2048..16384, a multiple of 1024) overrides it
+    p.slice = kStreamSlice;
+    if (const char *ov = std::getenv("SPECVERIFY_STREAM_SLICE")) {
+      const int sl = std::atoi(ov);
+      if (sl >= 2048 && sl <= 16384 && sl % 1024 == 0 && sl >= kSoftMinSlice) p.slice = sl;
+    }
   }
-  // stream kernel: fixed-size items (16 or 32 KB), a bulk-copy ring per CTA;
-  // SPECVERIFY_SOFT_VECS (4 or 8) and SPECVERIFY_SOFT_STAGES (2..4) override
-  // the defaults for tuning
-  nv = kSoftVecs;
-  if (const char *ov = std::getenv("SPECVERIFY_SOFT_VECS")) nv = std::atoi(ov) == 8 ? 8 : 4;
-  p.slice = kSoftThreads * nv * epv;
   p.nslices = ceil_div(a->V, p.slice);
-  p.buf_bytes = 2 * p.slice * esz;  // target tile + draft tile
-  p.stages = kSoftStages;
-  if (const char *ov = std::getenv("SPECVERIFY_SOFT_STAGES")) {
-    const int st = std::atoi(ov);
-    if (st >= 2 && st <= 4) p.stages = st;
-  }
-  smem = static_cast<size_t>(p.stages) * p.buf_bytes + kSoftCtrlBytes;
   {
     const size_t rows = static_cast<size_t>(a->B) * (K + 1) + static_cast<size_t>(a->B) * K;
     p.ylog = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) +
@@ -226,9 +247,22 @@ spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes
     p.trunc_area = reinterpret_cast<TruncRec *>(reinterpret_cast<char *>(p.ylog) + align_up(rows * 8, 256));
   }
   int per_sm = 0;
-  if (soft_blocks(dev, bf16, nv, smem, &per_sm) != cudaSuccess || per_sm < 1) return SPEC_ERR_CUDA;
-  const long long tiles = (static_cast<long long>(a->B) * (K + 1) + static_cast<long long>(a->B) * K) * p.nslices;
-  grid = static_cast<int>(std::min<long long>(tiles, static_cast<long long>(di.sms) * per_sm));
+  const long long rows_all = static_cast<long long>(a->B) * (K + 1) + static_cast<long long>(a->B) * K;
+  if (ring) {
+    if (ring_blocks(dev, bf16, p.stages, *smem, &per_sm) != cudaSuccess || per_sm < 1) return SPEC_ERR_CUDA;
+    const long long tiles = static_cast<long long>(a->B) * (K + 1) * p.nslices;
+    grid = static_cast<int>(std::min<long long>(tiles, static_cast<long long>(di.sms) * per_sm));
+  } else {
+    if (soft_blocks(dev, bf16, p.use_tma != 0, &per_sm) != cudaSuccess || per_sm < 1) return SPEC_ERR_CUDA;
+    const long long items = rows_all * p.nslices;
+    const long long warps_per_block = kStreamThreads / 32;
+    grid = static_cast<int>(std::max<long long>(
+        1, std::min<long long>((items + warps_per_block - 1) / warps_per_block, static_cast<long long>(di.sms) * per_sm)));
+  }
+  if (const char *ov = std::getenv("SPECVERIFY_STREAM_GRID")) {  // tuning override
+    const long long g = std::atoll(ov);
+    if (g >= 1 && g <= static_cast<long long>(di.sms) * per_sm) grid = static_cast<int>(g);
+  }
   // resolve kernel: a cluster of C CTAs per row, at most 16 rounds of 32
   // vectors per warp
   constexpr int kRW = kResolveThreads / 32;
@@ -246,8 +280,7 @@ spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes
   }
   p.L = static_cast<int>(align_up(static_cast<size_t>(ceil_div(a->V, C)), static_cast<size_t>(epv)));
   p.vpw = 32 * rounds(C);
-  report("stochastic slice nslices stages grid per_sm cluster L", p.slice, p.nslices, p.stages,
-         grid, per_sm, C, p.L);
+  report("stochastic slice nslices grid per_sm cluster L", p.slice, p.nslices, grid, per_sm, C, p.L, 0);
   return SPEC_OK;
 }
 
@@ -325,10 +358,10 @@ spec_status spec_verify_chain(const spec_chain_args *a, const spec_chain_out *o,
   }
 
   ChainStochParams p;
-  int grid = 0, nv = 0, C = 0;
+  int grid = 0, C = 0;
   size_t smem = 0;
   {
-    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, smem, nv, C);
+    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, C, true, &smem);
     if (st != SPEC_OK) return st;
   }
   p.accepted_len = o->accepted_len;
@@ -338,7 +371,7 @@ spec_status spec_verify_chain(const spec_chain_args *a, const spec_chain_out *o,
   p.p_at_draft = o->p_at_draft;
   p.q_at_draft = o->q_at_draft;
   p.resid_mass = o->resid_mass;
-  if (launch_chain_stochastic(p, bf16, nv, grid, smem, C, s) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (launch_chain_stochastic(p, bf16, grid, smem, C, s) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
 }
 
@@ -374,10 +407,10 @@ spec_status spec_verify_chain_truncated(const spec_chain_args *a, const spec_tru
   if (!ws || !aligned(ws, 256) || ws_bytes < need) return SPEC_ERR_WORKSPACE;
   if (static_cast<long long>(a->B) * (2 * K + 1) > 0x7fffffffLL) return SPEC_ERR_SHAPE;
   ChainStochParams p;
-  int grid = 0, nv = 0, C = 0;
+  int grid = 0, C = 0;
   size_t smem = 0;
   {
-    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, smem, nv, C);
+    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, C, false, &smem);
     if (st != SPEC_OK) return st;
   }
   p.accepted_len = o->accepted_len;
@@ -391,7 +424,7 @@ spec_status spec_verify_chain_truncated(const spec_chain_args *a, const spec_tru
   p.top_p = t->top_p;
   p.trunc = p.trunc_area;
   report("truncated grid cluster", grid, C, 0, 0, 0, 0, 0);
-  return launch_chain_truncated(p, a->dtype == SPEC_BF16, grid, smem, C,
+  return launch_chain_truncated(p, a->dtype == SPEC_BF16, grid, C,
                                 static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? SPEC_OK
              : SPEC_ERR_CUDA;
@@ -416,19 +449,18 @@ spec_status spec_drift_residuals(const spec_chain_args *a, int32_t m, int32_t *s
   const size_t need = spec_verify_chain_workspace_size(a->B, a->K, a->V);
   if (!ws || !aligned(ws, 256) || ws_bytes < need) return SPEC_ERR_WORKSPACE;
   ChainStochParams p;
-  int grid = 0, nv = 0, C = 0;
+  int grid = 0, C = 0;
   size_t smem = 0;
   {
-    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, smem, nv, C);
+    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, C, false, &smem);
     if (st != SPEC_OK) return st;
   }
-  p.dyn = 0;  // the selection kernel does not re-arm the workspace header
   p.row_status = row_status;
   p.drift_m = m;
   p.drift_support = support;
   p.drift_residual = residual;
   report("drift grid m", grid, m, 0, 0, 0, 0, 0);
-  return launch_drift(p, a->dtype == SPEC_BF16, grid, smem, static_cast<cudaStream_t>(stream)) ==
+  return launch_drift(p, a->dtype == SPEC_BF16, grid, static_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? SPEC_OK
              : SPEC_ERR_CUDA;

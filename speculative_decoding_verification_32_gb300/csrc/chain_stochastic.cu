@@ -451,10 +451,10 @@ __global__ void __launch_bounds__(kSoftThreads + 32, 3) softmax_partials_kernel(
   const int hi_a = phase_split(0, pa, B, K, nt, g + 1, G);
   const int lo_b = pa * nt + phase_split(pa, npos, B, K, nt, g, G);
   const int hi_b = pa * nt + phase_split(pa, npos, B, K, nt, g + 1, G);
-  // With an armed workspace only phase A is split statically; the tiles of
-  // phase B are claimed in chunks as CTAs run out of work, so CTAs that
-  // stream faster take more of the tail.
-  const bool dyn = P.dyn != 0 && *reinterpret_cast<volatile const unsigned long long *>(P.magic) == kWsMagic;
+  // Only phase A is split statically; the tiles of phase B are claimed in
+  // chunks (through the counter the generation step clears) as CTAs run out
+  // of work, so CTAs that stream faster take more of the tail.
+  const bool dyn = P.stream_dyn != 0;
   const int dyn_from = pa * nt;
   const int na = hi_a - lo_a;
   const int my_tiles = dyn ? na : na + (hi_b - lo_b);  // statically assigned tiles
@@ -671,6 +671,169 @@ __global__ void __launch_bounds__(kSoftThreads + 32, 3) softmax_partials_kernel(
           ctl.arrived[slot] = 0;
           ctl.tflags[slot] = 0;
         }
+      }
+    }
+  }
+}
+
+// Item `it` of the stream, in stream order.  Phase A: the bonus positions
+// (j = K), then j = K-1 down to 2, each over b = 0..B-1.  Phase B: positions
+// 1 and 0 row by row, so rows complete one after another and their likely
+// stopping positions are the last data streamed.  A position is its target
+// row's nt slices, then (j < K) its draft row's.
+__device__ __forceinline__ void stream_item_of(long long it, int B, int K, int nt, int *b, int *j,
+                                               bool *draft, int *sl) {
+  const long long pn = nt, pp = 2LL * nt;  // items of a bonus / a drafted position
+  long long q;
+  if (K >= 2) {
+    const long long a0 = (long long)B * pn;
+    const long long a1 = a0 + (long long)B * (K - 2) * pp;
+    if (it < a0) {
+      *j = K;
+      *b = (int)(it / pn);
+      q = it - *b * pn;
+    } else if (it < a1) {
+      const long long r = it - a0;
+      const long long k = r / ((long long)B * pp);
+      *j = K - 1 - (int)k;
+      const long long r2 = r - k * B * pp;
+      *b = (int)(r2 / pp);
+      q = r2 - *b * pp;
+    } else {
+      const long long r = it - a1;
+      *b = (int)(r / (2 * pp));
+      const long long r2 = r - *b * 2 * pp;
+      *j = 1 - (int)(r2 / pp);
+      q = r2 % pp;
+    }
+  } else if (K == 1) {  // per row: position 1 (the bonus), then 0
+    const long long per = pn + pp;
+    *b = (int)(it / per);
+    const long long r2 = it - *b * per;
+    *j = r2 < pn ? 1 : 0;
+    q = r2 < pn ? r2 : r2 - pn;
+  } else {
+    *b = (int)(it / pn);
+    *j = 0;
+    q = it - *b * pn;
+  }
+  *draft = q >= nt;
+  *sl = (int)(*draft ? q - nt : q);
+}
+
+// The plain-load stream, used by the truncated and DRIFT entry points (whose
+// second kernels wait for the whole stream): a persistent grid of warps; warp
+// w takes items w, w + W, ... in stream order.  A warp reads its item (one
+// logit row's vocabulary slice) with plain 16-byte loads, kStreamU per lane
+// in flight, folds it into the slice's max logit and sum of exp2((x - m) s2)
+// (each lane against its own running max, then a butterfly across the warp)
+// and stamps one record; the item holding the draft token also stamps that
+// token's logit.  No shared memory, no barrier, no atomics.  Positions >= 2
+// carry an L2 evict-first hint; positions 0 and 1 do not.  Alone it streams
+// c3 in 30 us against the ring's 33, but ahead of the resolve kernel the step
+// measured 47-53 us against the ring's 43.5, so the plain verify keeps the
+// ring.
+template <bool BF16, bool VEC>
+__global__ void __launch_bounds__(kStreamThreads, 4) stream_partials_kernel(const __grid_constant__ ChainStochParams P) {
+  using F = Fmt<BF16>;
+  constexpr int EPV = F::EPV, ESZ = F::ESZ, U = kStreamU;
+  // let the next kernel be scheduled; it waits for this grid on the device
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // forced-timeout test: no record of this call appears, so every reader's
+  // bounded wait gives up
+  if (P.force_timeout) return;
+  const int lane = threadIdx.x & 31;
+  const long long GW = (long long)gridDim.x * (kStreamThreads / 32);
+  const int B = P.B, K = P.K, V = P.V, nt = P.nslices;
+  const long long total = (long long)B * nt * (2 * K + 1);
+  const uint32_t tag = *reinterpret_cast<volatile const uint32_t *>(P.gen);
+  const uint64_t pol_first = l2_policy_evict_first(), pol_keep = l2_policy_evict_normal();
+  for (long long it = (long long)blockIdx.x * (kStreamThreads / 32) + (threadIdx.x >> 5); it < total; it += GW) {
+    int b, j, sl;
+    bool draft;
+    stream_item_of(it, B, K, nt, &b, &j, &draft, &sl);
+    const int s0 = sl * P.slice, len = min(V - s0, P.slice);
+    const int prow = draft ? B * (K + 1) + b * K + j : b * (K + 1) + j;
+    const char *src = static_cast<const char *>(draft ? P.draft : P.target) +
+                      ((size_t)row_offset(P, prow) + s0) * ESZ;
+    const uint64_t pol = j <= 1 ? pol_keep : pol_first;
+    const int nvec = (len + EPV - 1) / EPV;
+    uint32_t w[U][4];
+    auto load_one = [&](uint32_t *x, int v) {
+      if constexpr (VEC) {
+        const uint4 r = ld_stream_u4(src + (size_t)v * 16, pol);
+        x[0] = r.x; x[1] = r.y; x[2] = r.z; x[3] = r.w;
+      } else {
+        F::load_vec(x, nullptr, src, false, v, len);
+      }
+    };
+    auto load_batch = [&](int v0) {
+      if (v0 + 32 * U <= nvec) {  // every lane's vectors are in the slice
+#pragma unroll
+        for (int u = 0; u < U; ++u) load_one(w[u], v0 + u * 32 + lane);
+      } else {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + u * 32 + lane;
+          if (v < nvec) load_one(w[u], v);
+          else w[u][0] = w[u][1] = w[u][2] = w[u][3] = F::NEG_INF_WORD;
+        }
+      }
+    };
+    load_batch(0);  // in flight before anything else waits on memory
+    float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
+    if (!(T > 0.f && T < kInf)) T = 1.0f;  // the resolve kernel flags the row
+    const float s2 = __fdiv_rn(kLog2e, T);
+    const int y = (j < K && P.tokens) ? __ldg(P.tokens + (size_t)b * K + j) : -1;
+    const float2 s2v = make_float2(s2, s2);
+    float m = -kInf, sacc = 0.f;
+    for (int v0 = 0;;) {
+      uint32_t pm = F::NEG_INF_WORD;
+      if constexpr (BF16) {
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          pm = bf16x2_max_nan(pm, bf16x2_max_nan(bf16x2_max_nan(w[u][0], w[u][1]), bf16x2_max_nan(w[u][2], w[u][3])));
+      }
+      float bm;
+      if constexpr (BF16) {
+        bm = fmax_nan(bf16_lo(pm), bf16_hi(pm));
+      } else {
+        bm = -kInf;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          bm = fmax_nan(bm, fmax_nan(fmax_nan(__uint_as_float(w[u][0]), __uint_as_float(w[u][1])),
+                                     fmax_nan(__uint_as_float(w[u][2]), __uint_as_float(w[u][3]))));
+      }
+      const float mn = fmax_nan(m, bm);
+      if (mn != -kInf) {
+        const float off = -__fmul_rn(mn, s2);
+        const float2 offv = make_float2(off, off);
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+#pragma unroll
+          for (int i = 0; i < EPV / 2; ++i) {
+            const float2 a = ffma2(F::pair(w[u], i), s2v, offv);
+            if (i & 1) acc1 = fadd2(acc1, make_float2(ex2(a.x), ex2(a.y)));
+            else acc0 = fadd2(acc0, make_float2(ex2(a.x), ex2(a.y)));
+          }
+        }
+        sacc = (m == -kInf ? 0.f : sacc * ex2(__fmul_rn(m - mn, s2))) + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
+        m = mn;
+      }
+      v0 += 32 * U;
+      if (v0 >= nvec) break;
+      load_batch(v0);
+    }
+    float M, S;
+    fold_max_sum(m, sacc, s2, &M, &S);
+    if (lane == 0) {
+      store_part(P.part + (size_t)prow * nt + sl, M, S, 0u, tag);
+      if (y >= s0 && y < s0 + len) {  // the draft token's logit
+        const char *g = src + (size_t)(y - s0) * ESZ;
+        const float l = BF16 ? __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short *>(g))) << 16)
+                             : __ldg(reinterpret_cast<const float *>(g));
+        st_relaxed_u64(P.ylog + prow, __float_as_uint(l) | (static_cast<unsigned long long>(tag) << 32));
       }
     }
   }
@@ -901,15 +1064,10 @@ __global__ void __launch_bounds__(kResolveThreads, 4) chain_resolve_kernel(const
                          static_cast<uint32_t>(lenp) * ESZ);
     }
   }
-  // The stream kernel releases the claim counter only when it completes:
-  // block 0 re-arms the workspace header after waiting for that, on its way
-  // out.
-  auto rearm_header = [&]() {
-    if (blockIdx.x == 0 && tid == 0) {
-      asm volatile("griddepcontrol.wait;" ::: "memory");
-      *P.claim = 0u;
-      *P.magic = kWsMagic;
-    }
+  // Block 0 waits for the stream kernel on its way out, so this grid never
+  // completes before the one it depends on.
+  auto join_stream = [&]() {
+    if (blockIdx.x == 0 && tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
   };
   // Rank 0 of the cluster polls the row's partial records until every one
   // carries this call's tag -- the stream kernel stamps them as it goes, so
@@ -952,7 +1110,7 @@ __global__ void __launch_bounds__(kResolveThreads, 4) chain_resolve_kernel(const
         P.row_status[b] = lowest_code(flags);
       }
     }
-    rearm_header();
+    join_stream();
     return;
   }
 
@@ -1178,7 +1336,7 @@ __global__ void __launch_bounds__(kResolveThreads, 4) chain_resolve_kernel(const
     }
   }
   cluster_wait();  // no CTA leaves while a peer may still read its mailbox
-  rearm_header();
+  join_stream();
 }
 
 // ============================================================ block selection
@@ -1961,24 +2119,32 @@ size_t resolve_smem(const ChainStochParams &p) {
   return static_cast<size_t>(2 * p.K + 1) * 16 + static_cast<size_t>(p.vpw / 32) * kResolveThreads * 4;
 }
 
-// Function attributes are set once per device (again only when more shared
-// memory is needed), so steady-state launches make no other driver calls and
-// can be captured into a CUDA graph.
+// The resolve kernel's attributes are set once per device, so steady-state
+// launches make no other driver calls and can be captured into a CUDA graph.
+// The ring stream kernel's shared-memory attribute, set once per device
+// (again only when more is needed).
 template <bool BF16, int NV, int S>
-cudaError_t prepare(size_t smem, int cluster) {
+cudaError_t prepare_ring(size_t smem) {
   static std::atomic<size_t> done_smem[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (done_smem[dev].load() >= smem) return cudaSuccess;
+  e = cudaFuncSetAttribute(softmax_partials_kernel<BF16, NV, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
+  if (e == cudaSuccess) done_smem[dev].store(smem);
+  return e;
+}
+
+template <bool BF16>
+cudaError_t prepare(int cluster) {
   static std::atomic<int> done_nonportable[kMaxDevices];
   static std::atomic<int> done_resolve[kMaxDevices];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (done_smem[dev].load() < smem) {
-    e = cudaFuncSetAttribute(softmax_partials_kernel<BF16, NV, S>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    done_smem[dev].store(smem);
-  }
   if (!done_resolve[dev].load()) {
     e = cudaFuncSetAttribute(chain_resolve_kernel<BF16>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
@@ -1994,53 +2160,22 @@ cudaError_t prepare(size_t smem, int cluster) {
   return cudaSuccess;
 }
 
+// Advances the workspace's generation word (the call's tag) and clears the
+// stream's claim counter: one thread, a plain launch ahead of the stream.
+__global__ void advance_generation_kernel(uint32_t *gen, uint32_t *claim) {
+  *gen += 1u;
+  *claim = 0u;
+}
+
+// The generation step, then the stream (plain launches).
 template <bool BF16>
-cudaError_t launch_resolve(const ChainStochParams &p, int cluster, cudaStream_t s);
-
-// Advances the workspace's generation word: the call's tag (one thread, a
-// plain launch ahead of the stream kernel).
-__global__ void advance_generation_kernel(uint32_t *gen) { *gen += 1u; }
-
-cudaError_t launch_advance_generation(uint32_t *gen, cudaStream_t s) {
-  advance_generation_kernel<<<1, 1, 0, s>>>(gen);
+cudaError_t launch_stream(const ChainStochParams &p, int grid, cudaStream_t s) {
+  advance_generation_kernel<<<1, 1, 0, s>>>(p.gen, p.claim);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (p.use_tma) stream_partials_kernel<BF16, true><<<grid, kStreamThreads, 0, s>>>(p);
+  else stream_partials_kernel<BF16, false><<<grid, kStreamThreads, 0, s>>>(p);
   return cudaGetLastError();
-}
-
-template <bool BF16, int NV, int S>
-cudaError_t launch_t(const ChainStochParams &p, int grid, size_t smem, int cluster,
-                     cudaStream_t s) {
-  cudaError_t e = prepare<BF16, NV, S>(smem, cluster);
-  if (e != cudaSuccess) return e;
-  e = launch_advance_generation(p.gen, s);
-  if (e != cudaSuccess) return e;
-  softmax_partials_kernel<BF16, NV, S><<<grid, kSoftThreads + 32, smem, s>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  return launch_resolve<BF16>(p, cluster, s);
-}
-
-template <bool BF16, int NV, int S>
-cudaError_t launch_truncated_t(const ChainStochParams &p, int grid, size_t smem, int cluster,
-                               cudaStream_t s) {
-  cudaError_t e = prepare<BF16, NV, S>(smem, cluster);
-  if (e != cudaSuccess) return e;
-  e = launch_advance_generation(p.gen, s);
-  if (e != cudaSuccess) return e;
-  softmax_partials_kernel<BF16, NV, S><<<grid, kSoftThreads + 32, smem, s>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.B * (p.K + 1) + p.B * p.K));
-  cfg.blockDim = dim3(kDriftThreads);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, trunc_kernel<BF16>, p);
-  if (e != cudaSuccess) return e;
-  return launch_resolve<BF16>(p, cluster, s);
 }
 
 // The resolve kernel: a cluster of `cluster` CTAs per row, a programmatic
@@ -2064,17 +2199,12 @@ cudaError_t launch_resolve(const ChainStochParams &p, int cluster, cudaStream_t 
   return cudaLaunchKernelEx(&cfg, chain_resolve_kernel<BF16>, p);
 }
 
-template <bool BF16, int S>
-cudaError_t launch_drift_t(const ChainStochParams &p, int grid, size_t smem, cudaStream_t s) {
-  cudaError_t e = prepare<BF16, 4, S>(smem, 1);
-  if (e != cudaSuccess) return e;
-  e = launch_advance_generation(p.gen, s);
-  if (e != cudaSuccess) return e;
-  softmax_partials_kernel<BF16, 4, S><<<grid, kSoftThreads + 32, smem, s>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+// A one-CTA-per-item kernel (grid gx x gy) launched as a programmatic
+// dependent of the stream.
+template <typename Kern>
+cudaError_t launch_dependent(Kern k, const ChainStochParams &p, dim3 grid, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.K), static_cast<unsigned>(p.B));
+  cfg.gridDim = grid;
   cfg.blockDim = dim3(kDriftThreads);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -2082,48 +2212,79 @@ cudaError_t launch_drift_t(const ChainStochParams &p, int grid, size_t smem, cud
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, drift_select_kernel<BF16>, p);
+  return cudaLaunchKernelEx(&cfg, k, p);
 }
 
-template <bool BF16, int NV, int S>
-cudaError_t blocks_t(size_t smem, int *blocks) {
-  cudaError_t e = prepare<BF16, NV, S>(smem, 1);
+// The plain verify: the generation step, the bulk-copy ring stream, then the
+// resolve kernel.
+template <bool BF16, int S>
+cudaError_t launch_t(const ChainStochParams &p, int grid, size_t smem, int cluster, cudaStream_t s) {
+  cudaError_t e = prepare<BF16>(cluster);
+  if (e == cudaSuccess) e = prepare_ring<BF16, kSoftVecs, S>(smem);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, softmax_partials_kernel<BF16, NV, S>,
+  advance_generation_kernel<<<1, 1, 0, s>>>(p.gen, p.claim);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  softmax_partials_kernel<BF16, kSoftVecs, S><<<grid, kSoftThreads + 32, smem, s>>>(p);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) e = launch_resolve<BF16>(p, cluster, s);
+  return e;
+}
+
+template <bool BF16, int S>
+cudaError_t ring_blocks_t(size_t smem, int *blocks) {
+  cudaError_t e = prepare_ring<BF16, kSoftVecs, S>(smem);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, softmax_partials_kernel<BF16, kSoftVecs, S>,
                                                        kSoftThreads + 32, smem);
+}
+
+template <bool BF16>
+cudaError_t launch_truncated_t(const ChainStochParams &p, int grid, int cluster, cudaStream_t s) {
+  cudaError_t e = prepare<BF16>(cluster);
+  if (e == cudaSuccess) e = launch_stream<BF16>(p, grid, s);
+  if (e == cudaSuccess)
+    e = launch_dependent(trunc_kernel<BF16>, p, dim3(static_cast<unsigned>(p.B * (p.K + 1) + p.B * p.K)), s);
+  if (e == cudaSuccess) e = launch_resolve<BF16>(p, cluster, s);
+  return e;
+}
+
+template <bool BF16>
+cudaError_t launch_drift_t(const ChainStochParams &p, int grid, cudaStream_t s) {
+  cudaError_t e = launch_stream<BF16>(p, grid, s);
+  if (e == cudaSuccess)
+    e = launch_dependent(drift_select_kernel<BF16>, p,
+                         dim3(static_cast<unsigned>(p.K), static_cast<unsigned>(p.B)), s);
+  return e;
 }
 
 }  // namespace
 
-cudaError_t launch_chain_stochastic(const ChainStochParams &p, bool bf16, int nv, int grid,
-                                    size_t smem, int cluster, cudaStream_t s) {
-  (void)nv;
+cudaError_t launch_chain_stochastic(const ChainStochParams &p, bool bf16, int grid, size_t smem,
+                                    int cluster, cudaStream_t s) {
   if (p.stages == 3)
-    return bf16 ? launch_t<true, 4, 3>(p, grid, smem, cluster, s) : launch_t<false, 4, 3>(p, grid, smem, cluster, s);
-  return bf16 ? launch_t<true, 4, 2>(p, grid, smem, cluster, s) : launch_t<false, 4, 2>(p, grid, smem, cluster, s);
+    return bf16 ? launch_t<true, 3>(p, grid, smem, cluster, s) : launch_t<false, 3>(p, grid, smem, cluster, s);
+  return bf16 ? launch_t<true, 2>(p, grid, smem, cluster, s) : launch_t<false, 2>(p, grid, smem, cluster, s);
 }
 
-cudaError_t launch_chain_truncated(const ChainStochParams &p, bool bf16, int grid, size_t smem,
-                                   int cluster, cudaStream_t s) {
-  if (p.stages == 3)
-    return bf16 ? launch_truncated_t<true, 4, 3>(p, grid, smem, cluster, s)
-                : launch_truncated_t<false, 4, 3>(p, grid, smem, cluster, s);
-  return bf16 ? launch_truncated_t<true, 4, 2>(p, grid, smem, cluster, s)
-              : launch_truncated_t<false, 4, 2>(p, grid, smem, cluster, s);
+cudaError_t ring_blocks_per_sm(bool bf16, int stages, size_t smem, int *blocks) {
+  if (stages == 3) return bf16 ? ring_blocks_t<true, 3>(smem, blocks) : ring_blocks_t<false, 3>(smem, blocks);
+  return bf16 ? ring_blocks_t<true, 2>(smem, blocks) : ring_blocks_t<false, 2>(smem, blocks);
 }
 
-cudaError_t launch_drift(const ChainStochParams &p, bool bf16, int grid, size_t smem,
-                         cudaStream_t s) {
-  if (p.stages == 3)
-    return bf16 ? launch_drift_t<true, 3>(p, grid, smem, s) : launch_drift_t<false, 3>(p, grid, smem, s);
-  return bf16 ? launch_drift_t<true, 2>(p, grid, smem, s) : launch_drift_t<false, 2>(p, grid, smem, s);
+cudaError_t launch_chain_truncated(const ChainStochParams &p, bool bf16, int grid, int cluster,
+                                   cudaStream_t s) {
+  return bf16 ? launch_truncated_t<true>(p, grid, cluster, s) : launch_truncated_t<false>(p, grid, cluster, s);
 }
 
-cudaError_t soft_partials_blocks_per_sm(bool bf16, int nv, size_t smem, int *blocks) {
-  (void)nv;
-  if (smem > 80 * 1024)
-    return bf16 ? blocks_t<true, 4, 3>(smem, blocks) : blocks_t<false, 4, 3>(smem, blocks);
-  return bf16 ? blocks_t<true, 4, 2>(smem, blocks) : blocks_t<false, 4, 2>(smem, blocks);
+cudaError_t launch_drift(const ChainStochParams &p, bool bf16, int grid, cudaStream_t s) {
+  return bf16 ? launch_drift_t<true>(p, grid, s) : launch_drift_t<false>(p, grid, s);
+}
+
+cudaError_t stream_blocks_per_sm(bool bf16, bool vec, int *blocks) {
+  const void *k = bf16 ? (vec ? (const void *)stream_partials_kernel<true, true> : (const void *)stream_partials_kernel<true, false>)
+                       : (vec ? (const void *)stream_partials_kernel<false, true> : (const void *)stream_partials_kernel<false, false>);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, k, kStreamThreads, 0);
 }
 
 }  // namespace sv

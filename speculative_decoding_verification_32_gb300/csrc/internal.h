@@ -56,29 +56,24 @@ struct ChainStochParams {
   unsigned long long *ylog;  // [B*(K+1) + B*K] workspace: the draft token's logit per logit
                             // row, as (logit bits | tag << 32)
   int B, K, V;
-  int slice;       // elements per tile of the partial kernel
-  int nslices;     // tiles per logit row
-  int use_tma;     // rows are 16-byte aligned: bulk copies; else direct loads
-  int stages;      // bulk-copy pipeline depth of the partial kernel
-  int buf_bytes;   // bytes of one stage buffer
+  int slice;       // elements per stream item (one logit row's vocabulary slice)
+  int nslices;     // stream items per logit row
+  int use_tma;     // rows are 16-byte aligned: bulk copies / 16-byte loads; else element loads
+  int stages;      // ring stream kernel: bulk-copy pipeline depth
+  int buf_bytes;   // ring stream kernel: bytes of one stage buffer
+  int dyn_chunk;   // ring stream kernel: tiles per claim of its last phase
   int L;           // resolve kernel: vocabulary slice per cluster CTA
   int vpw;         // resolve kernel: 16-byte vectors per warp (multiple of 32)
   uint64_t wait_limit_ns;
   int force_timeout;
-  // Dynamic tail of the partial kernel.  The workspace ends with a header
-  // {claim counter, generation, magic}.  When the header holds kWsMagic the
-  // tiles of the last phase are claimed in chunks of dyn_chunk through the
-  // counter (the resolve kernel re-arms the header afterwards); otherwise
-  // every tile is assigned statically.  The generation word is advanced
-  // before every call and stamped on every record as its tag, which the
-  // readers check, so a record this call did not write is never used --
-  // whatever shapes earlier calls on the workspace had (their records sit at
-  // other offsets, but all carry older tags).
-  uint32_t *claim;
-  unsigned long long *magic;
+  // The workspace ends with a 16-byte header {claim counter, generation, -}.
+  // The generation is advanced before every call and stamped on every record
+  // as its tag, which the readers check, so a record this call did not write
+  // is never used -- whatever shapes earlier calls on the workspace had
+  // (their records sit at other offsets, but all carry older tags).
   uint32_t *gen;       // the workspace's generation word (the call's tag)
-  int dyn;             // 0: static assignment only
-  int dyn_chunk;       // tiles per claim
+  uint32_t *claim;     // the stream's claim counter (cleared before every call)
+  int stream_dyn;      // ring stream: 0 = every tile statically assigned
   // top-k / top-p truncation (spec_verify_chain_truncated): per-row
   // parameters (NULL: off) and one record per logit row
   const int32_t *top_k;
@@ -91,7 +86,6 @@ struct ChainStochParams {
   float *drift_residual;    // [B, K, m]
 };
 
-constexpr unsigned long long kWsMagic = 0x5EC7E21F1CA7E5EDull;  // armed workspace header
 // Workspace tail: the header (16 bytes), with room for its 16-byte alignment
 // below an arbitrary end.
 inline size_t ws_tail_bytes(long long) { return 256; }
@@ -128,20 +122,24 @@ struct RollbackParams {
   int32_t *num_emitted_out;
 };
 
-// Threads per CTA: greedy partial kernel, softmax partial kernel (consumer
-// warps; one producer warp comes on top), resolve kernel.
+// Threads per CTA: greedy partial kernel, the two stochastic stream kernels
+// (the bulk-copy ring's consumer warps, one producer warp on top; the plain-
+// load stream), resolve kernel.
 constexpr int kThreads = 512;
 constexpr int kSoftThreads = 256;
+constexpr int kStreamThreads = 256;
 constexpr int kResolveThreads = 256;
-// 16-byte vectors per consumer thread per tensor in a softmax-partial tile:
-// a tile is kSoftThreads * kSoftVecs vectors of the target row and as many of
-// the draft row (kSoftVecs = 4: 8192 bf16 or 4096 fp32 logits per tensor).
+// Ring stream: 16-byte vectors per consumer thread per tensor in a tile (a
+// tile is kSoftThreads * kSoftVecs vectors of the target row and as many of
+// the draft row: 8192 bf16 or 4096 fp32 logits per tensor) and ring depth.
 constexpr int kSoftVecs = 4;
-// Depth of the softmax-partial kernel's bulk-copy ring.
 constexpr int kSoftStages = 2;
-// Smallest tile (elements) any build of the partial kernel uses: sizes the
-// workspace.
-constexpr int kSoftMinSlice = kSoftThreads * 4 * 4;
+// Stochastic stream: 16-byte vectors in flight per lane, and logits per item
+// (one logit row's vocabulary slice: 8 KB in bf16, 16 KB in fp32).
+constexpr int kStreamU = 8;
+constexpr int kStreamSlice = 4096;
+// The slice sizes the workspace's record area.
+constexpr int kSoftMinSlice = kStreamSlice;
 // Largest rounds of 32 vectors per warp in the resolve kernel.
 constexpr int kResolveMaxRounds = 16;
 // Elements per greedy work item.
@@ -154,15 +152,17 @@ constexpr int kDriftMaxSupport = 64;  // largest support size m
 
 // Host launchers (defined next to their kernels); each returns the CUDA error
 // of its launches.
-cudaError_t launch_chain_stochastic(const ChainStochParams &p, bool bf16, int nv, int grid,
-                                    size_t smem, int cluster, cudaStream_t s);
-// Stream kernel, truncation thresholds, then the resolve kernel.
-cudaError_t launch_chain_truncated(const ChainStochParams &p, bool bf16, int grid, size_t smem,
-                                   int cluster, cudaStream_t s);
-// Stream kernel then the DRIFT selection kernel (one CTA per drafted position).
-cudaError_t launch_drift(const ChainStochParams &p, bool bf16, int grid, size_t smem,
-                         cudaStream_t s);
-cudaError_t soft_partials_blocks_per_sm(bool bf16, int nv, size_t smem, int *blocks);
+// Generation step, ring stream kernel, then the resolve kernel.
+cudaError_t launch_chain_stochastic(const ChainStochParams &p, bool bf16, int grid, size_t smem,
+                                    int cluster, cudaStream_t s);
+cudaError_t ring_blocks_per_sm(bool bf16, int stages, size_t smem, int *blocks);
+// Generation step, stream kernel, truncation thresholds, then the resolve kernel.
+cudaError_t launch_chain_truncated(const ChainStochParams &p, bool bf16, int grid, int cluster,
+                                   cudaStream_t s);
+// Generation step, stream kernel, then the DRIFT selection kernel (one CTA per
+// drafted position).
+cudaError_t launch_drift(const ChainStochParams &p, bool bf16, int grid, cudaStream_t s);
+cudaError_t stream_blocks_per_sm(bool bf16, bool vec, int *blocks);
 cudaError_t launch_greedy(const GreedyParams &p, bool bf16, int grid, cudaStream_t s);
 cudaError_t greedy_max_blocks_per_sm(bool bf16, bool vec, int *blocks);
 cudaError_t launch_rollback(const RollbackParams &p, cudaStream_t s);
