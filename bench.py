@@ -32,10 +32,10 @@ WORKLOAD = "c3"
 METRIC = "verify steps/s and achieved HBM GB/s (B=64,K=5,V=128256 bf16) vs 8 TB/s"
 UNIT = "verify steps/s"
 L2_BYTES = 129 * 1024 * 1024
-# ncu dram__bytes_read.sum + dram__bytes_write.sum of one stream_partials_kernel
-# launch on this workload (profiles/stream_partials_chain_c3.md): 180,649,728
-# read + 3,448,576 written; reset to None whenever that kernel changes
-TRAFFIC = None
+# ncu dram__bytes_read.sum + dram__bytes_write.sum of one softmax_partials_kernel
+# launch on this workload (profiles/softmax_partials_chain_c3.md): 180,649,216
+# read + 3,728,384 written; reset to None whenever that kernel changes
+TRAFFIC = 180649216 + 3728384
 # the same for one greedy_kernel launch on the tree workload
 # (profiles/greedy_tree_c4.md): 583,470,336 read + 3,753,984 written
 TREE_TRAFFIC = 583470336 + 3753984
@@ -360,7 +360,7 @@ def run_ours(args):
         "achieved_hbm_gbs": gbs,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                      "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
-                     "kernel": "stream_partials_kernel<bf16> (dominant) + "
+                     "kernel": "softmax_partials_kernel<bf16,4,2> (dominant) + "
                                "chain_resolve_kernel<bf16> (PDL); achieved = algorithmic "
                                "bytes / whole-step time, a lower bound for the stream kernel",
                      "algorithmic_bytes_per_launch": step_bytes, "traffic": TRAFFIC},
