@@ -39,20 +39,17 @@
  *  - Workspace: `ws` is caller-owned device memory of at least the size the
  *    matching *_workspace_size() returns, 256-byte aligned.  Its contents
  *    need no initialisation.  The stochastic chain calls keep a small header
- *    in the last 16 bytes of the `ws_bytes` they are given: a work counter
- *    and a generation count, advanced before every call and stamped on every
- *    record the call writes, so nothing an earlier call left behind is ever
- *    read, whatever its shapes.  On the first call with a given workspace
- *    the stream kernel assigns every tile statically; from the second call
- *    on it hands out the last tiles dynamically, which balances the stream
- *    (results are identical either way).  Keep passing the same `ws_bytes`
- *    for the same buffer to keep that benefit.  Calls on one stream may
- *    share a workspace; calls that may overlap in time (different streams)
- *    need separate workspaces.
+ *    in the last 16 bytes of the `ws_bytes` they are given: a work counter,
+ *    cleared before every call, and a generation count, advanced before
+ *    every call and stamped on every record the call writes, so nothing an
+ *    earlier call left behind is ever read, whatever its shapes.  Keep
+ *    passing the same `ws_bytes` for the same buffer.  Calls on one stream
+ *    may share a workspace; calls that may overlap in time (different
+ *    streams) need separate workspaces.
  *  - Each verify call enqueues a streaming kernel and a small per-row kernel
  *    that starts early and waits for it on the device (programmatic dependent
  *    launch); the stochastic calls first enqueue a one-thread kernel that
- *    advances the workspace's generation count.
+ *    advances the workspace's generation count and clears its work counter.
  *  - Logits are bf16 (SPEC_BF16) or fp32 (SPEC_F32).  Rows whose byte
  *    length is a multiple of 16 with a 16-byte aligned base take the bulk-
  *    copy (TMA) path; any other V still works, more slowly.
