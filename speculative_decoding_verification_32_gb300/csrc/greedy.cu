@@ -18,8 +18,6 @@
 // chain or the tree in one warp.
 #include <cuda_bf16.h>
 
-#include <atomic>
-
 #include "common.cuh"
 #include "internal.h"
 

@@ -122,10 +122,9 @@ struct RollbackParams {
   int32_t *num_emitted_out;
 };
 
-// Threads per CTA: greedy partial kernel, the two stochastic stream kernels
-// (the bulk-copy ring's consumer warps, one producer warp on top; the plain-
-// load stream), resolve kernel.
-constexpr int kThreads = 512;
+// Threads per CTA: the two stochastic stream kernels (the bulk-copy ring's
+// consumer warps, one producer warp on top; the plain-load stream), resolve
+// kernel.
 constexpr int kSoftThreads = 256;
 constexpr int kStreamThreads = 256;
 constexpr int kResolveThreads = 256;
