@@ -273,10 +273,11 @@ spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes
   C = 1;
   while (C < 16 && rounds(C) > kResolveMaxRounds) C *= 2;
   if (rounds(C) > kResolveMaxRounds) return SPEC_ERR_SHAPE;
+  const int c_min = C;
   while (C < 8 && ceil_div(a->V, 2 * C) >= 2048) C *= 2;  // spread each row's work
   if (const char *ov = std::getenv("SPECVERIFY_CLUSTER")) {  // tuning override
     const int c = std::atoi(ov);
-    if (c >= C && c <= 16 && (c & (c - 1)) == 0) C = c;
+    if (c >= c_min && c <= 16 && (c & (c - 1)) == 0) C = c;
   }
   p.L = static_cast<int>(align_up(static_cast<size_t>(ceil_div(a->V, C)), static_cast<size_t>(epv)));
   p.vpw = 32 * rounds(C);
