@@ -54,7 +54,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="chain",
-                    choices=["chain", "kv_compact", "policy", "drift", "truncated", "tree"],
+                    choices=["chain", "kv_compact", "policy", "drift", "truncated", "tree",
+                             "chain_c5", "greedy"],
                     help="chain: the headline verify step (default); kv_compact / policy: "
                          "the post-verification entry points")
     ap.add_argument("--sets", type=int, default=0,
@@ -490,6 +491,57 @@ def run_next(args):
                              "kernel": "stream_partials + trunc + chain_resolve",
                              "algorithmic_bytes_per_launch": step_bytes, "traffic": None},
                 "gpu_launches": 4 * n, "clocks": clocks}
+    elif args.workload in ("chain_c5", "greedy"):
+        # chain_c5: the stochastic step at scale (B=256, K=8, per-row
+        # temperatures, 10% of each draft row masked); greedy: argmax match with
+        # the margin rule on the headline shape, target logits only
+        greedy = args.workload == "greedy"
+        inp = S.make("c3" if greedy else "c5", greedy=greedy)
+        B, K = inp["draft_tokens"].shape
+        V = inp["target"].shape[-1]
+        step_bytes = inp["target"].nbytes + (0 if greedy else inp["draft"].nbytes)
+        n_sets = max(2, -(-3 * L2_BYTES // step_bytes) + 1)
+        tgt0 = to_cuda(inp["target"], dev)
+        drf0 = None if greedy else to_cuda(inp["draft"], dev)
+        sets = [(tgt0, drf0)] + [(tgt0.clone(), None if greedy else drf0.clone())
+                                 for _ in range(n_sets - 1)]
+        small = {k: to_cuda(inp[k], dev) for k in ("draft_tokens", "temperature", "u_accept",
+                                                    "u_sample") if inp.get(k) is not None}
+        outs = [dict(accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
+                     out_tokens=torch.empty(B, K + 1, dtype=torch.int32, device=dev),
+                     num_emitted=torch.empty(B, dtype=torch.int32, device=dev),
+                     row_status=torch.empty(B, dtype=torch.int32, device=dev))
+                for _ in range(n_sets)]
+
+        def step(i):
+            if greedy:
+                sv.spec_verify_chain(sets[i][0], None, small["draft_tokens"],
+                                     small["temperature"], mode="greedy", margin_kappa=0.3,
+                                     out=outs[i], stream=stream)
+            else:
+                sv.spec_verify_chain(sets[i][0], sets[i][1], small["draft_tokens"],
+                                     small["temperature"], small["u_accept"], small["u_sample"],
+                                     out=outs[i], stream=stream)
+        sampler.start()
+        time.sleep(0.3)
+        ms, n, w = _time_graph(torch, stream, step, n_sets, steps, warmup)
+        clocks = sampler.stop()
+        gbs = step_bytes / (ms / 1e3) / 1e9
+        desc = (f"chain B={B} K={K} V={V} bf16, greedy argmax match, T=0.7, kappa=0.3" if greedy else
+                f"chain verify, stochastic at scale: B={B} K={K} V={V} bf16, per-row T in "
+                "[0.3, 1.2], 10% of each draft row masked")
+        line = {"metric": ("greedy chain verify steps/s (margin rule)" if greedy else
+                           "verify steps/s at scale (B=256, K=8)"),
+                "workload": args.workload, "value": 1e3 / ms, "unit": "verify steps/s",
+                "n_gpus": 1, "steps": n, "warmup": w, "ms_per_step": ms,
+                "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": desc, "l2": f"{n_sets} rotating input sets > L2"},
+                "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                             "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
+                             "kernel": ("greedy_kernel + greedy_walk_kernel" if greedy else
+                                        "softmax_partials_kernel + chain_resolve_kernel"),
+                             "algorithmic_bytes_per_launch": step_bytes, "traffic": None},
+                "gpu_launches": (2 if greedy else KERNELS_PER_STEP) * n, "clocks": clocks}
     elif args.workload == "tree":
         # greedy tree verification with the margin rule on the tree workload
         inp = S.make("c4")
