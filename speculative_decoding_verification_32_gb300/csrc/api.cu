@@ -274,7 +274,10 @@ spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes
   while (C < 16 && rounds(C) > kResolveMaxRounds) C *= 2;
   if (rounds(C) > kResolveMaxRounds) return SPEC_ERR_SHAPE;
   const int c_min = C;
-  while (C < 8 && ceil_div(a->V, 2 * C) >= 2048) C *= 2;  // spread each row's work
+  // spread each row's work over up to 8 CTAs while the whole grid stays
+  // within one wave of resolve CTAs (c3: 8; B = 256: the minimum, 4)
+  const long long wave = static_cast<long long>(di.sms) * kResolveBlocksPerSm;
+  while (C < 8 && ceil_div(a->V, 2 * C) >= 2048 && static_cast<long long>(a->B) * 2 * C <= wave) C *= 2;
   if (const char *ov = std::getenv("SPECVERIFY_CLUSTER")) {  // tuning override
     const int c = std::atoi(ov);
     if (c >= c_min && c <= 16 && (c & (c - 1)) == 0) C = c;

@@ -1036,7 +1036,7 @@ __device__ void decide_row(const ChainStochParams &P, int b, float s2, uint32_t 
 }
 
 template <bool BF16>
-__global__ void __launch_bounds__(kResolveThreads, 4) chain_resolve_kernel(const __grid_constant__ ChainStochParams P) {
+__global__ void __launch_bounds__(kResolveThreads, kResolveBlocksPerSm) chain_resolve_kernel(const __grid_constant__ ChainStochParams P) {
   using F = Fmt<BF16>;
   constexpr int NT = kResolveThreads, NW = NT / 32, EPV = F::EPV, ESZ = F::ESZ;
   __shared__ ResolveCtrl ctl;

@@ -141,6 +141,9 @@ constexpr int kStreamSlice = 4096;
 constexpr int kSoftMinSlice = kStreamSlice;
 // Largest rounds of 32 vectors per warp in the resolve kernel.
 constexpr int kResolveMaxRounds = 16;
+// Resolve CTAs one SM holds (the kernel's launch bound): the cluster split
+// keeps B x C within one wave of them where the rounds allow.
+constexpr int kResolveBlocksPerSm = 4;
 // Elements per greedy work item.
 constexpr int kGreedySlice = 16384;  // largest slice (elements)
 constexpr int kGreedyThreads = 256;  // streaming greedy kernel block
