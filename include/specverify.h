@@ -282,8 +282,9 @@ spec_status spec_rollback_lengths(int32_t B, int32_t max_emit, const int32_t *kv
  * both NULL is spec_verify_chain.  The top-p boundary is a floating-point
  * decision taken in fp32 (the band rule covers rows whose cumulative mass
  * lands within ~1e-5 of top_p).  Same workspace as spec_verify_chain.
- * Three kernels: the stream, one threshold search per truncated logit row,
- * the per-row resolve.
+ * After the one-thread generation step, two kernels: one CTA per logit row,
+ * which forms the row's softmax statistics and, for a truncated row, its
+ * thresholds in the same pass over the logits; then the per-row resolve.
  */
 typedef struct {
   const int32_t *top_k;  /* [B] device, or NULL */

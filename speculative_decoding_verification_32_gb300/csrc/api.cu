@@ -178,11 +178,17 @@ spec_status run_greedy(GreedyParams &p, bool bf16, int esz, void *ws, cudaStream
   return SPEC_OK;
 }
 
+// How the first kernel of a stochastic call reads the logits: the bulk-copy
+// ring (plain verify), the plain-load stream (DRIFT), or one CTA per whole
+// logit row (truncated verify: one record per row).
+enum class StreamKind { kRing, kPlain, kWholeRow };
+
 // Parameters and launch shapes of the stochastic stream kernel and of the
 // resolve kernel's cluster split, from the arguments and the workspace;
 // output pointers are left for the caller.
 spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes, ChainStochParams &p,
-                             int &grid, int &C, bool ring, size_t *smem) {
+                             int &grid, int &C, StreamKind kind, size_t *smem) {
+  const bool ring = kind == StreamKind::kRing;
   const int K = a->K;
   const int esz = a->dtype == SPEC_BF16 ? 2 : 4;
   const bool bf16 = a->dtype == SPEC_BF16;
@@ -229,6 +235,8 @@ spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes
     }
     p.buf_bytes = 2 * p.slice * esz;  // target tile + draft tile
     *smem = static_cast<size_t>(p.stages) * p.buf_bytes + kRingCtrlBytes;
+  } else if (kind == StreamKind::kWholeRow) {
+    p.slice = a->V;  // the truncation kernel's CTA reads its whole row
   } else {
     // the plain-load stream: one item per (logit row, 4096-logit slice);
     // SPECVERIFY_STREAM_SLICE (2048..16384, a multiple of 1024) overrides it
@@ -252,6 +260,8 @@ spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes
     if (ring_blocks(dev, bf16, p.stages, *smem, &per_sm) != cudaSuccess || per_sm < 1) return SPEC_ERR_CUDA;
     const long long tiles = static_cast<long long>(a->B) * (K + 1) * p.nslices;
     grid = static_cast<int>(std::min<long long>(tiles, static_cast<long long>(di.sms) * per_sm));
+  } else if (kind == StreamKind::kWholeRow) {
+    grid = static_cast<int>(rows_all);
   } else {
     if (soft_blocks(dev, bf16, p.use_tma != 0, &per_sm) != cudaSuccess || per_sm < 1) return SPEC_ERR_CUDA;
     const long long items = rows_all * p.nslices;
@@ -365,7 +375,7 @@ spec_status spec_verify_chain(const spec_chain_args *a, const spec_chain_out *o,
   int grid = 0, C = 0;
   size_t smem = 0;
   {
-    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, C, true, &smem);
+    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, C, StreamKind::kRing, &smem);
     if (st != SPEC_OK) return st;
   }
   p.accepted_len = o->accepted_len;
@@ -414,7 +424,7 @@ spec_status spec_verify_chain_truncated(const spec_chain_args *a, const spec_tru
   int grid = 0, C = 0;
   size_t smem = 0;
   {
-    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, C, false, &smem);
+    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, C, StreamKind::kWholeRow, &smem);
     if (st != SPEC_OK) return st;
   }
   p.accepted_len = o->accepted_len;
@@ -456,7 +466,7 @@ spec_status spec_drift_residuals(const spec_chain_args *a, int32_t m, int32_t *s
   int grid = 0, C = 0;
   size_t smem = 0;
   {
-    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, C, false, &smem);
+    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, C, StreamKind::kPlain, &smem);
     if (st != SPEC_OK) return st;
   }
   p.row_status = row_status;

@@ -721,8 +721,8 @@ __device__ __forceinline__ void stream_item_of(long long it, int B, int K, int n
   *sl = (int)(*draft ? q - nt : q);
 }
 
-// The plain-load stream, used by the truncated and DRIFT entry points (whose
-// second kernels wait for the whole stream): a persistent grid of warps; warp
+// The plain-load stream, used by the DRIFT entry point (whose second kernel
+// waits for the whole stream): a persistent grid of warps; warp
 // w takes items w, w + W, ... in stream order.  A warp reads its item (one
 // logit row's vocabulary slice) with plain 16-byte loads, kStreamU per lane
 // in flight, folds it into the slice's max logit and sum of exp2((x - m) s2)
@@ -1792,6 +1792,7 @@ struct alignas(16) TruncCtrl {
   float fred[kDriftWarps];
   int ired[kDriftWarps];
   int chist[256];
+  float wm[kDriftWarps];
   int n_cand, digit, above, pos;
   float M, S;
   uint32_t flags;
@@ -1805,52 +1806,23 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
   __shared__ TruncCtrl ctl;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = P.K, V = P.V, npos = K + 1;
-  const int row = blockIdx.x;  // partial-row numbering: targets, then drafts
+  const int row = blockIdx.x;  // logit rows: targets b*(K+1)+j, then drafts B*(K+1)+b*K+j
   const bool is_target = row < P.B * npos;
   const int b = is_target ? row / npos : (row - P.B * npos) / max(K, 1);
+  const int j = is_target ? row - b * npos : row - P.B * npos - b * K;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // Every CTA waits for the stream kernel before it leaves, even when its
-  // row is not truncated: the resolve kernel waits only for this grid, so
-  // this grid must not complete before the stream kernel has.
+  // the generation step has advanced this call's tag
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // forced-timeout test: no record of this call appears, so the resolve
+  // kernel's bounded wait gives up
+  if (P.force_timeout) return;
   int tk;
   float tp;
-  if (!trunc_active(P, b, V, &tk, &tp)) return;
-  const float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
-  const float s2 = (T > 0.f && T < kInf) ? __fdiv_rn(kLog2e, T) : 1.f;
+  const bool active = trunc_active(P, b, V, &tk, &tp);
+  float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
+  if (!(T > 0.f && T < kInf)) T = 1.0f;  // the resolve kernel flags the row
+  const float s2 = __fdiv_rn(kLog2e, T);
   const uint32_t tag = *reinterpret_cast<volatile const uint32_t *>(P.gen);
-  // ---- this row's max and sum (warp 0 folds its partial records)
-  const int nt = P.nslices;
-  if (warp == 0) {
-    float m = -kInf, sacc = 0.f;
-    uint32_t f = 0;
-    for (int t = lane; t < nt; t += 32) {
-      float qm, qs;
-      uint32_t qf;
-      if (!load_part(P.part + (size_t)row * nt + t, tag, &qm, &qs, &qf)) f |= F_TIMEOUT;
-      f |= qf;
-      const float mn = fmax_nan(m, qm);
-      sacc = (m == -kInf ? 0.f : sacc * ex2(__fmul_rn(m - mn, s2))) +
-             (qm == -kInf ? 0.f : qs * ex2(__fmul_rn(qm - mn, s2)));
-      m = mn;
-    }
-    float Mw, Sw;
-    fold_max_sum(m, sacc, s2, &Mw, &Sw);
-    f = __reduce_or_sync(FULL_MASK, f);
-    if (lane == 0) {
-      if (Mw != Mw || Mw == kInf || Mw == -kInf) f |= F_NONFINITE;
-      ctl.M = Mw;
-      ctl.S = Sw;
-      ctl.flags = f;
-    }
-  }
-  __syncthreads();
-  TruncRec *rec = P.trunc + row;
-  if (ctl.flags) {  // the resolve kernel flags this row from its own fold
-    if (tid == 0) *rec = TruncRec{0u, 0.f, 1u, 0u};
-    return;
-  }
-  const float nM = -__fmul_rn(ctl.M, s2);
   const char *src = static_cast<const char *>(is_target ? P.target : P.draft) + (size_t)row_offset(P, row) * ESZ;
   const bool aligned = P.use_tma != 0;
   const int nvec = (V + EPV - 1) / EPV;
@@ -1858,10 +1830,15 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
     if constexpr (BF16) return __ldg(reinterpret_cast<const unsigned short *>(src) + i);
     else return __ldg(reinterpret_cast<const unsigned int *>(src) + i);
   };
-  auto mass_of = [&](uint32_t bits) {  // exp2((l - M) s2) of one element
-    const float l = BF16 ? __uint_as_float(bits << 16) : __uint_as_float(bits);
-    return l == -kInf ? 0.f : ex2(__fmaf_rn(l, s2, nM));
-  };
+  // the draft token's logit, stamped like the records
+  if (tid == 0 && j < K && P.tokens) {
+    const int y = __ldg(P.tokens + (size_t)b * K + j);
+    if (y >= 0 && y < V) {
+      const uint32_t bits = bits_at(y);
+      const float l = BF16 ? __uint_as_float(bits << 16) : __uint_as_float(bits);
+      st_relaxed_u64(P.ylog + row, __float_as_uint(l) | (static_cast<unsigned long long>(tag) << 32));
+    }
+  }
   // block sums in a fixed order
   auto block_sum_i = [&](int v) {
     v = __reduce_add_sync(FULL_MASK, v);
@@ -1886,10 +1863,12 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
   // key of every kDriftSample-th element
   constexpr int kNS = (SPEC_MAX_V + kDriftSample * kDriftThreads - 1) / (kDriftSample * kDriftThreads);
   uint32_t smp[kNS];  // this thread's samples, loaded once
+  if (active) {
 #pragma unroll
-  for (int q = 0; q < kNS; ++q) {
-    const int i = (tid + q * kDriftThreads) * kDriftSample;
-    smp[q] = i < V ? order_key<BF16>(bits_at(i)) : 0u;
+    for (int q = 0; q < kNS; ++q) {
+      const int i = (tid + q * kDriftThreads) * kDriftSample;
+      smp[q] = i < V ? order_key<BF16>(bits_at(i)) : 0u;
+    }
   }
   const int n_samples = (V + kDriftSample - 1) / kDriftSample;
   auto samples = [&](auto f) {
@@ -1903,31 +1882,67 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
     return block_kth_largest<KEYBITS, kDriftThreads>(samples, r, ctl.chist, &ctl.digit, &ctl.above,
                                                     na, ne);
   };
-  // ---- candidates: every key >= tau, with its mass
-  auto collect = [&](uint32_t tau) {
+  // ---- one pass over the row.  With `stats` it forms the row's max and sum
+  // of exp2((l - m) s2), each thread against its own running max; with
+  // `cands` it lists every key >= tau (a lane looks at its elements only when
+  // its vector's maximum reaches tau, and appends them one by one: they are
+  // sorted later).  Returns the candidate count.
+  float m = -kInf, sacc = 0.f;
+  auto pass = [&](bool stats, bool cands, uint32_t tau) {
     if (tid == 0) ctl.n_cand = 0;
     const float tau_f = key_value<BF16>(tau);
+    const float2 s2v = make_float2(s2, s2);
     __syncthreads();
     constexpr int U = 4;
     for (int v0 = tid; v0 < nvec; v0 += U * kDriftThreads) {
       uint32_t w[U][4];
 #pragma unroll
       for (int u = 0; u < U; ++u) F::load_vec(w[u], nullptr, src, aligned, v0 + u * kDriftThreads, V);
+      if (stats) {
+        float bm;
+        if constexpr (BF16) {
+          uint32_t pm = F::NEG_INF_WORD;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        // a lane looks at its elements only when its vector's maximum
-        // reaches tau, and appends them one by one (they are sorted later)
-        if (!vec_may_reach<BF16>(w[u], tau_f)) continue;
+          for (int u = 0; u < U; ++u)
+            pm = bf16x2_max_nan(pm, bf16x2_max_nan(bf16x2_max_nan(w[u][0], w[u][1]), bf16x2_max_nan(w[u][2], w[u][3])));
+          bm = fmax_nan(bf16_lo(pm), bf16_hi(pm));
+        } else {
+          bm = -kInf;
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          const int idx = (v0 + u * kDriftThreads) * EPV + e;
-          const uint32_t bits = elem_bits<BF16>(w[u], e);
-          const uint32_t k = order_key<BF16>(bits);
-          if (k >= tau && idx < V) {
-            const int slot = atomicAdd(&ctl.n_cand, 1);
-            if (slot < kDriftCand) {
-              ctl.ck[slot] = (static_cast<unsigned long long>(k) << 32) | (~static_cast<uint32_t>(idx));
-              ctl.e[slot] = mass_of(bits);
+          for (int u = 0; u < U; ++u)
+            bm = fmax_nan(bm, fmax_nan(fmax_nan(__uint_as_float(w[u][0]), __uint_as_float(w[u][1])),
+                                       fmax_nan(__uint_as_float(w[u][2]), __uint_as_float(w[u][3]))));
+        }
+        const float mn = fmax_nan(m, bm);
+        if (mn != -kInf) {
+          const float off = -__fmul_rn(mn, s2);
+          const float2 offv = make_float2(off, off);
+          float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+#pragma unroll
+            for (int i = 0; i < EPV / 2; ++i) {
+              const float2 a = ffma2(F::pair(w[u], i), s2v, offv);
+              if (i & 1) acc1 = fadd2(acc1, make_float2(ex2(a.x), ex2(a.y)));
+              else acc0 = fadd2(acc0, make_float2(ex2(a.x), ex2(a.y)));
+            }
+          }
+          sacc = (m == -kInf ? 0.f : sacc * ex2(__fmul_rn(m - mn, s2))) + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
+          m = mn;
+        }
+      }
+      if (cands) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          if (!vec_may_reach<BF16>(w[u], tau_f)) continue;
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) {
+            const int idx = (v0 + u * kDriftThreads) * EPV + e;
+            const uint32_t k = order_key<BF16>(elem_bits<BF16>(w[u], e));
+            if (k >= tau && idx < V) {
+              const int slot = atomicAdd(&ctl.n_cand, 1);
+              if (slot < kDriftCand)
+                ctl.ck[slot] = (static_cast<unsigned long long>(k) << 32) | (~static_cast<uint32_t>(idx));
             }
           }
         }
@@ -1935,6 +1950,51 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
     }
     __syncthreads();
     return ctl.n_cand;
+  };
+  int r = tk > 0 ? max(16, (2 * tk) / kDriftSample + 2) : 16;
+  uint32_t tau = active ? sample_tau(r) : 0u;
+  int nc = pass(true, active, tau);
+  // ---- the row's max and sum: warps, then warp 0 in a fixed order
+  {
+    float Mw, Sw;
+    fold_max_sum(m, sacc, s2, &Mw, &Sw);
+    if (lane == 0) {
+      ctl.wm[warp] = Mw;
+      ctl.fred[warp] = Sw;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const float mw = lane < kDriftWarps ? ctl.wm[lane] : -kInf;
+      const float sw = lane < kDriftWarps ? ctl.fred[lane] : 0.f;
+      fold_max_sum(mw, sw, s2, &Mw, &Sw);
+      if (lane == 0) {
+        ctl.M = Mw;
+        ctl.S = Sw;
+        ctl.flags = (Mw != Mw || Mw == kInf || Mw == -kInf) ? 1u : 0u;
+        // one record per logit row (the truncated verify's slice is the row)
+        store_part(P.part + row, Mw, Sw, 0u, tag);
+      }
+    }
+    __syncthreads();
+  }
+  if (!active) return;
+  TruncRec *rec = P.trunc + row;
+  if (ctl.flags) {  // the resolve kernel flags this row from the same record
+    if (tid == 0) *rec = TruncRec{0u, 0.f, 1u, 0u};
+    return;
+  }
+  const float nM = -__fmul_rn(ctl.M, s2);
+  auto mass_of = [&](uint32_t bits) {  // exp2((l - M) s2) of one element
+    const float l = BF16 ? __uint_as_float(bits << 16) : __uint_as_float(bits);
+    return l == -kInf ? 0.f : ex2(__fmaf_rn(l, s2, nM));
+  };
+  // the listed candidates' masses, from their keys, once M is known
+  auto fill_masses = [&](int n) {
+    for (int i = tid; i < min(n, kDriftCand); i += kDriftThreads) {
+      const float l = key_value<BF16>(static_cast<uint32_t>(ctl.ck[i] >> 32));
+      ctl.e[i] = l == -kInf ? 0.f : ex2(__fmaf_rn(l, s2, nM));
+    }
+    __syncthreads();
   };
   auto key_at = [&](int i) { return static_cast<uint32_t>(ctl.ck[i] >> 32); };
   // ---- sort the candidates (key desc, id asc) and prefix-sum their masses
@@ -1992,10 +2052,12 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
   uint32_t theta = 0;
   float kept = 0.f;
   bool done = false;
-  int r = tk > 0 ? max(16, (2 * tk) / kDriftSample + 2) : 16;
   for (int attempt = 0; attempt < 3 && !done; ++attempt) {
-    const uint32_t tau = sample_tau(r);
-    const int nc = collect(tau);
+    if (attempt > 0) {  // another threshold: list the candidates again
+      tau = sample_tau(r);
+      nc = pass(false, true, tau);
+    }
+    fill_masses(nc);
     if (nc > kDriftCand) {  // too many: raise the threshold
       if (r <= 1) break;
       r = max(1, r / 4);
@@ -2239,12 +2301,15 @@ cudaError_t ring_blocks_t(size_t smem, int *blocks) {
                                                        kSoftThreads + 32, smem);
 }
 
+// The truncated verify: the generation step, the truncation kernel (one CTA
+// per logit row, which also writes the row's record), then the resolve kernel.
 template <bool BF16>
 cudaError_t launch_truncated_t(const ChainStochParams &p, int grid, int cluster, cudaStream_t s) {
   cudaError_t e = prepare<BF16>(cluster);
-  if (e == cudaSuccess) e = launch_stream<BF16>(p, grid, s);
-  if (e == cudaSuccess)
-    e = launch_dependent(trunc_kernel<BF16>, p, dim3(static_cast<unsigned>(p.B * (p.K + 1) + p.B * p.K)), s);
+  if (e != cudaSuccess) return e;
+  advance_generation_kernel<<<1, 1, 0, s>>>(p.gen, p.claim);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) e = launch_dependent(trunc_kernel<BF16>, p, dim3(static_cast<unsigned>(grid)), s);
   if (e == cudaSuccess) e = launch_resolve<BF16>(p, cluster, s);
   return e;
 }
