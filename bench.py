@@ -603,7 +603,7 @@ def run_next(args):
                            "l2": f"{n_sets} rotating input sets > L2"},
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                              "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
-                             "kernel": "stream_partials_kernel + drift_select_kernel",
+                             "kernel": "drift_select_kernel (one pass per position) + drift_status_kernel",
                              "algorithmic_bytes_per_launch": alg, "traffic": None},
                 "gpu_launches": 3 * n, "clocks": clocks}
     else:

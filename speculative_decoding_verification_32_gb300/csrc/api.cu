@@ -80,23 +80,6 @@ cudaError_t device_info(int *dev, DevInfo *info) {
   return cudaSuccess;
 }
 
-cudaError_t soft_blocks(int dev, bool bf16, bool vec, int *out) {
-  auto key = std::make_tuple(dev, 2 + (int)bf16, static_cast<size_t>(vec));
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    auto it = g_blocks.find(key);
-    if (it != g_blocks.end()) {
-      *out = it->second;
-      return cudaSuccess;
-    }
-  }
-  cudaError_t e = stream_blocks_per_sm(bf16, vec, out);
-  if (e != cudaSuccess) return e;
-  std::lock_guard<std::mutex> lk(g_mu);
-  g_blocks[key] = *out;
-  return cudaSuccess;
-}
-
 cudaError_t ring_blocks(int dev, bool bf16, int stages, size_t smem, int *out) {
   auto key = std::make_tuple(dev, 8 + (int)bf16 + 2 * stages, smem);
   {
@@ -179,9 +162,9 @@ spec_status run_greedy(GreedyParams &p, bool bf16, int esz, void *ws, cudaStream
 }
 
 // How the first kernel of a stochastic call reads the logits: the bulk-copy
-// ring (plain verify), the plain-load stream (DRIFT), or one CTA per whole
-// logit row (truncated verify: one record per row).
-enum class StreamKind { kRing, kPlain, kWholeRow };
+// ring (plain verify), or one CTA per whole logit row (truncated verify and
+// DRIFT: one record per row).
+enum class StreamKind { kRing, kWholeRow };
 
 // Parameters and launch shapes of the stochastic stream kernel and of the
 // resolve kernel's cluster split, from the arguments and the workspace;
@@ -235,16 +218,8 @@ spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes
     }
     p.buf_bytes = 2 * p.slice * esz;  // target tile + draft tile
     *smem = static_cast<size_t>(p.stages) * p.buf_bytes + kRingCtrlBytes;
-  } else if (kind == StreamKind::kWholeRow) {
-    p.slice = a->V;  // the truncation kernel's CTA reads its whole row
   } else {
-    // the plain-load stream: one item per (logit row, 4096-logit slice);
-    // SPECVERIFY_STREAM_SLICE (2048..16384, a multiple of 1024) overrides it
-    p.slice = kStreamSlice;
-    if (const char *ov = std::getenv("SPECVERIFY_STREAM_SLICE")) {
-      const int sl = std::atoi(ov);
-      if (sl >= 2048 && sl <= 16384 && sl % 1024 == 0 && sl >= kSoftMinSlice) p.slice = sl;
-    }
+    p.slice = a->V;  // one CTA reads each whole row
   }
   p.nslices = ceil_div(a->V, p.slice);
   {
@@ -260,18 +235,8 @@ spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes
     if (ring_blocks(dev, bf16, p.stages, *smem, &per_sm) != cudaSuccess || per_sm < 1) return SPEC_ERR_CUDA;
     const long long tiles = static_cast<long long>(a->B) * (K + 1) * p.nslices;
     grid = static_cast<int>(std::min<long long>(tiles, static_cast<long long>(di.sms) * per_sm));
-  } else if (kind == StreamKind::kWholeRow) {
-    grid = static_cast<int>(rows_all);
   } else {
-    if (soft_blocks(dev, bf16, p.use_tma != 0, &per_sm) != cudaSuccess || per_sm < 1) return SPEC_ERR_CUDA;
-    const long long items = rows_all * p.nslices;
-    const long long warps_per_block = kStreamThreads / 32;
-    grid = static_cast<int>(std::max<long long>(
-        1, std::min<long long>((items + warps_per_block - 1) / warps_per_block, static_cast<long long>(di.sms) * per_sm)));
-  }
-  if (const char *ov = std::getenv("SPECVERIFY_STREAM_GRID")) {  // tuning override
-    const long long g = std::atoll(ov);
-    if (g >= 1 && g <= static_cast<long long>(di.sms) * per_sm) grid = static_cast<int>(g);
+    grid = static_cast<int>(rows_all);
   }
   // resolve kernel: a cluster of C CTAs per row, at most 16 rounds of 32
   // vectors per warp
@@ -466,15 +431,15 @@ spec_status spec_drift_residuals(const spec_chain_args *a, int32_t m, int32_t *s
   int grid = 0, C = 0;
   size_t smem = 0;
   {
-    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, C, StreamKind::kPlain, &smem);
+    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, C, StreamKind::kWholeRow, &smem);
     if (st != SPEC_OK) return st;
   }
   p.row_status = row_status;
   p.drift_m = m;
   p.drift_support = support;
   p.drift_residual = residual;
-  report("drift grid m", grid, m, 0, 0, 0, 0, 0);
-  return launch_drift(p, a->dtype == SPEC_BF16, grid, static_cast<cudaStream_t>(stream)) ==
+  report("drift m", m, 0, 0, 0, 0, 0, 0);
+  return launch_drift(p, a->dtype == SPEC_BF16, static_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? SPEC_OK
              : SPEC_ERR_CUDA;

@@ -250,6 +250,45 @@ __device__ __forceinline__ bool vec_may_reach(const uint32_t *w, float tf) {
 }
 
 // The row's top-k / top-p parameters; false when neither truncates.
+// Folds U 16-byte vectors into a thread's running (max, sum of exp2((x - max)
+// s2)): the vectors' largest element raises the max, the sum is rescaled to it
+// and every element adds its exp2 (-inf adds nothing; a NaN poisons both).
+template <bool BF16, int U>
+__device__ __forceinline__ void online_accumulate(const uint32_t (&w)[U][4], float s2, float &m, float &s) {
+  using F = Fmt<BF16>;
+  constexpr int EPV = F::EPV;
+  float bm;
+  if constexpr (BF16) {
+    uint32_t pm = F::NEG_INF_WORD;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      pm = bf16x2_max_nan(pm, bf16x2_max_nan(bf16x2_max_nan(w[u][0], w[u][1]), bf16x2_max_nan(w[u][2], w[u][3])));
+    bm = fmax_nan(bf16_lo(pm), bf16_hi(pm));
+  } else {
+    bm = -kInf;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      bm = fmax_nan(bm, fmax_nan(fmax_nan(__uint_as_float(w[u][0]), __uint_as_float(w[u][1])),
+                                 fmax_nan(__uint_as_float(w[u][2]), __uint_as_float(w[u][3]))));
+  }
+  const float mn = fmax_nan(m, bm);
+  if (mn == -kInf) return;
+  const float off = -__fmul_rn(mn, s2);
+  const float2 s2v = make_float2(s2, s2), offv = make_float2(off, off);
+  float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+#pragma unroll
+    for (int i = 0; i < EPV / 2; ++i) {
+      const float2 a = ffma2(F::pair(w[u], i), s2v, offv);
+      if (i & 1) acc1 = fadd2(acc1, make_float2(ex2(a.x), ex2(a.y)));
+      else acc0 = fadd2(acc0, make_float2(ex2(a.x), ex2(a.y)));
+    }
+  }
+  s = (m == -kInf ? 0.f : s * ex2(__fmul_rn(m - mn, s2))) + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
+  m = mn;
+}
+
 __device__ __forceinline__ bool trunc_active(const ChainStochParams &P, int b, int V, int *k,
                                              float *tp) {
   *k = P.top_k ? P.top_k[b] : 0;
@@ -671,169 +710,6 @@ __global__ void __launch_bounds__(kSoftThreads + 32, 3) softmax_partials_kernel(
           ctl.arrived[slot] = 0;
           ctl.tflags[slot] = 0;
         }
-      }
-    }
-  }
-}
-
-// Item `it` of the stream, in stream order.  Phase A: the bonus positions
-// (j = K), then j = K-1 down to 2, each over b = 0..B-1.  Phase B: positions
-// 1 and 0 row by row, so rows complete one after another and their likely
-// stopping positions are the last data streamed.  A position is its target
-// row's nt slices, then (j < K) its draft row's.
-__device__ __forceinline__ void stream_item_of(long long it, int B, int K, int nt, int *b, int *j,
-                                               bool *draft, int *sl) {
-  const long long pn = nt, pp = 2LL * nt;  // items of a bonus / a drafted position
-  long long q;
-  if (K >= 2) {
-    const long long a0 = (long long)B * pn;
-    const long long a1 = a0 + (long long)B * (K - 2) * pp;
-    if (it < a0) {
-      *j = K;
-      *b = (int)(it / pn);
-      q = it - *b * pn;
-    } else if (it < a1) {
-      const long long r = it - a0;
-      const long long k = r / ((long long)B * pp);
-      *j = K - 1 - (int)k;
-      const long long r2 = r - k * B * pp;
-      *b = (int)(r2 / pp);
-      q = r2 - *b * pp;
-    } else {
-      const long long r = it - a1;
-      *b = (int)(r / (2 * pp));
-      const long long r2 = r - *b * 2 * pp;
-      *j = 1 - (int)(r2 / pp);
-      q = r2 % pp;
-    }
-  } else if (K == 1) {  // per row: position 1 (the bonus), then 0
-    const long long per = pn + pp;
-    *b = (int)(it / per);
-    const long long r2 = it - *b * per;
-    *j = r2 < pn ? 1 : 0;
-    q = r2 < pn ? r2 : r2 - pn;
-  } else {
-    *b = (int)(it / pn);
-    *j = 0;
-    q = it - *b * pn;
-  }
-  *draft = q >= nt;
-  *sl = (int)(*draft ? q - nt : q);
-}
-
-// The plain-load stream, used by the DRIFT entry point (whose second kernel
-// waits for the whole stream): a persistent grid of warps; warp
-// w takes items w, w + W, ... in stream order.  A warp reads its item (one
-// logit row's vocabulary slice) with plain 16-byte loads, kStreamU per lane
-// in flight, folds it into the slice's max logit and sum of exp2((x - m) s2)
-// (each lane against its own running max, then a butterfly across the warp)
-// and stamps one record; the item holding the draft token also stamps that
-// token's logit.  No shared memory, no barrier, no atomics.  Positions >= 2
-// carry an L2 evict-first hint; positions 0 and 1 do not.  Alone it streams
-// c3 in 30 us against the ring's 33, but ahead of the resolve kernel the step
-// measured 47-53 us against the ring's 43.5, so the plain verify keeps the
-// ring.
-template <bool BF16, bool VEC>
-__global__ void __launch_bounds__(kStreamThreads, 4) stream_partials_kernel(const __grid_constant__ ChainStochParams P) {
-  using F = Fmt<BF16>;
-  constexpr int EPV = F::EPV, ESZ = F::ESZ, U = kStreamU;
-  // let the next kernel be scheduled; it waits for this grid on the device
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // forced-timeout test: no record of this call appears, so every reader's
-  // bounded wait gives up
-  if (P.force_timeout) return;
-  const int lane = threadIdx.x & 31;
-  const long long GW = (long long)gridDim.x * (kStreamThreads / 32);
-  const int B = P.B, K = P.K, V = P.V, nt = P.nslices;
-  const long long total = (long long)B * nt * (2 * K + 1);
-  const uint32_t tag = *reinterpret_cast<volatile const uint32_t *>(P.gen);
-  const uint64_t pol_first = l2_policy_evict_first(), pol_keep = l2_policy_evict_normal();
-  for (long long it = (long long)blockIdx.x * (kStreamThreads / 32) + (threadIdx.x >> 5); it < total; it += GW) {
-    int b, j, sl;
-    bool draft;
-    stream_item_of(it, B, K, nt, &b, &j, &draft, &sl);
-    const int s0 = sl * P.slice, len = min(V - s0, P.slice);
-    const int prow = draft ? B * (K + 1) + b * K + j : b * (K + 1) + j;
-    const char *src = static_cast<const char *>(draft ? P.draft : P.target) +
-                      ((size_t)row_offset(P, prow) + s0) * ESZ;
-    const uint64_t pol = j <= 1 ? pol_keep : pol_first;
-    const int nvec = (len + EPV - 1) / EPV;
-    uint32_t w[U][4];
-    auto load_one = [&](uint32_t *x, int v) {
-      if constexpr (VEC) {
-        const uint4 r = ld_stream_u4(src + (size_t)v * 16, pol);
-        x[0] = r.x; x[1] = r.y; x[2] = r.z; x[3] = r.w;
-      } else {
-        F::load_vec(x, nullptr, src, false, v, len);
-      }
-    };
-    auto load_batch = [&](int v0) {
-      if (v0 + 32 * U <= nvec) {  // every lane's vectors are in the slice
-#pragma unroll
-        for (int u = 0; u < U; ++u) load_one(w[u], v0 + u * 32 + lane);
-      } else {
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int v = v0 + u * 32 + lane;
-          if (v < nvec) load_one(w[u], v);
-          else w[u][0] = w[u][1] = w[u][2] = w[u][3] = F::NEG_INF_WORD;
-        }
-      }
-    };
-    load_batch(0);  // in flight before anything else waits on memory
-    float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
-    if (!(T > 0.f && T < kInf)) T = 1.0f;  // the resolve kernel flags the row
-    const float s2 = __fdiv_rn(kLog2e, T);
-    const int y = (j < K && P.tokens) ? __ldg(P.tokens + (size_t)b * K + j) : -1;
-    const float2 s2v = make_float2(s2, s2);
-    float m = -kInf, sacc = 0.f;
-    for (int v0 = 0;;) {
-      uint32_t pm = F::NEG_INF_WORD;
-      if constexpr (BF16) {
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-          pm = bf16x2_max_nan(pm, bf16x2_max_nan(bf16x2_max_nan(w[u][0], w[u][1]), bf16x2_max_nan(w[u][2], w[u][3])));
-      }
-      float bm;
-      if constexpr (BF16) {
-        bm = fmax_nan(bf16_lo(pm), bf16_hi(pm));
-      } else {
-        bm = -kInf;
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-          bm = fmax_nan(bm, fmax_nan(fmax_nan(__uint_as_float(w[u][0]), __uint_as_float(w[u][1])),
-                                     fmax_nan(__uint_as_float(w[u][2]), __uint_as_float(w[u][3]))));
-      }
-      const float mn = fmax_nan(m, bm);
-      if (mn != -kInf) {
-        const float off = -__fmul_rn(mn, s2);
-        const float2 offv = make_float2(off, off);
-        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-#pragma unroll
-          for (int i = 0; i < EPV / 2; ++i) {
-            const float2 a = ffma2(F::pair(w[u], i), s2v, offv);
-            if (i & 1) acc1 = fadd2(acc1, make_float2(ex2(a.x), ex2(a.y)));
-            else acc0 = fadd2(acc0, make_float2(ex2(a.x), ex2(a.y)));
-          }
-        }
-        sacc = (m == -kInf ? 0.f : sacc * ex2(__fmul_rn(m - mn, s2))) + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
-        m = mn;
-      }
-      v0 += 32 * U;
-      if (v0 >= nvec) break;
-      load_batch(v0);
-    }
-    float M, S;
-    fold_max_sum(m, sacc, s2, &M, &S);
-    if (lane == 0) {
-      store_part(P.part + (size_t)prow * nt + sl, M, S, 0u, tag);
-      if (y >= s0 && y < s0 + len) {  // the draft token's logit
-        const char *g = src + (size_t)(y - s0) * ESZ;
-        const float l = BF16 ? __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short *>(g))) << 16)
-                             : __ldg(reinterpret_cast<const float *>(g));
-        st_relaxed_u64(P.ylog + prow, __float_as_uint(l) | (static_cast<unsigned long long>(tag) << 32));
       }
     }
   }
@@ -1416,7 +1292,15 @@ constexpr int kDriftMaxM = kDriftMaxSupport;
 constexpr int kDriftMaxRows = kDriftMaxK;
 
 constexpr int kDriftCand = 2048;  // candidate list of the sampled-threshold path
-constexpr int kDriftSample = 64;  // sampling stride of that threshold
+constexpr int kDriftSample = 64;  // sampling stride of that threshold, in vectors
+
+// Elements of a V-long row in its sampled vectors (every kDriftSample-th
+// vector of EPV elements, the last one possibly short).
+__device__ __forceinline__ int sampled_count(int V, int epv) {
+  const int nvec = (V + epv - 1) / epv;
+  const int last = ((nvec - 1) / kDriftSample) * kDriftSample;  // last sampled vector
+  return (last / kDriftSample) * epv + min(epv, V - last * epv);
+}
 
 struct alignas(16) DriftCtrl {
   int hist[kDriftWarps][256];  // whole-row radix fallback
@@ -1430,57 +1314,32 @@ struct alignas(16) DriftCtrl {
   uint32_t sel_key[kDriftMaxM];
   int scan[kDriftWarps];
   int n_gt, n_eq, digit, above;
+  float fold[4][kDriftWarps];  // per-warp (max, sum) of the target and draft rows
   float Mp, Sp, Mq, Sq;
   uint32_t flags;
 };
 
-
-
 template <bool BF16>
-__global__ void __launch_bounds__(kDriftThreads) drift_select_kernel(const __grid_constant__ ChainStochParams P) {
+__global__ void __launch_bounds__(kDriftThreads, 2) drift_select_kernel(const __grid_constant__ ChainStochParams P) {
   using F = Fmt<BF16>;
   constexpr int EPV = F::EPV, ESZ = F::ESZ;
   constexpr int KEYBITS = BF16 ? 16 : 32;
   __shared__ DriftCtrl ctl;
-  __shared__ float4 rstat[2 * kDriftMaxRows + 1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int j = blockIdx.x, b = blockIdx.y;
   const int K = P.K, npos = K + 1, V = P.V, m = P.drift_m;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // the generation step has advanced this call's tag
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // forced-timeout test: no flag record of this call appears, so the status
+  // kernel reports a timeout
+  if (P.force_timeout) return;
   const float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
   const uint32_t tflags = (T > 0.f && T < kInf) ? 0u : F_BAD_TEMPERATURE;
   const float s2 = tflags ? 1.f : __fdiv_rn(kLog2e, T);
   const uint32_t tag = *reinterpret_cast<volatile const uint32_t *>(P.gen);
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  // every position's statistics (the row's status covers all of them)
-  bool ready = true;
-  if (warp < kResolveThreads / 32) ready = fold_rows(P, b, s2, tag, warp, lane, rstat);
-  ready = __syncthreads_and(ready);  // the stream kernel is done: stale means lost
-  if (tid == 0) {
-    uint32_t f = tflags | (ready ? 0u : F_TIMEOUT);
-    for (int r = 0; r < npos + K; ++r) {
-      if (r == K) continue;  // the bonus position is not a drafted one
-      const float4 v = rstat[r];
-      f |= __float_as_uint(v.w);
-      if (v.x != v.x || v.x == kInf) f |= F_NONFINITE;
-      else if (v.x == -kInf) f |= F_EMPTY;
-    }
-    ctl.flags = f;
-    ctl.Mp = rstat[j].x;
-    ctl.Sp = rstat[j].y;
-    ctl.Mq = rstat[npos + j].x;
-    ctl.Sq = rstat[npos + j].y;
-    if (j == 0 && P.row_status) P.row_status[b] = lowest_code(f);
-  }
-  __syncthreads();
   int32_t *sup = P.drift_support + ((size_t)b * K + j) * m;
   float *res = P.drift_residual + ((size_t)b * K + j) * m;
-  if (ctl.flags) {
-    for (int i = tid; i < m; i += kDriftThreads) {
-      sup[i] = -1;
-      res[i] = __int_as_float(0x7fc00000);
-    }
-    return;
-  }
   const char *tg = static_cast<const char *>(P.target) + ((size_t)(b * npos + j) * V) * ESZ;
   const bool aligned = P.use_tma != 0;
   const int nvec = (V + EPV - 1) / EPV;
@@ -1489,62 +1348,55 @@ __global__ void __launch_bounds__(kDriftThreads) drift_select_kernel(const __gri
     if constexpr (BF16) return __ldg(reinterpret_cast<const unsigned short *>(tg) + i);
     else return __ldg(reinterpret_cast<const unsigned int *>(tg) + i);
   };
-  const float nMp = -__fmul_rn(ctl.Mp, s2), nMq = -__fmul_rn(ctl.Mq, s2);
-  const float l2Sp = lg2(ctl.Sp), l2Sq = lg2(ctl.Sq);
   const char *dg = static_cast<const char *>(P.draft) + ((size_t)(b * K + j) * V) * ESZ;
-  // support entry `rank` is token ii: log2 p and log2 q as in the walk, the
-  // difference in nats
-  auto emit = [&](int rank, int ii) {
-    float lt, ld;
-    if constexpr (BF16) {
-      lt = bf16_lo(__ldg(reinterpret_cast<const unsigned short *>(tg) + ii));
-      ld = bf16_lo(__ldg(reinterpret_cast<const unsigned short *>(dg) + ii));
-    } else {
-      lt = __ldg(reinterpret_cast<const float *>(tg) + ii);
-      ld = __ldg(reinterpret_cast<const float *>(dg) + ii);
-    }
-    const float l2p = __fadd_rn(__fmaf_rn(lt, s2, nMp), -l2Sp);
-    const float l2q = ld == -kInf ? -kInf : __fadd_rn(__fmaf_rn(ld, s2, nMq), -l2Sq);
-    sup[rank] = ii;
-    res[rank] = __fmul_rn(__fadd_rn(l2p, -l2q), kLn2);
-  };
-
   auto kth_largest = [&](auto each, int r, int &n_above, int &n_equal) {
     return block_kth_largest<KEYBITS, kDriftThreads>(each, r, ctl.chist, &ctl.digit, &ctl.above,
                                                     n_above, n_equal);
   };
 
-  // ---- threshold: the r-th largest key of a strided sample (every
-  // kDriftSample-th token); about r * kDriftSample keys of the row lie at or
-  // above it
-  constexpr int kNS = (SPEC_MAX_V + kDriftSample * kDriftThreads - 1) / (kDriftSample * kDriftThreads);
-  uint32_t smp[kNS];
+  // ---- threshold: the r-th largest key of a strided sample (the elements
+  // of every kDriftSample-th 16-byte vector, one logit in kDriftSample);
+  // about r * kDriftSample keys of the row lie at or above it
+  constexpr int kNSV = (SPEC_MAX_V + EPV * kDriftSample * kDriftThreads - 1) / (EPV * kDriftSample * kDriftThreads);
+  uint32_t smp[kNSV][4];  // this thread's sampled vectors
 #pragma unroll
-  for (int q = 0; q < kNS; ++q) {
-    const int i = (tid + q * kDriftThreads) * kDriftSample;
-    smp[q] = i < V ? order_key<BF16>(bits_at(i)) : 0u;  // 0: no sample
-  }
-  const int n_samples = (V + kDriftSample - 1) / kDriftSample;
+  for (int q = 0; q < kNSV; ++q)
+    F::load_vec(smp[q], nullptr, tg, aligned, (tid + q * kDriftThreads) * kDriftSample, V);
+  const int n_samples = sampled_count(V, EPV);
   auto samples = [&](auto f) {
 #pragma unroll
-    for (int q = 0; q < kNS; ++q)
-      if ((tid + q * kDriftThreads) * kDriftSample < V) f(smp[q]);
+    for (int q = 0; q < kNSV; ++q) {
+      const int v = (tid + q * kDriftThreads) * kDriftSample;
+#pragma unroll
+      for (int e = 0; e < EPV; ++e)
+        if (v * EPV + e < V) f(order_key<BF16>(elem_bits<BF16>(smp[q], e)));
+    }
   };
   auto sample_rank = [&](int r) -> uint32_t {
     if (r > n_samples) return 0u;  // too few samples: every key qualifies
     int na, ne;
     return kth_largest(samples, r, na, ne);
   };
-  // ---- one pass: every key >= tau into the candidate list
-  auto collect = [&](uint32_t tau) {
+  // ---- one pass over the position's target and draft rows.  With `stats`
+  // it forms both rows' max and sum of exp2((l - m) s2), each thread against
+  // its own running maxima; it always lists the target keys >= tau.
+  float mp = -kInf, sp = 0.f, mq = -kInf, sq = 0.f;
+  auto pass = [&](bool stats, uint32_t tau) {
     if (tid == 0) ctl.n_cand = 0;
     const float tau_f = key_value<BF16>(tau);
     __syncthreads();
-    constexpr int U = 4;  // vectors in flight per thread
+    constexpr int U = 4;  // vectors in flight per thread and row
     for (int v0 = tid; v0 < nvec; v0 += U * kDriftThreads) {
       uint32_t w[U][4];
 #pragma unroll
       for (int u = 0; u < U; ++u) F::load_vec(w[u], nullptr, tg, aligned, v0 + u * kDriftThreads, V);
+      if (stats) {
+        uint32_t x[U][4];
+#pragma unroll
+        for (int u = 0; u < U; ++u) F::load_vec(x[u], nullptr, dg, aligned, v0 + u * kDriftThreads, V);
+        online_accumulate<BF16, U>(w, s2, mp, sp);
+        online_accumulate<BF16, U>(x, s2, mq, sq);
+      }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         // fewer than one vector in ten holds a candidate: each lane looks at
@@ -1569,8 +1421,67 @@ __global__ void __launch_bounds__(kDriftThreads) drift_select_kernel(const __gri
     return ctl.n_cand;
   };
   int r = 8;
+  int nc = pass(true, sample_rank(r));
+  // ---- both rows' max and sum: warps, then warp 0 in a fixed order; this
+  // position's flags go to the status kernel in a stamped record
+  {
+    float M1, S1, M2, S2;
+    fold_max_sum(mp, sp, s2, &M1, &S1);
+    fold_max_sum(mq, sq, s2, &M2, &S2);
+    if (lane == 0) {
+      ctl.fold[0][warp] = M1;
+      ctl.fold[1][warp] = S1;
+      ctl.fold[2][warp] = M2;
+      ctl.fold[3][warp] = S2;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const bool in = lane < kDriftWarps;
+      fold_max_sum(in ? ctl.fold[0][lane] : -kInf, in ? ctl.fold[1][lane] : 0.f, s2, &M1, &S1);
+      fold_max_sum(in ? ctl.fold[2][lane] : -kInf, in ? ctl.fold[3][lane] : 0.f, s2, &M2, &S2);
+      if (lane == 0) {
+        uint32_t f = tflags;
+        for (const float M : {M1, M2}) {
+          if (M != M || M == kInf) f |= F_NONFINITE;
+          else if (M == -kInf) f |= F_EMPTY;
+        }
+        ctl.flags = f;
+        ctl.Mp = M1;
+        ctl.Sp = S1;
+        ctl.Mq = M2;
+        ctl.Sq = S2;
+        store_part(P.part + (size_t)b * K + j, 0.f, 0.f, f, tag);
+      }
+    }
+    __syncthreads();
+  }
+  if (ctl.flags) {  // the status kernel blanks the whole row
+    for (int i = tid; i < m; i += kDriftThreads) {
+      sup[i] = -1;
+      res[i] = __int_as_float(0x7fc00000);
+    }
+    return;
+  }
+  const float nMp = -__fmul_rn(ctl.Mp, s2), nMq = -__fmul_rn(ctl.Mq, s2);
+  const float l2Sp = lg2(ctl.Sp), l2Sq = lg2(ctl.Sq);
+  // support entry `rank` is token ii: log2 p and log2 q as in the walk, the
+  // difference in nats
+  auto emit = [&](int rank, int ii) {
+    float lt, ld;
+    if constexpr (BF16) {
+      lt = bf16_lo(__ldg(reinterpret_cast<const unsigned short *>(tg) + ii));
+      ld = bf16_lo(__ldg(reinterpret_cast<const unsigned short *>(dg) + ii));
+    } else {
+      lt = __ldg(reinterpret_cast<const float *>(tg) + ii);
+      ld = __ldg(reinterpret_cast<const float *>(dg) + ii);
+    }
+    const float l2p = __fadd_rn(__fmaf_rn(lt, s2, nMp), -l2Sp);
+    const float l2q = ld == -kInf ? -kInf : __fadd_rn(__fmaf_rn(ld, s2, nMq), -l2Sq);
+    sup[rank] = ii;
+    res[rank] = __fmul_rn(__fadd_rn(l2p, -l2q), kLn2);
+  };
   for (int attempt = 0; attempt < 3; ++attempt) {
-    const int nc = collect(sample_rank(r));
+    if (attempt > 0) nc = pass(false, sample_rank(r));
     if (nc >= m && nc <= kDriftCand) {
       // the m-th largest candidate key; every candidate above it is taken,
       // and of those equal to it the lowest token ids
@@ -1776,6 +1687,33 @@ __global__ void __launch_bounds__(kDriftThreads) drift_select_kernel(const __gri
 
 // Largest key x (0 .. 2^bits - 1) with pred(x) true, pred being monotone
 // (true for small x).
+// DRIFT row status: one warp per row, a programmatic dependent of the
+// selection grid (whose writes it sees once that grid has completed).  It ORs
+// the row's stamped position flags -- a position whose record did not come is
+// a timeout -- writes the row's code and blanks every position of a flagged
+// row: support -1, residual NaN.
+__global__ void __launch_bounds__(32) drift_status_kernel(const __grid_constant__ ChainStochParams P) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int b = blockIdx.x, lane = threadIdx.x, K = P.K, m = P.drift_m;
+  const uint32_t tag = *reinterpret_cast<volatile const uint32_t *>(P.gen);
+  uint32_t f = 0;
+  for (int j = lane; j < K; j += 32) {
+    float x, y;
+    uint32_t qf;
+    if (!load_part(P.part + (size_t)b * K + j, tag, &x, &y, &qf)) f |= F_TIMEOUT;
+    f |= qf;
+  }
+  f = __reduce_or_sync(FULL_MASK, f);
+  if (lane == 0 && P.row_status) P.row_status[b] = lowest_code(f);
+  if (!f) return;
+  int32_t *sup = P.drift_support + (size_t)b * K * m;
+  float *res = P.drift_residual + (size_t)b * K * m;
+  for (int i = lane; i < K * m; i += 32) {
+    sup[i] = -1;
+    res[i] = __int_as_float(0x7fc00000);
+  }
+}
+
 template <typename Pred>
 __device__ __forceinline__ uint32_t largest_key(int bits, Pred pred) {
   uint32_t x = 0;
@@ -1860,21 +1798,24 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
     return t;
   };
   // ---- sampled threshold tau (as in the DRIFT selection): the r-th largest
-  // key of every kDriftSample-th element
-  constexpr int kNS = (SPEC_MAX_V + kDriftSample * kDriftThreads - 1) / (kDriftSample * kDriftThreads);
-  uint32_t smp[kNS];  // this thread's samples, loaded once
+  // sample, the samples being the elements of every kDriftSample-th 16-byte
+  // vector (one logit in kDriftSample, one DRAM sector per vector)
+  constexpr int kNSV = (SPEC_MAX_V + EPV * kDriftSample * kDriftThreads - 1) / (EPV * kDriftSample * kDriftThreads);
+  uint32_t smp[kNSV][4];  // this thread's sampled vectors, loaded once
   if (active) {
 #pragma unroll
-    for (int q = 0; q < kNS; ++q) {
-      const int i = (tid + q * kDriftThreads) * kDriftSample;
-      smp[q] = i < V ? order_key<BF16>(bits_at(i)) : 0u;
-    }
+    for (int q = 0; q < kNSV; ++q)
+      F::load_vec(smp[q], nullptr, src, aligned, (tid + q * kDriftThreads) * kDriftSample, V);
   }
-  const int n_samples = (V + kDriftSample - 1) / kDriftSample;
+  const int n_samples = sampled_count(V, EPV);
   auto samples = [&](auto f) {
 #pragma unroll
-    for (int q = 0; q < kNS; ++q)
-      if ((tid + q * kDriftThreads) * kDriftSample < V) f(smp[q]);
+    for (int q = 0; q < kNSV; ++q) {
+      const int v = (tid + q * kDriftThreads) * kDriftSample;
+#pragma unroll
+      for (int e = 0; e < EPV; ++e)
+        if (v * EPV + e < V) f(order_key<BF16>(elem_bits<BF16>(smp[q], e)));
+    }
   };
   auto sample_tau = [&](int r) -> uint32_t {
     if (r > n_samples) return 0u;
@@ -1891,46 +1832,13 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
   auto pass = [&](bool stats, bool cands, uint32_t tau) {
     if (tid == 0) ctl.n_cand = 0;
     const float tau_f = key_value<BF16>(tau);
-    const float2 s2v = make_float2(s2, s2);
     __syncthreads();
     constexpr int U = 4;
     for (int v0 = tid; v0 < nvec; v0 += U * kDriftThreads) {
       uint32_t w[U][4];
 #pragma unroll
       for (int u = 0; u < U; ++u) F::load_vec(w[u], nullptr, src, aligned, v0 + u * kDriftThreads, V);
-      if (stats) {
-        float bm;
-        if constexpr (BF16) {
-          uint32_t pm = F::NEG_INF_WORD;
-#pragma unroll
-          for (int u = 0; u < U; ++u)
-            pm = bf16x2_max_nan(pm, bf16x2_max_nan(bf16x2_max_nan(w[u][0], w[u][1]), bf16x2_max_nan(w[u][2], w[u][3])));
-          bm = fmax_nan(bf16_lo(pm), bf16_hi(pm));
-        } else {
-          bm = -kInf;
-#pragma unroll
-          for (int u = 0; u < U; ++u)
-            bm = fmax_nan(bm, fmax_nan(fmax_nan(__uint_as_float(w[u][0]), __uint_as_float(w[u][1])),
-                                       fmax_nan(__uint_as_float(w[u][2]), __uint_as_float(w[u][3]))));
-        }
-        const float mn = fmax_nan(m, bm);
-        if (mn != -kInf) {
-          const float off = -__fmul_rn(mn, s2);
-          const float2 offv = make_float2(off, off);
-          float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int u = 0; u < U; ++u) {
-#pragma unroll
-            for (int i = 0; i < EPV / 2; ++i) {
-              const float2 a = ffma2(F::pair(w[u], i), s2v, offv);
-              if (i & 1) acc1 = fadd2(acc1, make_float2(ex2(a.x), ex2(a.y)));
-              else acc0 = fadd2(acc0, make_float2(ex2(a.x), ex2(a.y)));
-            }
-          }
-          sacc = (m == -kInf ? 0.f : sacc * ex2(__fmul_rn(m - mn, s2))) + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
-          m = mn;
-        }
-      }
+      if (stats) online_accumulate<BF16, U>(w, s2, m, sacc);
       if (cands) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -2229,17 +2137,6 @@ __global__ void advance_generation_kernel(uint32_t *gen, uint32_t *claim) {
   *claim = 0u;
 }
 
-// The generation step, then the stream (plain launches).
-template <bool BF16>
-cudaError_t launch_stream(const ChainStochParams &p, int grid, cudaStream_t s) {
-  advance_generation_kernel<<<1, 1, 0, s>>>(p.gen, p.claim);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (p.use_tma) stream_partials_kernel<BF16, true><<<grid, kStreamThreads, 0, s>>>(p);
-  else stream_partials_kernel<BF16, false><<<grid, kStreamThreads, 0, s>>>(p);
-  return cudaGetLastError();
-}
-
 // The resolve kernel: a cluster of `cluster` CTAs per row, a programmatic
 // dependent of the kernel launched just before it.
 template <bool BF16>
@@ -2261,13 +2158,13 @@ cudaError_t launch_resolve(const ChainStochParams &p, int cluster, cudaStream_t 
   return cudaLaunchKernelEx(&cfg, chain_resolve_kernel<BF16>, p);
 }
 
-// A one-CTA-per-item kernel (grid gx x gy) launched as a programmatic
-// dependent of the stream.
+// A kernel of `threads`-thread CTAs launched as a programmatic dependent of
+// the kernel before it.
 template <typename Kern>
-cudaError_t launch_dependent(Kern k, const ChainStochParams &p, dim3 grid, cudaStream_t s) {
+cudaError_t launch_dependent(Kern k, const ChainStochParams &p, dim3 grid, int threads, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kDriftThreads);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -2309,17 +2206,32 @@ cudaError_t launch_truncated_t(const ChainStochParams &p, int grid, int cluster,
   if (e != cudaSuccess) return e;
   advance_generation_kernel<<<1, 1, 0, s>>>(p.gen, p.claim);
   e = cudaGetLastError();
-  if (e == cudaSuccess) e = launch_dependent(trunc_kernel<BF16>, p, dim3(static_cast<unsigned>(grid)), s);
+  if (e == cudaSuccess) e = launch_dependent(trunc_kernel<BF16>, p, dim3(static_cast<unsigned>(grid)), kDriftThreads, s);
   if (e == cudaSuccess) e = launch_resolve<BF16>(p, cluster, s);
   return e;
 }
 
+// DRIFT: the generation step, one selection CTA per drafted position (which
+// also forms both rows' statistics), then the per-row status.
 template <bool BF16>
-cudaError_t launch_drift_t(const ChainStochParams &p, int grid, cudaStream_t s) {
-  cudaError_t e = launch_stream<BF16>(p, grid, s);
+cudaError_t launch_drift_t(const ChainStochParams &p, cudaStream_t s) {
+  advance_generation_kernel<<<1, 1, 0, s>>>(p.gen, p.claim);
+  cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess)
     e = launch_dependent(drift_select_kernel<BF16>, p,
-                         dim3(static_cast<unsigned>(p.K), static_cast<unsigned>(p.B)), s);
+                         dim3(static_cast<unsigned>(p.K), static_cast<unsigned>(p.B)), kDriftThreads, s);
+  if (e == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.B));
+    cfg.blockDim = dim3(32);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, drift_status_kernel, p);
+  }
   return e;
 }
 
@@ -2342,14 +2254,8 @@ cudaError_t launch_chain_truncated(const ChainStochParams &p, bool bf16, int gri
   return bf16 ? launch_truncated_t<true>(p, grid, cluster, s) : launch_truncated_t<false>(p, grid, cluster, s);
 }
 
-cudaError_t launch_drift(const ChainStochParams &p, bool bf16, int grid, cudaStream_t s) {
-  return bf16 ? launch_drift_t<true>(p, grid, s) : launch_drift_t<false>(p, grid, s);
-}
-
-cudaError_t stream_blocks_per_sm(bool bf16, bool vec, int *blocks) {
-  const void *k = bf16 ? (vec ? (const void *)stream_partials_kernel<true, true> : (const void *)stream_partials_kernel<true, false>)
-                       : (vec ? (const void *)stream_partials_kernel<false, true> : (const void *)stream_partials_kernel<false, false>);
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, k, kStreamThreads, 0);
+cudaError_t launch_drift(const ChainStochParams &p, bool bf16, cudaStream_t s) {
+  return bf16 ? launch_drift_t<true>(p, s) : launch_drift_t<false>(p, s);
 }
 
 }  // namespace sv

@@ -122,23 +122,18 @@ struct RollbackParams {
   int32_t *num_emitted_out;
 };
 
-// Threads per CTA: the two stochastic stream kernels (the bulk-copy ring's
-// consumer warps, one producer warp on top; the plain-load stream), resolve
-// kernel.
+// Threads per CTA: the stochastic stream kernel (the bulk-copy ring's
+// consumer warps, one producer warp on top), resolve kernel.
 constexpr int kSoftThreads = 256;
-constexpr int kStreamThreads = 256;
 constexpr int kResolveThreads = 256;
 // Ring stream: 16-byte vectors per consumer thread per tensor in a tile (a
 // tile is kSoftThreads * kSoftVecs vectors of the target row and as many of
 // the draft row: 8192 bf16 or 4096 fp32 logits per tensor) and ring depth.
 constexpr int kSoftVecs = 4;
 constexpr int kSoftStages = 2;
-// Stochastic stream: 16-byte vectors in flight per lane, and logits per item
-// (one logit row's vocabulary slice: 8 KB in bf16, 16 KB in fp32).
-constexpr int kStreamU = 8;
-constexpr int kStreamSlice = 4096;
-// The slice sizes the workspace's record area.
-constexpr int kSoftMinSlice = kStreamSlice;
+// The smallest vocabulary slice with a record of its own (the ring's fp32
+// tile): it sizes the workspace's record area.
+constexpr int kSoftMinSlice = 4096;
 // Largest rounds of 32 vectors per warp in the resolve kernel.
 constexpr int kResolveMaxRounds = 16;
 // Resolve CTAs one SM holds (the kernel's launch bound): the cluster split
@@ -163,8 +158,7 @@ cudaError_t launch_chain_truncated(const ChainStochParams &p, bool bf16, int gri
                                    cudaStream_t s);
 // Generation step, stream kernel, then the DRIFT selection kernel (one CTA per
 // drafted position).
-cudaError_t launch_drift(const ChainStochParams &p, bool bf16, int grid, cudaStream_t s);
-cudaError_t stream_blocks_per_sm(bool bf16, bool vec, int *blocks);
+cudaError_t launch_drift(const ChainStochParams &p, bool bf16, cudaStream_t s);
 cudaError_t launch_greedy(const GreedyParams &p, bool bf16, int grid, cudaStream_t s);
 cudaError_t greedy_max_blocks_per_sm(bool bf16, bool vec, int *blocks);
 cudaError_t launch_rollback(const RollbackParams &p, cudaStream_t s);
