@@ -232,24 +232,48 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   }
 }
 
-// Whether some element of a 16-byte vector may have an order key >= the key
-// of value tf: its packed maximum is not below tf.  Conservative (a NaN
-// element or threshold answers yes); every element whose key reaches the
-// threshold has a value >= tf, so a "no" is exact.
+// Bit e is set for each element e of a 16-byte vector that is not below the
+// threshold value tf (tw: tf's bf16 bits in both halves, for bf16).  Every
+// element whose order key reaches the threshold's has a value >= tf, so a
+// clear bit is exact; a NaN element or threshold sets the bit.
 template <bool BF16>
-__device__ __forceinline__ bool vec_may_reach(const uint32_t *w, float tf) {
-  float m;
+__device__ __forceinline__ uint32_t may_reach_bits(const uint32_t *w, uint32_t tw, float tf) {
+  uint32_t bits = 0;
   if constexpr (BF16) {
-    const uint32_t p = bf16x2_max_nan(bf16x2_max_nan(w[0], w[1]), bf16x2_max_nan(w[2], w[3]));
-    m = fmax_nan(bf16_lo(p), bf16_hi(p));
+    const __nv_bfloat162 t2 = *reinterpret_cast<const __nv_bfloat162 *>(&tw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t ge = ~__hlt2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]), t2);
+      bits |= ((ge & 1u) | ((ge >> 15) & 2u)) << (2 * i);
+    }
   } else {
-    m = fmax_nan(fmax_nan(__uint_as_float(w[0]), __uint_as_float(w[1])),
-                 fmax_nan(__uint_as_float(w[2]), __uint_as_float(w[3])));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) bits |= (__uint_as_float(w[i]) < tf ? 0u : 1u) << i;
   }
-  return !(m < tf);
+  return bits;
 }
 
-// The row's top-k / top-p parameters; false when neither truncates.
+// Raw bits of element e (a run-time index) of a 16-byte vector held in
+// registers: the word is chosen by selects, not by indexing.
+template <bool BF16>
+__device__ __forceinline__ uint32_t elem_bits_at(const uint32_t *w, int e) {
+  const int i = BF16 ? (e >> 1) : e;
+  const uint32_t x = i < 2 ? (i == 0 ? w[0] : w[1]) : (i == 2 ? w[2] : w[3]);
+  if constexpr (BF16) return (e & 1) ? (x >> 16) : (x & 0xFFFFu);
+  else return x;
+}
+
+// The threshold value tf's bf16 bits in both halves of a word (any value for fp32).
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack_threshold(float tf) {
+  if constexpr (BF16) {
+    const uint32_t hb = __float_as_uint(tf) >> 16;
+    return hb | (hb << 16);
+  } else {
+    return 0u;
+  }
+}
+
 // Folds U 16-byte vectors into a thread's running (max, sum of exp2((x - max)
 // s2)): the vectors' largest element raises the max, the sum is rescaled to it
 // and every element adds its exp2 (-inf adds nothing; a NaN poisons both).
@@ -289,6 +313,7 @@ __device__ __forceinline__ void online_accumulate(const uint32_t (&w)[U][4], flo
   m = mn;
 }
 
+// The row's top-k / top-p parameters; false when neither truncates.
 __device__ __forceinline__ bool trunc_active(const ChainStochParams &P, int b, int V, int *k,
                                              float *tp) {
   *k = P.top_k ? P.top_k[b] : 0;
@@ -1384,6 +1409,7 @@ __global__ void __launch_bounds__(kDriftThreads, 2) drift_select_kernel(const __
   auto pass = [&](bool stats, uint32_t tau) {
     if (tid == 0) ctl.n_cand = 0;
     const float tau_f = key_value<BF16>(tau);
+    const uint32_t tau_w = pack_threshold<BF16>(tau_f);
     __syncthreads();
     constexpr int U = 4;  // vectors in flight per thread and row
     for (int v0 = tid; v0 < nvec; v0 += U * kDriftThreads) {
@@ -1399,14 +1425,15 @@ __global__ void __launch_bounds__(kDriftThreads, 2) drift_select_kernel(const __
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        // fewer than one vector in ten holds a candidate: each lane looks at
-        // its own elements only when its vector's maximum reaches tau, and
-        // appends them one by one (the selection does not depend on order)
-        if (!vec_may_reach<BF16>(w[u], tau_f)) continue;
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) {
+        // fewer than one vector in ten holds a candidate: each lane visits
+        // only its elements not below tau, one at a time, and appends them
+        // (the selection does not depend on order)
+        uint32_t msk = may_reach_bits<BF16>(w[u], tau_w, tau_f);
+        while (msk) {
+          const int e = __ffs(msk) - 1;
+          msk &= msk - 1;
           const int idx = (v0 + u * kDriftThreads) * EPV + e;
-          const uint32_t k = order_key<BF16>(elem_bits<BF16>(w[u], e));
+          const uint32_t k = order_key<BF16>(elem_bits_at<BF16>(w[u], e));
           if (k >= tau && idx < V) {
             const int slot = atomicAdd(&ctl.n_cand, 1);
             if (slot < kDriftCand) {
@@ -1832,6 +1859,7 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
   auto pass = [&](bool stats, bool cands, uint32_t tau) {
     if (tid == 0) ctl.n_cand = 0;
     const float tau_f = key_value<BF16>(tau);
+    const uint32_t tau_w = pack_threshold<BF16>(tau_f);
     __syncthreads();
     constexpr int U = 4;
     for (int v0 = tid; v0 < nvec; v0 += U * kDriftThreads) {
@@ -1842,11 +1870,14 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
       if (cands) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-          if (!vec_may_reach<BF16>(w[u], tau_f)) continue;
-#pragma unroll
-          for (int e = 0; e < EPV; ++e) {
+          // the elements not below tau, one at a time (rarely more than one
+          // in a vector: a lane's loop is as long as its own count)
+          uint32_t msk = may_reach_bits<BF16>(w[u], tau_w, tau_f);
+          while (msk) {
+            const int e = __ffs(msk) - 1;
+            msk &= msk - 1;
             const int idx = (v0 + u * kDriftThreads) * EPV + e;
-            const uint32_t k = order_key<BF16>(elem_bits<BF16>(w[u], e));
+            const uint32_t k = order_key<BF16>(elem_bits_at<BF16>(w[u], e));
             if (k >= tau && idx < V) {
               const int slot = atomicAdd(&ctl.n_cand, 1);
               if (slot < kDriftCand)
