@@ -1988,6 +1988,67 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
     }
     __syncthreads();
   };
+  // The same sort and scan for sets of at most 64 (a top-k set, normally):
+  // warp 0 holds entry i = lane + 32 h in registers and runs the same bitonic
+  // network with shuffles (the keys are unique but for the zero padding), so
+  // no block barrier is needed until it writes the 64 entries back.
+  auto warp_sort_and_scan = [&](int nc) {
+    if (warp == 0) {
+      unsigned long long k[2];
+      float e[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int i = lane + 32 * h;
+        k[h] = i < nc ? ctl.ck[i] : 0ull;
+        e[h] = i < nc ? ctl.e[i] : 0.f;
+      }
+#pragma unroll
+      for (int size = 2; size <= 64; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          if (stride == 32) {  // entries lane (lower) and lane + 32, ascending block: up
+            if (k[0] < k[1]) {
+              const unsigned long long tk0 = k[0];
+              k[0] = k[1];
+              k[1] = tk0;
+              const float te0 = e[0];
+              e[0] = e[1];
+              e[1] = te0;
+            }
+          } else {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int i = lane + 32 * h;
+              const bool lower = (i & stride) == 0, up = (i & size) == 0;
+              const unsigned long long pk = __shfl_xor_sync(FULL_MASK, k[h], stride);
+              const float pe = __shfl_xor_sync(FULL_MASK, e[h], stride);
+              // the pair swaps when (lower's key < upper's key) == up
+              if ((lower ? (k[h] < pk) : (pk < k[h])) == up) {
+                k[h] = pk;
+                e[h] = pe;
+              }
+            }
+          }
+        }
+      }
+      // inclusive prefix sums in sorted order
+      float s0 = e[0], s1 = e[1];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float n0 = __shfl_up_sync(FULL_MASK, s0, o), n1 = __shfl_up_sync(FULL_MASK, s1, o);
+        if (lane >= o) {
+          s0 += n0;
+          s1 += n1;
+        }
+      }
+      s1 += __shfl_sync(FULL_MASK, s0, 31);
+      ctl.ck[lane] = k[0];
+      ctl.ck[lane + 32] = k[1];
+      ctl.e[lane] = s0;
+      ctl.e[lane + 32] = s1;
+    }
+    __syncthreads();
+  };
   uint32_t theta = 0;
   float kept = 0.f;
   bool done = false;
@@ -2041,7 +2102,8 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
       __syncthreads();
       ns = ctl.n_cand;
     }
-    sort_and_scan(ns);
+    if (ns <= 64) warp_sort_and_scan(ns);
+    else sort_and_scan(ns);
     // top-k: the k-th candidate's key, through the end of its group of ties
     int gk = ns - 1;
     float Sk = ctl.S;
