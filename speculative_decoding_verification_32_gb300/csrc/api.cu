@@ -227,7 +227,7 @@ spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes
     p.ylog = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) +
                                                     align_up(rows * p.nslices * sizeof(SoftPart), 256));
     p.trunc = nullptr;  // set by the truncated entry point
-    p.trunc_area = reinterpret_cast<TruncRec *>(reinterpret_cast<char *>(p.ylog) + align_up(rows * 8, 256));
+    p.trunc_area = reinterpret_cast<SoftPart *>(reinterpret_cast<char *>(p.ylog) + align_up(rows * 8, 256));
   }
   int per_sm = 0;
   const long long rows_all = static_cast<long long>(a->B) * (K + 1) + static_cast<long long>(a->B) * K;
@@ -273,7 +273,7 @@ size_t spec_verify_chain_workspace_size(int32_t B, int32_t K, int32_t V) {
   // the fp32 one; greedy: one partial per (position, slice)
   const size_t rows = static_cast<size_t>(B) * (K + 1) + static_cast<size_t>(B) * K;
   const size_t soft = rows * ceil_div(V, kSoftMinSlice) * sizeof(SoftPart) + align_up(rows * 8, 256) +
-                      rows * sizeof(TruncRec);
+                      rows * sizeof(SoftPart);
   const size_t part = greedy_partials_max(B, K + 1, V);
   return align_up(std::max(std::max(soft, part), static_cast<size_t>(256)), 256) + ws_tail_bytes(B);
 }

@@ -781,7 +781,7 @@ __device__ __forceinline__ void cluster_wait() {
 // group folds tiles l, l+GS, ... in order, then the group folds in a fixed
 // butterfly order.  rstat[r] = (max, sum, draft-token logit, flags).
 __device__ bool fold_rows(const ChainStochParams &P, int b, float s2, uint32_t tag, int warp,
-                          int lane, float4 *rstat) {
+                          int lane, float4 *rstat, bool trunc) {
   bool ready = true;  // every record this lane read carries the tag
   constexpr int NW = kResolveThreads / 32;
   const int K = P.K, npos = K + 1, nt = P.nslices;
@@ -797,6 +797,11 @@ __device__ bool fold_rows(const ChainStochParams &P, int b, float s2, uint32_t t
       const bool draft = r > K;
       const int j = draft ? r - npos : r;
       const int prow = draft ? P.B * npos + b * K + j : b * npos + j;
+      if (sub == 0 && trunc) {  // the row's truncation record
+        float th, kp;
+        uint32_t tf;
+        ready &= load_part(P.trunc + prow, tag, &th, &kp, &tf);
+      }
       if (sub == 0 && j < K) {
         // the draft token's logit: written only when the token is in range
         const int y = P.tokens ? __ldg(P.tokens + (size_t)b * K + j) : -1;
@@ -873,11 +878,13 @@ __device__ void decide_row(const ChainStochParams &P, int b, float s2, uint32_t 
       if (!(us >= 0.f && us < 1.f)) flags |= F_BAD_UNIFORM;
       tp = rstat[j];
       flags |= __float_as_uint(tp.w);
-      if (trunc) {  // the kept mass replaces the full sum
-        const TruncRec rt = P.trunc[(size_t)b * npos + j];
-        flags |= rt.flags ? F_TIMEOUT : 0u;
-        thp = rt.theta;
-        tp.y = rt.kept;
+      if (trunc) {  // the kept mass replaces the full sum (records already checked)
+        float th, kp;
+        uint32_t tf;
+        load_part(P.trunc + (size_t)b * npos + j, 0u, &th, &kp, &tf);
+        flags |= tf ? F_TIMEOUT : 0u;
+        thp = __float_as_uint(th);
+        tp.y = kp;
       }
       if (tp.x != tp.x || tp.x == kInf) flags |= F_NONFINITE;
       else if (tp.x == -kInf) flags |= F_EMPTY;
@@ -889,10 +896,12 @@ __device__ void decide_row(const ChainStochParams &P, int b, float s2, uint32_t 
         dq = rstat[npos + j];
         flags |= __float_as_uint(dq.w);
         if (trunc) {
-          const TruncRec rd = P.trunc[(size_t)P.B * npos + (size_t)b * K + j];
-          flags |= rd.flags ? F_TIMEOUT : 0u;
-          thq = rd.theta;
-          dq.y = rd.kept;
+          float th, kp;
+          uint32_t tf;
+          load_part(P.trunc + (size_t)P.B * npos + (size_t)b * K + j, 0u, &th, &kp, &tf);
+          flags |= tf ? F_TIMEOUT : 0u;
+          thq = __float_as_uint(th);
+          dq.y = kp;
         }
         if (dq.x != dq.x || dq.x == kInf) flags |= F_NONFINITE;
         else if (dq.x == -kInf) flags |= F_EMPTY;
@@ -978,12 +987,14 @@ __global__ void __launch_bounds__(kResolveThreads, kResolveBlocksPerSm) chain_re
   if (crank == 0) {
     const RowScalars first = load_scalars(P, b, lane);
     const uint32_t tag = *reinterpret_cast<volatile const uint32_t *>(P.gen);
-    // a truncated verify also needs the threshold kernel's records (that
-    // grid completes after the stream kernel)
-    if (P.trunc) asm volatile("griddepcontrol.wait;" ::: "memory");
+    // a truncated verify also polls the row's truncation records, stamped
+    // the same way, so rows resolve while the truncation grid still runs
+    int tk_;
+    float tp_;
+    const bool trunc = P.trunc && trunc_active(P, b, V, &tk_, &tp_);
     bool gave_up = false;
     const uint64_t t0 = global_timer_ns();
-    while (!__syncthreads_and(fold_rows(P, b, s2, tag, warp, lane, rstat))) {
+    while (!__syncthreads_and(fold_rows(P, b, s2, tag, warp, lane, rstat, trunc))) {
       if (__syncthreads_or(global_timer_ns() - t0 > P.wait_limit_ns)) {  // bounded
         gave_up = true;
         break;
@@ -1050,18 +1061,37 @@ __global__ void __launch_bounds__(kResolveThreads, kResolveBlocksPerSm) chain_re
   while (true) {
     // ---- pass: per-round masses (kept for the search), then the CTA total
     float tsum = 0.f;
-    if (trunc) {  // truncated laws: element by element, with the thresholds
+    if (trunc) {
+      // truncated laws: four rounds of target loads in flight, then element
+      // by element with the thresholds -- only where some element of the
+      // target vector may reach p's threshold (the draft vector is loaded
+      // just then): elsewhere p' is 0 and so is the vector's mass under
+      // either task, exactly
+      const float thp_f = key_value<BF16>(thp);
+      const uint32_t thp_w = pack_threshold<BF16>(thp_f);
 #pragma unroll 1
-      for (int k = 0; k < nr; ++k) {
-        const int v = vbase + 32 * k + lane;
-        uint32_t wp[4], wq[4];
-        F::load_vec(wp, nullptr, tg, aligned, v, len);
-        if (task == 1) F::load_vec(wq, nullptr, dg, aligned, v, len);
-        float r = 0.f;
+      for (int k0 = 0; k0 < nr; k0 += 4) {
+        uint32_t wp[4][4];
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) r += mass(wp, wq, e);
-        rsum[k * NT + tid] = r;
-        tsum += r;
+        for (int k = 0; k < 4; ++k) {
+          const int vlen = (k0 + k < nr) ? len : 0;  // rounds past nr read nothing
+          F::load_vec(wp[k], nullptr, tg, aligned, vbase + 32 * (k0 + k) + lane, vlen);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float r = 0.f;
+          if (may_reach_bits<BF16>(wp[k], thp_w, thp_f) != 0) {
+            uint32_t wq[4];
+            if (task == 1) {
+              const int vlen = (k0 + k < nr) ? len : 0;
+              F::load_vec(wq, nullptr, dg, aligned, vbase + 32 * (k0 + k) + lane, vlen);
+            }
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) r += mass(wp[k], wq, e);
+          }
+          if (k0 + k < nr) rsum[(k0 + k) * NT + tid] = r;
+          tsum += r;
+        }
       }
     } else if (aligned && task == 1) {
 #pragma unroll 1
@@ -1771,13 +1801,16 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
   __shared__ TruncCtrl ctl;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = P.K, V = P.V, npos = K + 1;
-  const int row = blockIdx.x;  // logit rows: targets b*(K+1)+j, then drafts B*(K+1)+b*K+j
-  const bool is_target = row < P.B * npos;
-  const int b = is_target ? row / npos : (row - P.B * npos) / max(K, 1);
-  const int j = is_target ? row - b * npos : row - P.B * npos - b * K;
+  // CTAs in batch-row order (row b's target positions, then its drafts), so
+  // rows complete one after another and the resolve kernel, which polls each
+  // row's records, finishes most rows while this grid still runs.  Logit
+  // rows are numbered targets b*(K+1)+j, then drafts B*(K+1)+b*K+j.
+  const int b = blockIdx.x / (npos + K), q = blockIdx.x - b * (npos + K);
+  const bool is_target = q < npos;
+  const int j = is_target ? q : q - npos;
+  const int row = is_target ? b * npos + j : P.B * npos + b * K + j;
+  // a plain launch: the generation step (this call's tag) has completed
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // the generation step has advanced this call's tag
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   // forced-timeout test: no record of this call appears, so the resolve
   // kernel's bounded wait gives up
   if (P.force_timeout) return;
@@ -1917,9 +1950,9 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
     __syncthreads();
   }
   if (!active) return;
-  TruncRec *rec = P.trunc + row;
+  SoftPart *rec = P.trunc + row;
   if (ctl.flags) {  // the resolve kernel flags this row from the same record
-    if (tid == 0) *rec = TruncRec{0u, 0.f, 1u, 0u};
+    if (tid == 0) store_part(rec, 0.f, 0.f, 1u, tag);
     return;
   }
   const float nM = -__fmul_rn(ctl.M, s2);
@@ -2175,7 +2208,7 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
       kept = Sk;
     }
   }
-  if (tid == 0) *rec = TruncRec{theta, kept, 0u, 0u};
+  if (tid == 0) store_part(rec, __uint_as_float(theta), kept, 0u, tag);
 }
 
 size_t resolve_smem(const ChainStochParams &p) {
@@ -2299,7 +2332,9 @@ cudaError_t launch_truncated_t(const ChainStochParams &p, int grid, int cluster,
   if (e != cudaSuccess) return e;
   advance_generation_kernel<<<1, 1, 0, s>>>(p.gen, p.claim);
   e = cudaGetLastError();
-  if (e == cudaSuccess) e = launch_dependent(trunc_kernel<BF16>, p, dim3(static_cast<unsigned>(grid)), kDriftThreads, s);
+  if (e != cudaSuccess) return e;
+  trunc_kernel<BF16><<<grid, kDriftThreads, 0, s>>>(p);
+  e = cudaGetLastError();
   if (e == cudaSuccess) e = launch_resolve<BF16>(p, cluster, s);
   return e;
 }

@@ -19,15 +19,6 @@ struct alignas(16) SoftPart {
   unsigned long long a, b;
 };
 
-// Truncation of one logit row (top-k / top-p): the kept tokens are those
-// whose order-preserving key is >= theta; kept holds sum exp2((l - m) s2)
-// over them, m being the row's max logit.
-struct alignas(16) TruncRec {
-  uint32_t theta;
-  float kept;
-  uint32_t flags;  // nonzero: no threshold was found (the row is flagged)
-  uint32_t pad;
-};
 
 // One 16-byte partial per (row, position, vocabulary slice) written by the
 // greedy kernel: the slice's largest logit and its lowest index.
@@ -78,8 +69,12 @@ struct ChainStochParams {
   // parameters (NULL: off) and one record per logit row
   const int32_t *top_k;
   const float *top_p;
-  TruncRec *trunc;        // NULL: no truncation
-  TruncRec *trunc_area;   // where the workspace keeps the records
+  // Truncation of a logit row (top-k / top-p) is a stamped record like the
+  // partials: the kept tokens are those whose order-preserving key is >=
+  // theta (word a's value bits), kept = sum exp2((l - m) s2) over them (word
+  // b's), m being the row's max logit; flags nonzero: no threshold was found.
+  SoftPart *trunc;        // NULL: no truncation
+  SoftPart *trunc_area;   // where the workspace keeps the records
   // DRIFT residual extraction (spec_drift_residuals): support size and outputs
   int drift_m;
   int32_t *drift_support;   // [B, K, m]
