@@ -274,6 +274,24 @@ __device__ __forceinline__ uint32_t pack_threshold(float tf) {
   }
 }
 
+// The largest element of U 16-byte vectors (NaN wins), folded into m.
+template <bool BF16, int U>
+__device__ __forceinline__ void online_max(const uint32_t (&w)[U][4], float &m) {
+  using F = Fmt<BF16>;
+  if constexpr (BF16) {
+    uint32_t pm = F::NEG_INF_WORD;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      pm = bf16x2_max_nan(pm, bf16x2_max_nan(bf16x2_max_nan(w[u][0], w[u][1]), bf16x2_max_nan(w[u][2], w[u][3])));
+    m = fmax_nan(m, fmax_nan(bf16_lo(pm), bf16_hi(pm)));
+  } else {
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      m = fmax_nan(m, fmax_nan(fmax_nan(__uint_as_float(w[u][0]), __uint_as_float(w[u][1])),
+                               fmax_nan(__uint_as_float(w[u][2]), __uint_as_float(w[u][3]))));
+  }
+}
+
 // Folds U 16-byte vectors into a thread's running (max, sum of exp2((x - max)
 // s2)): the vectors' largest element raises the max, the sum is rescaled to it
 // and every element adds its exp2 (-inf adds nothing; a NaN poisons both).
@@ -1883,13 +1901,13 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
     return block_kth_largest<KEYBITS, kDriftThreads>(samples, r, ctl.chist, &ctl.digit, &ctl.above,
                                                     na, ne);
   };
-  // ---- one pass over the row.  With `stats` it forms the row's max and sum
-  // of exp2((l - m) s2), each thread against its own running max; with
-  // `cands` it lists every key >= tau (a lane looks at its elements only when
-  // its vector's maximum reaches tau, and appends them one by one: they are
-  // sorted later).  Returns the candidate count.
+  // ---- one pass over the row.  With stats == 2 it forms the row's max and
+  // sum of exp2((l - m) s2), each thread against its own running max; with
+  // stats == 1 the max alone; with `cands` it lists every key >= tau (a lane
+  // visits only its elements not below tau and appends them one by one: they
+  // are sorted later).  Returns the candidate count.
   float m = -kInf, sacc = 0.f;
-  auto pass = [&](bool stats, bool cands, uint32_t tau) {
+  auto pass = [&](int stats, bool cands, uint32_t tau) {
     if (tid == 0) ctl.n_cand = 0;
     const float tau_f = key_value<BF16>(tau);
     const uint32_t tau_w = pack_threshold<BF16>(tau_f);
@@ -1899,7 +1917,8 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
       uint32_t w[U][4];
 #pragma unroll
       for (int u = 0; u < U; ++u) F::load_vec(w[u], nullptr, src, aligned, v0 + u * kDriftThreads, V);
-      if (stats) online_accumulate<BF16, U>(w, s2, m, sacc);
+      if (stats == 2) online_accumulate<BF16, U>(w, s2, m, sacc);
+      else if (stats == 1) online_max<BF16, U>(w, m);
       if (cands) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -1925,7 +1944,12 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
   };
   int r = tk > 0 ? max(16, (2 * tk) / kDriftSample + 2) : 16;
   uint32_t tau = active ? sample_tau(r) : 0u;
-  int nc = pass(true, active, tau);
+  // Under top-k the law's normaliser is the kept mass, summed over the
+  // candidates, so the row needs only its max (no exp per logit: the pass is
+  // bound by the exp unit otherwise).  Untruncated and top-p-only rows need
+  // the full sum.
+  const bool full_sum = !active || tk == 0;
+  int nc = pass(full_sum ? 2 : 1, active, tau);
   // ---- the row's max and sum: warps, then warp 0 in a fixed order
   {
     float Mw, Sw;
@@ -2088,7 +2112,7 @@ __global__ void __launch_bounds__(kDriftThreads) trunc_kernel(const __grid_const
   for (int attempt = 0; attempt < 3 && !done; ++attempt) {
     if (attempt > 0) {  // another threshold: list the candidates again
       tau = sample_tau(r);
-      nc = pass(false, true, tau);
+      nc = pass(0, true, tau);
     }
     fill_masses(nc);
     if (nc > kDriftCand) {  // too many: raise the threshold
