@@ -7,7 +7,9 @@
 // the first rejection and draws the correction from the residual [p - q]+ by
 // inverse CDF; if every draft passes, the bonus token is drawn from p_K.
 //
-// Two kernels per call:
+// The plain verify runs two kernels per call after a one-thread step that
+// advances the workspace's generation (the stamp every record of the call
+// carries):
 //
 //  softmax_partials_kernel -- the HBM stream.  A persistent grid (several CTAs
 //    per SM, no clusters) walks (logit row, vocabulary slice) items through a
@@ -21,15 +23,22 @@
 //    most often stop are still in L2 for the second kernel.
 //
 //  chain_resolve_kernel -- one thread-block cluster per batch row, launched as
-//    a programmatic dependent of the first kernel.  Every CTA folds the row's
-//    partials into the global max and sum of each position, forms the
-//    acceptance ratios in log2 space and finds the first rejection.  The
-//    cluster then re-reads only the stopping position (the residual needs the
-//    global normalisers, so it cannot be formed during the stream): each CTA
-//    sums the residual mass of its vocabulary slice, one cluster barrier
-//    exchanges the masses through distributed shared memory, and the CTA,
-//    warp, round, lane and element whose cumulative interval holds u * mass
-//    are chosen in vocabulary order.
+//    a programmatic dependent of the first kernel.  Rank 0 polls the row's
+//    stamped partials, folds them into the global max and sum of each
+//    position, forms the acceptance ratios in log2 space and finds the first
+//    rejection; the other CTAs read its decision through distributed shared
+//    memory.  The cluster then re-reads only the stopping position (the
+//    residual needs the global normalisers, so it cannot be formed during the
+//    stream): each CTA sums the residual mass of its vocabulary slice, one
+//    cluster barrier exchanges the masses, and the CTA, warp, round, lane and
+//    element whose cumulative interval holds u * mass are chosen in
+//    vocabulary order.
+//
+// The truncated verify replaces the stream by trunc_kernel (one CTA per logit
+// row: its statistics and top-k / top-p thresholds in one pass) ahead of the
+// same resolve kernel.  DRIFT residuals run drift_select_kernel (one CTA per
+// drafted position: both rows' statistics and the target's top m in one
+// pass) and a one-warp-per-row status kernel.
 #include <cuda_bf16.h>
 
 #include <atomic>
