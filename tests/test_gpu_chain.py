@@ -290,6 +290,34 @@ def test_workspace_shared_across_shapes(sv):
         compare_stochastic(chain_via_abi(L, inp, ws), oracle_chain(inp))
 
 
+def test_truncated_drift_and_plain_share_one_workspace(sv):
+    """Truncated, DRIFT and plain calls of different shapes in turn on the
+    binding's one cached workspace (the largest shape comes first, so the
+    buffer is not reallocated): the truncation kernel's stamped records and
+    the DRIFT kernel's position flags sit at shape-dependent offsets, and only
+    the generation stamp keeps a call from taking another call's.  K = 0 (a
+    bonus-only truncated call) is among them."""
+    rng = np.random.default_rng(91)
+    shapes = [(8, 3, 20000), (6, 0, 4099), (5, 2, 7000), (8, 3, 20000), (6, 0, 4099)]
+    for i, (B, K, V) in enumerate(shapes):
+        inp = S.chain_inputs(B=B, K=K, V=V, dtype="bf16", sigma=3.0, seed=V + K, temperature=(0.7, 1.3),
+                             peaks=5, peak_boost=6.0)
+        k = rng.choice([0, 1, 20, 50, V], B).astype(np.int32)
+        p = rng.choice([1.0, 0.5, 0.9], B).astype(np.float32)
+        g = run_trunc(sv, inp, k, p)
+        o = O.verify_chain(inp["target"], inp["draft"], inp["draft_tokens"], inp.get("temperature"),
+                           inp["u_accept"], inp["u_sample"], top_k=k, top_p=p)
+        assert compare_stochastic(g, o) <= 1
+        if K > 0:  # DRIFT on the same shape, then a plain verify
+            sup, res, st = (x.cpu().numpy() for x in sv.spec_drift_residuals(
+                cuda(inp["target"]), cuda(inp["draft"]), cuda(inp["temperature"]), m=16))
+            osup, ores, ost = O.drift_residuals(inp["target"], inp["draft"], inp["temperature"], m=16)
+            assert np.array_equal(st, ost)
+            assert np.array_equal(sup, osup)
+            np.testing.assert_allclose(res, ores, rtol=0, atol=2e-4)
+            compare_stochastic(run_chain(sv, inp), oracle_chain(inp))
+
+
 # ------------------------------------------------------ top-k / top-p truncation
 def _trunc_params(rng, B, V):
     k = rng.choice([0, 1, 2, 20, 50, 1000, V], B).astype(np.int32)
