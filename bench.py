@@ -39,6 +39,12 @@ TRAFFIC = 180649216 + 3728384
 # the same for one greedy_kernel launch on the tree workload
 # (profiles/greedy_tree_c4.md): 583,470,336 read + 3,753,984 written
 TREE_TRAFFIC = 583470336 + 3753984
+# one trunc_kernel launch on the truncated workload
+# (profiles/trunc_kernel_truncated_c3.md): 180,795,392 read + 3,812,608 written
+TRUNC_TRAFFIC = 180795392 + 3812608
+# one drift_select_kernel launch on the DRIFT workload
+# (profiles/drift_select_c3.md): 169,471,232 read + 3,738,112 written
+DRIFT_TRAFFIC = 169471232 + 3738112
 # kernels one stochastic spec_verify_chain call enqueues: the one-thread
 # generation step, the stream kernel and the resolve kernel
 KERNELS_PER_STEP = 3
@@ -489,7 +495,7 @@ def run_next(args):
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                              "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
                              "kernel": "trunc_kernel (one pass per logit row) + chain_resolve",
-                             "algorithmic_bytes_per_launch": step_bytes, "traffic": None},
+                             "algorithmic_bytes_per_launch": step_bytes, "traffic": TRUNC_TRAFFIC},
                 "gpu_launches": 3 * n, "clocks": clocks}
     elif args.workload in ("chain_c5", "greedy"):
         # chain_c5: the stochastic step at scale (B=256, K=8, per-row
@@ -604,7 +610,7 @@ def run_next(args):
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                              "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
                              "kernel": "drift_select_kernel (one pass per position) + drift_status_kernel",
-                             "algorithmic_bytes_per_launch": alg, "traffic": None},
+                             "algorithmic_bytes_per_launch": alg, "traffic": DRIFT_TRAFFIC},
                 "gpu_launches": 3 * n, "clocks": clocks}
     else:
         B = 4096
