@@ -42,9 +42,6 @@ TREE_TRAFFIC = 583470336 + 3753984
 # one trunc_kernel launch on the truncated workload
 # (profiles/trunc_kernel_truncated_c3.md): 180,795,392 read + 3,812,608 written
 TRUNC_TRAFFIC = 180795392 + 3812608
-# one drift_select_kernel launch on the DRIFT workload
-# (profiles/drift_select_c3.md): 169,471,232 read + 3,738,112 written
-DRIFT_TRAFFIC = 169471232 + 3738112
 # kernels one stochastic spec_verify_chain call enqueues: the one-thread
 # generation step, the stream kernel and the resolve kernel
 KERNELS_PER_STEP = 3
@@ -609,9 +606,10 @@ def run_next(args):
                            "l2": f"{n_sets} rotating input sets > L2"},
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                              "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
-                             "kernel": "drift_select_kernel (one pass per position) + drift_status_kernel",
-                             "algorithmic_bytes_per_launch": alg, "traffic": DRIFT_TRAFFIC},
-                "gpu_launches": 3 * n, "clocks": clocks}
+                             "kernel": "draft_stats_kernel + drift_select_kernel (one pass over "
+                                       "each row between them) + drift_status_kernel",
+                             "algorithmic_bytes_per_launch": alg, "traffic": None},
+                "gpu_launches": 4 * n, "clocks": clocks}
     else:
         B = 4096
         rng = np.random.default_rng(3)

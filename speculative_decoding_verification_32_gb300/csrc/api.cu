@@ -162,9 +162,9 @@ spec_status run_greedy(GreedyParams &p, bool bf16, int esz, void *ws, cudaStream
 }
 
 // How the first kernel of a stochastic call reads the logits: the bulk-copy
-// ring (plain verify), or one CTA per whole logit row (truncated verify and
-// DRIFT: one record per row).
-enum class StreamKind { kRing, kWholeRow };
+// ring (plain verify), one CTA per whole logit row (truncated verify: one
+// record per row), or warps over draft-row slices (DRIFT's statistics).
+enum class StreamKind { kRing, kWholeRow, kStats };
 
 // Parameters and launch shapes of the stochastic stream kernel and of the
 // resolve kernel's cluster split, from the arguments and the workspace;
@@ -218,6 +218,8 @@ spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes
     }
     p.buf_bytes = 2 * p.slice * esz;  // target tile + draft tile
     *smem = static_cast<size_t>(p.stages) * p.buf_bytes + kRingCtrlBytes;
+  } else if (kind == StreamKind::kStats) {
+    p.slice = kStatsSlice;
   } else {
     p.slice = a->V;  // one CTA reads each whole row
   }
@@ -235,6 +237,11 @@ spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes
     if (ring_blocks(dev, bf16, p.stages, *smem, &per_sm) != cudaSuccess || per_sm < 1) return SPEC_ERR_CUDA;
     const long long tiles = static_cast<long long>(a->B) * (K + 1) * p.nslices;
     grid = static_cast<int>(std::min<long long>(tiles, static_cast<long long>(di.sms) * per_sm));
+  } else if (kind == StreamKind::kStats) {  // a persistent grid of warps, four CTAs per SM
+    const long long items = static_cast<long long>(a->B) * K * p.nslices;
+    const long long warps = kStatsThreads / 32;
+    grid = static_cast<int>(std::max<long long>(
+        1, std::min<long long>((items + warps - 1) / warps, static_cast<long long>(di.sms) * 4)));
   } else {
     grid = static_cast<int>(rows_all);
   }
@@ -431,15 +438,15 @@ spec_status spec_drift_residuals(const spec_chain_args *a, int32_t m, int32_t *s
   int grid = 0, C = 0;
   size_t smem = 0;
   {
-    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, C, StreamKind::kWholeRow, &smem);
+    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, C, StreamKind::kStats, &smem);
     if (st != SPEC_OK) return st;
   }
   p.row_status = row_status;
   p.drift_m = m;
   p.drift_support = support;
   p.drift_residual = residual;
-  report("drift m", m, 0, 0, 0, 0, 0, 0);
-  return launch_drift(p, a->dtype == SPEC_BF16, static_cast<cudaStream_t>(stream)) ==
+  report("drift grid m", grid, m, 0, 0, 0, 0, 0);
+  return launch_drift(p, a->dtype == SPEC_BF16, grid, static_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? SPEC_OK
              : SPEC_ERR_CUDA;

@@ -36,9 +36,10 @@
 //
 // The truncated verify replaces the stream by trunc_kernel (one CTA per logit
 // row: its statistics and top-k / top-p thresholds in one pass) ahead of the
-// same resolve kernel.  DRIFT residuals run drift_select_kernel (one CTA per
-// drafted position: both rows' statistics and the target's top m in one
-// pass) and a one-warp-per-row status kernel.
+// same resolve kernel.  DRIFT residuals run draft_stats_kernel (the draft
+// rows' statistics), drift_select_kernel (one CTA per drafted position: the
+// target row's statistics and top m in one pass) and a one-warp-per-row
+// status kernel.
 #include <cuda_bf16.h>
 
 #include <atomic>
@@ -1396,10 +1397,64 @@ struct alignas(16) DriftCtrl {
   uint32_t sel_key[kDriftMaxM];
   int scan[kDriftWarps];
   int n_gt, n_eq, digit, above;
-  float fold[4][kDriftWarps];  // per-warp (max, sum) of the target and draft rows
+  float slm[kStatsMaxSlices], sls[kStatsMaxSlices];  // the target row's per-slice (max, sum)
   float Mp, Sp, Mq, Sq;
   uint32_t flags;
 };
+
+// DRIFT, first kernel: the draft rows' statistics.  A persistent grid of
+// warps over (draft row, 4096-logit slice) items in row order; a warp streams
+// its item with plain 16-byte loads (kStatsU per lane in flight, L2
+// evict-first), folds it into the slice's max and sum of exp2((x - m) s2) and
+// stamps one record.  No shared memory, no barrier, no atomics.
+template <bool BF16, bool VEC>
+__global__ void __launch_bounds__(kStatsThreads, 4) draft_stats_kernel(const __grid_constant__ ChainStochParams P) {
+  using F = Fmt<BF16>;
+  constexpr int EPV = F::EPV, ESZ = F::ESZ, U = kStatsU;
+  // the selection kernel may be scheduled now; it waits for this grid on the
+  // device before it reads these records
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // forced-timeout test: no record of this call appears
+  if (P.force_timeout) return;
+  const int lane = threadIdx.x & 31;
+  const long long GW = (long long)gridDim.x * (kStatsThreads / 32);
+  const int nt = P.nslices, V = P.V, K = P.K;
+  const long long total = (long long)P.B * K * nt;
+  const uint32_t tag = *reinterpret_cast<volatile const uint32_t *>(P.gen);
+  const uint64_t pol = l2_policy_evict_first();
+  for (long long it = (long long)blockIdx.x * (kStatsThreads / 32) + (threadIdx.x >> 5); it < total; it += GW) {
+    const int drow = static_cast<int>(it / nt);  // b * K + j
+    const int sl = static_cast<int>(it - static_cast<long long>(drow) * nt);
+    const int b = drow / K;
+    const int s0 = sl * P.slice, len = min(V - s0, P.slice);
+    const char *src = static_cast<const char *>(P.draft) + ((size_t)drow * V + s0) * ESZ;
+    const int nvec = (len + EPV - 1) / EPV;
+    float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
+    const float s2 = (T > 0.f && T < kInf) ? __fdiv_rn(kLog2e, T) : 1.f;  // a bad T flags the row
+    float m = -kInf, sacc = 0.f;
+    for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
+      uint32_t w[U][4];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if constexpr (VEC) {
+          if (v < nvec) {
+            const uint4 r = ld_stream_u4(src + (size_t)v * 16, pol);
+            w[u][0] = r.x; w[u][1] = r.y; w[u][2] = r.z; w[u][3] = r.w;
+          } else {
+            w[u][0] = w[u][1] = w[u][2] = w[u][3] = F::NEG_INF_WORD;
+          }
+        } else {
+          F::load_vec(w[u], nullptr, src, false, v, len);
+        }
+      }
+      online_accumulate<BF16, U>(w, s2, m, sacc);
+    }
+    float M, S;
+    fold_max_sum(m, sacc, s2, &M, &S);
+    if (lane == 0) store_part(P.part + (size_t)drow * nt + sl, M, S, 0u, tag);
+  }
+}
 
 template <bool BF16>
 __global__ void __launch_bounds__(kDriftThreads, 2) drift_select_kernel(const __grid_constant__ ChainStochParams P) {
@@ -1411,10 +1466,10 @@ __global__ void __launch_bounds__(kDriftThreads, 2) drift_select_kernel(const __
   const int j = blockIdx.x, b = blockIdx.y;
   const int K = P.K, npos = K + 1, V = P.V, m = P.drift_m;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // the generation step has advanced this call's tag
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   // forced-timeout test: no flag record of this call appears, so the status
-  // kernel reports a timeout
+  // kernel reports a timeout.  The generation step completed before the
+  // statistics grid started, so the tag read below is this call's; the
+  // dependency wait on that grid comes just before its records are read.
   if (P.force_timeout) return;
   const float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
   const uint32_t tflags = (T > 0.f && T < kInf) ? 0u : F_BAD_TEMPERATURE;
@@ -1459,45 +1514,65 @@ __global__ void __launch_bounds__(kDriftThreads, 2) drift_select_kernel(const __
     int na, ne;
     return kth_largest(samples, r, na, ne);
   };
-  // ---- one pass over the position's target and draft rows.  With `stats`
-  // it forms both rows' max and sum of exp2((l - m) s2), each thread against
-  // its own running maxima; it always lists the target keys >= tau.
-  float mp = -kInf, sp = 0.f, mq = -kInf, sq = 0.f;
+  // ---- one pass over the position's target row, one warp per slice of
+  // kStatsSlice logits.  With `stats` a warp forms its slice's max and sum
+  // of exp2((l - m) s2) exactly as the draft-row kernel does (same lane
+  // mapping, batch and fold); it always lists the keys >= tau.
   auto pass = [&](bool stats, uint32_t tau) {
     if (tid == 0) ctl.n_cand = 0;
     const float tau_f = key_value<BF16>(tau);
     const uint32_t tau_w = pack_threshold<BF16>(tau_f);
     __syncthreads();
-    constexpr int U = 4;  // vectors in flight per thread and row
-    for (int v0 = tid; v0 < nvec; v0 += U * kDriftThreads) {
-      uint32_t w[U][4];
+    constexpr int U = kStatsU;
+    for (int sl = warp; sl < P.nslices; sl += kDriftWarps) {
+      const int s0 = sl * P.slice, len = min(V - s0, P.slice);
+      const char *src = tg + (size_t)s0 * ESZ;
+      const int snv = (len + EPV - 1) / EPV, sv0 = s0 / EPV;
+      float m = -kInf, sacc = 0.f;
+      for (int v0 = 0; v0 < snv; v0 += 32 * U) {
+        uint32_t w[U][4];
 #pragma unroll
-      for (int u = 0; u < U; ++u) F::load_vec(w[u], nullptr, tg, aligned, v0 + u * kDriftThreads, V);
-      if (stats) {
-        uint32_t x[U][4];
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + u * 32 + lane;
+          if (aligned) {
+            if (v < snv) {
+              const uint4 x = __ldg(reinterpret_cast<const uint4 *>(src) + v);
+              w[u][0] = x.x; w[u][1] = x.y; w[u][2] = x.z; w[u][3] = x.w;
+            } else {
+              w[u][0] = w[u][1] = w[u][2] = w[u][3] = F::NEG_INF_WORD;
+            }
+          } else {
+            F::load_vec(w[u], nullptr, src, false, v, len);
+          }
+        }
+        if (stats) online_accumulate<BF16, U>(w, s2, m, sacc);
 #pragma unroll
-        for (int u = 0; u < U; ++u) F::load_vec(x[u], nullptr, dg, aligned, v0 + u * kDriftThreads, V);
-        online_accumulate<BF16, U>(w, s2, mp, sp);
-        online_accumulate<BF16, U>(x, s2, mq, sq);
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        // fewer than one vector in ten holds a candidate: each lane visits
-        // only its elements not below tau, one at a time, and appends them
-        // (the selection does not depend on order)
-        uint32_t msk = may_reach_bits<BF16>(w[u], tau_w, tau_f);
-        while (msk) {
-          const int e = __ffs(msk) - 1;
-          msk &= msk - 1;
-          const int idx = (v0 + u * kDriftThreads) * EPV + e;
-          const uint32_t k = order_key<BF16>(elem_bits_at<BF16>(w[u], e));
-          if (k >= tau && idx < V) {
-            const int slot = atomicAdd(&ctl.n_cand, 1);
-            if (slot < kDriftCand) {
-              ctl.cand.key[slot] = k;
-              ctl.cand.idx[slot] = idx;
+        for (int u = 0; u < U; ++u) {
+          // fewer than one vector in ten holds a candidate: each lane visits
+          // only its elements not below tau, one at a time, and appends them
+          // (the selection does not depend on order)
+          uint32_t msk = may_reach_bits<BF16>(w[u], tau_w, tau_f);
+          while (msk) {
+            const int e = __ffs(msk) - 1;
+            msk &= msk - 1;
+            const int idx = (sv0 + v0 + u * 32 + lane) * EPV + e;
+            const uint32_t k = order_key<BF16>(elem_bits_at<BF16>(w[u], e));
+            if (k >= tau && idx < V) {
+              const int slot = atomicAdd(&ctl.n_cand, 1);
+              if (slot < kDriftCand) {
+                ctl.cand.key[slot] = k;
+                ctl.cand.idx[slot] = idx;
+              }
             }
           }
+        }
+      }
+      if (stats) {
+        float M, S;
+        fold_max_sum(m, sacc, s2, &M, &S);
+        if (lane == 0) {
+          ctl.slm[sl] = M;
+          ctl.sls[sl] = S;
         }
       }
     }
@@ -1506,25 +1581,38 @@ __global__ void __launch_bounds__(kDriftThreads, 2) drift_select_kernel(const __
   };
   int r = 8;
   int nc = pass(true, sample_rank(r));
-  // ---- both rows' max and sum: warps, then warp 0 in a fixed order; this
-  // position's flags go to the status kernel in a stamped record
+  // ---- the target row's max and sum: warps, then warp 0 in a fixed order;
+  // then the draft row's, folded by warp 0 from the statistics kernel's
+  // records (that grid has completed after the dependency wait).  This
+  // position's flags go to the status kernel in a stamped record.
   {
-    float M1, S1, M2, S2;
-    fold_max_sum(mp, sp, s2, &M1, &S1);
-    fold_max_sum(mq, sq, s2, &M2, &S2);
-    if (lane == 0) {
-      ctl.fold[0][warp] = M1;
-      ctl.fold[1][warp] = S1;
-      ctl.fold[2][warp] = M2;
-      ctl.fold[3][warp] = S2;
-    }
-    __syncthreads();
     if (warp == 0) {
-      const bool in = lane < kDriftWarps;
-      fold_max_sum(in ? ctl.fold[0][lane] : -kInf, in ? ctl.fold[1][lane] : 0.f, s2, &M1, &S1);
-      fold_max_sum(in ? ctl.fold[2][lane] : -kInf, in ? ctl.fold[3][lane] : 0.f, s2, &M2, &S2);
+      // both rows' slices fold the same way: lane t takes slices t, t + 32,
+      // ... in order, then the lanes fold in a fixed butterfly
+      const int nt = P.nslices;
+      auto fold_slices = [&](auto slice_stat, float *M, float *S) {
+        float mm = -kInf, ss = 0.f;
+        for (int t = lane; t < nt; t += 32) {
+          float qm, qs;
+          slice_stat(t, &qm, &qs);
+          const float mn = fmax_nan(mm, qm);
+          ss = (mm == -kInf ? 0.f : ss * ex2(__fmul_rn(mm - mn, s2))) +
+               (qm == -kInf ? 0.f : qs * ex2(__fmul_rn(qm - mn, s2)));
+          mm = mn;
+        }
+        fold_max_sum(mm, ss, s2, M, S);
+      };
+      float M1, S1, M2, S2;
+      fold_slices([&](int t, float *qm, float *qs) { *qm = ctl.slm[t]; *qs = ctl.sls[t]; }, &M1, &S1);
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      bool ready = true;
+      fold_slices([&](int t, float *qm, float *qs) {
+        uint32_t qf;
+        ready &= load_part(P.part + (size_t)(b * K + j) * nt + t, tag, qm, qs, &qf);
+      }, &M2, &S2);
+      ready = __all_sync(FULL_MASK, ready);
       if (lane == 0) {
-        uint32_t f = tflags;
+        uint32_t f = tflags | (ready ? 0u : F_TIMEOUT);
         for (const float M : {M1, M2}) {
           if (M != M || M == kInf) f |= F_NONFINITE;
           else if (M == -kInf) f |= F_EMPTY;
@@ -1534,7 +1622,7 @@ __global__ void __launch_bounds__(kDriftThreads, 2) drift_select_kernel(const __
         ctl.Sp = S1;
         ctl.Mq = M2;
         ctl.Sq = S2;
-        store_part(P.part + (size_t)b * K + j, 0.f, 0.f, f, tag);
+        store_part(P.trunc_area + (size_t)b * K + j, 0.f, 0.f, f, tag);
       }
     }
     __syncthreads();
@@ -1784,7 +1872,7 @@ __global__ void __launch_bounds__(32) drift_status_kernel(const __grid_constant_
   for (int j = lane; j < K; j += 32) {
     float x, y;
     uint32_t qf;
-    if (!load_part(P.part + (size_t)b * K + j, tag, &x, &y, &qf)) f |= F_TIMEOUT;
+    if (!load_part(P.trunc_area + (size_t)b * K + j, tag, &x, &y, &qf)) f |= F_TIMEOUT;
     f |= qf;
   }
   f = __reduce_or_sync(FULL_MASK, f);
@@ -2377,12 +2465,17 @@ cudaError_t launch_truncated_t(const ChainStochParams &p, int grid, int cluster,
   return e;
 }
 
-// DRIFT: the generation step, one selection CTA per drafted position (which
-// also forms both rows' statistics), then the per-row status.
+// DRIFT: the generation step, the draft rows' statistics, one selection CTA
+// per drafted position (which also forms the target row's statistics), then
+// the per-row status.
 template <bool BF16>
-cudaError_t launch_drift_t(const ChainStochParams &p, cudaStream_t s) {
+cudaError_t launch_drift_t(const ChainStochParams &p, int grid, cudaStream_t s) {
   advance_generation_kernel<<<1, 1, 0, s>>>(p.gen, p.claim);
   cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (p.use_tma) draft_stats_kernel<BF16, true><<<grid, kStatsThreads, 0, s>>>(p);
+  else draft_stats_kernel<BF16, false><<<grid, kStatsThreads, 0, s>>>(p);
+  e = cudaGetLastError();
   if (e == cudaSuccess)
     e = launch_dependent(drift_select_kernel<BF16>, p,
                          dim3(static_cast<unsigned>(p.K), static_cast<unsigned>(p.B)), kDriftThreads, s);
@@ -2420,8 +2513,8 @@ cudaError_t launch_chain_truncated(const ChainStochParams &p, bool bf16, int gri
   return bf16 ? launch_truncated_t<true>(p, grid, cluster, s) : launch_truncated_t<false>(p, grid, cluster, s);
 }
 
-cudaError_t launch_drift(const ChainStochParams &p, bool bf16, cudaStream_t s) {
-  return bf16 ? launch_drift_t<true>(p, s) : launch_drift_t<false>(p, s);
+cudaError_t launch_drift(const ChainStochParams &p, bool bf16, int grid, cudaStream_t s) {
+  return bf16 ? launch_drift_t<true>(p, grid, s) : launch_drift_t<false>(p, grid, s);
 }
 
 }  // namespace sv

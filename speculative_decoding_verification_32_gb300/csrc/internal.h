@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "specverify.h"
+
 namespace sv {
 
 // One 16-byte partial per (logit row, tile) written by the softmax-partial
@@ -129,6 +131,14 @@ constexpr int kSoftStages = 2;
 // The smallest vocabulary slice with a record of its own (the ring's fp32
 // tile): it sizes the workspace's record area.
 constexpr int kSoftMinSlice = 4096;
+// DRIFT's row statistics: threads per CTA of the draft-row kernel, 16-byte
+// vectors in flight per lane, and logits per slice.  The selection kernel
+// forms the target row's statistics with the same slices, lane mapping and
+// batch, so identical rows give identical bits.
+constexpr int kStatsThreads = 256;
+constexpr int kStatsU = 4;
+constexpr int kStatsSlice = 4096;
+constexpr int kStatsMaxSlices = (SPEC_MAX_V + kStatsSlice - 1) / kStatsSlice;
 // Largest rounds of 32 vectors per warp in the resolve kernel.
 constexpr int kResolveMaxRounds = 16;
 // Resolve CTAs one SM holds (the kernel's launch bound): the cluster split
@@ -153,7 +163,7 @@ cudaError_t launch_chain_truncated(const ChainStochParams &p, bool bf16, int gri
                                    cudaStream_t s);
 // Generation step, stream kernel, then the DRIFT selection kernel (one CTA per
 // drafted position).
-cudaError_t launch_drift(const ChainStochParams &p, bool bf16, cudaStream_t s);
+cudaError_t launch_drift(const ChainStochParams &p, bool bf16, int grid, cudaStream_t s);
 cudaError_t launch_greedy(const GreedyParams &p, bool bf16, int grid, cudaStream_t s);
 cudaError_t greedy_max_blocks_per_sm(bool bf16, bool vec, int *blocks);
 cudaError_t launch_rollback(const RollbackParams &p, cudaStream_t s);
