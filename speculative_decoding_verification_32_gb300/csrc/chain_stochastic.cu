@@ -1432,8 +1432,7 @@ __global__ void __launch_bounds__(kStatsThreads, 4) draft_stats_kernel(const __g
     float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
     const float s2 = (T > 0.f && T < kInf) ? __fdiv_rn(kLog2e, T) : 1.f;  // a bad T flags the row
     float m = -kInf, sacc = 0.f;
-    for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
-      uint32_t w[U][4];
+    auto load_batch = [&](uint32_t (&w)[U][4], int v0) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int v = v0 + u * 32 + lane;
@@ -1448,7 +1447,16 @@ __global__ void __launch_bounds__(kStatsThreads, 4) draft_stats_kernel(const __g
           F::load_vec(w[u], nullptr, src, false, v, len);
         }
       }
-      online_accumulate<BF16, U>(w, s2, m, sacc);
+    };
+    // two batches of U vectors in flight, folded in order: the same
+    // arithmetic as one batch at a time (a batch past the slice's end is all
+    // -inf and leaves (m, sum) unchanged)
+    for (int v0 = 0; v0 < nvec; v0 += 64 * U) {
+      uint32_t wa[U][4], wb[U][4];
+      load_batch(wa, v0);
+      load_batch(wb, v0 + 32 * U);
+      online_accumulate<BF16, U>(wa, s2, m, sacc);
+      online_accumulate<BF16, U>(wb, s2, m, sacc);
     }
     float M, S;
     fold_max_sum(m, sacc, s2, &M, &S);
