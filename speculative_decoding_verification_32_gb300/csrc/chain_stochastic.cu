@@ -1537,8 +1537,7 @@ __global__ void __launch_bounds__(kDriftThreads, 2) drift_select_kernel(const __
       const char *src = tg + (size_t)s0 * ESZ;
       const int snv = (len + EPV - 1) / EPV, sv0 = s0 / EPV;
       float m = -kInf, sacc = 0.f;
-      for (int v0 = 0; v0 < snv; v0 += 32 * U) {
-        uint32_t w[U][4];
+      auto load_batch = [&](uint32_t (&w)[U][4], int v0) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int v = v0 + u * 32 + lane;
@@ -1553,23 +1552,34 @@ __global__ void __launch_bounds__(kDriftThreads, 2) drift_select_kernel(const __
             F::load_vec(w[u], nullptr, src, false, v, len);
           }
         }
-        if (stats) online_accumulate<BF16, U>(w, s2, m, sacc);
+      };
+      // two batches in flight, folded in order as the draft-row kernel does
+      for (int v00 = 0; v00 < snv; v00 += 64 * U) {
+        uint32_t wab[2][U][4];
+        load_batch(wab[0], v00);
+        load_batch(wab[1], v00 + 32 * U);
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          // fewer than one vector in ten holds a candidate: each lane visits
-          // only its elements not below tau, one at a time, and appends them
-          // (the selection does not depend on order)
-          uint32_t msk = may_reach_bits<BF16>(w[u], tau_w, tau_f);
-          while (msk) {
-            const int e = __ffs(msk) - 1;
-            msk &= msk - 1;
-            const int idx = (sv0 + v0 + u * 32 + lane) * EPV + e;
-            const uint32_t k = order_key<BF16>(elem_bits_at<BF16>(w[u], e));
-            if (k >= tau && idx < V) {
-              const int slot = atomicAdd(&ctl.n_cand, 1);
-              if (slot < kDriftCand) {
-                ctl.cand.key[slot] = k;
-                ctl.cand.idx[slot] = idx;
+        for (int h = 0; h < 2; ++h) {
+          uint32_t (&w)[U][4] = wab[h];
+          const int v0 = v00 + 32 * U * h;
+          if (stats) online_accumulate<BF16, U>(w, s2, m, sacc);
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            // fewer than one vector in ten holds a candidate: each lane visits
+            // only its elements not below tau, one at a time, and appends them
+            // (the selection does not depend on order)
+            uint32_t msk = may_reach_bits<BF16>(w[u], tau_w, tau_f);
+            while (msk) {
+              const int e = __ffs(msk) - 1;
+              msk &= msk - 1;
+              const int idx = (sv0 + v0 + u * 32 + lane) * EPV + e;
+              const uint32_t k = order_key<BF16>(elem_bits_at<BF16>(w[u], e));
+              if (k >= tau && idx < V) {
+                const int slot = atomicAdd(&ctl.n_cand, 1);
+                if (slot < kDriftCand) {
+                  ctl.cand.key[slot] = k;
+                  ctl.cand.idx[slot] = idx;
+                }
               }
             }
           }
