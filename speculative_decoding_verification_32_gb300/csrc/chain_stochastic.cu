@@ -2033,27 +2033,37 @@ __global__ void __launch_bounds__(kTruncThreads) trunc_kernel(const __grid_const
     const uint32_t tau_w = pack_threshold<BF16>(tau_f);
     __syncthreads();
     constexpr int U = 4;
-    for (int v0 = tid; v0 < nvec; v0 += U * kTruncThreads) {
-      uint32_t w[U][4];
+    // two batches of U vectors per thread in flight, then each in turn
+    // (vectors past the row read as -inf and list nothing: their index is >= V)
+    for (int v00 = tid; v00 < nvec; v00 += 2 * U * kTruncThreads) {
+      uint32_t wab[2][U][4];
 #pragma unroll
-      for (int u = 0; u < U; ++u) F::load_vec(w[u], nullptr, src, aligned, v0 + u * kTruncThreads, V);
-      if (stats == 2) online_accumulate<BF16, U>(w, s2, m, sacc);
-      else if (stats == 1) online_max<BF16, U>(w, m);
-      if (cands) {
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          // the elements not below tau, one at a time (rarely more than one
-          // in a vector: a lane's loop is as long as its own count)
-          uint32_t msk = may_reach_bits<BF16>(w[u], tau_w, tau_f);
-          while (msk) {
-            const int e = __ffs(msk) - 1;
-            msk &= msk - 1;
-            const int idx = (v0 + u * kTruncThreads) * EPV + e;
-            const uint32_t k = order_key<BF16>(elem_bits_at<BF16>(w[u], e));
-            if (k >= tau && idx < V) {
-              const int slot = atomicAdd(&ctl.n_cand, 1);
-              if (slot < kDriftCand)
-                ctl.ck[slot] = (static_cast<unsigned long long>(k) << 32) | (~static_cast<uint32_t>(idx));
+        for (int u = 0; u < U; ++u)
+          F::load_vec(wab[h][u], nullptr, src, aligned, v00 + (h * U + u) * kTruncThreads, V);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t (&w)[U][4] = wab[h];
+        const int v0 = v00 + h * U * kTruncThreads;
+        if (stats == 2) online_accumulate<BF16, U>(w, s2, m, sacc);
+        else if (stats == 1) online_max<BF16, U>(w, m);
+        if (cands) {
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            // the elements not below tau, one at a time (rarely more than one
+            // in a vector: a lane's loop is as long as its own count)
+            uint32_t msk = may_reach_bits<BF16>(w[u], tau_w, tau_f);
+            while (msk) {
+              const int e = __ffs(msk) - 1;
+              msk &= msk - 1;
+              const int idx = (v0 + u * kTruncThreads) * EPV + e;
+              const uint32_t k = order_key<BF16>(elem_bits_at<BF16>(w[u], e));
+              if (k >= tau && idx < V) {
+                const int slot = atomicAdd(&ctl.n_cand, 1);
+                if (slot < kDriftCand)
+                  ctl.ck[slot] = (static_cast<unsigned long long>(k) << 32) | (~static_cast<uint32_t>(idx));
+              }
             }
           }
         }
