@@ -40,8 +40,12 @@ TRAFFIC = 180649216 + 3728384
 # (profiles/greedy_tree_c4.md): 583,470,336 read + 3,753,984 written
 TREE_TRAFFIC = 583470336 + 3753984
 # one trunc_kernel launch on the truncated workload
-# (profiles/trunc_kernel_truncated_c3.md): 180,795,392 read + 3,812,608 written
-TRUNC_TRAFFIC = 180795392 + 3812608
+# (profiles/trunc_kernel_truncated_c3.md): 180,934,144 read + 7,237,888 written
+TRUNC_TRAFFIC = 180934144 + 7237888
+# one DRIFT call's two streaming kernels, draft_stats_kernel and
+# drift_select_kernel (profiles/drift_select_c3.md), which between them read
+# the 164 MB of rows: 82,106,880 + 83,719,936 read, 1,701,376 + 1,669,632 written
+DRIFT_TRAFFIC = 82106880 + 83719936 + 1701376 + 1669632
 # kernels one stochastic spec_verify_chain call enqueues: the one-thread
 # generation step, the stream kernel and the resolve kernel
 KERNELS_PER_STEP = 3
@@ -608,7 +612,7 @@ def run_next(args):
                              "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
                              "kernel": "draft_stats_kernel + drift_select_kernel (one pass over "
                                        "each row between them) + drift_status_kernel",
-                             "algorithmic_bytes_per_launch": alg, "traffic": None},
+                             "algorithmic_bytes_per_launch": alg, "traffic": DRIFT_TRAFFIC},
                 "gpu_launches": 4 * n, "clocks": clocks}
     else:
         B = 4096
