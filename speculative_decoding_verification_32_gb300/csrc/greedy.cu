@@ -353,14 +353,55 @@ __global__ void __launch_bounds__(kWalkThreads) greedy_walk_kernel(const __grid_
   float *mx_s = reinterpret_cast<float *>(wsm + 16);
   int *top_s = reinterpret_cast<int *>(mx_s + npos);
   uint32_t *fl_s = reinterpret_cast<uint32_t *>(top_s + npos);
-  for (int j = warp; j < npos; j += kWalkWarps) {
-    float mx;
-    int top;
-    uint32_t f;
-    combine_position(P.part + ((size_t)b * npos + j) * P.nslices, P.nslices, lane, &mx, &top, &f);
-    if (lane == 0) {
-      mx_s[j] = mx;
-      top_s[j] = top;
+  // Each position's (max, lowest argmax, flags) from its slice partials, by
+  // whichever mapping takes fewer dependent rounds of loads: a warp per
+  // position (lanes over the slices; few positions with many slices, as in a
+  // chain), or a thread per position with four partials in flight (many
+  // positions, as in a tree).  Both take the largest value and, among the
+  // slices holding it, the lowest index; NaN partials are skipped and flagged.
+  const int nsl = P.nslices;
+  const int by_warp = ((npos + kWalkWarps - 1) / kWalkWarps) * ((nsl + 31) / 32);
+  const int by_thread = ((npos + kWalkThreads - 1) / kWalkThreads) * ((nsl + 3) / 4);
+  if (by_warp <= by_thread) {
+    for (int j = warp; j < npos; j += kWalkWarps) {
+      float mx;
+      int top;
+      uint32_t f;
+      combine_position(P.part + ((size_t)b * npos + j) * nsl, nsl, lane, &mx, &top, &f);
+      if (lane == 0) {
+        mx_s[j] = mx;
+        top_s[j] = top;
+        fl_s[j] = f;
+      }
+    }
+  } else {
+    // in vocabulary order, a later slice replacing only on a strictly larger
+    // value
+    for (int j = threadIdx.x; j < npos; j += kWalkThreads) {
+      const GreedyPart *pp = P.part + ((size_t)b * npos + j) * nsl;
+      float M = -kInf;
+      uint32_t bi = 0xFFFFFFFFu, f = 0;
+      auto fold = [&](const int4 &r) {
+        const float v = __int_as_float(r.x);
+        f |= static_cast<uint32_t>(r.z);
+        if (v > M) {
+          M = v;
+          bi = static_cast<uint32_t>(r.y);
+        }
+      };
+      int sl = 0;
+      for (; sl + 4 <= nsl; sl += 4) {
+        int4 r[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) r[q] = *reinterpret_cast<const int4 *>(pp + sl + q);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) fold(r[q]);
+      }
+      for (; sl < nsl; ++sl) fold(*reinterpret_cast<const int4 *>(pp + sl));
+      if (M == kInf) f |= F_NONFINITE;
+      else if (M == -kInf) f |= F_EMPTY;
+      mx_s[j] = M;
+      top_s[j] = bi == 0xFFFFFFFFu ? -1 : static_cast<int>(bi);
       fl_s[j] = f;
     }
   }
