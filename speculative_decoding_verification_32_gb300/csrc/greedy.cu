@@ -117,11 +117,11 @@ __device__ __forceinline__ bool margin_promotes(float l_d, float l_top, float T,
 
 // Chain walk: draft j is kept iff it is position j's argmax (or promoted by
 // the margin rule); the first miss emits that position's argmax, a full pass
-// the bonus argmax.  mx_s / top_s / fl_s hold the combined positions.
+// the bonus argmax.  mx_s / top_s / fl_s hold the combined positions, lg_s
+// the draft token's logit at each position (loaded for the margin rule).
 template <bool BF16>
 __device__ void walk_greedy_chain(const GreedyParams &P, int b, int lane, const float *mx_s,
-                                  const int *top_s, const uint32_t *fl_s) {
-  using F = GFmt<BF16>;
+                                  const int *top_s, const uint32_t *fl_s, const float *lg_s) {
   const int npos = P.npos, K = npos - 1, V = P.V;
   uint32_t flags = 0;
   float T = 1.0f;
@@ -144,9 +144,7 @@ __device__ void walk_greedy_chain(const GreedyParams &P, int b, int lane, const 
           flags |= F_BAD_TOKEN;
           ok = 0;
         } else if (y != top) {
-          ok = P.use_margin && !f &&
-               margin_promotes(F::load_logit(P.target, ((size_t)b * npos + j) * V + y), mx, T,
-                               P.ln_kappa);
+          ok = P.use_margin && !f && margin_promotes(lg_s[j], mx, T, P.ln_kappa);
         }
       }
     }
@@ -175,11 +173,11 @@ __device__ void walk_greedy_chain(const GreedyParams &P, int b, int lane, const 
 // Tree walk: node i >= 1 is accepted iff its parent is accepted and its token
 // is the parent's argmax (or promoted by the margin rule); keep the deepest
 // accepted node, lowest index on ties.  mx_s / top_s / fl_s hold the combined
-// nodes; `scr` is shared scratch of 12 bytes per node.
+// nodes, lg_s each node's token logit at its parent (for the margin rule);
+// `scr` is shared scratch of 12 bytes per node.
 template <bool BF16>
 __device__ void walk_tree(const GreedyParams &P, int b, int lane, const float *mx_s, const int *top_s,
-                          const uint32_t *fl_s, unsigned char *scr, int *shared_best) {
-  using F = GFmt<BF16>;
+                          const uint32_t *fl_s, const float *lg_s, unsigned char *scr, int *shared_best) {
   const int N = P.npos, V = P.V;
   int *par_s = reinterpret_cast<int *>(scr);
   int *path_s = par_s + N;
@@ -212,10 +210,7 @@ __device__ void walk_tree(const GreedyParams &P, int b, int lane, const float *m
       int ok = 1;
       if (i > 0) {
         const int pa = par_s[i], t = __ldg(tok_g + i);
-        ok = t == top_s[pa] ||
-             (P.use_margin &&
-              margin_promotes(F::load_logit(P.target, ((size_t)b * N + pa) * V + t), mx_s[pa], T,
-                              P.ln_kappa));
+        ok = t == top_s[pa] || (P.use_margin && margin_promotes(lg_s[i], mx_s[pa], T, P.ln_kappa));
       }
       ok_s[i] = static_cast<unsigned char>(ok);
     }
@@ -344,15 +339,36 @@ __global__ void __launch_bounds__(kGreedyThreads) greedy_kernel(const __grid_con
 // (programmatic dependent launch).
 template <bool BF16>
 __global__ void __launch_bounds__(kWalkThreads) greedy_walk_kernel(const __grid_constant__ GreedyParams P) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  using F = GFmt<BF16>;
   extern __shared__ __align__(16) unsigned char wsm[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int b = blockIdx.x;
-  const int npos = P.npos;
+  const int npos = P.npos, V = P.V;
   int *best = reinterpret_cast<int *>(wsm);
   float *mx_s = reinterpret_cast<float *>(wsm + 16);
   int *top_s = reinterpret_cast<int *>(mx_s + npos);
   uint32_t *fl_s = reinterpret_cast<uint32_t *>(top_s + npos);
+  float *lg_s = reinterpret_cast<float *>(fl_s + npos);
+  // The margin rule's logits -- each draft token's (chain) or each node's
+  // token at its parent (tree) -- are inputs the streaming kernel never
+  // writes: load them before the dependency wait, so they arrive while the
+  // stream finishes.  Out-of-range parents and tokens load nothing (the walk
+  // flags the row).
+  if (P.use_margin) {
+    for (int i = threadIdx.x; i < npos; i += kWalkThreads) {
+      float l = 0.f;
+      if (P.tree) {
+        const int pa = i > 0 ? __ldg(P.parent + (size_t)b * npos + i) : -1;
+        const int t = i > 0 ? __ldg(P.tokens + (size_t)b * npos + i) : -1;
+        if (pa >= 0 && pa < i && t >= 0 && t < V) l = F::load_logit(P.target, ((size_t)b * npos + pa) * V + t);
+      } else if (i < npos - 1) {
+        const int y = __ldg(P.tokens + (size_t)b * (npos - 1) + i);
+        if (y >= 0 && y < V) l = F::load_logit(P.target, ((size_t)b * npos + i) * V + y);
+      }
+      lg_s[i] = l;
+    }
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // Each position's (max, lowest argmax, flags) from its slice partials, by
   // whichever mapping takes fewer dependent rounds of loads: a warp per
   // position (lanes over the slices; few positions with many slices, as in a
@@ -407,8 +423,8 @@ __global__ void __launch_bounds__(kWalkThreads) greedy_walk_kernel(const __grid_
   }
   __syncthreads();
   if (warp != 0) return;
-  if (P.tree) walk_tree<BF16>(P, b, lane, mx_s, top_s, fl_s, reinterpret_cast<unsigned char *>(fl_s + npos), best);
-  else walk_greedy_chain<BF16>(P, b, lane, mx_s, top_s, fl_s);
+  if (P.tree) walk_tree<BF16>(P, b, lane, mx_s, top_s, fl_s, lg_s, reinterpret_cast<unsigned char *>(lg_s + npos), best);
+  else walk_greedy_chain<BF16>(P, b, lane, mx_s, top_s, fl_s, lg_s);
 }
 
 template <bool BF16, bool VEC>
@@ -423,12 +439,12 @@ cudaError_t launch_greedy(const GreedyParams &p, bool bf16, int grid, cudaStream
   else p.vec ? launch_stream<false, true>(p, grid, s) : launch_stream<false, false>(p, grid, s);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // walk: 16 bytes + 12 per position for the combined positions, and 12 more
-  // per node for the tree walk's scratch
+  // walk: 16 bytes + 16 per position for the combined positions and the
+  // margin logits, and 12 more per node for the tree walk's scratch
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.B));
   cfg.blockDim = dim3(kWalkThreads);
-  cfg.dynamicSmemBytes = 16 + static_cast<size_t>(p.npos) * (p.tree ? 24 : 12);
+  cfg.dynamicSmemBytes = 16 + static_cast<size_t>(p.npos) * (p.tree ? 28 : 16);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
