@@ -85,6 +85,27 @@ def test_tree_bad_inputs(sv):
     check_tree(g, o)
 
 
+def test_tree_nonfinite_and_cross_slice_ties(sv):
+    """The walk kernel's thread-per-node combine (60 nodes): a NaN, a +inf and
+    a node with no finite logit flag their rows; equal maxima in the first and
+    last vocabulary slices resolve to the lower index."""
+    inp = S.make("c4", B=6, V=9000)
+    t = S.as_float32(inp["target"]).copy()
+    t[1, 7, 4000] = np.nan
+    t[2, 3, 8999] = np.inf
+    t[3, 11, :] = -np.inf
+    t[4, 20, 100] = t[4, 20].max() + 1
+    t[4, 20, 8990] = t[4, 20, 100]
+    t[5, 0, 9] = t[5, 0].max() + 1  # root: argmax at the first slice's start...
+    t[5, 0, 8999] = t[5, 0, 9]      # ...tied at the last slice's end
+    target = S.f32_to_bf16_bits(t)
+    for kappa in (0.0, 0.3):
+        g = run_tree(sv, dict(target=target, parent=inp["parent"], node_tokens=inp["node_tokens"]), kappa)
+        o = O.verify_tree(target, inp["parent"], inp["node_tokens"], kappa=kappa)
+        assert list(o["row_status"]) == [0, 1, 1, 5, 0, 0]
+        check_tree(g, o)
+
+
 def test_single_node_tree(sv):
     inp = S.make("c4", B=3, N=1, V=2000)
     g = run_tree(sv, inp, 0.3)
