@@ -46,8 +46,9 @@
  *    passing the same `ws_bytes` for the same buffer.  Calls on one stream
  *    may share a workspace; calls that may overlap in time (different
  *    streams) need separate workspaces.
- *  - Each verify call enqueues a streaming kernel and a small per-row kernel
- *    that starts early and waits for it on the device (programmatic dependent
+ *  - Each verify call enqueues a streaming kernel (for a truncated verify,
+ *    the per-logit-row truncation kernel) and a small per-row kernel that
+ *    starts early and waits for it on the device (programmatic dependent
  *    launch); the stochastic calls first enqueue a one-thread kernel that
  *    advances the workspace's generation count and clears its work counter.
  *  - Logits are bf16 (SPEC_BF16) or fp32 (SPEC_F32).  Rows whose byte
@@ -419,10 +420,12 @@ const char *spec_status_string(spec_status s);
  * asynchronous copy or on another block's record gives up after this many
  * nanoseconds (default 1e9 = 1 s), marks the rows it served SPEC_ROW_TIMEOUT
  * and lets the kernel finish.  The greedy and tree kernels stream with plain
- * loads and never wait.  Process-wide
- * setting, read at each launch.  spec_debug_force_wait_timeout(1) makes every
- * kernel additionally wait on a barrier that nothing completes, so the give-up
- * path can be tested on a healthy GPU; 0 turns it off.
+ * loads and never wait.  Process-wide setting, read at each launch.
+ * spec_debug_force_wait_timeout(1) tests the give-up path on a healthy GPU:
+ * the bulk-copy stream waits on a barrier that nothing completes, and the
+ * truncation and DRIFT kernels withhold their records, so every reader gives
+ * up (or finds a record missing) and its rows report SPEC_ROW_TIMEOUT; 0
+ * turns it off.
  */
 void spec_set_wait_timeout_ns(uint64_t ns);
 uint64_t spec_get_wait_timeout_ns(void);
