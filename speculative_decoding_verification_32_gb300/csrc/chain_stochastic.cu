@@ -989,8 +989,9 @@ __global__ void __launch_bounds__(kResolveThreads, kResolveBlocksPerSm) chain_re
   const uint32_t tflags = (T > 0.f && T < kInf) ? 0u : F_BAD_TEMPERATURE;
   const float s2 = tflags ? 1.f : __fdiv_rn(kLog2e, T);
 
-  // The logits are inputs the stream kernel never writes, so the rows where
-  // walks most often stop (position 0) can be pulled into L2 before waiting.
+  // The logits are inputs the kernel before this one (the stream, or the
+  // truncation kernel) never writes, so the rows where walks most often stop
+  // (position 0) can be pulled into L2 before waiting.
   if (tid == 0 && P.use_tma) {
     const int s0p = crank * P.L;
     const int lenp = max(0, min(V, s0p + P.L) - s0p);
@@ -1002,16 +1003,17 @@ __global__ void __launch_bounds__(kResolveThreads, kResolveBlocksPerSm) chain_re
                          static_cast<uint32_t>(lenp) * ESZ);
     }
   }
-  // Block 0 waits for the stream kernel on its way out, so this grid never
-  // completes before the one it depends on.
+  // Block 0 waits for the kernel before this one on its way out, so this
+  // grid never completes before the one it depends on.
   auto join_stream = [&]() {
     if (blockIdx.x == 0 && tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
   };
-  // Rank 0 of the cluster polls the row's partial records until every one
-  // carries this call's tag -- the stream kernel stamps them as it goes, so
-  // a row is resolved as soon as its own tiles are done, not when the whole
-  // stream is -- folds them and takes the walk's decisions.  The other CTAs
-  // read those decisions after one cluster barrier.
+  // Rank 0 of the cluster polls the row's partial records (and, when
+  // truncated, its truncation records) until every one carries this call's
+  // tag -- the kernel before this one stamps them as it goes, so a row is
+  // resolved as soon as its own records are in, not when that whole grid is
+  // done -- folds them and takes the walk's decisions.  The other CTAs read
+  // those decisions after one cluster barrier.
   if (crank == 0) {
     const RowScalars first = load_scalars(P, b, lane);
     const uint32_t tag = *reinterpret_cast<volatile const uint32_t *>(P.gen);
