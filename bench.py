@@ -62,7 +62,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="chain",
                     choices=["chain", "kv_compact", "policy", "drift", "truncated", "tree",
-                             "chain_c5", "greedy"],
+                             "chain_c5", "greedy", "rollback"],
                     help="chain: the headline verify step (default); kv_compact / policy: "
                          "the post-verification entry points")
     ap.add_argument("--sets", type=int, default=0,
@@ -614,6 +614,35 @@ def run_next(args):
                                        "each row between them) + drift_status_kernel",
                              "algorithmic_bytes_per_launch": alg, "traffic": DRIFT_TRAFFIC},
                 "gpu_launches": 4 * n, "clocks": clocks}
+    elif args.workload == "rollback":
+        # committed KV lengths for 4096 rows of up to 9 emitted tokens (K = 8),
+        # with an EOS id and per-row length limits
+        B, E = 4096, 9
+        rng = np.random.default_rng(4)
+        acc_h = rng.integers(0, E, B).astype(np.int32)
+        kvl = torch.from_numpy(rng.integers(100, 4000, B).astype(np.int32)).to(dev)
+        acc = torch.from_numpy(acc_h).to(dev)
+        nem = torch.from_numpy(acc_h + 1).to(dev)
+        toks_h = rng.integers(0, 32000, (B, E)).astype(np.int32)
+        toks_h[rng.random((B, E)) < 0.02] = 2  # an EOS now and then
+        toks = torch.from_numpy(toks_h).to(dev)
+        mlen = torch.from_numpy(rng.integers(150, 4100, B).astype(np.int32)).to(dev)
+
+        def step(i):
+            sv.spec_rollback_lengths(kvl, acc, nem, toks, eos_id=2, max_len=mlen, stream=stream)
+        sampler.start()
+        time.sleep(0.3)
+        ms, n, w = _time_graph(torch, stream, step, 8, steps, warmup)
+        clocks = sampler.stop()
+        line = {"metric": "KV rollback length steps per second", "workload": "rollback",
+                "value": 1e3 / ms, "unit": "rollback steps/s", "n_gpus": 1, "steps": n,
+                "warmup": w, "ms_per_step": ms, "higher_is_better": True, "dtype": "int32",
+                "data": "synthetic",
+                "config": {"workload": f"{B} rows of up to {E} emitted tokens, EOS and max_len"},
+                "roofline": {"bound": "latency", "achieved": None, "peak": None,
+                             "kernel": "rollback_kernel",
+                             "note": "one thread per row; launch and latency bound"},
+                "gpu_launches": n, "clocks": clocks}
     else:
         B = 4096
         rng = np.random.default_rng(3)
