@@ -174,16 +174,17 @@ __device__ void walk_greedy_chain(const GreedyParams &P, int b, int lane, const 
 // is the parent's argmax (or promoted by the margin rule); keep the deepest
 // accepted node, lowest index on ties.  mx_s / top_s / fl_s hold the combined
 // nodes, lg_s each node's token logit at its parent (for the margin rule);
-// `scr` is shared scratch of 12 bytes per node.
+// `scr` is shared scratch of 20 bytes per node.
 template <bool BF16>
 __device__ void walk_tree(const GreedyParams &P, int b, int lane, const float *mx_s, const int *top_s,
                           const uint32_t *fl_s, const float *lg_s, unsigned char *scr, int *shared_best) {
   const int N = P.npos, V = P.V;
   int *par_s = reinterpret_cast<int *>(scr);
   int *path_s = par_s + N;
-  short *dep_s = reinterpret_cast<short *>(path_s + N);
-  unsigned char *ok_s = reinterpret_cast<unsigned char *>(dep_s + N);
-  unsigned char *acc_s = ok_s + N;
+  short *anc_s[2] = {reinterpret_cast<short *>(path_s + N), reinterpret_cast<short *>(path_s + N) + N};
+  short *dep_s[2] = {anc_s[1] + N, anc_s[1] + 2 * N};
+  unsigned char *ok_s = reinterpret_cast<unsigned char *>(dep_s[1] + N);
+  unsigned char *acc_s[2] = {ok_s + N, ok_s + 2 * N};
   const int32_t *par_g = P.parent + (size_t)b * N;
   const int32_t *tok_g = P.tokens + (size_t)b * N;
 
@@ -215,17 +216,40 @@ __device__ void walk_tree(const GreedyParams &P, int b, int lane, const float *m
       ok_s[i] = static_cast<unsigned char>(ok);
     }
     __syncwarp();
-    if (lane == 0) {
-      acc_s[0] = 1;
-      dep_s[0] = 0;
-      int best = 0;
-      for (int i = 1; i < N; ++i) {
-        const int pa = par_s[i];
-        acc_s[i] = acc_s[pa] & ok_s[i];
-        dep_s[i] = static_cast<short>(dep_s[pa] + 1);
-        if (acc_s[i] && dep_s[i] > dep_s[best]) best = i;
+    // Pointer jumping over the parent links: each round a node's link skips
+    // twice as far toward the root, its flag becomes the AND of ok over the
+    // path it spans and its depth the edges it spans (the root links to
+    // itself with depth 0 and flag 1).  When every link is the root, a node
+    // is accepted iff its whole root path is ok, and its depth is exact.
+    int cur = 0;
+    for (int i = lane; i < N; i += 32) {
+      anc_s[0][i] = static_cast<short>(par_s[i]);
+      dep_s[0][i] = static_cast<short>(i > 0 ? 1 : 0);
+      acc_s[0][i] = i > 0 ? ok_s[i] : 1;
+    }
+    __syncwarp();
+    for (int span = 1; span < N; span <<= 1) {
+      bool more = false;
+      for (int i = lane; i < N; i += 32) {
+        const int p = anc_s[cur][i];
+        const int pp = anc_s[cur][p];
+        acc_s[cur ^ 1][i] = acc_s[cur][i] & acc_s[cur][p];
+        dep_s[cur ^ 1][i] = static_cast<short>(dep_s[cur][i] + dep_s[cur][p]);
+        anc_s[cur ^ 1][i] = static_cast<short>(pp);
+        more |= pp != 0;
       }
-      const int d = dep_s[best];
+      cur ^= 1;
+      __syncwarp();
+      if (!__any_sync(FULL_MASK, more)) break;
+    }
+    // the deepest accepted node, lowest index on ties (node 0 always counts)
+    unsigned bk = 0;
+    for (int i = lane; i < N; i += 32)
+      if (acc_s[cur][i]) bk = max(bk, (static_cast<unsigned>(dep_s[cur][i]) << 16) | (0xFFFFu - i));
+    bk = __reduce_max_sync(FULL_MASK, bk);
+    if (lane == 0) {
+      const int best = static_cast<int>(0xFFFFu - (bk & 0xFFFFu));
+      const int d = static_cast<int>(bk >> 16);
       for (int n = best, k = d - 1; k >= 0; n = par_s[n], --k) path_s[k] = n;
       shared_best[0] = best;
       shared_best[1] = d;
@@ -440,11 +464,11 @@ cudaError_t launch_greedy(const GreedyParams &p, bool bf16, int grid, cudaStream
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // walk: 16 bytes + 16 per position for the combined positions and the
-  // margin logits, and 12 more per node for the tree walk's scratch
+  // margin logits, and 20 more per node for the tree walk's scratch
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.B));
   cfg.blockDim = dim3(kWalkThreads);
-  cfg.dynamicSmemBytes = 16 + static_cast<size_t>(p.npos) * (p.tree ? 28 : 16);
+  cfg.dynamicSmemBytes = 16 + static_cast<size_t>(p.npos) * (p.tree ? 36 : 16);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
