@@ -116,3 +116,52 @@ def test_tree_tie_rule_is_caught(tmp_path):
     toks = np.array([[0, 1, 1]], np.int32)  # two siblings with the same accepted token
     assert O.verify_tree(t, par, toks)["path_nodes"][0, 0] == 1
     assert O.verify_tree(t, par, toks, L=L)["path_nodes"][0, 0] == 2
+
+
+# ---------------------------------------------- band bookkeeping (row_margin)
+# The parity tests forgive a disagreement only where row_margin < 1e-5, so a
+# slip that inflates or shrinks these margins must fail a pin.
+
+def _split_row_margin(L, u_smp):
+    p, q = [0.1, 0.5, 0.4], [0.4, 0.3, 0.3]
+    tgt = np.stack([np.log(np.array(p)), np.log(np.array(p))]).astype(np.float32)[None]
+    drf = np.log(np.array(q)).astype(np.float32)[None, None]
+    out = O.verify_chain(tgt, drf, np.array([[0]], np.int32),
+                         u_accept=np.array([[0.5]], np.float32),
+                         u_sample=np.full((1, 2), u_smp, np.float32), L=L)
+    return out["row_margin"][0]
+
+
+def test_gap_far_edge_is_caught(tmp_path):
+    """The gap is the distance to the NEARER end of the chosen interval."""
+    L = _mutant(tmp_path, "gapmax", "double g = fmin(t - prev, c - t);",
+                "double g = fmax(t - prev, c - t);")
+    assert abs(_split_row_margin(None, 0.5) - 0.05 / 0.3) < 1e-7
+    assert abs(_split_row_margin(L, 0.5) - 0.05 / 0.3) > 1e-3
+
+
+def test_gap_not_relative_is_caught(tmp_path):
+    """The gap is measured relative to the total mass Z."""
+    L = _mutant(tmp_path, "gapabs", "*gap = total > 0.0 ? g / total : 0.0;",
+                "*gap = total > 0.0 ? g : 0.0;")
+    assert abs(_split_row_margin(L, 0.5) - 0.05 / 0.3) > 1e-3
+
+
+def test_accept_margin_against_raw_ratio_is_caught(tmp_path):
+    """The accept margin is taken against min(1, ratio), not the ratio."""
+    L = _mutant(tmp_path, "rawratio", "fabs((double)u - fmin(1.0, ratio))",
+                "fabs((double)u - ratio)")
+    p, q = [0.6, 0.3, 0.1], [0.2, 0.5, 0.3]
+    tgt = np.log(np.array([p, p])).astype(np.float32)[None]
+    drf = np.log(np.array(q)).astype(np.float32)[None, None]
+    kw = dict(u_accept=np.array([[0.75]], np.float32), u_sample=np.full((1, 2), 0.5, np.float32))
+    good = O.verify_chain(tgt, drf, np.array([[0]], np.int32), **kw)
+    bad = O.verify_chain(tgt, drf, np.array([[0]], np.int32), L=L, **kw)
+    assert abs(good["accept_margin"][0, 0] - 0.25) < 1e-7
+    assert abs(bad["accept_margin"][0, 0] - 0.25) > 1e-3
+
+
+def test_row_margin_without_the_draw_gap_is_caught(tmp_path):
+    """row_margin includes the gap of the draw at a rejection."""
+    L = _mutant(tmp_path, "nogap", "          if (gap < margin) margin = gap;\n", "")
+    assert abs(_split_row_margin(L, 0.5) - 0.05 / 0.3) > 1e-3

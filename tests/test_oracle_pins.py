@@ -406,3 +406,104 @@ def test_row_status_codes():
     t = np.zeros((1, 4, 8), np.float32)
     o = O.verify_tree(t, par, np.zeros((1, 4), np.int32))
     assert o["row_status"][0] == 4
+
+
+# ------------------------------------------------------- band bookkeeping pins
+# The parity tests forgive a GPU/oracle disagreement only where the oracle's
+# decision margin (row_margin) is below 1e-5, so these margins are pinned to
+# hand-computed values.  Inputs are log-probabilities in fp32, which moves
+# each probability by at most a few 1e-8; the uniforms are exact in fp32.
+
+def test_accept_margin_worked_example():
+    """Draft, Verify, and Correct -- 'Three possible next tokens': with
+    p = (.6, .3, .1) and q = (.2, .5, .3) the acceptance probabilities are
+    min(1, p/q) = (1, .6, 1/3).  The accept margin is |u - min(1, p/q)|,
+    worked out by hand for each (token, u) below."""
+    p, q = [0.6, 0.3, 0.1], [0.2, 0.5, 0.3]
+    #          y, u_accept, hand margin, accepted?
+    cases = [(0, 0.75, 0.25, True),      # ratio 3: min(1, 3) = 1
+             (0, 0.0, 1.0, True),
+             (1, 0.25, 0.35, True),      # ratio .6
+             (1, 0.875, 0.275, False),
+             (2, 0.5, 0.5 - 1 / 3, False),  # ratio 1/3
+             (2, 0.125, 1 / 3 - 0.125, True)]
+    y = [c[0] for c in cases]
+    ua = [c[1] for c in cases]
+    out = O.verify_chain(**_single_position(p, q, y, ua, [0.5] * len(cases)))
+    np.testing.assert_allclose(out["accept_margin"][:, 0], [c[2] for c in cases], atol=1e-7)
+    np.testing.assert_array_equal(out["accepted_len"] >= 1, [c[3] for c in cases])
+
+
+# residual spread over two tokens: p = (.1, .5, .4), q = (.4, .3, .3) gives
+# [p - q]+ = (0, .2, .1) with Z = .3 and running sums (0, .2, .3)
+SPLIT_P, SPLIT_Q = [0.1, 0.5, 0.4], [0.4, 0.3, 0.3]
+
+
+@pytest.mark.parametrize("u_smp,token,gap", [
+    # t = u * Z; the gap is the distance of t to the nearer end of the chosen
+    # token's interval, divided by Z
+    (0.5, 1, 0.05 / 0.3),     # t = .15 in (0, .2]: ends .15 and .05 away
+    (0.625, 1, 0.0125 / 0.3),  # t = .1875: .0125 below .2
+    (0.25, 1, 0.075 / 0.3),    # t = .075: .075 above 0
+    (0.75, 2, 0.025 / 0.3),    # t = .225 in (.2, .3]: .025 above .2
+    (0.875, 2, 0.0375 / 0.3),  # t = .2625: .0375 below .3
+])
+def test_residual_gap_split_example(u_smp, token, gap):
+    """Draft, Verify, and Correct -- 'Why the correction recovers the target';
+    why correcting a rejection is not resampling, section 2: the correction is
+    the inverse CDF of the residual at u * Z.  Position 0 rejects (y = 0,
+    ratio .25, u_accept .5: accept margin .25), so row_margin is the smaller of
+    .25 and the residual gap, both by hand."""
+    out = O.verify_chain(**_single_position(SPLIT_P, SPLIT_Q, [0], [0.5], [u_smp]))
+    assert out["accepted_len"][0] == 0
+    assert out["out_tokens"][0, 0] == token
+    np.testing.assert_allclose(out["resid_mass"][0, 0], 0.3, atol=1e-7)
+    np.testing.assert_allclose(out["accept_margin"][0, 0], 0.25, atol=1e-7)
+    np.testing.assert_allclose(out["row_margin"][0], min(0.25, gap), atol=1e-7)
+
+
+@pytest.mark.parametrize("delta,token", [(2e-7, 1), (-2e-7, 0), (6e-7, 1), (-6e-7, 0)])
+def test_bonus_draw_at_a_cdf_boundary(delta, token):
+    """A bonus draw (K = 0) from p = (.6, .3, .1) at u = .6 + delta lands
+    |delta| away from the boundary between tokens 0 and 1 (up to the fp32
+    rounding of the inputs, a few 1e-8), so row_margin is about |delta|: below
+    1e-6 here, inside the band that forgives a disagreement."""
+    p = [0.6, 0.3, 0.1]
+    tgt = log_probs(p)[None, None, :]
+    us = np.array([[0.6 + delta]], np.float32)
+    out = O.verify_chain(tgt, np.zeros((1, 0, 3), np.float32), np.zeros((1, 0), np.int32),
+                         u_accept=np.zeros((1, 0), np.float32), u_sample=us)
+    assert out["accepted_len"][0] == 0 and out["out_tokens"][0, 0] == token
+    assert abs(out["row_margin"][0] - abs(delta)) < 1e-7
+    assert out["row_margin"][0] < 1e-6
+
+
+def test_row_margin_is_the_smallest_margin_of_the_walk():
+    """Verify several proposed tokens in one target pass: the walk reads the
+    accept test of positions 0..stop and the draw at the stop; row_margin is
+    the least of those margins and ignores positions after the stop.
+    Position 0 (DVC example, y = 1, u = .5) accepts with margin .1; position 1
+    (split example, y = 0, u = .5) rejects with margin .25 and draws at u = .5
+    (gap 1/6); position 2 (y = 1, ratio .6, u = .59) would have margin .01 but
+    is never read."""
+    p0, q0 = [0.6, 0.3, 0.1], [0.2, 0.5, 0.3]
+    tgt = np.stack([log_probs(p0), log_probs(SPLIT_P), log_probs(p0), log_probs(p0)])[None]
+    drf = np.stack([log_probs(q0), log_probs(SPLIT_Q), log_probs(q0)])[None]
+    out = O.verify_chain(tgt, drf, np.array([[1, 0, 1]], np.int32),
+                         u_accept=np.array([[0.5, 0.5, 0.59]], np.float32),
+                         u_sample=np.full((1, 4), 0.5, np.float32))
+    assert out["accepted_len"][0] == 1 and list(out["out_tokens"][0, :2]) == [1, 1]
+    np.testing.assert_allclose(out["accept_margin"][0], [0.1, 0.25, 0.01], atol=1e-7)
+    np.testing.assert_allclose(out["row_margin"][0], 0.1, atol=1e-7)
+    # with position 0 at u = .3 (margin .3) the draw's gap 1/6 is the least
+    out = O.verify_chain(tgt, drf, np.array([[1, 0, 1]], np.int32),
+                         u_accept=np.array([[0.3, 0.5, 0.59]], np.float32),
+                         u_sample=np.full((1, 4), 0.5, np.float32))
+    np.testing.assert_allclose(out["row_margin"][0], 0.05 / 0.3, atol=1e-7)
+
+
+def test_row_margin_of_greedy_rows_is_infinite():
+    """Greedy verification takes no floating-point draw, so no band applies."""
+    t = log_probs([0.6, 0.3, 0.1])[None, None, :].repeat(2, axis=1)
+    out = O.verify_chain(t, None, np.array([[0]], np.int32), mode=O.GREEDY)
+    assert np.isinf(out["row_margin"][0])
