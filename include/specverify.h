@@ -41,8 +41,9 @@
  *    need no initialisation.  The stochastic chain calls keep a small header
  *    in the last 16 bytes of the `ws_bytes` they are given: a work counter,
  *    cleared before every call, and a generation count, advanced before
- *    every call and stamped on every record the call writes, so nothing an
- *    earlier call left behind is ever read, whatever its shapes.  Keep
+ *    every call (skipping 0, so zero-filled memory never looks current) and
+ *    stamped on every record the call writes, so nothing an earlier call
+ *    left behind is ever read, whatever its shapes.  Keep
  *    passing the same `ws_bytes` for the same buffer.  Calls on one stream
  *    may share a workspace; calls that may overlap in time (different
  *    streams) need separate workspaces.

@@ -2415,7 +2415,9 @@ cudaError_t prepare(int cluster) {
 // Advances the workspace's generation word (the call's tag) and clears the
 // stream's claim counter: one thread, a plain launch ahead of the stream.
 __global__ void advance_generation_kernel(uint32_t *gen, uint32_t *claim) {
-  *gen += 1u;
+  // the tag is never 0, so zero-filled memory never passes for a record
+  const uint32_t g = *gen + 1u;
+  *gen = g ? g : 1u;
   *claim = 0u;
 }
 

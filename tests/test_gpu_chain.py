@@ -244,7 +244,8 @@ def test_bounded_wait_gives_up_and_recovers(sv):
 @pytest.mark.parametrize("name", ["c2", "c3"])
 def test_workspace_first_use_and_reuse(sv, name):
     """Any workspace works, whatever it holds on its first call (zero-filled
-    or arbitrary contents).  Each call advances the generation word in the
+    or arbitrary contents, including a generation word about to wrap to 0).
+    Each call advances the generation word in the
     header (the second 4-byte word of the last 16 bytes of the size given,
     kept 16-byte aligned when that size is not a multiple of 16) and every
     call matches the oracle."""
@@ -263,7 +264,9 @@ def test_workspace_first_use_and_reuse(sv, name):
             g = chain_via_abi(L, inp, ws)
             compare_stochastic(g, o)
             now = int(ws[end - 12:end - 8].cpu().numpy().view(np.uint32)[0])
-            assert now == (gen + 1) % (1 << 32), (fill, call, gen, now)
+            # the generation skips 0, so zero-filled memory never carries a
+            # current stamp
+            assert now == ((gen + 1) % (1 << 32) or 1), (fill, call, gen, now)
             gen = now
 
 
