@@ -432,6 +432,23 @@ void spec_set_wait_timeout_ns(uint64_t ns);
 uint64_t spec_get_wait_timeout_ns(void);
 void spec_debug_force_wait_timeout(int on);
 
+#ifdef SV_BOUNDS
+/*
+ * Bounds-check builds only (the library compiled with -DSV_BOUNDS, e.g.
+ * libspecverify_bounds.so; the pages have no counterpart: a test aid that
+ * stands in for a memory checker).  Their chain and tree kernels check every
+ * computed global or shared-memory index before the access; a bad one is
+ * counted, the first one's source line kept, and the access skipped, never
+ * trapped (the row's outputs then come out wrong or flagged).
+ * spec_debug_bounds writes the count and that line of every kernel launched
+ * since its last call, then clears them; it returns the CUDA error of the
+ * reads (synchronous).  spec_debug_bounds_selftest enqueues one check that
+ * fails by design without touching memory, so the record can be seen to work.
+ */
+int spec_debug_bounds(unsigned *count, unsigned *line);
+int spec_debug_bounds_selftest(void *stream);
+#endif
+
 #ifdef __cplusplus
 }
 #endif

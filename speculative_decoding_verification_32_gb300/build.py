@@ -2,6 +2,11 @@
 
 Each .cu translation unit compiles in parallel, then nvcc links them into one
 shared library next to this file.  No cmake, no torch extension machinery.
+
+build(variant="bounds") makes libspecverify_bounds.so instead: the same
+sources with -DSV_BOUNDS, whose kernels check every computed index before
+the access and record the bad ones (read back with spec_debug_bounds); the
+GPU tests run their guard-region cases through it as well.
 """
 import os
 import subprocess
@@ -14,6 +19,9 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspecverify.so")
+VARIANTS = {None: (BUILD, LIB, []),
+            "bounds": (os.path.join(HERE, "_build_bounds"),
+                       os.path.join(HERE, "libspecverify_bounds.so"), ["-DSV_BOUNDS"])}
 SOURCES = ["api.cu", "chain_stochastic.cu", "greedy.cu", "rollback.cu", "kv_policy.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -32,23 +40,24 @@ def _deps():
     return files
 
 
-def build(force=False, verbose_ptxas=False):
+def build(force=False, verbose_ptxas=False, variant=None):
     """Compile and link; skip when the library is newer than every source."""
-    if not force and os.path.exists(LIB):
+    build_dir, lib, extra = VARIANTS[variant]
+    if not force and os.path.exists(lib):
         newest = max(os.path.getmtime(f) for f in _deps())
-        if os.path.getmtime(LIB) >= newest:
-            return LIB
-    os.makedirs(BUILD, exist_ok=True)
+        if os.path.getmtime(lib) >= newest:
+            return lib
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     flags = [*ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
-             "-I", INCLUDE, "-I", CSRC]
+             "-I", INCLUDE, "-I", CSRC, *extra]
     if verbose_ptxas:
         flags += ["-Xptxas", "-v"]
-    # extra nvcc flags for tuning builds (e.g. -DSV_FUSED_U=4)
+    # extra nvcc flags for measurement builds (e.g. -DSV_TIMELINE)
     flags += os.environ.get("SPECVERIFY_NVCC_FLAGS", "").split()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -61,11 +70,12 @@ def build(force=False, verbose_ptxas=False):
         for _, err in results:
             sys.stderr.write(err)
     objs = [o for o, _ in results]
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv,
+                variant="bounds" if "--bounds" in sys.argv else None))

@@ -562,4 +562,23 @@ void spec_set_wait_timeout_ns(uint64_t ns) { g_wait_ns.store(ns); }
 uint64_t spec_get_wait_timeout_ns(void) { return g_wait_ns.load(); }
 void spec_debug_force_wait_timeout(int on) { g_force_timeout.store(on ? 1 : 0); }
 
+#ifdef SV_BOUNDS
+// Bounds-check builds only (-DSV_BOUNDS): the number of bad indexes the
+// chain and tree kernels met since the last call, and the source line of the
+// first; both records are cleared.  Returns the CUDA error of the reads.
+int spec_debug_bounds(unsigned *count, unsigned *line) {
+  *count = 0u;
+  *line = 0u;
+  cudaError_t e = oob_record_chain(count, line);
+  if (e == cudaSuccess) e = oob_record_greedy(count, line);
+  return static_cast<int>(e);
+}
+
+// Bounds-check builds only: enqueue a check that fails by design, touching
+// no memory, so that a test can see the record work.
+int spec_debug_bounds_selftest(void *stream) {
+  return static_cast<int>(oob_selftest(static_cast<cudaStream_t>(stream)));
+}
+#endif
+
 }  // extern "C"

@@ -414,11 +414,11 @@ __device__ __forceinline__ TileInfo make_tile(const ChainStochParams &P, int gt,
   it.first = (gt == lo) || it.t == 0;
   it.last = (gt == hi - 1) || it.t == nt - 1;
   it.run0 = max(lo - (gt - it.t), 0);
-  float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
+  float T = P.temperature && SV_INB(b, B) ? __ldg(P.temperature + b) : 1.0f;
   if (!(T > 0.f && T < kInf)) T = 1.0f;  // the resolve kernel flags the row
   it.s2 = __fdiv_rn(kLog2e, T);
   it.yl = -1;
-  if (j < K && P.tokens) {
+  if (j < K && P.tokens && SV_INB((long long)b * K + j, (long long)B * K)) {
     const int y = __ldg(P.tokens + (size_t)b * K + j);
     if (y >= s0 && y < s0 + it.len) it.yl = y - s0;
   }
@@ -600,9 +600,13 @@ __global__ void __launch_bounds__(kSoftThreads + 32, 3) softmax_partials_kernel(
         const uint32_t bytes = static_cast<uint32_t>(it.len) * ESZ;
         const uint64_t pol = it.keep ? pol_normal : pol_first;
         mbar_arrive_expect_tx(&ctl.full[s], it.drow >= 0 ? 2 * bytes : bytes);  // release: info[s] too
-        bulk_g2s(smem + (size_t)s * P.buf_bytes, static_cast<const char *>(P.target) + it.tsrc,
-                 bytes, &ctl.full[s], pol);
-        if (it.drow >= 0)
+        // (bounds build: a copy out of range is skipped; its consumers time out)
+        if (SV_INR(it.tsrc, bytes, (long long)B * (K + 1) * P.V * ESZ) &&
+            SV_INR((long long)s * P.buf_bytes, bytes, (long long)S * P.buf_bytes))
+          bulk_g2s(smem + (size_t)s * P.buf_bytes, static_cast<const char *>(P.target) + it.tsrc,
+                   bytes, &ctl.full[s], pol);
+        if (it.drow >= 0 && SV_INR(it.dsrc, bytes, (long long)B * K * P.V * ESZ) &&
+            SV_INR((long long)s * P.buf_bytes + half, bytes, (long long)S * P.buf_bytes))
           bulk_g2s(smem + (size_t)s * P.buf_bytes + half,
                    static_cast<const char *>(P.draft) + it.dsrc, bytes, &ctl.full[s], pol);
       } else {
@@ -681,11 +685,28 @@ __global__ void __launch_bounds__(kSoftThreads + 32, 3) softmax_partials_kernel(
     const bool pair = it.drow >= 0;
     const unsigned char *sb = smem + (size_t)s * P.buf_bytes;
     const int nvec = (it.len + EPV - 1) / EPV;
+#ifdef SV_BOUNDS
+    // the tile's vectors in the stage, its elements in the logit tensors, its
+    // rows' records; the warp stops at a bad tile (its records stay
+    // unwritten and their rows time out)
+    {
+      const bool ok = SV_INB(s, kMaxStages) && SV_INR(it.tsrc / ESZ, it.len, (long long)B * (K + 1) * P.V) &&
+                      (!pair || SV_INR(it.dsrc / ESZ, it.len, (long long)B * K * P.V)) &&
+                      (!tma || SV_INR((long long)s * P.buf_bytes, (long long)nvec * 16 + (pair ? half : 0),
+                                      (long long)S * P.buf_bytes)) &&
+                      SV_INR((long long)it.trow * nt + it.run0, it.t - it.run0 + 1,
+                             (long long)(2 * K + 1) * B * nt) &&
+                      (!pair || SV_INR((long long)it.drow * nt + it.run0, it.t - it.run0 + 1,
+                                       (long long)(2 * K + 1) * B * nt));
+      if (!__all_sync(FULL_MASK, ok)) break;
+    }
+#endif
 
     const uint32_t sbase = smem0 + s * P.buf_bytes;
     uint32_t wp[NV * 4];
     load_tile<BF16, NV>(wp, tma, sbase, static_cast<const char *>(P.target) + it.tsrc, tid, nvec, it.len);
-    if (it.yl >= 0 && tid == 0) {  // the draft token's logits, if this tile holds them
+    if (it.yl >= 0 && tid == 0 && SV_INB(it.yl, it.len) && SV_INB(it.trow, (2 * K + 1) * B) &&
+        SV_INB(it.drow, (2 * K + 1) * B)) {  // the draft token's logits, if this tile holds them
       float a, c;
       if (tma) {
         const unsigned char *pv = sb + (size_t)it.yl * ESZ;
@@ -730,7 +751,7 @@ __global__ void __launch_bounds__(kSoftThreads + 32, 3) softmax_partials_kernel(
     if (warp_to) run_to = F_TIMEOUT;
     if (pair) tile_accumulate<BF16, NV>(wp, s2, tid, nvec, mq, sq);
 
-    if (it.last) {  // the run ends: fold the CTA's partials
+    if (it.last && SV_INB(runs % (2 * S), 2 * kMaxStages)) {  // the run ends: fold the CTA's partials
       const int slot = runs % (2 * S);
       ++runs;
       float Mpw, Spw, Mqw, Sqw;
@@ -825,15 +846,16 @@ __device__ bool fold_rows(const ChainStochParams &P, int b, float s2, uint32_t t
       const bool draft = r > K;
       const int j = draft ? r - npos : r;
       const int prow = draft ? P.B * npos + b * K + j : b * npos + j;
-      if (sub == 0 && trunc) {  // the row's truncation record
+      if (sub == 0 && trunc && SV_INB(prow, (long long)P.B * (npos + K))) {  // the row's truncation record
         float th, kp;
         uint32_t tf;
         ready &= load_part(P.trunc + prow, tag, &th, &kp, &tf);
       }
       if (sub == 0 && j < K) {
         // the draft token's logit: written only when the token is in range
-        const int y = P.tokens ? __ldg(P.tokens + (size_t)b * K + j) : -1;
-        if (y >= 0 && y < P.V) {
+        const int y = P.tokens && SV_INB((long long)b * K + j, (long long)P.B * K)
+                          ? __ldg(P.tokens + (size_t)b * K + j) : -1;
+        if (y >= 0 && y < P.V && SV_INB(prow, (long long)P.B * (npos + K))) {
           const unsigned long long w = ld_relaxed_u64(P.ylog + prow);
           yv = __uint_as_float(static_cast<uint32_t>(w));
           ready &= static_cast<uint32_t>(w >> 32) == tag;
@@ -842,6 +864,7 @@ __device__ bool fold_rows(const ChainStochParams &P, int b, float s2, uint32_t t
       for (int t = sub; t < nt; t += GS) {
         float qm, qs;
         uint32_t qf;
+        if (!SV_INB((long long)prow * nt + t, (long long)P.B * (npos + K) * nt)) continue;
         ready &= load_part(P.part + (size_t)prow * nt + t, tag, &qm, &qs, &qf);
         f |= qf;
         const float mn = fmax_nan(m, qm);
@@ -858,7 +881,7 @@ __device__ bool fold_rows(const ChainStochParams &P, int b, float s2, uint32_t t
       v += __shfl_xor_sync(FULL_MASK, v, o);
       f |= __shfl_xor_sync(FULL_MASK, f, o);
     }
-    if (sub == 0 && r < npos + K) rstat[r] = make_float4(M, v, yv, __uint_as_float(f));
+    if (sub == 0 && r < npos + K && SV_INB(r, npos + K)) rstat[r] = make_float4(M, v, yv, __uint_as_float(f));
   }
   return ready;
 }
@@ -877,8 +900,9 @@ struct RowScalars {
 __device__ __forceinline__ RowScalars load_scalars(const ChainStochParams &P, int b, int j) {
   RowScalars r = {0.f, 0.f, -1};
   const int K = P.K;
-  if (j <= K) r.us = __ldg(P.u_sample + (size_t)b * (K + 1) + j);
-  if (j < K) {
+  if (j <= K && SV_INB((long long)b * (K + 1) + j, (long long)P.B * (K + 1)))
+    r.us = __ldg(P.u_sample + (size_t)b * (K + 1) + j);
+  if (j < K && SV_INB((long long)b * K + j, (long long)P.B * K)) {
     r.y = __ldg(P.tokens + (size_t)b * K + j);
     r.ua = __ldg(P.u_accept + (size_t)b * K + j);
   }
@@ -906,7 +930,8 @@ __device__ void decide_row(const ChainStochParams &P, int b, float s2, uint32_t 
       if (!(us >= 0.f && us < 1.f)) flags |= F_BAD_UNIFORM;
       tp = rstat[j];
       flags |= __float_as_uint(tp.w);
-      if (trunc) {  // the kept mass replaces the full sum (records already checked)
+      if (trunc && SV_INB((long long)b * npos + j, (long long)P.B * (npos + K))) {
+        // the kept mass replaces the full sum (records already checked)
         float th, kp;
         uint32_t tf;
         load_part(P.trunc + (size_t)b * npos + j, 0u, &th, &kp, &tf);
@@ -923,7 +948,7 @@ __device__ void decide_row(const ChainStochParams &P, int b, float s2, uint32_t 
         if (y < 0 || y >= V) flags |= F_BAD_TOKEN;
         dq = rstat[npos + j];
         flags |= __float_as_uint(dq.w);
-        if (trunc) {
+        if (trunc && SV_INB((long long)P.B * npos + (long long)b * K + j, (long long)P.B * (npos + K))) {
           float th, kp;
           uint32_t tf;
           load_part(P.trunc + (size_t)P.B * npos + (size_t)b * K + j, 0u, &th, &kp, &tf);
@@ -941,7 +966,7 @@ __device__ void decide_row(const ChainStochParams &P, int b, float s2, uint32_t 
                         : __fadd_rn(__fmaf_rn(dq.z, s2, -__fmul_rn(dq.x, s2)), -lg2(dq.y));
         const float l2r = __fadd_rn(l2p, -l2q);
         rejects = !((l2r >= 0.f) || (ua < ex2(l2r)));
-        if (diag) {
+        if (diag && SV_INB((long long)b * K + j, (long long)P.B * K)) {
           const size_t d = (size_t)b * K + j;
           if (P.p_at_draft) P.p_at_draft[d] = ex2(l2p);
           if (P.q_at_draft) P.q_at_draft[d] = ex2(l2q);
@@ -965,7 +990,7 @@ __device__ void decide_row(const ChainStochParams &P, int b, float s2, uint32_t 
   flags = __reduce_or_sync(FULL_MASK, flags);
   if (diag && P.resid_mass)
     for (int j = lane; j < K; j += 32)
-      if (j != stop) P.resid_mass[(size_t)b * K + j] = 0.f;
+      if (j != stop && SV_INB((long long)b * K + j, (long long)P.B * K)) P.resid_mass[(size_t)b * K + j] = 0.f;
   if (lane == 0) {
     ctl.stop = stop;
     ctl.flags = flags;
@@ -1044,7 +1069,7 @@ __global__ void __launch_bounds__(kResolveThreads, kResolveBlocksPerSm) chain_re
   const uint32_t flags = ctl.flags;
   const int stop = ctl.stop;
   if (flags) {  // rank 0's decision: every CTA of the cluster leaves here
-    if (crank == 0 && warp == 0) {
+    if (crank == 0 && warp == 0 && SV_INB(b, P.B)) {
       for (int j = lane; j < npos; j += 32) P.out_tokens[(size_t)b * npos + j] = -1;
       if (lane == 0) {
         P.accepted_len[b] = -1;
@@ -1062,7 +1087,16 @@ __global__ void __launch_bounds__(kResolveThreads, kResolveBlocksPerSm) chain_re
   const float2 s2v = make_float2(s2, s2), nMpv = make_float2(nMp, nMp), nMqv = make_float2(nMq, nMq);
   const float2 iSpv = make_float2(iSp, iSp), niSqv = make_float2(-iSq, -iSq);
   const int s0 = crank * P.L;
-  const int len = max(0, min(V, s0 + P.L) - s0);
+  const int len = [&] {
+    const int l = max(0, min(V, s0 + P.L) - s0);
+    // bounds build: the stopping position's slice of this CTA must lie in
+    // the logit tensors, else the CTA reads nothing (the row comes out wrong)
+    if (!(SV_INB(b, P.B) && SV_INB(stop, npos) &&
+          SV_INR((long long)(b * npos + stop) * V + s0, l, (long long)P.B * npos * V) &&
+          (stop == K || SV_INR((long long)(b * K + stop) * V + s0, l, (long long)P.B * K * V))))
+      return 0;
+    return l;
+  }();
   const int nr = P.vpw / 32;  // rounds of 32 vectors per warp
   const int vbase = warp * P.vpw;
   const bool aligned = P.use_tma != 0;
@@ -1284,11 +1318,11 @@ __global__ void __launch_bounds__(kResolveThreads, kResolveBlocksPerSm) chain_re
         token = __shfl_sync(FULL_MASK, pos, ls);
       }
       // ---- the row's outputs
-      for (int j = lane; j < npos; j += 32) {
+      for (int j = lane; j < npos && SV_INB(b, P.B); j += 32) {
         const int o = j < stop ? __ldg(P.tokens + (size_t)b * K + j) : (j == stop ? token : -1);
         P.out_tokens[(size_t)b * npos + j] = o;
       }
-      if (lane == 0) {
+      if (lane == 0 && SV_INB(b, P.B)) {
         P.accepted_len[b] = stop;
         P.num_emitted[b] = stop + 1;
         P.row_status[b] = 0;
@@ -2527,6 +2561,19 @@ cudaError_t launch_drift_t(const ChainStochParams &p, int grid, cudaStream_t s) 
 }
 
 }  // namespace
+
+#ifdef SV_BOUNDS
+SV_OOB_READER(oob_record_chain)
+
+// The checker's own check: one thread tests index 5 against an extent of 3
+// (nothing is read or written there), which must leave one record.
+__global__ void oob_selftest_kernel() { (void)SV_INB(5, 3); }
+
+cudaError_t oob_selftest(cudaStream_t s) {
+  oob_selftest_kernel<<<1, 1, 0, s>>>();
+  return cudaGetLastError();
+}
+#endif
 
 cudaError_t launch_chain_stochastic(const ChainStochParams &p, bool bf16, int grid, size_t smem,
                                     int cluster, cudaStream_t s) {

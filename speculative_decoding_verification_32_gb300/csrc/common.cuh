@@ -28,6 +28,42 @@ __host__ __device__ inline int lowest_code(uint32_t flags) {
   return 0;
 }
 
+// ------------------------------------------------------------- bounds checks
+// A measurement and test aid: built with -DSV_BOUNDS, the kernels check every
+// computed global or shared-memory index (SV_INB: 0 <= i < n; SV_INR: the
+// range [i, i + len) inside [0, n)) before the access.  A bad index is
+// counted, the first one's source line kept, and the access skipped: nothing
+// traps, and the row comes out wrong or flagged instead.  Each translation
+// unit keeps its own record (g_sv_oob: {count, first line}); the library's
+// spec_debug_bounds reads and clears them all.  In the default build both
+// macros are the constant true.
+#ifdef SV_BOUNDS
+static __device__ unsigned int g_sv_oob[2];
+__device__ __forceinline__ bool sv_in_bounds(long long i, long long len, long long n, int line) {
+  if (i >= 0 && len >= 0 && i + len <= n) return true;
+  if (atomicAdd(&g_sv_oob[0], 1u) == 0u) g_sv_oob[1] = static_cast<unsigned>(line);
+  return false;
+}
+#define SV_INB(i, n) ::sv::sv_in_bounds(static_cast<long long>(i), 1LL, static_cast<long long>(n), __LINE__)
+#define SV_INR(i, len, n)                                                                     \
+  ::sv::sv_in_bounds(static_cast<long long>(i), static_cast<long long>(len), static_cast<long long>(n), \
+                     __LINE__)
+// host side: this unit's record, then cleared
+#define SV_OOB_READER(fn)                                                       \
+  cudaError_t fn(unsigned *count, unsigned *line) {                             \
+    unsigned h[2] = {0u, 0u};                                                   \
+    cudaError_t e = cudaMemcpyFromSymbol(h, g_sv_oob, sizeof(h));               \
+    if (e != cudaSuccess) return e;                                             \
+    *count += h[0];                                                             \
+    if (!*line) *line = h[1];                                                   \
+    const unsigned z[2] = {0u, 0u};                                             \
+    return cudaMemcpyToSymbol(g_sv_oob, z, sizeof(z));                          \
+  }
+#else
+#define SV_INB(i, n) true
+#define SV_INR(i, len, n) true
+#endif
+
 // ------------------------------------------------------------ shared memory
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -138,7 +138,7 @@ __device__ void walk_greedy_chain(const GreedyParams &P, int b, int lane, const 
       const uint32_t f = fl_s[j];
       top = top_s[j];
       flags |= f;
-      if (j < K) {
+      if (j < K && SV_INB((long long)b * K + j, (long long)P.B * K)) {
         const int y = __ldg(P.tokens + (size_t)b * K + j);
         if (y < 0 || y >= V) {
           flags |= F_BAD_TOKEN;
@@ -158,7 +158,7 @@ __device__ void walk_greedy_chain(const GreedyParams &P, int b, int lane, const 
   }
   flags = __reduce_or_sync(FULL_MASK, flags);
   const int tok = stop == K ? last_top : stop_top;
-  for (int j = lane; j < npos; j += 32) {
+  for (int j = lane; j < npos && SV_INB(b, P.B); j += 32) {
     int o = -1;
     if (!flags) o = j < stop ? __ldg(P.tokens + (size_t)b * K + j) : (j == stop ? tok : -1);
     P.out_tokens[(size_t)b * npos + j] = o;
@@ -211,7 +211,8 @@ __device__ void walk_tree(const GreedyParams &P, int b, int lane, const float *m
       int ok = 1;
       if (i > 0) {
         const int pa = par_s[i], t = __ldg(tok_g + i);
-        ok = t == top_s[pa] || (P.use_margin && margin_promotes(lg_s[i], mx_s[pa], T, P.ln_kappa));
+        ok = SV_INB(pa, N) &&
+             (t == top_s[pa] || (P.use_margin && margin_promotes(lg_s[i], mx_s[pa], T, P.ln_kappa)));
       }
       ok_s[i] = static_cast<unsigned char>(ok);
     }
@@ -231,8 +232,8 @@ __device__ void walk_tree(const GreedyParams &P, int b, int lane, const float *m
     for (int span = 1; span < N; span <<= 1) {
       bool more = false;
       for (int i = lane; i < N; i += 32) {
-        const int p = anc_s[cur][i];
-        const int pp = anc_s[cur][p];
+        const int p = SV_INB(anc_s[cur][i], N) ? anc_s[cur][i] : 0;
+        const int pp = SV_INB(anc_s[cur][p], N) ? anc_s[cur][p] : 0;
         acc_s[cur ^ 1][i] = acc_s[cur][i] & acc_s[cur][p];
         dep_s[cur ^ 1][i] = static_cast<short>(dep_s[cur][i] + dep_s[cur][p]);
         anc_s[cur ^ 1][i] = static_cast<short>(pp);
@@ -250,7 +251,7 @@ __device__ void walk_tree(const GreedyParams &P, int b, int lane, const float *m
     if (lane == 0) {
       const int best = static_cast<int>(0xFFFFu - (bk & 0xFFFFu));
       const int d = static_cast<int>(bk >> 16);
-      for (int n = best, k = d - 1; k >= 0; n = par_s[n], --k) path_s[k] = n;
+      for (int n = best, k = d - 1; k >= 0 && SV_INB(n, N) && SV_INB(k, N); n = par_s[n], --k) path_s[k] = n;
       shared_best[0] = best;
       shared_best[1] = d;
     }
@@ -263,9 +264,9 @@ __device__ void walk_tree(const GreedyParams &P, int b, int lane, const float *m
     if (!flags) {
       if (i < d) {
         pn = path_s[i];
-        ot = __ldg(tok_g + pn);
+        ot = SV_INB(pn, N) ? __ldg(tok_g + pn) : -1;
       } else if (i == d) {
-        ot = top_s[best];
+        ot = SV_INB(best, N) ? top_s[best] : -1;
       }
     }
     P.path_nodes[(size_t)b * N + i] = pn;
@@ -304,6 +305,13 @@ __global__ void __launch_bounds__(kGreedyThreads) greedy_kernel(const __grid_con
     const int len = min(V - s0, P.slice);
     const int nvec = (len + EPV - 1) / EPV;
     const char *src = static_cast<const char *>(P.target) + ((size_t)pos * V + s0) * ESZ;
+#ifdef SV_BOUNDS
+    // the item's elements in the logits and its partial record; a bad item
+    // is skipped (its row reads an old partial)
+    if (!__all_sync(FULL_MASK, SV_INR((long long)pos * V + s0, len, (long long)P.B * P.npos * V) &&
+                                   SV_INB(it, W)))
+      continue;
+#endif
     float best = -kInf, nan_acc = -kInf;
     int bv = -1;
     uint32_t wb[4] = {0u, 0u, 0u, 0u};
@@ -382,12 +390,16 @@ __global__ void __launch_bounds__(kWalkThreads) greedy_walk_kernel(const __grid_
     for (int i = threadIdx.x; i < npos; i += kWalkThreads) {
       float l = 0.f;
       if (P.tree) {
-        const int pa = i > 0 ? __ldg(P.parent + (size_t)b * npos + i) : -1;
-        const int t = i > 0 ? __ldg(P.tokens + (size_t)b * npos + i) : -1;
-        if (pa >= 0 && pa < i && t >= 0 && t < V) l = F::load_logit(P.target, ((size_t)b * npos + pa) * V + t);
-      } else if (i < npos - 1) {
+        const bool in = SV_INB((long long)b * npos + i, (long long)P.B * npos);
+        const int pa = i > 0 && in ? __ldg(P.parent + (size_t)b * npos + i) : -1;
+        const int t = i > 0 && in ? __ldg(P.tokens + (size_t)b * npos + i) : -1;
+        if (pa >= 0 && pa < i && t >= 0 && t < V &&
+            SV_INB(((long long)b * npos + pa) * V + t, (long long)P.B * npos * V))
+          l = F::load_logit(P.target, ((size_t)b * npos + pa) * V + t);
+      } else if (i < npos - 1 && SV_INB((long long)b * (npos - 1) + i, (long long)P.B * (npos - 1))) {
         const int y = __ldg(P.tokens + (size_t)b * (npos - 1) + i);
-        if (y >= 0 && y < V) l = F::load_logit(P.target, ((size_t)b * npos + i) * V + y);
+        if (y >= 0 && y < V && SV_INB(((long long)b * npos + i) * V + y, (long long)P.B * npos * V))
+          l = F::load_logit(P.target, ((size_t)b * npos + i) * V + y);
       }
       lg_s[i] = l;
     }
@@ -407,6 +419,7 @@ __global__ void __launch_bounds__(kWalkThreads) greedy_walk_kernel(const __grid_
       float mx;
       int top;
       uint32_t f;
+      if (!SV_INR(((long long)b * npos + j) * nsl, nsl, (long long)P.B * npos * nsl)) continue;
       combine_position(P.part + ((size_t)b * npos + j) * nsl, nsl, lane, &mx, &top, &f);
       if (lane == 0) {
         mx_s[j] = mx;
@@ -418,6 +431,7 @@ __global__ void __launch_bounds__(kWalkThreads) greedy_walk_kernel(const __grid_
     // in vocabulary order, a later slice replacing only on a strictly larger
     // value
     for (int j = threadIdx.x; j < npos; j += kWalkThreads) {
+      if (!SV_INR(((long long)b * npos + j) * nsl, nsl, (long long)P.B * npos * nsl)) continue;
       const GreedyPart *pp = P.part + ((size_t)b * npos + j) * nsl;
       float M = -kInf;
       uint32_t bi = 0xFFFFFFFFu, f = 0;
@@ -457,6 +471,10 @@ void launch_stream(const GreedyParams &p, int grid, cudaStream_t s) {
 }
 
 }  // namespace
+
+#ifdef SV_BOUNDS
+SV_OOB_READER(oob_record_greedy)
+#endif
 
 cudaError_t launch_greedy(const GreedyParams &p, bool bf16, int grid, cudaStream_t s) {
   if (bf16) p.vec ? launch_stream<true, true>(p, grid, s) : launch_stream<true, false>(p, grid, s);

@@ -167,5 +167,13 @@ cudaError_t launch_drift(const ChainStochParams &p, bool bf16, int grid, cudaStr
 cudaError_t launch_greedy(const GreedyParams &p, bool bf16, int grid, cudaStream_t s);
 cudaError_t greedy_max_blocks_per_sm(bool bf16, bool vec, int *blocks);
 cudaError_t launch_rollback(const RollbackParams &p, cudaStream_t s);
+#ifdef SV_BOUNDS
+// Bounds-check builds: each unit's record of bad indexes (count added to
+// *count, first source line kept in *line if none yet), then cleared.
+cudaError_t oob_record_chain(unsigned *count, unsigned *line);
+cudaError_t oob_record_greedy(unsigned *count, unsigned *line);
+// Enqueues one check that fails by design (no memory is touched).
+cudaError_t oob_selftest(cudaStream_t s);
+#endif
 
 }  // namespace sv

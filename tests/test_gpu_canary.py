@@ -1,5 +1,9 @@
 """Guard-region (canary) checks of every entry point's writes (needs a GB300).
 
+Every case runs twice: through the library, and through its bounds-check
+copy (-DSV_BOUNDS), whose kernels check each computed index before the access
+and must record no bad one.
+
 compute-sanitizer is closed on this machine, so out-of-bounds writes are caught
 the old way: every buffer a call receives -- inputs, outputs, workspace --
 is carved out of a larger allocation whose head and tail are filled with a
@@ -69,12 +73,62 @@ class Arena:
         return view.cpu().numpy().view(dtype).reshape(shape)
 
 
-@pytest.fixture(scope="module")
-def L():
+class BoundsChecked:
+    """The bounds-check copy of the library (built with -DSV_BOUNDS): after
+    every call, the kernels' record of bad indexes must be empty."""
+
+    def __init__(self, lib):
+        self._lib = lib
+        lib.spec_debug_bounds.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.POINTER(ctypes.c_uint)]
+        lib.spec_debug_bounds.restype = ctypes.c_int
+        lib.spec_debug_bounds_selftest.argtypes = [ctypes.c_void_p]
+        lib.spec_debug_bounds_selftest.restype = ctypes.c_int
+
+    def record(self):
+        import torch
+        torch.cuda.synchronize()
+        count, line = ctypes.c_uint(0), ctypes.c_uint(0)
+        assert self._lib.spec_debug_bounds(ctypes.byref(count), ctypes.byref(line)) == 0
+        return count.value, line.value
+
+    def __getattr__(self, name):
+        fn = getattr(self._lib, name)
+        if not name.startswith(("spec_verify", "spec_rollback", "spec_kv", "spec_adaptive", "spec_drift")):
+            return fn
+
+        def checked(*args):
+            rc = fn(*args)
+            count, line = self.record()
+            assert count == 0, f"{name}: {count} bad indexes, the first at source line {line}"
+            return rc
+        return checked
+
+
+@pytest.fixture(scope="module", params=["default", "bounds"])
+def L(request):
+    """Each case runs through the library and through its bounds-check copy."""
     import torch
     import speculative_decoding_verification_32_gb300 as sv
+    from speculative_decoding_verification_32_gb300 import _binding
+    from speculative_decoding_verification_32_gb300 import build as lib_build
     assert torch.cuda.is_available()
-    return sv.lib()
+    if request.param == "default":
+        return sv.lib()
+    return BoundsChecked(_binding._bind(ctypes.CDLL(lib_build.build(variant="bounds"))))
+
+
+def test_bounds_record_sees_a_failed_check():
+    """The checker's own check: the self-test kernel tests an index of 5
+    against an extent of 3 (touching no memory), which must be recorded."""
+    import torch
+    from speculative_decoding_verification_32_gb300 import _binding
+    from speculative_decoding_verification_32_gb300 import build as lib_build
+    B = BoundsChecked(_binding._bind(ctypes.CDLL(lib_build.build(variant="bounds"))))
+    B.record()  # clears what earlier calls left
+    assert B.spec_debug_bounds_selftest(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)) == 0
+    count, line = B.record()
+    assert count == 1 and line > 0
+    assert B.record() == (0, 0)  # read and cleared
 
 
 def _stream():

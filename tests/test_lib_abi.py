@@ -20,9 +20,16 @@ def L():
     return _binding.lib()
 
 
-def declared_functions():
+def declared_functions(bounds=False):
+    """Entry points the header declares; those under #ifdef SV_BOUNDS exist
+    only in the bounds-check build (bounds=True: only those)."""
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    guarded = "".join(re.findall(r"#ifdef SV_BOUNDS(.*?)#endif", text, flags=re.S))
+    if bounds:
+        text = guarded
+    else:
+        text = re.sub(r"#ifdef SV_BOUNDS.*?#endif", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(spec_[a-z_]+)\s*\(", text)))
 
 
@@ -32,6 +39,17 @@ def test_every_declared_symbol_is_exported(L):
     assert "spec_rollback_lengths" in names
     for n in names:
         assert hasattr(L, n), f"{n} declared in specverify.h but not exported"
+    for n in declared_functions(bounds=True):  # bounds-check builds only
+        assert not hasattr(L, n), f"{n} exported by the default build"
+
+
+def test_bounds_build_exports_its_extra_entry_points():
+    from speculative_decoding_verification_32_gb300 import build as lib_build
+    B = ctypes.CDLL(lib_build.build(variant="bounds"))
+    names = declared_functions(bounds=True)
+    assert names == ["spec_debug_bounds", "spec_debug_bounds_selftest"]
+    for n in names + declared_functions():
+        assert hasattr(B, n), f"{n} not exported by the bounds-check build"
 
 
 def test_status_strings(L):
