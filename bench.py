@@ -2,9 +2,16 @@
 
 One step = one spec_verify_chain call (stochastic mode) on the headline
 workload: B=64 rows, K=5 drafts, V=128256, bf16 logits, T=0.7 (synthetic,
-seeded).  Reports verify steps/s and the achieved HBM bandwidth of the
-streaming kernel against the measured copy peak, plus an end-to-end number
-with host buffers, the CPU oracle as a baseline, and the SM clocks seen.
+seeded).  Reports verify steps/s (the median of five timed runs of exactly
+--steps steps after --warmup steps) and the achieved HBM bandwidth against
+the measured copy peak, plus: an end-to-end number with host buffers; the
+parity of every row of the timed steps against the oracle (disagreements
+inside and outside the 1e-5 band); the accepted-length histogram, mean
+emitted tokens and residual draws; the CPU oracle on all host cores and on
+one; the other chain and tree workloads (C2, C4, C5) with their rooflines;
+the DRAM traffic of the stream kernel from the ncu capture on record
+(profiles/traffic.json, refused once the kernel's source changed); and the
+SM clocks seen.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -32,23 +39,33 @@ WORKLOAD = "c3"
 METRIC = "verify steps/s and achieved HBM GB/s (B=64,K=5,V=128256 bf16) vs 8 TB/s"
 UNIT = "verify steps/s"
 L2_BYTES = 129 * 1024 * 1024
-# ncu dram__bytes_read.sum + dram__bytes_write.sum of one softmax_partials_kernel
-# launch on this workload (profiles/softmax_partials_chain_c3.md): 180,649,216
-# read + 3,728,384 written; reset to None whenever that kernel changes
-TRAFFIC = 180649216 + 3728384
-# the same for one greedy_kernel launch on the tree workload
-# (profiles/greedy_tree_c4.md): 583,470,336 read + 3,753,984 written
-TREE_TRAFFIC = 583470336 + 3753984
-# one trunc_kernel launch on the truncated workload
-# (profiles/trunc_kernel_truncated_c3.md): 180,934,144 read + 7,237,888 written
-TRUNC_TRAFFIC = 180934144 + 7237888
-# one DRIFT call's two streaming kernels, draft_stats_kernel and
-# drift_select_kernel (profiles/drift_select_c3.md), which between them read
-# the 164 MB of rows: 82,106,880 + 83,719,936 read, 1,701,376 + 1,669,632 written
-DRIFT_TRAFFIC = 82106880 + 83719936 + 1701376 + 1669632
 # kernels one stochastic spec_verify_chain call enqueues: the one-thread
 # generation step, the stream kernel and the resolve kernel
 KERNELS_PER_STEP = 3
+# timed repeats of the K steps (the reported time is their median), and the
+# untimed replays around each, so that the clock sampler sees a busy GPU
+REPEATS = 5
+FILLER_MS = 25.0
+# DRAM traffic of captured kernels: per kernel, the bytes one launch read and
+# wrote under ncu and the SHA-256 of the source file the capture was taken
+# with.  A value whose source has changed since is not reported.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def measured_traffic(kernel):
+    """(bytes per launch, note) of `kernel` from the capture record, or
+    (None, why) when there is no record or the source changed since."""
+    import hashlib
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)[kernel]
+    except (OSError, KeyError, ValueError):
+        return None, "no capture on record"
+    with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    if sha != rec["sha256"]:
+        return None, f"{rec['source']} changed since the capture"
+    return int(rec["dram_bytes_read"]) + int(rec["dram_bytes_write"]), rec["capture"]
 
 
 def parse():
@@ -60,6 +77,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the other workloads' keys in the default line")
     ap.add_argument("--workload", default="chain",
                     choices=["chain", "kv_compact", "policy", "drift", "truncated", "tree",
                              "chain_c5", "greedy", "rollback"],
@@ -179,21 +198,95 @@ def to_cuda(a, dev):
     return torch.from_numpy(a).to(dev)
 
 
-def cpu_baseline(inp, seconds):
-    """The fp64 oracle, as it stands, on this host's cores: full steps of the
-    same workload repeated for about `seconds` seconds."""
+def cpu_baseline(inp, seconds, threads=0):
+    """The fp64 oracle, as it stands, on this host's cores (threads 0: all of
+    them; 1: one core): full steps of the same workload repeated for about
+    `seconds` seconds."""
     from oracle import oracle as O
     n = 0
     t0 = time.perf_counter()
     while True:
         O.verify_chain(inp["target"], inp["draft"], inp["draft_tokens"], inp["temperature"],
-                       inp["u_accept"], inp["u_sample"])
+                       inp["u_accept"], inp["u_sample"], nthreads=threads)
         n += 1
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return {"value": n / el, "unit": UNIT, "cores": O.max_threads(), "kind": "oracle",
+    cores = threads if threads > 0 else O.max_threads()
+    return {"value": n / el, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{n} full steps of the workload (B=64 rows each), {el:.1f} s"}
+
+
+def time_steps(torch, stream, step, n_sets, K, W, repeats=REPEATS, filler_ms=FILLER_MS):
+    """W warm-up steps, then `repeats` timed runs of exactly K steps each
+    (CUDA events on `stream` around graph replays; step i uses input set
+    i mod n_sets), each run preceded by untimed replays for about filler_ms so
+    that the GPU is busy around it.  Returns (median ms per step, the ms per
+    step of every run)."""
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            step(i % n_sets)
+    torch.cuda.synchronize()
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                step(i)
+        return g
+    g_main = capture(n_sets)
+    rem = K % n_sets
+    g_rem = capture(rem) if rem else None
+    reps = K // n_sets
+    # one replay's time, to size the filler
+    with torch.cuda.stream(stream):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g_main.replay()
+        e0.record(stream)
+        for _ in range(3):
+            g_main.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    per_replay = max(e0.elapsed_time(e1) / 3, 1e-3)
+    n_fill = max(1, int(filler_ms / per_replay))
+    evs = []
+    with torch.cuda.stream(stream):
+        for _ in range(repeats):
+            for _ in range(n_fill):
+                g_main.replay()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                g_main.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            b.record(stream)
+            evs.append((a, b))
+        for _ in range(n_fill):
+            g_main.replay()
+    torch.cuda.synchronize()
+    per_step = [a.elapsed_time(b) / K for a, b in evs]
+    return statistics.median(per_step), per_step
+
+
+def band_parity(g_len, g_tok, o, band=1e-5):
+    """Rows where the GPU and the oracle disagree: inside the band (the
+    oracle's smallest decision margin is below `band`, where fp32 and fp64
+    may legitimately differ) and outside it (a real disagreement)."""
+    ok = o["row_status"] == 0
+    same = (g_len == o["accepted_len"]) & np.all(g_tok == o["out_tokens"], axis=1)
+    mism = ~same
+    inside = mism & ok & (o["row_margin"] < band)
+    return {"rows": int(len(g_len)), "band_mismatches": int(inside.sum()),
+            "outside_band": int((mism & ~inside).sum())}
+
+
+def walk_stats(acc_len, K):
+    """Accepted-length histogram, mean emitted tokens and residual draws."""
+    a = acc_len[acc_len >= 0]
+    return {"accepted_len_histogram": np.bincount(a, minlength=K + 1).tolist(),
+            "mean_emitted": float((a + 1).mean()) if a.size else None,
+            "residual_draws": int((a < K).sum()), "bonus_draws": int((a == K).sum())}
 
 
 def run_reference(args):
@@ -237,6 +330,113 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def rotating_chain(torch, sv, inp, dev, stream, greedy=False, kappa=0.0):
+    """Input copies (together more than 3 x L2, so each step reads a set not
+    touched for several steps), output buffers and the step function."""
+    B, K = inp["draft_tokens"].shape
+    step_bytes = inp["target"].nbytes + (0 if greedy else inp["draft"].nbytes)
+    n_sets = max(2, -(-3 * L2_BYTES // step_bytes) + 1)
+    small = {k: to_cuda(inp[k], dev) for k in ("draft_tokens", "temperature", "u_accept", "u_sample")
+             if inp.get(k) is not None}
+    tgt0 = to_cuda(inp["target"], dev)
+    drf0 = None if greedy else to_cuda(inp["draft"], dev)
+    copies = [(tgt0, drf0)] + [(tgt0.clone(), None if greedy else drf0.clone())
+                               for _ in range(n_sets - 1)]
+    outs = [dict(accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
+                 out_tokens=torch.empty(B, K + 1, dtype=torch.int32, device=dev),
+                 num_emitted=torch.empty(B, dtype=torch.int32, device=dev),
+                 row_status=torch.empty(B, dtype=torch.int32, device=dev)) for _ in range(n_sets)]
+
+    def step(i):
+        t, d = copies[i % n_sets]
+        if greedy:
+            sv.spec_verify_chain(t, None, small["draft_tokens"], small.get("temperature"),
+                                 mode="greedy", margin_kappa=kappa, out=outs[i % n_sets], stream=stream)
+        else:
+            sv.spec_verify_chain(t, d, small["draft_tokens"], small["temperature"], small["u_accept"],
+                                 small["u_sample"], out=outs[i % n_sets], stream=stream)
+    return step, n_sets, outs, step_bytes, small
+
+
+def set_parity(outs, o, band_only=True):
+    """Band parity of every input set's outputs against the oracle's."""
+    tot = None
+    for out in outs:
+        g_len = out["accepted_len"].cpu().numpy()
+        g_tok = out["out_tokens"].cpu().numpy()
+        if band_only:
+            p = band_parity(g_len, g_tok, o)
+        else:  # bit-exact work (greedy): any difference is outside
+            diff = int((~((g_len == o["accepted_len"]) & np.all(g_tok == o["out_tokens"], axis=1))).sum())
+            p = {"rows": int(len(g_len)), "band_mismatches": 0, "outside_band": diff}
+        tot = p if tot is None else {k: tot[k] + p[k] for k in tot}
+    tot["input_sets"] = len(outs)
+    return tot
+
+
+def extra_workloads(torch, sv, dev, stream, peak, peak_kind, K=100, W=5):
+    """The other chain and tree workloads, each timed as a median of three
+    runs of K steps (CUDA graphs over rotating input sets), with their
+    roofline against the copy peak and their parity against the oracle."""
+    from oracle import oracle as O
+    res = {}
+    cases = [("c2_stochastic", "c2", False), ("c2_greedy", "c2", True), ("c5_stochastic", "c5", False)]
+    for key, name, greedy in cases:
+        inp = S.make(name, greedy=greedy)
+        step, n_sets, outs, nbytes, _ = rotating_chain(torch, sv, inp, dev, stream, greedy=greedy,
+                                                      kappa=0.3 if greedy else 0.0)
+        ms, runs = time_steps(torch, stream, step, n_sets, K, W, repeats=3, filler_ms=10.0)
+        if greedy:
+            o = O.verify_chain(inp["target"], None, inp["draft_tokens"], mode=O.GREEDY, kappa=0.3)
+        else:
+            o = O.verify_chain(inp["target"], inp["draft"], inp["draft_tokens"], inp["temperature"],
+                               inp["u_accept"], inp["u_sample"])
+        B, Kd = inp["draft_tokens"].shape
+        gbs = nbytes / (ms / 1e3) / 1e9
+        res[key] = {"workload": f"{name} chain B={B} K={Kd} V={inp['target'].shape[-1]}"
+                                + (" greedy, kappa=0.3" if greedy else " stochastic"),
+                    "value": 1e3 / ms, "unit": "verify steps/s", "ms_per_step": ms,
+                    "runs_ms_per_step": runs, "steps": K, "warmup": W,
+                    "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                                 "frac": gbs / peak, "peak_kind": peak_kind,
+                                 "algorithmic_bytes_per_launch": nbytes},
+                    "parity": set_parity(outs, o, band_only=not greedy),
+                    **walk_stats(outs[0]["accepted_len"].cpu().numpy(), Kd)}
+        del step, outs
+        torch.cuda.empty_cache()
+    # the tree workload
+    inp = S.make("c4")
+    B, N = inp["parent"].shape
+    nbytes = inp["target"].nbytes
+    n_sets = max(2, -(-3 * L2_BYTES // nbytes) + 1)
+    tgt0 = to_cuda(inp["target"], dev)
+    sets = [tgt0] + [tgt0.clone() for _ in range(n_sets - 1)]
+    par, toks = to_cuda(inp["parent"], dev), to_cuda(inp["node_tokens"], dev)
+    outs = [dict(accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
+                 path_nodes=torch.empty(B, N, dtype=torch.int32, device=dev),
+                 out_tokens=torch.empty(B, N, dtype=torch.int32, device=dev),
+                 num_emitted=torch.empty(B, dtype=torch.int32, device=dev),
+                 row_status=torch.empty(B, dtype=torch.int32, device=dev)) for _ in range(n_sets)]
+
+    def tstep(i):
+        sv.spec_verify_tree(sets[i % n_sets], par, toks, margin_kappa=inp["kappa"], out=outs[i % n_sets],
+                            stream=stream)
+    ms, runs = time_steps(torch, stream, tstep, n_sets, K, W, repeats=3, filler_ms=10.0)
+    o = O.verify_tree(inp["target"], inp["parent"], inp["node_tokens"], kappa=inp["kappa"])
+    diff = sum(int((~np.all(out["out_tokens"].cpu().numpy() == o["out_tokens"], axis=1)).sum()) for out in outs)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    res["c4_tree"] = {"workload": f"c4 tree B={B} N={N} V={inp['target'].shape[-1]} greedy, kappa=0.3",
+                      "value": 1e3 / ms, "unit": "verify steps/s", "ms_per_step": ms,
+                      "runs_ms_per_step": runs, "steps": K, "warmup": W,
+                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                                   "frac": gbs / peak, "peak_kind": peak_kind,
+                                   "algorithmic_bytes_per_launch": nbytes},
+                      "parity": {"rows": B * n_sets, "band_mismatches": 0, "outside_band": diff,
+                                 "input_sets": n_sets},
+                      "mean_accepted_depth": float(outs[0]["accepted_len"].cpu().numpy().clip(0).mean())}
+    return res
+
+
 def run_ours(args):
     import torch
     import speculative_decoding_verification_32_gb300 as sv
@@ -250,75 +450,36 @@ def run_ours(args):
     seed = rank_seed(rank)
     inp = S.make(WORKLOAD, seed=seed)
     B, K = inp["draft_tokens"].shape
-    V = inp["target"].shape[-1]
-    step_bytes = inp["target"].nbytes + inp["draft"].nbytes
-    sets = args.sets or max(2, -(-3 * L2_BYTES // step_bytes) + 1)  # rotating copies, > 3x L2
-    small = {k: to_cuda(inp[k], dev) for k in ("draft_tokens", "temperature", "u_accept", "u_sample")}
-    tgt0 = to_cuda(inp["target"], dev)
-    drf0 = to_cuda(inp["draft"], dev)
-    copies = [(tgt0, drf0)] + [(tgt0.clone(), drf0.clone()) for _ in range(sets - 1)]
-    outs = [dict(accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
-                 out_tokens=torch.empty(B, K + 1, dtype=torch.int32, device=dev),
-                 num_emitted=torch.empty(B, dtype=torch.int32, device=dev),
-                 row_status=torch.empty(B, dtype=torch.int32, device=dev)) for _ in range(sets)]
     stream = torch.cuda.Stream(device=dev)
-
-    def step(i):
-        t, d = copies[i % sets]
-        sv.spec_verify_chain(t, d, small["draft_tokens"], small["temperature"], small["u_accept"],
-                             small["u_sample"], out=outs[i % sets], stream=stream)
-
-    # eager warm-up (first call caches occupancy queries and attributes)
-    with torch.cuda.stream(stream):
-        for i in range(sets):
-            step(i)
-    torch.cuda.synchronize()
-    # correctness spot check of this very launch configuration against the oracle
-    spot = None
-    if rank == 0:
-        from oracle import oracle as O
-        o = O.verify_chain(inp["target"][:8], inp["draft"][:8], inp["draft_tokens"][:8],
-                           inp["temperature"][:8], inp["u_accept"][:8], inp["u_sample"][:8])
-        g_len = outs[0]["accepted_len"][:8].cpu().numpy()
-        g_tok = outs[0]["out_tokens"][:8].cpu().numpy()
-        same = (g_len == o["accepted_len"]) & np.all(g_tok == o["out_tokens"], axis=1)
-        spot = bool(np.all(same | (o["row_margin"] < 1e-5)))
-
-    # one CUDA graph = one step on each rotating input set
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(sets):
-            step(i)
-    reps_w = max(1, args.warmup // sets)
-    reps = max(1, args.steps // sets)
-    steps = reps * sets
+    step, sets, outs, step_bytes, small = rotating_chain(torch, sv, inp, dev, stream)
+    if args.sets:
+        sets = args.sets  # fewer rotating sets (profiling runs)
+    steps, warmup = args.steps, max(args.warmup, 0)
 
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    with torch.cuda.stream(stream):
-        for _ in range(reps_w):
-            graph.replay()
     if ws > 1:
         torch.distributed.barrier()
-    torch.cuda.synchronize()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(reps):
-            graph.replay()
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    ms_med, ms_runs = time_steps(torch, stream, step, sets, steps, warmup)
     if ws > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    ms = ev0.elapsed_time(ev1)
-    ms = max_over_ranks(ms, dev)
-    ms_per_step = ms / steps
-    value = job_value(ws, steps, ms)
+    ms_per_step = max_over_ranks(ms_med, dev)
+    value = job_value(ws, steps, ms_per_step * steps)
     gbs = step_bytes / (ms_per_step / 1e3) / 1e9
     peak, peak_kind = peaks()
+    traffic, traffic_note = measured_traffic("softmax_partials_kernel")
+
+    # parity of every row of every input set of the timed steps (the last
+    # replay's outputs) against the oracle
+    parity = stats = None
+    if rank == 0:
+        from oracle import oracle as O
+        o = O.verify_chain(inp["target"], inp["draft"], inp["draft_tokens"], inp["temperature"],
+                           inp["u_accept"], inp["u_sample"])
+        parity = set_parity(outs[:sets], o)
+        stats = walk_stats(outs[0]["accepted_len"].cpu().numpy(), K)
 
     # end to end through the public API with host buffers: every step copies
     # its inputs from pinned host memory and reads its results back
@@ -333,11 +494,11 @@ def run_ours(args):
     def e2e_step():
         for k in h:
             d[k].copy_(h[k], non_blocking=True)
-        o = sv.spec_verify_chain(d["target"].view(torch.bfloat16), d["draft"].view(torch.bfloat16),
-                                 d["draft_tokens"], d["temperature"], d["u_accept"],
-                                 d["u_sample"], out=outs[0], stream=stream)
+        o_ = sv.spec_verify_chain(d["target"].view(torch.bfloat16), d["draft"].view(torch.bfloat16),
+                                  d["draft_tokens"], d["temperature"], d["u_accept"],
+                                  d["u_sample"], out=outs[0], stream=stream)
         for k in ho:
-            ho[k].copy_(o[k], non_blocking=True)
+            ho[k].copy_(o_[k], non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -359,55 +520,43 @@ def run_ours(args):
         return
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": steps,
-        "warmup": reps_w * sets, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": dict(workload_config(seed), l2=f"{sets} rotating input sets "
                        f"({sets * step_bytes / 1e6:.0f} MB) > L2; each step reads a set not "
-                       f"touched for {sets - 1} steps", graph="one CUDA graph of "
-                       f"{sets} steps replayed {reps} times"),
+                       f"touched for {sets - 1} steps", timing=f"median of {REPEATS} timed runs of "
+                       f"{steps} steps (CUDA graphs over the input sets), each after "
+                       f"{FILLER_MS:.0f} ms of untimed replays"),
+        "runs_ms_per_step": ms_runs,
         "achieved_hbm_gbs": gbs,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                      "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
                      "kernel": "softmax_partials_kernel<bf16,4,2> (dominant) + "
                                "chain_resolve_kernel<bf16> (PDL); achieved = algorithmic "
                                "bytes / whole-step time, a lower bound for the stream kernel",
-                     "algorithmic_bytes_per_launch": step_bytes, "traffic": TRAFFIC},
+                     "algorithmic_bytes_per_launch": step_bytes, "traffic": traffic,
+                     "traffic_source": traffic_note},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": KERNELS_PER_STEP * steps,
+        "gpu_launches": KERNELS_PER_STEP * steps * REPEATS,
         "clocks": clocks,
-        "parity_spot_check": spot,
+        "parity": parity,
+        **stats,
     }
     if ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
+        line["cpu_baseline_1core"] = cpu_baseline(inp, min(args.cpu_seconds, 10.0), threads=1)
+    if ws == 1 and not args.no_extra:
+        line["workloads"] = extra_workloads(torch, sv, dev, stream, peak, f"{peak_kind} copy bandwidth")
     print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
 
 
 def _time_graph(torch, stream, step, n_sets, steps, warmup):
-    """CUDA-event time per step of a graph of n_sets steps replayed."""
-    with torch.cuda.stream(stream):
-        for i in range(n_sets):
-            step(i)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(n_sets):
-            step(i)
-    reps_w, reps = max(1, warmup // n_sets), max(1, steps // n_sets)
-    with torch.cuda.stream(stream):
-        for _ in range(reps_w):
-            graph.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(reps):
-            graph.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / (reps * n_sets), reps * n_sets, reps_w * n_sets
+    """Median ms per step of timed runs of `steps` steps after `warmup` ones."""
+    ms, _ = time_steps(torch, stream, step, n_sets, steps, warmup)
+    return ms, steps, warmup
 
 
 def run_next(args):
@@ -496,7 +645,7 @@ def run_next(args):
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                              "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
                              "kernel": "trunc_kernel (one pass per logit row) + chain_resolve",
-                             "algorithmic_bytes_per_launch": step_bytes, "traffic": TRUNC_TRAFFIC},
+                             "algorithmic_bytes_per_launch": step_bytes, "traffic": measured_traffic("trunc_kernel")[0]},
                 "gpu_launches": 3 * n, "clocks": clocks}
     elif args.workload in ("chain_c5", "greedy"):
         # chain_c5: the stochastic step at scale (B=256, K=8, per-row
@@ -580,7 +729,7 @@ def run_next(args):
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                              "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
                              "kernel": "greedy_kernel + greedy_walk_kernel",
-                             "algorithmic_bytes_per_launch": step_bytes, "traffic": TREE_TRAFFIC},
+                             "algorithmic_bytes_per_launch": step_bytes, "traffic": measured_traffic("greedy_kernel")[0]},
                 "gpu_launches": 2 * n, "clocks": clocks}
     elif args.workload == "drift":
         # top-32 DRIFT residuals on the headline chain workload
@@ -612,7 +761,7 @@ def run_next(args):
                              "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
                              "kernel": "draft_stats_kernel + drift_select_kernel (one pass over "
                                        "each row between them) + drift_status_kernel",
-                             "algorithmic_bytes_per_launch": alg, "traffic": DRIFT_TRAFFIC},
+                             "algorithmic_bytes_per_launch": alg, "traffic": measured_traffic("drift_kernels")[0]},
                 "gpu_launches": 4 * n, "clocks": clocks}
     elif args.workload == "rollback":
         # committed KV lengths for 4096 rows of up to 9 emitted tokens (K = 8),

@@ -53,7 +53,7 @@ def build(force=False, verbose_ptxas=False, variant=None):
              "-I", INCLUDE, "-I", CSRC, *extra]
     if verbose_ptxas:
         flags += ["-Xptxas", "-v"]
-    # extra nvcc flags for measurement builds (e.g. -DSV_TIMELINE)
+    # extra nvcc flags for measurement and tuning builds
     flags += os.environ.get("SPECVERIFY_NVCC_FLAGS", "").split()
 
     def compile_one(src):
