@@ -190,12 +190,17 @@ spec_status spec_verify_chain(const spec_chain_args *args, const spec_chain_out 
  * Set-up: the first call on a device (with that device current) looks up
  * the buffer's device address once; that lookup may load the library's
  * kernels onto the device.  Make that first call before any stream capture
- * begins.
+ * begins.  The address is kept for the life of the process: it does not
+ * survive cudaDeviceReset (or any other teardown of the device's primary
+ * context), after which this entry point must not be called again.
  *
  * Concurrency: all calls on one device share the one buffer.  Calls queued
  * on one stream run one after another and are safe; calls whose kernels may
- * overlap on the GPU (other streams, other host threads) race on the buffer
- * and produce wrong results.  The buffer never needs clearing.
+ * overlap on the GPU (other streams, other host threads) race on the buffer.
+ * Such a call may return wrong tokens, or stall for up to the wait limit
+ * (spec_set_wait_timeout_ns, 1 s by default) because another call advanced
+ * the buffer's generation under its readers, and then report its rows as
+ * SPEC_ROW_TIMEOUT.  The buffer never needs clearing.
  *
  * Arguments, outputs and status codes are otherwise those of
  * spec_verify_chain.

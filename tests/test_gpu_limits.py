@@ -82,14 +82,37 @@ def test_long_chains(sv, K):
 
 
 def test_largest_tree(sv):
-    """N = 1024 nodes: the walk kernel's combine over every node (one warp
-    per node, eight at a time) and its serial accept pass over all of them."""
+    """N = 1024 nodes: the walk kernel's combine over every node and its
+    root-path AND by pointer jumping over all of them."""
     inp = S.tree_inputs(B=2, N=MAX_NODES, V=512, dtype="bf16", sigma=2.0, max_depth=40,
                         branch=(1, 3), seed=74)
     for kappa in (0.0, 0.3):
         g = host(sv.spec_verify_tree(cuda(inp["target"]), cuda(inp["parent"]),
                                      cuda(inp["node_tokens"]), margin_kappa=kappa))
         o = O.verify_tree(inp["target"], inp["parent"], inp["node_tokens"], kappa=kappa)
+        for k in ("accepted_len", "path_nodes", "out_tokens", "num_emitted", "row_status"):
+            assert np.array_equal(g[k], o[k]), (kappa, k)
+
+
+def test_deepest_tree_pointer_jumping(sv):
+    """A 1024-node tree that is one chain (parent[i] = i - 1) is 1023 edges
+    deep, so the walk's pointer jumping takes its full 10 rounds before the
+    links all reach the root.  Row 0 accepts every node; rows 1 and 2 have a
+    single mismatch (at node 3 and node 700) that the margin rule cannot
+    promote (the token with the smallest logit).  Checked at kappa 0 and 0.3."""
+    rng = np.random.default_rng(1023)
+    B, N, V = 3, MAX_NODES, 512
+    t = S.f32_to_bf16_bits(rng.normal(0.0, 2.0, (B, N, V)).astype(np.float32))
+    tv = S.as_float32(t)
+    parent = np.tile(np.arange(-1, N - 1, dtype=np.int32), (B, 1))
+    toks = np.zeros((B, N), np.int32)
+    toks[:, 1:] = np.argmax(tv[:, :-1], axis=-1)  # first index of the maximum
+    for b, node in ((1, 3), (2, 700)):
+        toks[b, node] = int(np.argmin(tv[b, node - 1]))
+    for kappa in (0.0, 0.3):
+        g = host(sv.spec_verify_tree(cuda(t), cuda(parent), cuda(toks), margin_kappa=kappa))
+        o = O.verify_tree(t, parent, toks, kappa=kappa)
+        assert list(o["accepted_len"]) == [N - 1, 2, 699]
         for k in ("accepted_len", "path_nodes", "out_tokens", "num_emitted", "row_status"):
             assert np.array_equal(g[k], o[k]), (kappa, k)
 
