@@ -206,11 +206,14 @@ spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes
   *smem = 0;
   if (ring) {
     // the bulk-copy ring: pair tiles of 8192 bf16 / 4096 fp32 logits per law;
-    // SPECVERIFY_SOFT_STAGES (2 or 3) and SPECVERIFY_DYN_CHUNK (tiles per
+    // SPECVERIFY_SOFT_STAGES (2 to 4) and SPECVERIFY_DYN_CHUNK (tiles per
     // claim) override the defaults for tuning
     p.slice = kSoftThreads * kSoftVecs * epv;
     p.stages = kSoftStages;
-    if (const char *ov = std::getenv("SPECVERIFY_SOFT_STAGES")) p.stages = std::atoi(ov) == 3 ? 3 : 2;
+    if (const char *ov = std::getenv("SPECVERIFY_SOFT_STAGES")) {
+      const int st = std::atoi(ov);
+      p.stages = st >= 2 && st <= 4 ? st : 2;
+    }
     p.dyn_chunk = 2;
     if (const char *dc = std::getenv("SPECVERIFY_DYN_CHUNK")) {
       const int c = std::atoi(dc);

@@ -487,7 +487,8 @@ __device__ __forceinline__ float tile_max(const uint32_t (&w)[NV * 4]) {
   }
 }
 
-// Fold one tile into a running (max, sum of exp2((x - max) s2)).
+// Fold one tile into a running (max, sum of exp2((x - max) s2)); element
+// pairs through packed fp32 (one fma and one add per pair).
 template <bool BF16, int NV>
 __device__ __forceinline__ void tile_accumulate(const uint32_t (&w)[NV * 4], float s2, int tid,
                                                 int nvec, float &m_run, float &s_run) {
@@ -497,22 +498,22 @@ __device__ __forceinline__ void tile_accumulate(const uint32_t (&w)[NV * 4], flo
   if (m_run != -kInf && m_new != m_run) s_run *= ex2(__fmul_rn(m_run - m_new, s2));
   m_run = m_new;
   const float off = (m_run == -kInf) ? 0.f : -__fmul_rn(m_run, s2);
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};  // independent chains for the adds
-  if (nvec == NV * kSoftThreads) {  // full tile: no bounds
+  const float2 s2v = make_float2(s2, s2), offv = make_float2(off, off);
+  float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);  // independent chains
+  const bool full = nvec == NV * kSoftThreads;  // no bounds
 #pragma unroll
-    for (int k = 0; k < NV; ++k)
+  for (int k = 0; k < NV; ++k) {
+    if (full || tid + k * kSoftThreads < nvec) {
 #pragma unroll
-      for (int e = 0; e < F::EPV; ++e) acc[e & 3] += ex2(__fmaf_rn(F::elem(w + 4 * k, e), s2, off));
-  } else {
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-      if (tid + k * kSoftThreads < nvec) {
-#pragma unroll
-        for (int e = 0; e < F::EPV; ++e) acc[e & 3] += ex2(__fmaf_rn(F::elem(w + 4 * k, e), s2, off));
+      for (int i = 0; i < F::EPV / 2; ++i) {
+        const float2 a = ffma2(F::pair(w + 4 * k, i), s2v, offv);
+        const float2 e = make_float2(ex2(a.x), ex2(a.y));
+        if (i & 1) acc1 = fadd2(acc1, e);
+        else acc0 = fadd2(acc0, e);
       }
     }
   }
-  s_run += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+  s_run += (acc0.x + acc0.y) + (acc1.x + acc1.y);
 }
 
 // Warp-specialised stream.  Each CTA owns one contiguous share (even in cost)
@@ -1033,13 +1034,16 @@ __global__ void __launch_bounds__(kResolveThreads, kResolveBlocksPerSm) chain_re
   auto join_stream = [&]() {
     if (blockIdx.x == 0 && tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
   };
-  // Rank 0 of the cluster polls the row's partial records (and, when
+  // Every CTA of the cluster polls the row's partial records (and, when
   // truncated, its truncation records) until every one carries this call's
   // tag -- the kernel before this one stamps them as it goes, so a row is
   // resolved as soon as its own records are in, not when that whole grid is
-  // done -- folds them and takes the walk's decisions.  The other CTAs read
-  // those decisions after one cluster barrier.
-  if (crank == 0) {
+  // done -- folds them and takes the walk's decisions itself: the same
+  // arithmetic in the same order gives the same bits in every CTA, so the
+  // draw starts without a cluster barrier.  The CTAs agree on the row's
+  // status at the draw's one barrier (a wait that gave up in one CTA only
+  // flags the row there).
+  {
     const RowScalars first = load_scalars(P, b, lane);
     const uint32_t tag = *reinterpret_cast<volatile const uint32_t *>(P.gen);
     // a truncated verify also polls the row's truncation records, stamped
@@ -1057,29 +1061,11 @@ __global__ void __launch_bounds__(kResolveThreads, kResolveBlocksPerSm) chain_re
       __nanosleep(200);
     }
     if (warp == 0)
-      decide_row(P, b, s2, tflags | (gave_up ? F_TIMEOUT : 0u), lane, true, rstat, first, ctl, BF16);
+      decide_row(P, b, s2, tflags | (gave_up ? F_TIMEOUT : 0u), lane, crank == 0, rstat, first, ctl, BF16);
     __syncthreads();
   }
-  cluster_sync();  // rank 0's decisions are in its shared memory
-  if (crank != 0 && tid < 3) {  // Mp..Sq, u..trunc, thp..: three 16-byte blocks
-    char *mine = reinterpret_cast<char *>(&ctl.Mp) + 16 * tid;
-    *reinterpret_cast<float4 *>(mine) = ld_dsmem_f4(dsmem_addr(mine, 0));
-  }
-  __syncthreads();
-  const uint32_t flags = ctl.flags;
+  const uint32_t my_flags = ctl.flags;
   const int stop = ctl.stop;
-  if (flags) {  // rank 0's decision: every CTA of the cluster leaves here
-    if (crank == 0 && warp == 0 && SV_INB(b, P.B)) {
-      for (int j = lane; j < npos; j += 32) P.out_tokens[(size_t)b * npos + j] = -1;
-      if (lane == 0) {
-        P.accepted_len[b] = -1;
-        P.num_emitted[b] = 0;
-        P.row_status[b] = lowest_code(flags);
-      }
-    }
-    join_stream();
-    return;
-  }
 
   const float nMp = -__fmul_rn(ctl.Mp, s2), nMq = -__fmul_rn(ctl.Mq, s2);
   const float iSp = __frcp_rn(ctl.Sp), iSq = ctl.Sq > 0.f ? __frcp_rn(ctl.Sq) : 0.f;
@@ -1106,6 +1092,7 @@ __global__ void __launch_bounds__(kResolveThreads, kResolveBlocksPerSm) chain_re
                        : nullptr;
 
   int task = stop < K ? 1 : 2;  // 1: residual [p - q]+, 2: the target law p
+  uint32_t row_flags = 0;       // every CTA's status bits, from the exchange
   float Z = 0.f;
   int xs = 0;
   int owner_cta = -1;
@@ -1239,11 +1226,15 @@ __global__ void __launch_bounds__(kResolveThreads, kResolveBlocksPerSm) chain_re
     if (tid == 0) {
       float c = 0.f;
       for (int w2 = 0; w2 < NW; ++w2) c += ctl.wsum[w2];
-      ctl.mailbox[xs] = make_float4(c, 0.f, 0.f, 0.f);
+      ctl.mailbox[xs] = make_float4(c, __uint_as_float(my_flags), 0.f, 0.f);
     }
     cluster_sync();
-    const float cm = lane < C ? ld_dsmem_f4(dsmem_addr(&ctl.mailbox[xs], (uint32_t)lane)).x : 0.f;
+    const float4 mb = lane < C ? ld_dsmem_f4(dsmem_addr(&ctl.mailbox[xs], (uint32_t)lane))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float cm = mb.x;
     xs ^= 1;
+    row_flags = __reduce_or_sync(FULL_MASK, __float_as_uint(mb.y));
+    if (row_flags) break;  // the row's status: no token
     const float tot = sum_lanes(cm, C);
     if (task == 1 && !(tot > 0.f)) {  // the residual vanished in fp32: draw from p
       task = 2;
@@ -1255,7 +1246,16 @@ __global__ void __launch_bounds__(kResolveThreads, kResolveBlocksPerSm) chain_re
   }
   cluster_arrive();  // done with the peers' mailboxes
 
-  if (crank == owner_cta) {
+  if (row_flags) {  // the agreed status: rank 0 writes the row's outputs
+    if (crank == 0 && warp == 0 && SV_INB(b, P.B)) {
+      for (int j = lane; j < npos; j += 32) P.out_tokens[(size_t)b * npos + j] = -1;
+      if (lane == 0) {
+        P.accepted_len[b] = -1;
+        P.num_emitted[b] = 0;
+        P.row_status[b] = lowest_code(row_flags);
+      }
+    }
+  } else if (crank == owner_cta) {
     float t_w;
     const float wm = lane < NW ? ctl.wsum[lane] : 0.f;
     const int owner_warp = pick_entry(wm, NW, t_c, &t_w);
@@ -2577,12 +2577,15 @@ cudaError_t oob_selftest(cudaStream_t s) {
 
 cudaError_t launch_chain_stochastic(const ChainStochParams &p, bool bf16, int grid, size_t smem,
                                     int cluster, cudaStream_t s) {
+  if (p.stages == 4)
+    return bf16 ? launch_t<true, 4>(p, grid, smem, cluster, s) : launch_t<false, 4>(p, grid, smem, cluster, s);
   if (p.stages == 3)
     return bf16 ? launch_t<true, 3>(p, grid, smem, cluster, s) : launch_t<false, 3>(p, grid, smem, cluster, s);
   return bf16 ? launch_t<true, 2>(p, grid, smem, cluster, s) : launch_t<false, 2>(p, grid, smem, cluster, s);
 }
 
 cudaError_t ring_blocks_per_sm(bool bf16, int stages, size_t smem, int *blocks) {
+  if (stages == 4) return bf16 ? ring_blocks_t<true, 4>(smem, blocks) : ring_blocks_t<false, 4>(smem, blocks);
   if (stages == 3) return bf16 ? ring_blocks_t<true, 3>(smem, blocks) : ring_blocks_t<false, 3>(smem, blocks);
   return bf16 ? ring_blocks_t<true, 2>(smem, blocks) : ring_blocks_t<false, 2>(smem, blocks);
 }

@@ -126,11 +126,15 @@ constexpr int kResolveThreads = 256;
 // Ring stream: 16-byte vectors per consumer thread per tensor in a tile (a
 // tile is kSoftThreads * kSoftVecs vectors of the target row and as many of
 // the draft row: 8192 bf16 or 4096 fp32 logits per tensor) and ring depth.
-constexpr int kSoftVecs = 4;
+#ifndef SV_SOFT_VECS
+#define SV_SOFT_VECS 4
+#endif
+constexpr int kSoftVecs = SV_SOFT_VECS;
 constexpr int kSoftStages = 2;
 // The smallest vocabulary slice with a record of its own (the ring's fp32
 // tile): it sizes the workspace's record area.
-constexpr int kSoftMinSlice = 4096;
+constexpr int kSoftMinSlice = kSoftThreads * kSoftVecs * 4;
+static_assert(kSoftMinSlice <= 4096, "the DRIFT statistics share the record area");
 // DRIFT's row statistics: threads per CTA of the draft-row kernel, 16-byte
 // vectors in flight per lane, and logits per slice.  The selection kernel
 // forms the target row's statistics with the same slices, lane mapping and
