@@ -482,34 +482,49 @@ def run_ours(args):
         stats = walk_stats(outs[0]["accepted_len"].cpu().numpy(), K)
 
     # end to end through the public API with host buffers: every step copies
-    # its inputs from pinned host memory and reads its results back
+    # its inputs from pinned host memory and reads its results back.  Two
+    # buffer sets: while step i verifies, step i+1's inputs cross the host
+    # link on a copy stream (the link, not the verification, bounds this).
     h = {k: torch.from_numpy(np.ascontiguousarray(inp[k]).view(np.int16)
                              if inp[k].dtype == np.uint16 else np.ascontiguousarray(inp[k])).pin_memory()
          for k in ("target", "draft", "draft_tokens", "temperature", "u_accept", "u_sample")}
-    d = {k: torch.empty(h[k].shape, dtype=h[k].dtype, device=dev) for k in h}
-    ho = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs[0].items()}
+    dbuf = [{k: torch.empty(h[k].shape, dtype=h[k].dtype, device=dev) for k in h} for _ in range(2)]
+    obuf = [{k: torch.empty_like(v) for k, v in outs[0].items()} for _ in range(2)]
+    hbuf = [{k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs[0].items()}
+            for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in h.values())
-    d2h = sum(v.numel() * v.element_size() for v in ho.values())
+    d2h = sum(v.numel() * v.element_size() for v in hbuf[0].values())
+    copy_stream = torch.cuda.Stream(device=dev)
+    copied = [torch.cuda.Event() for _ in range(2)]
+    freed = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        for k in h:
-            d[k].copy_(h[k], non_blocking=True)
-        o_ = sv.spec_verify_chain(d["target"].view(torch.bfloat16), d["draft"].view(torch.bfloat16),
-                                  d["draft_tokens"], d["temperature"], d["u_accept"],
-                                  d["u_sample"], out=outs[0], stream=stream)
-        for k in ho:
-            ho[k].copy_(o_[k], non_blocking=True)
+    def e2e_step(i):
+        x = i % 2
+        d, o, ho = dbuf[x], obuf[x], hbuf[x]
+        with torch.cuda.stream(copy_stream):
+            if i >= 2:
+                copy_stream.wait_event(freed[x])  # step i-2 is done with this set
+            for k in h:
+                d[k].copy_(h[k], non_blocking=True)
+            copied[x].record(copy_stream)
+        with torch.cuda.stream(stream):
+            stream.wait_event(copied[x])
+            sv.spec_verify_chain(d["target"].view(torch.bfloat16), d["draft"].view(torch.bfloat16),
+                                 d["draft_tokens"], d["temperature"], d["u_accept"],
+                                 d["u_sample"], out=o, stream=stream)
+            for k in ho:
+                ho[k].copy_(o[k], non_blocking=True)
+            freed[x].record(stream)
 
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            e2e_step()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        e1.record(stream)
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(copy_stream)
+    for i in range(args.e2e_steps):
+        e2e_step(i)
+    e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
     e2e_value = ws * 1e3 / e2e_ms
@@ -537,7 +552,10 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": step_bytes, "traffic": traffic,
                      "traffic_source": traffic_note},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "note": "two buffer sets: each step's inputs cross the host link on a copy "
+                        "stream while the step before verifies; every step copies all its "
+                        "inputs in and its results out"},
         "gpu_launches": KERNELS_PER_STEP * steps * REPEATS,
         "clocks": clocks,
         "parity": parity,
