@@ -282,7 +282,7 @@ size_t spec_verify_chain_workspace_size(int32_t B, int32_t K, int32_t V) {
   // stochastic: one partial per (logit row, slice), the smallest slice being
   // the fp32 one; greedy: one partial per (position, slice)
   const size_t rows = static_cast<size_t>(B) * (K + 1) + static_cast<size_t>(B) * K;
-  const size_t soft = rows * ceil_div(V, kSoftMinSlice) * sizeof(SoftPart) + align_up(rows * 8, 256) +
+  const size_t soft = rows * ceil_div(V, kRecordSlice) * sizeof(SoftPart) + align_up(rows * 8, 256) +
                       rows * sizeof(SoftPart);
   const size_t part = greedy_partials_max(B, K + 1, V);
   return align_up(std::max(std::max(soft, part), static_cast<size_t>(256)), 256) + ws_tail_bytes(B);

@@ -526,7 +526,7 @@ __device__ __forceinline__ void tile_accumulate(const uint32_t (&w)[NV * 4], flo
 // rescale per tile and a single CTA-wide fold at its end.  Producer and
 // consumers meet only on the full/empty barriers of each stage.
 template <bool BF16, int NV, int S>
-__global__ void __launch_bounds__(kSoftThreads + 32, 3) softmax_partials_kernel(const __grid_constant__ ChainStochParams P) {
+__global__ void __launch_bounds__(kSoftThreads + 32, kSoftMinBlocks) softmax_partials_kernel(const __grid_constant__ ChainStochParams P) {
   using F = Fmt<BF16>;
   constexpr int NT = kSoftThreads, NW = NT / 32;
   constexpr int EPV = F::EPV, ESZ = F::ESZ;

@@ -130,11 +130,15 @@ constexpr int kResolveThreads = 256;
 #define SV_SOFT_VECS 4
 #endif
 constexpr int kSoftVecs = SV_SOFT_VECS;
+// The ring stream kernel's launch bound (CTAs per SM it is compiled for).
+#ifndef SV_SOFT_MINB
+#define SV_SOFT_MINB 3
+#endif
+constexpr int kSoftMinBlocks = SV_SOFT_MINB;
 constexpr int kSoftStages = 2;
 // The smallest vocabulary slice with a record of its own (the ring's fp32
 // tile): it sizes the workspace's record area.
 constexpr int kSoftMinSlice = kSoftThreads * kSoftVecs * 4;
-static_assert(kSoftMinSlice <= 4096, "the DRIFT statistics share the record area");
 // DRIFT's row statistics: threads per CTA of the draft-row kernel, 16-byte
 // vectors in flight per lane, and logits per slice.  The selection kernel
 // forms the target row's statistics with the same slices, lane mapping and
@@ -143,6 +147,9 @@ constexpr int kStatsThreads = 256;
 constexpr int kStatsU = 4;
 constexpr int kStatsSlice = 4096;
 constexpr int kStatsMaxSlices = (SPEC_MAX_V + kStatsSlice - 1) / kStatsSlice;
+// The record area holds one record per (logit row, smallest slice of any
+// stochastic path).
+constexpr int kRecordSlice = kSoftMinSlice < kStatsSlice ? kSoftMinSlice : kStatsSlice;
 // Largest rounds of 32 vectors per warp in the resolve kernel.
 constexpr int kResolveMaxRounds = 16;
 // Resolve CTAs one SM holds (the kernel's launch bound): the cluster split
