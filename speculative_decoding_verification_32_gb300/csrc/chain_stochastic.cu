@@ -9,7 +9,10 @@
 //
 // The plain verify runs two kernels per call after a one-thread step that
 // advances the workspace's generation (the stamp every record of the call
-// carries):
+// carries).  Each of the three is a programmatic dependent of the kernel
+// before it, so a call's stream starts loading while the previous call's
+// last rows still resolve; no kernel touches the workspace before the
+// generation step has completed.
 //
 //  softmax_partials_kernel -- the HBM stream.  A persistent grid (several CTAs
 //    per SM, no clusters) walks (logit row, vocabulary slice) items through a
@@ -17,22 +20,21 @@
 //    logit m and sum of exp2((x - m) log2(e) / T) (an online softmax: each
 //    thread exponentiates against its own max, warps and the CTA fold the
 //    pairs) and, if the slice holds the draft token, its logit.  Every logit
-//    is read from HBM exactly once here, with one exp per logit.  Rows are
-//    streamed from the last draft position down to position 0, and positions
-//    0 and 1 are loaded without the evict-first hint, so the rows where walks
-//    most often stop are still in L2 for the second kernel.
+//    is read from HBM exactly once here, with one exp per logit.  Positions
+//    j >= 2 are streamed first and positions 0 and 1 last, loaded without the
+//    evict-first hint, so the rows where walks most often stop are still in
+//    L2 for the second kernel.
 //
 //  chain_resolve_kernel -- one thread-block cluster per batch row, launched as
-//    a programmatic dependent of the first kernel.  Rank 0 polls the row's
-//    stamped partials, folds them into the global max and sum of each
-//    position, forms the acceptance ratios in log2 space and finds the first
-//    rejection; the other CTAs read its decision through distributed shared
-//    memory.  The cluster then re-reads only the stopping position (the
-//    residual needs the global normalisers, so it cannot be formed during the
-//    stream): each CTA sums the residual mass of its vocabulary slice, one
-//    cluster barrier exchanges the masses, and the CTA, warp, round, lane and
-//    element whose cumulative interval holds u * mass are chosen in
-//    vocabulary order.
+//    a programmatic dependent of the first kernel.  Every CTA of the cluster
+//    polls the row's stamped partials, folds them into the global max and sum
+//    of each position, forms the acceptance ratios in log2 space and finds the
+//    first rejection (the same arithmetic in every CTA gives the same bits).
+//    The cluster then re-reads only the stopping position (the residual needs
+//    the global normalisers, so it cannot be formed during the stream): each
+//    CTA sums the residual mass of its vocabulary slice, one cluster barrier
+//    exchanges the masses, and the CTA, warp, round, lane and element whose
+//    cumulative interval holds u * mass are chosen in vocabulary order.
 //
 // The truncated verify replaces the stream by trunc_kernel (one CTA per logit
 // row: its statistics and top-k / top-p thresholds in one pass) ahead of the
@@ -185,7 +187,6 @@ struct alignas(16) TileInfo {
   int keep;        // 1: load without the evict-first hint
   int first;       // 1: first tile of a run
   int last;        // 1: last tile of a run
-  uint32_t tag;    // the call's tag: stamped on the partial records
 };
 
 struct alignas(16) SoftCtrl {
@@ -422,7 +423,6 @@ __device__ __forceinline__ TileInfo make_tile(const ChainStochParams &P, int gt,
     const int y = __ldg(P.tokens + (size_t)b * K + j);
     if (y >= s0 && y < s0 + it.len) it.yl = y - s0;
   }
-  it.tag = *reinterpret_cast<volatile const uint32_t *>(P.gen);
   return it;
 }
 
@@ -530,9 +530,6 @@ __global__ void __launch_bounds__(kSoftThreads + 32, kSoftMinBlocks) softmax_par
   using F = Fmt<BF16>;
   constexpr int NT = kSoftThreads, NW = NT / 32;
   constexpr int EPV = F::EPV, ESZ = F::ESZ;
-  // let the resolve kernel be scheduled; it waits for this grid on the device
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
   extern __shared__ __align__(128) unsigned char smem[];
   SoftCtrl &ctl = *reinterpret_cast<SoftCtrl *>(smem + (size_t)S * P.buf_bytes);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -627,7 +624,9 @@ __global__ void __launch_bounds__(kSoftThreads + 32, kSoftMinBlocks) softmax_par
       const int nchunks = (total - dyn_from + P.dyn_chunk - 1) / P.dyn_chunk;
       // A chunk is claimed only when the previous one is down to its last
       // tile, so no CTA holds more of the tail than its ring can take; the
-      // claim's round trip overlaps the wait for that tile's stage.
+      // claim's round trip overlaps the wait for that tile's stage.  The
+      // counter is this call's once the generation step has completed.
+      grid_dependency_wait();
       uint32_t claim = atomicAdd(P.claim, 1u);
       while (ok && claim < static_cast<uint32_t>(nchunks)) {
         const int lo = dyn_from + static_cast<int>(claim) * P.dyn_chunk;
@@ -660,6 +659,23 @@ __global__ void __launch_bounds__(kSoftThreads + 32, kSoftMinBlocks) softmax_par
   int s = 0;
   uint32_t parity = 0;
   const uint32_t smem0 = smem_u32(smem);
+  // This grid may start while the previous call's kernels still run (it is a
+  // programmatic dependent of the generation step, itself one of whatever
+  // came before).  Loading and folding tiles needs nothing from them; the
+  // workspace does: a thread first waits for the generation step to complete
+  // (its tag is this call's then, and no earlier kernel still reads the
+  // records) just before its first store there, and only then lets the
+  // resolve kernel, which reads the tag as it starts, be scheduled.
+  uint32_t tag = 0;
+  bool joined = false;
+  auto join_generation = [&]() {
+    if (!joined) {
+      grid_dependency_wait();
+      tag = *reinterpret_cast<volatile const uint32_t *>(P.gen);
+      allow_dependents();
+      joined = true;
+    }
+  };
   // Stages arrive in the producer's order until its end marker (len < 0).
   for (int n = 0;; ++n, s = (s + 1 == S) ? 0 : s + 1, parity ^= (s == 0)) {
     bool timed_out = false;
@@ -729,8 +745,9 @@ __global__ void __launch_bounds__(kSoftThreads + 32, kSoftMinBlocks) softmax_par
           c = __ldg(reinterpret_cast<const float *>(dg) + it.yl);
         }
       }
-      st_relaxed_u64(P.ylog + it.trow, __float_as_uint(a) | (static_cast<unsigned long long>(it.tag) << 32));
-      st_relaxed_u64(P.ylog + it.drow, __float_as_uint(c) | (static_cast<unsigned long long>(it.tag) << 32));
+      join_generation();
+      st_relaxed_u64(P.ylog + it.trow, __float_as_uint(a) | (static_cast<unsigned long long>(tag) << 32));
+      st_relaxed_u64(P.ylog + it.drow, __float_as_uint(c) | (static_cast<unsigned long long>(tag) << 32));
     }
     const float s2 = it.s2;
     if (it.first) {
@@ -753,6 +770,7 @@ __global__ void __launch_bounds__(kSoftThreads + 32, kSoftMinBlocks) softmax_par
     if (pair) tile_accumulate<BF16, NV>(wp, s2, tid, nvec, mq, sq);
 
     if (it.last && SV_INB(runs % (2 * S), 2 * kMaxStages)) {  // the run ends: fold the CTA's partials
+      join_generation();
       const int slot = runs % (2 * S);
       ++runs;
       float Mpw, Spw, Mqw, Sqw;
@@ -776,12 +794,12 @@ __global__ void __launch_bounds__(kSoftThreads + 32, kSoftMinBlocks) softmax_par
         SoftPart *rp = P.part + (size_t)it.trow * nt;
         SoftPart *rq = pair ? P.part + (size_t)it.drow * nt : nullptr;
         for (int t = it.run0 + 1 + lane; t <= it.t; t += 32) {
-          store_part(rp + t, -kInf, 0.f, 0u, it.tag);
-          if (pair) store_part(rq + t, -kInf, 0.f, 0u, it.tag);
+          store_part(rp + t, -kInf, 0.f, 0u, tag);
+          if (pair) store_part(rq + t, -kInf, 0.f, 0u, tag);
         }
         if (lane == 0) {
-          store_part(rp + it.run0, M1, S1, tf, it.tag);
-          if (pair) store_part(rq + it.run0, M2, S2, tf, it.tag);
+          store_part(rp + it.run0, M1, S1, tf, tag);
+          if (pair) store_part(rq + it.run0, M2, S2, tf, tag);
           ctl.arrived[slot] = 0;
           ctl.tflags[slot] = 0;
         }
@@ -1014,6 +1032,11 @@ __global__ void __launch_bounds__(kResolveThreads, kResolveBlocksPerSm) chain_re
   const float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
   const uint32_t tflags = (T > 0.f && T < kInf) ? 0u : F_BAD_TEMPERATURE;
   const float s2 = tflags ? 1.f : __fdiv_rn(kLog2e, T);
+  // The next call's generation step may launch once every CTA of this grid
+  // runs: it waits for this grid to complete before it advances the tag, and
+  // the next stream's CTAs, launched behind it, load and fold their first
+  // tiles on the SMs this grid frees while its last rows resolve.
+  allow_dependents();
 
   // The logits are inputs the kernel before this one (the stream, or the
   // truncation kernel) never writes, so the rows where walks most often stop
@@ -1032,7 +1055,7 @@ __global__ void __launch_bounds__(kResolveThreads, kResolveBlocksPerSm) chain_re
   // Block 0 waits for the kernel before this one on its way out, so this
   // grid never completes before the one it depends on.
   auto join_stream = [&]() {
-    if (blockIdx.x == 0 && tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (blockIdx.x == 0 && tid == 0) grid_dependency_wait();
   };
   // Every CTA of the cluster polls the row's partial records (and, when
   // truncated, its truncation records) until every one carries this call's
@@ -1449,7 +1472,7 @@ __global__ void __launch_bounds__(kStatsThreads, 4) draft_stats_kernel(const __g
   constexpr int EPV = F::EPV, ESZ = F::ESZ, U = kStatsU;
   // the selection kernel may be scheduled now; it waits for this grid on the
   // device before it reads these records
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  allow_dependents();
   // forced-timeout test: no record of this call appears
   if (P.force_timeout) return;
   const int lane = threadIdx.x & 31;
@@ -1509,7 +1532,7 @@ __global__ void __launch_bounds__(kDriftThreads, 2) drift_select_kernel(const __
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int j = blockIdx.x, b = blockIdx.y;
   const int K = P.K, npos = K + 1, V = P.V, m = P.drift_m;
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  allow_dependents();
   // forced-timeout test: no flag record of this call appears, so the status
   // kernel reports a timeout.  The generation step completed before the
   // statistics grid started, so the tag read below is this call's; the
@@ -1658,7 +1681,7 @@ __global__ void __launch_bounds__(kDriftThreads, 2) drift_select_kernel(const __
       };
       float M1, S1, M2, S2;
       fold_slices([&](int t, float *qm, float *qs) { *qm = ctl.slm[t]; *qs = ctl.sls[t]; }, &M1, &S1);
-      asm volatile("griddepcontrol.wait;" ::: "memory");
+      grid_dependency_wait();
       bool ready = true;
       fold_slices([&](int t, float *qm, float *qs) {
         uint32_t qf;
@@ -1919,7 +1942,7 @@ __global__ void __launch_bounds__(kDriftThreads, 2) drift_select_kernel(const __
 // a timeout -- writes the row's code and blanks every position of a flagged
 // row: support -1, residual NaN.
 __global__ void __launch_bounds__(32) drift_status_kernel(const __grid_constant__ ChainStochParams P) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  grid_dependency_wait();
   const int b = blockIdx.x, lane = threadIdx.x, K = P.K, m = P.drift_m;
   const uint32_t tag = *reinterpret_cast<volatile const uint32_t *>(P.gen);
   uint32_t f = 0;
@@ -1984,7 +2007,7 @@ __global__ void __launch_bounds__(kTruncThreads) trunc_kernel(const __grid_const
   const int j = is_target ? q : q - npos;
   const int row = is_target ? b * npos + j : P.B * npos + b * K + j;
   // a plain launch: the generation step (this call's tag) has completed
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  allow_dependents();
   // forced-timeout test: no record of this call appears, so the resolve
   // kernel's bounded wait gives up
   if (P.force_timeout) return;
@@ -2447,8 +2470,13 @@ cudaError_t prepare(int cluster) {
 }
 
 // Advances the workspace's generation word (the call's tag) and clears the
-// stream's claim counter: one thread, a plain launch ahead of the stream.
+// stream's claim counter: one thread, launched as a programmatic dependent of
+// the kernel before it (often the previous call's resolve kernel) and waiting
+// for that kernel to complete before it writes; the kernel after it may start
+// at once and waits for this one before touching the workspace.
 __global__ void advance_generation_kernel(uint32_t *gen, uint32_t *claim) {
+  allow_dependents();
+  grid_dependency_wait();
   // the tag is never 0, so zero-filled memory never passes for a record
   const uint32_t g = *gen + 1u;
   *gen = g ? g : 1u;
@@ -2478,32 +2506,37 @@ cudaError_t launch_resolve(const ChainStochParams &p, int cluster, cudaStream_t 
 
 // A kernel of `threads`-thread CTAs launched as a programmatic dependent of
 // the kernel before it.
-template <typename Kern>
-cudaError_t launch_dependent(Kern k, const ChainStochParams &p, dim3 grid, int threads, cudaStream_t s) {
+template <typename Kern, typename... Args>
+cudaError_t launch_dependent(Kern k, dim3 grid, int threads, size_t smem, cudaStream_t s,
+                             Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, p);
+  return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
+cudaError_t launch_generation(const ChainStochParams &p, cudaStream_t s) {
+  return launch_dependent(advance_generation_kernel, dim3(1), 1, 0, s, p.gen, p.claim);
 }
 
 // The plain verify: the generation step, the bulk-copy ring stream, then the
-// resolve kernel.
+// resolve kernel, each a programmatic dependent of the one before.
 template <bool BF16, int S>
 cudaError_t launch_t(const ChainStochParams &p, int grid, size_t smem, int cluster, cudaStream_t s) {
   cudaError_t e = prepare<BF16>(cluster);
   if (e == cudaSuccess) e = prepare_ring<BF16, kSoftVecs, S>(smem);
   if (e != cudaSuccess) return e;
-  advance_generation_kernel<<<1, 1, 0, s>>>(p.gen, p.claim);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  softmax_partials_kernel<BF16, kSoftVecs, S><<<grid, kSoftThreads + 32, smem, s>>>(p);
-  e = cudaGetLastError();
+  e = launch_generation(p, s);
+  if (e == cudaSuccess)
+    e = launch_dependent(softmax_partials_kernel<BF16, kSoftVecs, S>, dim3(static_cast<unsigned>(grid)),
+                         kSoftThreads + 32, smem, s, p);
   if (e == cudaSuccess) e = launch_resolve<BF16>(p, cluster, s);
   return e;
 }
@@ -2522,8 +2555,7 @@ template <bool BF16>
 cudaError_t launch_truncated_t(const ChainStochParams &p, int grid, int cluster, cudaStream_t s) {
   cudaError_t e = prepare<BF16>(cluster);
   if (e != cudaSuccess) return e;
-  advance_generation_kernel<<<1, 1, 0, s>>>(p.gen, p.claim);
-  e = cudaGetLastError();
+  e = launch_generation(p, s);
   if (e != cudaSuccess) return e;
   trunc_kernel<BF16><<<grid, kTruncThreads, 0, s>>>(p);
   e = cudaGetLastError();
@@ -2536,15 +2568,14 @@ cudaError_t launch_truncated_t(const ChainStochParams &p, int grid, int cluster,
 // the per-row status.
 template <bool BF16>
 cudaError_t launch_drift_t(const ChainStochParams &p, int grid, cudaStream_t s) {
-  advance_generation_kernel<<<1, 1, 0, s>>>(p.gen, p.claim);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_generation(p, s);
   if (e != cudaSuccess) return e;
   if (p.use_tma) draft_stats_kernel<BF16, true><<<grid, kStatsThreads, 0, s>>>(p);
   else draft_stats_kernel<BF16, false><<<grid, kStatsThreads, 0, s>>>(p);
   e = cudaGetLastError();
   if (e == cudaSuccess)
-    e = launch_dependent(drift_select_kernel<BF16>, p,
-                         dim3(static_cast<unsigned>(p.K), static_cast<unsigned>(p.B)), kDriftThreads, s);
+    e = launch_dependent(drift_select_kernel<BF16>, dim3(static_cast<unsigned>(p.K), static_cast<unsigned>(p.B)),
+                         kDriftThreads, 0, s, p);
   if (e == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.B));

@@ -112,6 +112,19 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// Programmatic dependent launch.  grid_dependency_wait returns once every grid
+// this one was launched as a programmatic dependent of has completed and its
+// memory operations are visible (at once for a plain launch); the kernels it
+// waits for are bounded themselves.  allow_dependents lets the grid launched
+// after this one as a programmatic dependent be scheduled once every CTA of
+// this grid has issued it or exited.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Wait for phase `parity` of `bar` to complete; give up after limit_ns.
 // Returns false on timeout.  Never spins without a bound.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,

@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kGreedyThreads) greedy_kernel(const __grid_con
   constexpr int EPV = F::EPV;
   constexpr int ESZ = F::ESZ;
   // let the walk kernel be scheduled now; it waits for this grid anyway
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  allow_dependents();
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * kGWarps + (threadIdx.x >> 5);
   const int GW = gridDim.x * kGWarps;
@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(kWalkThreads) greedy_walk_kernel(const __grid_
       lg_s[i] = l;
     }
   }
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  grid_dependency_wait();
   // Each position's (max, lowest argmax, flags) from its slice partials, by
   // whichever mapping takes fewer dependent rounds of loads: a warp per
   // position (lanes over the slices; few positions with many slices, as in a
