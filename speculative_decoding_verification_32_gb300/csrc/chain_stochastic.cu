@@ -10,9 +10,9 @@
 // The plain verify runs two kernels per call after a one-thread step that
 // advances the workspace's generation (the stamp every record of the call
 // carries).  Each of the three is a programmatic dependent of the kernel
-// before it, so a call's stream starts loading while the previous call's
-// last rows still resolve; no kernel touches the workspace before the
-// generation step has completed.
+// before it; the generation step lets the stream start only once every
+// earlier kernel has completed, and no kernel touches the workspace before
+// the generation step itself has.
 //
 //  softmax_partials_kernel -- the HBM stream.  A persistent grid (several CTAs
 //    per SM, no clusters) walks (logit row, vocabulary slice) items through a
@@ -659,13 +659,11 @@ __global__ void __launch_bounds__(kSoftThreads + 32, kSoftMinBlocks) softmax_par
   int s = 0;
   uint32_t parity = 0;
   const uint32_t smem0 = smem_u32(smem);
-  // This grid may start while the previous call's kernels still run (it is a
-  // programmatic dependent of the generation step, itself one of whatever
-  // came before).  Loading and folding tiles needs nothing from them; the
-  // workspace does: a thread first waits for the generation step to complete
-  // (its tag is this call's then, and no earlier kernel still reads the
-  // records) just before its first store there, and only then lets the
-  // resolve kernel, which reads the tag as it starts, be scheduled.
+  // This grid is a programmatic dependent of the generation step and may
+  // start before that step has written the tag.  Loading and folding tiles
+  // needs nothing from it; a thread waits for it to complete just before its
+  // first store to the workspace, and only then lets the resolve kernel,
+  // which reads the tag as it starts, be scheduled.
   uint32_t tag = 0;
   bool joined = false;
   auto join_generation = [&]() {
@@ -1033,9 +1031,8 @@ __global__ void __launch_bounds__(kResolveThreads, kResolveBlocksPerSm) chain_re
   const uint32_t tflags = (T > 0.f && T < kInf) ? 0u : F_BAD_TEMPERATURE;
   const float s2 = tflags ? 1.f : __fdiv_rn(kLog2e, T);
   // The next call's generation step may launch once every CTA of this grid
-  // runs: it waits for this grid to complete before it advances the tag, and
-  // the next stream's CTAs, launched behind it, load and fold their first
-  // tiles on the SMs this grid frees while its last rows resolve.
+  // runs: it waits, resident, for this grid to complete before it advances
+  // the tag.
   allow_dependents();
 
   // The logits are inputs the kernel before this one (the stream, or the
@@ -2471,12 +2468,13 @@ cudaError_t prepare(int cluster) {
 
 // Advances the workspace's generation word (the call's tag) and clears the
 // stream's claim counter: one thread, launched as a programmatic dependent of
-// the kernel before it (often the previous call's resolve kernel) and waiting
-// for that kernel to complete before it writes; the kernel after it may start
-// at once and waits for this one before touching the workspace.
+// the kernel before it, so it is resident and waiting when that kernel ends.
+// It lets the stream launch only once that kernel (and so every kernel before
+// it, the producers of this call's logits included) has completed: the
+// stream reads its inputs from its first instruction on.
 __global__ void advance_generation_kernel(uint32_t *gen, uint32_t *claim) {
-  allow_dependents();
   grid_dependency_wait();
+  allow_dependents();
   // the tag is never 0, so zero-filled memory never passes for a record
   const uint32_t g = *gen + 1u;
   *gen = g ? g : 1u;
