@@ -1428,7 +1428,6 @@ __device__ uint32_t block_kth_largest(Each each, int r, int *chist, int *s_digit
 constexpr int kDriftThreads = 512;
 constexpr int kDriftWarps = kDriftThreads / 32;
 constexpr int kDriftMaxM = kDriftMaxSupport;
-constexpr int kDriftMaxRows = kDriftMaxK;
 
 constexpr int kDriftCand = 2048;  // candidate list of the sampled-threshold path
 constexpr int kDriftSample = 64;  // sampling stride of that threshold, in vectors
