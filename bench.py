@@ -80,10 +80,10 @@ def parse():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the other workloads' keys in the default line")
     ap.add_argument("--workload", default="chain",
-                    choices=["chain", "kv_compact", "policy", "drift", "truncated", "tree",
-                             "chain_c5", "greedy", "rollback"],
-                    help="chain: the headline verify step (default); kv_compact / policy: "
-                         "the post-verification entry points")
+                    choices=["chain", "kv_compact", "kv_compact_deep", "policy", "drift",
+                             "truncated", "tree", "chain_c5", "greedy", "rollback"],
+                    help="chain: the headline verify step (default); kv_compact / "
+                         "kv_compact_deep / policy: the post-verification entry points")
     ap.add_argument("--sets", type=int, default=0,
                     help="rotating input sets (0: enough to exceed 3x L2)")
     return ap.parse_args()
@@ -587,15 +587,23 @@ def run_next(args):
     peak, peak_kind = peaks()
     sampler = ClockSampler(0)
     steps, warmup = min(args.steps, 2000), max(args.warmup, 3)
-    if args.workload == "kv_compact":
-        # paths from verifying the tree workload; a Llama-8B-like cache:
-        # 32 layers x {K, V} planes, 8 KV heads x 128 bf16 per entry
-        inp = S.make("c4")
+    if args.workload in ("kv_compact", "kv_compact_deep"):
+        # paths from verifying a tree workload; a Llama-8B-like cache:
+        # 32 layers x {K, V} planes, 8 KV heads x 128 bf16 per entry.
+        # kv_compact: the c4 trees (B=32, mostly shallow accepted paths);
+        # kv_compact_deep: 256 trees of depth <= 6 whose drafts follow the
+        # target's own ranking (so most paths run deep), verified at a small
+        # vocabulary -- the cache move depends on the paths only
+        if args.workload == "kv_compact":
+            inp = S.make("c4")
+        else:
+            inp = S.make("c4", B=256, V=4096, draft_noise=0.0)
         g = sv.spec_verify_tree(to_cuda(inp["target"], dev), to_cuda(inp["parent"], dev),
                                 to_cuda(inp["node_tokens"], dev), margin_kappa=0.3)
         torch.cuda.synchronize()
         B, N = inp["parent"].shape
-        planes, S_max, heads, hd = 64, 128, 8, 128
+        planes, heads, hd = 64, 8, 128
+        S_max = 128 if args.workload == "kv_compact" else 64  # slots per row (N = 60 nodes)
         E = heads * hd * 2
         kvl = torch.zeros(B, dtype=torch.int32, device=dev)
         one = planes * B * S_max * E
@@ -613,7 +621,9 @@ def run_next(args):
         ms, n, w = _time_graph(torch, stream, step, n_sets, steps, warmup)
         clocks = sampler.stop()
         gbs = moved / (ms / 1e3) / 1e9
-        line = {"metric": "KV path compaction: bytes moved per second", "workload": "kv_compact",
+        kv_traffic, kv_note = measured_traffic(
+            "kv_compact_tree_kernel" if args.workload == "kv_compact" else "kv_compact_tree_kernel_deep")
+        line = {"metric": "KV path compaction: bytes moved per second", "workload": args.workload,
                 "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": n, "warmup": w,
                 "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
                 "data": "synthetic",
@@ -624,7 +634,8 @@ def run_next(args):
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                              "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
                              "kernel": "kv_compact_tree_kernel",
-                             "algorithmic_bytes_per_launch": moved, "traffic": None},
+                             "algorithmic_bytes_per_launch": moved, "traffic": kv_traffic,
+                             "traffic_source": kv_note},
                 "gpu_launches": n, "clocks": clocks}
     elif args.workload == "truncated":
         # the headline chain step with top-k = 50 and top-p = 0.9 on every row

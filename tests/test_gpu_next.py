@@ -51,11 +51,14 @@ def _cache(rng, planes, B, S, E):
     return rng.integers(0, 256, (planes, B, S, E), dtype=np.uint8)
 
 
-def test_kv_compaction_of_verified_tree_paths(sv):
+@pytest.mark.parametrize("draft_noise", [2.0, 0.0])
+def test_kv_compaction_of_verified_tree_paths(sv, draft_noise):
     """Paths straight from spec_verify_tree on the tree workload (scaled
-    down), entries of 2 KB (8 heads x 128 bf16) in 6 planes."""
+    down), entries of 2 KB (8 heads x 128 bf16) in 6 planes.  With no draft
+    noise the drafts follow the target's own ranking, so most accepted paths
+    run to the trees' depth (up to 6 moved entries a row)."""
     import torch
-    inp = S.make("c4", B=32, V=4096)
+    inp = S.make("c4", B=32, V=4096, draft_noise=draft_noise)
     g = sv.spec_verify_tree(cuda(inp["target"]), cuda(inp["parent"]), cuda(inp["node_tokens"]),
                             margin_kappa=0.3)
     h = host(g)
@@ -71,6 +74,8 @@ def test_kv_compaction_of_verified_tree_paths(sv):
     assert np.array_equal(out["st"], st_o)
     assert np.array_equal(out["kv"], want)
     assert (h["accepted_len"] > 1).any()  # some path really moved
+    if draft_noise == 0.0:
+        assert h["accepted_len"].mean() >= 3  # deep paths
 
 
 @pytest.mark.parametrize("E", [16, 2048 + 16, 4096])
