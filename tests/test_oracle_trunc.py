@@ -34,6 +34,23 @@ def test_truncated_worked_example(kw):
     np.testing.assert_allclose(o["resid_mass"][1:, 0], [2 / 3] * 3, rtol=1e-6)
 
 
+def test_top_k_then_top_p_on_the_renormalised_law():
+    """Top-k first, then top-p on the renormalised top-k law, written out by
+    hand.  top-2 of p = (.6, .3, .1) is (2/3, 1/3, 0); its top-0.65 set is
+    {0} alone (2/3 >= 0.65), so p'' = (1, 0, 0).  top-2 of q = (.2, .5, .3)
+    is (0, .625, .375); .625 < 0.65, so q'' keeps both: (0, .625, .375).
+    Draft token 1: p''(1) = 0 rejects it whatever u, and the residual
+    (p'' - q'')+ = (1, 0, 0) emits token 0.  (Counting the top-p mass on the
+    law before the top-k renormalisation would keep token 1 in p'': .6 <
+    0.65.)"""
+    o = _example([1, 1], [0.0, 0.99], [0.5] * 4, top_k=[2] * 2, top_p=[0.65] * 2)
+    assert o["accepted_len"].tolist() == [0, 0]
+    assert o["out_tokens"][:, 0].tolist() == [0, 0]
+    np.testing.assert_allclose(o["p_at_draft"][:, 0], [0.0, 0.0], atol=1e-12)
+    np.testing.assert_allclose(o["q_at_draft"][:, 0], [0.625, 0.625], rtol=1e-6)
+    np.testing.assert_allclose(o["resid_mass"][:, 0], [1.0, 1.0], rtol=1e-6)
+
+
 def test_truncated_exact_law_by_enumeration():
     """Draft tokens drawn from q' and uniforms on a fine grid: the first
     emitted token follows p' exactly (accepted mass + residual mass)."""
