@@ -38,10 +38,11 @@
 //
 // The truncated verify replaces the stream by trunc_kernel (one CTA per logit
 // row: its statistics and top-k / top-p thresholds in one pass) ahead of the
-// same resolve kernel.  DRIFT residuals run draft_stats_kernel (the draft
-// rows' statistics), drift_select_kernel (one CTA per drafted position: the
-// target row's statistics and top m in one pass) and a one-warp-per-row
-// status kernel.
+// same resolve kernel.  DRIFT residuals run drift_select_kernel (one CTA per
+// drafted position: the target row's statistics and top m in one pass),
+// draft_stats_kernel (the draft rows' statistics, on the SMs the selection's
+// last, partial wave leaves idle) and drift_finish_kernel (one CTA per row:
+// log q at the support, the residuals and the row status).
 #include <cuda_bf16.h>
 
 #include <atomic>
@@ -1426,6 +1427,7 @@ __device__ uint32_t block_kth_largest(Each each, int r, int *chist, int *s_digit
 // taken in vocabulary order, so the support matches the oracle's exactly.
 
 constexpr int kDriftThreads = 512;
+constexpr int kDriftFinishThreads = 256;
 constexpr int kDriftWarps = kDriftThreads / 32;
 constexpr int kDriftMaxM = kDriftMaxSupport;
 
@@ -1453,28 +1455,30 @@ struct alignas(16) DriftCtrl {
   int scan[kDriftWarps];
   int n_gt, n_eq, digit, above;
   float slm[kStatsMaxSlices], sls[kStatsMaxSlices];  // the target row's per-slice (max, sum)
-  float Mp, Sp, Mq, Sq;
+  float Mp, Sp;
   uint32_t flags;
 };
 
-// DRIFT, first kernel: the draft rows' statistics.  A persistent grid of
+// DRIFT, second kernel: the draft rows' statistics.  A persistent grid of
 // warps over (draft row, 4096-logit slice) items in row order; a warp streams
 // its item with plain 16-byte loads (kStatsU per lane in flight, L2
 // evict-first), folds it into the slice's max and sum of exp2((x - m) s2) and
-// stamps one record.  No shared memory, no barrier, no atomics.
+// stamps one record.  No shared memory, no barrier, no atomics.  It is a
+// programmatic dependent of the selection grid and needs nothing from it, so
+// its CTAs fill the SMs that grid's last, partial wave leaves idle; block 0
+// waits for that grid on its way out, so this grid never completes before it.
 template <bool BF16, bool VEC>
 __global__ void __launch_bounds__(kStatsThreads, 4) draft_stats_kernel(const __grid_constant__ ChainStochParams P) {
   using F = Fmt<BF16>;
   constexpr int EPV = F::EPV, ESZ = F::ESZ, U = kStatsU;
-  // the selection kernel may be scheduled now; it waits for this grid on the
+  // the finishing kernel may be scheduled now; it waits for this grid on the
   // device before it reads these records
   allow_dependents();
-  // forced-timeout test: no record of this call appears
-  if (P.force_timeout) return;
   const int lane = threadIdx.x & 31;
   const long long GW = (long long)gridDim.x * (kStatsThreads / 32);
   const int nt = P.nslices, V = P.V, K = P.K;
-  const long long total = (long long)P.B * K * nt;
+  // forced-timeout test: no record of this call appears
+  const long long total = P.force_timeout ? 0 : (long long)P.B * K * nt;
   const uint32_t tag = *reinterpret_cast<volatile const uint32_t *>(P.gen);
   const uint64_t pol = l2_policy_evict_first();
   for (long long it = (long long)blockIdx.x * (kStatsThreads / 32) + (threadIdx.x >> 5); it < total; it += GW) {
@@ -1517,6 +1521,29 @@ __global__ void __launch_bounds__(kStatsThreads, 4) draft_stats_kernel(const __g
     fold_max_sum(m, sacc, s2, &M, &S);
     if (lane == 0) store_part(P.part + (size_t)drow * nt + sl, M, S, 0u, tag);
   }
+  // block 0 waits for the selection grid on its way out
+  if (blockIdx.x == 0 && threadIdx.x == 0) grid_dependency_wait();
+}
+
+// A row's (max, sum) from its slices' (max, sum) pairs, in one fixed order:
+// lane t folds slices t, t + 32, ... in order, then the lanes fold in a fixed
+// butterfly (fold_max_sum).  slice(t, &m, &s) returns false for a record that
+// is not in yet; the result is whether every lane's were.
+template <typename Slice>
+__device__ __forceinline__ bool fold_slice_stats(int nt, int lane, float s2, Slice slice, float *M,
+                                                 float *S) {
+  float mm = -kInf, ss = 0.f;
+  bool ready = true;
+  for (int t = lane; t < nt; t += 32) {
+    float qm, qs;
+    ready &= slice(t, &qm, &qs);
+    const float mn = fmax_nan(mm, qm);
+    ss = (mm == -kInf ? 0.f : ss * ex2(__fmul_rn(mm - mn, s2))) +
+         (qm == -kInf ? 0.f : qs * ex2(__fmul_rn(qm - mn, s2)));
+    mm = mn;
+  }
+  fold_max_sum(mm, ss, s2, M, S);
+  return __all_sync(FULL_MASK, ready);
 }
 
 template <bool BF16>
@@ -1528,11 +1555,12 @@ __global__ void __launch_bounds__(kDriftThreads, 2) drift_select_kernel(const __
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int j = blockIdx.x, b = blockIdx.y;
   const int K = P.K, npos = K + 1, V = P.V, m = P.drift_m;
+  // the draft rows' statistics grid may start as soon as every CTA of this
+  // grid runs: it reads and writes nothing this grid touches
   allow_dependents();
-  // forced-timeout test: no flag record of this call appears, so the status
-  // kernel reports a timeout.  The generation step completed before the
-  // statistics grid started, so the tag read below is this call's; the
-  // dependency wait on that grid comes just before its records are read.
+  // forced-timeout test: no record of this call appears, so the finishing
+  // kernel reports a timeout.  This grid is a plain launch behind the
+  // generation step, so the tag read below is this call's.
   if (P.force_timeout) return;
   const float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
   const uint32_t tflags = (T > 0.f && T < kInf) ? 0u : F_BAD_TEMPERATURE;
@@ -1548,7 +1576,6 @@ __global__ void __launch_bounds__(kDriftThreads, 2) drift_select_kernel(const __
     if constexpr (BF16) return __ldg(reinterpret_cast<const unsigned short *>(tg) + i);
     else return __ldg(reinterpret_cast<const unsigned int *>(tg) + i);
   };
-  const char *dg = static_cast<const char *>(P.draft) + ((size_t)(b * K + j) * V) * ESZ;
   auto kth_largest = [&](auto each, int r, int &n_above, int &n_equal) {
     return block_kth_largest<KEYBITS, kDriftThreads>(each, r, ctl.chist, &ctl.digit, &ctl.above,
                                                     n_above, n_equal);
@@ -1654,76 +1681,47 @@ __global__ void __launch_bounds__(kDriftThreads, 2) drift_select_kernel(const __
   };
   int r = 8;
   int nc = pass(true, sample_rank(r));
-  // ---- the target row's max and sum: warps, then warp 0 in a fixed order;
-  // then the draft row's, folded by warp 0 from the statistics kernel's
-  // records (that grid has completed after the dependency wait).  This
-  // position's flags go to the status kernel in a stamped record.
+  // ---- the target row's max and sum: warps, then warp 0 folds the slices
+  // in the fixed order the finishing kernel uses for the draft row's
+  // records, so identical rows give identical bits.  The (max, sum) and this
+  // position's flags go to the finishing kernel in a stamped record.
   {
     if (warp == 0) {
-      // both rows' slices fold the same way: lane t takes slices t, t + 32,
-      // ... in order, then the lanes fold in a fixed butterfly
-      const int nt = P.nslices;
-      auto fold_slices = [&](auto slice_stat, float *M, float *S) {
-        float mm = -kInf, ss = 0.f;
-        for (int t = lane; t < nt; t += 32) {
-          float qm, qs;
-          slice_stat(t, &qm, &qs);
-          const float mn = fmax_nan(mm, qm);
-          ss = (mm == -kInf ? 0.f : ss * ex2(__fmul_rn(mm - mn, s2))) +
-               (qm == -kInf ? 0.f : qs * ex2(__fmul_rn(qm - mn, s2)));
-          mm = mn;
-        }
-        fold_max_sum(mm, ss, s2, M, S);
-      };
-      float M1, S1, M2, S2;
-      fold_slices([&](int t, float *qm, float *qs) { *qm = ctl.slm[t]; *qs = ctl.sls[t]; }, &M1, &S1);
-      grid_dependency_wait();
-      bool ready = true;
-      fold_slices([&](int t, float *qm, float *qs) {
-        uint32_t qf;
-        ready &= load_part(P.part + (size_t)(b * K + j) * nt + t, tag, qm, qs, &qf);
-      }, &M2, &S2);
-      ready = __all_sync(FULL_MASK, ready);
+      float M1, S1;
+      fold_slice_stats(P.nslices, lane, s2, [&](int t, float *qm, float *qs) {
+        *qm = ctl.slm[t];
+        *qs = ctl.sls[t];
+        return true;
+      }, &M1, &S1);
       if (lane == 0) {
-        uint32_t f = tflags | (ready ? 0u : F_TIMEOUT);
-        for (const float M : {M1, M2}) {
-          if (M != M || M == kInf) f |= F_NONFINITE;
-          else if (M == -kInf) f |= F_EMPTY;
-        }
+        uint32_t f = tflags;
+        if (M1 != M1 || M1 == kInf) f |= F_NONFINITE;
+        else if (M1 == -kInf) f |= F_EMPTY;
         ctl.flags = f;
         ctl.Mp = M1;
         ctl.Sp = S1;
-        ctl.Mq = M2;
-        ctl.Sq = S2;
-        store_part(P.trunc_area + (size_t)b * K + j, 0.f, 0.f, f, tag);
+        store_part(P.trunc_area + (size_t)b * K + j, M1, S1, f, tag);
       }
     }
     __syncthreads();
   }
-  if (ctl.flags) {  // the status kernel blanks the whole row
+  if (ctl.flags) {  // the finishing kernel blanks the whole row
     for (int i = tid; i < m; i += kDriftThreads) {
       sup[i] = -1;
       res[i] = __int_as_float(0x7fc00000);
     }
     return;
   }
-  const float nMp = -__fmul_rn(ctl.Mp, s2), nMq = -__fmul_rn(ctl.Mq, s2);
-  const float l2Sp = lg2(ctl.Sp), l2Sq = lg2(ctl.Sq);
-  // support entry `rank` is token ii: log2 p and log2 q as in the walk, the
-  // difference in nats
+  const float nMp = -__fmul_rn(ctl.Mp, s2);
+  const float l2Sp = lg2(ctl.Sp);
+  // support entry `rank` is token ii: its log2 p as in the walk, kept in the
+  // residual's place until the finishing kernel subtracts log2 q
   auto emit = [&](int rank, int ii) {
-    float lt, ld;
-    if constexpr (BF16) {
-      lt = bf16_lo(__ldg(reinterpret_cast<const unsigned short *>(tg) + ii));
-      ld = bf16_lo(__ldg(reinterpret_cast<const unsigned short *>(dg) + ii));
-    } else {
-      lt = __ldg(reinterpret_cast<const float *>(tg) + ii);
-      ld = __ldg(reinterpret_cast<const float *>(dg) + ii);
-    }
-    const float l2p = __fadd_rn(__fmaf_rn(lt, s2, nMp), -l2Sp);
-    const float l2q = ld == -kInf ? -kInf : __fadd_rn(__fmaf_rn(ld, s2, nMq), -l2Sq);
+    float lt;
+    if constexpr (BF16) lt = bf16_lo(__ldg(reinterpret_cast<const unsigned short *>(tg) + ii));
+    else lt = __ldg(reinterpret_cast<const float *>(tg) + ii);
     sup[rank] = ii;
-    res[rank] = __fmul_rn(__fadd_rn(l2p, -l2q), kLn2);
+    res[rank] = __fadd_rn(__fmaf_rn(lt, s2, nMp), -l2Sp);
   };
   for (int attempt = 0; attempt < 3; ++attempt) {
     if (attempt > 0) nc = pass(false, sample_rank(r));
@@ -1932,30 +1930,73 @@ __global__ void __launch_bounds__(kDriftThreads, 2) drift_select_kernel(const __
 
 // Largest key x (0 .. 2^bits - 1) with pred(x) true, pred being monotone
 // (true for small x).
-// DRIFT row status: one warp per row, a programmatic dependent of the
-// selection grid (whose writes it sees once that grid has completed).  It ORs
-// the row's stamped position flags -- a position whose record did not come is
-// a timeout -- writes the row's code and blanks every position of a flagged
-// row: support -1, residual NaN.
-__global__ void __launch_bounds__(32) drift_status_kernel(const __grid_constant__ ChainStochParams P) {
+// DRIFT, third kernel: one CTA per row, a programmatic dependent of the
+// draft rows' statistics grid (which completes only after the selection grid
+// has), so both grids' writes are visible after its dependency wait.  Each
+// warp takes drafted positions in turn: it folds the draft row's slice
+// records in the order the selection kernel folded the target row's, forms
+// log2 q at the m support tokens and replaces the log2 p the selection kernel
+// left there by the residual log p - log q in nats.  A position whose record
+// (the selection's, or a draft slice's) did not come is a timeout.  The row
+// status ORs every position's flags; a flagged row gets support -1 and
+// residual NaN everywhere, since no single selection CTA sees the whole row.
+template <bool BF16>
+__global__ void __launch_bounds__(kDriftFinishThreads) drift_finish_kernel(const __grid_constant__ ChainStochParams P) {
+  __shared__ uint32_t row_f;
+  __shared__ float s_mq[kDriftMaxK], s_lsq[kDriftMaxK];
   grid_dependency_wait();
-  const int b = blockIdx.x, lane = threadIdx.x, K = P.K, m = P.drift_m;
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K = P.K, V = P.V, m = P.drift_m, nt = P.nslices;
+  constexpr int NW = kDriftFinishThreads / 32;
   const uint32_t tag = *reinterpret_cast<volatile const uint32_t *>(P.gen);
-  uint32_t f = 0;
-  for (int j = lane; j < K; j += 32) {
-    float x, y;
-    uint32_t qf;
-    if (!load_part(P.trunc_area + (size_t)b * K + j, tag, &x, &y, &qf)) f |= F_TIMEOUT;
-    f |= qf;
+  const float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
+  const float s2 = (T > 0.f && T < kInf) ? __fdiv_rn(kLog2e, T) : 1.f;
+  if (tid == 0) row_f = 0u;
+  __syncthreads();
+  for (int j = warp; j < K && SV_INB(j, kDriftMaxK); j += NW) {
+    float M1 = 0.f, S1 = 0.f, M2, S2;
+    uint32_t f1 = 0;
+    const bool sel_in = load_part(P.trunc_area + (size_t)b * K + j, tag, &M1, &S1, &f1);
+    const bool stats_in = fold_slice_stats(nt, lane, s2, [&](int t, float *qm, float *qs) {
+      uint32_t qf;
+      if (!SV_INB((long long)(b * K + j) * nt + t, (long long)P.B * K * nt)) {
+        *qm = -kInf;
+        *qs = 0.f;
+        return false;
+      }
+      return load_part(P.part + (size_t)(b * K + j) * nt + t, tag, qm, qs, &qf);
+    }, &M2, &S2);
+    uint32_t f = f1 | (sel_in && stats_in ? 0u : F_TIMEOUT);
+    if (M2 != M2 || M2 == kInf) f |= F_NONFINITE;
+    else if (M2 == -kInf) f |= F_EMPTY;
+    if (lane == 0) {
+      s_mq[j] = M2;
+      s_lsq[j] = lg2(S2);
+      if (f) atomicOr(&row_f, f);
+    }
   }
-  f = __reduce_or_sync(FULL_MASK, f);
-  if (lane == 0 && P.row_status) P.row_status[b] = lowest_code(f);
-  if (!f) return;
+  __syncthreads();
+  const uint32_t f = row_f;
+  if (tid == 0 && P.row_status) P.row_status[b] = lowest_code(f);
   int32_t *sup = P.drift_support + (size_t)b * K * m;
   float *res = P.drift_residual + (size_t)b * K * m;
-  for (int i = lane; i < K * m; i += 32) {
-    sup[i] = -1;
-    res[i] = __int_as_float(0x7fc00000);
+  if (f) {
+    for (int i = tid; i < K * m; i += kDriftFinishThreads) {
+      sup[i] = -1;
+      res[i] = __int_as_float(0x7fc00000);
+    }
+    return;
+  }
+  for (int i = tid; i < K * m; i += kDriftFinishThreads) {
+    const int j = i / m;
+    const int ii = sup[i];
+    if (!(ii >= 0 && ii < V) || !SV_INB(j, kDriftMaxK)) continue;  // m > V: no token here
+    const size_t at = ((size_t)b * K + j) * V + ii;
+    float ld;
+    if constexpr (BF16) ld = bf16_lo(__ldg(static_cast<const unsigned short *>(P.draft) + at));
+    else ld = __ldg(static_cast<const float *>(P.draft) + at);
+    const float l2q = ld == -kInf ? -kInf : __fadd_rn(__fmaf_rn(ld, s2, -__fmul_rn(s_mq[j], s2)), -s_lsq[j]);
+    res[i] = __fmul_rn(__fadd_rn(res[i], -l2q), kLn2);
   }
 }
 
@@ -2560,31 +2601,21 @@ cudaError_t launch_truncated_t(const ChainStochParams &p, int grid, int cluster,
   return e;
 }
 
-// DRIFT: the generation step, the draft rows' statistics, one selection CTA
-// per drafted position (which also forms the target row's statistics), then
-// the per-row status.
+// DRIFT: the generation step, one selection CTA per drafted position (the
+// target row's statistics and top m), the draft rows' statistics on the SMs
+// the selection's last, partial wave leaves idle, then one CTA per row that
+// forms the residuals and the row status.
 template <bool BF16>
 cudaError_t launch_drift_t(const ChainStochParams &p, int grid, cudaStream_t s) {
   cudaError_t e = launch_generation(p, s);
   if (e != cudaSuccess) return e;
-  if (p.use_tma) draft_stats_kernel<BF16, true><<<grid, kStatsThreads, 0, s>>>(p);
-  else draft_stats_kernel<BF16, false><<<grid, kStatsThreads, 0, s>>>(p);
+  drift_select_kernel<BF16><<<dim3(static_cast<unsigned>(p.K), static_cast<unsigned>(p.B)), kDriftThreads, 0, s>>>(p);
   e = cudaGetLastError();
   if (e == cudaSuccess)
-    e = launch_dependent(drift_select_kernel<BF16>, dim3(static_cast<unsigned>(p.K), static_cast<unsigned>(p.B)),
-                         kDriftThreads, 0, s, p);
-  if (e == cudaSuccess) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.B));
-    cfg.blockDim = dim3(32);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, drift_status_kernel, p);
-  }
+    e = p.use_tma ? launch_dependent(draft_stats_kernel<BF16, true>, dim3(static_cast<unsigned>(grid)), kStatsThreads, 0, s, p)
+                  : launch_dependent(draft_stats_kernel<BF16, false>, dim3(static_cast<unsigned>(grid)), kStatsThreads, 0, s, p);
+  if (e == cudaSuccess)
+    e = launch_dependent(drift_finish_kernel<BF16>, dim3(static_cast<unsigned>(p.B)), kDriftFinishThreads, 0, s, p);
   return e;
 }
 
