@@ -375,9 +375,10 @@ def set_parity(outs, o, band_only=True):
 
 
 def extra_workloads(torch, sv, dev, stream, peak, peak_kind, K=100, W=5):
-    """The other chain and tree workloads, each timed as a median of three
-    runs of K steps (CUDA graphs over rotating input sets), with their
-    roofline against the copy peak and their parity against the oracle."""
+    """The other chain and tree workloads, the truncated verify and the DRIFT
+    residuals on the headline shape, each timed as a median of three runs of
+    K steps (CUDA graphs over rotating input sets), with their roofline
+    against the copy peak and their parity against the oracle."""
     from oracle import oracle as O
     res = {}
     cases = [("c2_stochastic", "c2", False), ("c2_greedy", "c2", True), ("c5_stochastic", "c5", False)]
@@ -434,6 +435,67 @@ def extra_workloads(torch, sv, dev, stream, peak, peak_kind, K=100, W=5):
                       "parity": {"rows": B * n_sets, "band_mismatches": 0, "outside_band": diff,
                                  "input_sets": n_sets},
                       "mean_accepted_depth": float(outs[0]["accepted_len"].cpu().numpy().clip(0).mean())}
+    del sets, outs
+    torch.cuda.empty_cache()
+    # the headline shape with top-k 50 / top-p 0.9 on every row, and its
+    # DRIFT residuals (m = 32)
+    inp = S.make(WORKLOAD)
+    B, Kd = inp["draft_tokens"].shape
+    V = inp["target"].shape[-1]
+    nbytes = inp["target"].nbytes + inp["draft"].nbytes
+    n_sets = max(2, -(-3 * L2_BYTES // nbytes) + 1)
+    tgt0, drf0 = to_cuda(inp["target"], dev), to_cuda(inp["draft"], dev)
+    sets = [(tgt0, drf0)] + [(tgt0.clone(), drf0.clone()) for _ in range(n_sets - 1)]
+    small = {k: to_cuda(inp[k], dev) for k in ("draft_tokens", "temperature", "u_accept", "u_sample")}
+    tk = torch.full((B,), 50, dtype=torch.int32, device=dev)
+    tp = torch.full((B,), 0.9, dtype=torch.float32, device=dev)
+    outs = [dict(accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
+                 out_tokens=torch.empty(B, Kd + 1, dtype=torch.int32, device=dev),
+                 num_emitted=torch.empty(B, dtype=torch.int32, device=dev),
+                 row_status=torch.empty(B, dtype=torch.int32, device=dev)) for _ in range(n_sets)]
+
+    def trstep(i):
+        j = i % n_sets
+        sv.spec_verify_chain(sets[j][0], sets[j][1], small["draft_tokens"], small["temperature"],
+                             small["u_accept"], small["u_sample"], out=outs[j], stream=stream,
+                             top_k=tk, top_p=tp)
+    ms, runs = time_steps(torch, stream, trstep, n_sets, K, W, repeats=3, filler_ms=10.0)
+    o = O.verify_chain(inp["target"], inp["draft"], inp["draft_tokens"], inp["temperature"],
+                       inp["u_accept"], inp["u_sample"], top_k=np.full(B, 50, np.int32),
+                       top_p=np.full(B, 0.9, np.float32))
+    gbs = nbytes / (ms / 1e3) / 1e9
+    res["c3_truncated"] = {"workload": f"c3 chain B={B} K={Kd} V={V} stochastic, top_k=50, top_p=0.9",
+                           "value": 1e3 / ms, "unit": "verify steps/s", "ms_per_step": ms,
+                           "runs_ms_per_step": runs, "steps": K, "warmup": W,
+                           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                                        "frac": gbs / peak, "peak_kind": peak_kind,
+                                        "algorithmic_bytes_per_launch": nbytes},
+                           "parity": set_parity(outs, o, band_only=True),
+                           **walk_stats(outs[0]["accepted_len"].cpu().numpy(), Kd)}
+    m = 32
+    alg = 2 * B * Kd * V * inp["target"].itemsize
+    temp = small["temperature"]
+    dres = [None] * n_sets
+
+    def drstep(i):
+        j = i % n_sets
+        dres[j] = sv.spec_drift_residuals(sets[j][0], sets[j][1], temp, m=m, stream=stream)
+    ms, runs = time_steps(torch, stream, drstep, n_sets, K, W, repeats=3, filler_ms=10.0)
+    sup_o, res_o, st_o = O.drift_residuals(inp["target"], inp["draft"], inp["temperature"], m=m)
+    sup_g, res_g, st_g = (x.cpu().numpy() for x in dres[0])
+    fin = np.isfinite(res_o)
+    gbs = alg / (ms / 1e3) / 1e9
+    res["c3_drift"] = {"workload": f"c3 chain B={B} K={Kd} V={V}, DRIFT residuals m={m}",
+                       "value": 1e3 / ms, "unit": "steps/s", "ms_per_step": ms,
+                       "runs_ms_per_step": runs, "steps": K, "warmup": W,
+                       "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                                    "frac": gbs / peak, "peak_kind": peak_kind,
+                                    "algorithmic_bytes_per_launch": alg},
+                       "parity": {"positions": int(B * Kd),
+                                  "support_mismatches": int((sup_g != sup_o).any(axis=-1).sum()),
+                                  "status_mismatches": int((st_g != st_o).sum()),
+                                  "residual_max_abs_err_nats": float(np.abs(res_g[fin] - res_o[fin]).max()),
+                                  "tolerance_nats": 2e-4}}
     return res
 
 
