@@ -27,6 +27,7 @@ std::atomic<int> g_force_timeout{0};
 struct DevInfo {
   int sms = 0;
   int smem_optin = 0;
+  int l2_bytes = 0;
 };
 
 std::mutex g_mu;
@@ -74,6 +75,8 @@ cudaError_t device_info(int *dev, DevInfo *info) {
   e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, *dev);
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, *dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, *dev);
   if (e != cudaSuccess) return e;
   g_dev[*dev] = d;
   *info = d;
@@ -214,6 +217,13 @@ spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes
       const int st = std::atoi(ov);
       p.stages = st >= 2 && st <= 4 ? st : 2;
     }
+    // positions 0 and 1 (where walks mostly stop) stay in L2 for the resolve
+    // kernel's second look when both fit well inside it (c3: 66 MB); larger
+    // batches stream every position evict-first (c5, 131 MB: 196.4 against
+    // 198.6 us per step with positions 0 and 1 kept, 198.1 with position 0)
+    const double pos01 = 4.0 * a->B * static_cast<double>(a->V) * esz;
+    p.keep_pos = pos01 <= 0.6 * di.l2_bytes ? 2 : 0;
+    if (const char *kp = std::getenv("SPECVERIFY_KEEP_POS")) p.keep_pos = std::atoi(kp);  // tuning override
     p.dyn_chunk = 2;
     if (const char *dc = std::getenv("SPECVERIFY_DYN_CHUNK")) {
       const int c = std::atoi(dc);

@@ -22,8 +22,8 @@
 //    pairs) and, if the slice holds the draft token, its logit.  Every logit
 //    is read from HBM exactly once here, with one exp per logit.  Positions
 //    j >= 2 are streamed first and positions 0 and 1 last, loaded without the
-//    evict-first hint, so the rows where walks most often stop are still in
-//    L2 for the second kernel.
+//    evict-first hint when they fit well inside L2, so the rows where walks
+//    most often stop are still there for the second kernel.
 //
 //  chain_resolve_kernel -- one thread-block cluster per batch row, launched as
 //    a programmatic dependent of the first kernel.  Every CTA of the cluster
@@ -410,7 +410,7 @@ __device__ __forceinline__ TileInfo make_tile(const ChainStochParams &P, int gt,
     it.drow = -1;
     it.dsrc = 0;
   }
-  it.keep = j <= 1;
+  it.keep = j < P.keep_pos;
   // a run is the part of a row inside [lo, hi): it starts at the later of lo
   // and the row's first tile
   it.first = (gt == lo) || it.t == 0;

@@ -55,6 +55,7 @@ struct ChainStochParams {
   int stages;      // ring stream kernel: bulk-copy pipeline depth
   int buf_bytes;   // ring stream kernel: bytes of one stage buffer
   int dyn_chunk;   // ring stream kernel: tiles per claim of its last phase
+  int keep_pos;    // ring stream kernel: positions below it stay in L2 (evict-normal)
   int L;           // resolve kernel: vocabulary slice per cluster CTA
   int vpw;         // resolve kernel: 16-byte vectors per warp (multiple of 32)
   uint64_t wait_limit_ns;
