@@ -319,11 +319,12 @@ spec_status spec_verify_chain_truncated(const spec_chain_args *args, const spec_
  * (device, caller-owned): a row with a non-finite logit, no finite logit or
  * a bad temperature at any drafted position gets its code and support -1,
  * residual NaN.  The workspace is spec_verify_chain's (same size function).
- * After the one-thread generation step, three kernels: a stream over the
- * draft rows for their softmax statistics; one CTA per drafted position,
- * which reads its target row once for its statistics and selects the
- * support by radix selection on the target logits; then one warp per row
- * for the row's status.  Residuals carry fp32 rounding: agreement with an exact
+ * After the one-thread generation step, three kernels: one CTA per drafted
+ * position, which reads its target row once for its statistics and selects
+ * the support by radix selection on the target logits; a stream over the
+ * draft rows for their softmax statistics, on the SMs the first kernel's
+ * last wave leaves idle; then one CTA per row for the residuals and the
+ * row's status.  Residuals carry fp32 rounding: agreement with an exact
  * computation is within about 1e-4 nats for logits of magnitude up to ~50/T.
  */
 spec_status spec_drift_residuals(const spec_chain_args *args, int32_t m, int32_t *support,
