@@ -52,6 +52,13 @@
  *    starts early and waits for it on the device (programmatic dependent
  *    launch); the stochastic calls first enqueue a one-thread kernel that
  *    advances the workspace's generation count and clears its work counter.
+ *    That kernel is itself a programmatic dependent of whatever precedes it
+ *    and waits for it to complete before anything of the call reads its
+ *    inputs.  The last kernel of a stochastic chain call lets the kernel
+ *    after it start early if that kernel is launched as a programmatic
+ *    dependent: such a kernel must wait for its dependency
+ *    (cudaGridDependencySynchronize) before it reads this call's outputs,
+ *    as programmatic dependent launch requires of every dependent.
  *  - Logits are bf16 (SPEC_BF16) or fp32 (SPEC_F32).  Rows whose byte
  *    length is a multiple of 16 with a 16-byte aligned base take the bulk-
  *    copy (TMA) path; any other V still works, more slowly.
