@@ -373,3 +373,68 @@ def test_truncated_flat_rows_ties_and_fp32(sv, dtype):
     o = O.verify_chain(t, d, toks, inp["temperature"], inp["u_accept"], inp["u_sample"],
                        top_k=k, top_p=p)
     assert compare_stochastic(g, o) <= 1
+
+
+def test_back_to_back_calls_of_every_mode_without_a_sync(sv):
+    """Plain, DRIFT, truncated, greedy, tree and plain calls enqueued on one
+    stream with no host synchronisation between them, then checked against
+    the oracle.  Each call's first kernel may be scheduled while the previous
+    call's last one still runs (programmatic dependent launch), so this is
+    where a call could read its inputs, the workspace's generation or another
+    call's records too early."""
+    import torch
+    rng = np.random.default_rng(2027)
+    plain = S.make("c2")
+    deep = S.chain_inputs(B=12, K=4, V=30000, dtype="bf16", sigma=3.0, seed=77, temperature=(0.7, 1.3))
+    tree = S.make("c4", B=4, V=4096)
+    k, p = _trunc_params(rng, 12, 30000)
+    dev_inp = {n: {key: cuda(v) for key, v in d.items() if isinstance(v, np.ndarray)}
+               for n, d in (("plain", plain), ("deep", deep), ("tree", tree))}
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        a, d = dev_inp["plain"], dev_inp["deep"]
+        outs = []
+        for _ in range(2):
+            outs.append(("plain", sv.spec_verify_chain(a["target"], a["draft"], a["draft_tokens"],
+                                                       a["temperature"], a["u_accept"], a["u_sample"],
+                                                       stream=s)))
+            outs.append(("drift", sv.spec_drift_residuals(d["target"], d["draft"], d["temperature"],
+                                                          m=16, stream=s)))
+            outs.append(("trunc", sv.spec_verify_chain(d["target"], d["draft"], d["draft_tokens"],
+                                                       d["temperature"], d["u_accept"], d["u_sample"],
+                                                       top_k=cuda(k), top_p=cuda(p), stream=s)))
+            outs.append(("greedy", sv.spec_verify_chain(a["target"], None, a["draft_tokens"],
+                                                        mode="greedy", margin_kappa=0.3, stream=s)))
+            t = dev_inp["tree"]
+            outs.append(("tree", sv.spec_verify_tree(t["target"], t["parent"], t["node_tokens"],
+                                                     margin_kappa=tree["kappa"], stream=s)))
+            outs.append(("deep", sv.spec_verify_chain(d["target"], d["draft"], d["draft_tokens"],
+                                                      d["temperature"], d["u_accept"], d["u_sample"],
+                                                      stream=s)))
+    s.synchronize()
+    want = {
+        "plain": oracle_chain(plain),
+        "deep": oracle_chain(deep),
+        "greedy": O.verify_chain(plain["target"], None, plain["draft_tokens"], mode=O.GREEDY, kappa=0.3),
+        "trunc": O.verify_chain(deep["target"], deep["draft"], deep["draft_tokens"], deep["temperature"],
+                                deep["u_accept"], deep["u_sample"], top_k=k, top_p=p),
+        "drift": O.drift_residuals(deep["target"], deep["draft"], deep["temperature"], m=16),
+        "tree": O.verify_tree(tree["target"], tree["parent"], tree["node_tokens"], kappa=tree["kappa"]),
+    }
+    for name, g in outs:
+        o = want[name]
+        if name == "drift":
+            sup, res, st = (x.cpu().numpy() for x in g)
+            assert np.array_equal(st, o[2]) and np.array_equal(sup, o[0])
+            np.testing.assert_allclose(res, o[1], rtol=0, atol=2e-4)
+        elif name == "tree":
+            h = host(g)
+            assert np.array_equal(h["path_nodes"], o["path_nodes"])
+            assert np.array_equal(h["out_tokens"], o["out_tokens"])
+        elif name == "greedy":
+            h = host(g)
+            assert np.array_equal(h["out_tokens"], o["out_tokens"])
+            assert np.array_equal(h["accepted_len"], o["accepted_len"])
+        else:
+            assert compare_stochastic(host(g), o) <= 1
