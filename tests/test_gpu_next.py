@@ -166,3 +166,34 @@ def test_drift_ties_unaligned_and_edges(sv, dtype, V):
     assert g[2][4] == 1 and g[2][5] == 7
     assert np.all(g[1][3] == 0.0)  # identical laws: exactly zero
     assert np.isinf(g[1][2, 0]).sum() == 5
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_drift_edge_rows_in_the_last_wave(sv, dtype):
+    """43 rows x 8 drafted positions: on a GB300 (304 selection CTAs a wave)
+    the last 40 positions, rows 38-42, run in the selection's second wave,
+    beside the draft rows' statistics.  Those rows carry ties that straddle
+    the support boundary (in both halves of the row), an all-equal row,
+    identical laws, masked drafts, a NaN and a bad temperature."""
+    rng = np.random.default_rng(4343)
+    B, K, V, m = 43, 8, 20000, 32
+    t = rng.normal(0, 3, (B, K + 1, V)).astype(np.float32)
+    d = (t[:, :K] + rng.normal(0, 2, (B, K, V))).astype(np.float32)
+    # row 38: forty equal logits in both halves straddle the boundary
+    t[38, 1, :] = np.minimum(t[38, 1, :], 5.0)
+    t[38, 1, np.r_[rng.choice(V // 2, 20, replace=False), V // 2 + rng.choice(V // 2, 20, replace=False)]] = 5.0
+    t[38, 4, :] = 1.25          # all logits equal
+    d[39] = t[39, :K]           # identical laws
+    d[40, 2, np.argsort(-t[40, 2])[:5]] = -np.inf  # masked drafts in the support
+    t[41, 6, 17000] = np.nan    # a NaN in the second half
+    temp = np.full(B, 0.8, np.float32)
+    temp[42] = -1.0             # bad temperature
+    if dtype == "bf16":
+        t, d = S.f32_to_bf16_bits(t), S.f32_to_bf16_bits(d)
+    inp = dict(target=t, draft=d, temperature=temp)
+    o = O.drift_residuals(t, d, temp, m=m)
+    g = run_drift(sv, inp, m)
+    compare_drift(g, o)
+    assert g[2][41] == 1 and g[2][42] == 7
+    assert np.all(g[1][39] == 0.0)  # identical laws: exactly zero
+    assert np.isinf(g[1][40, 2]).sum() == 5
