@@ -735,9 +735,11 @@ def run_next(args):
                            "l2": f"{n_sets} rotating input sets > L2"},
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                              "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
-                             "kernel": "trunc_kernel (one pass per logit row) + chain_resolve",
-                             "algorithmic_bytes_per_launch": step_bytes, "traffic": measured_traffic("trunc_kernel")[0]},
-                "gpu_launches": 3 * n, "clocks": clocks}
+                             "kernel": "softmax_partials_kernel (with chunk maxima) + "
+                                       "trunc_select_kernel + chain_resolve_kernel of one call",
+                             "algorithmic_bytes_per_launch": step_bytes,
+                             "traffic": measured_traffic("truncated_kernels")[0]},
+                "gpu_launches": 4 * n, "clocks": clocks}
     elif args.workload in ("chain_c5", "greedy"):
         # chain_c5: the stochastic step at scale (B=256, K=8, per-row
         # temperatures, 10% of each draft row masked); greedy: argmax match with

@@ -47,12 +47,12 @@
  *    passing the same `ws_bytes` for the same buffer.  Calls on one stream
  *    may share a workspace; calls that may overlap in time (different
  *    streams) need separate workspaces.
- *  - Each verify call enqueues a streaming kernel (for a truncated verify,
- *    the per-logit-row truncation kernel) and a small per-row kernel that
- *    starts early and waits for it on the device (programmatic dependent
- *    launch); the stochastic calls first enqueue a one-thread kernel that
- *    advances the workspace's generation count and clears its work counter.
- *    That kernel is itself a programmatic dependent of whatever precedes it
+ *  - Each verify call enqueues a streaming kernel (a truncated verify adds
+ *    a selection kernel after it) and a small per-row kernel that starts
+ *    early and waits for it on the device (programmatic dependent launch);
+ *    the stochastic calls first enqueue a one-thread kernel that advances
+ *    the workspace's generation count and clears its work counter.  That
+ *    kernel is itself a programmatic dependent of whatever precedes it
  *    and waits for it to complete before anything of the call reads its
  *    inputs.  The last kernel of a stochastic chain call lets the kernel
  *    after it start early if that kernel is launched as a programmatic
@@ -152,6 +152,14 @@ typedef struct {
 /* Bytes of workspace spec_verify_chain needs for these sizes (any mode and
  * dtype).  0 on invalid sizes. */
 size_t spec_verify_chain_workspace_size(int32_t B, int32_t K, int32_t V);
+
+/* Bytes of workspace spec_verify_chain_truncated needs for these sizes (any
+ * dtype): the records of spec_verify_chain plus a 2-byte maximum per chunk
+ * of logits that the selection of the thresholds reads, about V / 8 bytes
+ * per logit row (c3: 11.5 MB).  Never less than
+ * spec_verify_chain_workspace_size, so one such workspace serves both calls.
+ * 0 on invalid sizes. */
+size_t spec_verify_chain_truncated_workspace_size(int32_t B, int32_t K, int32_t V);
 
 /*
  * spec_verify_chain -- one verification step of B independent chains.
@@ -295,10 +303,15 @@ spec_status spec_rollback_lengths(int32_t B, int32_t max_emit, const int32_t *kv
  * residual and the bonus are drawn from them.  Either array may be NULL;
  * both NULL is spec_verify_chain.  The top-p boundary is a floating-point
  * decision taken in fp32 (the band rule covers rows whose cumulative mass
- * lands within ~1e-5 of top_p).  Same workspace as spec_verify_chain.
- * After the one-thread generation step, two kernels: one CTA per logit row,
- * which forms the row's softmax statistics and, for a truncated row, its
- * thresholds in the same pass over the logits; then the per-row resolve.
+ * lands within ~1e-5 of top_p).  The workspace must hold
+ * spec_verify_chain_truncated_workspace_size(B, K, V) bytes (when both
+ * arrays are NULL, spec_verify_chain's size).
+ * After the one-thread generation step, three kernels: the stream of
+ * spec_verify_chain, which also keeps, per truncated logit row, the largest
+ * logit of every chunk of 32 (bf16) or 16 (fp32) it reads; per truncated
+ * logit row the top-k and top-p thresholds, from the logits of the chunks
+ * whose maxima can reach them (a row they cannot settle passes over its own
+ * logits); then the per-row resolve.
  */
 typedef struct {
   const int32_t *top_k;  /* [B] device, or NULL */

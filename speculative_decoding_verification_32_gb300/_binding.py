@@ -94,6 +94,8 @@ def _bind(L):
     i32, u64, sz = _c.c_int32, _c.c_uint64, _c.c_size_t
     L.spec_verify_chain_workspace_size.argtypes = [i32, i32, i32]
     L.spec_verify_chain_workspace_size.restype = sz
+    L.spec_verify_chain_truncated_workspace_size.argtypes = [i32, i32, i32]
+    L.spec_verify_chain_truncated_workspace_size.restype = sz
     L.spec_verify_tree_workspace_size.argtypes = [i32, i32, i32]
     L.spec_verify_tree_workspace_size.restype = sz
     L.spec_verify_chain.argtypes = [_c.POINTER(SpecChainArgs), _c.POINTER(SpecChainOut), _P, sz, _P]
@@ -221,10 +223,12 @@ def spec_verify_chain(target_logits, draft_logits, draft_tokens, temperature=Non
                      _ptr(out.get("p_at_draft")), _ptr(out.get("q_at_draft")),
                      _ptr(out.get("resid_mass")))
     L = lib()
-    nbytes = L.spec_verify_chain_workspace_size(B, K, V)
+    truncated = top_k is not None or top_p is not None
+    nbytes = (L.spec_verify_chain_truncated_workspace_size if truncated
+              else L.spec_verify_chain_workspace_size)(B, K, V)
     s, sp = _stream(dev, stream)
     ws = workspace(dev, nbytes, s.cuda_stream)
-    if top_k is None and top_p is None:
+    if not truncated:
         _check(L.spec_verify_chain(_c.byref(args), _c.byref(o), _ptr(ws), ws.numel(), sp))
     else:
         if greedy:

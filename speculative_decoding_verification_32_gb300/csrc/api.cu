@@ -121,6 +121,13 @@ size_t greedy_partials_max(int32_t B, int32_t npos, int32_t V) {
   return static_cast<size_t>(B) * npos * ceil_div(V, kMinGreedySlice) * sizeof(GreedyPart);
 }
 
+// The truncated verify's chunk maxima, after the records: 2 bytes per
+// (logit row, ring tile, consumer thread), for the fp32 tiling (the one with
+// more tiles).
+size_t chunk_max_bytes(size_t rows, int32_t V) {
+  return align_up(rows * ceil_div(V, kSoftMinSlice) * kSoftThreads * 2, 256);
+}
+
 bool valid_sizes(int32_t B, int32_t V) { return B >= 0 && V >= 1 && V <= SPEC_MAX_V; }
 
 // Greedy launch shared by the chain (GREEDY mode) and tree entry points.
@@ -165,16 +172,17 @@ spec_status run_greedy(GreedyParams &p, bool bf16, int esz, void *ws, cudaStream
 }
 
 // How the first kernel of a stochastic call reads the logits: the bulk-copy
-// ring (plain verify), one CTA per whole logit row (truncated verify: one
-// record per row), or warps over draft-row slices (DRIFT's statistics).
-enum class StreamKind { kRing, kWholeRow, kStats };
+// ring (plain verify; the truncated verify's, which also keeps chunk maxima,
+// is always kSoftStages deep), or warps over draft-row slices (DRIFT's
+// statistics).
+enum class StreamKind { kRing, kRingListed, kStats };
 
 // Parameters and launch shapes of the stochastic stream kernel and of the
 // resolve kernel's cluster split, from the arguments and the workspace;
 // output pointers are left for the caller.
 spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes, ChainStochParams &p,
                              int &grid, int &C, StreamKind kind, size_t *smem) {
-  const bool ring = kind == StreamKind::kRing;
+  const bool ring = kind == StreamKind::kRing || kind == StreamKind::kRingListed;
   const int K = a->K;
   const int esz = a->dtype == SPEC_BF16 ? 2 : 4;
   const bool bf16 = a->dtype == SPEC_BF16;
@@ -213,7 +221,8 @@ spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes
     // claim) override the defaults for tuning
     p.slice = kSoftThreads * kSoftVecs * epv;
     p.stages = kSoftStages;
-    if (const char *ov = std::getenv("SPECVERIFY_SOFT_STAGES")) {
+    const char *ov = kind == StreamKind::kRing ? std::getenv("SPECVERIFY_SOFT_STAGES") : nullptr;
+    if (ov) {
       const int st = std::atoi(ov);
       p.stages = st >= 2 && st <= 4 ? st : 2;
     }
@@ -231,10 +240,8 @@ spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes
     }
     p.buf_bytes = 2 * p.slice * esz;  // target tile + draft tile
     *smem = static_cast<size_t>(p.stages) * p.buf_bytes + kRingCtrlBytes;
-  } else if (kind == StreamKind::kStats) {
-    p.slice = kStatsSlice;
   } else {
-    p.slice = a->V;  // one CTA reads each whole row
+    p.slice = kStatsSlice;
   }
   p.nslices = ceil_div(a->V, p.slice);
   {
@@ -245,18 +252,15 @@ spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes
     p.trunc_area = reinterpret_cast<SoftPart *>(reinterpret_cast<char *>(p.ylog) + align_up(rows * 8, 256));
   }
   int per_sm = 0;
-  const long long rows_all = static_cast<long long>(a->B) * (K + 1) + static_cast<long long>(a->B) * K;
   if (ring) {
     if (ring_blocks(dev, bf16, p.stages, *smem, &per_sm) != cudaSuccess || per_sm < 1) return SPEC_ERR_CUDA;
     const long long tiles = static_cast<long long>(a->B) * (K + 1) * p.nslices;
     grid = static_cast<int>(std::min<long long>(tiles, static_cast<long long>(di.sms) * per_sm));
-  } else if (kind == StreamKind::kStats) {  // a persistent grid of warps, four CTAs per SM
+  } else {  // a persistent grid of warps, four CTAs per SM
     const long long items = static_cast<long long>(a->B) * K * p.nslices;
     const long long warps = kStatsThreads / 32;
     grid = static_cast<int>(std::max<long long>(
         1, std::min<long long>((items + warps - 1) / warps, static_cast<long long>(di.sms) * 4)));
-  } else {
-    grid = static_cast<int>(rows_all);
   }
   // resolve kernel: a cluster of C CTAs per row, at most 16 rounds of 32
   // vectors per warp
@@ -296,6 +300,17 @@ size_t spec_verify_chain_workspace_size(int32_t B, int32_t K, int32_t V) {
                       rows * sizeof(SoftPart);
   const size_t part = greedy_partials_max(B, K + 1, V);
   return align_up(std::max(std::max(soft, part), static_cast<size_t>(256)), 256) + ws_tail_bytes(B);
+}
+
+size_t spec_verify_chain_truncated_workspace_size(int32_t B, int32_t K, int32_t V) {
+  if (!valid_sizes(B, V) || K < 0 || K > SPEC_MAX_K) return 0;
+  // the records (every area 256-byte aligned, as setup_stochastic lays them
+  // out), then the chunk maxima
+  const size_t rows = static_cast<size_t>(B) * (K + 1) + static_cast<size_t>(B) * K;
+  const size_t records = align_up(rows * ceil_div(V, kRecordSlice) * sizeof(SoftPart), 256) +
+                         align_up(rows * 8, 256) + align_up(rows * sizeof(SoftPart), 256);
+  return std::max(records + chunk_max_bytes(rows, V) + ws_tail_bytes(B),
+                  spec_verify_chain_workspace_size(B, K, V));
 }
 
 size_t spec_verify_tree_workspace_size(int32_t B, int32_t N, int32_t V) {
@@ -402,15 +417,20 @@ spec_status spec_verify_chain_truncated(const spec_chain_args *a, const spec_tru
                         o->p_at_draft, o->q_at_draft, o->resid_mass};
   for (const void *x : i32s)
     if (x && !aligned(x, 4)) return SPEC_ERR_ALIGN;
-  const size_t need = spec_verify_chain_workspace_size(a->B, K, a->V);
+  const size_t need = spec_verify_chain_truncated_workspace_size(a->B, K, a->V);
   if (!ws || !aligned(ws, 256) || ws_bytes < need) return SPEC_ERR_WORKSPACE;
   if (static_cast<long long>(a->B) * (2 * K + 1) > 0x7fffffffLL) return SPEC_ERR_SHAPE;
   ChainStochParams p;
   int grid = 0, C = 0;
   size_t smem = 0;
   {
-    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, C, StreamKind::kWholeRow, &smem);
+    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, C, StreamKind::kRingListed, &smem);
     if (st != SPEC_OK) return st;
+  }
+  {  // the chunk maxima, after the truncation records
+    const size_t rows = static_cast<size_t>(a->B) * (2 * K + 1);
+    p.cmax = reinterpret_cast<unsigned short *>(reinterpret_cast<char *>(p.trunc_area) +
+                                                align_up(rows * sizeof(SoftPart), 256));
   }
   p.accepted_len = o->accepted_len;
   p.out_tokens = o->out_tokens;
@@ -423,7 +443,7 @@ spec_status spec_verify_chain_truncated(const spec_chain_args *a, const spec_tru
   p.top_p = t->top_p;
   p.trunc = p.trunc_area;
   report("truncated grid cluster", grid, C, 0, 0, 0, 0, 0);
-  return launch_chain_truncated(p, a->dtype == SPEC_BF16, grid, C,
+  return launch_chain_truncated(p, a->dtype == SPEC_BF16, grid, smem, C,
                                 static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? SPEC_OK
              : SPEC_ERR_CUDA;

@@ -36,9 +36,10 @@
 //    exchanges the masses, and the CTA, warp, round, lane and element whose
 //    cumulative interval holds u * mass are chosen in vocabulary order.
 //
-// The truncated verify replaces the stream by trunc_kernel (one CTA per logit
-// row: its statistics and top-k / top-p thresholds in one pass) ahead of the
-// same resolve kernel.  DRIFT residuals run drift_select_kernel (one CTA per
+// The truncated verify lets the stream also keep, per truncated logit row,
+// the maximum of every consumer thread's chunk of each tile, and selects each
+// row's top-k / top-p thresholds from the chunks those maxima point to (one
+// CTA per logit row) ahead of the same resolve kernel.  DRIFT residuals run drift_select_kernel (one CTA per
 // drafted position: the target row's statistics and top m in one pass),
 // draft_stats_kernel (the draft rows' statistics, on the SMs the selection's
 // last, partial wave leaves idle) and drift_finish_kernel (one CTA per row:
@@ -188,6 +189,7 @@ struct alignas(16) TileInfo {
   int keep;        // 1: load without the evict-first hint
   int first;       // 1: first tile of a run
   int last;        // 1: last tile of a run
+  int sketch;      // truncated verify: 1 = store the tile's chunk maxima
 };
 
 struct alignas(16) SoftCtrl {
@@ -362,6 +364,15 @@ __device__ __forceinline__ void store_part(SoftPart *d, float m, float s, uint32
   st_relaxed_u64(&d->b, static_cast<unsigned long long>(__float_as_uint(s)) |
                             (static_cast<unsigned long long>((flags & 0xffu) | (tag << 8)) << 32));
 }
+// A record's two words, decoded; false while either holds an older record.
+__device__ __forceinline__ bool decode_part(unsigned long long a, unsigned long long b, uint32_t tag,
+                                            float *m, float *s, uint32_t *flags) {
+  *m = __uint_as_float(static_cast<uint32_t>(a));
+  *s = __uint_as_float(static_cast<uint32_t>(b));
+  const uint32_t hb = static_cast<uint32_t>(b >> 32);
+  *flags = hb & 0xffu;
+  return static_cast<uint32_t>(a >> 32) == tag && (hb >> 8) == (tag & 0xffffffu);
+}
 // false while either word still holds an older record
 __device__ __forceinline__ bool load_part(const SoftPart *d, uint32_t tag, float *m, float *s,
                                           uint32_t *flags) {
@@ -391,7 +402,7 @@ __device__ __forceinline__ int phase_split(int p0, int p1, int B, int K, int nt,
   return c <= nb ? (int)c : nb + (int)((c - nb + 1) / 2);
 }
 
-template <bool BF16>
+template <bool BF16, bool CAND>
 __device__ __forceinline__ TileInfo make_tile(const ChainStochParams &P, int gt, int lo, int hi) {
   TileInfo it;
   const int B = P.B, K = P.K, nt = P.nslices;
@@ -424,15 +435,21 @@ __device__ __forceinline__ TileInfo make_tile(const ChainStochParams &P, int gt,
     const int y = __ldg(P.tokens + (size_t)b * K + j);
     if (y >= s0 && y < s0 + it.len) it.yl = y - s0;
   }
+  it.sketch = 0;
+  if constexpr (CAND) {
+    int tk;
+    float tp;
+    it.sketch = SV_INB(b, B) && trunc_active(P, b, P.V, &tk, &tp);
+  }
   return it;
 }
 
 // The n-th tile of the CTA, rebuilt by a consumer after a wait gave up.
-template <bool BF16>
+template <bool BF16, bool CAND>
 __device__ __noinline__ TileInfo rebuild_tile(const ChainStochParams &P, int n, int na, int lo_a,
                                               int hi_a, int lo_b, int hi_b) {
-  return n < na ? make_tile<BF16>(P, lo_a + n, lo_a, hi_a)
-                : make_tile<BF16>(P, lo_b + (n - na), lo_b, hi_b);
+  return n < na ? make_tile<BF16, CAND>(P, lo_a + n, lo_a, hi_a)
+                : make_tile<BF16, CAND>(P, lo_b + (n - na), lo_b, hi_b);
 }
 
 template <bool BF16, int NV>
@@ -489,10 +506,11 @@ __device__ __forceinline__ float tile_max(const uint32_t (&w)[NV * 4]) {
 }
 
 // Fold one tile into a running (max, sum of exp2((x - max) s2)); element
-// pairs through packed fp32 (one fma and one add per pair).
+// pairs through packed fp32 (one fma and one add per pair).  Returns the
+// largest of the thread's elements of the tile.
 template <bool BF16, int NV>
-__device__ __forceinline__ void tile_accumulate(const uint32_t (&w)[NV * 4], float s2, int tid,
-                                                int nvec, float &m_run, float &s_run) {
+__device__ __forceinline__ float tile_accumulate(const uint32_t (&w)[NV * 4], float s2, int tid,
+                                                 int nvec, float &m_run, float &s_run) {
   using F = Fmt<BF16>;
   const float m = tile_max<BF16, NV>(w);
   const float m_new = fmax_nan(m_run, m);
@@ -515,6 +533,7 @@ __device__ __forceinline__ void tile_accumulate(const uint32_t (&w)[NV * 4], flo
     }
   }
   s_run += (acc0.x + acc0.y) + (acc1.x + acc1.y);
+  return m;
 }
 
 // Warp-specialised stream.  Each CTA owns one contiguous share (even in cost)
@@ -526,7 +545,12 @@ __device__ __forceinline__ void tile_accumulate(const uint32_t (&w)[NV * 4], flo
 // sum) per thread and per law: a run of tiles of one position costs one
 // rescale per tile and a single CTA-wide fold at its end.  Producer and
 // consumers meet only on the full/empty barriers of each stage.
-template <bool BF16, int NV, int S>
+//
+// With CAND (the truncated verify) each consumer thread also stores, for a
+// truncated row, the largest of its elements of the tile (its "chunk": 4
+// vectors, 32 bf16 or 16 fp32 logits), which the fold computes anyway: one
+// 2-byte store per chunk, 1/16 of the bf16 logit bytes.
+template <bool BF16, int NV, int S, bool CAND>
 __global__ void __launch_bounds__(kSoftThreads + 32, kSoftMinBlocks) softmax_partials_kernel(const __grid_constant__ ChainStochParams P) {
   using F = Fmt<BF16>;
   constexpr int NT = kSoftThreads, NW = NT / 32;
@@ -593,7 +617,7 @@ __global__ void __launch_bounds__(kSoftThreads + 32, kSoftMinBlocks) softmax_par
     auto post = [&](int gt, int lo, int hi) {
       if (!next_stage()) return false;
       const int s = issued % S;
-      const TileInfo it = make_tile<BF16>(P, gt, lo, hi);
+      const TileInfo it = make_tile<BF16, CAND>(P, gt, lo, hi);
       ctl.info[s] = it;
       if (tma) {
         const uint32_t bytes = static_cast<uint32_t>(it.len) * ESZ;
@@ -675,6 +699,13 @@ __global__ void __launch_bounds__(kSoftThreads + 32, kSoftMinBlocks) softmax_par
       joined = true;
     }
   };
+  // CAND: the chunk maximum of this thread's vectors of one row's tile, as
+  // the top 16 bits of its order key, for the selection kernel
+  auto store_chunk_max = [&](float m, int row, int t) {
+    const long long at = ((long long)row * nt + t) * NT + tid;
+    if (SV_INB(at, (long long)(2 * K + 1) * B * nt * NT))
+      P.cmax[at] = static_cast<unsigned short>(order_key<false>(__float_as_uint(m)) >> 16);
+  };
   // Stages arrive in the producer's order until its end marker (len < 0).
   for (int n = 0;; ++n, s = (s + 1 == S) ? 0 : s + 1, parity ^= (s == 0)) {
     bool timed_out = false;
@@ -693,7 +724,7 @@ __global__ void __launch_bounds__(kSoftThreads + 32, kSoftMinBlocks) softmax_par
     TileInfo it;
     if (timed_out) {
       if (n >= my_tiles) break;
-      it = rebuild_tile<BF16>(P, n, na, lo_a, hi_a, lo_b, hi_b);
+      it = rebuild_tile<BF16, CAND>(P, n, na, lo_a, hi_a, lo_b, hi_b);
     } else {
       it = ctl.info[s];
       if (it.len < 0) break;  // end marker
@@ -753,7 +784,12 @@ __global__ void __launch_bounds__(kSoftThreads + 32, kSoftMinBlocks) softmax_par
       mp = mq = -kInf;
       sp = sq = 0.f;
     }
-    tile_accumulate<BF16, NV>(wp, s2, tid, nvec, mp, sp);
+    {
+      const float cm = tile_accumulate<BF16, NV>(wp, s2, tid, nvec, mp, sp);
+      if constexpr (CAND) {
+        if (it.sketch) store_chunk_max(cm, it.trow, it.t);
+      }
+    }
     if (pair) {
       load_tile<BF16, NV>(wp, tma, sbase + half, static_cast<const char *>(P.draft) + it.dsrc, tid, nvec,
                           it.len);
@@ -766,7 +802,12 @@ __global__ void __launch_bounds__(kSoftThreads + 32, kSoftMinBlocks) softmax_par
       mbar_arrive(&ctl.empty[s]);
     }
     if (warp_to) run_to = F_TIMEOUT;
-    if (pair) tile_accumulate<BF16, NV>(wp, s2, tid, nvec, mq, sq);
+    if (pair) {
+      const float cm = tile_accumulate<BF16, NV>(wp, s2, tid, nvec, mq, sq);
+      if constexpr (CAND) {
+        if (it.sketch) store_chunk_max(cm, it.drow, it.t);
+      }
+    }
 
     if (it.last && SV_INB(runs % (2 * S), 2 * kMaxStages)) {  // the run ends: fold the CTA's partials
       join_generation();
@@ -1913,23 +1954,6 @@ __global__ void __launch_bounds__(kDriftThreads, 2) drift_select_kernel(const __
   }
 }
 
-// ============================================================ truncation
-//
-// "Speculative Decoding: Draft, Verify, and Correct", 'Preserve the
-// distribution you actually intend': when top-k / top-p define the sampling
-// law, acceptance and correction use the truncated p, and q is the truncated
-// law that produced the draft.  Per logit row this kernel finds the key
-// threshold theta of the kept set -- top-k: the largest theta with at least
-// k keys >= theta (boundary ties kept); then top-p: the largest theta whose
-// keys >= theta carry at least top_p of the top-k mass -- and the kept mass.
-// Both searches are bisections on the integer key over a candidate list
-// (every key at or above a sampled threshold); rows the candidates cannot
-// settle are searched over the whole row.  Sums run in a fixed order, so
-// the result is deterministic.
-
-
-// Largest key x (0 .. 2^bits - 1) with pred(x) true, pred being monotone
-// (true for small x).
 // DRIFT, third kernel: one CTA per row, a programmatic dependent of the
 // draft rows' statistics grid (which completes only after the selection grid
 // has), so both grids' writes are visible after its dependency wait.  Each
@@ -2000,6 +2024,8 @@ __global__ void __launch_bounds__(kDriftFinishThreads) drift_finish_kernel(const
   }
 }
 
+// Largest key x (0 .. 2^bits - 1) with pred(x) true, pred being monotone
+// (true for small x).
 template <typename Pred>
 __device__ __forceinline__ uint32_t largest_key(int bits, Pred pred) {
   uint32_t x = 0;
@@ -2010,47 +2036,126 @@ __device__ __forceinline__ uint32_t largest_key(int bits, Pred pred) {
   return x;
 }
 
-// The truncation CTA: 512 threads, two per SM (256 threads at four per SM
-// measured slower: 90.6 against 85.7 us on the c3 truncated step).
-constexpr int kTruncThreads = 512;
-constexpr int kTruncWarps = kTruncThreads / 32;
+// ============================================================ truncation
+//
+// "Speculative Decoding: Draft, Verify, and Correct", 'Preserve the
+// distribution you actually intend': when top-k / top-p define the sampling
+// law, acceptance and correction use the truncated p, and q is the truncated
+// law that produced the draft.  Per logit row the selection kernel finds the
+// key threshold theta of the kept set -- top-k: the largest theta with at
+// least k keys >= theta (boundary ties kept); then top-p: the largest theta
+// whose keys >= theta carry at least top_p of the top-k mass -- and the kept
+// mass.  Sums run in a fixed order, so the result is deterministic.
+//
+// The ring stream (CAND) leaves, for every truncated logit row, the maximum
+// of each consumer thread's chunk of every tile.  The k-th largest chunk
+// maximum is at most the row's k-th largest logit (k chunks hold a logit at
+// least that large), so every logit the top-k keeps lies in a chunk whose
+// maximum reaches it: the selection re-reads only those chunks (about k of
+// c3's 4096) and takes their logits at or above it as candidates.  A row
+// whose candidates cannot settle the thresholds (too many chunks or
+// candidates, or a nucleus that reaches below them) takes a sampled
+// threshold and lists its candidates in a pass over its own logits, and
+// after that searches the whole row.
+
+// The sample rank r of a row's sampled threshold: about r * kDriftSample of
+// its keys reach the r-th largest sampled key.
+__device__ __forceinline__ int trunc_sample_rank(int tk) {
+  return tk > 0 ? max(16, (2 * tk) / kDriftSample + 2) : 16;
+}
+
+// The selection CTA: 192 threads, six per SM (c3's 704 logit rows in one
+// wave; 56 registers, none spilled -- at 256 threads and five per SM the
+// kernel spilled, and its warp sort ran 7 times slower).
+constexpr int kSelThreads = 192;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kMaxRowTiles = (SPEC_MAX_V + kSoftMinSlice - 1) / kSoftMinSlice;
+constexpr int kMaxRowChunks = kMaxRowTiles * kSoftThreads;
+constexpr int kMaxSelChunks = 256;  // chunks one row re-reads at most
+constexpr int kTopPChunks = 64;     // chunks a top-p-only row starts from
+
+// The r-th largest of n 16-bit keys in shared memory (n even, 1 <= r <= n),
+// bit by bit from the top: the largest th with at least r keys >= th.  Each
+// step is one block-wide count; red holds two rounds of per-warp counts.
+// Every thread of the block calls it.
+template <int NT>
+__device__ uint32_t kth_largest_key16(const unsigned short *keys, int n, int r, int (*red)[NT / 32]) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t *wk = reinterpret_cast<const uint32_t *>(keys);
+  const int nw = n / 2;
+  uint32_t th = 0;
+#pragma unroll 1
+  for (int bit = 15; bit >= 0; --bit) {
+    const uint32_t c = th | (1u << bit);
+    int cnt = 0;
+    for (int w = tid; w < nw; w += NT) {
+      const uint32_t x = wk[w];
+      cnt += ((x & 0xFFFFu) >= c ? 1 : 0) + ((x >> 16) >= c ? 1 : 0);
+    }
+    cnt = __reduce_add_sync(FULL_MASK, cnt);
+    int *slot = red[bit & 1];
+    if (lane == 0) slot[warp] = cnt;
+    __syncthreads();
+    int tot = 0;
+#pragma unroll
+    for (int w2 = 0; w2 < NT / 32; ++w2) tot += slot[w2];
+    if (tot >= r) th = c;
+  }
+  return th;
+}
 
 struct alignas(16) TruncCtrl {
-  unsigned long long ck[kDriftCand];  // (key << 32) | (~token id): sorts key desc, id asc
-  float e[kDriftCand];                // candidate masses, then their prefix sums
-  float fred[kTruncWarps];
-  int ired[kTruncWarps];
+  // the row's chunk maxima, then (once they are used) the candidates:
+  // (key << 32) | (~token id), which sorts key desc, id asc, and their
+  // masses, then prefix sums
+  union {
+    unsigned short chunk[kMaxRowChunks];
+    struct {
+      unsigned long long ck[kDriftCand];
+      float e[kDriftCand];
+    };
+  };
+  int clist[kMaxSelChunks];  // chunks to re-read
+  uint32_t aux[kSelThreads]; // the threads' largest keys, then the keys above their bound
+  int cred[2][kSelWarps];    // counts of the threshold search
+  int n_surv;
+  uint32_t bound;
+  int settled;               // warp 0's settling of a small list: 1 done, 0 retry
+  uint32_t theta_w;
+  float kept_w;
+  float fred[kSelWarps];
+  int ired[kSelWarps];
   int chist[256];
-  float wm[kTruncWarps];
-  int n_cand, digit, above, pos;
+  int n_cand, n_chunks, digit, above, pos;
   float M, S;
   uint32_t flags;
 };
 
 template <bool BF16>
-__global__ void __launch_bounds__(kTruncThreads) trunc_kernel(const __grid_constant__ ChainStochParams P) {
+__global__ void __launch_bounds__(kSelThreads, 6) trunc_select_kernel(const __grid_constant__ ChainStochParams P) {
   using F = Fmt<BF16>;
   constexpr int EPV = F::EPV, ESZ = F::ESZ;
   constexpr int KEYBITS = BF16 ? 16 : 32;
   __shared__ TruncCtrl ctl;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int K = P.K, V = P.V, npos = K + 1;
+  const int K = P.K, V = P.V, npos = K + 1, nt = P.nslices;
   // CTAs in batch-row order (row b's target positions, then its drafts), so
   // rows complete one after another and the resolve kernel, which polls each
-  // row's records, finishes most rows while this grid still runs.  Logit
-  // rows are numbered targets b*(K+1)+j, then drafts B*(K+1)+b*K+j.
+  // row's records, finishes most rows while this grid still runs.
   const int b = blockIdx.x / (npos + K), q = blockIdx.x - b * (npos + K);
   const bool is_target = q < npos;
   const int j = is_target ? q : q - npos;
   const int row = is_target ? b * npos + j : P.B * npos + b * K + j;
-  // a plain launch: the generation step (this call's tag) has completed
+  // The stream has completed, and with it the generation step: its tile
+  // records and chunk maxima are in, and the tag read below is this call's.
+  grid_dependency_wait();
   allow_dependents();
   // forced-timeout test: no record of this call appears, so the resolve
   // kernel's bounded wait gives up
   if (P.force_timeout) return;
   int tk;
   float tp;
-  const bool active = trunc_active(P, b, V, &tk, &tp);
+  if (!trunc_active(P, b, V, &tk, &tp)) return;
   float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
   if (!(T > 0.f && T < kInf)) T = 1.0f;  // the resolve kernel flags the row
   const float s2 = __fdiv_rn(kLog2e, T);
@@ -2062,22 +2167,13 @@ __global__ void __launch_bounds__(kTruncThreads) trunc_kernel(const __grid_const
     if constexpr (BF16) return __ldg(reinterpret_cast<const unsigned short *>(src) + i);
     else return __ldg(reinterpret_cast<const unsigned int *>(src) + i);
   };
-  // the draft token's logit, stamped like the records
-  if (tid == 0 && j < K && P.tokens) {
-    const int y = __ldg(P.tokens + (size_t)b * K + j);
-    if (y >= 0 && y < V) {
-      const uint32_t bits = bits_at(y);
-      const float l = BF16 ? __uint_as_float(bits << 16) : __uint_as_float(bits);
-      st_relaxed_u64(P.ylog + row, __float_as_uint(l) | (static_cast<unsigned long long>(tag) << 32));
-    }
-  }
   // block sums in a fixed order
   auto block_sum_i = [&](int v) {
     v = __reduce_add_sync(FULL_MASK, v);
     if (lane == 0) ctl.ired[warp] = v;
     __syncthreads();
     int t = 0;
-    for (int w2 = 0; w2 < kTruncWarps; ++w2) t += ctl.ired[w2];
+    for (int w2 = 0; w2 < kSelWarps; ++w2) t += ctl.ired[w2];
     __syncthreads();
     return t;
   };
@@ -2087,79 +2183,97 @@ __global__ void __launch_bounds__(kTruncThreads) trunc_kernel(const __grid_const
     if (lane == 0) ctl.fred[warp] = v;
     __syncthreads();
     float t = 0.f;
-    for (int w2 = 0; w2 < kTruncWarps; ++w2) t += ctl.fred[w2];
+    for (int w2 = 0; w2 < kSelWarps; ++w2) t += ctl.fred[w2];
     __syncthreads();
     return t;
   };
-  // ---- sampled threshold tau (as in the DRIFT selection): the r-th largest
-  // sample, the samples being the elements of every kDriftSample-th 16-byte
-  // vector (one logit in kDriftSample, one DRAM sector per vector)
-  constexpr int kNSV = (SPEC_MAX_V + EPV * kDriftSample * kTruncThreads - 1) / (EPV * kDriftSample * kTruncThreads);
-  uint32_t smp[kNSV][4];  // this thread's sampled vectors, loaded once
-  if (active) {
-#pragma unroll
-    for (int q = 0; q < kNSV; ++q)
-      F::load_vec(smp[q], nullptr, src, aligned, (tid + q * kTruncThreads) * kDriftSample, V);
+  // The chunk maxima a row starts from: rc of them, the row's top_k, or
+  // kTopPChunks for top-p alone.  Their copy into shared memory starts now
+  // and lands while warp 0 folds the records.
+  const int nch = nt * kSoftThreads;
+  const int rc = tk > 0 ? tk : min(kTopPChunks, nch);
+  const bool use_chunks = rc <= kMaxSelChunks && rc <= nch && nch <= kMaxRowChunks;
+  if (use_chunks) {
+    const uint4 *srcm = reinterpret_cast<const uint4 *>(P.cmax + (size_t)row * nch);
+    const int nv = nch / 8;  // every row's maxima start 512-byte aligned
+    for (int v = tid; v < nv; v += kSelThreads)
+      if (SV_INB((long long)row * nv + v, (long long)P.B * (2 * K + 1) * nv))
+        cp_async16(reinterpret_cast<uint4 *>(ctl.chunk) + v, srcm + v);
   }
-  const int n_samples = sampled_count(V, EPV);
-  auto samples = [&](auto f) {
+  // The row's tile records (lane t of warp 0: tiles t and t + 32), loaded
+  // now and folded once the candidates are gathered.
+  unsigned long long rec_a[2] = {0ull, 0ull}, rec_b[2] = {0ull, 0ull};
+  if (warp == 0) {
 #pragma unroll
-    for (int q = 0; q < kNSV; ++q) {
-      const int v = (tid + q * kTruncThreads) * kDriftSample;
-#pragma unroll
-      for (int e = 0; e < EPV; ++e)
-        if (v * EPV + e < V) f(order_key<BF16>(elem_bits<BF16>(smp[q], e)));
+    for (int h = 0; h < 2; ++h) {
+      const int t = lane + 32 * h;
+      if (t < nt && SV_INB((long long)row * nt + t, (long long)P.B * (2 * K + 1) * nt)) {
+        rec_a[h] = ld_relaxed_u64(&P.part[(size_t)row * nt + t].a);
+        rec_b[h] = ld_relaxed_u64(&P.part[(size_t)row * nt + t].b);
+      }
     }
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  SoftPart *rec = P.trunc + row;
+  float nM = 0.f;  // -M s2, once the records are folded
+  auto mass_of = [&](uint32_t bits) {  // exp2((l - M) s2) of one element
+    const float l = BF16 ? __uint_as_float(bits << 16) : __uint_as_float(bits);
+    return l == -kInf ? 0.f : ex2(__fmaf_rn(l, s2, nM));
   };
+  // ---- other listing thresholds: the r-th largest of every kDriftSample-th
+  // vector's keys, as the listing kernel takes them
+  constexpr int kNSV = (SPEC_MAX_V + EPV * kDriftSample * kSelThreads - 1) / (EPV * kDriftSample * kSelThreads);
+  const int n_samples = sampled_count(V, EPV);
   auto sample_tau = [&](int r) -> uint32_t {
     if (r > n_samples) return 0u;
+    uint32_t smp[kNSV][4];
+#pragma unroll
+    for (int q2 = 0; q2 < kNSV; ++q2)
+      F::load_vec(smp[q2], nullptr, src, aligned, (tid + q2 * kSelThreads) * kDriftSample, V);
+    auto samples = [&](auto f) {
+#pragma unroll
+      for (int q2 = 0; q2 < kNSV; ++q2) {
+        const int v = (tid + q2 * kSelThreads) * kDriftSample;
+#pragma unroll
+        for (int e = 0; e < EPV; ++e)
+          if (v * EPV + e < V) f(order_key<BF16>(elem_bits<BF16>(smp[q2], e)));
+      }
+    };
     int na, ne;
-    return block_kth_largest<KEYBITS, kTruncThreads>(samples, r, ctl.chist, &ctl.digit, &ctl.above,
-                                                    na, ne);
+    return block_kth_largest<KEYBITS, kSelThreads>(samples, r, ctl.chist, &ctl.digit, &ctl.above, na, ne);
   };
-  // ---- one pass over the row.  With stats == 2 it forms the row's max and
-  // sum of exp2((l - m) s2), each thread against its own running max; with
-  // stats == 1 the max alone; with `cands` it lists every key >= tau (a lane
-  // visits only its elements not below tau and appends them one by one: they
-  // are sorted later).  Returns the candidate count.
-  float m = -kInf, sacc = 0.f;
-  auto pass = [&](int stats, bool cands, uint32_t tau) {
+  // ---- one pass over the row listing every key >= tau (a lane visits only
+  // its elements not below tau and appends them one by one: they are sorted
+  // later).  Returns the candidate count.
+  auto pass = [&](uint32_t tau) {
     if (tid == 0) ctl.n_cand = 0;
     const float tau_f = key_value<BF16>(tau);
     const uint32_t tau_w = pack_threshold<BF16>(tau_f);
     __syncthreads();
-    constexpr int U = 4;
-    // two batches of U vectors per thread in flight, then each in turn
-    // (vectors past the row read as -inf and list nothing: their index is >= V)
-    for (int v00 = tid; v00 < nvec; v00 += 2 * U * kTruncThreads) {
+    constexpr int U = 2;
+    for (int v00 = tid; v00 < nvec; v00 += 2 * U * kSelThreads) {
       uint32_t wab[2][U][4];
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int u = 0; u < U; ++u)
-          F::load_vec(wab[h][u], nullptr, src, aligned, v00 + (h * U + u) * kTruncThreads, V);
+          F::load_vec(wab[h][u], nullptr, src, aligned, v00 + (h * U + u) * kSelThreads, V);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        uint32_t (&w)[U][4] = wab[h];
-        const int v0 = v00 + h * U * kTruncThreads;
-        if (stats == 2) online_accumulate<BF16, U>(w, s2, m, sacc);
-        else if (stats == 1) online_max<BF16, U>(w, m);
-        if (cands) {
+        const int v0 = v00 + h * U * kSelThreads;
 #pragma unroll
-          for (int u = 0; u < U; ++u) {
-            // the elements not below tau, one at a time (rarely more than one
-            // in a vector: a lane's loop is as long as its own count)
-            uint32_t msk = may_reach_bits<BF16>(w[u], tau_w, tau_f);
-            while (msk) {
-              const int e = __ffs(msk) - 1;
-              msk &= msk - 1;
-              const int idx = (v0 + u * kTruncThreads) * EPV + e;
-              const uint32_t k = order_key<BF16>(elem_bits_at<BF16>(w[u], e));
-              if (k >= tau && idx < V) {
-                const int slot = atomicAdd(&ctl.n_cand, 1);
-                if (slot < kDriftCand)
-                  ctl.ck[slot] = (static_cast<unsigned long long>(k) << 32) | (~static_cast<uint32_t>(idx));
-              }
+        for (int u = 0; u < U; ++u) {
+          uint32_t msk = may_reach_bits<BF16>(wab[h][u], tau_w, tau_f);
+          while (msk) {
+            const int e = __ffs(msk) - 1;
+            msk &= msk - 1;
+            const int idx = (v0 + u * kSelThreads) * EPV + e;
+            const uint32_t k = order_key<BF16>(elem_bits_at<BF16>(wab[h][u], e));
+            if (k >= tau && idx < V) {
+              const int slot = atomicAdd(&ctl.n_cand, 1);
+              if (slot < kDriftCand)
+                ctl.ck[slot] = (static_cast<unsigned long long>(k) << 32) | (~static_cast<uint32_t>(idx));
             }
           }
         }
@@ -2168,51 +2282,129 @@ __global__ void __launch_bounds__(kTruncThreads) trunc_kernel(const __grid_const
     __syncthreads();
     return ctl.n_cand;
   };
-  int r = tk > 0 ? max(16, (2 * tk) / kDriftSample + 2) : 16;
-  uint32_t tau = active ? sample_tau(r) : 0u;
-  // Under top-k the law's normaliser is the kept mass, summed over the
-  // candidates, so the row needs only its max (no exp per logit: the pass is
-  // bound by the exp unit otherwise).  Untruncated and top-p-only rows need
-  // the full sum.
-  const bool full_sum = !active || tk == 0;
-  int nc = pass(full_sum ? 2 : 1, active, tau);
-  // ---- the row's max and sum: warps, then warp 0 in a fixed order
-  {
-    float Mw, Sw;
-    fold_max_sum(m, sacc, s2, &Mw, &Sw);
-    if (lane == 0) {
-      ctl.wm[warp] = Mw;
-      ctl.fred[warp] = Sw;
+  // ---- the candidates from the chunk maxima: the rc-th largest maximum is
+  // the threshold; returns the candidate count, or -1 when the chunks cannot
+  // give a list (the row's maxima do not fit, or too many chunks reach it)
+  auto gather_chunks = [&]() -> int {
+    if (!use_chunks) return -1;
+    if (tid == 0) {
+      ctl.n_chunks = 0;
+      ctl.n_cand = 0;
+    }
+    // The threshold th is the rc-th largest maximum.  A lower bound first:
+    // the rc-th largest of the threads' largest keys (rc threads hold a key at
+    // least that large, so at least rc keys reach it); only the keys that
+    // reach it can be th, and warp 0 searches those when they are few.
+    const uint32_t *wk = reinterpret_cast<const uint32_t *>(ctl.chunk);
+    const int nw = nch / 2;
+    auto warp_kth = [&](int n) {  // warp 0: the rc-th largest of aux[0 .. n), n <= kSelThreads
+      constexpr int PL = kSelThreads / 32;
+      uint32_t v[PL];
+#pragma unroll
+      for (int i = 0; i < PL; ++i) v[i] = lane + 32 * i < n ? ctl.aux[lane + 32 * i] : 0u;
+      uint32_t x = 0;
+#pragma unroll 1
+      for (int bit = 15; bit >= 0; --bit) {  // (a candidate is >= 1: padding never counts)
+        const uint32_t c = x | (1u << bit);
+        int cnt = 0;
+#pragma unroll
+        for (int i = 0; i < PL; ++i) cnt += v[i] >= c ? 1 : 0;
+        if (static_cast<int>(__reduce_add_sync(FULL_MASK, static_cast<unsigned>(cnt))) >= rc) x = c;
+      }
+      return x;
+    };
+    {
+      uint32_t tmax = 0;
+      for (int w = tid; w < nw; w += kSelThreads) {
+        const uint32_t x = wk[w];
+        tmax = max(tmax, max(x & 0xFFFFu, x >> 16));
+      }
+      ctl.aux[tid] = tmax;
     }
     __syncthreads();
     if (warp == 0) {
-      const float mw = lane < kTruncWarps ? ctl.wm[lane] : -kInf;
-      const float sw = lane < kTruncWarps ? ctl.fred[lane] : 0.f;
-      fold_max_sum(mw, sw, s2, &Mw, &Sw);
+      const uint32_t lb = warp_kth(kSelThreads);
       if (lane == 0) {
-        ctl.M = Mw;
-        ctl.S = Sw;
-        ctl.flags = (Mw != Mw || Mw == kInf || Mw == -kInf) ? 1u : 0u;
-        // one record per logit row (the truncated verify's slice is the row)
-        store_part(P.part + row, Mw, Sw, 0u, tag);
+        ctl.bound = lb;
+        ctl.n_surv = 0;
       }
     }
     __syncthreads();
-  }
-  if (!active) return;
-  SoftPart *rec = P.trunc + row;
-  if (ctl.flags) {  // the resolve kernel flags this row from the same record
-    if (tid == 0) store_part(rec, 0.f, 0.f, 1u, tag);
-    return;
-  }
-  const float nM = -__fmul_rn(ctl.M, s2);
-  auto mass_of = [&](uint32_t bits) {  // exp2((l - M) s2) of one element
-    const float l = BF16 ? __uint_as_float(bits << 16) : __uint_as_float(bits);
-    return l == -kInf ? 0.f : ex2(__fmaf_rn(l, s2, nM));
+    {
+      const uint32_t lb = ctl.bound;
+      for (int w = tid; w < nw; w += kSelThreads) {
+        const uint32_t x = wk[w];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t k = h ? (x >> 16) : (x & 0xFFFFu);
+          if (k >= lb) {
+            const int slot = atomicAdd(&ctl.n_surv, 1);
+            if (slot < kSelThreads) ctl.aux[slot] = k;
+          }
+        }
+      }
+    }
+    __syncthreads();
+    uint32_t th;
+    if (ctl.n_surv <= kSelThreads) {
+      if (warp == 0) {
+        const uint32_t x = warp_kth(ctl.n_surv);
+        if (lane == 0) ctl.bound = x;
+      }
+      __syncthreads();
+      th = ctl.bound;
+    } else {
+      th = kth_largest_key16<kSelThreads>(ctl.chunk, nch, rc, ctl.cred);
+    }
+    // the chunks whose maximum reaches it
+    for (int c = tid; c < nch; c += kSelThreads) {
+      if (ctl.chunk[c] >= th) {
+        const int slot = atomicAdd(&ctl.n_chunks, 1);
+        if (slot < kMaxSelChunks) ctl.clist[slot] = c;
+      }
+    }
+    __syncthreads();
+    const int nsel = ctl.n_chunks;
+    if (nsel > kMaxSelChunks) return -1;
+    // their vectors, all loads in flight at once, then every logit whose key
+    // reaches th (the maxima keep the top 16 bits of a logit's key)
+    constexpr int PERV = (kMaxSelChunks * kSoftVecs + kSelThreads - 1) / kSelThreads;
+    uint32_t w[PERV][4];
+    int vid[PERV];
+#pragma unroll
+    for (int q2 = 0; q2 < PERV; ++q2) {
+      const int i = tid + q2 * kSelThreads;  // (chunk i / kSoftVecs, vector i % kSoftVecs)
+      vid[q2] = -1;
+      if (i < nsel * kSoftVecs) {
+        const int c = ctl.clist[i / kSoftVecs];
+        const int t = c / kSoftThreads, lt = c - t * kSoftThreads;
+        vid[q2] = t * (kSoftThreads * kSoftVecs) + lt + (i % kSoftVecs) * kSoftThreads;
+      }
+      F::load_vec(w[q2], nullptr, src, aligned, vid[q2] < 0 ? nvec : vid[q2], V);
+    }
+    __syncthreads();  // the maxima are read: the candidates may overwrite them
+#pragma unroll
+    for (int q2 = 0; q2 < PERV; ++q2) {
+      if (vid[q2] < 0) continue;
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const uint32_t bits = elem_bits<BF16>(w[q2], e);
+        const uint32_t k = order_key<BF16>(bits);
+        const uint32_t k16 = BF16 ? k : (k >> 16);
+        const int idx = vid[q2] * EPV + e;
+        if (k16 >= th && idx < V) {
+          const int slot = atomicAdd(&ctl.n_cand, 1);
+          if (slot < kDriftCand)
+            ctl.ck[slot] = (static_cast<unsigned long long>(k) << 32) | (~static_cast<uint32_t>(idx));
+        }
+      }
+    }
+    __syncthreads();
+    return ctl.n_cand;
   };
   // the listed candidates' masses, from their keys, once M is known
   auto fill_masses = [&](int n) {
-    for (int i = tid; i < min(n, kDriftCand); i += kTruncThreads) {
+    for (int i = tid; i < min(n, kDriftCand); i += kSelThreads) {
       const float l = key_value<BF16>(static_cast<uint32_t>(ctl.ck[i] >> 32));
       ctl.e[i] = l == -kInf ? 0.f : ex2(__fmaf_rn(l, s2, nM));
     }
@@ -2223,14 +2415,14 @@ __global__ void __launch_bounds__(kTruncThreads) trunc_kernel(const __grid_const
   auto sort_and_scan = [&](int nc) {
     int N = 64;
     while (N < nc) N <<= 1;
-    for (int i = nc + tid; i < N; i += kTruncThreads) {
+    for (int i = nc + tid; i < N; i += kSelThreads) {
       ctl.ck[i] = 0ull;
       ctl.e[i] = 0.f;
     }
     __syncthreads();
     for (int size = 2; size <= N; size <<= 1) {  // bitonic, descending
       for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        for (int t = tid; t < N / 2; t += kTruncThreads) {
+        for (int t = tid; t < N / 2; t += kSelThreads) {
           const int lo = 2 * t - (t & (stride - 1)), hi = lo + stride;
           const bool up = (lo & size) == 0;
           const unsigned long long a = ctl.ck[lo], c = ctl.ck[hi];
@@ -2245,8 +2437,8 @@ __global__ void __launch_bounds__(kTruncThreads) trunc_kernel(const __grid_const
         __syncthreads();
       }
     }
-    // inclusive prefix sums in sorted order: four consecutive per thread
-    constexpr int PER = kDriftCand / kTruncThreads;
+    // inclusive prefix sums in sorted order: PER consecutive per thread
+    constexpr int PER = (kDriftCand + kSelThreads - 1) / kSelThreads;
     float v[PER], run = 0.f;
 #pragma unroll
     for (int q = 0; q < PER; ++q) {
@@ -2332,15 +2524,124 @@ __global__ void __launch_bounds__(kTruncThreads) trunc_kernel(const __grid_const
     }
     __syncthreads();
   };
+  // A list of at most 64 candidates, settled without a sorting network:
+  // thread i < n takes candidate i's mass and its rank (the candidates whose
+  // (key, ~id) is larger: the keys are unique) and puts both at that rank,
+  // which is the order of warp_sort_and_scan; warp 0 then forms its prefix
+  // sums and the boundaries of the code below (the k-th key's group of ties;
+  // the first prefix that reaches top_p of the kept mass, and its group) by
+  // ballots.  The same arithmetic in the same order gives the same threshold
+  // and kept mass.
+  auto settle_small = [&](int n) {
+    unsigned long long *sk = ctl.ck + kDriftCand / 2;  // the sorted keys (n <= 64)
+    if (tid < n) {
+      const unsigned long long mine = ctl.ck[tid];
+      int rank = 0;
+#pragma unroll 4
+      for (int j2 = 0; j2 < n; ++j2) rank += ctl.ck[j2] > mine ? 1 : 0;
+      const float l = key_value<BF16>(static_cast<uint32_t>(mine >> 32));
+      sk[rank] = mine;
+      ctl.e[rank] = l == -kInf ? 0.f : ex2(__fmaf_rn(l, s2, nM));
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    unsigned long long k[2];
+    float e[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = lane + 32 * h;
+      k[h] = i < n ? sk[i] : 0ull;
+      e[h] = i < n ? ctl.e[i] : 0.f;
+    }
+    float s0 = e[0], s1 = e[1];
+#pragma unroll 1
+    for (int o = 1; o < 32; o <<= 1) {
+      const float n0 = __shfl_up_sync(FULL_MASK, s0, o), n1 = __shfl_up_sync(FULL_MASK, s1, o);
+      if (lane >= o) {
+        s0 += n0;
+        s1 += n1;
+      }
+    }
+    s1 += __shfl_sync(FULL_MASK, s0, 31);
+    const uint32_t k0 = static_cast<uint32_t>(k[0] >> 32), k1 = static_cast<uint32_t>(k[1] >> 32);
+    auto key_at_w = [&](int i) {  // sorted entry i's key (every lane gets it)
+      const uint32_t a0 = __shfl_sync(FULL_MASK, k0, i & 31), a1 = __shfl_sync(FULL_MASK, k1, i & 31);
+      return i < 32 ? a0 : a1;
+    };
+    auto prefix_at_w = [&](int i) {
+      const float a0 = __shfl_sync(FULL_MASK, s0, i & 31), a1 = __shfl_sync(FULL_MASK, s1, i & 31);
+      return i < 32 ? a0 : a1;
+    };
+    auto group_end = [&](int i) {  // last entry (< n) with entry i's key
+      const uint32_t ki = key_at_w(i);
+      const unsigned b0 = __ballot_sync(FULL_MASK, lane < n && k0 == ki);
+      const unsigned b1 = __ballot_sync(FULL_MASK, lane + 32 < n && k1 == ki);
+      return b1 ? 63 - __clz(b1) : 31 - __clz(b0);
+    };
+    int gk = n - 1;
+    float Sk = ctl.S;
+    if (tk > 0) {
+      gk = group_end(tk - 1);
+      Sk = prefix_at_w(gk);
+    }
+    int ok = 1;
+    uint32_t th = 0;
+    float kp = 0.f;
+    if (tp < 1.f) {
+      const float target = __fmul_rn(tp, Sk);
+      if (tk == 0 && !(prefix_at_w(n - 1) >= target)) {
+        ok = 0;
+      } else {
+        const unsigned c0 = __ballot_sync(FULL_MASK, lane <= gk && s0 >= target);
+        const unsigned c1 = __ballot_sync(FULL_MASK, lane + 32 <= gk && s1 >= target);
+        const int pos = c0 ? __ffs(c0) - 1 : (c1 ? 31 + __ffs(c1) : gk);
+        th = key_at_w(pos);
+        kp = prefix_at_w(group_end(pos));
+      }
+    } else {
+      th = key_at_w(gk);
+      kp = Sk;
+    }
+    if (lane == 0) {
+      ctl.settled = ok;
+      ctl.theta_w = th;
+      ctl.kept_w = kp;
+    }
+  };
   uint32_t theta = 0;
   float kept = 0.f;
   bool done = false;
-  for (int attempt = 0; attempt < 3 && !done; ++attempt) {
-    if (attempt > 0) {  // another threshold: list the candidates again
-      tau = sample_tau(r);
-      nc = pass(0, true, tau);
+  int r = trunc_sample_rank(tk);
+  int nc = gather_chunks();
+  // ---- the row's max and sum from the stream's tile records (warp 0); a
+  // record missing or flagged, or a non-finite or empty row, gets no
+  // thresholds (the resolve kernel reports the row from the same records)
+  if (warp == 0) {
+    float Mw, Sw;
+    uint32_t f = 0;
+    const bool ready = fold_slice_stats(nt, lane, s2, [&](int t, float *m, float *s) {
+      uint32_t qf = 0;
+      const int h = t >> 5;  // t = lane + 32 h
+      const bool ok = decode_part(h ? rec_a[1] : rec_a[0], h ? rec_b[1] : rec_b[0], tag, m, s, &qf);
+      f |= qf;
+      return ok;
+    }, &Mw, &Sw);
+    f = __reduce_or_sync(FULL_MASK, f);
+    if (lane == 0) {
+      ctl.M = Mw;
+      ctl.S = Sw;
+      ctl.flags = (!ready || f || Mw != Mw || Mw == kInf || Mw == -kInf) ? 1u : 0u;
     }
-    fill_masses(nc);
+  }
+  __syncthreads();
+  if (ctl.flags) {
+    if (tid == 0) store_part(rec, 0.f, 0.f, 1u, tag);
+    return;
+  }
+  nM = -__fmul_rn(ctl.M, s2);
+  // attempt 0 takes the chunks' candidates; 1 to 3 a sampled threshold each
+  for (int attempt = nc >= 0 ? 0 : 1; attempt < 4 && !done; ++attempt) {
+    if (attempt > 0) nc = pass(sample_tau(r));
     if (nc > kDriftCand) {  // too many: raise the threshold
       if (r <= 1) break;
       r = max(1, r / 4);
@@ -2350,24 +2651,39 @@ __global__ void __launch_bounds__(kTruncThreads) trunc_kernel(const __grid_const
       r *= 4;
       continue;
     }
+    if (nc <= 64) {  // a small list: ranks, then warp 0
+      settle_small(nc);
+      __syncthreads();
+      if (!ctl.settled) {  // (top-p alone) the nucleus reaches below the list
+        r *= 4;
+        __syncthreads();
+        continue;
+      }
+      theta = ctl.theta_w;
+      kept = ctl.kept_w;
+      done = true;
+      break;
+    }
+    fill_masses(nc);
     // With top-k only the candidates at or above the k-th largest key (ties
     // included) can be kept, and the nucleus lies among them: select that key
     // by radix, keep those candidates, sort only them.  Their order and prefix
-    // sums are those of the full sort's first entries.
+    // sums are those of the full sort's first entries, so a set of 64 or
+    // fewer goes to the warp sort whole.
     int ns = nc;
-    if (tk > 0) {
+    if (tk > 0 && nc > 64) {
       auto cand_keys = [&](auto f) {
-        for (int i = tid; i < nc; i += kTruncThreads) f(key_at(i));
+        for (int i = tid; i < nc; i += kSelThreads) f(key_at(i));
       };
       int na, ne;
-      const uint32_t thk = block_kth_largest<KEYBITS, kTruncThreads>(cand_keys, tk, ctl.chist, &ctl.digit,
+      const uint32_t thk = block_kth_largest<KEYBITS, kSelThreads>(cand_keys, tk, ctl.chist, &ctl.digit,
                                                                     &ctl.above, na, ne);
-      constexpr int PER = kDriftCand / kTruncThreads;
+      constexpr int PER = (kDriftCand + kSelThreads - 1) / kSelThreads;
       unsigned long long kk[PER];
       float ee[PER];
 #pragma unroll
       for (int q = 0; q < PER; ++q) {
-        const int i = tid + q * kTruncThreads;
+        const int i = tid + q * kSelThreads;
         kk[q] = i < nc ? ctl.ck[i] : 0ull;
         ee[q] = i < nc ? ctl.e[i] : 0.f;
       }
@@ -2375,7 +2691,7 @@ __global__ void __launch_bounds__(kTruncThreads) trunc_kernel(const __grid_const
       __syncthreads();
 #pragma unroll
       for (int q = 0; q < PER; ++q) {
-        const int i = tid + q * kTruncThreads;
+        const int i = tid + q * kSelThreads;
         if (i < nc && static_cast<uint32_t>(kk[q] >> 32) >= thk) {
           const int slot = atomicAdd(&ctl.n_cand, 1);
           ctl.ck[slot] = kk[q];
@@ -2432,12 +2748,12 @@ __global__ void __launch_bounds__(kTruncThreads) trunc_kernel(const __grid_const
     // the whole row: the same searches, every evaluation one pass over it
     auto row_count = [&](uint32_t x) {
       int c = 0;
-      for (int i = tid; i < V; i += kTruncThreads) c += order_key<BF16>(bits_at(i)) >= x;
+      for (int i = tid; i < V; i += kSelThreads) c += order_key<BF16>(bits_at(i)) >= x;
       return block_sum_i(c);
     };
     auto row_mass = [&](uint32_t x) {
       float sm = 0.f;
-      for (int i = tid; i < V; i += kTruncThreads) {
+      for (int i = tid; i < V; i += kSelThreads) {
         const uint32_t bits = bits_at(i);
         if (order_key<BF16>(bits) >= x) sm += mass_of(bits);
       }
@@ -2469,7 +2785,7 @@ size_t resolve_smem(const ChainStochParams &p) {
 // launches make no other driver calls and can be captured into a CUDA graph.
 // The ring stream kernel's shared-memory attribute, set once per device
 // (again only when more is needed).
-template <bool BF16, int NV, int S>
+template <bool BF16, int NV, int S, bool CAND = false>
 cudaError_t prepare_ring(size_t smem) {
   static std::atomic<size_t> done_smem[kMaxDevices];
   int dev = 0;
@@ -2477,7 +2793,7 @@ cudaError_t prepare_ring(size_t smem) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (done_smem[dev].load() >= smem) return cudaSuccess;
-  e = cudaFuncSetAttribute(softmax_partials_kernel<BF16, NV, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(softmax_partials_kernel<BF16, NV, S, CAND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem);
   if (e == cudaSuccess) done_smem[dev].store(smem);
   return e;
@@ -2573,7 +2889,7 @@ cudaError_t launch_t(const ChainStochParams &p, int grid, size_t smem, int clust
   if (e != cudaSuccess) return e;
   e = launch_generation(p, s);
   if (e == cudaSuccess)
-    e = launch_dependent(softmax_partials_kernel<BF16, kSoftVecs, S>, dim3(static_cast<unsigned>(grid)),
+    e = launch_dependent(softmax_partials_kernel<BF16, kSoftVecs, S, false>, dim3(static_cast<unsigned>(grid)),
                          kSoftThreads + 32, smem, s, p);
   if (e == cudaSuccess) e = launch_resolve<BF16>(p, cluster, s);
   return e;
@@ -2583,20 +2899,25 @@ template <bool BF16, int S>
 cudaError_t ring_blocks_t(size_t smem, int *blocks) {
   cudaError_t e = prepare_ring<BF16, kSoftVecs, S>(smem);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, softmax_partials_kernel<BF16, kSoftVecs, S>,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, softmax_partials_kernel<BF16, kSoftVecs, S, false>,
                                                        kSoftThreads + 32, smem);
 }
 
-// The truncated verify: the generation step, the truncation kernel (one CTA
-// per logit row, which also writes the row's record), then the resolve kernel.
+// The truncated verify: the generation step, the ring stream with its chunk
+// maxima (always kSoftStages deep), the selection kernel, then the resolve
+// kernel, each a programmatic dependent of the one before.
 template <bool BF16>
-cudaError_t launch_truncated_t(const ChainStochParams &p, int grid, int cluster, cudaStream_t s) {
+cudaError_t launch_truncated_t(const ChainStochParams &p, int grid, size_t smem, int cluster,
+                               cudaStream_t s) {
   cudaError_t e = prepare<BF16>(cluster);
+  if (e == cudaSuccess) e = prepare_ring<BF16, kSoftVecs, kSoftStages, true>(smem);
   if (e != cudaSuccess) return e;
+  const dim3 rows(static_cast<unsigned>(p.B * (2 * p.K + 1)));
   e = launch_generation(p, s);
-  if (e != cudaSuccess) return e;
-  trunc_kernel<BF16><<<grid, kTruncThreads, 0, s>>>(p);
-  e = cudaGetLastError();
+  if (e == cudaSuccess)
+    e = launch_dependent(softmax_partials_kernel<BF16, kSoftVecs, kSoftStages, true>,
+                         dim3(static_cast<unsigned>(grid)), kSoftThreads + 32, smem, s, p);
+  if (e == cudaSuccess) e = launch_dependent(trunc_select_kernel<BF16>, rows, kSelThreads, 0, s, p);
   if (e == cudaSuccess) e = launch_resolve<BF16>(p, cluster, s);
   return e;
 }
@@ -2649,9 +2970,10 @@ cudaError_t ring_blocks_per_sm(bool bf16, int stages, size_t smem, int *blocks) 
   return bf16 ? ring_blocks_t<true, 2>(smem, blocks) : ring_blocks_t<false, 2>(smem, blocks);
 }
 
-cudaError_t launch_chain_truncated(const ChainStochParams &p, bool bf16, int grid, int cluster,
-                                   cudaStream_t s) {
-  return bf16 ? launch_truncated_t<true>(p, grid, cluster, s) : launch_truncated_t<false>(p, grid, cluster, s);
+cudaError_t launch_chain_truncated(const ChainStochParams &p, bool bf16, int grid, size_t smem,
+                                   int cluster, cudaStream_t s) {
+  return bf16 ? launch_truncated_t<true>(p, grid, smem, cluster, s)
+              : launch_truncated_t<false>(p, grid, smem, cluster, s);
 }
 
 cudaError_t launch_drift(const ChainStochParams &p, bool bf16, int grid, cudaStream_t s) {

@@ -78,6 +78,12 @@ struct ChainStochParams {
   // b's), m being the row's max logit; flags nonzero: no threshold was found.
   SoftPart *trunc;        // NULL: no truncation
   SoftPart *trunc_area;   // where the workspace keeps the records
+  // The truncated verify's chunk maxima: the ring stream's consumer thread i
+  // of tile t of a truncated logit row stores the largest of its elements
+  // there (its chunk: vectors i, i + 256, i + 512, i + 768 of the tile) as
+  // the top 16 bits of the order key of its fp32 value.  Written in every
+  // call before the selection kernel reads them, so they carry no stamp.
+  unsigned short *cmax;       // [rows * nslices * kSoftThreads]
   // DRIFT residual extraction (spec_drift_residuals): support size and outputs
   int drift_m;
   int32_t *drift_support;   // [B, K, m]
@@ -170,9 +176,10 @@ constexpr int kDriftMaxSupport = 64;  // largest support size m
 cudaError_t launch_chain_stochastic(const ChainStochParams &p, bool bf16, int grid, size_t smem,
                                     int cluster, cudaStream_t s);
 cudaError_t ring_blocks_per_sm(bool bf16, int stages, size_t smem, int *blocks);
-// Generation step, stream kernel, truncation thresholds, then the resolve kernel.
-cudaError_t launch_chain_truncated(const ChainStochParams &p, bool bf16, int grid, int cluster,
-                                   cudaStream_t s);
+// Generation step, ring stream kernel (with the chunk maxima), selection of
+// the truncation thresholds, then the resolve kernel.
+cudaError_t launch_chain_truncated(const ChainStochParams &p, bool bf16, int grid, size_t smem,
+                                   int cluster, cudaStream_t s);
 // Generation step, stream kernel, then the DRIFT selection kernel (one CTA per
 // drafted position).
 cudaError_t launch_drift(const ChainStochParams &p, bool bf16, int grid, cudaStream_t s);

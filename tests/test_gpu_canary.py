@@ -167,7 +167,8 @@ def _chain_case(L, A, inp, mode, static=False, trunc=None):
     if static:
         rc = L.spec_verify_chain_static(ctypes.byref(a), ctypes.byref(o), _stream())
     else:
-        nb = L.spec_verify_chain_workspace_size(B, K, V)
+        nb = (L.spec_verify_chain_workspace_size if trunc is None
+              else L.spec_verify_chain_truncated_workspace_size)(B, K, V)
         ws = A.put("workspace", (nb,), np.uint8)
         if trunc is not None:
             tk = A.put("top_k", (B,), np.int32, trunc[0])

@@ -230,10 +230,15 @@ def test_bounded_wait_gives_up_and_recovers(sv):
         g = run_chain(sv, inp)
         assert np.all(g["row_status"] == 6)
         assert np.all(g["accepted_len"] == -1)
+        # the truncated chain: the stream gives up the same way and the
+        # selection kernel withholds its records
+        B = inp["target"].shape[0]
+        gt = run_trunc(sv, inp, np.full(B, 20, np.int32), np.full(B, 0.9, np.float32))
+        assert np.all(gt["row_status"] == 6)
         # the greedy kernels stream with plain loads: no wait, nothing to give up
         t = S.make("c4", B=2, V=4096)
-        gt = sv.spec_verify_tree(cuda(t["target"]), cuda(t["parent"]), cuda(t["node_tokens"]))
-        assert np.all(host(gt)["row_status"] == 0)
+        gtr = sv.spec_verify_tree(cuda(t["target"]), cuda(t["parent"]), cuda(t["node_tokens"]))
+        assert np.all(host(gtr)["row_status"] == 0)
     finally:
         sv.debug_force_wait_timeout(False)
         sv.set_wait_timeout_ns(old)

@@ -70,6 +70,28 @@ def test_workspace_sizes(L):
     assert L.spec_verify_tree_workspace_size(32, 1025, 100) == 0
 
 
+def test_truncated_workspace_holds_the_lists(L):
+    """A truncated call lays out, each area 256-byte aligned: one record per
+    (logit row, ring tile), the draft-token logits, the truncation records
+    and a 2-byte chunk maximum per (logit row, tile, consumer thread of 256),
+    with the 16-byte header in the last 256 bytes.  The size covers that for
+    bf16 (8192-logit) and fp32 (4096-logit) tiles, and a truncated workspace
+    also serves a plain call."""
+    def al(x):
+        return -(-x // 256) * 256
+    for B, K, V in [(64, 5, 128256), (1, 0, 1), (3, 63, 4099), (256, 8, 262144), (5, 2, 8193)]:
+        rows = B * (2 * K + 1)
+        need = L.spec_verify_chain_truncated_workspace_size(B, K, V)
+        assert need >= L.spec_verify_chain_workspace_size(B, K, V)
+        for tile in (8192, 4096):
+            nt = -(-V // tile)
+            used = al(rows * nt * 16) + al(rows * 8) + al(rows * 16) + rows * nt * 256 * 2 + 256
+            assert need >= used, (B, K, V, tile)
+    assert L.spec_verify_chain_truncated_workspace_size(-1, 5, 100) == 0
+    assert L.spec_verify_chain_truncated_workspace_size(4, -1, 100) == 0
+    assert L.spec_verify_chain_truncated_workspace_size(4, 5, 262145) == 0
+
+
 def _fake(addr):
     return ctypes.c_void_p(addr)
 
