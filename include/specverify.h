@@ -156,7 +156,8 @@ size_t spec_verify_chain_workspace_size(int32_t B, int32_t K, int32_t V);
 /* Bytes of workspace spec_verify_chain_truncated needs for these sizes (any
  * dtype): the records of spec_verify_chain plus a 2-byte maximum per chunk
  * of logits that the selection of the thresholds reads, about V / 8 bytes
- * per logit row (c3: 11.5 MB).  Never less than
+ * per logit row, and 512 bytes per target row for small kept sets (c3:
+ * 11.7 MB).  Never less than
  * spec_verify_chain_workspace_size, so one such workspace serves both calls.
  * 0 on invalid sizes. */
 size_t spec_verify_chain_truncated_workspace_size(int32_t B, int32_t K, int32_t V);
@@ -311,7 +312,9 @@ spec_status spec_rollback_lengths(int32_t B, int32_t max_emit, const int32_t *kv
  * logit of every chunk of 32 (bf16) or 16 (fp32) it reads; per truncated
  * logit row the top-k and top-p thresholds, from the logits of the chunks
  * whose maxima can reach them (a row they cannot settle passes over its own
- * logits); then the per-row resolve.
+ * logits); then the per-row resolve, which draws from p's kept set when the
+ * selection handed it over (at most 64 tokens) and passes over the
+ * stopping position's logits otherwise.
  */
 typedef struct {
   const int32_t *top_k;  /* [B] device, or NULL */

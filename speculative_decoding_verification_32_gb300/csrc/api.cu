@@ -305,11 +305,12 @@ size_t spec_verify_chain_workspace_size(int32_t B, int32_t K, int32_t V) {
 size_t spec_verify_chain_truncated_workspace_size(int32_t B, int32_t K, int32_t V) {
   if (!valid_sizes(B, V) || K < 0 || K > SPEC_MAX_K) return 0;
   // the records (every area 256-byte aligned, as setup_stochastic lays them
-  // out), then the chunk maxima
+  // out), then the chunk maxima and the kept lists
   const size_t rows = static_cast<size_t>(B) * (K + 1) + static_cast<size_t>(B) * K;
   const size_t records = align_up(rows * ceil_div(V, kRecordSlice) * sizeof(SoftPart), 256) +
                          align_up(rows * 8, 256) + align_up(rows * sizeof(SoftPart), 256);
-  return std::max(records + chunk_max_bytes(rows, V) + ws_tail_bytes(B),
+  const size_t lists = align_up(static_cast<size_t>(B) * (K + 1) * kKeptMax * 8, 256);
+  return std::max(records + chunk_max_bytes(rows, V) + lists + ws_tail_bytes(B),
                   spec_verify_chain_workspace_size(B, K, V));
 }
 
@@ -427,10 +428,12 @@ spec_status spec_verify_chain_truncated(const spec_chain_args *a, const spec_tru
     const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, C, StreamKind::kRingListed, &smem);
     if (st != SPEC_OK) return st;
   }
-  {  // the chunk maxima, after the truncation records
+  {  // the chunk maxima, after the truncation records, then the kept lists
     const size_t rows = static_cast<size_t>(a->B) * (2 * K + 1);
-    p.cmax = reinterpret_cast<unsigned short *>(reinterpret_cast<char *>(p.trunc_area) +
-                                                align_up(rows * sizeof(SoftPart), 256));
+    char *at = reinterpret_cast<char *>(p.trunc_area) + align_up(rows * sizeof(SoftPart), 256);
+    p.cmax = reinterpret_cast<unsigned short *>(at);
+    at += align_up(rows * p.nslices * kSoftThreads * 2, 256);
+    p.klist = reinterpret_cast<unsigned long long *>(at);
   }
   p.accepted_len = o->accepted_len;
   p.out_tokens = o->out_tokens;

@@ -859,7 +859,8 @@ struct alignas(16) ResolveCtrl {
   uint32_t flags;            // row status bits
   int trunc;                 // the row is truncated (top-k / top-p)
   uint32_t thp, thq;         // key thresholds of the stopping position's p and q
-  int pad2[2];
+  int klen;                  // entries of the kept list of p at the stopping position (0: none)
+  int pad2;
 };
 
 // Non-zero ranks copy Mp .. thq (three 16-byte blocks) from rank 0.
@@ -983,6 +984,7 @@ __device__ void decide_row(const ChainStochParams &P, int b, float s2, uint32_t 
     float4 tp = make_float4(-kInf, 0.f, 0.f, 0.f), dq = make_float4(-kInf, 0.f, 0.f, 0.f);
     float us = 0.f;
     uint32_t thp = 0, thq = 0;  // truncation thresholds (0: keep all)
+    int klen = 0;               // p's kept list (truncated rows)
     if (j < npos) {
       const RowScalars sc = j0 == 0 ? first : load_scalars(P, b, j);
       us = sc.us;
@@ -994,8 +996,9 @@ __device__ void decide_row(const ChainStochParams &P, int b, float s2, uint32_t 
         float th, kp;
         uint32_t tf;
         load_part(P.trunc + (size_t)b * npos + j, 0u, &th, &kp, &tf);
-        flags |= tf ? F_TIMEOUT : 0u;
+        flags |= (tf & 1u) ? F_TIMEOUT : 0u;  // bits 1..7: the kept list's length
         thp = __float_as_uint(th);
+        klen = static_cast<int>(tf >> 1);
         tp.y = kp;
       }
       if (tp.x != tp.x || tp.x == kInf) flags |= F_NONFINITE;
@@ -1011,7 +1014,7 @@ __device__ void decide_row(const ChainStochParams &P, int b, float s2, uint32_t 
           float th, kp;
           uint32_t tf;
           load_part(P.trunc + (size_t)P.B * npos + (size_t)b * K + j, 0u, &th, &kp, &tf);
-          flags |= tf ? F_TIMEOUT : 0u;
+          flags |= (tf & 1u) ? F_TIMEOUT : 0u;
           thq = __float_as_uint(th);
           dq.y = kp;
         }
@@ -1043,6 +1046,7 @@ __device__ void decide_row(const ChainStochParams &P, int b, float s2, uint32_t 
       ctl.u = us;
       ctl.thp = thp;
       ctl.thq = found_here ? thq : 0u;
+      ctl.klen = klen;
     }
     if (found_here) stop = j0 + src;
   }
@@ -1171,10 +1175,18 @@ __global__ void __launch_bounds__(kResolveThreads, kResolveBlocksPerSm) chain_re
     const float qe = kq ? ex2(__fmaf_rn(F::elem(wq, e), s2, nMq)) : 0.f;
     return fmaxf(__fmaf_rn(pe, iSp, -__fmul_rn(qe, iSq)), 0.f);
   };
+  // A truncated row whose kept set of p at the stopping position came as a
+  // list with its record draws from that list: p, and so the residual, is 0
+  // outside it, and nothing else of the row is read.  The CTAs agree on it
+  // at the exchange, as on the row's status.
+  const bool by_list = trunc && ctl.klen > 0;
+  bool list_draw = false;
   while (true) {
     // ---- pass: per-round masses (kept for the search), then the CTA total
     float tsum = 0.f;
-    if (trunc) {
+    if (by_list) {
+      // no pass: the list is drawn from after the exchange
+    } else if (trunc) {
       // truncated laws: four rounds of target loads in flight, then element
       // by element with the thresholds -- only where some element of the
       // target vector may reach p's threshold (the draft vector is loaded
@@ -1288,7 +1300,7 @@ __global__ void __launch_bounds__(kResolveThreads, kResolveBlocksPerSm) chain_re
     if (tid == 0) {
       float c = 0.f;
       for (int w2 = 0; w2 < NW; ++w2) c += ctl.wsum[w2];
-      ctl.mailbox[xs] = make_float4(c, __uint_as_float(my_flags), 0.f, 0.f);
+      ctl.mailbox[xs] = make_float4(c, __uint_as_float(my_flags), by_list ? 1.f : 0.f, 0.f);
     }
     cluster_sync();
     const float4 mb = lane < C ? ld_dsmem_f4(dsmem_addr(&ctl.mailbox[xs], (uint32_t)lane))
@@ -1297,6 +1309,12 @@ __global__ void __launch_bounds__(kResolveThreads, kResolveBlocksPerSm) chain_re
     xs ^= 1;
     row_flags = __reduce_or_sync(FULL_MASK, __float_as_uint(mb.y));
     if (row_flags) break;  // the row's status: no token
+    const int n_list = static_cast<int>(__reduce_add_sync(FULL_MASK, lane < C && mb.z != 0.f ? 1u : 0u));
+    if (n_list != 0) {  // (the same records give every CTA the same choice)
+      if (n_list == C) list_draw = true;
+      else row_flags = F_TIMEOUT;
+      break;
+    }
     const float tot = sum_lanes(cm, C);
     if (task == 1 && !(tot > 0.f)) {  // the residual vanished in fp32: draw from p
       task = 2;
@@ -1308,6 +1326,19 @@ __global__ void __launch_bounds__(kResolveThreads, kResolveBlocksPerSm) chain_re
   }
   cluster_arrive();  // done with the peers' mailboxes
 
+  // the row's outputs, by one warp
+  auto write_row = [&](int token) {
+    for (int j = lane; j < npos && SV_INB(b, P.B); j += 32) {
+      const int o = j < stop ? __ldg(P.tokens + (size_t)b * K + j) : (j == stop ? token : -1);
+      P.out_tokens[(size_t)b * npos + j] = o;
+    }
+    if (lane == 0 && SV_INB(b, P.B)) {
+      P.accepted_len[b] = stop;
+      P.num_emitted[b] = stop + 1;
+      P.row_status[b] = 0;
+      if (stop < K && P.resid_mass) P.resid_mass[(size_t)b * K + stop] = Z;
+    }
+  };
   if (row_flags) {  // the agreed status: rank 0 writes the row's outputs
     if (crank == 0 && warp == 0 && SV_INB(b, P.B)) {
       for (int j = lane; j < npos; j += 32) P.out_tokens[(size_t)b * npos + j] = -1;
@@ -1316,6 +1347,82 @@ __global__ void __launch_bounds__(kResolveThreads, kResolveBlocksPerSm) chain_re
         P.num_emitted[b] = 0;
         P.row_status[b] = lowest_code(row_flags);
       }
+    }
+  } else if (list_draw) {
+    // Rank 0's warp 0 draws from the kept list of p at the stopping position
+    // (at most 64 entries, key desc): the masses under the task, in vocabulary
+    // order, then the first entry whose cumulative mass exceeds u times the
+    // total, or the last one with mass.
+    if (crank == 0 && warp == 0) {
+      __threadfence();  // the list was written before the record polled above
+      const int n = min(ctl.klen, kKeptMax);
+      const int prow = b * npos + stop;
+      const unsigned long long *kl = P.klist + (size_t)prow * kKeptMax;
+      int tok[2];
+      float pe[2], ms[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int i = lane + 32 * h;
+        const bool in = i < n && SV_INB((long long)prow * kKeptMax + i, (long long)P.B * npos * kKeptMax);
+        const unsigned long long ent = in ? ld_relaxed_u64(kl + i) : 0ull;
+        tok[h] = in ? static_cast<int>(~static_cast<uint32_t>(ent)) : 0x7fffffff;
+        const float lp = key_value<BF16>(static_cast<uint32_t>(ent >> 32));
+        pe[h] = in ? ex2(__fmaf_rn(lp, s2, nMp)) : 0.f;
+        ms[h] = pe[h];
+        if (in && task == 1 && SV_INB(tok[h], V)) {
+          const size_t at = ((size_t)b * K + stop) * V + tok[h];
+          uint32_t bits;
+          if constexpr (BF16) bits = __ldg(static_cast<const unsigned short *>(P.draft) + at);
+          else bits = __ldg(static_cast<const unsigned int *>(P.draft) + at);
+          const float ld = BF16 ? __uint_as_float(bits << 16) : __uint_as_float(bits);
+          const float qe = order_key<BF16>(bits) >= thq ? ex2(__fmaf_rn(ld, s2, nMq)) : 0.f;
+          ms[h] = fmaxf(__fmaf_rn(pe[h], iSp, -__fmul_rn(qe, iSq)), 0.f);
+        }
+      }
+      // vocabulary order: each entry's rank among the token ids
+      int rk[2] = {0, 0};
+      for (int j2 = 0; j2 < n; ++j2) {
+        const int tj = __shfl_sync(FULL_MASK, j2 < 32 ? tok[0] : tok[1], j2 & 31);
+        rk[0] += tj < tok[0] ? 1 : 0;
+        rk[1] += tj < tok[1] ? 1 : 0;
+      }
+      float *s_ms = rsum, *s_pe = rsum + kKeptMax;
+      int *s_tok = reinterpret_cast<int *>(rsum + 2 * kKeptMax);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (lane + 32 * h < n) {
+          s_ms[rk[h]] = ms[h];
+          s_pe[rk[h]] = pe[h];
+          s_tok[rk[h]] = tok[h];
+        }
+      }
+      __syncwarp();
+      auto scan = [&](const float *src, float &m0, float &m1, float &c0, float &c1) {
+        m0 = lane < n ? src[lane] : 0.f;
+        m1 = lane + 32 < n ? src[lane + 32] : 0.f;
+        c0 = warp_inclusive_scan(m0, lane);
+        c1 = warp_inclusive_scan(m1, lane) + __shfl_sync(FULL_MASK, c0, 31);
+      };
+      float m0, m1, c0, c1;
+      scan(s_ms, m0, m1, c0, c1);
+      float tot = __shfl_sync(FULL_MASK, c1, 31);
+      if (task == 1 && tot > 0.f) Z = tot;
+      if (task == 1 && !(tot > 0.f)) {  // the residual vanished in fp32: draw from p
+        task = 2;
+        scan(s_pe, m0, m1, c0, c1);
+        tot = __shfl_sync(FULL_MASK, c1, 31);
+      }
+      const float t = __fmul_rn(ctl.u, tot);
+      const unsigned h0 = __ballot_sync(FULL_MASK, m0 > 0.f && c0 > t);
+      const unsigned h1 = __ballot_sync(FULL_MASK, m1 > 0.f && c1 > t);
+      int pos;
+      if (h0) pos = __ffs(h0) - 1;
+      else if (h1) pos = 31 + __ffs(h1);
+      else {  // past the total: the last entry with mass
+        const unsigned p0 = __ballot_sync(FULL_MASK, m0 > 0.f), p1 = __ballot_sync(FULL_MASK, m1 > 0.f);
+        pos = p1 ? 63 - __clz(p1) : (p0 ? 31 - __clz(p0) : 0);
+      }
+      write_row(s_tok[pos]);
     }
   } else if (crank == owner_cta) {
     float t_w;
@@ -1379,17 +1486,7 @@ __global__ void __launch_bounds__(kResolveThreads, kResolveBlocksPerSm) chain_re
         }
         token = __shfl_sync(FULL_MASK, pos, ls);
       }
-      // ---- the row's outputs
-      for (int j = lane; j < npos && SV_INB(b, P.B); j += 32) {
-        const int o = j < stop ? __ldg(P.tokens + (size_t)b * K + j) : (j == stop ? token : -1);
-        P.out_tokens[(size_t)b * npos + j] = o;
-      }
-      if (lane == 0 && SV_INB(b, P.B)) {
-        P.accepted_len[b] = stop;
-        P.num_emitted[b] = stop + 1;
-        P.row_status[b] = 0;
-        if (stop < K && P.resid_mass) P.resid_mass[(size_t)b * K + stop] = Z;
-      }
+      write_row(token);
     }
   }
   cluster_wait();  // no CTA leaves while a peer may still read its mailbox
@@ -2123,6 +2220,7 @@ struct alignas(16) TruncCtrl {
   int settled;               // warp 0's settling of a small list: 1 done, 0 retry
   uint32_t theta_w;
   float kept_w;
+  int kept_n;                // entries of the kept set (a prefix of the sorted list)
   float fred[kSelWarps];
   int ired[kSelWarps];
   int chist[256];
@@ -2584,7 +2682,7 @@ __global__ void __launch_bounds__(kSelThreads, 6) trunc_select_kernel(const __gr
       gk = group_end(tk - 1);
       Sk = prefix_at_w(gk);
     }
-    int ok = 1;
+    int ok = 1, kn = 0;
     uint32_t th = 0;
     float kp = 0.f;
     if (tp < 1.f) {
@@ -2595,21 +2693,26 @@ __global__ void __launch_bounds__(kSelThreads, 6) trunc_select_kernel(const __gr
         const unsigned c0 = __ballot_sync(FULL_MASK, lane <= gk && s0 >= target);
         const unsigned c1 = __ballot_sync(FULL_MASK, lane + 32 <= gk && s1 >= target);
         const int pos = c0 ? __ffs(c0) - 1 : (c1 ? 31 + __ffs(c1) : gk);
+        const int ge = group_end(pos);
         th = key_at_w(pos);
-        kp = prefix_at_w(group_end(pos));
+        kp = prefix_at_w(ge);
+        kn = ge + 1;
       }
     } else {
       th = key_at_w(gk);
       kp = Sk;
+      kn = gk + 1;
     }
     if (lane == 0) {
       ctl.settled = ok;
       ctl.theta_w = th;
       ctl.kept_w = kp;
+      ctl.kept_n = kn;
     }
   };
   uint32_t theta = 0;
   float kept = 0.f;
+  int klen = 0;  // entries of the kept list written for the resolve kernel
   bool done = false;
   int r = trunc_sample_rank(tk);
   int nc = gather_chunks();
@@ -2661,6 +2764,17 @@ __global__ void __launch_bounds__(kSelThreads, 6) trunc_select_kernel(const __gr
       }
       theta = ctl.theta_w;
       kept = ctl.kept_w;
+      // a target row's kept set, in the order above, for the resolve kernel
+      // (its record, stored after this, gives the length)
+      if (is_target) {
+        const int kn = ctl.kept_n;
+        if (tid < kn && SV_INB((long long)row * kKeptMax + tid, (long long)P.B * npos * kKeptMax)) {
+          P.klist[(size_t)row * kKeptMax + tid] = ctl.ck[kDriftCand / 2 + tid];
+          __threadfence();
+        }
+        klen = kn;
+      }
+      __syncthreads();
       done = true;
       break;
     }
@@ -2774,7 +2888,8 @@ __global__ void __launch_bounds__(kSelThreads, 6) trunc_select_kernel(const __gr
       kept = Sk;
     }
   }
-  if (tid == 0) store_part(rec, __uint_as_float(theta), kept, 0u, tag);
+  // flags bits 1..7: the kept list's length (at most 64)
+  if (tid == 0) store_part(rec, __uint_as_float(theta), kept, static_cast<uint32_t>(klen) << 1, tag);
 }
 
 size_t resolve_smem(const ChainStochParams &p) {

@@ -84,6 +84,10 @@ struct ChainStochParams {
   // the top 16 bits of the order key of its fp32 value.  Written in every
   // call before the selection kernel reads them, so they carry no stamp.
   unsigned short *cmax;       // [rows * nslices * kSoftThreads]
+  // A target logit row's kept set of p (at most kKeptMax (key << 32 |
+  // ~token) entries, key desc), written by the selection kernel when the set
+  // is that small; the row's truncation record gives its length.
+  unsigned long long *klist;  // [B * (K+1) * kKeptMax]
   // DRIFT residual extraction (spec_drift_residuals): support size and outputs
   int drift_m;
   int32_t *drift_support;   // [B, K, m]
@@ -157,6 +161,8 @@ constexpr int kStatsMaxSlices = (SPEC_MAX_V + kStatsSlice - 1) / kStatsSlice;
 // The record area holds one record per (logit row, smallest slice of any
 // stochastic path).
 constexpr int kRecordSlice = kSoftMinSlice < kStatsSlice ? kSoftMinSlice : kStatsSlice;
+// Entries of a kept list (the truncated verify's small kept sets).
+constexpr int kKeptMax = 64;
 // Largest rounds of 32 vectors per warp in the resolve kernel.
 constexpr int kResolveMaxRounds = 16;
 // Resolve CTAs one SM holds (the kernel's launch bound): the cluster split

@@ -73,8 +73,9 @@ def test_workspace_sizes(L):
 def test_truncated_workspace_holds_the_lists(L):
     """A truncated call lays out, each area 256-byte aligned: one record per
     (logit row, ring tile), the draft-token logits, the truncation records
-    and a 2-byte chunk maximum per (logit row, tile, consumer thread of 256),
-    with the 16-byte header in the last 256 bytes.  The size covers that for
+    a 2-byte chunk maximum per (logit row, tile, consumer thread of 256) and
+    a kept list of 64 8-byte entries per target row, with the 16-byte header
+    in the last 256 bytes.  The size covers that for
     bf16 (8192-logit) and fp32 (4096-logit) tiles, and a truncated workspace
     also serves a plain call."""
     def al(x):
@@ -85,7 +86,8 @@ def test_truncated_workspace_holds_the_lists(L):
         assert need >= L.spec_verify_chain_workspace_size(B, K, V)
         for tile in (8192, 4096):
             nt = -(-V // tile)
-            used = al(rows * nt * 16) + al(rows * 8) + al(rows * 16) + rows * nt * 256 * 2 + 256
+            used = (al(rows * nt * 16) + al(rows * 8) + al(rows * 16) + al(rows * nt * 256 * 2) +
+                    B * (K + 1) * 64 * 8 + 256)
             assert need >= used, (B, K, V, tile)
     assert L.spec_verify_chain_truncated_workspace_size(-1, 5, 100) == 0
     assert L.spec_verify_chain_truncated_workspace_size(4, -1, 100) == 0
