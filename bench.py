@@ -852,8 +852,8 @@ def run_next(args):
                            "l2": f"{n_sets} rotating input sets > L2"},
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                              "frac": gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
-                             "kernel": "drift_select_kernel + draft_stats_kernel (one pass over "
-                                       "each row between them) + drift_finish_kernel",
+                             "kernel": "softmax_partials_kernel (positions 0..K-1, chunk maxima) + "
+                                       "drift_pick_kernel + drift_finish_kernel",
                              "algorithmic_bytes_per_launch": alg, "traffic": measured_traffic("drift_kernels")[0]},
                 "gpu_launches": 4 * n, "clocks": clocks}
     elif args.workload == "rollback":

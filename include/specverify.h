@@ -158,8 +158,8 @@ size_t spec_verify_chain_workspace_size(int32_t B, int32_t K, int32_t V);
  * of logits that the selection of the thresholds reads, about V / 8 bytes
  * per logit row, and 512 bytes per target row for small kept sets (c3:
  * 11.7 MB).  Never less than
- * spec_verify_chain_workspace_size, so one such workspace serves both calls.
- * 0 on invalid sizes. */
+ * spec_verify_chain_workspace_size, so one such workspace serves both calls;
+ * spec_drift_residuals needs this size too.  0 on invalid sizes. */
 size_t spec_verify_chain_truncated_workspace_size(int32_t B, int32_t K, int32_t V);
 
 /*
@@ -341,12 +341,14 @@ spec_status spec_verify_chain_truncated(const spec_chain_args *args, const spec_
  * support [B, K, m] int32, residual [B, K, m] float32, row_status [B]
  * (device, caller-owned): a row with a non-finite logit, no finite logit or
  * a bad temperature at any drafted position gets its code and support -1,
- * residual NaN.  The workspace is spec_verify_chain's (same size function).
- * After the one-thread generation step, three kernels: one CTA per drafted
- * position, which reads its target row once for its statistics and selects
- * the support by radix selection on the target logits; a stream over the
- * draft rows for their softmax statistics, on the SMs the first kernel's
- * last wave leaves idle; then one CTA per row for the residuals and the
+ * residual NaN.  The workspace must hold
+ * spec_verify_chain_truncated_workspace_size(B, K, V) bytes.
+ * After the one-thread generation step, three kernels: the stream of
+ * spec_verify_chain over positions 0 .. K-1 of both laws, which also keeps
+ * the largest logit of every chunk of 32 (bf16) or 16 (fp32) target logits;
+ * one CTA per drafted position, which takes the support from the logits of
+ * the chunks whose maxima can reach the m-th largest (a row they cannot
+ * settle is searched whole); then one CTA per row for the residuals and the
  * row's status.  Residuals carry fp32 rounding: agreement with an exact
  * computation is within about 1e-4 nats for logits of magnitude up to ~50/T.
  */

@@ -311,7 +311,7 @@ def spec_drift_residuals(target_logits, draft_logits, temperature=None, m=32, st
                          _ptr(target_logits), _ptr(draft_logits), None, _ptr(temperature),
                          None, None)
     L = lib()
-    nbytes = L.spec_verify_chain_workspace_size(B, K, V)
+    nbytes = L.spec_verify_chain_truncated_workspace_size(B, K, V)
     s, sp = _stream(dev, stream)
     ws = workspace(dev, nbytes, s.cuda_stream)
     _check(L.spec_drift_residuals(_c.byref(args), int(m), _ptr(sup), _ptr(res), _ptr(st),

@@ -171,18 +171,16 @@ spec_status run_greedy(GreedyParams &p, bool bf16, int esz, void *ws, cudaStream
   return SPEC_OK;
 }
 
-// How the first kernel of a stochastic call reads the logits: the bulk-copy
-// ring (plain verify; the truncated verify's, which also keeps chunk maxima,
-// is always kSoftStages deep), or warps over draft-row slices (DRIFT's
-// statistics).
-enum class StreamKind { kRing, kRingListed, kStats };
+// The stochastic calls' stream is the bulk-copy ring: the plain verify's, or
+// the one that also keeps chunk maxima (truncated verify and DRIFT), which is
+// always kSoftStages deep.
+enum class StreamKind { kRing, kRingListed };
 
 // Parameters and launch shapes of the stochastic stream kernel and of the
 // resolve kernel's cluster split, from the arguments and the workspace;
 // output pointers are left for the caller.
 spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes, ChainStochParams &p,
                              int &grid, int &C, StreamKind kind, size_t *smem) {
-  const bool ring = kind == StreamKind::kRing || kind == StreamKind::kRingListed;
   const int K = a->K;
   const int esz = a->dtype == SPEC_BF16 ? 2 : 4;
   const bool bf16 = a->dtype == SPEC_BF16;
@@ -214,8 +212,7 @@ spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes
   // SPECVERIFY_DYNAMIC=0: no claimed tail in either stream kernel (tuning)
   p.stream_dyn = 1;
   if (const char *ov = std::getenv("SPECVERIFY_DYNAMIC")) p.stream_dyn = std::atoi(ov) != 0;
-  *smem = 0;
-  if (ring) {
+  {
     // the bulk-copy ring: pair tiles of 8192 bf16 / 4096 fp32 logits per law;
     // SPECVERIFY_SOFT_STAGES (2 to 4) and SPECVERIFY_DYN_CHUNK (tiles per
     // claim) override the defaults for tuning
@@ -240,8 +237,6 @@ spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes
     }
     p.buf_bytes = 2 * p.slice * esz;  // target tile + draft tile
     *smem = static_cast<size_t>(p.stages) * p.buf_bytes + kRingCtrlBytes;
-  } else {
-    p.slice = kStatsSlice;
   }
   p.nslices = ceil_div(a->V, p.slice);
   {
@@ -252,15 +247,10 @@ spec_status setup_stochastic(const spec_chain_args *a, void *ws, size_t ws_bytes
     p.trunc_area = reinterpret_cast<SoftPart *>(reinterpret_cast<char *>(p.ylog) + align_up(rows * 8, 256));
   }
   int per_sm = 0;
-  if (ring) {
+  {
     if (ring_blocks(dev, bf16, p.stages, *smem, &per_sm) != cudaSuccess || per_sm < 1) return SPEC_ERR_CUDA;
     const long long tiles = static_cast<long long>(a->B) * (K + 1) * p.nslices;
     grid = static_cast<int>(std::min<long long>(tiles, static_cast<long long>(di.sms) * per_sm));
-  } else {  // a persistent grid of warps, four CTAs per SM
-    const long long items = static_cast<long long>(a->B) * K * p.nslices;
-    const long long warps = kStatsThreads / 32;
-    grid = static_cast<int>(std::max<long long>(
-        1, std::min<long long>((items + warps - 1) / warps, static_cast<long long>(di.sms) * 4)));
   }
   // resolve kernel: a cluster of C CTAs per row, at most 16 rounds of 32
   // vectors per warp
@@ -468,21 +458,26 @@ spec_status spec_drift_residuals(const spec_chain_args *a, int32_t m, int32_t *s
   const void *i32s[] = {a->temperature, a->draft_tokens, support, residual, row_status};
   for (const void *q : i32s)
     if (q && !aligned(q, 4)) return SPEC_ERR_ALIGN;
-  const size_t need = spec_verify_chain_workspace_size(a->B, a->K, a->V);
+  const size_t need = spec_verify_chain_truncated_workspace_size(a->B, a->K, a->V);
   if (!ws || !aligned(ws, 256) || ws_bytes < need) return SPEC_ERR_WORKSPACE;
   ChainStochParams p;
   int grid = 0, C = 0;
   size_t smem = 0;
   {
-    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, C, StreamKind::kStats, &smem);
+    const spec_status st = setup_stochastic(a, ws, ws_bytes, p, grid, C, StreamKind::kRingListed, &smem);
     if (st != SPEC_OK) return st;
+  }
+  {  // the target rows' chunk maxima, after the per-position records
+    const size_t rows = static_cast<size_t>(a->B) * (2 * a->K + 1);
+    p.cmax = reinterpret_cast<unsigned short *>(reinterpret_cast<char *>(p.trunc_area) +
+                                                align_up(rows * sizeof(SoftPart), 256));
   }
   p.row_status = row_status;
   p.drift_m = m;
   p.drift_support = support;
   p.drift_residual = residual;
   report("drift grid m", grid, m, 0, 0, 0, 0, 0);
-  return launch_drift(p, a->dtype == SPEC_BF16, grid, static_cast<cudaStream_t>(stream)) ==
+  return launch_drift(p, a->dtype == SPEC_BF16, grid, smem, static_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? SPEC_OK
              : SPEC_ERR_CUDA;

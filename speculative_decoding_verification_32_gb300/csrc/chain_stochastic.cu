@@ -39,11 +39,11 @@
 // The truncated verify lets the stream also keep, per truncated logit row,
 // the maximum of every consumer thread's chunk of each tile, and selects each
 // row's top-k / top-p thresholds from the chunks those maxima point to (one
-// CTA per logit row) ahead of the same resolve kernel.  DRIFT residuals run drift_select_kernel (one CTA per
-// drafted position: the target row's statistics and top m in one pass),
-// draft_stats_kernel (the draft rows' statistics, on the SMs the selection's
-// last, partial wave leaves idle) and drift_finish_kernel (one CTA per row:
-// log q at the support, the residuals and the row status).
+// CTA per logit row) ahead of the same resolve kernel.  DRIFT residuals run
+// the stream over positions 0 .. K-1 (chunk maxima for the target rows),
+// drift_pick_kernel (one CTA per drafted position: the top m of its target
+// row from those chunks) and drift_finish_kernel (one CTA per row: log q at
+// the support, the residuals and the row status).
 #include <cuda_bf16.h>
 
 #include <atomic>
@@ -409,7 +409,7 @@ __device__ __forceinline__ TileInfo make_tile(const ChainStochParams &P, int gt,
   const int i = gt / nt;
   it.t = gt - i * nt;
   int b, j;
-  stream_pos(i, B, K, &b, &j);
+  stream_pos(i, B, P.drift_m > 0 ? K - 1 : K, &b, &j);  // DRIFT: no bonus position
   const int s0 = it.t * P.slice;
   it.len = min(P.V - s0, P.slice);
   it.trow = b * (K + 1) + j;
@@ -439,7 +439,7 @@ __device__ __forceinline__ TileInfo make_tile(const ChainStochParams &P, int gt,
   if constexpr (CAND) {
     int tk;
     float tp;
-    it.sketch = SV_INB(b, B) && trunc_active(P, b, P.V, &tk, &tp);
+    it.sketch = P.drift_m > 0 || (SV_INB(b, B) && trunc_active(P, b, P.V, &tk, &tp));
   }
   return it;
 }
@@ -559,13 +559,16 @@ __global__ void __launch_bounds__(kSoftThreads + 32, kSoftMinBlocks) softmax_par
   SoftCtrl &ctl = *reinterpret_cast<SoftCtrl *>(smem + (size_t)S * P.buf_bytes);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nt = P.nslices, B = P.B, K = P.K;
-  const int npos = B * (K + 1);
-  const int pa = K >= 2 ? B * (K - 1) : 0;  // positions with j >= 2 come first
+  // DRIFT streams positions 0 .. K-1 only (every tile a pair): the stream
+  // order of a chain with K-1 drafts, over the real rows
+  const int Ks = P.drift_m > 0 ? K - 1 : K;
+  const int npos = B * (Ks + 1);
+  const int pa = Ks >= 2 ? B * (Ks - 1) : 0;  // positions with j >= 2 come first
   const int G = (int)gridDim.x, g = (int)blockIdx.x;
-  const int lo_a = phase_split(0, pa, B, K, nt, g, G);
-  const int hi_a = phase_split(0, pa, B, K, nt, g + 1, G);
-  const int lo_b = pa * nt + phase_split(pa, npos, B, K, nt, g, G);
-  const int hi_b = pa * nt + phase_split(pa, npos, B, K, nt, g + 1, G);
+  const int lo_a = phase_split(0, pa, B, Ks, nt, g, G);
+  const int hi_a = phase_split(0, pa, B, Ks, nt, g + 1, G);
+  const int lo_b = pa * nt + phase_split(pa, npos, B, Ks, nt, g, G);
+  const int hi_b = pa * nt + phase_split(pa, npos, B, Ks, nt, g + 1, G);
   // Only phase A is split statically; the tiles of phase B are claimed in
   // chunks (through the counter the generation step clears) as CTAs run out
   // of work, so CTAs that stream faster take more of the tail.
@@ -805,7 +808,7 @@ __global__ void __launch_bounds__(kSoftThreads + 32, kSoftMinBlocks) softmax_par
     if (pair) {
       const float cm = tile_accumulate<BF16, NV>(wp, s2, tid, nvec, mq, sq);
       if constexpr (CAND) {
-        if (it.sketch) store_chunk_max(cm, it.drow, it.t);
+        if (it.sketch && P.drift_m == 0) store_chunk_max(cm, it.drow, it.t);  // (DRIFT: targets only)
       }
     }
 
@@ -1554,19 +1557,20 @@ __device__ uint32_t block_kth_largest(Each each, int r, int *chist, int *s_digit
   return prefix;
 }
 
-// ============================================================ DRIFT selection
+// ============================================================ DRIFT
 //
 // "Speculative Decoding Under Distribution Shift: DRIFT Recalibration" (the
 // residual paragraph of its method): at every drafted position, restrict
 // target and draft to the m tokens of highest target probability and report
-// log p - log q there.  One CTA per (position j < K, row b).  The m-th
-// largest target logit is found by radix selection on order-preserving
-// integer keys, 8 bits a pass from the top; equal keys at the boundary are
-// taken in vocabulary order, so the support matches the oracle's exactly.
+// log p - log q there.  The ring stream reads positions 0 .. K-1 of target
+// and draft (records for both, chunk maxima for the target rows); then
+// drift_pick_kernel (one CTA per position j < K of row b, with the
+// truncation kernels below) takes the m largest target keys from the chunks
+// those maxima point to, equal keys at the boundary in vocabulary order, so
+// the support matches the oracle's exactly; drift_finish_kernel forms the
+// residuals.
 
-constexpr int kDriftThreads = 512;
 constexpr int kDriftFinishThreads = 256;
-constexpr int kDriftWarps = kDriftThreads / 32;
 constexpr int kDriftMaxM = kDriftMaxSupport;
 
 constexpr int kDriftCand = 2048;  // candidate list of the sampled-threshold path
@@ -1578,89 +1582,6 @@ __device__ __forceinline__ int sampled_count(int V, int epv) {
   const int nvec = (V + epv - 1) / epv;
   const int last = ((nvec - 1) / kDriftSample) * kDriftSample;  // last sampled vector
   return (last / kDriftSample) * epv + min(epv, V - last * epv);
-}
-
-struct alignas(16) DriftCtrl {
-  int hist[kDriftWarps][256];  // whole-row radix fallback
-  struct {
-    uint32_t key[kDriftCand];
-    int idx[kDriftCand];
-  } cand;                      // candidates at or above the sampled threshold
-  int chist[256];              // radix digits over samples and candidates
-  int n_cand;
-  int sel_idx[kDriftMaxM];
-  uint32_t sel_key[kDriftMaxM];
-  int scan[kDriftWarps];
-  int n_gt, n_eq, digit, above;
-  float slm[kStatsMaxSlices], sls[kStatsMaxSlices];  // the target row's per-slice (max, sum)
-  float Mp, Sp;
-  uint32_t flags;
-};
-
-// DRIFT, second kernel: the draft rows' statistics.  A persistent grid of
-// warps over (draft row, 4096-logit slice) items in row order; a warp streams
-// its item with plain 16-byte loads (kStatsU per lane in flight, L2
-// evict-first), folds it into the slice's max and sum of exp2((x - m) s2) and
-// stamps one record.  No shared memory, no barrier, no atomics.  It is a
-// programmatic dependent of the selection grid and needs nothing from it, so
-// its CTAs fill the SMs that grid's last, partial wave leaves idle; block 0
-// waits for that grid on its way out, so this grid never completes before it.
-template <bool BF16, bool VEC>
-__global__ void __launch_bounds__(kStatsThreads, 4) draft_stats_kernel(const __grid_constant__ ChainStochParams P) {
-  using F = Fmt<BF16>;
-  constexpr int EPV = F::EPV, ESZ = F::ESZ, U = kStatsU;
-  // the finishing kernel may be scheduled now; it waits for this grid on the
-  // device before it reads these records
-  allow_dependents();
-  const int lane = threadIdx.x & 31;
-  const long long GW = (long long)gridDim.x * (kStatsThreads / 32);
-  const int nt = P.nslices, V = P.V, K = P.K;
-  // forced-timeout test: no record of this call appears
-  const long long total = P.force_timeout ? 0 : (long long)P.B * K * nt;
-  const uint32_t tag = *reinterpret_cast<volatile const uint32_t *>(P.gen);
-  const uint64_t pol = l2_policy_evict_first();
-  for (long long it = (long long)blockIdx.x * (kStatsThreads / 32) + (threadIdx.x >> 5); it < total; it += GW) {
-    const int drow = static_cast<int>(it / nt);  // b * K + j
-    const int sl = static_cast<int>(it - static_cast<long long>(drow) * nt);
-    const int b = drow / K;
-    const int s0 = sl * P.slice, len = min(V - s0, P.slice);
-    const char *src = static_cast<const char *>(P.draft) + ((size_t)drow * V + s0) * ESZ;
-    const int nvec = (len + EPV - 1) / EPV;
-    float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
-    const float s2 = (T > 0.f && T < kInf) ? __fdiv_rn(kLog2e, T) : 1.f;  // a bad T flags the row
-    float m = -kInf, sacc = 0.f;
-    auto load_batch = [&](uint32_t (&w)[U][4], int v0) {
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int v = v0 + u * 32 + lane;
-        if constexpr (VEC) {
-          if (v < nvec) {
-            const uint4 r = ld_stream_u4(src + (size_t)v * 16, pol);
-            w[u][0] = r.x; w[u][1] = r.y; w[u][2] = r.z; w[u][3] = r.w;
-          } else {
-            w[u][0] = w[u][1] = w[u][2] = w[u][3] = F::NEG_INF_WORD;
-          }
-        } else {
-          F::load_vec(w[u], nullptr, src, false, v, len);
-        }
-      }
-    };
-    // two batches of U vectors in flight, folded in order: the same
-    // arithmetic as one batch at a time (a batch past the slice's end is all
-    // -inf and leaves (m, sum) unchanged)
-    for (int v0 = 0; v0 < nvec; v0 += 64 * U) {
-      uint32_t wa[U][4], wb[U][4];
-      load_batch(wa, v0);
-      load_batch(wb, v0 + 32 * U);
-      online_accumulate<BF16, U>(wa, s2, m, sacc);
-      online_accumulate<BF16, U>(wb, s2, m, sacc);
-    }
-    float M, S;
-    fold_max_sum(m, sacc, s2, &M, &S);
-    if (lane == 0) store_part(P.part + (size_t)drow * nt + sl, M, S, 0u, tag);
-  }
-  // block 0 waits for the selection grid on its way out
-  if (blockIdx.x == 0 && threadIdx.x == 0) grid_dependency_wait();
 }
 
 // A row's (max, sum) from its slices' (max, sum) pairs, in one fixed order:
@@ -1684,380 +1605,13 @@ __device__ __forceinline__ bool fold_slice_stats(int nt, int lane, float s2, Sli
   return __all_sync(FULL_MASK, ready);
 }
 
-template <bool BF16>
-__global__ void __launch_bounds__(kDriftThreads, 2) drift_select_kernel(const __grid_constant__ ChainStochParams P) {
-  using F = Fmt<BF16>;
-  constexpr int EPV = F::EPV, ESZ = F::ESZ;
-  constexpr int KEYBITS = BF16 ? 16 : 32;
-  __shared__ DriftCtrl ctl;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int j = blockIdx.x, b = blockIdx.y;
-  const int K = P.K, npos = K + 1, V = P.V, m = P.drift_m;
-  // the draft rows' statistics grid may start as soon as every CTA of this
-  // grid runs: it reads and writes nothing this grid touches
-  allow_dependents();
-  // forced-timeout test: no record of this call appears, so the finishing
-  // kernel reports a timeout.  This grid is a plain launch behind the
-  // generation step, so the tag read below is this call's.
-  if (P.force_timeout) return;
-  const float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
-  const uint32_t tflags = (T > 0.f && T < kInf) ? 0u : F_BAD_TEMPERATURE;
-  const float s2 = tflags ? 1.f : __fdiv_rn(kLog2e, T);
-  const uint32_t tag = *reinterpret_cast<volatile const uint32_t *>(P.gen);
-  int32_t *sup = P.drift_support + ((size_t)b * K + j) * m;
-  float *res = P.drift_residual + ((size_t)b * K + j) * m;
-  const char *tg = static_cast<const char *>(P.target) + ((size_t)(b * npos + j) * V) * ESZ;
-  const bool aligned = P.use_tma != 0;
-  const int nvec = (V + EPV - 1) / EPV;
-
-  auto bits_at = [&](int i) -> uint32_t {
-    if constexpr (BF16) return __ldg(reinterpret_cast<const unsigned short *>(tg) + i);
-    else return __ldg(reinterpret_cast<const unsigned int *>(tg) + i);
-  };
-  auto kth_largest = [&](auto each, int r, int &n_above, int &n_equal) {
-    return block_kth_largest<KEYBITS, kDriftThreads>(each, r, ctl.chist, &ctl.digit, &ctl.above,
-                                                    n_above, n_equal);
-  };
-
-  // ---- threshold: the r-th largest key of a strided sample (the elements
-  // of every kDriftSample-th 16-byte vector, one logit in kDriftSample);
-  // about r * kDriftSample keys of the row lie at or above it
-  constexpr int kNSV = (SPEC_MAX_V + EPV * kDriftSample * kDriftThreads - 1) / (EPV * kDriftSample * kDriftThreads);
-  uint32_t smp[kNSV][4];  // this thread's sampled vectors
-#pragma unroll
-  for (int q = 0; q < kNSV; ++q)
-    F::load_vec(smp[q], nullptr, tg, aligned, (tid + q * kDriftThreads) * kDriftSample, V);
-  const int n_samples = sampled_count(V, EPV);
-  auto samples = [&](auto f) {
-#pragma unroll
-    for (int q = 0; q < kNSV; ++q) {
-      const int v = (tid + q * kDriftThreads) * kDriftSample;
-#pragma unroll
-      for (int e = 0; e < EPV; ++e)
-        if (v * EPV + e < V) f(order_key<BF16>(elem_bits<BF16>(smp[q], e)));
-    }
-  };
-  auto sample_rank = [&](int r) -> uint32_t {
-    if (r > n_samples) return 0u;  // too few samples: every key qualifies
-    int na, ne;
-    return kth_largest(samples, r, na, ne);
-  };
-  // ---- one pass over the position's target row, one warp per slice of
-  // kStatsSlice logits.  With `stats` a warp forms its slice's max and sum
-  // of exp2((l - m) s2) exactly as the draft-row kernel does (same lane
-  // mapping, batch and fold); it always lists the keys >= tau.
-  auto pass = [&](bool stats, uint32_t tau) {
-    if (tid == 0) ctl.n_cand = 0;
-    const float tau_f = key_value<BF16>(tau);
-    const uint32_t tau_w = pack_threshold<BF16>(tau_f);
-    __syncthreads();
-    constexpr int U = kStatsU;
-    for (int sl = warp; sl < P.nslices; sl += kDriftWarps) {
-      const int s0 = sl * P.slice, len = min(V - s0, P.slice);
-      const char *src = tg + (size_t)s0 * ESZ;
-      const int snv = (len + EPV - 1) / EPV, sv0 = s0 / EPV;
-      float m = -kInf, sacc = 0.f;
-      auto load_batch = [&](uint32_t (&w)[U][4], int v0) {
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int v = v0 + u * 32 + lane;
-          if (aligned) {
-            if (v < snv) {
-              const uint4 x = __ldg(reinterpret_cast<const uint4 *>(src) + v);
-              w[u][0] = x.x; w[u][1] = x.y; w[u][2] = x.z; w[u][3] = x.w;
-            } else {
-              w[u][0] = w[u][1] = w[u][2] = w[u][3] = F::NEG_INF_WORD;
-            }
-          } else {
-            F::load_vec(w[u], nullptr, src, false, v, len);
-          }
-        }
-      };
-      // two batches in flight, folded in order as the draft-row kernel does
-      for (int v00 = 0; v00 < snv; v00 += 64 * U) {
-        uint32_t wab[2][U][4];
-        load_batch(wab[0], v00);
-        load_batch(wab[1], v00 + 32 * U);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t (&w)[U][4] = wab[h];
-          const int v0 = v00 + 32 * U * h;
-          if (stats) online_accumulate<BF16, U>(w, s2, m, sacc);
-#pragma unroll
-          for (int u = 0; u < U; ++u) {
-            // fewer than one vector in ten holds a candidate: each lane visits
-            // only its elements not below tau, one at a time, and appends them
-            // (the selection does not depend on order)
-            uint32_t msk = may_reach_bits<BF16>(w[u], tau_w, tau_f);
-            while (msk) {
-              const int e = __ffs(msk) - 1;
-              msk &= msk - 1;
-              const int idx = (sv0 + v0 + u * 32 + lane) * EPV + e;
-              const uint32_t k = order_key<BF16>(elem_bits_at<BF16>(w[u], e));
-              if (k >= tau && idx < V) {
-                const int slot = atomicAdd(&ctl.n_cand, 1);
-                if (slot < kDriftCand) {
-                  ctl.cand.key[slot] = k;
-                  ctl.cand.idx[slot] = idx;
-                }
-              }
-            }
-          }
-        }
-      }
-      if (stats) {
-        float M, S;
-        fold_max_sum(m, sacc, s2, &M, &S);
-        if (lane == 0) {
-          ctl.slm[sl] = M;
-          ctl.sls[sl] = S;
-        }
-      }
-    }
-    __syncthreads();
-    return ctl.n_cand;
-  };
-  int r = 8;
-  int nc = pass(true, sample_rank(r));
-  // ---- the target row's max and sum: warps, then warp 0 folds the slices
-  // in the fixed order the finishing kernel uses for the draft row's
-  // records, so identical rows give identical bits.  The (max, sum) and this
-  // position's flags go to the finishing kernel in a stamped record.
-  {
-    if (warp == 0) {
-      float M1, S1;
-      fold_slice_stats(P.nslices, lane, s2, [&](int t, float *qm, float *qs) {
-        *qm = ctl.slm[t];
-        *qs = ctl.sls[t];
-        return true;
-      }, &M1, &S1);
-      if (lane == 0) {
-        uint32_t f = tflags;
-        if (M1 != M1 || M1 == kInf) f |= F_NONFINITE;
-        else if (M1 == -kInf) f |= F_EMPTY;
-        ctl.flags = f;
-        ctl.Mp = M1;
-        ctl.Sp = S1;
-        store_part(P.trunc_area + (size_t)b * K + j, M1, S1, f, tag);
-      }
-    }
-    __syncthreads();
-  }
-  if (ctl.flags) {  // the finishing kernel blanks the whole row
-    for (int i = tid; i < m; i += kDriftThreads) {
-      sup[i] = -1;
-      res[i] = __int_as_float(0x7fc00000);
-    }
-    return;
-  }
-  const float nMp = -__fmul_rn(ctl.Mp, s2);
-  const float l2Sp = lg2(ctl.Sp);
-  // support entry `rank` is token ii: its log2 p as in the walk, kept in the
-  // residual's place until the finishing kernel subtracts log2 q
-  auto emit = [&](int rank, int ii) {
-    float lt;
-    if constexpr (BF16) lt = bf16_lo(__ldg(reinterpret_cast<const unsigned short *>(tg) + ii));
-    else lt = __ldg(reinterpret_cast<const float *>(tg) + ii);
-    sup[rank] = ii;
-    res[rank] = __fadd_rn(__fmaf_rn(lt, s2, nMp), -l2Sp);
-  };
-  for (int attempt = 0; attempt < 3; ++attempt) {
-    if (attempt > 0) nc = pass(false, sample_rank(r));
-    if (nc >= m && nc <= kDriftCand) {
-      // the m-th largest candidate key; every candidate above it is taken,
-      // and of those equal to it the lowest token ids
-      auto cands = [&](auto f) {
-        for (int i = tid; i < nc; i += kDriftThreads) f(ctl.cand.key[i]);
-      };
-      int n_above, n_equal;
-      const uint32_t tkey = kth_largest(cands, m, n_above, n_equal);
-      const int need_eq = m - n_above;
-      if (tid == 0) {
-        ctl.n_gt = 0;
-        ctl.n_eq = 0;
-      }
-      __syncthreads();
-      for (int i = tid; i < nc; i += kDriftThreads) {
-        const uint32_t k = ctl.cand.key[i];
-        const int ii = ctl.cand.idx[i];
-        if (k > tkey) {
-          const int slot = atomicAdd(&ctl.n_gt, 1);
-          ctl.sel_idx[slot] = ii;
-          ctl.sel_key[slot] = k;
-        } else if (k == tkey) {
-          bool take = true;
-          if (n_equal > need_eq) {  // ties straddle the boundary: lowest ids
-            int before = 0;
-            for (int q = 0; q < nc; ++q)
-              before += ctl.cand.key[q] == tkey && ctl.cand.idx[q] < ii;
-            take = before < need_eq;
-          }
-          if (take) {
-            const int slot = n_above + atomicAdd(&ctl.n_eq, 1);
-            ctl.sel_idx[slot] = ii;
-            ctl.sel_key[slot] = k;
-          }
-        }
-      }
-      __syncthreads();
-      for (int i = tid; i < m; i += kDriftThreads) {
-        const uint32_t ki = ctl.sel_key[i];
-        const int ii = ctl.sel_idx[i];
-        int rank = 0;
-        for (int q = 0; q < m; ++q) {
-          const uint32_t kq = ctl.sel_key[q];
-          rank += (kq > ki) || (kq == ki && ctl.sel_idx[q] < ii);
-        }
-        emit(rank, ii);
-      }
-      return;
-    }
-    if (nc < m) r *= 4;                  // threshold too high: lower it
-    else if (r > 1) r = max(1, r / 4);   // too many candidates: raise it
-    else break;                          // even the largest sample admits too many
-    __syncthreads();
-  }
-  __syncthreads();
-  // ---- fallback (the sample missed: too few or too many candidates):
-  // radix selection of the m-th largest key over the whole row
-  uint32_t prefix = 0, pmask = 0;
-  int rem = m;  // rank still to find within the keys matching prefix
-  int last_count = 0;
-  for (int shift = KEYBITS - 8; shift >= 0; shift -= 8) {
-    for (int i = tid; i < kDriftWarps * 256; i += kDriftThreads) (&ctl.hist[0][0])[i] = 0;
-    __syncthreads();
-    for (int v = tid; v < nvec; v += kDriftThreads) {
-      uint32_t w[4];
-      F::load_vec(w, nullptr, tg, aligned, v, V);
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) {
-        const uint32_t k = order_key<BF16>(elem_bits<BF16>(w, e));
-        if ((k & pmask) == prefix && v * EPV + e < V) {
-          const uint32_t d = (k >> shift) & 255u;
-          const unsigned same = __match_any_sync(__activemask(), d);
-          if (lane == __ffs(same) - 1) atomicAdd(&ctl.hist[warp][d], __popc(same));
-        }
-      }
-    }
-    __syncthreads();
-    if (tid < 256) {
-      int c = 0;
-      for (int w2 = 0; w2 < kDriftWarps; ++w2) c += ctl.hist[w2][tid];
-      ctl.hist[0][tid] = c;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // lane l owns bins 255-8l .. 248-8l (descending); suffix counts from the top
-      int cnt[8], own = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        cnt[i] = ctl.hist[0][255 - 8 * lane - i];
-        own += cnt[i];
-      }
-      int incl = own;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(FULL_MASK, incl, o);
-        if (lane >= o) incl += n;
-      }
-      int above = incl - own;  // keys in higher bins than this lane's
-      if (above < rem && rem <= incl) {
-        int dgt = 255 - 8 * lane;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (above + cnt[i] >= rem) {
-            dgt = 255 - 8 * lane - i;
-            break;
-          }
-          above += cnt[i];
-        }
-        ctl.digit = dgt;
-        ctl.above = above;
-      }
-    }
-    __syncthreads();
-    const int dgt = ctl.digit;
-    rem -= ctl.above;
-    last_count = ctl.hist[0][dgt];
-    prefix |= static_cast<uint32_t>(dgt) << shift;
-    pmask |= 255u << shift;
-    __syncthreads();  // hist and digit are reused by the next pass
-  }
-  const uint32_t tkey = prefix;  // key of the m-th largest
-  const int n_gt = m - rem;      // keys above it, all selected
-  // ---- collect: every key above tkey; rem keys equal to it, lowest index first
-  if (tid == 0) {
-    ctl.n_gt = 0;
-    ctl.n_eq = 0;
-  }
-  __syncthreads();
-  const bool take_all_eq = last_count == rem;
-  for (int v = tid; v < nvec; v += kDriftThreads) {
-    uint32_t w[4];
-    F::load_vec(w, nullptr, tg, aligned, v, V);
-#pragma unroll
-    for (int e = 0; e < EPV; ++e) {
-      const int idx = v * EPV + e;
-      if (idx >= V) continue;
-      const uint32_t k = order_key<BF16>(elem_bits<BF16>(w, e));
-      if (k > tkey) {
-        const int slot = atomicAdd(&ctl.n_gt, 1);
-        ctl.sel_idx[slot] = idx;
-        ctl.sel_key[slot] = k;
-      } else if (k == tkey && take_all_eq) {
-        const int slot = n_gt + atomicAdd(&ctl.n_eq, 1);
-        ctl.sel_idx[slot] = idx;
-        ctl.sel_key[slot] = k;
-      }
-    }
-  }
-  if (!take_all_eq) {
-    // ties straddle the boundary: each thread counts the equal keys of its
-    // contiguous index range, an exclusive scan orders them, and the first
-    // rem in vocabulary order are taken
-    const int span = (V + kDriftThreads - 1) / kDriftThreads;
-    const int i0 = min(V, tid * span), i1 = min(V, i0 + span);
-    int mine = 0;
-    for (int i = i0; i < i1; ++i) mine += order_key<BF16>(bits_at(i)) == tkey;
-    int incl = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(FULL_MASK, incl, o);
-      if (lane >= o) incl += n;
-    }
-    if (lane == 31) ctl.scan[warp] = incl;
-    __syncthreads();
-    int base = incl - mine;
-    for (int w2 = 0; w2 < warp; ++w2) base += ctl.scan[w2];
-    for (int i = i0; i < i1 && base < rem; ++i) {
-      if (order_key<BF16>(bits_at(i)) == tkey) {
-        ctl.sel_idx[n_gt + base] = i;
-        ctl.sel_key[n_gt + base] = tkey;
-        ++base;
-      }
-    }
-  }
-  __syncthreads();
-  // ---- rank (key descending, index ascending) among the m selected
-  for (int i = tid; i < m; i += kDriftThreads) {
-    const uint32_t ki = ctl.sel_key[i];
-    const int ii = ctl.sel_idx[i];
-    int rank = 0;
-    for (int q = 0; q < m; ++q) {
-      const uint32_t kq = ctl.sel_key[q];
-      rank += (kq > ki) || (kq == ki && ctl.sel_idx[q] < ii);
-    }
-    emit(rank, ii);
-  }
-}
-
-// DRIFT, third kernel: one CTA per row, a programmatic dependent of the
-// draft rows' statistics grid (which completes only after the selection grid
-// has), so both grids' writes are visible after its dependency wait.  Each
-// warp takes drafted positions in turn: it folds the draft row's slice
-// records in the order the selection kernel folded the target row's, forms
-// log2 q at the m support tokens and replaces the log2 p the selection kernel
-// left there by the residual log p - log q in nats.  A position whose record
+// DRIFT, last kernel: one CTA per row, a programmatic dependent of the pick
+// grid (which completes only after the stream grid has), so both grids'
+// writes are visible after its dependency wait.  Each warp takes drafted
+// positions in turn: it folds the draft row's tile records in the order the
+// pick kernel folded the target row's, forms log2 q at the m support tokens
+// and replaces the log2 p the pick kernel left there by the residual
+// log p - log q in nats.  A position whose record
 // (the selection's, or a draft slice's) did not come is a timeout.  The row
 // status ORs every position's flags; a flagged row gets support -1 and
 // residual NaN everywhere, since no single selection CTA sees the whole row.
@@ -2078,16 +1632,22 @@ __global__ void __launch_bounds__(kDriftFinishThreads) drift_finish_kernel(const
     float M1 = 0.f, S1 = 0.f, M2, S2;
     uint32_t f1 = 0;
     const bool sel_in = load_part(P.trunc_area + (size_t)b * K + j, tag, &M1, &S1, &f1);
+    // the draft row's records, in the stream's row numbering
+    const long long drow = (long long)P.B * (K + 1) + (long long)b * K + j;
+    uint32_t df = 0;
     const bool stats_in = fold_slice_stats(nt, lane, s2, [&](int t, float *qm, float *qs) {
-      uint32_t qf;
-      if (!SV_INB((long long)(b * K + j) * nt + t, (long long)P.B * K * nt)) {
+      uint32_t qf = 0;
+      if (!SV_INB(drow * nt + t, (long long)P.B * (2 * K + 1) * nt)) {
         *qm = -kInf;
         *qs = 0.f;
         return false;
       }
-      return load_part(P.part + (size_t)(b * K + j) * nt + t, tag, qm, qs, &qf);
+      const bool ok = load_part(P.part + (size_t)drow * nt + t, tag, qm, qs, &qf);
+      df |= qf;
+      return ok;
     }, &M2, &S2);
-    uint32_t f = f1 | (sel_in && stats_in ? 0u : F_TIMEOUT);
+    df = __reduce_or_sync(FULL_MASK, df);
+    uint32_t f = f1 | (sel_in && stats_in && !df ? 0u : F_TIMEOUT);
     if (M2 != M2 || M2 == kInf) f |= F_NONFINITE;
     else if (M2 == -kInf) f |= F_EMPTY;
     if (lane == 0) {
@@ -2201,6 +1761,150 @@ __device__ uint32_t kth_largest_key16(const unsigned short *keys, int n, int r, 
   return th;
 }
 
+// Scratch of chunk_candidates, kept in the calling kernel's control block.
+struct ChunkScratch {
+  int clist[kMaxSelChunks];  // chunks to re-read
+  uint32_t aux[kSelThreads]; // the threads' largest keys, then the keys above their bound
+  int cred[2][kSelWarps];    // counts of the threshold search
+  int n_surv, n_chunks, n_cand;
+  uint32_t bound;
+};
+
+// The candidates of one logit row from its chunk maxima (nch of them in
+// shared memory, the top 16 bits of each chunk's largest order key): the
+// rc-th largest maximum th is the threshold, and every logit of a chunk whose
+// maximum reaches th is listed into ck as (key << 32) | ~index when its key
+// reaches th too.  Every logit of the row whose key reaches th is listed.
+// ck may share memory with the maxima (they are read before it is written).
+// With exact false, th is the lower bound below instead (also at most the
+// row's rc-th largest logit: fewer steps, a few more candidates).  Returns
+// the candidate count (possibly above cap, which ck holds at most), or -1
+// when more than kMaxSelChunks chunks reach th.  The 192 threads of the
+// block call it.
+template <bool BF16>
+__device__ int chunk_candidates(const unsigned short *chunk, int nch, int rc, const char *src,
+                                bool aligned, int nvec, int V, ChunkScratch &cs,
+                                unsigned long long *ck, int cap, bool exact) {
+  using F = Fmt<BF16>;
+  constexpr int EPV = F::EPV;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    cs.n_chunks = 0;
+    cs.n_cand = 0;
+  }
+  // A lower bound first: the rc-th largest of the threads' largest keys (rc
+  // threads hold a key at least that large, so at least rc keys reach it);
+  // only the keys that reach it can be th, and warp 0 searches those when
+  // they are few.
+  const uint32_t *wk = reinterpret_cast<const uint32_t *>(chunk);
+  const int nw = nch / 2;
+  auto warp_kth = [&](int n) {  // warp 0: the rc-th largest of aux[0 .. n), n <= kSelThreads
+    constexpr int PL = kSelThreads / 32;
+    uint32_t v[PL];
+#pragma unroll
+    for (int i = 0; i < PL; ++i) v[i] = lane + 32 * i < n ? cs.aux[lane + 32 * i] : 0u;
+    uint32_t x = 0;
+#pragma unroll 1
+    for (int bit = 15; bit >= 0; --bit) {  // (a candidate is >= 1: padding never counts)
+      const uint32_t c = x | (1u << bit);
+      int cnt = 0;
+#pragma unroll
+      for (int i = 0; i < PL; ++i) cnt += v[i] >= c ? 1 : 0;
+      if (static_cast<int>(__reduce_add_sync(FULL_MASK, static_cast<unsigned>(cnt))) >= rc) x = c;
+    }
+    return x;
+  };
+  {
+    uint32_t tmax = 0;
+    for (int w = tid; w < nw; w += kSelThreads) {
+      const uint32_t x = wk[w];
+      tmax = max(tmax, max(x & 0xFFFFu, x >> 16));
+    }
+    cs.aux[tid] = tmax;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t lb = warp_kth(kSelThreads);
+    if (lane == 0) {
+      cs.bound = lb;
+      cs.n_surv = 0;
+    }
+  }
+  __syncthreads();
+  if (exact) {
+    const uint32_t lb = cs.bound;
+    for (int w = tid; w < nw; w += kSelThreads) {
+      const uint32_t x = wk[w];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t k = h ? (x >> 16) : (x & 0xFFFFu);
+        if (k >= lb) {
+          const int slot = atomicAdd(&cs.n_surv, 1);
+          if (slot < kSelThreads) cs.aux[slot] = k;
+        }
+      }
+    }
+  }
+  uint32_t th = cs.bound;
+  if (exact) {
+    __syncthreads();
+    if (cs.n_surv <= kSelThreads) {
+      if (warp == 0) {
+        const uint32_t x = warp_kth(cs.n_surv);
+        if (lane == 0) cs.bound = x;
+      }
+      __syncthreads();
+      th = cs.bound;
+    } else {
+      th = kth_largest_key16<kSelThreads>(chunk, nch, rc, cs.cred);
+    }
+  }
+  // the chunks whose maximum reaches it
+  for (int c = tid; c < nch; c += kSelThreads) {
+    if (chunk[c] >= th) {
+      const int slot = atomicAdd(&cs.n_chunks, 1);
+      if (slot < kMaxSelChunks) cs.clist[slot] = c;
+    }
+  }
+  __syncthreads();
+  const int nsel = cs.n_chunks;
+  if (nsel > kMaxSelChunks) return -1;
+  // their vectors, all loads in flight at once, then every logit whose key
+  // reaches th (the maxima keep the top 16 bits of a logit's key)
+  constexpr int PERV = (kMaxSelChunks * kSoftVecs + kSelThreads - 1) / kSelThreads;
+  uint32_t w[PERV][4];
+  int vid[PERV];
+#pragma unroll
+  for (int q2 = 0; q2 < PERV; ++q2) {
+    const int i = tid + q2 * kSelThreads;  // (chunk i / kSoftVecs, vector i % kSoftVecs)
+    vid[q2] = -1;
+    if (i < nsel * kSoftVecs) {
+      const int c = cs.clist[i / kSoftVecs];
+      const int t = c / kSoftThreads, lt = c - t * kSoftThreads;
+      vid[q2] = t * (kSoftThreads * kSoftVecs) + lt + (i % kSoftVecs) * kSoftThreads;
+    }
+    F::load_vec(w[q2], nullptr, src, aligned, vid[q2] < 0 ? nvec : vid[q2], V);
+  }
+  __syncthreads();  // the maxima are read: the candidates may overwrite them
+#pragma unroll
+  for (int q2 = 0; q2 < PERV; ++q2) {
+    if (vid[q2] < 0) continue;
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) {
+      const uint32_t bits = elem_bits<BF16>(w[q2], e);
+      const uint32_t k = order_key<BF16>(bits);
+      const uint32_t k16 = BF16 ? k : (k >> 16);
+      const int idx = vid[q2] * EPV + e;
+      if (k16 >= th && idx < V) {
+        const int slot = atomicAdd(&cs.n_cand, 1);
+        if (slot < cap) ck[slot] = (static_cast<unsigned long long>(k) << 32) | (~static_cast<uint32_t>(idx));
+      }
+    }
+  }
+  __syncthreads();
+  return cs.n_cand;
+}
+
 struct alignas(16) TruncCtrl {
   // the row's chunk maxima, then (once they are used) the candidates:
   // (key << 32) | (~token id), which sorts key desc, id asc, and their
@@ -2212,11 +1916,7 @@ struct alignas(16) TruncCtrl {
       float e[kDriftCand];
     };
   };
-  int clist[kMaxSelChunks];  // chunks to re-read
-  uint32_t aux[kSelThreads]; // the threads' largest keys, then the keys above their bound
-  int cred[2][kSelWarps];    // counts of the threshold search
-  int n_surv;
-  uint32_t bound;
+  ChunkScratch cs;
   int settled;               // warp 0's settling of a small list: 1 done, 0 retry
   uint32_t theta_w;
   float kept_w;
@@ -2224,7 +1924,7 @@ struct alignas(16) TruncCtrl {
   float fred[kSelWarps];
   int ired[kSelWarps];
   int chist[256];
-  int n_cand, n_chunks, digit, above, pos;
+  int n_cand, digit, above, pos;
   float M, S;
   uint32_t flags;
 };
@@ -2374,126 +2074,6 @@ __global__ void __launch_bounds__(kSelThreads, 6) trunc_select_kernel(const __gr
                 ctl.ck[slot] = (static_cast<unsigned long long>(k) << 32) | (~static_cast<uint32_t>(idx));
             }
           }
-        }
-      }
-    }
-    __syncthreads();
-    return ctl.n_cand;
-  };
-  // ---- the candidates from the chunk maxima: the rc-th largest maximum is
-  // the threshold; returns the candidate count, or -1 when the chunks cannot
-  // give a list (the row's maxima do not fit, or too many chunks reach it)
-  auto gather_chunks = [&]() -> int {
-    if (!use_chunks) return -1;
-    if (tid == 0) {
-      ctl.n_chunks = 0;
-      ctl.n_cand = 0;
-    }
-    // The threshold th is the rc-th largest maximum.  A lower bound first:
-    // the rc-th largest of the threads' largest keys (rc threads hold a key at
-    // least that large, so at least rc keys reach it); only the keys that
-    // reach it can be th, and warp 0 searches those when they are few.
-    const uint32_t *wk = reinterpret_cast<const uint32_t *>(ctl.chunk);
-    const int nw = nch / 2;
-    auto warp_kth = [&](int n) {  // warp 0: the rc-th largest of aux[0 .. n), n <= kSelThreads
-      constexpr int PL = kSelThreads / 32;
-      uint32_t v[PL];
-#pragma unroll
-      for (int i = 0; i < PL; ++i) v[i] = lane + 32 * i < n ? ctl.aux[lane + 32 * i] : 0u;
-      uint32_t x = 0;
-#pragma unroll 1
-      for (int bit = 15; bit >= 0; --bit) {  // (a candidate is >= 1: padding never counts)
-        const uint32_t c = x | (1u << bit);
-        int cnt = 0;
-#pragma unroll
-        for (int i = 0; i < PL; ++i) cnt += v[i] >= c ? 1 : 0;
-        if (static_cast<int>(__reduce_add_sync(FULL_MASK, static_cast<unsigned>(cnt))) >= rc) x = c;
-      }
-      return x;
-    };
-    {
-      uint32_t tmax = 0;
-      for (int w = tid; w < nw; w += kSelThreads) {
-        const uint32_t x = wk[w];
-        tmax = max(tmax, max(x & 0xFFFFu, x >> 16));
-      }
-      ctl.aux[tid] = tmax;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const uint32_t lb = warp_kth(kSelThreads);
-      if (lane == 0) {
-        ctl.bound = lb;
-        ctl.n_surv = 0;
-      }
-    }
-    __syncthreads();
-    {
-      const uint32_t lb = ctl.bound;
-      for (int w = tid; w < nw; w += kSelThreads) {
-        const uint32_t x = wk[w];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t k = h ? (x >> 16) : (x & 0xFFFFu);
-          if (k >= lb) {
-            const int slot = atomicAdd(&ctl.n_surv, 1);
-            if (slot < kSelThreads) ctl.aux[slot] = k;
-          }
-        }
-      }
-    }
-    __syncthreads();
-    uint32_t th;
-    if (ctl.n_surv <= kSelThreads) {
-      if (warp == 0) {
-        const uint32_t x = warp_kth(ctl.n_surv);
-        if (lane == 0) ctl.bound = x;
-      }
-      __syncthreads();
-      th = ctl.bound;
-    } else {
-      th = kth_largest_key16<kSelThreads>(ctl.chunk, nch, rc, ctl.cred);
-    }
-    // the chunks whose maximum reaches it
-    for (int c = tid; c < nch; c += kSelThreads) {
-      if (ctl.chunk[c] >= th) {
-        const int slot = atomicAdd(&ctl.n_chunks, 1);
-        if (slot < kMaxSelChunks) ctl.clist[slot] = c;
-      }
-    }
-    __syncthreads();
-    const int nsel = ctl.n_chunks;
-    if (nsel > kMaxSelChunks) return -1;
-    // their vectors, all loads in flight at once, then every logit whose key
-    // reaches th (the maxima keep the top 16 bits of a logit's key)
-    constexpr int PERV = (kMaxSelChunks * kSoftVecs + kSelThreads - 1) / kSelThreads;
-    uint32_t w[PERV][4];
-    int vid[PERV];
-#pragma unroll
-    for (int q2 = 0; q2 < PERV; ++q2) {
-      const int i = tid + q2 * kSelThreads;  // (chunk i / kSoftVecs, vector i % kSoftVecs)
-      vid[q2] = -1;
-      if (i < nsel * kSoftVecs) {
-        const int c = ctl.clist[i / kSoftVecs];
-        const int t = c / kSoftThreads, lt = c - t * kSoftThreads;
-        vid[q2] = t * (kSoftThreads * kSoftVecs) + lt + (i % kSoftVecs) * kSoftThreads;
-      }
-      F::load_vec(w[q2], nullptr, src, aligned, vid[q2] < 0 ? nvec : vid[q2], V);
-    }
-    __syncthreads();  // the maxima are read: the candidates may overwrite them
-#pragma unroll
-    for (int q2 = 0; q2 < PERV; ++q2) {
-      if (vid[q2] < 0) continue;
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) {
-        const uint32_t bits = elem_bits<BF16>(w[q2], e);
-        const uint32_t k = order_key<BF16>(bits);
-        const uint32_t k16 = BF16 ? k : (k >> 16);
-        const int idx = vid[q2] * EPV + e;
-        if (k16 >= th && idx < V) {
-          const int slot = atomicAdd(&ctl.n_cand, 1);
-          if (slot < kDriftCand)
-            ctl.ck[slot] = (static_cast<unsigned long long>(k) << 32) | (~static_cast<uint32_t>(idx));
         }
       }
     }
@@ -2715,7 +2295,10 @@ __global__ void __launch_bounds__(kSelThreads, 6) trunc_select_kernel(const __gr
   int klen = 0;  // entries of the kept list written for the resolve kernel
   bool done = false;
   int r = trunc_sample_rank(tk);
-  int nc = gather_chunks();
+  // the candidates from the chunk maxima (-1: they cannot give a list)
+  int nc = use_chunks ? chunk_candidates<BF16>(ctl.chunk, nch, rc, src, aligned, nvec, V, ctl.cs, ctl.ck, kDriftCand,
+                                               true)
+                      : -1;
   // ---- the row's max and sum from the stream's tile records (warp 0); a
   // record missing or flagged, or a non-finite or empty row, gets no
   // thresholds (the resolve kernel reports the row from the same records)
@@ -2892,6 +2475,279 @@ __global__ void __launch_bounds__(kSelThreads, 6) trunc_select_kernel(const __gr
   if (tid == 0) store_part(rec, __uint_as_float(theta), kept, static_cast<uint32_t>(klen) << 1, tag);
 }
 
+// ---- DRIFT's pick: one CTA of kSelThreads per drafted position j < K of
+// row b, a programmatic dependent of the ring stream (no bonus position;
+// chunk maxima for the target rows).
+
+constexpr int kPickCand = kSelThreads;  // candidates ranked one per thread
+
+struct alignas(16) PickCtrl {
+  // the row's chunk maxima, then (once they are used) the candidates, or
+  // the whole-row radix histograms of the fallback
+  union {
+    unsigned short chunk[kMaxRowChunks];
+    unsigned long long ck[kPickCand];
+    int hist[kSelWarps][256];
+  };
+  ChunkScratch cs;
+  int sel_idx[kDriftMaxM];
+  uint32_t sel_key[kDriftMaxM];
+  int scan[kSelWarps];
+  int n_gt, n_eq, digit, above;
+  float Mp, Sp;
+  uint32_t flags;
+};
+
+template <bool BF16>
+__global__ void __launch_bounds__(kSelThreads, 6) drift_pick_kernel(const __grid_constant__ ChainStochParams P) {
+  using F = Fmt<BF16>;
+  constexpr int EPV = F::EPV, ESZ = F::ESZ;
+  constexpr int KEYBITS = BF16 ? 16 : 32;
+  constexpr int NW = kSelWarps;
+  __shared__ PickCtrl ctl;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K = P.K, npos = K + 1, V = P.V, m = P.drift_m, nt = P.nslices;
+  const int b = blockIdx.x / K, j = blockIdx.x - b * K;
+  const int row = b * npos + j;  // the target row of position j
+  // The stream has completed, and with it the generation step: its tile
+  // records and chunk maxima are in, and the tag read below is this call's.
+  grid_dependency_wait();
+  allow_dependents();
+  // forced-timeout test: no record of this call appears, so the finishing
+  // kernel reports a timeout
+  if (P.force_timeout) return;
+  const float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
+  const uint32_t tflags = (T > 0.f && T < kInf) ? 0u : F_BAD_TEMPERATURE;
+  const float s2 = __fdiv_rn(kLog2e, tflags ? 1.0f : T);  // the stream's (a bad T flags the row)
+  const uint32_t tag = *reinterpret_cast<volatile const uint32_t *>(P.gen);
+  int32_t *sup = P.drift_support + ((size_t)b * K + j) * m;
+  float *res = P.drift_residual + ((size_t)b * K + j) * m;
+  const char *tg = static_cast<const char *>(P.target) + (size_t)row * V * ESZ;
+  const bool aligned = P.use_tma != 0;
+  const int nvec = (V + EPV - 1) / EPV;
+  // the chunk maxima (copied while warp 0 loads the tile records)
+  const int nch = nt * kSoftThreads;
+  const bool use_chunks = m <= kMaxSelChunks && m <= nch && nch <= kMaxRowChunks;
+  if (use_chunks) {
+    const uint4 *srcm = reinterpret_cast<const uint4 *>(P.cmax + (size_t)row * nch);
+    const int nv = nch / 8;
+    for (int v = tid; v < nv; v += kSelThreads)
+      if (SV_INB((long long)row * nv + v, (long long)P.B * (2 * K + 1) * nv))
+        cp_async16(reinterpret_cast<uint4 *>(ctl.chunk) + v, srcm + v);
+  }
+  unsigned long long rec_a[2] = {0ull, 0ull}, rec_b[2] = {0ull, 0ull};
+  if (warp == 0) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int t = lane + 32 * h;
+      if (t < nt && SV_INB((long long)row * nt + t, (long long)P.B * (2 * K + 1) * nt)) {
+        rec_a[h] = ld_relaxed_u64(&P.part[(size_t)row * nt + t].a);
+        rec_b[h] = ld_relaxed_u64(&P.part[(size_t)row * nt + t].b);
+      }
+    }
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  const int nc = use_chunks ? chunk_candidates<BF16>(ctl.chunk, nch, m, tg, aligned, nvec, V, ctl.cs, ctl.ck, kPickCand,
+                                                     false)
+                            : -1;
+  // ---- the target row's max and sum, folded from its tile records in the
+  // order the finishing kernel folds the draft row's; with this position's
+  // flags they go to the finishing kernel in a stamped record
+  if (warp == 0) {
+    float M1, S1;
+    uint32_t rf = 0;
+    const bool ready = fold_slice_stats(nt, lane, s2, [&](int t, float *qm, float *qs) {
+      uint32_t qf = 0;
+      const int h = t >> 5;  // t = lane + 32 h
+      const bool ok = decode_part(h ? rec_a[1] : rec_a[0], h ? rec_b[1] : rec_b[0], tag, qm, qs, &qf);
+      rf |= qf;
+      return ok;
+    }, &M1, &S1);
+    rf = __reduce_or_sync(FULL_MASK, rf);
+    if (lane == 0) {
+      uint32_t f = tflags | (ready && !rf ? 0u : F_TIMEOUT);
+      if (M1 != M1 || M1 == kInf) f |= F_NONFINITE;
+      else if (M1 == -kInf) f |= F_EMPTY;
+      ctl.flags = f;
+      ctl.Mp = M1;
+      ctl.Sp = S1;
+      store_part(P.trunc_area + (size_t)b * K + j, M1, S1, f, tag);
+    }
+  }
+  __syncthreads();
+  if (ctl.flags) {  // the finishing kernel blanks the whole row
+    for (int i = tid; i < m; i += kSelThreads) {
+      sup[i] = -1;
+      res[i] = __int_as_float(0x7fc00000);
+    }
+    return;
+  }
+  const float nMp = -__fmul_rn(ctl.Mp, s2);
+  const float l2Sp = lg2(ctl.Sp);
+  // support entry `rank` is token ii with logit lt: its log2 p as in the
+  // walk, kept in the residual's place until the finishing kernel subtracts
+  // log2 q
+  auto emit = [&](int rank, int ii, float lt) {
+    sup[rank] = ii;
+    res[rank] = __fadd_rn(__fmaf_rn(lt, s2, nMp), -l2Sp);
+  };
+  if (nc >= m && nc <= kPickCand) {
+    // every logit at or above the threshold is a candidate: the m of highest
+    // (key, ~id) are the support, in that order
+    if (tid < nc) {
+      const unsigned long long mine = ctl.ck[tid];
+      int rank = 0;
+#pragma unroll 4
+      for (int q = 0; q < nc; ++q) rank += ctl.ck[q] > mine ? 1 : 0;
+      if (rank < m) emit(rank, static_cast<int>(~static_cast<uint32_t>(mine)),
+                         key_value<BF16>(static_cast<uint32_t>(mine >> 32)));
+    }
+    return;
+  }
+  // ---- fallback (the chunks cannot give the list: ties over too many
+  // chunks, or too many candidates): radix selection of the m-th largest
+  // key over the whole row, 8 bits a pass from the top
+  auto bits_at = [&](int i) -> uint32_t {
+    if constexpr (BF16) return __ldg(reinterpret_cast<const unsigned short *>(tg) + i);
+    else return __ldg(reinterpret_cast<const unsigned int *>(tg) + i);
+  };
+  __syncthreads();
+  uint32_t prefix = 0, pmask = 0;
+  int rem = m;  // rank still to find within the keys matching prefix
+  int last_count = 0;
+  for (int shift = KEYBITS - 8; shift >= 0; shift -= 8) {
+    for (int i = tid; i < NW * 256; i += kSelThreads) (&ctl.hist[0][0])[i] = 0;
+    __syncthreads();
+    for (int v = tid; v < nvec; v += kSelThreads) {
+      uint32_t w[4];
+      F::load_vec(w, nullptr, tg, aligned, v, V);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const uint32_t k = order_key<BF16>(elem_bits<BF16>(w, e));
+        if ((k & pmask) == prefix && v * EPV + e < V) {
+          const uint32_t d = (k >> shift) & 255u;
+          const unsigned same = __match_any_sync(__activemask(), d);
+          if (lane == __ffs(same) - 1) atomicAdd(&ctl.hist[warp][d], __popc(same));
+        }
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < 256; i += kSelThreads) {
+      int c = 0;
+      for (int w2 = 0; w2 < NW; ++w2) c += ctl.hist[w2][i];
+      ctl.hist[0][i] = c;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns bins 255-8l .. 248-8l (descending); suffix counts from the top
+      int cnt[8], own = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        cnt[i] = ctl.hist[0][255 - 8 * lane - i];
+        own += cnt[i];
+      }
+      int incl = own;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(FULL_MASK, incl, o);
+        if (lane >= o) incl += n;
+      }
+      int above = incl - own;  // keys in higher bins than this lane's
+      if (above < rem && rem <= incl) {
+        int dgt = 255 - 8 * lane;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (above + cnt[i] >= rem) {
+            dgt = 255 - 8 * lane - i;
+            break;
+          }
+          above += cnt[i];
+        }
+        ctl.digit = dgt;
+        ctl.above = above;
+      }
+    }
+    __syncthreads();
+    const int dgt = ctl.digit;
+    rem -= ctl.above;
+    last_count = ctl.hist[0][dgt];
+    prefix |= static_cast<uint32_t>(dgt) << shift;
+    pmask |= 255u << shift;
+    __syncthreads();  // hist and digit are reused by the next pass
+  }
+  const uint32_t tkey = prefix;  // key of the m-th largest
+  const int n_gt = m - rem;      // keys above it, all selected
+  // ---- collect: every key above tkey; rem keys equal to it, lowest index first
+  if (tid == 0) {
+    ctl.n_gt = 0;
+    ctl.n_eq = 0;
+  }
+  __syncthreads();
+  const bool take_all_eq = last_count == rem;
+  for (int v = tid; v < nvec; v += kSelThreads) {
+    uint32_t w[4];
+    F::load_vec(w, nullptr, tg, aligned, v, V);
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) {
+      const int idx = v * EPV + e;
+      if (idx >= V) continue;
+      const uint32_t k = order_key<BF16>(elem_bits<BF16>(w, e));
+      if (k > tkey) {
+        const int slot = atomicAdd(&ctl.n_gt, 1);
+        if (SV_INB(slot, kDriftMaxM)) {
+          ctl.sel_idx[slot] = idx;
+          ctl.sel_key[slot] = k;
+        }
+      } else if (k == tkey && take_all_eq) {
+        const int slot = n_gt + atomicAdd(&ctl.n_eq, 1);
+        if (SV_INB(slot, kDriftMaxM)) {
+          ctl.sel_idx[slot] = idx;
+          ctl.sel_key[slot] = k;
+        }
+      }
+    }
+  }
+  if (!take_all_eq) {
+    // ties straddle the boundary: each thread counts the equal keys of its
+    // contiguous index range, an exclusive scan orders them, and the first
+    // rem in vocabulary order are taken
+    const int span = (V + kSelThreads - 1) / kSelThreads;
+    const int i0 = min(V, tid * span), i1 = min(V, i0 + span);
+    int mine = 0;
+    for (int i = i0; i < i1; ++i) mine += order_key<BF16>(bits_at(i)) == tkey;
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(FULL_MASK, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) ctl.scan[warp] = incl;
+    __syncthreads();
+    int base = incl - mine;
+    for (int w2 = 0; w2 < warp; ++w2) base += ctl.scan[w2];
+    for (int i = i0; i < i1 && base < rem; ++i) {
+      if (order_key<BF16>(bits_at(i)) == tkey && SV_INB(n_gt + base, kDriftMaxM)) {
+        ctl.sel_idx[n_gt + base] = i;
+        ctl.sel_key[n_gt + base] = tkey;
+        ++base;
+      }
+    }
+  }
+  __syncthreads();
+  // ---- rank (key descending, index ascending) among the m selected
+  for (int i = tid; i < m; i += kSelThreads) {
+    const uint32_t ki = ctl.sel_key[i];
+    const int ii = ctl.sel_idx[i];
+    int rank = 0;
+    for (int q = 0; q < m; ++q) {
+      const uint32_t kq = ctl.sel_key[q];
+      rank += (kq > ki) || (kq == ki && ctl.sel_idx[q] < ii);
+    }
+    emit(rank, ii, key_value<BF16>(ki));
+  }
+}
+
 size_t resolve_smem(const ChainStochParams &p) {
   return static_cast<size_t>(2 * p.K + 1) * 16 + static_cast<size_t>(p.vpw / 32) * kResolveThreads * 4;
 }
@@ -3037,19 +2893,20 @@ cudaError_t launch_truncated_t(const ChainStochParams &p, int grid, size_t smem,
   return e;
 }
 
-// DRIFT: the generation step, one selection CTA per drafted position (the
-// target row's statistics and top m), the draft rows' statistics on the SMs
-// the selection's last, partial wave leaves idle, then one CTA per row that
-// forms the residuals and the row status.
+// DRIFT: the generation step, the ring stream over positions 0 .. K-1 (with
+// the target rows' chunk maxima), one pick CTA per drafted position (the
+// top m of its target row), then one CTA per row that forms the residuals
+// and the row status, each a programmatic dependent of the one before.
 template <bool BF16>
-cudaError_t launch_drift_t(const ChainStochParams &p, int grid, cudaStream_t s) {
-  cudaError_t e = launch_generation(p, s);
+cudaError_t launch_drift_t(const ChainStochParams &p, int grid, size_t smem, cudaStream_t s) {
+  cudaError_t e = prepare_ring<BF16, kSoftVecs, kSoftStages, true>(smem);
   if (e != cudaSuccess) return e;
-  drift_select_kernel<BF16><<<dim3(static_cast<unsigned>(p.K), static_cast<unsigned>(p.B)), kDriftThreads, 0, s>>>(p);
-  e = cudaGetLastError();
+  e = launch_generation(p, s);
   if (e == cudaSuccess)
-    e = p.use_tma ? launch_dependent(draft_stats_kernel<BF16, true>, dim3(static_cast<unsigned>(grid)), kStatsThreads, 0, s, p)
-                  : launch_dependent(draft_stats_kernel<BF16, false>, dim3(static_cast<unsigned>(grid)), kStatsThreads, 0, s, p);
+    e = launch_dependent(softmax_partials_kernel<BF16, kSoftVecs, kSoftStages, true>,
+                         dim3(static_cast<unsigned>(grid)), kSoftThreads + 32, smem, s, p);
+  if (e == cudaSuccess)
+    e = launch_dependent(drift_pick_kernel<BF16>, dim3(static_cast<unsigned>(p.B * p.K)), kSelThreads, 0, s, p);
   if (e == cudaSuccess)
     e = launch_dependent(drift_finish_kernel<BF16>, dim3(static_cast<unsigned>(p.B)), kDriftFinishThreads, 0, s, p);
   return e;
@@ -3091,8 +2948,8 @@ cudaError_t launch_chain_truncated(const ChainStochParams &p, bool bf16, int gri
               : launch_truncated_t<false>(p, grid, smem, cluster, s);
 }
 
-cudaError_t launch_drift(const ChainStochParams &p, bool bf16, int grid, cudaStream_t s) {
-  return bf16 ? launch_drift_t<true>(p, grid, s) : launch_drift_t<false>(p, grid, s);
+cudaError_t launch_drift(const ChainStochParams &p, bool bf16, int grid, size_t smem, cudaStream_t s) {
+  return bf16 ? launch_drift_t<true>(p, grid, smem, s) : launch_drift_t<false>(p, grid, smem, s);
 }
 
 }  // namespace sv

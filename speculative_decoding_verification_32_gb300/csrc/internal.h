@@ -150,17 +150,9 @@ constexpr int kSoftStages = 2;
 // The smallest vocabulary slice with a record of its own (the ring's fp32
 // tile): it sizes the workspace's record area.
 constexpr int kSoftMinSlice = kSoftThreads * kSoftVecs * 4;
-// DRIFT's row statistics: threads per CTA of the draft-row kernel, 16-byte
-// vectors in flight per lane, and logits per slice.  The selection kernel
-// forms the target row's statistics with the same slices, lane mapping and
-// batch, so identical rows give identical bits.
-constexpr int kStatsThreads = 256;
-constexpr int kStatsU = 4;
-constexpr int kStatsSlice = 4096;
-constexpr int kStatsMaxSlices = (SPEC_MAX_V + kStatsSlice - 1) / kStatsSlice;
 // The record area holds one record per (logit row, smallest slice of any
-// stochastic path).
-constexpr int kRecordSlice = kSoftMinSlice < kStatsSlice ? kSoftMinSlice : kStatsSlice;
+// stochastic path: the ring's fp32 tile).
+constexpr int kRecordSlice = kSoftMinSlice;
 // Entries of a kept list (the truncated verify's small kept sets).
 constexpr int kKeptMax = 64;
 // Largest rounds of 32 vectors per warp in the resolve kernel.
@@ -186,9 +178,9 @@ cudaError_t ring_blocks_per_sm(bool bf16, int stages, size_t smem, int *blocks);
 // the truncation thresholds, then the resolve kernel.
 cudaError_t launch_chain_truncated(const ChainStochParams &p, bool bf16, int grid, size_t smem,
                                    int cluster, cudaStream_t s);
-// Generation step, stream kernel, then the DRIFT selection kernel (one CTA per
-// drafted position).
-cudaError_t launch_drift(const ChainStochParams &p, bool bf16, int grid, cudaStream_t s);
+// Generation step, ring stream kernel (no bonus position, chunk maxima), the
+// DRIFT pick (one CTA per drafted position), then the residuals per row.
+cudaError_t launch_drift(const ChainStochParams &p, bool bf16, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_greedy(const GreedyParams &p, bool bf16, int grid, cudaStream_t s);
 cudaError_t greedy_max_blocks_per_sm(bool bf16, bool vec, int *blocks);
 cudaError_t launch_rollback(const RollbackParams &p, cudaStream_t s);

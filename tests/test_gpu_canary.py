@@ -292,7 +292,7 @@ def test_drift_writes_stay_in_bounds(L, V, K, m, dtype):
     sup = A.put("support", (B, K, m), np.int32)
     res = A.put("residual", (B, K, m), np.float32)
     st = A.put("row_status", (B,), np.int32)
-    nb = L.spec_verify_chain_workspace_size(B, K, V)
+    nb = L.spec_verify_chain_truncated_workspace_size(B, K, V)
     ws = A.put("workspace", (nb,), np.uint8)
     p = A.ptr
     dt = SPEC_BF16 if dtype == "bf16" else SPEC_F32

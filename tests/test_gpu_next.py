@@ -170,11 +170,12 @@ def test_drift_ties_unaligned_and_edges(sv, dtype, V):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_drift_edge_rows_in_the_last_wave(sv, dtype):
-    """43 rows x 8 drafted positions: on a GB300 (304 selection CTAs a wave)
-    the last 40 positions, rows 38-42, run in the selection's second wave,
-    beside the draft rows' statistics.  Those rows carry ties that straddle
-    the support boundary (in both halves of the row), an all-equal row,
-    identical laws, masked drafts, a NaN and a bad temperature."""
+    """43 rows x 8 drafted positions over V = 20000 (three ring tiles a row),
+    the last rows carrying the edge cases: ties that straddle the support
+    boundary in both halves of the row (many chunks share the largest
+    maximum), an all-equal row (every chunk ties: the whole-row search),
+    identical laws (exactly zero), masked drafts, a NaN and a bad
+    temperature."""
     rng = np.random.default_rng(4343)
     B, K, V, m = 43, 8, 20000, 32
     t = rng.normal(0, 3, (B, K + 1, V)).astype(np.float32)
