@@ -2210,16 +2210,24 @@ __global__ void __launch_bounds__(kSelThreads, 6) trunc_select_kernel(const __gr
   // the first prefix that reaches top_p of the kept mass, and its group) by
   // ballots.  The same arithmetic in the same order gives the same threshold
   // and kept mass.
-  auto settle_small = [&](int n) {
-    unsigned long long *sk = ctl.ck + kDriftCand / 2;  // the sorted keys (n <= 64)
-    if (tid < n) {
+  //
+  // A list of up to kSelThreads candidates under top-k is settled the same
+  // way from its 64 highest: the kept set lies among them unless the k-th
+  // key's group of ties reaches rank 63 (settled = 2: the block path below
+  // takes the list).
+  auto settle_small = [&](int n_all) {
+    const int n = min(n_all, 64);
+    unsigned long long *sk = ctl.ck + kDriftCand / 2;  // the 64 highest, sorted
+    if (tid < n_all) {
       const unsigned long long mine = ctl.ck[tid];
       int rank = 0;
 #pragma unroll 4
-      for (int j2 = 0; j2 < n; ++j2) rank += ctl.ck[j2] > mine ? 1 : 0;
-      const float l = key_value<BF16>(static_cast<uint32_t>(mine >> 32));
-      sk[rank] = mine;
-      ctl.e[rank] = l == -kInf ? 0.f : ex2(__fmaf_rn(l, s2, nM));
+      for (int j2 = 0; j2 < n_all; ++j2) rank += ctl.ck[j2] > mine ? 1 : 0;
+      if (rank < 64) {
+        const float l = key_value<BF16>(static_cast<uint32_t>(mine >> 32));
+        sk[rank] = mine;
+        ctl.e[rank] = l == -kInf ? 0.f : ex2(__fmaf_rn(l, s2, nM));
+      }
     }
     __syncthreads();
     if (warp != 0) return;
@@ -2256,6 +2264,10 @@ __global__ void __launch_bounds__(kSelThreads, 6) trunc_select_kernel(const __gr
       const unsigned b1 = __ballot_sync(FULL_MASK, lane + 32 < n && k1 == ki);
       return b1 ? 63 - __clz(b1) : 31 - __clz(b0);
     };
+    if (n_all > n && (tk > n || group_end(tk - 1) == n - 1)) {  // the kept set may go past rank 63
+      if (lane == 0) ctl.settled = 2;
+      return;
+    }
     int gk = n - 1;
     float Sk = ctl.S;
     if (tk > 0) {
@@ -2297,7 +2309,7 @@ __global__ void __launch_bounds__(kSelThreads, 6) trunc_select_kernel(const __gr
   int r = trunc_sample_rank(tk);
   // the candidates from the chunk maxima (-1: they cannot give a list)
   int nc = use_chunks ? chunk_candidates<BF16>(ctl.chunk, nch, rc, src, aligned, nvec, V, ctl.cs, ctl.ck, kDriftCand,
-                                               true)
+                                               tk == 0)
                       : -1;
   // ---- the row's max and sum from the stream's tile records (warp 0); a
   // record missing or flagged, or a non-finite or empty row, gets no
@@ -2337,14 +2349,19 @@ __global__ void __launch_bounds__(kSelThreads, 6) trunc_select_kernel(const __gr
       r *= 4;
       continue;
     }
-    if (nc <= 64) {  // a small list: ranks, then warp 0
+    bool small_done = false;
+    if (nc <= 64 || (tk > 0 && nc <= kSelThreads)) {  // a small list: ranks, then warp 0
       settle_small(nc);
       __syncthreads();
-      if (!ctl.settled) {  // (top-p alone) the nucleus reaches below the list
+      const int st = ctl.settled;
+      __syncthreads();
+      if (st == 0) {  // (top-p alone) the nucleus reaches below the list
         r *= 4;
-        __syncthreads();
         continue;
       }
+      small_done = st == 1;
+    }
+    if (small_done) {
       theta = ctl.theta_w;
       kept = ctl.kept_w;
       // a target row's kept set, in the order above, for the resolve kernel
