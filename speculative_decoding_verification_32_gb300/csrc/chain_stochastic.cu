@@ -2019,8 +2019,8 @@ __global__ void __launch_bounds__(kSelThreads, 6) trunc_select_kernel(const __gr
     const float l = BF16 ? __uint_as_float(bits << 16) : __uint_as_float(bits);
     return l == -kInf ? 0.f : ex2(__fmaf_rn(l, s2, nM));
   };
-  // ---- other listing thresholds: the r-th largest of every kDriftSample-th
-  // vector's keys, as the listing kernel takes them
+  // ---- sampled thresholds, for rows the chunks cannot settle: the r-th
+  // largest of the keys of every kDriftSample-th vector
   constexpr int kNSV = (SPEC_MAX_V + EPV * kDriftSample * kSelThreads - 1) / (EPV * kDriftSample * kSelThreads);
   const int n_samples = sampled_count(V, EPV);
   auto sample_tau = [&](int r) -> uint32_t {
