@@ -1607,77 +1607,36 @@ __device__ __forceinline__ bool fold_slice_stats(int nt, int lane, float s2, Sli
 
 // DRIFT, last kernel: one CTA per row, a programmatic dependent of the pick
 // grid (which completes only after the stream grid has), so both grids'
-// writes are visible after its dependency wait.  Each warp takes drafted
-// positions in turn: it folds the draft row's tile records in the order the
-// pick kernel folded the target row's, forms log2 q at the m support tokens
-// and replaces the log2 p the pick kernel left there by the residual
-// log p - log q in nats.  A position whose record
-// (the selection's, or a draft slice's) did not come is a timeout.  The row
-// status ORs every position's flags; a flagged row gets support -1 and
-// residual NaN everywhere, since no single selection CTA sees the whole row.
+// writes are visible after its dependency wait.  The row status ORs every
+// position's flags from the pick kernel's records (a record that did not
+// come is a timeout); a flagged row gets support -1 and residual NaN
+// everywhere, since no single pick CTA sees the whole row.
 template <bool BF16>
 __global__ void __launch_bounds__(kDriftFinishThreads) drift_finish_kernel(const __grid_constant__ ChainStochParams P) {
   __shared__ uint32_t row_f;
-  __shared__ float s_mq[kDriftMaxK], s_lsq[kDriftMaxK];
   grid_dependency_wait();
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int K = P.K, V = P.V, m = P.drift_m, nt = P.nslices;
-  constexpr int NW = kDriftFinishThreads / 32;
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int K = P.K, m = P.drift_m;
   const uint32_t tag = *reinterpret_cast<volatile const uint32_t *>(P.gen);
-  const float T = P.temperature ? __ldg(P.temperature + b) : 1.0f;
-  const float s2 = (T > 0.f && T < kInf) ? __fdiv_rn(kLog2e, T) : 1.f;
   if (tid == 0) row_f = 0u;
   __syncthreads();
-  for (int j = warp; j < K && SV_INB(j, kDriftMaxK); j += NW) {
-    float M1 = 0.f, S1 = 0.f, M2, S2;
+  for (int j = tid; j < K && SV_INB(j, kDriftMaxK); j += kDriftFinishThreads) {
+    float M1, S1;
     uint32_t f1 = 0;
-    const bool sel_in = load_part(P.trunc_area + (size_t)b * K + j, tag, &M1, &S1, &f1);
-    // the draft row's records, in the stream's row numbering
-    const long long drow = (long long)P.B * (K + 1) + (long long)b * K + j;
-    uint32_t df = 0;
-    const bool stats_in = fold_slice_stats(nt, lane, s2, [&](int t, float *qm, float *qs) {
-      uint32_t qf = 0;
-      if (!SV_INB(drow * nt + t, (long long)P.B * (2 * K + 1) * nt)) {
-        *qm = -kInf;
-        *qs = 0.f;
-        return false;
-      }
-      const bool ok = load_part(P.part + (size_t)drow * nt + t, tag, qm, qs, &qf);
-      df |= qf;
-      return ok;
-    }, &M2, &S2);
-    df = __reduce_or_sync(FULL_MASK, df);
-    uint32_t f = f1 | (sel_in && stats_in && !df ? 0u : F_TIMEOUT);
-    if (M2 != M2 || M2 == kInf) f |= F_NONFINITE;
-    else if (M2 == -kInf) f |= F_EMPTY;
-    if (lane == 0) {
-      s_mq[j] = M2;
-      s_lsq[j] = lg2(S2);
-      if (f) atomicOr(&row_f, f);
-    }
+    const bool in = load_part(P.trunc_area + (size_t)b * K + j, tag, &M1, &S1, &f1);
+    const uint32_t f = in ? f1 : F_TIMEOUT;
+    if (f) atomicOr(&row_f, f);
   }
   __syncthreads();
   const uint32_t f = row_f;
   if (tid == 0 && P.row_status) P.row_status[b] = lowest_code(f);
-  int32_t *sup = P.drift_support + (size_t)b * K * m;
-  float *res = P.drift_residual + (size_t)b * K * m;
   if (f) {
+    int32_t *sup = P.drift_support + (size_t)b * K * m;
+    float *res = P.drift_residual + (size_t)b * K * m;
     for (int i = tid; i < K * m; i += kDriftFinishThreads) {
       sup[i] = -1;
       res[i] = __int_as_float(0x7fc00000);
     }
-    return;
-  }
-  for (int i = tid; i < K * m; i += kDriftFinishThreads) {
-    const int j = i / m;
-    const int ii = sup[i];
-    if (!(ii >= 0 && ii < V) || !SV_INB(j, kDriftMaxK)) continue;  // m > V: no token here
-    const size_t at = ((size_t)b * K + j) * V + ii;
-    float ld;
-    if constexpr (BF16) ld = bf16_lo(__ldg(static_cast<const unsigned short *>(P.draft) + at));
-    else ld = __ldg(static_cast<const float *>(P.draft) + at);
-    const float l2q = ld == -kInf ? -kInf : __fadd_rn(__fmaf_rn(ld, s2, -__fmul_rn(s_mq[j], s2)), -s_lsq[j]);
-    res[i] = __fmul_rn(__fadd_rn(res[i], -l2q), kLn2);
   }
 }
 
@@ -2511,8 +2470,9 @@ struct alignas(16) PickCtrl {
   uint32_t sel_key[kDriftMaxM];
   int scan[kSelWarps];
   int n_gt, n_eq, digit, above;
-  float Mp, Sp;
-  uint32_t flags;
+  float Mp, Sp;     // the target row's max and sum
+  float Mq, lSq;    // the draft row's max and log2 sum
+  uint32_t tflags, dflags, flags;
 };
 
 template <bool BF16>
@@ -2552,14 +2512,18 @@ __global__ void __launch_bounds__(kSelThreads, 6) drift_pick_kernel(const __grid
       if (SV_INB((long long)row * nv + v, (long long)P.B * (2 * K + 1) * nv))
         cp_async16(reinterpret_cast<uint4 *>(ctl.chunk) + v, srcm + v);
   }
+  // tile records: warp 0 the target row's, warp 1 the draft row's (the
+  // stream's row numbering), folded once the candidates are listed
+  const long long drow = (long long)P.B * npos + (long long)b * K + j;
   unsigned long long rec_a[2] = {0ull, 0ull}, rec_b[2] = {0ull, 0ull};
-  if (warp == 0) {
+  if (warp <= 1) {
+    const long long r = warp == 0 ? row : drow;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int t = lane + 32 * h;
-      if (t < nt && SV_INB((long long)row * nt + t, (long long)P.B * (2 * K + 1) * nt)) {
-        rec_a[h] = ld_relaxed_u64(&P.part[(size_t)row * nt + t].a);
-        rec_b[h] = ld_relaxed_u64(&P.part[(size_t)row * nt + t].b);
+      if (t < nt && SV_INB(r * nt + t, (long long)P.B * (2 * K + 1) * nt)) {
+        rec_a[h] = ld_relaxed_u64(&P.part[(size_t)r * nt + t].a);
+        rec_b[h] = ld_relaxed_u64(&P.part[(size_t)r * nt + t].b);
       }
     }
   }
@@ -2568,10 +2532,11 @@ __global__ void __launch_bounds__(kSelThreads, 6) drift_pick_kernel(const __grid
   const int nc = use_chunks ? chunk_candidates<BF16>(ctl.chunk, nch, m, tg, aligned, nvec, V, ctl.cs, ctl.ck, kPickCand,
                                                      false)
                             : -1;
-  // ---- the target row's max and sum, folded from its tile records in the
-  // order the finishing kernel folds the draft row's; with this position's
-  // flags they go to the finishing kernel in a stamped record
-  if (warp == 0) {
+  // ---- the target row's and the draft row's max and sum, each folded from
+  // its tile records in one fixed order (identical rows give identical
+  // bits); this position's flags go to the finishing kernel in a stamped
+  // record
+  if (warp <= 1) {
     float M1, S1;
     uint32_t rf = 0;
     const bool ready = fold_slice_stats(nt, lane, s2, [&](int t, float *qm, float *qs) {
@@ -2583,14 +2548,25 @@ __global__ void __launch_bounds__(kSelThreads, 6) drift_pick_kernel(const __grid
     }, &M1, &S1);
     rf = __reduce_or_sync(FULL_MASK, rf);
     if (lane == 0) {
-      uint32_t f = tflags | (ready && !rf ? 0u : F_TIMEOUT);
+      uint32_t f = ready && !rf ? 0u : F_TIMEOUT;
       if (M1 != M1 || M1 == kInf) f |= F_NONFINITE;
       else if (M1 == -kInf) f |= F_EMPTY;
-      ctl.flags = f;
-      ctl.Mp = M1;
-      ctl.Sp = S1;
-      store_part(P.trunc_area + (size_t)b * K + j, M1, S1, f, tag);
+      if (warp == 0) {
+        ctl.tflags = f;
+        ctl.Mp = M1;
+        ctl.Sp = S1;
+      } else {
+        ctl.dflags = f;
+        ctl.Mq = M1;
+        ctl.lSq = lg2(S1);
+      }
     }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const uint32_t f = tflags | ctl.tflags | ctl.dflags;
+    ctl.flags = f;
+    store_part(P.trunc_area + (size_t)b * K + j, ctl.Mp, ctl.Sp, f, tag);
   }
   __syncthreads();
   if (ctl.flags) {  // the finishing kernel blanks the whole row
@@ -2602,12 +2578,19 @@ __global__ void __launch_bounds__(kSelThreads, 6) drift_pick_kernel(const __grid
   }
   const float nMp = -__fmul_rn(ctl.Mp, s2);
   const float l2Sp = lg2(ctl.Sp);
-  // support entry `rank` is token ii with logit lt: its log2 p as in the
-  // walk, kept in the residual's place until the finishing kernel subtracts
-  // log2 q
+  const float nMq = -__fmul_rn(ctl.Mq, s2), l2Sq = ctl.lSq;
+  // support entry `rank` is token ii with target logit lt: log2 p and log2 q
+  // as in the walk, the residual log p - log q in nats (a masked draft logit
+  // gives +inf)
   auto emit = [&](int rank, int ii, float lt) {
+    const size_t at = ((size_t)b * K + j) * V + ii;
+    float ld;
+    if constexpr (BF16) ld = bf16_lo(__ldg(static_cast<const unsigned short *>(P.draft) + at));
+    else ld = __ldg(static_cast<const float *>(P.draft) + at);
+    const float l2p = __fadd_rn(__fmaf_rn(lt, s2, nMp), -l2Sp);
+    const float l2q = ld == -kInf ? -kInf : __fadd_rn(__fmaf_rn(ld, s2, nMq), -l2Sq);
     sup[rank] = ii;
-    res[rank] = __fadd_rn(__fmaf_rn(lt, s2, nMp), -l2Sp);
+    res[rank] = __fmul_rn(__fadd_rn(l2p, -l2q), kLn2);
   };
   if (nc >= m && nc <= kPickCand) {
     // every logit at or above the threshold is a candidate: the m of highest
