@@ -288,63 +288,6 @@ __device__ __forceinline__ uint32_t pack_threshold(float tf) {
   }
 }
 
-// The largest element of U 16-byte vectors (NaN wins), folded into m.
-template <bool BF16, int U>
-__device__ __forceinline__ void online_max(const uint32_t (&w)[U][4], float &m) {
-  using F = Fmt<BF16>;
-  if constexpr (BF16) {
-    uint32_t pm = F::NEG_INF_WORD;
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      pm = bf16x2_max_nan(pm, bf16x2_max_nan(bf16x2_max_nan(w[u][0], w[u][1]), bf16x2_max_nan(w[u][2], w[u][3])));
-    m = fmax_nan(m, fmax_nan(bf16_lo(pm), bf16_hi(pm)));
-  } else {
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      m = fmax_nan(m, fmax_nan(fmax_nan(__uint_as_float(w[u][0]), __uint_as_float(w[u][1])),
-                               fmax_nan(__uint_as_float(w[u][2]), __uint_as_float(w[u][3]))));
-  }
-}
-
-// Folds U 16-byte vectors into a thread's running (max, sum of exp2((x - max)
-// s2)): the vectors' largest element raises the max, the sum is rescaled to it
-// and every element adds its exp2 (-inf adds nothing; a NaN poisons both).
-template <bool BF16, int U>
-__device__ __forceinline__ void online_accumulate(const uint32_t (&w)[U][4], float s2, float &m, float &s) {
-  using F = Fmt<BF16>;
-  constexpr int EPV = F::EPV;
-  float bm;
-  if constexpr (BF16) {
-    uint32_t pm = F::NEG_INF_WORD;
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      pm = bf16x2_max_nan(pm, bf16x2_max_nan(bf16x2_max_nan(w[u][0], w[u][1]), bf16x2_max_nan(w[u][2], w[u][3])));
-    bm = fmax_nan(bf16_lo(pm), bf16_hi(pm));
-  } else {
-    bm = -kInf;
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      bm = fmax_nan(bm, fmax_nan(fmax_nan(__uint_as_float(w[u][0]), __uint_as_float(w[u][1])),
-                                 fmax_nan(__uint_as_float(w[u][2]), __uint_as_float(w[u][3]))));
-  }
-  const float mn = fmax_nan(m, bm);
-  if (mn == -kInf) return;
-  const float off = -__fmul_rn(mn, s2);
-  const float2 s2v = make_float2(s2, s2), offv = make_float2(off, off);
-  float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-#pragma unroll
-    for (int i = 0; i < EPV / 2; ++i) {
-      const float2 a = ffma2(F::pair(w[u], i), s2v, offv);
-      if (i & 1) acc1 = fadd2(acc1, make_float2(ex2(a.x), ex2(a.y)));
-      else acc0 = fadd2(acc0, make_float2(ex2(a.x), ex2(a.y)));
-    }
-  }
-  s = (m == -kInf ? 0.f : s * ex2(__fmul_rn(m - mn, s2))) + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
-  m = mn;
-}
-
 // The row's top-k / top-p parameters; false when neither truncates.
 __device__ __forceinline__ bool trunc_active(const ChainStochParams &P, int b, int V, int *k,
                                              float *tp) {

@@ -311,11 +311,6 @@ __device__ __forceinline__ float warp_sum(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL_MASK, v, o);
   return v;
 }
-__device__ __forceinline__ float warp_max_nan(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmax_nan(v, __shfl_xor_sync(FULL_MASK, v, o));
-  return v;
-}
 // inclusive prefix sum over the lanes of a warp (Hillis-Steele)
 __device__ __forceinline__ float warp_inclusive_scan(float v, int lane) {
 #pragma unroll
