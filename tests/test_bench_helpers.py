@@ -49,3 +49,20 @@ def test_committed_traffic_record_is_well_formed():
     for name, r in rec.items():
         assert {"source", "sha256", "dram_bytes_read", "dram_bytes_write", "capture"} <= set(r), name
         assert r["capture"].startswith("profiles/")
+
+
+def test_every_traffic_record_the_bench_reads_is_on_file():
+    """Each kernel name bench.py looks up has a record whose capture summary
+    exists, so a renamed kernel or record cannot turn the figure into a
+    silent null."""
+    import os
+    import re
+    with open(bench.__file__) as fh:
+        names = set(re.findall(r'measured_traffic\("([^"]+)"\)', fh.read()))
+    with open(bench.TRAFFIC_FILE) as fh:
+        rec = json.load(fh)
+    assert names, "bench.py reads no traffic record"
+    for name in names:
+        assert name in rec, name
+        assert os.path.exists(os.path.join(bench.ROOT, rec[name]["capture"])), name
+
