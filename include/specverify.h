@@ -348,8 +348,8 @@ spec_status spec_verify_chain_truncated(const spec_chain_args *args, const spec_
  * the largest logit of every chunk of 32 (bf16) or 16 (fp32) target logits;
  * one CTA per drafted position, which takes the support from the logits of
  * the chunks whose maxima can reach the m-th largest (a row they cannot
- * settle is searched whole); then one CTA per row for the residuals and the
- * row's status.  Residuals carry fp32 rounding: agreement with an exact
+ * settle is searched whole) and writes the residuals; then one CTA per row
+ * for the row's status.  Residuals carry fp32 rounding: agreement with an exact
  * computation is within about 1e-4 nats for logits of magnitude up to ~50/T.
  */
 spec_status spec_drift_residuals(const spec_chain_args *args, int32_t m, int32_t *support,
